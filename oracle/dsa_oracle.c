@@ -1,0 +1,205 @@
+/*
+ * dsa_oracle.c -- host oracle for the DeepSeek-Sparse-Attention hot path.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE: see dsa_oracle.h for who may call it,
+ * the sources each function follows, and the argument conventions.
+ *
+ * Plain C11, double accumulation, no blocking or reordering beyond the plain
+ * definition.  The optional OpenMP pragmas only split independent outputs (one
+ * key, one head) between threads; every individual sum runs in index order, so
+ * results are identical with any thread count.
+ */
+#include "dsa_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+int oracle_index_scores(const float *q, const float *w, const float *keys,
+                        int64_t n_keys, int32_t heads, int32_t dim, double *scores)
+{
+    if (n_keys < 0 || heads <= 0 || dim <= 0) return -1;
+    if (n_keys > 0 && (!q || !w || !keys || !scores)) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n_keys; t++) {
+        const float *kt = keys + t * (int64_t)dim;
+        double s = 0.0;
+        for (int32_t h = 0; h < heads; h++) {
+            const float *qh = q + (int64_t)h * dim;
+            double d = 0.0;
+            for (int32_t i = 0; i < dim; i++) d += (double)qh[i] * (double)kt[i];
+            double relu = d > 0.0 ? d : 0.0;          /* ReLU on the per-head dot */
+            s += (double)w[h] * relu;                 /* weighted sum over heads  */
+        }
+        scores[t] = s;
+    }
+    return 0;
+}
+
+typedef struct {
+    double s;
+    int64_t i;
+} scored_t;
+
+/* Total order of the selection: higher score first, then lower index first. */
+static int cmp_score_desc_index_asc(const void *pa, const void *pb)
+{
+    const scored_t *a = (const scored_t *)pa, *b = (const scored_t *)pb;
+    if (a->s > b->s) return -1;
+    if (a->s < b->s) return 1;
+    return (a->i < b->i) ? -1 : (a->i > b->i) ? 1 : 0;
+}
+
+static int cmp_i32_asc(const void *pa, const void *pb)
+{
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a < b) ? -1 : (a > b) ? 1 : 0;
+}
+
+int oracle_topk(const double *scores, int64_t n, int64_t k, int32_t *idx, int64_t *n_sel)
+{
+    if (n < 0 || k < 0 || !n_sel) return -1;
+    if (n > 0 && (!scores || !idx)) return -1;
+    if (n > INT32_MAX) return -1;
+    if (n <= k) {                                     /* dense: every index */
+        for (int64_t t = 0; t < n; t++) idx[t] = (int32_t)t;
+        *n_sel = n;
+        return 0;
+    }
+    scored_t *all = (scored_t *)malloc((size_t)n * sizeof(scored_t));
+    if (!all) return -2;
+    for (int64_t t = 0; t < n; t++) { all[t].s = scores[t]; all[t].i = t; }
+    qsort(all, (size_t)n, sizeof(scored_t), cmp_score_desc_index_asc);
+    for (int64_t j = 0; j < k; j++) idx[j] = (int32_t)all[j].i;
+    free(all);
+    qsort(idx, (size_t)k, sizeof(int32_t), cmp_i32_asc);   /* emit ascending */
+    *n_sel = k;
+    return 0;
+}
+
+int oracle_kpool_select(const double *pool_scores, int64_t L, int64_t k, int32_t kpool,
+                        int32_t *idx, int64_t *n_sel)
+{
+    if (L < 0 || k <= 0 || kpool <= 0 || !n_sel || !idx) return -1;
+    if (k % kpool != 0) return -1;
+    if (L > INT32_MAX) return -1;
+    int64_t n_pool = L / kpool;                       /* complete pools */
+    int64_t keep = k / kpool;                         /* pools a query may keep */
+    if (n_pool <= keep) {                             /* dense: every token */
+        for (int64_t t = 0; t < L; t++) idx[t] = (int32_t)t;
+        *n_sel = L;
+        return 0;
+    }
+    if (!pool_scores) return -1;
+    int32_t *pools = (int32_t *)malloc((size_t)keep * sizeof(int32_t));
+    if (!pools) return -2;
+    int64_t n_pools_sel = 0;
+    int rc = oracle_topk(pool_scores, n_pool, keep, pools, &n_pools_sel);
+    if (rc != 0) { free(pools); return rc; }
+    int64_t m = 0;
+    for (int64_t j = 0; j < n_pools_sel; j++)         /* expand pools to tokens */
+        for (int32_t r = 0; r < kpool; r++) idx[m++] = (int32_t)((int64_t)pools[j] * kpool + r);
+    for (int64_t t = n_pool * kpool; t < L; t++) idx[m++] = (int32_t)t;   /* unfilled tail */
+    free(pools);
+    *n_sel = m;
+    return 0;
+}
+
+/* Softmax-weighted pooling of the latent for one head over a list of logits. */
+static void attend_head(const double *z, const float *const *row_ptr, int64_t n, int32_t dv,
+                        double *out_h, double *lse_h)
+{
+    double m = -INFINITY;
+    for (int64_t j = 0; j < n; j++) if (z[j] > m) m = z[j];
+    double l = 0.0;
+    for (int32_t c = 0; c < dv; c++) out_h[c] = 0.0;
+    for (int64_t j = 0; j < n; j++) {
+        if (z[j] == -INFINITY) continue;              /* masked row: weight exactly 0 */
+        double p = exp(z[j] - m);
+        l += p;
+        const float *r = row_ptr[j];
+        for (int32_t c = 0; c < dv; c++) out_h[c] += p * (double)r[c];
+    }
+    for (int32_t c = 0; c < dv; c++) out_h[c] /= l;
+    if (lse_h) *lse_h = m + log(l);
+}
+
+static double dot_row(const float *q, const float *r, int32_t width)
+{
+    double a = 0.0;
+    for (int32_t c = 0; c < width; c++) a += (double)q[c] * (double)r[c];
+    return a;
+}
+
+int oracle_sparse_mla(const float *q_abs, const float *rows, int64_t n_rows, int32_t heads,
+                      int32_t width, int32_t dv, double scale, const int32_t *idx,
+                      int64_t n_sel, double *out, double *lse)
+{
+    if (heads <= 0 || width <= 0 || dv <= 0 || dv > width || n_sel <= 0 || n_rows <= 0) return -1;
+    if (!q_abs || !rows || !idx || !out) return -1;
+    for (int64_t j = 0; j < n_sel; j++) if (idx[j] < 0 || idx[j] >= n_rows) return -1;
+    const float **row_ptr = (const float **)malloc((size_t)n_sel * sizeof(float *));
+    double *zall = (double *)malloc((size_t)n_sel * (size_t)heads * sizeof(double));
+    if (!row_ptr || !zall) { free(row_ptr); free(zall); return -2; }
+    for (int64_t j = 0; j < n_sel; j++) row_ptr[j] = rows + (int64_t)idx[j] * width;
+#pragma omp parallel for schedule(static)
+    for (int32_t h = 0; h < heads; h++) {
+        const float *qh = q_abs + (int64_t)h * width;
+        double *z = zall + (int64_t)h * n_sel;
+        for (int64_t j = 0; j < n_sel; j++) z[j] = scale * dot_row(qh, row_ptr[j], width);
+        attend_head(z, row_ptr, n_sel, dv, out + (int64_t)h * dv, lse ? lse + h : NULL);
+    }
+    free(zall);
+    free(row_ptr);
+    return 0;
+}
+
+int oracle_dense_masked_mla(const float *q_abs, const float *rows, int64_t n_rows,
+                            int32_t heads, int32_t width, int32_t dv, double scale,
+                            const uint8_t *mask, double *out, double *lse)
+{
+    if (heads <= 0 || width <= 0 || dv <= 0 || dv > width || n_rows <= 0) return -1;
+    if (!q_abs || !rows || !mask || !out) return -1;
+    int64_t n_on = 0;
+    for (int64_t t = 0; t < n_rows; t++) n_on += mask[t] != 0;
+    if (n_on == 0) return -1;
+    const float **row_ptr = (const float **)malloc((size_t)n_rows * sizeof(float *));
+    double *zall = (double *)malloc((size_t)n_rows * (size_t)heads * sizeof(double));
+    if (!row_ptr || !zall) { free(row_ptr); free(zall); return -2; }
+    for (int64_t t = 0; t < n_rows; t++) row_ptr[t] = rows + t * (int64_t)width;
+#pragma omp parallel for schedule(static)
+    for (int32_t h = 0; h < heads; h++) {
+        const float *qh = q_abs + (int64_t)h * width;
+        double *z = zall + (int64_t)h * n_rows;
+        for (int64_t t = 0; t < n_rows; t++)
+            z[t] = mask[t] ? scale * dot_row(qh, row_ptr[t], width) : -INFINITY;
+        attend_head(z, row_ptr, n_rows, dv, out + (int64_t)h * dv, lse ? lse + h : NULL);
+    }
+    free(zall);
+    free(row_ptr);
+    return 0;
+}
+
+int oracle_decode_step(const float *q_idx, const float *w, const float *keys,
+                       int32_t idx_heads, int32_t idx_dim, const float *q_abs,
+                       const float *rows, int64_t L, int32_t heads, int32_t width,
+                       int32_t dv, double scale, int64_t k, int32_t kpool,
+                       double *scores_out, int32_t *idx, int64_t *n_sel,
+                       double *out, double *lse)
+{
+    if (L <= 0 || kpool <= 0 || k <= 0) return -1;
+    int64_t n_keys = L / kpool;
+    double *sc = scores_out;
+    if (!sc && n_keys > 0) {
+        sc = (double *)malloc((size_t)n_keys * sizeof(double));
+        if (!sc) return -2;
+    }
+    int rc = 0;
+    /* The dense shortcut skips scoring entirely ([GLM-DOC] "The sparse-attention
+     * path"); the scores are still produced here so callers can inspect them. */
+    if (n_keys > 0) rc = oracle_index_scores(q_idx, w, keys, n_keys, idx_heads, idx_dim, sc);
+    if (rc == 0) rc = oracle_kpool_select(sc, L, k, kpool, idx, n_sel);
+    if (rc == 0) rc = oracle_sparse_mla(q_abs, rows, L, heads, width, dv, scale, idx, *n_sel, out, lse);
+    if (sc != scores_out) free(sc);
+    return rc;
+}

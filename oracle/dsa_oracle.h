@@ -1,0 +1,108 @@
+/*
+ * dsa_oracle.h -- host oracle for the DeepSeek-Sparse-Attention hot path.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test-suite, the smoke check
+ * of the package entry point and the CPU-baseline leg of the benchmark may load
+ * or call this library.  The CUDA library never includes, links or calls it, and
+ * it shares no code, header, table or helper with the CUDA library.
+ *
+ * Every function is a direct, unblocked restatement of what the method computes,
+ * accumulated in double precision from float inputs (bf16 inputs are widened to
+ * float exactly by the caller).  All sizes are element counts; all pointers are
+ * host pointers owned by the caller.  Functions return 0 on success and a
+ * negative value on a bad argument; they never allocate memory that outlives the
+ * call.
+ *
+ * Sources (page title -- section):
+ *   [GLM-DOC]   "GLM-5.x (glm-dsa, glm5next)" (TensorSharp model notes) --
+ *               "The block" table; "The sparse-attention path";
+ *               "GLM-5.3-Flash (glm5next)" table, row "Pooled indexer".
+ *   [WASTE]     "GLM-5.3-Flash on WASTE" -- "DeepSeek Sparse Attention,
+ *               k-pool flavour"; "What is checked".
+ *   [ONE-C]     "GLM 5.2 in one C file" (blog) -- "Attention: Multi head Latent
+ *               Attention With a Tiny KV Cache"; "The Lightning Indexer: Sparse
+ *               Attention When It Helps".
+ *   [STRATA]    "Add GLM-5.3-Flash support" (Strata pull request) -- "What a
+ *               glm5-next block has that nothing else in the engine does";
+ *               "Known gaps".
+ */
+#ifndef DSA_ORACLE_H
+#define DSA_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Lightning-indexer score of n_keys keys against one query.
+ *   q      [heads * dim]   indexer query, head-major
+ *   w      [heads]         per-head weights
+ *   keys   [n_keys * dim]  indexer keys (or pool keys), one row per key
+ *   scores [n_keys]        out: s_t = sum_h w_h * max(0, sum_i q[h,i]*keys[t,i])
+ * [ONE-C] "The Lightning Indexer": ReLU'd per-head dot product, weighted sum over
+ * heads.  The page's positive factors 1/sqrt(dim) and 1/sqrt(heads) are omitted:
+ * ReLU is positively homogeneous, so they fold into w and cannot change a
+ * selection.  [GLM-DOC] "The block", row "DSA indexer": 32 heads x 128. */
+int oracle_index_scores(const float *q, const float *w, const float *keys,
+                        int64_t n_keys, int32_t heads, int32_t dim, double *scores);
+
+/* Top-k selection over n scores.
+ *   If n <= k every index 0..n-1 is selected (the dense shortcut, [GLM-DOC]
+ *   "The sparse-attention path"; [ONE-C] "The Lightning Indexer").
+ *   Otherwise the k indices that come first in the total order
+ *   (score descending, index ascending) -- ties go to the lower index.
+ *   idx [>= min(n,k)] receives the selection in ascending index order;
+ *   *n_sel receives min(n, k). */
+int oracle_topk(const double *scores, int64_t n, int64_t k, int32_t *idx, int64_t *n_sel);
+
+/* k-pool selection for a query that sees L tokens, given the scores of its
+ * n_pool = floor(L / kpool) complete pools ([WASTE] "DeepSeek Sparse Attention,
+ * k-pool flavour"; [GLM-DOC] row "Pooled indexer").
+ *   If n_pool <= k / kpool, every token 0..L-1 is selected (dense).
+ *   Otherwise the top k/kpool pools (oracle_topk order) are expanded to their
+ *   kpool member tokens and the tail tokens kpool*n_pool .. L-1 of the unfilled
+ *   pool are appended ([STRATA] "Known gaps": the tail is appended).
+ *   idx [>= k + kpool - 1] receives ascending token indices; *n_sel the count.
+ * kpool == 1 is token mode and equals oracle_topk. */
+int oracle_kpool_select(const double *pool_scores, int64_t L, int64_t k, int32_t kpool,
+                        int32_t *idx, int64_t *n_sel);
+
+/* Absorbed-MLA attention of one query over the selected cache rows.
+ *   q_abs [heads * width]     absorbed query (latent part then rope part)
+ *   rows  [n_rows * width]    latent cache, width = kv_lora (+ rope)
+ *   idx   [n_sel]             selected row indices (any order, each < n_rows)
+ *   out   [heads * dv]        out: o[h,c] = sum_j p[h,j] * rows[idx_j, c], c < dv
+ *   lse   [heads] or NULL     out: log sum_j exp(z[h,j])
+ * with z[h,j] = scale * sum_{c<width} q_abs[h,c] * rows[idx_j, c] and
+ * p = softmax_j(z).  [ONE-C] "Attention: Multi head Latent Attention ...":
+ * absorbed score against the latent plus the rope dot, scaled, softmax, pooled
+ * latent.  [GLM-DOC] "The block": scale 1/16, cache row 512 + 64.  [STRATA]:
+ * the value of a NoPE row is the 512-wide latent itself. */
+int oracle_sparse_mla(const float *q_abs, const float *rows, int64_t n_rows, int32_t heads,
+                      int32_t width, int32_t dv, double scale, const int32_t *idx,
+                      int64_t n_sel, double *out, double *lse);
+
+/* The same attention written the way [GLM-DOC] "The sparse-attention path"
+ * states it: dense attention over all n_rows rows with the logit of every row
+ * whose mask byte is 0 set to minus infinity. */
+int oracle_dense_masked_mla(const float *q_abs, const float *rows, int64_t n_rows,
+                            int32_t heads, int32_t width, int32_t dv, double scale,
+                            const uint8_t *mask, double *out, double *lse);
+
+/* One query through the whole path: indexer scores over its keys (L token
+ * keys when kpool == 1, floor(L/kpool) pool keys otherwise), selection, and
+ * attention over the selected rows of its L cache rows.
+ *   scores_out [n_keys] or NULL, idx [k + kpool - 1], n_sel, out [heads*dv],
+ *   lse [heads] or NULL. */
+int oracle_decode_step(const float *q_idx, const float *w, const float *keys,
+                       int32_t idx_heads, int32_t idx_dim, const float *q_abs,
+                       const float *rows, int64_t L, int32_t heads, int32_t width,
+                       int32_t dv, double scale, int64_t k, int32_t kpool,
+                       double *scores_out, int32_t *idx, int64_t *n_sel,
+                       double *out, double *lse);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,350 @@
+"""Pins of the host oracle against what the pages and the mathematics fix.
+
+Each test pins one oracle function to something other than itself: a value
+printed on (or worked by hand from) a page, a closed form, a special case that
+reduces to a library routine, or a brute-force property on tiny inputs.  The
+rival-reading tests check that a plausible wrong reading of a page would be
+caught.  CPU only.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- indexer score
+
+def test_index_scores_hand_worked_example():
+    """'GLM 5.2 in one C file', 'The Lightning Indexer': worked by hand."""
+    rows = _table("index_score_hand.txt")
+    q = np.array([[1, 2, 0], [3, -1, 2]], dtype=np.float32)
+    w = np.array([0.5, -2.0], dtype=np.float32)
+    keys = np.array([[float(x) for x in r[1:4]] for r in rows], dtype=np.float32)
+    expect = np.array([float(r[4]) for r in rows])
+    got = oracle.index_scores(q, w, keys)
+    assert np.array_equal(got, expect)
+
+
+def test_index_scores_planted_closed_form():
+    """q_h = u for every head, w_h = 1/heads, k_t = a_t u  =>  s_t = relu(a_t) |u|^2."""
+    rng = np.random.default_rng(1)
+    heads, dim, n = 32, 128, 300
+    u = rng.integers(-3, 4, size=dim).astype(np.float32)        # small ints: exact
+    a = rng.integers(-20, 21, size=n).astype(np.float32) / 4.0
+    q = np.tile(u, (heads, 1))
+    w = np.full(heads, 1.0 / heads, dtype=np.float32)            # 1/32 exact in float
+    keys = (a[:, None] * u[None, :]).astype(np.float32)
+    got = oracle.index_scores(q, w, keys)
+    expect = np.maximum(a.astype(np.float64), 0.0) * float(np.dot(u, u))
+    np.testing.assert_allclose(got, expect, rtol=0, atol=1e-9)
+    # and the selection is the k largest a_t (ties to the lower index)
+    k = 40
+    sel = oracle.topk(got, k)
+    order = sorted(range(n), key=lambda t: (-max(a[t], 0.0), t))[:k]
+    assert sel.tolist() == sorted(order)
+
+
+def test_index_scores_positive_homogeneity():
+    """Scaling w by c > 0 scales every score by c, so the selection is unchanged
+    (why the page's positive factors 1/sqrt(128), 1/sqrt(32) may be dropped)."""
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((32, 128)).astype(np.float32)
+    w = rng.standard_normal(32).astype(np.float32)
+    keys = rng.standard_normal((500, 128)).astype(np.float32)
+    s1 = oracle.index_scores(q, w, keys)
+    c = np.float32(1.0 / (math.sqrt(128.0) * math.sqrt(32.0)))
+    s2 = oracle.index_scores(q, (w * c).astype(np.float32), keys)
+    np.testing.assert_allclose(s2, s1 * float(c), rtol=1e-6, atol=1e-12)
+    assert oracle.topk(s1, 64).tolist() == oracle.topk(s2, 64).tolist()
+
+
+def test_index_scores_key_permutation_equivariance():
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((4, 16)).astype(np.float32)
+    w = rng.standard_normal(4).astype(np.float32)
+    keys = rng.standard_normal((50, 16)).astype(np.float32)
+    perm = rng.permutation(50)
+    np.testing.assert_array_equal(oracle.index_scores(q, w, keys)[perm],
+                                  oracle.index_scores(q, w, keys[perm]))
+
+
+# ---------------------------------------------------------------------- top-k
+
+def _valid_selection(scores, sel, k):
+    """Brute force: |S| = min(n, k) and every member beats every non-member under
+    (score desc, index asc)."""
+    n = len(scores)
+    S = set(sel.tolist())
+    if len(S) != min(n, k) or len(sel) != len(S):
+        return False
+    if list(sel) != sorted(sel):
+        return False
+    for i in S:
+        for j in range(n):
+            if j in S:
+                continue
+            if not (scores[i] > scores[j] or (scores[i] == scores[j] and i < j)):
+                return False
+    return True
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_topk_brute_force_with_ties(seed):
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(1, 40))
+    k = int(rng.integers(1, 12))
+    scores = rng.integers(-3, 4, size=n).astype(np.float64)      # many exact ties
+    sel = oracle.topk(scores, k)
+    assert _valid_selection(scores, sel, k)
+
+
+def test_topk_exhaustive_small():
+    """Every score vector over {0,1,2}^5 and every k: brute-force validity."""
+    for vals in itertools.product([0.0, 1.0, 2.0], repeat=5):
+        s = np.array(vals)
+        for k in range(1, 7):
+            assert _valid_selection(s, oracle.topk(s, k), k)
+
+
+def test_topk_all_equal_takes_lowest_indices():
+    """Ties go to the lower index ('Add GLM-5.3-Flash support', router: ties by
+    ascending index); the rival 'ties to the higher index' would give the top."""
+    s = np.zeros(100)
+    assert oracle.topk(s, 10).tolist() == list(range(10))
+
+
+def test_topk_dense_when_n_le_k():
+    """'GLM-5.x (glm-dsa, glm5next)', 'The sparse-attention path': top-k over
+    n_kv <= k keeps every cell."""
+    s = np.random.default_rng(4).standard_normal(2048)
+    assert oracle.topk(s, 2048).tolist() == list(range(2048))
+    assert oracle.topk(s[:17], 2048).tolist() == list(range(17))
+
+
+def test_topk_exact_count_not_strict_threshold():
+    """The page's scan keeps scores strictly above the k-th largest, which keeps
+    at most k-1; the reading adopted keeps exactly k."""
+    s = np.arange(10, dtype=np.float64)
+    sel = oracle.topk(s, 4)
+    assert sel.tolist() == [6, 7, 8, 9]
+    strict = [t for t in range(10) if s[t] > np.sort(s)[::-1][3]]
+    assert len(strict) == 3 and len(sel) == 4
+
+
+# --------------------------------------------------------------------- k-pool
+
+@pytest.mark.parametrize("row", _table("pool_arithmetic.txt"))
+def test_kpool_count_table(row):
+    L, k, kp, n_pool, tail, dense, n_sel = (int(x) for x in row[:7])
+    assert L // kp == n_pool and L % kp == tail
+    rng = np.random.default_rng(L)
+    ps = rng.standard_normal(n_pool)
+    sel = oracle.kpool_select(ps, L, k, kp)
+    assert len(sel) == n_sel
+    if dense:
+        assert sel.tolist() == list(range(L))
+    else:
+        assert sel.tolist() == sorted(sel.tolist())
+        # the tail is always attended and every pool is taken whole
+        assert all(t in set(sel.tolist()) for t in range(n_pool * kp, L))
+        body = [t for t in sel.tolist() if t < n_pool * kp]
+        assert len(body) == k and all(body[i] // kp == body[i + 3] // kp
+                                      for i in range(0, len(body), kp))
+
+
+def test_kpool_planted_pools():
+    """Pool scores planted so the kept pools are known: 16 tokens, top-k 8,
+    pools of 4 ('GLM-5.3-Flash on WASTE', 'What is checked')."""
+    ps = np.array([0.1, 3.0, -1.0, 2.0])
+    sel = oracle.kpool_select(ps, 16, 8, 4)
+    assert sel.tolist() == [4, 5, 6, 7, 12, 13, 14, 15]
+    # 19 tokens: same pools plus the 3-token tail 16, 17, 18
+    sel = oracle.kpool_select(ps, 19, 8, 4)
+    assert sel.tolist() == [4, 5, 6, 7, 12, 13, 14, 15, 16, 17, 18]
+
+
+def test_kpool_zero_scores_tie_to_lower_pool():
+    """A pool whose every head scored negative lands at exactly 0 after the ReLU
+    ('GLM-5.3-Flash on WASTE', k-pool flavour); among equal pools the lower
+    index is kept."""
+    ps = np.array([0.0, 0.0, 0.0, 5.0, 0.0])
+    assert oracle.kpool_select(ps, 20, 8, 4).tolist() == [0, 1, 2, 3, 12, 13, 14, 15]
+
+
+def test_kpool_one_is_token_mode():
+    rng = np.random.default_rng(5)
+    s = rng.standard_normal(3000)
+    assert oracle.kpool_select(s, 3000, 2048, 1).tolist() == oracle.topk(s, 2048).tolist()
+
+
+def test_kpool_equal_member_keys_gives_same_pools():
+    """When a pool's four member keys all equal its pool key, token mode ranks the
+    members exactly as pool mode ranks the pool."""
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((8, 16)).astype(np.float32)
+    w = rng.standard_normal(8).astype(np.float32)
+    pool_keys = rng.standard_normal((30, 16)).astype(np.float32)
+    member_keys = np.repeat(pool_keys, 4, axis=0)
+    ps = oracle.index_scores(q, w, pool_keys)
+    ts = oracle.index_scores(q, w, member_keys)
+    assert oracle.kpool_select(ps, 120, 32, 4).tolist() == oracle.topk(ts, 32).tolist()
+
+
+# ----------------------------------------------------------------- attention
+
+def test_attention_identical_rows_return_the_latent():
+    rng = np.random.default_rng(7)
+    row = rng.standard_normal(576).astype(np.float32)
+    rows = np.tile(row, (10, 1))
+    q = rng.standard_normal((64, 576)).astype(np.float32)
+    out, lse = oracle.sparse_mla(q, rows, np.arange(10), 1 / 16, 512)
+    np.testing.assert_allclose(out, np.tile(row[:512].astype(np.float64), (64, 1)), atol=1e-12)
+    z = (q.astype(np.float64) @ row.astype(np.float64)) / 16
+    np.testing.assert_allclose(lse, z + math.log(10), atol=1e-9)
+
+
+def test_attention_zero_query_is_mean_latent():
+    rng = np.random.default_rng(8)
+    rows = rng.standard_normal((40, 576)).astype(np.float32)
+    idx = np.array([3, 9, 17, 25, 39], dtype=np.int32)
+    out, lse = oracle.sparse_mla(np.zeros((64, 576), np.float32), rows, idx, 1 / 16, 512)
+    mean = rows[idx, :512].astype(np.float64).mean(axis=0)
+    np.testing.assert_allclose(out, np.tile(mean, (64, 1)), atol=1e-12)
+    np.testing.assert_allclose(lse, math.log(5), atol=1e-12)
+
+
+def test_attention_two_rows_sigmoid_pins_scale_1_over_16():
+    """Two rows: p_1 = sigmoid(z_1 - z_2) with z = dot/16 ('GLM-5.x', 'The block':
+    softmax scale 1/16, not 1/sqrt(576) nor 1/sqrt(512))."""
+    width, dv = 576, 512
+    q = np.zeros((1, width), np.float32)
+    q[0, 0] = 8.0
+    rows = np.zeros((2, width), np.float32)
+    rows[0, 0], rows[0, 1] = 1.0, 1.0
+    rows[1, 0], rows[1, 1] = -1.0, 3.0
+    out, lse = oracle.sparse_mla(q, rows, np.array([0, 1]), 1 / 16, dv)
+    # z_1 = 8/16 = 0.5, z_2 = -0.5
+    p1 = 1.0 / (1.0 + math.exp(-1.0))
+    assert out[0, 0] == pytest.approx(p1 * 1.0 + (1 - p1) * -1.0, abs=1e-14)
+    assert out[0, 1] == pytest.approx(p1 * 1.0 + (1 - p1) * 3.0, abs=1e-14)
+    assert lse[0] == pytest.approx(math.log(math.exp(0.5) + math.exp(-0.5)), abs=1e-14)
+    # rival scales would give a visibly different weight
+    for rival in (1 / math.sqrt(576), 1 / math.sqrt(512)):
+        pr = 1.0 / (1.0 + math.exp(-16.0 * rival))
+        assert abs((pr - (1 - pr)) - out[0, 0]) > 1e-3
+
+
+def test_attention_rope_columns_score_but_never_enter_output():
+    """576 = 512 latent + 64 rope: the rope part adds to the score, the value is
+    the 512-wide latent only ('GLM 5.2 in one C file', MLA decode path)."""
+    width, dv = 576, 512
+    q = np.zeros((2, width), np.float32)
+    q[:, 512] = 16.0                       # rope-only query
+    rows = np.zeros((2, width), np.float32)
+    rows[0, :512] = 1.0
+    rows[1, :512] = 2.0
+    rows[0, 512] = 1.0                     # z_1 = 1, z_2 = 0
+    rows[1, 575] = 100.0                   # rope column the query does not read
+    out, _ = oracle.sparse_mla(q, rows, np.array([0, 1]), 1 / 16, dv)
+    assert out.shape == (2, 512)
+    p1 = 1.0 / (1.0 + math.exp(-1.0))
+    np.testing.assert_allclose(out, p1 * 1.0 + (1 - p1) * 2.0, atol=1e-14)
+
+
+def test_attention_large_gap_selects_argmax_row():
+    rng = np.random.default_rng(9)
+    rows = rng.standard_normal((6, 64)).astype(np.float32)
+    q = np.zeros((1, 64), np.float32)
+    q[0] = rows[4] * 1000.0
+    out, _ = oracle.sparse_mla(q, rows, np.arange(6), 1.0, 32)
+    np.testing.assert_allclose(out[0], rows[4, :32], atol=1e-12)
+
+
+def test_sparse_equals_dense_masked_brute_force():
+    """The gather formulation equals dense attention with a -inf mask on every
+    tiny case ('GLM-5.x', 'The sparse-attention path': a mask that starts fully
+    masked and is unmasked at the selected positions)."""
+    rng = np.random.default_rng(10)
+    for L in (1, 2, 5, 17, 64):
+        for k in (1, 3, 8):
+            q = rng.standard_normal((4, 24)).astype(np.float32)
+            rows = rng.standard_normal((L, 24)).astype(np.float32)
+            scores = rng.standard_normal(L)
+            sel = oracle.topk(scores, k)
+            mask = np.zeros(L, np.uint8)
+            mask[sel] = 1
+            o1, l1 = oracle.sparse_mla(q, rows, sel, 0.3, 16)
+            o2, l2 = oracle.dense_masked_mla(q, rows, mask, 0.3, 16)
+            np.testing.assert_allclose(o1, o2, atol=1e-12)
+            np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+def test_sparse_equals_dense_when_context_le_k():
+    """'GLM 5.2 in one C file': below index_topk keys the indexer keeps all of
+    them and attention is exactly dense."""
+    rng = np.random.default_rng(11)
+    L = 300
+    q_idx = rng.standard_normal((32, 128)).astype(np.float32)
+    w = rng.standard_normal(32).astype(np.float32)
+    keys = rng.standard_normal((L, 128)).astype(np.float32)
+    q = rng.standard_normal((64, 576)).astype(np.float32)
+    rows = rng.standard_normal((L, 576)).astype(np.float32)
+    r = oracle.decode_step(q_idx, w, keys, q, rows, L, 2048, 1, 1 / 16, 512)
+    assert r["idx"].tolist() == list(range(L))
+    o2, l2 = oracle.dense_masked_mla(q, rows, np.ones(L, np.uint8), 1 / 16, 512)
+    np.testing.assert_allclose(r["out"], o2, atol=1e-12)
+    np.testing.assert_allclose(r["lse"], l2, atol=1e-12)
+
+
+def test_attention_row_permutation_invariance():
+    rng = np.random.default_rng(12)
+    rows = rng.standard_normal((30, 40)).astype(np.float32)
+    q = rng.standard_normal((3, 40)).astype(np.float32)
+    idx = np.array([1, 4, 9, 20, 29], dtype=np.int32)
+    o1, l1 = oracle.sparse_mla(q, rows, idx, 0.2, 32)
+    o2, l2 = oracle.sparse_mla(q, rows, idx[::-1].copy(), 0.2, 32)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+
+
+def test_decode_step_kpool_nope_composition():
+    """k-pool NoPE: scores over pool keys, 512 pools kept, tail appended, 512-wide
+    rows that are both key and value ('Add GLM-5.3-Flash support': K and V are
+    the same tensor)."""
+    rng = np.random.default_rng(13)
+    L, k, kp = 4 * 40 + 3, 32, 4
+    q_idx = rng.standard_normal((32, 128)).astype(np.float32)
+    w = rng.standard_normal(32).astype(np.float32)
+    pkeys = rng.standard_normal((L // kp, 128)).astype(np.float32)
+    q = rng.standard_normal((64, 512)).astype(np.float32)
+    rows = rng.standard_normal((L, 512)).astype(np.float32)
+    r = oracle.decode_step(q_idx, w, pkeys, q, rows, L, k, kp, 1 / 16, 512)
+    pools = oracle.topk(oracle.index_scores(q_idx, w, pkeys), k // kp)
+    expect = [4 * p + j for p in pools for j in range(4)] + [160, 161, 162]
+    assert r["idx"].tolist() == expect
+    o, l = oracle.sparse_mla(q, rows, np.array(expect, np.int32), 1 / 16, 512)
+    np.testing.assert_array_equal(r["out"], o)
+
+
+def test_oracle_rejects_bad_arguments():
+    with pytest.raises(ValueError):
+        oracle.sparse_mla(np.zeros((2, 8), np.float32), np.zeros((4, 8), np.float32),
+                          np.array([0, 4]), 1.0, 8)        # index out of range
+    with pytest.raises(ValueError):
+        oracle.kpool_select(np.zeros(2), 8, 6, 4)          # top_k not a multiple of kpool
