@@ -1,0 +1,303 @@
+// dsa_api.cu -- the extern "C" entry points of libdsa: host-side validation,
+// workspace layout, and the order in which the kernels are enqueued.
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "dsa.h"
+#include "dsa_kernels.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool trace_on() {
+    static const bool on = [] {
+        const char* e = getenv("DSA_TRACE");
+        return e != nullptr && e[0] != '\0' && e[0] != '0';
+    }();
+    return on;
+}
+
+dsa_status check_shape(const dsa_shape* s, Shape* out) {
+    if (s == nullptr) return DSA_ERR_INVALID_ARG;
+    if (s->idx_heads <= 0 || s->idx_dim <= 0 || s->heads <= 0 || s->kv_lora <= 0 ||
+        s->rope_dim < 0 || s->top_k <= 0 || s->kpool <= 0)
+        return DSA_ERR_INVALID_ARG;
+    if (s->top_k % s->kpool != 0) return DSA_ERR_INVALID_ARG;
+    if (!isfinite(s->scale) || !(s->scale > 0.f)) return DSA_ERR_INVALID_ARG;
+    if (s->dtype != DSA_F32 && s->dtype != DSA_BF16) return DSA_ERR_INVALID_ARG;
+    // What this build implements: the layer geometry of the pages.
+    if (s->idx_heads > 64 || s->idx_dim != 128 || s->heads != 64 || s->kv_lora != 512 ||
+        (s->rope_dim != 0 && s->rope_dim != 64) || s->kpool > 16 || s->top_k > 65536)
+        return DSA_ERR_UNSUPPORTED;
+    *out = Shape{s->idx_heads, s->idx_dim, s->heads, s->kv_lora, s->rope_dim,
+                 s->top_k, s->kpool, s->scale, s->dtype};
+    return DSA_OK;
+}
+
+dsa_status check_batch(const dsa_batch* b, const Shape& sh, BatchDev* out) {
+    if (b == nullptr) return DSA_ERR_INVALID_ARG;
+    if (b->n_seq < 0 || b->n_q < 0 || b->max_q_len < 0 || b->max_kv_len < 0 || b->reserved != 0)
+        return DSA_ERR_INVALID_ARG;
+    if (b->n_q > 0) {
+        if (b->n_seq < 1 || b->row_off == nullptr || b->key_off == nullptr || b->q_off == nullptr)
+            return DSA_ERR_INVALID_ARG;
+        if (b->max_q_len < 1 || b->max_kv_len < b->max_q_len) return DSA_ERR_INVALID_ARG;
+        if ((int64_t)b->max_q_len > (int64_t)b->n_q) return DSA_ERR_INVALID_ARG;
+    }
+    if (b->max_kv_len >= ((int64_t)1 << 31)) return DSA_ERR_UNSUPPORTED;
+    if (b->n_q > 65535) return DSA_ERR_UNSUPPORTED;
+    *out = BatchDev{b->row_off, b->key_off, b->q_off, b->n_seq, b->n_q, b->max_kv_len, sh.kpool};
+    return DSA_OK;
+}
+
+// Keys a query may score at most, and the default score row stride.
+int64_t max_keys(const Shape& sh, const BatchDev& b) { return b.max_kv_len / sh.kpool; }
+int64_t default_ld(const Shape& sh, const BatchDev& b) {
+    const int64_t k = max_keys(sh, b);
+    return k < 4 ? 4 : (k + 3) / 4 * 4;
+}
+
+struct StepLayout {
+    size_t scores, idx, n_sel, attn, total;
+};
+
+StepLayout step_layout(const Shape& sh, const BatchDev& b) {
+    StepLayout L{};
+    size_t off = kWsHeaderBytes;
+    L.scores = off;
+    off = align_up(off + (size_t)b.n_q * default_ld(sh, b) * sizeof(float));
+    L.idx = off;
+    off = align_up(off + (size_t)b.n_q * sh.index_row_width() * sizeof(int32_t));
+    L.n_sel = off;
+    off = align_up(off + (size_t)b.n_q * sizeof(int32_t));
+    L.attn = off;
+    off = align_up(off + sparse_mla_scratch_bytes(sh, b.n_q, b.max_kv_len));
+    L.total = off;
+    return L;
+}
+
+size_t op_bytes(const Shape& sh, const BatchDev& b, int32_t op) {
+    switch (op) {
+        case DSA_OP_INDEX_SCORES:
+        case DSA_OP_TOPK_SELECT: return kWsHeaderBytes;
+        case DSA_OP_SPARSE_MLA:
+            return align_up(kWsHeaderBytes + sparse_mla_scratch_bytes(sh, b.n_q, b.max_kv_len));
+        case DSA_OP_DECODE_STEP: return step_layout(sh, b).total;
+        default: return 0;
+    }
+}
+
+dsa_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < need)
+        return DSA_ERR_WORKSPACE;
+    return DSA_OK;
+}
+
+dsa_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return DSA_OK;
+    if (trace_on()) fprintf(stderr, "[dsa] %s: %s\n", what, cudaGetErrorString(e));
+    return DSA_ERR_CUDA;
+}
+
+unsigned char* bytes(void* p) { return static_cast<unsigned char*>(p); }
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_status_string(int32_t status) {
+    switch (status) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARG: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported shape or size";
+        case DSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case DSA_ERR_CUDA: return "CUDA runtime or launch error";
+        case DSA_ERR_DEVICE: return "a kernel reported invalid data";
+        case DSA_ERR_TIMEOUT: return "a bounded device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int64_t dsa_index_row_width(const dsa_shape* shape) {
+    Shape sh;
+    if (check_shape(shape, &sh) != DSA_OK) return -1;
+    return sh.index_row_width();
+}
+
+dsa_status dsa_workspace_size(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
+                              size_t* out_bytes) {
+    Shape sh;
+    BatchDev b;
+    if (out_bytes == nullptr) return DSA_ERR_INVALID_ARG;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    // Sizing needs only the host scalars of the batch.
+    if (batch == nullptr || batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
+    if (batch->max_kv_len >= ((int64_t)1 << 31) || batch->n_q > 65535) return DSA_ERR_UNSUPPORTED;
+    b = BatchDev{nullptr, nullptr, nullptr, batch->n_seq, batch->n_q, batch->max_kv_len, sh.kpool};
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_DECODE_STEP) return DSA_ERR_INVALID_ARG;
+    *out_bytes = op_bytes(sh, b, op);
+    return DSA_OK;
+}
+
+dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
+                    dsa_plan_info* info) {
+    Shape sh;
+    if (info == nullptr || batch == nullptr) return DSA_ERR_INVALID_ARG;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if (batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_DECODE_STEP) return DSA_ERR_INVALID_ARG;
+    int32_t rps = 0, splits = 0;
+    plan_attention_splits(sh, batch->n_q > 0 ? batch->n_q : 1, batch->max_kv_len, &rps, &splits);
+    const int32_t attn = splits > 1 ? 2 : 1;
+    int32_t n = 0;
+    if (batch->n_q > 0) {
+        switch (op) {
+            case DSA_OP_INDEX_SCORES: n = batch->max_kv_len / sh.kpool > 0 ? 1 : 0; break;
+            case DSA_OP_TOPK_SELECT: n = 1; break;
+            case DSA_OP_SPARSE_MLA: n = attn; break;
+            default: n = (batch->max_kv_len / sh.kpool > 0 ? 1 : 0) + 1 + attn; break;
+        }
+    }
+    *info = dsa_plan_info{n, splits, rps, 0};
+    return DSA_OK;
+}
+
+dsa_status dsa_index_scores(const dsa_shape* shape, const dsa_batch* batch, const void* q_idx,
+                            const float* w, const void* k_idx, float* scores, int64_t ld,
+                            void* ws, size_t ws_bytes, void* stream) {
+    Shape sh;
+    BatchDev b;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    if (b.n_q > 0 && (q_idx == nullptr || w == nullptr || k_idx == nullptr || scores == nullptr))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(scores))
+        return DSA_ERR_INVALID_ARG;
+    if (ld < max_keys(sh, b) || ld < 1) return DSA_ERR_INVALID_ARG;
+    if ((s = check_ws(ws, ws_bytes, op_bytes(sh, b, DSA_OP_INDEX_SCORES))) != DSA_OK) return s;
+    int32_t* err = static_cast<int32_t*>(ws);
+    return cuda_status(launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld,
+                                           err, static_cast<cudaStream_t>(stream)),
+                       "index_scores");
+}
+
+dsa_status dsa_topk_select(const dsa_shape* shape, const dsa_batch* batch, const float* scores,
+                           int64_t ld, int32_t* idx, int32_t* n_sel, void* ws, size_t ws_bytes,
+                           void* stream) {
+    Shape sh;
+    BatchDev b;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    if (b.n_q > 0 && (scores == nullptr || idx == nullptr || n_sel == nullptr))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(scores) || !aligned16(idx) || !aligned16(n_sel)) return DSA_ERR_INVALID_ARG;
+    if (ld < max_keys(sh, b) || ld < 1) return DSA_ERR_INVALID_ARG;
+    if ((s = check_ws(ws, ws_bytes, op_bytes(sh, b, DSA_OP_TOPK_SELECT))) != DSA_OK) return s;
+    int32_t* err = static_cast<int32_t*>(ws);
+    return cuda_status(launch_topk_select(sh, b, scores, ld, idx, n_sel, err,
+                                          static_cast<cudaStream_t>(stream)),
+                       "topk_select");
+}
+
+dsa_status dsa_sparse_mla_attn(const dsa_shape* shape, const dsa_batch* batch, const void* q_abs,
+                               const void* cache, const int32_t* idx, const int32_t* n_sel,
+                               float* out, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    Shape sh;
+    BatchDev b;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    if (b.n_q > 0 && (q_abs == nullptr || cache == nullptr || idx == nullptr || n_sel == nullptr ||
+                      out == nullptr))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_abs) || !aligned16(cache) || !aligned16(out) || !aligned16(idx))
+        return DSA_ERR_INVALID_ARG;
+    const size_t need = op_bytes(sh, b, DSA_OP_SPARSE_MLA);
+    if ((s = check_ws(ws, ws_bytes, need)) != DSA_OK) return s;
+    int32_t* err = static_cast<int32_t*>(ws);
+    return cuda_status(launch_sparse_mla(sh, b, q_abs, cache, idx, n_sel, out, lse,
+                                         bytes(ws) + kWsHeaderBytes, need - kWsHeaderBytes, err,
+                                         static_cast<cudaStream_t>(stream)),
+                       "sparse_mla_attn");
+}
+
+dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const void* q_idx,
+                           const float* w, const void* k_idx, const void* q_abs,
+                           const void* cache, float* out, float* lse, int32_t* idx_out,
+                           int32_t* n_sel_out, void* ws, size_t ws_bytes, void* stream) {
+    Shape sh;
+    BatchDev b;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    if (b.n_q > 0 && (q_idx == nullptr || w == nullptr || k_idx == nullptr || q_abs == nullptr ||
+                      cache == nullptr || out == nullptr))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q_abs) ||
+        !aligned16(cache) || !aligned16(out) || !aligned16(idx_out) || !aligned16(n_sel_out))
+        return DSA_ERR_INVALID_ARG;
+    const StepLayout lay = step_layout(sh, b);
+    if ((s = check_ws(ws, ws_bytes, lay.total)) != DSA_OK) return s;
+    if (b.n_q == 0) return DSA_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* scores = reinterpret_cast<float*>(bytes(ws) + lay.scores);
+    int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(bytes(ws) + lay.idx);
+    int32_t* n_sel = n_sel_out ? n_sel_out : reinterpret_cast<int32_t*>(bytes(ws) + lay.n_sel);
+    const int64_t ld = default_ld(sh, b);
+    if (trace_on())
+        fprintf(stderr, "[dsa] decode_step n_q=%d max_kv=%lld ld=%lld ws=%zu\n", b.n_q,
+                (long long)b.max_kv_len, (long long)ld, lay.total);
+    cudaError_t e = launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld, err, st);
+    if (e != cudaSuccess) return cuda_status(e, "decode_step/index_scores");
+    e = launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
+    if (e != cudaSuccess) return cuda_status(e, "decode_step/topk_select");
+    e = launch_sparse_mla(sh, b, q_abs, cache, idx, n_sel, out, lse, bytes(ws) + lay.attn,
+                          lay.total - lay.attn, err, st);
+    return cuda_status(e, "decode_step/sparse_mla_attn");
+}
+
+dsa_status dsa_check_device_error(void* ws, size_t ws_bytes, void* stream, int32_t* code) {
+    if (ws == nullptr || ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e, "check_device_error/sync");
+    int32_t words[3] = {0, 0, 0};
+    e = cudaMemcpy(words, ws, sizeof(words), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e, "check_device_error/read");
+    if (code != nullptr) *code = words[0];
+    if (words[0] == 0) return DSA_OK;
+    if (trace_on())
+        fprintf(stderr, "[dsa] device error %d (detail %d, kernel %d)\n", words[0], words[1],
+                words[2]);
+    e = cudaMemset(ws, 0, sizeof(words));
+    if (e != cudaSuccess) return cuda_status(e, "check_device_error/clear");
+    return words[0] == kDevTimeout ? DSA_ERR_TIMEOUT : DSA_ERR_DEVICE;
+}
+
+dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (ws == nullptr || ws_bytes < kWsHeaderBytes ||
+        (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
+        return DSA_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(ws, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream)),
+                       "workspace_init");
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// dsa_common.cuh -- device helpers shared by the DSA kernels (sm_103a).
+//
+// Batch decoding (which sequence a query belongs to and how many rows it sees),
+// the device error word, element loads for the two input dtypes, and the
+// order-preserving float -> uint32 map the radix selection runs on.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+// Every workspace starts with this many bytes of header; word 0 is the device
+// error code, word 1 the first error's detail, word 2 the kernel that set it.
+constexpr size_t kWsHeaderBytes = 256;
+
+enum DeviceError : int32_t {
+    kDevOk = 0,
+    kDevBadIndex = 1,      // a selected index outside [0, L)
+    kDevBadBatch = 2,      // offsets inconsistent with the host bounds
+    kDevTimeout = 3,       // a bounded wait gave up
+};
+
+__device__ __forceinline__ void record_error(int32_t* err, int32_t code, int32_t detail,
+                                             int32_t where) {
+    if (err != nullptr && atomicCAS(err, 0, code) == 0) {
+        err[1] = detail;
+        err[2] = where;
+    }
+}
+
+// Batch description as the kernels receive it (plain device pointers).
+struct BatchDev {
+    const int64_t* row_off;
+    const int64_t* key_off;
+    const int64_t* q_off;
+    int32_t n_seq;
+    int32_t n_q;
+    int64_t max_kv_len;
+    int32_t kpool;
+};
+
+struct QueryInfo {
+    int32_t seq;
+    int64_t row0;      // first cache row of the sequence
+    int64_t key0;      // first indexer / pool key of the sequence
+    int64_t L;         // rows this query sees, its own included
+    int64_t n_keys;    // keys it scores: floor(L / kpool)
+};
+
+// Sequence of query q by binary search over q_off, then its visible length.
+// Returns false (and records kDevBadBatch) when the offsets contradict the
+// host bounds; the caller then skips the query.
+__device__ __forceinline__ bool query_info(const BatchDev& b, int64_t q, QueryInfo& qi,
+                                           int32_t* err, int32_t where) {
+    int32_t lo = 0, hi = b.n_seq - 1;
+    while (lo < hi) {                       // last s with q_off[s] <= q
+        int32_t mid = (lo + hi + 1) >> 1;
+        if (b.q_off[mid] <= q) lo = mid; else hi = mid - 1;
+    }
+    const int32_t s = lo;
+    const int64_t q0 = b.q_off[s], q1 = b.q_off[s + 1];
+    const int64_t r0 = b.row_off[s], r1 = b.row_off[s + 1];
+    const int64_t kv_len = r1 - r0, q_len = q1 - q0;
+    const int64_t L = kv_len - q_len + 1 + (q - q0);
+    if (q < q0 || q >= q1 || q_len > kv_len || kv_len > b.max_kv_len || L < 1) {
+        record_error(err, kDevBadBatch, (int32_t)q, where);
+        return false;
+    }
+    qi.seq = s;
+    qi.row0 = r0;
+    qi.key0 = b.key_off[s];
+    qi.L = L;
+    qi.n_keys = L / b.kpool;
+    if (b.key_off[s + 1] - qi.key0 < kv_len / b.kpool) {
+        record_error(err, kDevBadBatch, (int32_t)q, where);
+        return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Order-preserving map: a > b as floats  <=>  order_key(a) > order_key(b) as
+// unsigned integers.  Both zeros map to the key of +0 so that they tie and the
+// lower index wins, as for every other tie.  Inputs are finite.
+__device__ __forceinline__ uint32_t order_key(float s) {
+    const uint32_t u = (s == 0.0f) ? 0u : __float_as_uint(s);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace dsa

@@ -1,0 +1,42 @@
+// dsa_kernels.cuh -- host-side launchers of the DSA kernels (internal to libdsa).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dsa_common.cuh"
+
+namespace dsa {
+
+// Validated layer geometry (see dsa_shape in dsa.h).
+struct Shape {
+    int32_t idx_heads, idx_dim, heads, kv_lora, rope, top_k, kpool;
+    float scale;
+    int32_t dtype;                                   // DSA_F32 or DSA_BF16
+    int32_t width() const { return kv_lora + rope; } // cache row / q_abs head width
+    int64_t index_row_width() const { return (int64_t)top_k + kpool - 1; }
+    size_t elem_bytes() const { return dtype == DSA_F32 ? 4 : 2; }
+};
+
+// Step 1.  scores[q, t] for t < n_keys(q); grid covers max_keys keys.
+cudaError_t launch_index_scores(const Shape& sh, const BatchDev& b, int64_t max_keys,
+                                const void* q_idx, const float* w, const void* k_idx,
+                                float* scores, int64_t ld, int32_t* err, cudaStream_t st);
+
+// Step 2.  One selection row per query.
+cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* scores,
+                               int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
+                               cudaStream_t st);
+
+// Step 3.  Row splits per query (a multiple of 16 rows each) and the scratch
+// for the split-row partials (bytes; 0 if none is needed).
+void plan_attention_splits(const Shape& sh, int32_t n_q, int64_t max_kv_len,
+                           int32_t* rows_per_split, int32_t* n_split);
+size_t sparse_mla_scratch_bytes(const Shape& sh, int32_t n_q, int64_t max_kv_len);
+cudaError_t launch_sparse_mla(const Shape& sh, const BatchDev& b, const void* q_abs,
+                              const void* cache, const int32_t* idx, const int32_t* n_sel,
+                              float* out, float* lse, void* scratch, size_t scratch_bytes,
+                              int32_t* err, cudaStream_t st);
+
+}  // namespace dsa

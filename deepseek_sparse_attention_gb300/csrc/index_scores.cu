@@ -1,0 +1,105 @@
+// index_scores.cu -- lightning-indexer scoring, CUDA-core path.
+//
+// s_t = sum_h w_h * relu(q_h . k_t) for every key a query sees ("GLM 5.2 in one
+// C file", "The Lightning Indexer": per-head ReLU'd dot, weighted sum over
+// heads; "GLM-5.x (glm-dsa, glm5next)", "The block": 32 heads x 128).
+//
+// One CTA scores 128 consecutive keys of one query: the query's heads are
+// widened to float in shared memory, each thread owns one key row in registers
+// and accumulates the 32 head dots in float.  This path serves float32 inputs
+// and is the reference point the tensor-core path is measured against.
+#include "dsa_kernels.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kDim = 128;        // indexer head width this build supports
+constexpr int kMaxHeads = 64;
+constexpr int kKeysPerCta = 128;
+
+__device__ __forceinline__ void load_row(const float* __restrict__ src, float* dst) {
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+    for (int i = 0; i < kDim / 4; ++i) {
+        const float4 v = __ldg(s4 + i);
+        dst[4 * i + 0] = v.x; dst[4 * i + 1] = v.y; dst[4 * i + 2] = v.z; dst[4 * i + 3] = v.w;
+    }
+}
+
+__device__ __forceinline__ void load_row(const __nv_bfloat16* __restrict__ src, float* dst) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int i = 0; i < kDim / 8; ++i) {
+        const uint4 v = __ldg(s4 + i);
+        const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&wds[j]);
+            const float2 f = __bfloat1622float2(p);
+            dst[8 * i + 2 * j + 0] = f.x;
+            dst[8 * i + 2 * j + 1] = f.y;
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kKeysPerCta)
+index_scores_simt(BatchDev b, int32_t hi, const T* __restrict__ q_idx,
+                  const float* __restrict__ w, const T* __restrict__ k_idx,
+                  float* __restrict__ scores, int64_t ld, int32_t* err) {
+    __shared__ float4 qs[kMaxHeads * kDim / 4];
+    __shared__ float wsh[kMaxHeads];
+    const int64_t q = blockIdx.y;
+    QueryInfo qi;
+    if (!query_info(b, q, qi, err, /*where=*/1)) return;          // uniform in the CTA
+    const int64_t t0 = (int64_t)blockIdx.x * kKeysPerCta;
+    if (t0 >= qi.n_keys) return;
+
+    const T* qsrc = q_idx + q * (int64_t)hi * kDim;
+    float* qf = reinterpret_cast<float*>(qs);
+    for (int i = threadIdx.x; i < hi * kDim; i += blockDim.x) qf[i] = to_float(qsrc[i]);
+    for (int i = threadIdx.x; i < hi; i += blockDim.x) wsh[i] = w[q * hi + i];
+    __syncthreads();
+
+    const int64_t t = t0 + threadIdx.x;
+    if (t >= qi.n_keys) return;
+    float key[kDim];
+    load_row(k_idx + (qi.key0 + t) * kDim, key);
+
+    float acc = 0.f;
+    for (int h = 0; h < hi; ++h) {
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < kDim / 4; ++c) {
+            const float4 qv = qs[h * (kDim / 4) + c];
+            d0 = fmaf(qv.x, key[4 * c + 0], d0);
+            d1 = fmaf(qv.y, key[4 * c + 1], d1);
+            d2 = fmaf(qv.z, key[4 * c + 2], d2);
+            d3 = fmaf(qv.w, key[4 * c + 3], d3);
+        }
+        const float d = (d0 + d1) + (d2 + d3);
+        acc = fmaf(wsh[h], fmaxf(d, 0.f), acc);                      // weight * relu
+    }
+    scores[q * ld + t] = acc;
+}
+
+}  // namespace
+
+cudaError_t launch_index_scores(const Shape& sh, const BatchDev& b, int64_t max_keys,
+                                const void* q_idx, const float* w, const void* k_idx,
+                                float* scores, int64_t ld, int32_t* err, cudaStream_t st) {
+    if (b.n_q == 0 || max_keys == 0) return cudaSuccess;
+    const dim3 grid((unsigned)((max_keys + kKeysPerCta - 1) / kKeysPerCta), (unsigned)b.n_q);
+    if (sh.dtype == DSA_F32) {
+        index_scores_simt<float><<<grid, kKeysPerCta, 0, st>>>(
+            b, sh.idx_heads, static_cast<const float*>(q_idx), w,
+            static_cast<const float*>(k_idx), scores, ld, err);
+    } else {
+        index_scores_simt<__nv_bfloat16><<<grid, kKeysPerCta, 0, st>>>(
+            b, sh.idx_heads, static_cast<const __nv_bfloat16*>(q_idx), w,
+            static_cast<const __nv_bfloat16*>(k_idx), scores, ld, err);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dsa

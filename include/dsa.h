@@ -1,0 +1,210 @@
+/*
+ * dsa.h -- C ABI of the GB300 DeepSeek-Sparse-Attention hot path (libdsa.so).
+ *
+ * The hot path of one DSA attention layer, for a batch of queries over their
+ * sequences' caches:
+ *
+ *   1. lightning-indexer scores   s_t = sum_h w_h * relu(q_h . k_t)
+ *   2. per-query top-k selection  (or top k/kpool pools + the unfilled tail)
+ *   3. absorbed-MLA attention     over only the selected 576-wide (512 latent +
+ *      64 rope) or 512-wide (NoPE) cache rows, output in the 512-wide latent
+ *
+ * Sources (page title -- section):
+ *   "GLM-5.x (glm-dsa, glm5next)" (TensorSharp model notes) -- "The block"
+ *     (64 query heads, one 576-wide cache row per token, indexer 32 x 128,
+ *     top-k 2048, softmax scale 1/16); "The sparse-attention path" (dense
+ *     below top-k, mask unmasked at the selected positions); "GLM-5.3-Flash"
+ *     table, row "Pooled indexer" (4-token pools, dense below 2051 tokens).
+ *   "GLM-5.3-Flash on WASTE" -- "DeepSeek Sparse Attention, k-pool flavour".
+ *   "GLM 5.2 in one C file" (blog) -- "Attention: Multi head Latent Attention
+ *     With a Tiny KV Cache" (absorbed decode path); "The Lightning Indexer".
+ *   "Add GLM-5.3-Flash support" (Strata pull request) -- absorbed NoPE MLA
+ *     (K and V are the same 512-wide latent, scale 1/sqrt(256)).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a DEVICE pointer owned by the caller, row-major and
+ *   densely packed as documented; the library never allocates, frees or keeps a
+ *   pointer past the call.  Scratch memory is the caller's workspace `ws` of
+ *   `ws_bytes` bytes (256-byte aligned), sized by dsa_workspace_size().
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Calls only enqueue work on it: they never synchronise, except
+ *   dsa_check_device_error().
+ * - Arguments are validated on the host before anything is enqueued; a bad
+ *   argument returns DSA_ERR_INVALID_ARG (malformed) or DSA_ERR_UNSUPPORTED
+ *   (well formed but outside what this build implements) and enqueues nothing.
+ *   A failed launch returns DSA_ERR_CUDA.  Conditions only the device can see
+ *   (an index out of range, a sequence shorter than its queries) set an error
+ *   word in the workspace and the affected output is left as written by the
+ *   kernel; dsa_check_device_error() reads and clears it.
+ * - No exceptions cross the ABI.  There is no global mutable state beyond
+ *   per-device attribute caches, so calls on different streams may run
+ *   concurrently as long as they use distinct workspaces.
+ *
+ * Batch layout (varlen, causal, aligned to the end of each sequence)
+ * ------------------------------------------------------------------
+ * Sequence s owns cache rows row_off[s] .. row_off[s+1]-1 (kv_len_s rows),
+ * indexer keys key_off[s] .. key_off[s+1]-1 and queries q_off[s] .. q_off[s+1]-1
+ * (q_len_s queries, q_len_s <= kv_len_s).  Query i of sequence s sees
+ *     L = kv_len_s - q_len_s + 1 + i
+ * rows, its own row included: decode is q_len_s = 1 (L = kv_len_s); a chunk of
+ * prefill is q_len_s > 1.  With kpool == 1 a sequence has one indexer key per
+ * row (key_off may equal row_off); with kpool > 1 it has floor(kv_len_s/kpool)
+ * pool keys and a query scores the first floor(L/kpool) of them.
+ * Selected indices are row indices RELATIVE TO THE SEQUENCE.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+typedef enum {
+    DSA_OK = 0,
+    DSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shape */
+    DSA_ERR_UNSUPPORTED = 2,   /* valid, but outside what this build implements  */
+    DSA_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small      */
+    DSA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed            */
+    DSA_ERR_DEVICE = 5,        /* a kernel reported bad data (error word set)     */
+    DSA_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up              */
+} dsa_status;
+
+typedef enum {
+    DSA_F32 = 0,               /* float32 q_idx, k_idx, q_abs, cache              */
+    DSA_BF16 = 1               /* bfloat16 q_idx, k_idx, q_abs, cache             */
+} dsa_dtype;
+
+/* Layer geometry.  The weights w and all outputs are float32 in both dtypes. */
+typedef struct {
+    int32_t idx_heads;         /* indexer heads Hi (32)                           */
+    int32_t idx_dim;           /* indexer head width Di (128)                     */
+    int32_t heads;             /* MLA query heads H (64); one shared KV head      */
+    int32_t kv_lora;           /* latent width, the value width (512)             */
+    int32_t rope_dim;          /* rope tail of a cache row (64), 0 for NoPE       */
+    int32_t top_k;             /* tokens kept per query (2048)                    */
+    int32_t kpool;             /* 1 = token mode; 4 = one pool key per 4 tokens   */
+    float scale;               /* softmax scale (1/16 = 1/sqrt(256))              */
+    int32_t dtype;             /* a dsa_dtype                                     */
+} dsa_shape;
+
+/* Batch description.  The three offset arrays are DEVICE arrays of n_seq+1
+ * non-decreasing int64 values starting at 0; the host scalars must bound them
+ * (they size grids and are checked on the device). */
+typedef struct {
+    int32_t n_seq;             /* sequences                                        */
+    int32_t n_q;               /* queries in total, = q_off[n_seq]                 */
+    int32_t max_q_len;         /* host bound: max_s q_len_s                        */
+    int32_t reserved;          /* must be 0                                        */
+    int64_t max_kv_len;        /* host bound: max_s kv_len_s (< 2^31)              */
+    const int64_t *row_off;    /* device [n_seq+1] cache-row offsets               */
+    const int64_t *key_off;    /* device [n_seq+1] indexer-key / pool-key offsets  */
+    const int64_t *q_off;      /* device [n_seq+1] query offsets                   */
+} dsa_batch;
+
+/* Library version (DSA_ABI_VERSION) and a static description of a status. */
+int dsa_version(void);
+const char *dsa_status_string(int32_t status);
+
+/* Width of one query's index row: top_k + kpool - 1 when the query's selection
+ * is sparse, and the dense selection of a query with L <= that bound also fits. */
+int64_t dsa_index_row_width(const dsa_shape *shape);
+
+/* Bytes of workspace each entry point needs for this shape and batch bound
+ * (host-only, enqueues nothing).  `op` is one of the DSA_OP_* values.  The
+ * same workspace may be reused by consecutive calls on one stream. */
+#define DSA_OP_INDEX_SCORES 0
+#define DSA_OP_TOPK_SELECT 1
+#define DSA_OP_SPARSE_MLA 2
+#define DSA_OP_DECODE_STEP 3
+dsa_status dsa_workspace_size(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
+                              size_t *bytes);
+
+/* Execution plan of one entry point for this shape and batch bound (host-only,
+ * enqueues nothing): how many kernels it launches, and into how many row
+ * splits the attention step divides each query's selection. */
+typedef struct {
+    int32_t kernel_launches;   /* kernels one call enqueues                        */
+    int32_t attn_splits;       /* row splits per query in the attention step       */
+    int32_t attn_rows_per_split;
+    int32_t reserved;
+} dsa_plan_info;
+dsa_status dsa_plan(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
+                    dsa_plan_info *info);
+
+/* Zeroes the workspace header (its device error word) on `stream`.  Call once
+ * on a freshly allocated workspace that was not allocated zero-filled; after
+ * that dsa_check_device_error() keeps the word clear.  `ws` must be 256-byte
+ * aligned and at least 256 bytes. */
+dsa_status dsa_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Step 1: lightning-indexer scores ("GLM 5.2 in one C file", "The Lightning
+ * Indexer"; "GLM-5.x", "The block", row "DSA indexer").
+ *   q_idx  [n_q, idx_heads, idx_dim]   dtype
+ *   w      [n_q, idx_heads]            float32
+ *   k_idx  [key_off[n_seq], idx_dim]   dtype (token keys, or pool keys)
+ *   scores [n_q, ld] float32 out: scores[q, t] = sum_h w[q,h] *
+ *          relu(q_idx[q,h,:] . k_idx[key_off[s]+t, :]) for t < n_keys(q),
+ *          where n_keys(q) = floor(L/kpool); entries t >= n_keys(q) are not written.
+ *   ld >= floor(max_kv_len / kpool).  The page's positive factors 1/sqrt(Di) and
+ *   1/sqrt(Hi) are not applied: they fold into w and do not change a selection. */
+dsa_status dsa_index_scores(const dsa_shape *shape, const dsa_batch *batch, const void *q_idx,
+                            const float *w, const void *k_idx, float *scores, int64_t ld,
+                            void *ws, size_t ws_bytes, void *stream);
+
+/* Step 2: per-query selection from the scores of step 1.
+ *   kpool == 1: if L <= top_k every row 0..L-1; else the top_k rows in the
+ *   order (score descending, index ascending) -- ties go to the lower index.
+ *   kpool > 1 ("GLM-5.3-Flash on WASTE", k-pool flavour): with n_pool =
+ *   floor(L/kpool) and tail = L mod kpool, if n_pool <= top_k/kpool every row
+ *   0..L-1; else the top top_k/kpool pools in the same order, expanded to their
+ *   kpool rows, followed by the tail rows kpool*n_pool .. L-1.
+ *   idx   [n_q, dsa_index_row_width(shape)] int32 out: ascending row indices,
+ *         unused slots set to -1;
+ *   n_sel [n_q] int32 out: number of valid entries (dense: L; sparse: top_k
+ *         plus the tail).
+ * A dense selection always fits the row width: it has L <= top_k + kpool - 1
+ * rows. */
+dsa_status dsa_topk_select(const dsa_shape *shape, const dsa_batch *batch, const float *scores,
+                           int64_t ld, int32_t *idx, int32_t *n_sel, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/* Step 3: absorbed-MLA attention over the selected rows ("GLM 5.2 in one C
+ * file", MLA decode path; "GLM-5.x", "The block").
+ *   q_abs [n_q, heads, kv_lora + rope_dim] dtype (absorbed latent part, then rope)
+ *   cache [row_off[n_seq], kv_lora + rope_dim] dtype
+ *   idx, n_sel as produced by dsa_topk_select (any order is accepted; each
+ *   index must satisfy 0 <= idx < L, otherwise the error word is set and the
+ *   row is skipped)
+ *   out [n_q, heads, kv_lora] float32: o = sum_j softmax_j(z)_j * latent_j with
+ *       z_j = scale * (q_abs . row_j) over the full row width
+ *   lse [n_q, heads] float32 or NULL: log sum_j exp(z_j).
+ * A query with n_sel == 0 gets out = 0 and lse = -inf. */
+dsa_status dsa_sparse_mla_attn(const dsa_shape *shape, const dsa_batch *batch, const void *q_abs,
+                               const void *cache, const int32_t *idx, const int32_t *n_sel,
+                               float *out, float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* The whole hot path for every query of the batch: steps 1-3 in one call.
+ * Scores and selections live in the workspace unless idx_out / n_sel_out are
+ * given (then the selection is also written there, laid out as for
+ * dsa_topk_select).  Works for decode and for chunks of prefill alike. */
+dsa_status dsa_decode_step(const dsa_shape *shape, const dsa_batch *batch, const void *q_idx,
+                           const float *w, const void *k_idx, const void *q_abs,
+                           const void *cache, float *out, float *lse, int32_t *idx_out,
+                           int32_t *n_sel_out, void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the workspace error word.
+ * *code (may be NULL) receives the first device-side error recorded (0 if
+ * none).  Returns DSA_OK, DSA_ERR_DEVICE / DSA_ERR_TIMEOUT when a kernel
+ * reported one, or DSA_ERR_CUDA. */
+dsa_status dsa_check_device_error(void *ws, size_t ws_bytes, void *stream, int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H */

@@ -1,0 +1,127 @@
+"""The C-ABI library loads, exports every symbol its header declares, and
+rejects bad arguments on the host before touching a device.  CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import deepseek_sparse_attention_gb300 as dsa
+from deepseek_sparse_attention_gb300 import build as dsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dsa_build.build()
+    return dsa.load()
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(dsa_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("dsa_index_scores", "dsa_topk_select", "dsa_sparse_mla_attn", "dsa_decode_step",
+              "dsa_workspace_size", "dsa_check_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert missing == []
+
+
+def test_version_and_row_width(lib):
+    assert dsa.dsa_version() == 1
+    assert dsa.dsa_index_row_width(dsa.make_shape(kpool=1)) == 2048
+    assert dsa.dsa_index_row_width(dsa.make_shape(kpool=4)) == 2051
+    assert dsa.dsa_index_row_width(dsa.make_shape(heads=32)) == -1   # unsupported geometry
+
+
+def _batch(n_seq=1, n_q=1, max_q=1, max_kv=4096):
+    b = dsa.Batch(n_seq, n_q, max_q, 0, max_kv, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                  ctypes.c_void_p(16))
+    return b
+
+
+def _size(shape, batch, op):
+    n = ctypes.c_size_t(0)
+    rc = dsa.load().dsa_workspace_size(ctypes.byref(shape), ctypes.byref(batch), op,
+                                       ctypes.byref(n))
+    return rc, n.value
+
+
+def test_workspace_sizes(lib):
+    sh = dsa.make_shape()
+    rc, n = _size(sh, _batch(max_kv=131072), dsa.OP_DECODE_STEP)
+    assert rc == 0
+    # header + scores (131072 floats) + one index row + n_sel, 256-byte aligned
+    assert n >= 256 + 131072 * 4 + 2048 * 4 + 4 and n % 256 == 0
+    rc, n = _size(sh, _batch(), dsa.OP_INDEX_SCORES)
+    assert rc == 0 and n == 256
+    rc, _ = _size(sh, _batch(), 7)
+    assert rc == 1
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("heads", 32, 2), ("idx_dim", 64, 2), ("kv_lora", 256, 2), ("rope_dim", 32, 2),
+    ("top_k", 0, 1), ("kpool", 0, 1), ("scale", float("nan"), 1), ("scale", -1.0, 1),
+    ("dtype", 7, 1),
+])
+def test_shape_validation(lib, field, value, code):
+    sh = dsa.make_shape(kpool=1)
+    setattr(sh, field, value)
+    rc, _ = _size(sh, _batch(), dsa.OP_DECODE_STEP)
+    assert rc == code
+
+
+def test_topk_not_multiple_of_kpool_rejected(lib):
+    sh = dsa.make_shape(top_k=2046, kpool=4)
+    assert _size(sh, _batch(), dsa.OP_DECODE_STEP)[0] == 1
+
+
+def test_entry_points_reject_before_enqueue(lib):
+    """Each call below is malformed; it must return its status without any CUDA
+    call (there is no device here, so an enqueue would surface as DSA_ERR_CUDA)."""
+    sh = dsa.make_shape()
+    P = ctypes.c_void_p
+    good = P(256)
+    b = _batch()
+    assert lib.dsa_index_scores(None, ctypes.byref(b), good, good, good, good, 4096, good, 256,
+                                None) == 1
+    assert lib.dsa_index_scores(ctypes.byref(sh), ctypes.byref(b), None, good, good, good, 4096,
+                                good, 256, None) == 1
+    assert lib.dsa_index_scores(ctypes.byref(sh), ctypes.byref(b), good, good, good, good, 100,
+                                good, 256, None) == 1          # ld too small
+    assert lib.dsa_index_scores(ctypes.byref(sh), ctypes.byref(b), good, good, good, good, 4096,
+                                None, 256, None) == 3          # no workspace
+    assert lib.dsa_index_scores(ctypes.byref(sh), ctypes.byref(b), good, good, good, good, 4096,
+                                P(264), 256, None) == 3        # misaligned workspace
+    assert lib.dsa_index_scores(ctypes.byref(sh), ctypes.byref(b), P(258), good, good, good,
+                                4096, good, 256, None) == 1    # misaligned tensor
+    bad = _batch(max_q=2, max_kv=1)
+    assert lib.dsa_topk_select(ctypes.byref(sh), ctypes.byref(bad), good, 4096, good, good, good,
+                               256, None) == 1
+    big = _batch(max_kv=1 << 31)
+    assert lib.dsa_sparse_mla_attn(ctypes.byref(sh), ctypes.byref(big), good, good, good, good,
+                                   good, None, good, 1 << 20, None) == 2
+    assert lib.dsa_decode_step(ctypes.byref(sh), ctypes.byref(b), good, good, good, good, good,
+                               good, None, None, None, good, 16, None) == 3   # ws too small
+    assert lib.dsa_check_device_error(None, 0, None, None) == 3
+
+
+def test_python_binding_rejects_host_tensors(lib):
+    sh = dsa.make_shape()
+    with pytest.raises(ValueError):
+        dsa._ptr(torch.zeros(4))

@@ -161,11 +161,12 @@ def make(wl: Workload, device="cpu", copies: int = 1) -> Dict[str, object]:
         out = [0]
         for x in xs:
             out.append(out[-1] + x)
-        return torch.tensor(out, dtype=torch.int64)
+        return torch.tensor(out, dtype=torch.int64, device=device)
 
     d["row_off"] = prefix(wl.kv_lens)
     d["key_off"] = prefix(wl.key_counts())
     d["q_off"] = prefix(wl.q_lens)
+    # host-side bookkeeping (never passed to the library)
     d["q_nvis"] = torch.tensor(wl.q_nvis(), dtype=torch.int64)
     d["q_seq"] = torch.tensor([s for s, nq in enumerate(wl.q_lens) for _ in range(nq)],
                               dtype=torch.int32)
