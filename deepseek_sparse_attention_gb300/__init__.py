@@ -30,7 +30,7 @@ __all__ = [
     "DsaError", "Shape", "Batch", "load", "make_shape", "make_batch", "workspace_size",
     "alloc_workspace", "dsa_version", "dsa_index_row_width", "dsa_workspace_size",
     "dsa_workspace_init", "dsa_plan", "dsa_index_scores", "dsa_topk_select", "dsa_sparse_mla_attn",
-    "dsa_decode_step", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
+    "dsa_decode_step", "dsa_decode_step_noalloc", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
     "OP_INDEX_SCORES", "OP_TOPK_SELECT", "OP_SPARSE_MLA", "OP_DECODE_STEP",
 ]
 
@@ -96,6 +96,7 @@ def load() -> ctypes.CDLL:
             "dsa_sparse_mla_attn": ([S, B, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_decode_step": ([S, B, P, P, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_check_device_error": ([P, sz, P, ctypes.POINTER(i32)], ctypes.c_int),
+            "dsa_decode_step_noalloc": ([S, B, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -211,6 +212,15 @@ def dsa_decode_step(shape, batch, q_idx, w, k_idx, q_abs, cache, out, lse=None, 
     _call("dsa_decode_step", ctypes.byref(shape), ctypes.byref(batch), _ptr(q_idx), _ptr(w),
           _ptr(k_idx), _ptr(q_abs), _ptr(cache), _ptr(out), _ptr(lse), _ptr(idx_out),
           _ptr(n_sel_out), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream))
+
+
+def dsa_decode_step_noalloc(shape, batch, q_idx, w, k_idx, q_abs, cache, out, lse=None,
+                            idx_out=None, n_sel_out=None, stream=None) -> None:
+    """dsa_decode_step without a workspace, for callers that cannot allocate
+    device memory: the scratch is a fixed array inside libdsa (see dsa.h)."""
+    _call("dsa_decode_step_noalloc", ctypes.byref(shape), ctypes.byref(batch), _ptr(q_idx),
+          _ptr(w), _ptr(k_idx), _ptr(q_abs), _ptr(cache), _ptr(out), _ptr(lse), _ptr(idx_out),
+          _ptr(n_sel_out), _stream(stream))
 
 
 def dsa_check_device_error(ws: torch.Tensor, stream=None) -> int:

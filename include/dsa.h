@@ -198,6 +198,32 @@ dsa_status dsa_decode_step(const dsa_shape *shape, const dsa_batch *batch, const
                            const void *cache, float *out, float *lse, int32_t *idx_out,
                            int32_t *n_sel_out, void *ws, size_t ws_bytes, void *stream);
 
+/* dsa_decode_step for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a convenience of this library.  Some callers may
+ * not call cudaMalloc where they run the layer -- while a framework captures
+ * the stream into a CUDA graph, inside a host engine that gives a plugin only
+ * its input and output buffers, or in a loop that cannot afford cudaMalloc's
+ * implicit device synchronisation.  This entry point takes no workspace: its
+ * scratch is one fixed array of DSA_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, held by every GPU that loads it until the process exits, and it
+ * calls no allocator.
+ *   Arguments and results are those of dsa_decode_step without ws/ws_bytes.
+ *   Returns DSA_ERR_UNSUPPORTED when the step needs more scratch than the
+ *   array holds (dsa_workspace_size(DSA_OP_DECODE_STEP) > the limit; a batch-1
+ *   decode at 131072 tokens needs under 5 MiB).
+ *   The first call on a device looks up the array's device address (with that
+ *   device current) and caches it; make that first call before any stream
+ *   capture.  All calls share the array and it keeps the previous call's
+ *   contents; each call zeroes its error word on `stream` first.  Calls whose
+ *   work overlaps on the GPU (other streams, other threads) race on the array:
+ *   serialise them.  Device-side checks record into the array's error word,
+ *   which is not reported back; use dsa_decode_step to read it. */
+#define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+dsa_status dsa_decode_step_noalloc(const dsa_shape *shape, const dsa_batch *batch,
+                                   const void *q_idx, const float *w, const void *k_idx,
+                                   const void *q_abs, const void *cache, float *out, float *lse,
+                                   int32_t *idx_out, int32_t *n_sel_out, void *stream);
+
 /* Synchronises `stream`, then reads and clears the workspace error word.
  * *code (may be NULL) receives the first device-side error recorded (0 if
  * none).  Returns DSA_OK, DSA_ERR_DEVICE / DSA_ERR_TIMEOUT when a kernel
