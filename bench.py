@@ -349,7 +349,7 @@ def run_ours(args):
     sh = dsa.make_shape(wl.idx_heads, wl.idx_dim, wl.heads, wl.kv_lora, wl.rope, wl.top_k,
                         wl.kpool, wl.scale, wl.dtype)
     b = dsa.make_batch(d["row_off"], d["key_off"], d["q_off"], wl.n_q, max(wl.q_lens),
-                       max(wl.kv_lens))
+                       max(wl.kv_lens), sum(wl.kv_lens), sum(wl.key_counts()))
     ws = dsa.alloc_workspace(sh, b, dsa.OP_DECODE_STEP, dev)
     width = dsa.dsa_index_row_width(sh)
     plan = dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP)

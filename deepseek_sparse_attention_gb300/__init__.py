@@ -58,7 +58,8 @@ class Shape(ctypes.Structure):
 class Batch(ctypes.Structure):
     _fields_ = [("n_seq", ctypes.c_int32), ("n_q", ctypes.c_int32),
                 ("max_q_len", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("max_kv_len", ctypes.c_int64), ("row_off", ctypes.c_void_p),
+                ("max_kv_len", ctypes.c_int64), ("total_rows", ctypes.c_int64),
+                ("total_keys", ctypes.c_int64), ("row_off", ctypes.c_void_p),
                 ("key_off", ctypes.c_void_p), ("q_off", ctypes.c_void_p)]
 
 
@@ -138,18 +139,19 @@ def make_shape(idx_heads=32, idx_dim=128, heads=64, kv_lora=512, rope_dim=64, to
 
 
 def make_batch(row_off: torch.Tensor, key_off: torch.Tensor, q_off: torch.Tensor, n_q: int,
-               max_q_len: int, max_kv_len: int) -> Batch:
+               max_q_len: int, max_kv_len: int, total_rows: int, total_keys: int) -> Batch:
     """Batch descriptor over int64 device offset arrays of n_seq+1 entries.
 
-    The returned structure holds raw pointers: keep the three tensors alive
-    while it is in use.
+    ``total_rows`` / ``total_keys`` are the row counts of the cache and key
+    tensors.  The returned structure holds raw pointers: keep the three
+    tensors alive while it is in use.
     """
     for t in (row_off, key_off, q_off):
         if t.dtype != torch.int64:
             raise ValueError("offset arrays are int64")
     n_seq = row_off.numel() - 1
-    b = Batch(n_seq, int(n_q), int(max_q_len), 0, int(max_kv_len), _ptr(row_off), _ptr(key_off),
-              _ptr(q_off))
+    b = Batch(n_seq, int(n_q), int(max_q_len), 0, int(max_kv_len), int(total_rows),
+              int(total_keys), _ptr(row_off), _ptr(key_off), _ptr(q_off))
     b._keep = (row_off, key_off, q_off)
     return b
 
@@ -244,7 +246,8 @@ class DecodeStep:
     def __init__(self, wl, row_off, key_off, q_off, device="cuda"):
         self.shape = make_shape(wl.idx_heads, wl.idx_dim, wl.heads, wl.kv_lora, wl.rope, wl.top_k,
                                 wl.kpool, wl.scale, wl.dtype)
-        self.batch = make_batch(row_off, key_off, q_off, wl.n_q, max(wl.q_lens), max(wl.kv_lens))
+        self.batch = make_batch(row_off, key_off, q_off, wl.n_q, max(wl.q_lens), max(wl.kv_lens),
+                                sum(wl.kv_lens), sum(wl.key_counts()))
         self.ws = alloc_workspace(self.shape, self.batch, OP_DECODE_STEP, device)
         self.width = dsa_index_row_width(self.shape)
         self.n_q = wl.n_q

@@ -44,17 +44,20 @@ dsa_status check_shape(const dsa_shape* s, Shape* out) {
 
 dsa_status check_batch(const dsa_batch* b, const Shape& sh, BatchDev* out) {
     if (b == nullptr) return DSA_ERR_INVALID_ARG;
-    if (b->n_seq < 0 || b->n_q < 0 || b->max_q_len < 0 || b->max_kv_len < 0 || b->reserved != 0)
+    if (b->n_seq < 0 || b->n_q < 0 || b->max_q_len < 0 || b->max_kv_len < 0 || b->reserved != 0 ||
+        b->total_rows < 0 || b->total_keys < 0)
         return DSA_ERR_INVALID_ARG;
     if (b->n_q > 0) {
         if (b->n_seq < 1 || b->row_off == nullptr || b->key_off == nullptr || b->q_off == nullptr)
             return DSA_ERR_INVALID_ARG;
         if (b->max_q_len < 1 || b->max_kv_len < b->max_q_len) return DSA_ERR_INVALID_ARG;
         if ((int64_t)b->max_q_len > (int64_t)b->n_q) return DSA_ERR_INVALID_ARG;
+        if (b->total_rows < 1) return DSA_ERR_INVALID_ARG;
     }
     if (b->max_kv_len >= ((int64_t)1 << 31)) return DSA_ERR_UNSUPPORTED;
     if (b->n_q > 65535) return DSA_ERR_UNSUPPORTED;
-    *out = BatchDev{b->row_off, b->key_off, b->q_off, b->n_seq, b->n_q, b->max_kv_len, sh.kpool};
+    *out = BatchDev{b->row_off,    b->key_off,    b->q_off,      b->n_seq, b->n_q,
+                    b->max_q_len,  b->max_kv_len, b->total_rows, b->total_keys, sh.kpool};
     return DSA_OK;
 }
 
@@ -66,12 +69,14 @@ int64_t default_ld(const Shape& sh, const BatchDev& b) {
 }
 
 struct StepLayout {
-    size_t scores, idx, n_sel, attn, total;
+    size_t idx_plan, scores, idx, n_sel, attn, total;
 };
 
 StepLayout step_layout(const Shape& sh, const BatchDev& b) {
     StepLayout L{};
     size_t off = kWsHeaderBytes;
+    L.idx_plan = off;
+    off = align_up(off + index_scores_scratch_bytes(sh, b));
     L.scores = off;
     off = align_up(off + (size_t)b.n_q * default_ld(sh, b) * sizeof(float));
     L.idx = off;
@@ -87,6 +92,7 @@ StepLayout step_layout(const Shape& sh, const BatchDev& b) {
 size_t op_bytes(const Shape& sh, const BatchDev& b, int32_t op) {
     switch (op) {
         case DSA_OP_INDEX_SCORES:
+            return align_up(kWsHeaderBytes + index_scores_scratch_bytes(sh, b));
         case DSA_OP_TOPK_SELECT: return kWsHeaderBytes;
         case DSA_OP_SPARSE_MLA:
             return align_up(kWsHeaderBytes + sparse_mla_scratch_bytes(sh, b.n_q, b.max_kv_len));
@@ -147,7 +153,9 @@ dsa_status dsa_workspace_size(const dsa_shape* shape, const dsa_batch* batch, in
     // Sizing needs only the host scalars of the batch.
     if (batch == nullptr || batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
     if (batch->max_kv_len >= ((int64_t)1 << 31) || batch->n_q > 65535) return DSA_ERR_UNSUPPORTED;
-    b = BatchDev{nullptr, nullptr, nullptr, batch->n_seq, batch->n_q, batch->max_kv_len, sh.kpool};
+    b = BatchDev{nullptr,           nullptr,           nullptr,           batch->n_seq,
+                 batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
+                 batch->total_keys, sh.kpool};
     if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_DECODE_STEP) return DSA_ERR_INVALID_ARG;
     *out_bytes = op_bytes(sh, b, op);
     return DSA_OK;
@@ -164,13 +172,18 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
     int32_t rps = 0, splits = 0;
     plan_attention_splits(sh, batch->n_q > 0 ? batch->n_q : 1, batch->max_kv_len, &rps, &splits);
     const int32_t attn = splits > 1 ? 2 : 1;
+    const BatchDev bh{nullptr,           nullptr,           nullptr,           batch->n_seq,
+                      batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
+                      batch->total_keys, sh.kpool};
+    const int32_t idx = batch->max_kv_len / sh.kpool > 0
+                            ? (index_scores_tc_eligible(sh, bh) ? 2 : 1) : 0;
     int32_t n = 0;
     if (batch->n_q > 0) {
         switch (op) {
-            case DSA_OP_INDEX_SCORES: n = batch->max_kv_len / sh.kpool > 0 ? 1 : 0; break;
+            case DSA_OP_INDEX_SCORES: n = idx; break;
             case DSA_OP_TOPK_SELECT: n = 1; break;
             case DSA_OP_SPARSE_MLA: n = attn; break;
-            default: n = (batch->max_kv_len / sh.kpool > 0 ? 1 : 0) + 1 + attn; break;
+            default: n = idx + 1 + attn; break;
         }
     }
     *info = dsa_plan_info{n, splits, rps, 0};
@@ -193,7 +206,8 @@ dsa_status dsa_index_scores(const dsa_shape* shape, const dsa_batch* batch, cons
     if ((s = check_ws(ws, ws_bytes, op_bytes(sh, b, DSA_OP_INDEX_SCORES))) != DSA_OK) return s;
     int32_t* err = static_cast<int32_t*>(ws);
     return cuda_status(launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld,
-                                           err, static_cast<cudaStream_t>(stream)),
+                                           bytes(ws) + kWsHeaderBytes, err,
+                                           static_cast<cudaStream_t>(stream)),
                        "index_scores");
 }
 
@@ -265,7 +279,8 @@ dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const
     if (trace_on())
         fprintf(stderr, "[dsa] decode_step n_q=%d max_kv=%lld ld=%lld ws=%zu\n", b.n_q,
                 (long long)b.max_kv_len, (long long)ld, lay.total);
-    cudaError_t e = launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld, err, st);
+    cudaError_t e = launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld,
+                                        bytes(ws) + lay.idx_plan, err, st);
     if (e != cudaSuccess) return cuda_status(e, "decode_step/index_scores");
     e = launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
     if (e != cudaSuccess) return cuda_status(e, "decode_step/topk_select");

@@ -39,7 +39,10 @@ struct BatchDev {
     const int64_t* q_off;
     int32_t n_seq;
     int32_t n_q;
+    int32_t max_q_len;
     int64_t max_kv_len;
+    int64_t total_rows;
+    int64_t total_keys;
     int32_t kpool;
 };
 
@@ -66,7 +69,8 @@ __device__ __forceinline__ bool query_info(const BatchDev& b, int64_t q, QueryIn
     const int64_t r0 = b.row_off[s], r1 = b.row_off[s + 1];
     const int64_t kv_len = r1 - r0, q_len = q1 - q0;
     const int64_t L = kv_len - q_len + 1 + (q - q0);
-    if (q < q0 || q >= q1 || q_len > kv_len || kv_len > b.max_kv_len || L < 1) {
+    if (q < q0 || q >= q1 || q_len > kv_len || kv_len > b.max_kv_len || L < 1 || r0 < 0 ||
+        r1 > b.total_rows) {
         record_error(err, kDevBadBatch, (int32_t)q, where);
         return false;
     }
@@ -75,7 +79,8 @@ __device__ __forceinline__ bool query_info(const BatchDev& b, int64_t q, QueryIn
     qi.key0 = b.key_off[s];
     qi.L = L;
     qi.n_keys = L / b.kpool;
-    if (b.key_off[s + 1] - qi.key0 < kv_len / b.kpool) {
+    if (b.key_off[s + 1] - qi.key0 < kv_len / b.kpool || qi.key0 < 0 ||
+        b.key_off[s + 1] > b.total_keys) {
         record_error(err, kDevBadBatch, (int32_t)q, where);
         return false;
     }

@@ -19,10 +19,19 @@ struct Shape {
     size_t elem_bytes() const { return dtype == DSA_F32 ? 4 : 2; }
 };
 
-// Step 1.  scores[q, t] for t < n_keys(q); grid covers max_keys keys.
+// Step 1.  scores[q, t] for t < n_keys(q).  bf16 inputs with 32 indexer heads
+// run on the tensor cores (index_scores_tc.cu), everything else on CUDA cores
+// (index_scores.cu).  `scratch` holds index_scores_scratch_bytes() bytes.
+size_t index_scores_scratch_bytes(const Shape& sh, const BatchDev& b);
 cudaError_t launch_index_scores(const Shape& sh, const BatchDev& b, int64_t max_keys,
                                 const void* q_idx, const float* w, const void* k_idx,
-                                float* scores, int64_t ld, int32_t* err, cudaStream_t st);
+                                float* scores, int64_t ld, void* scratch, int32_t* err,
+                                cudaStream_t st);
+bool index_scores_tc_eligible(const Shape& sh, const BatchDev& b);
+size_t index_scores_tc_scratch_bytes(int32_t n_seq, int32_t n_q);
+cudaError_t launch_index_scores_tc(const Shape& sh, const BatchDev& b, const void* q_idx,
+                                   const float* w, const void* k_idx, float* scores, int64_t ld,
+                                   void* scratch, int32_t* err, cudaStream_t st);
 
 // Step 2.  One selection row per query.
 cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* scores,

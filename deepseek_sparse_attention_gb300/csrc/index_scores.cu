@@ -6,8 +6,9 @@
 //
 // One CTA scores 128 consecutive keys of one query: the query's heads are
 // widened to float in shared memory, each thread owns one key row in registers
-// and accumulates the 32 head dots in float.  This path serves float32 inputs
-// and is the reference point the tensor-core path is measured against.
+// and accumulates the head dots in float.  This path serves float32 inputs
+// (exact float products, which the bf16 tensor-core path cannot give) and
+// indexer head counts other than 32.
 #include "dsa_kernels.cuh"
 
 namespace dsa {
@@ -85,10 +86,17 @@ index_scores_simt(BatchDev b, int32_t hi, const T* __restrict__ q_idx,
 
 }  // namespace
 
+size_t index_scores_scratch_bytes(const Shape& sh, const BatchDev& b) {
+    return index_scores_tc_eligible(sh, b) ? index_scores_tc_scratch_bytes(b.n_seq, b.n_q) : 0;
+}
+
 cudaError_t launch_index_scores(const Shape& sh, const BatchDev& b, int64_t max_keys,
                                 const void* q_idx, const float* w, const void* k_idx,
-                                float* scores, int64_t ld, int32_t* err, cudaStream_t st) {
+                                float* scores, int64_t ld, void* scratch, int32_t* err,
+                                cudaStream_t st) {
     if (b.n_q == 0 || max_keys == 0) return cudaSuccess;
+    if (index_scores_tc_eligible(sh, b))
+        return launch_index_scores_tc(sh, b, q_idx, w, k_idx, scores, ld, scratch, err, st);
     const dim3 grid((unsigned)((max_keys + kKeysPerCta - 1) / kKeysPerCta), (unsigned)b.n_q);
     if (sh.dtype == DSA_F32) {
         index_scores_simt<float><<<grid, kKeysPerCta, 0, st>>>(

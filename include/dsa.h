@@ -95,13 +95,16 @@ typedef struct {
 
 /* Batch description.  The three offset arrays are DEVICE arrays of n_seq+1
  * non-decreasing int64 values starting at 0; the host scalars must bound them
- * (they size grids and are checked on the device). */
+ * (they size grids and tensor maps, and the kernels check the offsets against
+ * them, setting the error word and skipping a sequence that breaks a bound). */
 typedef struct {
     int32_t n_seq;             /* sequences                                        */
     int32_t n_q;               /* queries in total, = q_off[n_seq]                 */
     int32_t max_q_len;         /* host bound: max_s q_len_s                        */
     int32_t reserved;          /* must be 0                                        */
     int64_t max_kv_len;        /* host bound: max_s kv_len_s (< 2^31)              */
+    int64_t total_rows;        /* rows of `cache` (bounds row_off[n_seq])          */
+    int64_t total_keys;        /* rows of `k_idx` (bounds key_off[n_seq])          */
     const int64_t *row_off;    /* device [n_seq+1] cache-row offsets               */
     const int64_t *key_off;    /* device [n_seq+1] indexer-key / pool-key offsets  */
     const int64_t *q_off;      /* device [n_seq+1] query offsets                   */

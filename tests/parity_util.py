@@ -48,7 +48,7 @@ def gpu_shape(wl):
 
 def gpu_batch(wl, d):
     return dsa.make_batch(d["row_off"], d["key_off"], d["q_off"], wl.n_q, max(wl.q_lens),
-                          max(wl.kv_lens))
+                          max(wl.kv_lens), sum(wl.kv_lens), sum(wl.key_counts()))
 
 
 def query_slices(wl, d, q):

@@ -50,8 +50,8 @@ def test_version_and_row_width(lib):
 
 
 def _batch(n_seq=1, n_q=1, max_q=1, max_kv=4096):
-    b = dsa.Batch(n_seq, n_q, max_q, 0, max_kv, ctypes.c_void_p(16), ctypes.c_void_p(16),
-                  ctypes.c_void_p(16))
+    b = dsa.Batch(n_seq, n_q, max_q, 0, max_kv, max_kv, max_kv, ctypes.c_void_p(16),
+                  ctypes.c_void_p(16), ctypes.c_void_p(16))
     return b
 
 
@@ -69,6 +69,8 @@ def test_workspace_sizes(lib):
     # header + scores (131072 floats) + one index row + n_sel, 256-byte aligned
     assert n >= 256 + 131072 * 4 + 2048 * 4 + 4 and n % 256 == 0
     rc, n = _size(sh, _batch(), dsa.OP_INDEX_SCORES)
+    assert rc == 0 and n >= 256 and n % 256 == 0
+    rc, n = _size(sh, _batch(), dsa.OP_TOPK_SELECT)
     assert rc == 0 and n == 256
     rc, _ = _size(sh, _batch(), 7)
     assert rc == 1

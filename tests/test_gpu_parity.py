@@ -31,6 +31,8 @@ SMALL = [
     workloads.small("kpool_boundary", [2052, 2051, 4099, 9000], top_k=2048, kpool=4, rope=0),
     workloads.small("kpool_prefill", [1000], q_lens=[40], top_k=64, kpool=4, rope=0),
     workloads.small("fp32_kpool", [777, 130], top_k=64, kpool=4, rope=0, dtype="f32"),
+    workloads.small("mixed_chunks", [3000, 2100, 900, 5000], q_lens=[1, 37, 1, 8], top_k=256),
+    workloads.small("small_chunk", [600], q_lens=[5], top_k=128),
 ]
 
 
@@ -102,7 +104,8 @@ def _select(scores_np, L_list, top_k, kpool):
                            dtype=torch.int64).cuda()
     q_off = torch.arange(n + 1, dtype=torch.int64).cuda()
     sh = dsa.make_shape(top_k=top_k, kpool=kpool, rope_dim=0 if kpool > 1 else 64)
-    b = dsa.make_batch(row_off, key_off, q_off, n, 1, max(L_list))
+    b = dsa.make_batch(row_off, key_off, q_off, n, 1, max(L_list), sum(L_list),
+                       sum(L // kpool for L in L_list))
     ws = dsa.alloc_workspace(sh, b, dsa.OP_TOPK_SELECT)
     width = dsa.dsa_index_row_width(sh)
     idx = torch.full((n, width), -7, dtype=torch.int32, device="cuda")

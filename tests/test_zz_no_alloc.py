@@ -57,7 +57,7 @@ def test_noalloc_rejects_steps_larger_than_its_scratch():
             torch.tensor([0, 65536], dtype=torch.int64, device=dev),
             torch.tensor([0, 4096], dtype=torch.int64, device=dev)]
     sh = gpu_shape(wl)
-    b = dsa.make_batch(*offs, 4096, 4096, 65536)
+    b = dsa.make_batch(*offs, 4096, 4096, 65536, 65536, 65536)
     assert dsa.dsa_workspace_size(sh, b, dsa.OP_DECODE_STEP) > (8 << 20)
     t = torch.empty(16, device=dev)
     with pytest.raises(dsa.DsaError) as e:
