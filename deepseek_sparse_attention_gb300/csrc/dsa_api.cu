@@ -84,7 +84,7 @@ StepLayout step_layout(const Shape& sh, const BatchDev& b) {
     L.n_sel = off;
     off = align_up(off + (size_t)b.n_q * sizeof(int32_t));
     L.attn = off;
-    off = align_up(off + sparse_mla_scratch_bytes(sh, b.n_q, b.max_kv_len));
+    off = align_up(off + sparse_mla_scratch_bytes(sh, b));
     L.total = off;
     return L;
 }
@@ -95,7 +95,7 @@ size_t op_bytes(const Shape& sh, const BatchDev& b, int32_t op) {
             return align_up(kWsHeaderBytes + index_scores_scratch_bytes(sh, b));
         case DSA_OP_TOPK_SELECT: return kWsHeaderBytes;
         case DSA_OP_SPARSE_MLA:
-            return align_up(kWsHeaderBytes + sparse_mla_scratch_bytes(sh, b.n_q, b.max_kv_len));
+            return align_up(kWsHeaderBytes + sparse_mla_scratch_bytes(sh, b));
         case DSA_OP_DECODE_STEP: return step_layout(sh, b).total;
         default: return 0;
     }
@@ -169,12 +169,12 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
     if (s != DSA_OK) return s;
     if (batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
     if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_DECODE_STEP) return DSA_ERR_INVALID_ARG;
-    int32_t rps = 0, splits = 0;
-    plan_attention_splits(sh, batch->n_q > 0 ? batch->n_q : 1, batch->max_kv_len, &rps, &splits);
-    const int32_t attn = splits > 1 ? 2 : 1;
     const BatchDev bh{nullptr,           nullptr,           nullptr,           batch->n_seq,
                       batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
                       batch->total_keys, sh.kpool};
+    int32_t rps = 0, splits = 0;
+    plan_attention_splits(sh, bh, &rps, &splits);
+    const int32_t attn = splits > 1 ? 2 : 1;
     const int32_t idx = batch->max_kv_len / sh.kpool > 0
                             ? (index_scores_tc_eligible(sh, bh) ? 2 : 1) : 0;
     int32_t n = 0;

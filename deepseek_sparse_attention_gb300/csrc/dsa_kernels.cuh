@@ -38,11 +38,21 @@ cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* 
                                int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
                                cudaStream_t st);
 
-// Step 3.  Row splits per query (a multiple of 16 rows each) and the scratch
-// for the split-row partials (bytes; 0 if none is needed).
-void plan_attention_splits(const Shape& sh, int32_t n_q, int64_t max_kv_len,
-                           int32_t* rows_per_split, int32_t* n_split);
-size_t sparse_mla_scratch_bytes(const Shape& sh, int32_t n_q, int64_t max_kv_len);
+// Step 3.  bf16 rows run on the tensor cores (sparse_mla_tc.cu), float32 rows
+// on CUDA cores (sparse_mla.cu).  Row splits per query and the scratch for the
+// split-row partials (bytes; 0 if none is needed).
+void plan_attention_splits(const Shape& sh, const BatchDev& b, int32_t* rows_per_split,
+                           int32_t* n_split);
+size_t sparse_mla_scratch_bytes(const Shape& sh, const BatchDev& b);
+cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
+                                const float* part_ml, float* out, float* lse, cudaStream_t st);
+bool sparse_mla_tc_eligible(const Shape& sh, const BatchDev& b);
+void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
+                              int32_t* rows_per_split, int32_t* n_split);
+cudaError_t launch_sparse_mla_tc(const Shape& sh, const BatchDev& b, const void* q_abs,
+                                 const void* cache, const int32_t* idx, const int32_t* n_sel,
+                                 float* out, float* lse, float* part_o, float* part_ml,
+                                 int32_t rps, int32_t n_split, int32_t* err, cudaStream_t st);
 cudaError_t launch_sparse_mla(const Shape& sh, const BatchDev& b, const void* q_abs,
                               const void* cache, const int32_t* idx, const int32_t* n_sel,
                               float* out, float* lse, void* scratch, size_t scratch_bytes,

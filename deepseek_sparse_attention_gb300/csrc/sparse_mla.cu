@@ -257,11 +257,9 @@ merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __r
         lse[q * kHeads + h] = Lsum > 0.f ? M + logf(Lsum) : -INFINITY;
 }
 
-}  // namespace
-
 // Rows per split: enough CTAs to fill the GPU about twice, at least 64 rows each.
-void plan_attention_splits(const Shape& sh, int32_t n_q, int64_t max_kv_len, int32_t* rows_per_split,
-                 int32_t* n_split) {
+void plan_splits_simt(const Shape& sh, int32_t n_q, int64_t max_kv_len, int32_t* rows_per_split,
+                      int32_t* n_split) {
     int64_t max_rows = sh.index_row_width();
     if (max_kv_len < max_rows) max_rows = max_kv_len;
     if (max_rows < 1) max_rows = 1;
@@ -276,8 +274,6 @@ void plan_attention_splits(const Shape& sh, int32_t n_q, int64_t max_kv_len, int
     *rows_per_split = (int32_t)rps;
     *n_split = (int32_t)splits;
 }
-
-namespace {
 
 template <typename T, int W>
 cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, const void* cache,
@@ -296,17 +292,31 @@ cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, 
                                             part_ml, err);
     e = cudaGetLastError();
     if (e != cudaSuccess || n_split == 1) return e;
-    merge_splits<<<dim3(kHeads, (unsigned)b.n_q), 128, 0, st>>>(n_split, part_o, part_ml, out, lse);
-    return cudaGetLastError();
+    return launch_merge_splits(b.n_q, n_split, part_o, part_ml, out, lse, st);
 }
 
 }  // namespace
 
-size_t sparse_mla_scratch_bytes(const Shape& sh, int32_t n_q, int64_t max_kv_len) {
+cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
+                                const float* part_ml, float* out, float* lse, cudaStream_t st) {
+    merge_splits<<<dim3(kHeads, (unsigned)n_q), 128, 0, st>>>(n_split, part_o, part_ml, out, lse);
+    return cudaGetLastError();
+}
+
+void plan_attention_splits(const Shape& sh, const BatchDev& b, int32_t* rows_per_split,
+                           int32_t* n_split) {
+    const int32_t n_q = b.n_q > 0 ? b.n_q : 1;
+    if (sparse_mla_tc_eligible(sh, b))
+        plan_attention_splits_tc(sh, n_q, b.max_kv_len, rows_per_split, n_split);
+    else
+        plan_splits_simt(sh, n_q, b.max_kv_len, rows_per_split, n_split);
+}
+
+size_t sparse_mla_scratch_bytes(const Shape& sh, const BatchDev& b) {
     int32_t rps, n_split;
-    plan_attention_splits(sh, n_q > 0 ? n_q : 1, max_kv_len, &rps, &n_split);
+    plan_attention_splits(sh, b, &rps, &n_split);
     if (n_split == 1) return 0;
-    const size_t parts = (size_t)n_q * n_split * kHeads;
+    const size_t parts = (size_t)b.n_q * n_split * kHeads;
     return parts * kLatent * sizeof(float) + parts * 2 * sizeof(float);
 }
 
@@ -316,7 +326,7 @@ cudaError_t launch_sparse_mla(const Shape& sh, const BatchDev& b, const void* q_
                               int32_t* err, cudaStream_t st) {
     if (b.n_q == 0) return cudaSuccess;
     int32_t rps, n_split;
-    plan_attention_splits(sh, b.n_q, b.max_kv_len, &rps, &n_split);
+    plan_attention_splits(sh, b, &rps, &n_split);
     float* part_o = nullptr;
     float* part_ml = nullptr;
     if (n_split > 1) {
@@ -326,6 +336,9 @@ cudaError_t launch_sparse_mla(const Shape& sh, const BatchDev& b, const void* q_
         part_o = static_cast<float*>(scratch);
         part_ml = part_o + parts * kLatent;
     }
+    if (sparse_mla_tc_eligible(sh, b))
+        return launch_sparse_mla_tc(sh, b, q_abs, cache, idx, n_sel, out, lse, part_o, part_ml,
+                                    rps, n_split, err, st);
     const bool f32 = sh.dtype == DSA_F32;
     if (sh.width() == 576) {
         return f32 ? launch_typed<float, 576>(sh, b, q_abs, cache, idx, n_sel, out, lse, part_o,

@@ -1,0 +1,495 @@
+// sparse_mla_tc.cu -- absorbed-MLA attention over the selected cache rows on
+// the tcgen05 tensor cores.
+//
+// z[h,j] = scale * q_abs[h,:] . row_j (latent + rope), p = softmax_j(z),
+// out[h,c] = sum_j p[h,j] row_j[c] for the 512 latent columns ("GLM 5.2 in one
+// C file", "Attention: Multi head Latent Attention With a Tiny KV Cache";
+// "GLM-5.x (glm-dsa, glm5next)", "The block": 64 heads, one 576-wide row,
+// scale 1/16; "Add GLM-5.3-Flash support": a NoPE row is the 512-wide latent,
+// key and value alike).
+//
+// One CTA handles a range of one query's selected rows in tiles of 128 rows:
+//   warp 0     loads the query once (TMA tiles) and gathers each tile's rows
+//              with TMA gather4 (four arbitrary rows per instruction, 128-byte
+//              swizzle) into shared memory;
+//   warp 1     issues S^T = R . Q^T (M = 128 rows, N = 64 heads, K = the row
+//              width) into TMEM, then O^T += R^T . P^T (M = 128 latent columns
+//              x 4, N = 64 heads, K = 128 rows) with both operands MN-major --
+//              the same gathered tile serves as K-major A for the scores and as
+//              MN-major A for the values;
+//   warps 4-7  softmax across the tile's rows: one TMEM lane (row) per thread,
+//              per-head tile maxima by warp reductions, a running maximum that
+//              is raised (and O^T rescaled in TMEM) only when a tile exceeds it
+//              by more than 2^8, exp2, P^T written to shared memory (into the
+//              rope block, which the scores no longer need), per-thread partial
+//              row sums reduced once at the end.
+// Splits of one query are combined by the log-sum-exp merge.
+#include <math.h>
+
+#include "dsa_kernels.cuh"
+#include "sm100.cuh"
+
+namespace dsa {
+namespace {
+
+using namespace sm100;
+
+constexpr int kHeads = 64;
+constexpr int kTileRows = 128;
+constexpr int kLatent = 512;
+constexpr uint32_t kQBlock = kHeads * 128;          // one 64-column block of Q: 8 KB
+constexpr uint32_t kRBlock = kTileRows * 128;       // one 64-column block of a row tile: 16 KB
+constexpr uint32_t kTmemCols = 512;                 // S^T 0..63, O^T 64..319, P lo 320..351
+constexpr uint32_t kOCol = 64;
+constexpr uint32_t kLoCol = 320;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kSlack = 8.f;                       // lazy rescale threshold (log2 units)
+
+template <int W>
+struct Cfg {
+    static constexpr int kCB = W / 64;               // 64-column blocks of a row
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffR = kCB * kQBlock;
+    // P^T [128 rows x 64 heads] bf16: the rope block of the tile when there is
+    // one (no longer needed once the scores are formed), else its own block.
+    static constexpr uint32_t kOffP = W == 576 ? kOffR + 8 * kRBlock : kOffR + kCB * kRBlock;
+    static constexpr uint32_t kOffBar = (W == 576 ? kOffR + kCB * kRBlock : kOffP + kRBlock);
+    // q_full, r_full, s_full, p_full, pv_done, drain, pv_hi
+    static constexpr uint32_t kOffRed = kOffBar + 64;          // [2][4][64] int
+    static constexpr uint32_t kOffL = kOffRed + 2 * 4 * 64 * 4; // [64] float
+    static constexpr uint32_t kOffM = kOffL + 64 * 4;           // [64] float
+    static constexpr uint32_t kOffMisc = kOffM + 64 * 4;
+    static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ int fkey(float f) {           // order-preserving float -> int
+    const int i = __float_as_int(f);
+    return i >= 0 ? i : i ^ 0x7fffffff;
+}
+__device__ __forceinline__ float fval(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
+
+template <int W>
+__global__ void __launch_bounds__(256, 1)
+sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
+              BatchDev b, float scale, const int32_t* __restrict__ idx,
+              const int32_t* __restrict__ n_sel, int64_t idx_width, int32_t rows_per_split,
+              int32_t n_split, float* __restrict__ out, float* __restrict__ lse,
+              float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* err) {
+    using C = Cfg<W>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t *q_full = bars, *r_full = bars + 1, *s_full = bars + 2, *p_full = bars + 3,
+             *pv_done = bars + 4, *drain = bars + 5, *pv_hi = bars + 6;
+    int* red = reinterpret_cast<int*>(smem + C::kOffRed);
+    float* l_fin = reinterpret_cast<float*>(smem + C::kOffL);
+    float* m_fin = reinterpret_cast<float*>(smem + C::kOffM);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t q = blockIdx.y;
+    const int split = blockIdx.x;
+    QueryInfo qi;
+    if (!query_info(b, q, qi, err, /*where=*/8)) return;
+    int64_t ns = n_sel[q];
+    ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
+    const int64_t j0 = (int64_t)split * rows_per_split;
+    const int64_t j1 = j0 + rows_per_split < ns ? j0 + rows_per_split : ns;
+    if (j0 >= j1) {                                   // empty split: neutral partial
+        if (n_split == 1) {
+            for (int i = threadIdx.x; i < kHeads * kLatent; i += blockDim.x)
+                out[q * kHeads * kLatent + i] = 0.f;
+            if (lse != nullptr && threadIdx.x < kHeads) lse[q * kHeads + threadIdx.x] = -INFINITY;
+        } else {
+            const int64_t part = q * n_split + split;
+            for (int i = threadIdx.x; i < kHeads * kLatent; i += blockDim.x)
+                part_o[part * kHeads * kLatent + i] = 0.f;
+            if (threadIdx.x < kHeads) {
+                part_ml[(part * kHeads + threadIdx.x) * 2] = -INFINITY;
+                part_ml[(part * kHeads + threadIdx.x) * 2 + 1] = 0.f;
+            }
+        }
+        return;
+    }
+    const int n_tiles = (int)((j1 - j0 + kTileRows - 1) / kTileRows);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 7; ++i) mbar_init(&bars[i], i == 3 ? 128 : 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_c);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {                                                  // ---- loads
+        bool ok = true;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, C::kCB * kQBlock);
+            for (int cb = 0; cb < C::kCB; ++cb)
+                tma_load_2d(smem + C::kOffQ + cb * kQBlock, &tm_q, q_full, 64 * cb,
+                            (int32_t)(q * kHeads));
+        }
+        const int32_t* irow = idx + q * idx_width;
+        for (int t = 0; t < n_tiles && ok; ++t) {
+            if (t > 0) {                       // the previous tile's values are consumed
+                int o = 1;
+                if (lane == 0) o = mbar_wait(pv_done, (uint32_t)((t - 1) & 1), kWaitNs);
+                ok = __shfl_sync(0xffffffffu, o, 0) != 0;
+            }
+            if (!ok) break;
+            int32_t g[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t j = j0 + (int64_t)t * kTileRows + 4 * lane + i;
+                int32_t r = 0;
+                if (j < j1) {
+                    r = irow[j];
+                    if (r < 0 || r >= qi.L) {
+                        record_error(err, kDevBadIndex, (int32_t)q, /*where=*/8);
+                        r = 0;
+                    }
+                }
+                g[i] = (int32_t)(qi.row0 + r);
+            }
+            if (lane == 0) mbar_arrive_expect_tx(r_full, C::kCB * kRBlock);
+            __syncwarp();
+            uint8_t* rdst = smem + C::kOffR + lane * 512;
+            for (int cb = 0; cb < C::kCB; ++cb)
+                tma_gather4(rdst + cb * kRBlock, &tm_c, r_full, 64 * cb, g[0], g[1], g[2], g[3]);
+        }
+        if (!ok && lane == 0) record_error(err, kDevTimeout, (int32_t)q, /*where=*/9);
+    } else if (warp == 1) {                                           // ---- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kTileRows, kHeads);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32_major(kTileRows, kHeads, 1, 1);
+            const uint32_t q0 = smem_u32(smem + C::kOffQ);
+            const uint32_t r0 = smem_u32(smem + C::kOffR);
+            const uint32_t p0 = smem_u32(smem + C::kOffP);
+            bool ok = mbar_wait(q_full, 0, kWaitNs);
+            for (int t = 0; t < n_tiles && ok; ++t) {
+                ok = mbar_wait(r_full, (uint32_t)(t & 1), kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                for (int cb = 0; cb < C::kCB; ++cb) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        mma_bf16_ss(tmem_base, sdesc_kmajor_sw128(r0 + cb * kRBlock + kk * 32),
+                                    sdesc_kmajor_sw128(q0 + cb * kQBlock + kk * 32), idesc_s,
+                                    (cb | kk) != 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(s_full);
+                // P = P_hi + P_lo, both bf16, through the same buffer: the value
+                // product carries P to ~2^-16 relative, not bf16's 2^-9.
+                for (int part = 0; part < 2 && ok; ++part) {
+                    ok = mbar_wait(p_full, (uint32_t)part, kWaitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // A = R^T: MN-major, 64-column blocks 16 KB apart, 8-row groups
+                    // 1 KB apart.  B = P^T: MN-major, the 64 heads are one block.
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                        for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                            mma_bf16_ss(tmem_base + kOCol + 64 * i,
+                                        sdesc_sw128(r0 + 2 * i * kRBlock + kk * 2048, kRBlock, 1024),
+                                        sdesc_sw128(p0 + kk * 2048, 1024, 1024), idesc_pv,
+                                        (t > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(part == 0 ? pv_hi : pv_done);
+                }
+                if (!ok) break;
+            }
+            if (!ok) record_error(err, kDevTimeout, (int32_t)q, /*where=*/10);
+            mma_commit(drain);
+            mbar_wait(drain, 0, 50000000ull);
+        }
+    } else if (warp >= 4) {                                           // ---- softmax
+        const int wq = warp & 3;
+        const int row = 32 * wq + lane;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * wq) << 16);
+        const float c2 = scale * kLog2e;
+        float l_part[kHeads];
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) l_part[h] = 0.f;
+        // running maxima (one writer per head) and rescale factors live in shared memory
+        float* m_sh = m_fin;
+        float* alpha_s = l_fin;
+        if (row < kHeads) m_sh[row] = -INFINITY;
+        uint8_t* prow = smem + C::kOffP + row * 128;
+        bool ok = true;
+        for (int t = 0; t < n_tiles; ++t) {
+            if (ok) ok = mbar_wait(s_full, (uint32_t)(t & 1), kWaitNs);
+            tc_fence_after();
+            // rows past the split, and rows whose index is out of range (reported
+            // by the loader), take no weight
+            const int64_t jrow = j0 + (int64_t)t * kTileRows + row;
+            bool valid = jrow < j1;
+            if (valid) {
+                const int32_t r = idx[q * idx_width + jrow];
+                valid = r >= 0 && r < qi.L;
+            }
+            // per-head maximum over the tile's 128 rows
+            int* rb = red + (t & 1) * 4 * kHeads + wq * kHeads;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[32];
+                tmem_ld_32cols(lane_addr + 32 * hh, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int mk = __reduce_max_sync(0xffffffffu, fkey(valid ? v[e] * c2 : -INFINITY));
+                    if (lane == e) rb[32 * hh + e] = mk;
+                }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            uint32_t raised = 0;
+            if (row < kHeads) {                        // head `row`: raise its running maximum?
+                const int* rt = red + (t & 1) * 4 * kHeads;
+                const int mk = max(max(rt[row], rt[kHeads + row]),
+                                   max(rt[2 * kHeads + row], rt[3 * kHeads + row]));
+                const float tmax = fval(mk), m_old = m_sh[row];
+                float a = 1.f;
+                if (tmax > m_old + kSlack) {
+                    a = m_old == -INFINITY ? 0.f : exp2f(m_old - tmax);
+                    m_sh[row] = tmax;
+                    raised = 1;
+                }
+                alpha_s[row] = a;
+            }
+            uint32_t any_raised;
+            asm volatile(
+                "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                : "=r"(any_raised)
+                : "r"(raised)
+                : "memory");
+            if (any_raised) {
+#pragma unroll
+                for (int h = 0; h < kHeads; ++h) l_part[h] *= alpha_s[h];
+            }
+            if (any_raised && t > 0) {                 // O^T follows the new maxima
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float v[32];
+                        const uint32_t a = lane_addr + kOCol + 64 * i + 32 * hh;
+                        tmem_ld_32cols(a, v);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) v[c] *= alpha_s[32 * hh + c];
+                        tmem_st_32cols(a, v);
+                    }
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+            // P^T row of this thread: 64 bf16 in the 128-byte swizzle layout.
+            // p = hi + lo with hi = bf16(p), lo = bf16(p - hi); hi goes to shared
+            // memory now, lo waits in spare TMEM columns for the second pass.
+            float lo_bits[32];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[32];
+                tmem_ld_32cols(lane_addr + 32 * hh, v);
+#pragma unroll
+                for (int c16 = 0; c16 < 4; ++c16) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int hl = 8 * c16 + 2 * e, h = 32 * hh + hl;
+                        const float x0 = valid ? v[hl] * c2 : -INFINITY;
+                        const float x1 = valid ? v[hl + 1] * c2 : -INFINITY;
+                        const float p0 = exp2f(x0 - m_sh[h]);
+                        const float p1 = exp2f(x1 - m_sh[h + 1]);
+                        const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+                        const float2 hf = __bfloat1622float2(hi);
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+                        const float2 lf = __bfloat1622float2(lo);
+                        l_part[h] += hf.x + lf.x;
+                        l_part[h + 1] += hf.y + lf.y;
+                        w4[e] = *reinterpret_cast<const uint32_t*>(&hi);
+                        lo_bits[16 * hh + 4 * c16 + e] =
+                            __uint_as_float(*reinterpret_cast<const uint32_t*>(&lo));
+                    }
+                    const int chunk = 4 * hh + c16;
+                    *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+            tmem_st_32cols(lane_addr + kLoCol, lo_bits);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full);
+            // second pass: the lo parts, once the hi product has read the buffer
+            if (ok) ok = mbar_wait(pv_hi, (uint32_t)(t & 1), kWaitNs);
+            tc_fence_after();
+            tmem_ld_32cols(lane_addr + kLoCol, lo_bits);
+#pragma unroll
+            for (int chunk = 0; chunk < 8; ++chunk) {
+                *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
+                    make_uint4(__float_as_uint(lo_bits[4 * chunk]), __float_as_uint(lo_bits[4 * chunk + 1]),
+                               __float_as_uint(lo_bits[4 * chunk + 2]), __float_as_uint(lo_bits[4 * chunk + 3]));
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+        if (ok) ok = mbar_wait(pv_done, (uint32_t)((n_tiles - 1) & 1), kWaitNs);
+        if (!ok) record_error(err, kDevTimeout, (int32_t)q, /*where=*/11);
+        tc_fence_after();
+        // row sums: per-thread partials -> per-head totals (through shared memory;
+        // the row tile is free once the last PV has completed)
+        float* lsc = reinterpret_cast<float*>(smem + C::kOffR);
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) lsc[row * (kHeads + 1) + h] = l_part[h];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (row < kHeads) {
+            float s = 0.f;
+            for (int r = 0; r < kTileRows; ++r) s += lsc[r * (kHeads + 1) + row];
+            l_fin[row] = s;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        // O^T lane `row` holds latent columns row + 128 i
+        const bool final_out = n_split == 1;
+        const int64_t part = q * n_split + split;
+        float* dst = final_out ? out + q * kHeads * kLatent : part_o + part * kHeads * kLatent;
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+            const int c = row + kTileRows * i;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[32];
+                tmem_ld_32cols(lane_addr + kOCol + 64 * i + 32 * hh, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int h = 32 * hh + e;
+                    const float l = l_fin[h];
+                    dst[h * kLatent + c] = final_out ? (l > 0.f ? v[e] / l : 0.f) : v[e];
+                }
+            }
+        }
+        if (row < kHeads) {
+            const float l = l_fin[row];
+            const float m = m_fin[row];
+            if (final_out) {
+                if (lse != nullptr)
+                    lse[q * kHeads + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            } else {
+                part_ml[(part * kHeads + row) * 2] = l > 0.f ? m * kLn2 : -INFINITY;
+                part_ml[(part * kHeads + row) * 2 + 1] = l;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &qr) != cudaSuccess ||
+            qr != cudaDriverEntryPointSuccess)
+            return (EncodeTiledFn) nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Row-major [rows, width] bf16 matrix read in boxes of box_rows x 64 columns
+// with the 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t width, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr || rows == 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)width * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int W>
+cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, const void* cache,
+                     const int32_t* idx, const int32_t* n_sel, float* out, float* lse,
+                     float* part_o, float* part_ml, int32_t rps, int32_t n_split, int32_t* err,
+                     cudaStream_t st) {
+    using C = Cfg<W>;
+    CUtensorMap tm_q, tm_c;
+    if (!make_map(&tm_q, q_abs, (uint64_t)b.n_q * kHeads, W, kHeads) ||
+        !make_map(&tm_c, cache, (uint64_t)b.total_rows, W, 1))
+        return cudaErrorInvalidValue;
+    auto kern = sparse_mla_tc<W>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3((unsigned)n_split, (unsigned)b.n_q), 256, C::kSmemBytes, st>>>(
+        tm_q, tm_c, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split, out, lse, part_o,
+        part_ml, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || n_split == 1) return e;
+    return launch_merge_splits(b.n_q, n_split, part_o, part_ml, out, lse, st);
+}
+
+}  // namespace
+
+bool sparse_mla_tc_eligible(const Shape& sh, const BatchDev& b) {
+    return sh.dtype == DSA_BF16 && sh.heads == kHeads && sh.kv_lora == kLatent &&
+           (sh.width() == 576 || sh.width() == 512) && b.total_rows >= 1 &&
+           b.total_rows < ((int64_t)1 << 31) && (int64_t)b.n_q * kHeads < ((int64_t)1 << 31);
+}
+
+// Tiles of 128 rows; enough CTAs (one per SM) to fill the GPU about twice.
+void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
+                              int32_t* rows_per_split, int32_t* n_split) {
+    int64_t max_rows = sh.index_row_width();
+    if (max_kv_len < max_rows) max_rows = max_kv_len;
+    if (max_rows < 1) max_rows = 1;
+    const int64_t tiles = (max_rows + kTileRows - 1) / kTileRows;
+    const int64_t target_ctas = 2 * 152;
+    int64_t splits = (target_ctas + n_q - 1) / n_q;
+    if (splits > tiles) splits = tiles;
+    if (splits < 1) splits = 1;
+    const int64_t tiles_per = (tiles + splits - 1) / splits;
+    splits = (tiles + tiles_per - 1) / tiles_per;
+    *rows_per_split = (int32_t)(tiles_per * kTileRows);
+    *n_split = (int32_t)splits;
+}
+
+cudaError_t launch_sparse_mla_tc(const Shape& sh, const BatchDev& b, const void* q_abs,
+                                 const void* cache, const int32_t* idx, const int32_t* n_sel,
+                                 float* out, float* lse, float* part_o, float* part_ml,
+                                 int32_t rps, int32_t n_split, int32_t* err, cudaStream_t st) {
+    if (sh.width() == 576)
+        return launch_w<576>(sh, b, q_abs, cache, idx, n_sel, out, lse, part_o, part_ml, rps,
+                             n_split, err, st);
+    return launch_w<512>(sh, b, q_abs, cache, idx, n_sel, out, lse, part_o, part_ml, rps, n_split,
+                         err, st);
+}
+
+}  // namespace dsa

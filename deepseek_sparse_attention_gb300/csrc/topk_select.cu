@@ -8,19 +8,54 @@
 // tail, dense when floor(L/kpool) <= k/kpool ("GLM-5.3-Flash on WASTE",
 // "DeepSeek Sparse Attention, k-pool flavour").
 //
-// Scores are mapped to order-preserving uint32 keys.  Three radix levels (12,
-// 10 and 10 bits) over the query's scores find the exact k-th largest key T
-// and how many keys equal to T are taken; the emission pass then walks the
-// scores in ascending index order and keeps every key > T plus the first
-// (lowest-index) keys == T, compacting with block-wide prefix sums, so the
-// output is ascending without a sort.  One CTA per query.
+// Scores are mapped to order-preserving uint32 keys; the selection is every
+// key above the exact k-th largest key T plus the lowest-index keys equal to T.
+// One CTA per query:
+//   sample  a strided sample of 2048 scores bounds the k-th largest from below
+//           (t_lo: the lower edge of the coarse bin that holds 1.5x the kept
+//           fraction of the sample);
+//   pass    one streaming read of the scores appends every score >= t_lo
+//           (typically a few percent) to a shared-memory candidate list;
+//   exact   three radix levels over the candidates alone give T; candidates
+//           above T set bits of a shared bitmap, those equal to T of a second;
+//   emit    the bitmaps are scanned in ascending order (block prefix sums of
+//           popcounts), taking equal keys lowest index first, so the output
+//           is ascending without a sort.
+// When the sample bound admits fewer than k or more candidates than the list
+// holds (many equal or adversarially ordered scores), the CTA falls back to
+// three radix levels over the scores in global memory and an emission pass that
+// re-reads them; queries too long for the shared bitmaps use that path.
 #include "dsa_kernels.cuh"
 
 namespace dsa {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kItems = 8;        // consecutive scores per thread in the emission pass
+constexpr int kWarps = kThreads / 32;
+constexpr int kL1Bits = 11;                   // first radix level: top 11 key bits
+constexpr int kL1Bins = 1 << kL1Bits;
+constexpr int kHistCopies = 4;
+constexpr int kCandCap = 8192;
+constexpr int kSample = 2048;                 // scores sampled to bound the threshold
+constexpr int kItems = 8;                     // scores per thread per emission round (fallback)
+constexpr size_t kFixedSmem = (size_t)kHistCopies * kL1Bins * 4 + (size_t)kCandCap * 8 + 256;
+static_assert(kSample <= kCandCap, "the sample is staged in the candidate list");
+constexpr size_t kMaxSmem = 200 * 1024;
+constexpr int kBatch = 16;                    // loads in flight per lane in the streaming passes
+
+// Keys of 32*kBatch consecutive scores starting at `base`: lane l gets
+// elements base + l + 32*r, all loads issued before any is used.
+__device__ __forceinline__ void load_keys(const float* __restrict__ sc, int64_t base, int64_t n,
+                                          int lane, uint32_t (&key)[kBatch]) {
+    float v[kBatch];
+#pragma unroll
+    for (int r = 0; r < kBatch; ++r) {
+        const int64_t t = base + lane + 32 * r;
+        v[r] = t < n ? __ldg(sc + t) : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < kBatch; ++r) key[r] = order_key(v[r]);
+}
 
 // Exclusive prefix sum over the CTA in thread order; *total gets the sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* warp_sums) {
@@ -50,16 +85,140 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* warp
     return before + x - v;
 }
 
-__global__ void __launch_bounds__(kThreads)
+// The digit d of a histogram of nb bins at which the count of keys in bins
+// above d is < k_rem <= that count plus hist[d]; *above gets the former.
+__device__ void find_digit(const uint32_t* hist, int nb, int64_t k_rem, int* warp_sums,
+                           uint32_t* s_digit, int64_t* s_above) {
+    const int per = nb >= kThreads ? nb / kThreads : 1;
+    const int first = threadIdx.x * per;
+    int local = 0;
+    for (int r = 0; r < per; ++r)
+        if (first + r < nb) local += (int)hist[first + r];
+    int total;
+    const int excl = block_exclusive_scan(local, &total, warp_sums);
+    int64_t run = (int64_t)total - excl - local;
+    for (int r = per - 1; r >= 0; --r) {
+        const int bin = first + r;
+        if (bin >= nb) continue;
+        const int64_t h = hist[bin];
+        if (run < k_rem && run + h >= k_rem) {
+            *s_digit = (uint32_t)bin;
+            *s_above = run;
+        }
+        run += h;
+    }
+    __syncthreads();
+}
+
+// Inverse of order_key.
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+    const uint32_t u = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+    return __uint_as_float(u);
+}
+
+// Writes selected unit t (a row, or a pool of kpool rows) at position pos.
+__device__ __forceinline__ void put(int32_t* out, int64_t pos, int64_t t, int kpool) {
+    if (kpool == 1) {
+        out[pos] = (int32_t)t;
+    } else {
+        for (int r = 0; r < kpool; ++r) out[pos * kpool + r] = (int32_t)(t * kpool + r);
+    }
+}
+
+// Selection by three radix levels over the scores in global memory, then an
+// emission pass over them in ascending order.  `hist` has 4096 entries.
+__device__ void select_multilevel(const float* __restrict__ sc, int64_t n, int64_t keep, int kpool,
+                                  int32_t* out, uint32_t* hist, int* warp_sums, uint32_t* s_digit,
+                                  int64_t* s_above, int64_t* n_out) {
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0;
+    int pbits = 0;
+    int64_t k_rem = keep;
+#pragma unroll 1
+    for (int lvl = 0; lvl < 3; ++lvl) {
+        const int bits = lvl == 0 ? 12 : 10;
+        const int nb = 1 << bits;
+        for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        const int shift = 32 - pbits - bits;
+        const int lane = tid & 31, warp = tid >> 5;
+        for (int64_t base = (int64_t)warp * 32 * kBatch; base < n;
+             base += (int64_t)kWarps * 32 * kBatch) {
+            uint32_t key[kBatch];
+            load_keys(sc, base, n, lane, key);
+#pragma unroll
+            for (int r = 0; r < kBatch; ++r) {
+                const bool match = base + lane + 32 * r < n &&
+                                   (pbits == 0 || (key[r] >> (32 - pbits)) == prefix);
+                if (match) atomicAdd(&hist[(key[r] >> shift) & (uint32_t)(nb - 1)], 1u);
+            }
+        }
+        __syncthreads();
+        find_digit(hist, nb, k_rem, warp_sums, s_digit, s_above);
+        k_rem -= *s_above;
+        prefix = (prefix << bits) | *s_digit;
+        pbits += bits;
+        __syncthreads();
+    }
+    const uint32_t T = prefix;
+    int64_t eq_base = 0, out_base = 0;
+    for (int64_t c0 = 0; c0 < n; c0 += (int64_t)kThreads * kItems) {
+        const int64_t t_begin = c0 + (int64_t)tid * kItems;
+        uint32_t keys[kItems];
+        int n_eq = 0, valid = 0;
+#pragma unroll
+        for (int i = 0; i < kItems; ++i) {
+            const int64_t t = t_begin + i;
+            keys[i] = 0;
+            if (t < n) {
+                keys[i] = order_key(__ldg(sc + t));
+                valid |= 1 << i;
+                n_eq += keys[i] == T;
+            }
+        }
+        int eq_total;
+        const int eq_excl = block_exclusive_scan(n_eq, &eq_total, warp_sums);
+        int64_t eq_rank = eq_base + eq_excl;
+        int selmask = 0, n_s = 0;
+#pragma unroll
+        for (int i = 0; i < kItems; ++i) {
+            if (!((valid >> i) & 1)) continue;
+            const bool eq = keys[i] == T;
+            const bool s = keys[i] > T || (eq && eq_rank < k_rem);
+            eq_rank += eq;
+            if (s) { selmask |= 1 << i; ++n_s; }
+        }
+        int sel_total;
+        const int sel_excl = block_exclusive_scan(n_s, &sel_total, warp_sums);
+        int64_t pos = out_base + sel_excl;
+#pragma unroll
+        for (int i = 0; i < kItems; ++i) {
+            if (!((selmask >> i) & 1)) continue;
+            if (pos >= keep) break;                 // never write past the kept count
+            put(out, pos++, t_begin + i, kpool);
+        }
+        eq_base += eq_total;
+        out_base += sel_total;
+    }
+    *n_out = out_base;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
 topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __restrict__ scores,
                    int64_t ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
-                   int64_t width, int32_t* err) {
-    __shared__ uint32_t hist[4096];
-    __shared__ int warp_sums[32];
-    __shared__ uint32_t s_digit;
-    __shared__ int64_t s_above;
+                   int64_t width, int32_t bitmap_words, int32_t* err) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem);                 // [copies][kL1Bins]
+    uint32_t* cand_key = hist + kHistCopies * kL1Bins;                  // [kCandCap]
+    int32_t* cand_idx = reinterpret_cast<int32_t*>(cand_key + kCandCap);
+    int* warp_sums = cand_idx + kCandCap;                               // [32]
+    uint32_t* s_digit = reinterpret_cast<uint32_t*>(warp_sums + 32);
+    int* s_count = reinterpret_cast<int*>(s_digit + 1);
+    int64_t* s_above = reinterpret_cast<int64_t*>(s_digit + 2);
+    uint32_t* sel_bits = reinterpret_cast<uint32_t*>(smem + kFixedSmem);   // [bitmap_words]
+    uint32_t* eq_bits = sel_bits + bitmap_words;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t q = blockIdx.x;
     int32_t* out = idx + q * width;
     QueryInfo qi;
@@ -77,101 +236,131 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
         if (tid == 0) n_sel[q] = (int32_t)L;
         return;
     }
-
     const float* sc = scores + q * ld;
+    int64_t n_out = 0;
+    const int64_t words = (n + 31) / 32;
 
-    // ---- radix levels: exact k-th largest key T, and how many keys == T to take
-    uint32_t prefix = 0;
-    int pbits = 0;
-    int64_t k_rem = keep;
+    bool done = false;
+    if (words <= bitmap_words) {
+        // ---- a lower bound t_lo on the k-th largest score from a strided sample:
+        // the key (to 22 bits) of the sample element ranked at 1.5x the kept
+        // fraction plus a margin, found by two radix levels over the sample.
+        uint32_t* samp = cand_key;                       // the sample lives where candidates will
+        for (int i = tid; i < kL1Bins; i += kThreads) hist[i] = 0;
+        if (tid == 0) *s_count = 0;
+        const int64_t n_samp = n < kSample ? n : kSample;
+        for (int64_t i = tid; i < n_samp; i += kThreads) samp[i] = order_key(__ldg(sc + i * n / n_samp));
+        __syncthreads();
+        for (int64_t i = tid; i < n_samp; i += kThreads) atomicAdd(&hist[samp[i] >> 21], 1u);
+        __syncthreads();
+        int64_t target = (keep * n_samp * 3 + 2 * n - 1) / (2 * n) + 8;
+        target = target < n_samp ? target : n_samp;
+        find_digit(hist, kL1Bins, target, warp_sums, s_digit, s_above);
+        const uint32_t sb1 = *s_digit;
+        target -= *s_above;
+        __syncthreads();
+        for (int i = tid; i < kL1Bins; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        for (int64_t i = tid; i < n_samp; i += kThreads)
+            if ((samp[i] >> 21) == sb1) atomicAdd(&hist[(samp[i] >> 10) & (kL1Bins - 1)], 1u);
+        __syncthreads();
+        find_digit(hist, kL1Bins, target, warp_sums, s_digit, s_above);
+        const float t_lo = key_to_float((sb1 << 21) | (*s_digit << 10));
+        __syncthreads();
+
+        // ---- one streaming pass: every score >= t_lo becomes a candidate
+        for (int64_t base = (int64_t)warp * 32 * kBatch; base < n;
+             base += (int64_t)kWarps * 32 * kBatch) {
+            float v[kBatch];
+#pragma unroll
+            for (int r = 0; r < kBatch; ++r) {
+                const int64_t t = base + lane + 32 * r;
+                v[r] = t < n ? __ldg(sc + t) : -INFINITY;
+            }
+#pragma unroll
+            for (int r = 0; r < kBatch; ++r) {
+                const uint32_t hit = __ballot_sync(0xffffffffu, v[r] >= t_lo);
+                if (hit) {
+                    int slot0 = 0;
+                    if (lane == 0) slot0 = atomicAdd(s_count, __popc(hit));
+                    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+                    if ((hit >> lane) & 1u) {
+                        const int slot = slot0 + __popc(hit & ((1u << lane) - 1u));
+                        if (slot < kCandCap) {
+                            cand_key[slot] = order_key(v[r]);
+                            cand_idx[slot] = (int32_t)(base + lane + 32 * r);
+                        }
+                    }
+                }
+            }
+        }
+        for (int64_t w = tid; w < words; w += kThreads) { sel_bits[w] = 0; eq_bits[w] = 0; }
+        __syncthreads();
+        const int n_cand = *s_count;
+        __syncthreads();
+        if (n_cand >= keep && n_cand <= kCandCap) {
+            // ---- exact k-th key T among the candidates (three radix levels)
+            uint32_t prefix = 0;
+            int pbits = 0;
+            int64_t k_rem = keep;
 #pragma unroll 1
-    for (int lvl = 0; lvl < 3; ++lvl) {
-        const int bits = lvl == 0 ? 12 : 10;
-        const int nb = 1 << bits;
-        for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
-        __syncthreads();
-        const int shift = 32 - pbits - bits;
-        for (int64_t t = tid; t < n; t += kThreads) {
-            const uint32_t key = order_key(__ldg(sc + t));
-            const bool match = pbits == 0 || (key >> (32 - pbits)) == prefix;
-            if (match) atomicAdd(&hist[(key >> shift) & (uint32_t)(nb - 1)], 1u);
-        }
-        __syncthreads();
-        // Thread j owns bins [j*per, (j+1)*per); above_j counts the bins of all
-        // higher threads.  The digit d is the bin where the running count from
-        // the top first reaches k_rem.
-        const int per = nb / kThreads;
-        int local = 0;
-        for (int r = 0; r < per; ++r) local += (int)hist[tid * per + r];
-        int total;
-        const int excl = block_exclusive_scan(local, &total, warp_sums);
-        int64_t run = (int64_t)total - excl - local;
-        for (int r = per - 1; r >= 0; --r) {
-            const int bin = tid * per + r;
-            const int64_t h = hist[bin];
-            if (run < k_rem && run + h >= k_rem) {
-                s_digit = (uint32_t)bin;
-                s_above = run;
+            for (int lvl = 0; lvl < 3; ++lvl) {
+                const int bits = lvl == 2 ? 10 : 11;
+                const int nb = 1 << bits;
+                const int shift = 32 - pbits - bits;
+                for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
+                __syncthreads();
+                for (int i = tid; i < n_cand; i += kThreads) {
+                    const uint32_t key = cand_key[i];
+                    if (pbits == 0 || (key >> (32 - pbits)) == prefix)
+                        atomicAdd(&hist[(key >> shift) & (uint32_t)(nb - 1)], 1u);
+                }
+                __syncthreads();
+                find_digit(hist, nb, k_rem, warp_sums, s_digit, s_above);
+                k_rem -= *s_above;
+                prefix = (prefix << bits) | *s_digit;
+                pbits += bits;
+                __syncthreads();
             }
-            run += h;
+            const uint32_t T = prefix;
+            for (int i = tid; i < n_cand; i += kThreads) {
+                const uint32_t key = cand_key[i];
+                const int32_t t = cand_idx[i];
+                if (key > T) atomicOr(&sel_bits[t >> 5], 1u << (t & 31));
+                else if (key == T) atomicOr(&eq_bits[t >> 5], 1u << (t & 31));
+            }
+            __syncthreads();
+            // ---- emission in ascending order: keys > T, then the first k_rem keys == T
+            int64_t eq_base = 0, out_base = 0;
+            for (int64_t w0 = 0; w0 < words; w0 += kThreads) {
+                const int64_t w = w0 + tid;
+                const uint32_t sw = w < words ? sel_bits[w] : 0u;
+                const uint32_t ew = w < words ? eq_bits[w] : 0u;
+                int eq_total;
+                const int eq_excl = block_exclusive_scan(__popc(ew), &eq_total, warp_sums);
+                int64_t take = k_rem - (eq_base + eq_excl);
+                take = take < 0 ? 0 : (take > __popc(ew) ? __popc(ew) : take);
+                uint32_t m = ew, taken = 0;
+                for (int i = 0; i < take; ++i) { taken |= m & (~m + 1u); m &= m - 1u; }
+                uint32_t comb = sw | taken;
+                int sel_total;
+                const int sel_excl = block_exclusive_scan(__popc(comb), &sel_total, warp_sums);
+                int64_t pos = out_base + sel_excl;
+                while (comb != 0u && pos < keep) {
+                    const int bit = __ffs(comb) - 1;
+                    comb &= comb - 1u;
+                    put(out, pos++, w * 32 + bit, kpool);
+                }
+                eq_base += eq_total;
+                out_base += sel_total;
+            }
+            n_out = out_base;
+            done = true;
         }
-        __syncthreads();
-        k_rem -= s_above;
-        prefix = (prefix << bits) | s_digit;
-        pbits += bits;
-        __syncthreads();
     }
-    const uint32_t T = prefix;
-
-    // ---- emission in ascending index order
-    int64_t eq_base = 0, out_base = 0;
-    for (int64_t c0 = 0; c0 < n; c0 += (int64_t)kThreads * kItems) {
-        const int64_t t_begin = c0 + (int64_t)tid * kItems;
-        uint32_t keys[kItems];
-        int n_eq = 0, valid = 0;
-#pragma unroll
-        for (int i = 0; i < kItems; ++i) {
-            const int64_t t = t_begin + i;
-            if (t < n) {
-                keys[i] = order_key(__ldg(sc + t));
-                valid |= 1 << i;
-                n_eq += keys[i] == T;
-            } else {
-                keys[i] = 0;
-            }
-        }
-        int eq_total;
-        const int eq_excl = block_exclusive_scan(n_eq, &eq_total, warp_sums);
-        int64_t eq_rank = eq_base + eq_excl;
-        int selmask = 0, n_s = 0;
-#pragma unroll
-        for (int i = 0; i < kItems; ++i) {
-            if (!((valid >> i) & 1)) continue;
-            const bool gt = keys[i] > T;
-            const bool eq = keys[i] == T;
-            const bool s = gt || (eq && eq_rank < k_rem);
-            eq_rank += eq;
-            if (s) { selmask |= 1 << i; ++n_s; }
-        }
-        int sel_total;
-        const int sel_excl = block_exclusive_scan(n_s, &sel_total, warp_sums);
-        int64_t pos = out_base + sel_excl;
-#pragma unroll
-        for (int i = 0; i < kItems; ++i) {
-            if (!((selmask >> i) & 1)) continue;
-            if (pos >= keep) break;                 // never write past the kept count
-            const int64_t t = t_begin + i;
-            if (kpool == 1) {
-                out[pos] = (int32_t)t;
-            } else {
-                for (int r = 0; r < kpool; ++r) out[pos * kpool + r] = (int32_t)(t * kpool + r);
-            }
-            ++pos;
-        }
-        eq_base += eq_total;
-        out_base += sel_total;
-    }
-    if (tid == 0 && out_base != keep) record_error(err, kDevBadIndex, (int32_t)q, /*where=*/2);
+    if (!done)
+        select_multilevel(sc, n, keep, kpool, out, hist, warp_sums, s_digit, s_above, &n_out);
+    if (tid == 0 && n_out != keep) record_error(err, kDevBadIndex, (int32_t)q, /*where=*/2);
 
     // ---- unfilled tail (k-pool), then padding
     const int64_t body = keep * kpool;
@@ -188,8 +377,16 @@ cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* 
                                int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
                                cudaStream_t st) {
     if (b.n_q == 0) return cudaSuccess;
-    topk_select_kernel<<<b.n_q, kThreads, 0, st>>>(b, sh.top_k, sh.kpool, scores, ld, idx, n_sel,
-                                                   sh.index_row_width(), err);
+    // Bitmaps for the longest query if they fit; otherwise every query that
+    // needs more takes the multi-level path.
+    int64_t words = (b.max_kv_len / sh.kpool + 31) / 32;
+    if (kFixedSmem + (size_t)words * 8 > kMaxSmem) words = 0;
+    const size_t smem = kFixedSmem + (size_t)words * 8;
+    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_select_kernel<<<b.n_q, kThreads, smem, st>>>(b, sh.top_k, sh.kpool, scores, ld, idx, n_sel,
+                                                      sh.index_row_width(), (int32_t)words, err);
     return cudaGetLastError();
 }
 
