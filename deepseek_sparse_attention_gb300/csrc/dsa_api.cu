@@ -176,7 +176,8 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
     plan_attention_splits(sh, bh, &rps, &splits);
     const int32_t attn = splits > 1 ? 2 : 1;
     const int32_t idx = batch->max_kv_len / sh.kpool > 0
-                            ? (index_scores_tc_eligible(sh, bh) ? 2 : 1) : 0;
+                            ? (index_scores_tc_eligible(sh, bh) ? index_scores_tc_launches(sh, bh) : 1)
+                            : 0;
     int32_t n = 0;
     if (batch->n_q > 0) {
         switch (op) {

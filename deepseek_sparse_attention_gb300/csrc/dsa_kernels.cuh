@@ -29,11 +29,17 @@ cudaError_t launch_index_scores(const Shape& sh, const BatchDev& b, int64_t max_
                                 cudaStream_t st);
 bool index_scores_tc_eligible(const Shape& sh, const BatchDev& b);
 size_t index_scores_tc_scratch_bytes(int32_t n_seq, int32_t n_q);
+int32_t index_scores_tc_launches(const Shape& sh, const BatchDev& b);
 cudaError_t launch_index_scores_tc(const Shape& sh, const BatchDev& b, const void* q_idx,
                                    const float* w, const void* k_idx, float* scores, int64_t ld,
                                    void* scratch, int32_t* err, cudaStream_t st);
 
-// Step 2.  One selection row per query.
+// Step 2.  One selection row per query: one CTA per query (topk_select.cu), or
+// a 16-CTA cluster per query when there are few queries (topk_select_cluster.cu).
+bool topk_cluster_eligible(const Shape& sh, const BatchDev& b);
+cudaError_t launch_topk_select_cluster(const Shape& sh, const BatchDev& b, const float* scores,
+                                       int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
+                                       cudaStream_t st);
 cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* scores,
                                int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
                                cudaStream_t st);

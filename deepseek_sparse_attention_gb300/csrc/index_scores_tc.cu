@@ -60,7 +60,11 @@ struct Cfg {
     // full[S], empty[S], b_full, b_empty, acc_full[2], acc_empty[2], drain
     static constexpr int kNumBars = 2 * kStages + 7;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+    // decode batches plan their (query, key tile) units in shared memory
+    static constexpr int kLocalMaxQ = 256;
+    static constexpr uint32_t kOffPlanG = (kOffMisc + 16 + 15) / 16 * 16;           // IdxGroup[256]
+    static constexpr uint32_t kOffPlanT = kOffPlanG + kLocalMaxQ * 24;             // int64[257]
+    static constexpr uint32_t kSmemBytes = kOffPlanT + (kLocalMaxQ + 1) * 8 + 1024;
     static_assert(kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
                   "TMEM allocation must be a power of two");
 };
@@ -165,7 +169,7 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 const float* __restrict__ w, const IdxGroup* __restrict__ groups,
                 const int64_t* __restrict__ tile_off, const int64_t* __restrict__ seq_goff,
                 int32_t n_seq, int32_t kpool, float* __restrict__ scores, int64_t ld,
-                int32_t* err) {
+                BatchDev bq, int32_t local_plan, int32_t* err) {
     using C = Cfg<GQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -181,7 +185,34 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_groups = seq_goff[n_seq];
+    int64_t n_groups;
+    if (local_plan) {
+        // one group per query (decode); every CTA derives the schedule itself
+        IdxGroup* gs = reinterpret_cast<IdxGroup*>(smem + C::kOffPlanG);
+        int64_t* ts = reinterpret_cast<int64_t*>(smem + C::kOffPlanT);
+        if (threadIdx.x < bq.n_q) {
+            QueryInfo qi;
+            IdxGroup G{0, (int32_t)threadIdx.x, 0, 0, 0};
+            if (query_info(bq, threadIdx.x, qi, err, /*where=*/4)) {
+                G.key0 = qi.key0;
+                G.nq = 1;
+                G.L_last = (int32_t)qi.L;
+            }
+            gs[threadIdx.x] = G;
+            ts[threadIdx.x + 1] = G.nq ? (G.L_last / kpool + kTileKeys - 1) / kTileKeys : 0;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            ts[0] = 0;
+            for (int i = 1; i <= bq.n_q; ++i) ts[i] += ts[i - 1];
+        }
+        __syncthreads();
+        groups = gs;
+        tile_off = ts;
+        n_groups = bq.n_q;
+    } else {
+        n_groups = seq_goff[n_seq];
+    }
     const int64_t U = tile_off[n_groups];
     const int64_t u_begin = (int64_t)blockIdx.x * U / gridDim.x;
     const int64_t u_end = (int64_t)(blockIdx.x + 1) * U / gridDim.x;
@@ -417,15 +448,19 @@ cudaError_t launch_tc(const Shape& sh, const BatchDev& b, const void* q_idx, con
     if (!make_rows128_map(&tm_k, k_idx, (uint64_t)b.total_keys, kTileKeys) ||
         !make_rows128_map(&tm_q, q_idx, (uint64_t)b.n_q * kIdxHeads, C::N))
         return cudaErrorInvalidValue;
-    idx_group_plan<<<1, 1024, 0, st>>>(b, GQ, pa.seq_goff, pa.groups, pa.tile_off, err);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    const bool local = GQ == 1 && b.n_q <= C::kLocalMaxQ;
+    cudaError_t e;
+    if (!local) {
+        idx_group_plan<<<1, 1024, 0, st>>>(b, GQ, pa.seq_goff, pa.groups, pa.tile_off, err);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     auto kern = index_scores_tc<GQ>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<sm_count(), C::kThreads, C::kSmemBytes, st>>>(tm_k, tm_q, w, pa.groups, pa.tile_off,
                                                          pa.seq_goff, b.n_seq, sh.kpool, scores,
-                                                         ld, err);
+                                                         ld, b, local ? 1 : 0, err);
     return cudaGetLastError();
 }
 
@@ -436,6 +471,12 @@ bool index_scores_tc_eligible(const Shape& sh, const BatchDev& b) {
     return sh.dtype == DSA_BF16 && sh.idx_heads == kIdxHeads && sh.idx_dim == kIdxDim &&
            b.total_keys >= kTileKeys && b.total_keys < ((int64_t)1 << 31) &&
            (int64_t)b.n_q * kIdxHeads < ((int64_t)1 << 31);
+}
+
+int32_t index_scores_tc_launches(const Shape& sh, const BatchDev& b) {
+    (void)sh;
+    const bool gq1 = b.max_q_len <= 1 || b.n_q < 8;
+    return (gq1 && b.n_q <= Cfg<1>::kLocalMaxQ) ? 1 : 2;
 }
 
 size_t index_scores_tc_scratch_bytes(int32_t n_seq, int32_t n_q) {

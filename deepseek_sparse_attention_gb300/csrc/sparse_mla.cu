@@ -226,35 +226,29 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
     }
 }
 
-// Log-sum-exp merge of the splits of one (query, head): 128 threads x 4 columns.
+// Log-sum-exp merge of the splits of one query: one CTA per (head, 128 latent
+// columns), one column per thread, so the partials are read by many SMs at once.
 __global__ void __launch_bounds__(128)
 merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __restrict__ part_ml,
              float* __restrict__ out, float* __restrict__ lse) {
-    const int h = blockIdx.x;
+    const int h = blockIdx.x >> 2;
+    const int c = ((blockIdx.x & 3) << 7) + threadIdx.x;
     const int64_t q = blockIdx.y;
+    const float* ml = part_ml + (q * n_split * kHeads + h) * 2;     // split s at + s*kHeads*2
     float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, part_ml[((q * n_split + s) * kHeads + h) * 2]);
-    float Lsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldg(ml + (int64_t)s * kHeads * 2));
+    float Lsum = 0.f, acc = 0.f;
     if (M != -INFINITY) {
         for (int s = 0; s < n_split; ++s) {
-            const int64_t part = q * n_split + s;
-            const float ms = part_ml[(part * kHeads + h) * 2];
-            const float ls = part_ml[(part * kHeads + h) * 2 + 1];
+            const float ms = __ldg(ml + (int64_t)s * kHeads * 2);
             if (ms == -INFINITY) continue;
             const float f = expf(ms - M);
-            Lsum = fmaf(ls, f, Lsum);
-            const float4 v = *reinterpret_cast<const float4*>(
-                part_o + (part * kHeads + h) * (int64_t)kLatent + 4 * threadIdx.x);
-            acc.x = fmaf(v.x, f, acc.x); acc.y = fmaf(v.y, f, acc.y);
-            acc.z = fmaf(v.z, f, acc.z); acc.w = fmaf(v.w, f, acc.w);
+            Lsum = fmaf(__ldg(ml + (int64_t)s * kHeads * 2 + 1), f, Lsum);
+            acc = fmaf(__ldg(part_o + ((q * n_split + s) * kHeads + h) * (int64_t)kLatent + c), f, acc);
         }
     }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    *reinterpret_cast<float4*>(out + (q * kHeads + h) * (int64_t)kLatent + 4 * threadIdx.x) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (lse != nullptr && threadIdx.x == 0)
-        lse[q * kHeads + h] = Lsum > 0.f ? M + logf(Lsum) : -INFINITY;
+    out[(q * kHeads + h) * (int64_t)kLatent + c] = Lsum > 0.f ? acc / Lsum : 0.f;
+    if (lse != nullptr && c == 0) lse[q * kHeads + h] = Lsum > 0.f ? M + logf(Lsum) : -INFINITY;
 }
 
 // Rows per split: enough CTAs to fill the GPU about twice, at least 64 rows each.
@@ -299,7 +293,8 @@ cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, 
 
 cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
                                 const float* part_ml, float* out, float* lse, cudaStream_t st) {
-    merge_splits<<<dim3(kHeads, (unsigned)n_q), 128, 0, st>>>(n_split, part_o, part_ml, out, lse);
+    merge_splits<<<dim3(kHeads * (kLatent / 128), (unsigned)n_q), 128, 0, st>>>(n_split, part_o,
+                                                                               part_ml, out, lse);
     return cudaGetLastError();
 }
 

@@ -9,16 +9,17 @@
 // key and value alike).
 //
 // One CTA handles a range of one query's selected rows in tiles of 128 rows:
-//   warp 0     loads the query once (TMA tiles) and gathers each tile's rows
-//              with TMA gather4 (four arbitrary rows per instruction, 128-byte
-//              swizzle) into shared memory;
+//   warps 0,2,3 load the query once (TMA tiles) and gather each tile's rows
+//              with 16-byte cp.async copies straight into the 128-byte swizzle
+//              layout -- thousands of copies in flight per SM, where a TMA
+//              gather4 (four 128-byte row pieces per request) kept too few;
 //   warp 1     issues S^T = R . Q^T (M = 128 rows, N = 64 heads, K = the row
 //              width) into TMEM, then O^T += R^T . P^T (M = 128 latent columns
 //              x 4, N = 64 heads, K = 128 rows) with both operands MN-major --
 //              the same gathered tile serves as K-major A for the scores and as
 //              MN-major A for the values;
-//   warps 4-7  softmax across the tile's rows: one TMEM lane (row) per thread,
-//              per-head tile maxima by warp reductions, a running maximum that
+//   warps 4-11 softmax across the tile's rows: one TMEM lane (row) and half the
+//              heads per thread, per-head tile maxima by warp reductions, a running maximum that
 //              is raised (and O^T rescaled in TMEM) only when a tile exceeds it
 //              by more than 2^8, exp2, P^T written to shared memory (into the
 //              rope block, which the scores no longer need), per-thread partial
@@ -46,6 +47,9 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kSlack = 8.f;                       // lazy rescale threshold (log2 units)
+constexpr int kLoaders = 96;                        // threads that gather rows
+constexpr int kSoftmaxThreads = 256;                // two warpgroups
+constexpr int kThreads = 128 + kSoftmaxThreads;     // loaders + MMA warp, then softmax
 
 template <int W>
 struct Cfg {
@@ -60,7 +64,8 @@ struct Cfg {
     static constexpr uint32_t kOffRed = kOffBar + 64;          // [2][4][64] int
     static constexpr uint32_t kOffL = kOffRed + 2 * 4 * 64 * 4; // [64] float
     static constexpr uint32_t kOffM = kOffL + 64 * 4;           // [64] float
-    static constexpr uint32_t kOffMisc = kOffM + 64 * 4;
+    static constexpr uint32_t kOffRows = kOffM + 64 * 4;       // [128] int64 row addresses
+    static constexpr uint32_t kOffMisc = kOffRows + 128 * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -72,8 +77,8 @@ __device__ __forceinline__ int fkey(float f) {           // order-preserving flo
 __device__ __forceinline__ float fval(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff); }
 
 template <int W>
-__global__ void __launch_bounds__(256, 1)
-sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__ cache,
               BatchDev b, float scale, const int32_t* __restrict__ idx,
               const int32_t* __restrict__ n_sel, int64_t idx_width, int32_t rows_per_split,
               int32_t n_split, float* __restrict__ out, float* __restrict__ lse,
@@ -87,6 +92,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     int* red = reinterpret_cast<int*>(smem + C::kOffRed);
     float* l_fin = reinterpret_cast<float*>(smem + C::kOffL);
     float* m_fin = reinterpret_cast<float*>(smem + C::kOffM);
+    int64_t* row_s = reinterpret_cast<int64_t*>(smem + C::kOffRows);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -117,59 +123,77 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int n_tiles = (int)((j1 - j0 + kTileRows - 1) / kTileRows);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(&bars[i], i == 3 ? 128 : 1);
+        for (int i = 0; i < 7; ++i)
+            mbar_init(&bars[i], i == 3 ? kSoftmaxThreads : (i == 1 ? kLoaders : 1));
         fence_mbarrier_init();
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_c);
-    }
+    if (warp == 0 && lane == 0) prefetch_tensormap(&tm_q);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {                                                  // ---- loads
+    if (warp != 1 && warp < 4) {                                      // ---- loads
+        // warps 0, 2, 3: 96 threads copy each tile's rows with 16-byte cp.async
+        // into the 128-byte swizzle layout (many copies in flight per SM), then
+        // make them visible to the tensor core's async proxy and arrive.
+        const int p = warp == 0 ? lane : 32 * (warp - 1) + lane;
         bool ok = true;
-        if (lane == 0) {
+        if (p == 0) {
             mbar_arrive_expect_tx(q_full, C::kCB * kQBlock);
             for (int cb = 0; cb < C::kCB; ++cb)
                 tma_load_2d(smem + C::kOffQ + cb * kQBlock, &tm_q, q_full, 64 * cb,
                             (int32_t)(q * kHeads));
         }
         const int32_t* irow = idx + q * idx_width;
+        const unsigned char* cbase = static_cast<const unsigned char*>(cache);
         for (int t = 0; t < n_tiles && ok; ++t) {
-            if (t > 0) {                       // the previous tile's values are consumed
-                int o = 1;
-                if (lane == 0) o = mbar_wait(pv_done, (uint32_t)((t - 1) & 1), kWaitNs);
-                ok = __shfl_sync(0xffffffffu, o, 0) != 0;
-            }
-            if (!ok) break;
-            int32_t g[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int64_t j = j0 + (int64_t)t * kTileRows + 4 * lane + i;
-                int32_t r = 0;
+            if (t > 0) ok = mbar_wait(pv_done, (uint32_t)((t - 1) & 1), kWaitNs);
+            // this tile's row addresses, staged in shared memory
+            for (int r = p; r < kTileRows; r += kLoaders) {
+                const int64_t j = j0 + (int64_t)t * kTileRows + r;
+                int32_t rr = 0;
                 if (j < j1) {
-                    r = irow[j];
-                    if (r < 0 || r >= qi.L) {
+                    rr = irow[j];
+                    if (rr < 0 || rr >= qi.L) {
                         record_error(err, kDevBadIndex, (int32_t)q, /*where=*/8);
-                        r = 0;
+                        rr = 0;
                     }
                 }
-                g[i] = (int32_t)(qi.row0 + r);
+                row_s[r] = qi.row0 + rr;
             }
-            if (lane == 0) mbar_arrive_expect_tx(r_full, C::kCB * kRBlock);
-            __syncwarp();
-            uint8_t* rdst = smem + C::kOffR + lane * 512;
-            for (int cb = 0; cb < C::kCB; ++cb)
-                tma_gather4(rdst + cb * kRBlock, &tm_c, r_full, 64 * cb, g[0], g[1], g[2], g[3]);
+            {   // all loaders agree on whether to proceed
+                uint32_t all_ok;
+                asm volatile(
+                    "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                    "bar.red.and.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                    : "=r"(all_ok)
+                    : "r"((uint32_t)ok), "n"(kLoaders)
+                    : "memory");
+                ok = all_ok != 0;
+            }
+            if (ok) {
+                constexpr int kChunks = W / 8;                 // 16-byte chunks per row
+                for (int c = p; c < kTileRows * kChunks; c += kLoaders) {
+                    const int r = c / kChunks, c16 = c - r * kChunks;
+                    const int cb = c16 >> 3, k = c16 & 7;
+                    const uint32_t dst = smem_u32(smem + C::kOffR + cb * kRBlock + r * 128 +
+                                                  ((k ^ (r & 7)) << 4));
+                    const unsigned char* src = cbase + (row_s[r] * W + c16 * 8) * 2;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src)
+                                 : "memory");
+                }
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                fence_proxy_async_smem();
+            }
+            mbar_arrive(r_full);
+            asm volatile("bar.sync 2, %0;" ::"n"(kLoaders) : "memory");   // row_s reusable
         }
-        if (!ok && lane == 0) record_error(err, kDevTimeout, (int32_t)q, /*where=*/9);
+        if (!ok && p == 0) record_error(err, kDevTimeout, (int32_t)q, /*where=*/9);
     } else if (warp == 1) {                                           // ---- MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kTileRows, kHeads);
@@ -218,17 +242,20 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_wait(drain, 0, 50000000ull);
         }
     } else if (warp >= 4) {                                           // ---- softmax
-        const int wq = warp & 3;
+        // two warpgroups over the same 128 rows: warpgroup sg owns heads
+        // [32 sg, 32 sg + 32) of every row (warps w and w + 4 share a TMEM quadrant)
+        const int wq = warp & 3, sg = (warp - 4) >> 2;
         const int row = 32 * wq + lane;
+        const int hb = 32 * sg;                      // first head of this thread
         const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * wq) << 16);
         const float c2 = scale * kLog2e;
-        float l_part[kHeads];
+        float l_part[32];
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) l_part[h] = 0.f;
+        for (int e = 0; e < 32; ++e) l_part[e] = 0.f;
         // running maxima (one writer per head) and rescale factors live in shared memory
         float* m_sh = m_fin;
         float* alpha_s = l_fin;
-        if (row < kHeads) m_sh[row] = -INFINITY;
+        if (row < 32) m_sh[hb + row] = -INFINITY;
         uint8_t* prow = smem + C::kOffP + row * 128;
         bool ok = true;
         for (int t = 0; t < n_tiles; ++t) {
@@ -242,105 +269,97 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const int32_t r = idx[q * idx_width + jrow];
                 valid = r >= 0 && r < qi.L;
             }
-            // per-head maximum over the tile's 128 rows
-            int* rb = red + (t & 1) * 4 * kHeads + wq * kHeads;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+            float x[32];
+            {
                 float v[32];
-                tmem_ld_32cols(lane_addr + 32 * hh, v);
+                tmem_ld_32cols(lane_addr + hb, v);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int mk = __reduce_max_sync(0xffffffffu, fkey(valid ? v[e] * c2 : -INFINITY));
-                    if (lane == e) rb[32 * hh + e] = mk;
-                }
+                for (int e = 0; e < 32; ++e) x[e] = valid ? v[e] * c2 : -INFINITY;
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            // per-head maximum over the tile's 128 rows
+            int* rb = red + (t & 1) * 4 * kHeads + wq * kHeads + hb;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int mk = __reduce_max_sync(0xffffffffu, fkey(x[e]));
+                if (lane == e) rb[e] = mk;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
             uint32_t raised = 0;
-            if (row < kHeads) {                        // head `row`: raise its running maximum?
+            if (row < 32) {                            // head hb + row: raise its running maximum?
+                const int h = hb + row;
                 const int* rt = red + (t & 1) * 4 * kHeads;
-                const int mk = max(max(rt[row], rt[kHeads + row]),
-                                   max(rt[2 * kHeads + row], rt[3 * kHeads + row]));
-                const float tmax = fval(mk), m_old = m_sh[row];
+                const int mk = max(max(rt[h], rt[kHeads + h]), max(rt[2 * kHeads + h], rt[3 * kHeads + h]));
+                const float tmax = fval(mk), m_old = m_sh[h];
                 float a = 1.f;
                 if (tmax > m_old + kSlack) {
                     a = m_old == -INFINITY ? 0.f : exp2f(m_old - tmax);
-                    m_sh[row] = tmax;
+                    m_sh[h] = tmax;
                     raised = 1;
                 }
-                alpha_s[row] = a;
+                alpha_s[h] = a;
             }
             uint32_t any_raised;
             asm volatile(
                 "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-                "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
                 : "=r"(any_raised)
-                : "r"(raised)
+                : "r"(raised), "n"(kSoftmaxThreads)
                 : "memory");
             if (any_raised) {
 #pragma unroll
-                for (int h = 0; h < kHeads; ++h) l_part[h] *= alpha_s[h];
+                for (int e = 0; e < 32; ++e) l_part[e] *= alpha_s[hb + e];
             }
             if (any_raised && t > 0) {                 // O^T follows the new maxima
 #pragma unroll 1
                 for (int i = 0; i < 4; ++i) {
-#pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        float v[32];
-                        const uint32_t a = lane_addr + kOCol + 64 * i + 32 * hh;
-                        tmem_ld_32cols(a, v);
+                    float v[32];
+                    const uint32_t a = lane_addr + kOCol + 64 * i + hb;
+                    tmem_ld_32cols(a, v);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) v[c] *= alpha_s[32 * hh + c];
-                        tmem_st_32cols(a, v);
-                    }
+                    for (int c = 0; c < 32; ++c) v[c] *= alpha_s[hb + c];
+                    tmem_st_32cols(a, v);
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
             }
-            // P^T row of this thread: 64 bf16 in the 128-byte swizzle layout.
-            // p = hi + lo with hi = bf16(p), lo = bf16(p - hi); hi goes to shared
-            // memory now, lo waits in spare TMEM columns for the second pass.
-            float lo_bits[32];
+            // this thread's half of its P^T row: 32 bf16 in the 128-byte swizzle
+            // layout.  p = hi + lo with hi = bf16(p), lo = bf16(p - hi); hi goes to
+            // shared memory now, lo waits in spare TMEM columns for the second pass.
+            float lo_bits[16];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[32];
-                tmem_ld_32cols(lane_addr + 32 * hh, v);
+            for (int c16 = 0; c16 < 4; ++c16) {
+                uint32_t w4[4];
 #pragma unroll
-                for (int c16 = 0; c16 < 4; ++c16) {
-                    uint32_t w4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int hl = 8 * c16 + 2 * e, h = 32 * hh + hl;
-                        const float x0 = valid ? v[hl] * c2 : -INFINITY;
-                        const float x1 = valid ? v[hl + 1] * c2 : -INFINITY;
-                        const float p0 = exp2f(x0 - m_sh[h]);
-                        const float p1 = exp2f(x1 - m_sh[h + 1]);
-                        const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
-                        const float2 hf = __bfloat1622float2(hi);
-                        const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-                        const float2 lf = __bfloat1622float2(lo);
-                        l_part[h] += hf.x + lf.x;
-                        l_part[h + 1] += hf.y + lf.y;
-                        w4[e] = *reinterpret_cast<const uint32_t*>(&hi);
-                        lo_bits[16 * hh + 4 * c16 + e] =
-                            __uint_as_float(*reinterpret_cast<const uint32_t*>(&lo));
-                    }
-                    const int chunk = 4 * hh + c16;
-                    *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                for (int e = 0; e < 4; ++e) {
+                    const int hl = 8 * c16 + 2 * e;
+                    const float p0 = exp2f(x[hl] - m_sh[hb + hl]);
+                    const float p1 = exp2f(x[hl + 1] - m_sh[hb + hl + 1]);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+                    const float2 hf = __bfloat1622float2(hi);
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+                    const float2 lf = __bfloat1622float2(lo);
+                    l_part[hl] += hf.x + lf.x;
+                    l_part[hl + 1] += hf.y + lf.y;
+                    w4[e] = *reinterpret_cast<const uint32_t*>(&hi);
+                    lo_bits[4 * c16 + e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&lo));
                 }
+                const int chunk = 4 * sg + c16;
+                *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            tmem_st_32cols(lane_addr + kLoCol, lo_bits);
+            tmem_st_16cols(lane_addr + kLoCol + 16 * sg, lo_bits);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(p_full);
             // second pass: the lo parts, once the hi product has read the buffer
             if (ok) ok = mbar_wait(pv_hi, (uint32_t)(t & 1), kWaitNs);
             tc_fence_after();
-            tmem_ld_32cols(lane_addr + kLoCol, lo_bits);
+            tmem_ld_16cols(lane_addr + kLoCol + 16 * sg, lo_bits);
 #pragma unroll
-            for (int chunk = 0; chunk < 8; ++chunk) {
+            for (int c16 = 0; c16 < 4; ++c16) {
+                const int chunk = 4 * sg + c16;
                 *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-                    make_uint4(__float_as_uint(lo_bits[4 * chunk]), __float_as_uint(lo_bits[4 * chunk + 1]),
-                               __float_as_uint(lo_bits[4 * chunk + 2]), __float_as_uint(lo_bits[4 * chunk + 3]));
+                    make_uint4(__float_as_uint(lo_bits[4 * c16]), __float_as_uint(lo_bits[4 * c16 + 1]),
+                               __float_as_uint(lo_bits[4 * c16 + 2]), __float_as_uint(lo_bits[4 * c16 + 3]));
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -353,34 +372,30 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // the row tile is free once the last PV has completed)
         float* lsc = reinterpret_cast<float*>(smem + C::kOffR);
 #pragma unroll
-        for (int h = 0; h < kHeads; ++h) lsc[row * (kHeads + 1) + h] = l_part[h];
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (row < kHeads) {
-            float s = 0.f;
-            for (int r = 0; r < kTileRows; ++r) s += lsc[r * (kHeads + 1) + row];
-            l_fin[row] = s;
+        for (int e = 0; e < 32; ++e) lsc[row * (kHeads + 1) + hb + e] = l_part[e];
+        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        if (sg == 0 && row < kHeads) {
+            float sum = 0.f;
+            for (int r = 0; r < kTileRows; ++r) sum += lsc[r * (kHeads + 1) + row];
+            l_fin[row] = sum;
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        // O^T lane `row` holds latent columns row + 128 i
+        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        // O^T lane `row` holds latent columns row + 128 i; this thread writes heads hb..
         const bool final_out = n_split == 1;
         const int64_t part = q * n_split + split;
         float* dst = final_out ? out + q * kHeads * kLatent : part_o + part * kHeads * kLatent;
 #pragma unroll 1
         for (int i = 0; i < 4; ++i) {
             const int c = row + kTileRows * i;
+            float v[32];
+            tmem_ld_32cols(lane_addr + kOCol + 64 * i + hb, v);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[32];
-                tmem_ld_32cols(lane_addr + kOCol + 64 * i + 32 * hh, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int h = 32 * hh + e;
-                    const float l = l_fin[h];
-                    dst[h * kLatent + c] = final_out ? (l > 0.f ? v[e] / l : 0.f) : v[e];
-                }
+            for (int e = 0; e < 32; ++e) {
+                const float l = l_fin[hb + e];
+                dst[(hb + e) * kLatent + c] = final_out ? (l > 0.f ? v[e] / l : 0.f) : v[e];
             }
         }
-        if (row < kHeads) {
+        if (sg == 0 && row < kHeads) {
             const float l = l_fin[row];
             const float m = m_fin[row];
             if (final_out) {
@@ -440,16 +455,14 @@ cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, cons
                      float* part_o, float* part_ml, int32_t rps, int32_t n_split, int32_t* err,
                      cudaStream_t st) {
     using C = Cfg<W>;
-    CUtensorMap tm_q, tm_c;
-    if (!make_map(&tm_q, q_abs, (uint64_t)b.n_q * kHeads, W, kHeads) ||
-        !make_map(&tm_c, cache, (uint64_t)b.total_rows, W, 1))
-        return cudaErrorInvalidValue;
+    CUtensorMap tm_q;
+    if (!make_map(&tm_q, q_abs, (uint64_t)b.n_q * kHeads, W, kHeads)) return cudaErrorInvalidValue;
     auto kern = sparse_mla_tc<W>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3((unsigned)n_split, (unsigned)b.n_q), 256, C::kSmemBytes, st>>>(
-        tm_q, tm_c, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split, out, lse, part_o,
+    kern<<<dim3((unsigned)n_split, (unsigned)b.n_q), kThreads, C::kSmemBytes, st>>>(
+        tm_q, cache, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split, out, lse, part_o,
         part_ml, err);
     e = cudaGetLastError();
     if (e != cudaSuccess || n_split == 1) return e;

@@ -377,6 +377,8 @@ cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* 
                                int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
                                cudaStream_t st) {
     if (b.n_q == 0) return cudaSuccess;
+    if (topk_cluster_eligible(sh, b))
+        return launch_topk_select_cluster(sh, b, scores, ld, idx, n_sel, err, st);
     // Bitmaps for the longest query if they fit; otherwise every query that
     // needs more takes the multi-level path.
     int64_t words = (b.max_kv_len / sh.kpool + 31) / 32;
