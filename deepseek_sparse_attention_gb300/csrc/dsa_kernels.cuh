@@ -9,6 +9,26 @@
 
 namespace dsa {
 
+// Launches `kern` on `st` with programmatic stream serialization allowed, so
+// its prologue may overlap the previous kernel's tail (the kernel itself waits,
+// with griddepcontrol.wait, before it touches memory the previous kernel
+// writes or reads).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Validated layer geometry (see dsa_shape in dsa.h).
 struct Shape {
     int32_t idx_heads, idx_dim, heads, kv_lora, rope, top_k, kpool;

@@ -185,7 +185,9 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
     int64_t n_groups;
+    if (!local_plan) pdl_wait();                      // the plan kernel's arrays
     if (local_plan) {
         // one group per query (decode); every CTA derives the schedule itself
         IdxGroup* gs = reinterpret_cast<IdxGroup*>(smem + C::kOffPlanG);
@@ -337,6 +339,7 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         c.seek(u_begin, n_groups);
         int ab = 0;
         uint32_t acc_par = 0;
+        pdl_wait();                                    // the score rows may still be read
         for (int64_t u = u_begin; u < u_end; ++u) {
             const IdxGroup G = groups[c.g];
             if (*abort_flag || !mbar_wait(&acc_full[ab], acc_par, kWaitNs)) {
@@ -458,10 +461,10 @@ cudaError_t launch_tc(const Shape& sh, const BatchDev& b, const void* q_idx, con
     auto kern = index_scores_tc<GQ>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<sm_count(), C::kThreads, C::kSmemBytes, st>>>(tm_k, tm_q, w, pa.groups, pa.tile_off,
-                                                         pa.seq_goff, b.n_seq, sh.kpool, scores,
-                                                         ld, b, local ? 1 : 0, err);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(sm_count()), dim3(C::kThreads), C::kSmemBytes, st, tm_k, tm_q, w,
+                      (const IdxGroup*)pa.groups, (const int64_t*)pa.tile_off,
+                      (const int64_t*)pa.seq_goff, b.n_seq, sh.kpool, scores, ld, b,
+                      local ? 1 : 0, err);
 }
 
 }  // namespace

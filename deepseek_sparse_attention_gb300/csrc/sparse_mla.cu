@@ -231,6 +231,8 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
 __global__ void __launch_bounds__(128)
 merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __restrict__ part_ml,
              float* __restrict__ out, float* __restrict__ lse) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");      // the partials must be complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int h = blockIdx.x >> 2;
     const int c = ((blockIdx.x & 3) << 7) + threadIdx.x;
     const int64_t q = blockIdx.y;
@@ -293,9 +295,8 @@ cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, 
 
 cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
                                 const float* part_ml, float* out, float* lse, cudaStream_t st) {
-    merge_splits<<<dim3(kHeads * (kLatent / 128), (unsigned)n_q), 128, 0, st>>>(n_split, part_o,
-                                                                               part_ml, out, lse);
-    return cudaGetLastError();
+    return launch_pdl(merge_splits, dim3(kHeads * (kLatent / 128), (unsigned)n_q), dim3(128), 0, st,
+                      n_split, part_o, part_ml, out, lse);
 }
 
 void plan_attention_splits(const Shape& sh, const BatchDev& b, int32_t* rows_per_split,

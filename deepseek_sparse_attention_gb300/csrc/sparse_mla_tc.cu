@@ -98,6 +98,8 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t q = blockIdx.y;
     const int split = blockIdx.x;
+    pdl_wait();                                       // the selection must be complete
+    pdl_trigger();
     QueryInfo qi;
     if (!query_info(b, q, qi, err, /*where=*/8)) return;
     int64_t ns = n_sel[q];
@@ -461,10 +463,9 @@ cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, cons
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3((unsigned)n_split, (unsigned)b.n_q), kThreads, C::kSmemBytes, st>>>(
-        tm_q, cache, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split, out, lse, part_o,
-        part_ml, err);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3((unsigned)n_split, (unsigned)b.n_q), dim3(kThreads), C::kSmemBytes, st,
+                   tm_q, cache, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split, out,
+                   lse, part_o, part_ml, err);
     if (e != cudaSuccess || n_split == 1) return e;
     return launch_merge_splits(b.n_q, n_split, part_o, part_ml, out, lse, st);
 }

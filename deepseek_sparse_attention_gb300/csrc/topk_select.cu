@@ -221,6 +221,8 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t q = blockIdx.x;
     int32_t* out = idx + q * width;
+    asm volatile("griddepcontrol.wait;" ::: "memory");      // the scores must be complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     QueryInfo qi;
     if (!query_info(b, q, qi, err, /*where=*/2)) {
         for (int64_t i = tid; i < width; i += kThreads) out[i] = -1;
@@ -387,9 +389,9 @@ cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* 
     cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_select_kernel<<<b.n_q, kThreads, smem, st>>>(b, sh.top_k, sh.kpool, scores, ld, idx, n_sel,
-                                                      sh.index_row_width(), (int32_t)words, err);
-    return cudaGetLastError();
+    return launch_pdl(topk_select_kernel, dim3((unsigned)b.n_q), dim3(kThreads), smem, st, b,
+                      sh.top_k, sh.kpool, scores, ld, idx, n_sel, sh.index_row_width(),
+                      (int32_t)words, err);
 }
 
 }  // namespace dsa

@@ -158,6 +158,8 @@ topk_select_cluster(BatchDev b, int32_t top_k, int32_t kpool, const float* __res
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t q = blockIdx.y;
     int32_t* out = idx + q * width;
+    asm volatile("griddepcontrol.wait;" ::: "memory");      // the scores must be complete
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     QueryInfo qi;
     const bool qok = query_info(b, q, qi, err, /*where=*/12);
@@ -362,9 +364,8 @@ cudaError_t launch_topk_select_cluster(const Shape& sh, const BatchDev& b, const
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk_select_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    topk_select_cluster<<<dim3(kCtas, (unsigned)b.n_q), kThreads, smem, st>>>(
-        b, sh.top_k, sh.kpool, scores, ld, idx, n_sel, sh.index_row_width(), err);
-    return cudaGetLastError();
+    return launch_pdl(topk_select_cluster, dim3(kCtas, (unsigned)b.n_q), dim3(kThreads), smem, st, b,
+                      sh.top_k, sh.kpool, scores, ld, idx, n_sel, sh.index_row_width(), err);
 }
 
 }  // namespace dsa
