@@ -1,0 +1,269 @@
+// index_pipeline.cuh -- the warp-specialised tcgen05 indexer pipeline, shared
+// by the standalone indexer kernel and the fused decode kernel.
+//
+// One CTA walks a contiguous range [u_begin, u_end) of (query group, key tile)
+// units.  warp 0: TMA producer (key tiles into a shared-memory ring with the
+// 128-byte swizzle, the group's query rows once per group); warp 1: one thread
+// issues tcgen05.mma (M = 128 keys, N = 32 heads per query, K = 128) into two
+// TMEM accumulators; warps 4..: epilogue, one TMEM lane (key) per thread,
+// relu and the weighted head sum, handed to an epilogue policy `Epi`:
+//   epi.begin()                              once per epilogue thread
+//   epi.emit(G, j, t_row, valid, u, row, s)  score s of key t_row of query
+//                                            G.q0 + j (valid: t_row is visible)
+// All waits are bounded; a timeout sets the error word and winds down.
+#pragma once
+
+#include "dsa_kernels.cuh"
+#include "sm100.cuh"
+
+namespace dsa {
+namespace idxp {
+
+using namespace sm100;
+
+constexpr int kTileKeys = 128;                      // MMA M
+constexpr int kIdxDim = 128;                        // MMA K
+constexpr int kIdxHeads = 32;
+constexpr uint32_t kRowHalfBytes = 128;             // 64 bf16: one swizzle row
+constexpr uint32_t kABoxBytes = kTileKeys * kRowHalfBytes;    // 16 KB
+constexpr uint32_t kABytes = 2 * kABoxBytes;                  // 32 KB per key tile
+constexpr uint64_t kWaitNs = 2000000000ull;         // bounded waits: 2 s
+
+struct IdxGroup {          // consecutive queries of one sequence scored together
+    int64_t key0;          // first indexer key of the sequence
+    int32_t q0;            // first query of the group
+    int32_t nq;            // queries in the group
+    int32_t L_last;        // rows seen by the group's last query
+    int32_t pad;
+};
+
+template <int GQ, int STAGES = (GQ == 1 ? 6 : 4)>
+struct Cfg {
+    static constexpr int N = kIdxHeads * GQ;
+    static constexpr int kStages = STAGES;
+    static constexpr uint32_t kBBoxBytes = N * kRowHalfBytes;
+    static constexpr uint32_t kBBytes = 2 * kBBoxBytes;
+    static constexpr uint32_t kTmemCols = 2 * N;                  // two accumulators
+    static constexpr int kEpiWarps = GQ == 1 ? 4 : 8;
+    static constexpr int kEpiGroups = kEpiWarps / 4;              // warpgroups in the epilogue
+    static constexpr int kThreads = (4 + kEpiWarps) * 32;
+    static constexpr uint32_t kOffA = 0;
+    static constexpr uint32_t kOffB = kStages * kABytes;
+    static constexpr uint32_t kOffBar = kOffB + kBBytes;
+    // full[S], empty[S], b_full, b_empty, acc_full[2], acc_empty[2], drain
+    static constexpr int kNumBars = 2 * kStages + 7;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    // decode batches plan their (query, key tile) units in shared memory
+    static constexpr int kLocalMaxQ = 256;
+    static constexpr uint32_t kOffPlanG = (kOffMisc + 16 + 15) / 16 * 16;           // IdxGroup[256]
+    static constexpr uint32_t kOffPlanT = kOffPlanG + kLocalMaxQ * 24;             // int64[257]
+    static constexpr uint32_t kSmemBytes = kOffPlanT + (kLocalMaxQ + 1) * 8 + 1024;
+    static_assert(kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
+                  "TMEM allocation must be a power of two");
+};
+
+struct Cursor {                       // walks (group, tile) units in order
+    const int64_t* tile_off;
+    int64_t g, t;
+    __device__ void seek(int64_t u, int64_t n_groups) {
+        int64_t lo = 0, hi = n_groups - 1;           // last g with tile_off[g] <= u
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (tile_off[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        g = lo;
+        t = u - tile_off[g];
+    }
+    __device__ void next() {
+        ++t;
+        while (tile_off[g] + t >= tile_off[g + 1]) { ++g; t = 0; }
+    }
+    __device__ bool last_of_group() const { return tile_off[g] + t + 1 >= tile_off[g + 1]; }
+};
+
+// Barrier init, TMEM allocation, the three roles over [u_begin, u_end), and
+// TMEM release.  Called by every thread of the CTA (Cfg::kThreads).
+template <int GQ, int STAGES, class Epi>
+__device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p,
+                    const IdxGroup* __restrict__ groups, const int64_t* __restrict__ tile_off,
+                    int64_t n_groups, int64_t u_begin, int64_t u_end,
+                    const float* __restrict__ w, int32_t kpool, Epi& epi, int32_t* err) {
+    using C = Cfg<GQ, STAGES>;
+    const CUtensorMap& tm_k = *tm_k_p;
+    const CUtensorMap& tm_q = *tm_q_p;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::kStages;
+    uint64_t* b_full = bars + 2 * C::kStages;
+    uint64_t* b_empty = b_full + 1;
+    uint64_t* acc_full = b_full + 2;
+    uint64_t* acc_empty = b_full + 4;
+    uint64_t* drain = b_full + 6;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(b_full, 1);
+        mbar_init(b_empty, 1);
+        for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], C::kEpiWarps); }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_q);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {                                           // ---- TMA producer
+            Cursor c{tile_off, 0, 0};
+            c.seek(u_begin, n_groups);
+            int stage = 0;
+            uint32_t phase = 0, b_empty_par = 0;
+            int64_t b_group = -1;
+            int8_t issued_par[C::kStages];
+            for (int s = 0; s < C::kStages; ++s) issued_par[s] = -1;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok; ++u) {
+                const IdxGroup G = groups[c.g];
+                if (c.g != b_group) {
+                    if (b_group >= 0) {
+                        ok = mbar_wait(b_empty, b_empty_par, kWaitNs);
+                        b_empty_par ^= 1;
+                        if (!ok) break;
+                    }
+                    uint8_t* bsm = smem + C::kOffB;
+                    mbar_arrive_expect_tx(b_full, C::kBBytes);
+                    tma_load_2d(bsm, &tm_q, b_full, 0, G.q0 * kIdxHeads);
+                    tma_load_2d(bsm + C::kBBoxBytes, &tm_q, b_full, 64, G.q0 * kIdxHeads);
+                    b_group = c.g;
+                }
+                ok = mbar_wait(&empty[stage], phase ^ 1, kWaitNs);
+                if (!ok) break;
+                uint8_t* asm_ = smem + C::kOffA + stage * kABytes;
+                const int32_t y = (int32_t)(G.key0 + c.t * kTileKeys);
+                mbar_arrive_expect_tx(&full[stage], kABytes);
+                tma_load_2d(asm_, &tm_k, &full[stage], 0, y);
+                tma_load_2d(asm_ + kABoxBytes, &tm_k, &full[stage], 64, y);
+                issued_par[stage] = (int8_t)phase;
+                if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+                if (u + 1 < u_end) c.next();
+            }
+            if (!ok) {
+                record_error(err, kDevTimeout, blockIdx.x, /*where=*/5);
+                *abort_flag = 1;
+                // let this CTA's copies in flight land before the CTA retires
+                for (int s = 0; s < C::kStages; ++s)
+                    if (issued_par[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_par[s], 50000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {                                           // ---- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(kTileKeys, C::N);
+            Cursor c{tile_off, 0, 0};
+            c.seek(u_begin, n_groups);
+            int stage = 0, ab = 0;
+            uint32_t phase = 0, acc_par = 0, b_full_par = 0;
+            int64_t b_group = -1;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok; ++u) {
+                if (*abort_flag) { ok = false; break; }
+                if (c.g != b_group) {
+                    ok = mbar_wait(b_full, b_full_par, kWaitNs);
+                    b_full_par ^= 1;
+                    b_group = c.g;
+                    if (!ok) break;
+                }
+                ok = mbar_wait(&acc_empty[ab], acc_par ^ 1, kWaitNs) &&
+                     mbar_wait(&full[stage], phase, kWaitNs);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(smem + C::kOffA + stage * kABytes);
+                const uint32_t b0 = smem_u32(smem + C::kOffB);
+                const uint32_t d = tmem_base + (uint32_t)(ab * C::N);
+#pragma unroll
+                for (int kk = 0; kk < kIdxDim / 16; ++kk) {
+                    const uint32_t koff = (uint32_t)(kk & 3) * 32u, half = (uint32_t)(kk >> 2);
+                    mma_bf16_ss(d, sdesc_kmajor_sw128(a0 + half * kABoxBytes + koff),
+                                sdesc_kmajor_sw128(b0 + half * C::kBBoxBytes + koff), idesc,
+                                kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&empty[stage]);                 // stage reusable once these finish
+                mma_commit(&acc_full[ab]);                 // accumulator ready for the epilogue
+                if (c.last_of_group()) mma_commit(b_empty);
+                if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+                if (++ab == 2) { ab = 0; acc_par ^= 1; }
+                if (u + 1 < u_end) c.next();
+            }
+            if (!ok) {
+                record_error(err, kDevTimeout, blockIdx.x, /*where=*/6);
+                *abort_flag = 1;
+            }
+            mma_commit(drain);                             // all issued MMAs retired
+            mbar_wait(drain, 0, 50000000ull);
+        }
+    } else if (warp >= 4) {                                        // ---- epilogue
+        const int ew = warp - 4;
+        const int wg = ew >> 2;                                    // epilogue warpgroup
+        const int lane_base = 32 * (warp & 3);                     // this warp's TMEM lanes
+        const int row = lane_base + lane;
+        Cursor c{tile_off, 0, 0};
+        c.seek(u_begin, n_groups);
+        int ab = 0;
+        uint32_t acc_par = 0;
+        epi.begin();
+        for (int64_t u = u_begin; u < u_end; ++u) {
+            const IdxGroup G = groups[c.g];
+            if (*abort_flag || !mbar_wait(&acc_full[ab], acc_par, kWaitNs)) {
+                record_error(err, kDevTimeout, blockIdx.x, /*where=*/7);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const int64_t t_row = c.t * kTileKeys + row;
+            for (int j = wg; j < G.nq; j += C::kEpiGroups) {
+                float v[32];
+                tmem_ld_32cols(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(ab * C::N + 32 * j), v);
+                // the query's head weights: warp-uniform addresses, one broadcast each
+                const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)(G.q0 + j) * kIdxHeads);
+                float s = 0.f;
+#pragma unroll
+                for (int h4 = 0; h4 < kIdxHeads / 4; ++h4) {
+                    const float4 wv = __ldg(w4 + h4);
+                    s = fmaf(wv.x, fmaxf(v[4 * h4 + 0], 0.f), s);
+                    s = fmaf(wv.y, fmaxf(v[4 * h4 + 1], 0.f), s);
+                    s = fmaf(wv.z, fmaxf(v[4 * h4 + 2], 0.f), s);
+                    s = fmaf(wv.w, fmaxf(v[4 * h4 + 3], 0.f), s);
+                }
+                const int64_t nk = (int64_t)(G.L_last - (G.nq - 1 - j)) / kpool;
+                epi.emit(G, j, t_row, t_row < nk, u, row, s);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            if (++ab == 2) { ab = 0; acc_par ^= 1; }
+            if (u + 1 < u_end) c.next();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+}  // namespace idxp
+}  // namespace dsa
