@@ -15,6 +15,12 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+}  // namespace
+
+size_t ws_zero_bytes() { return kWsHeaderBytes + index_select_fused_state_bytes(); }
+
+namespace {
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool trace_on() {
@@ -69,12 +75,16 @@ int64_t default_ld(const Shape& sh, const BatchDev& b) {
 }
 
 struct StepLayout {
-    size_t idx_plan, scores, idx, n_sel, attn, total;
+    size_t sel, idx_plan, scores, idx, n_sel, attn, total;
 };
 
+// Decode-step workspace: header | fused selection state (fixed size, kept zero
+// between launches) | indexer plan | scores | selections | counts | attention.
 StepLayout step_layout(const Shape& sh, const BatchDev& b) {
     StepLayout L{};
     size_t off = kWsHeaderBytes;
+    L.sel = off;
+    off = align_up(off + index_select_fused_state_bytes());
     L.idx_plan = off;
     off = align_up(off + index_scores_scratch_bytes(sh, b));
     L.scores = off;
@@ -184,7 +194,7 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
             case DSA_OP_INDEX_SCORES: n = idx; break;
             case DSA_OP_TOPK_SELECT: n = 1; break;
             case DSA_OP_SPARSE_MLA: n = attn; break;
-            default: n = idx + 1 + attn; break;
+            default: n = (index_select_fused_eligible(sh, bh) ? 1 : idx + 1) + attn; break;
         }
     }
     *info = dsa_plan_info{n, splits, rps, 0};
@@ -280,11 +290,20 @@ dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const
     if (trace_on())
         fprintf(stderr, "[dsa] decode_step n_q=%d max_kv=%lld ld=%lld ws=%zu\n", b.n_q,
                 (long long)b.max_kv_len, (long long)ld, lay.total);
-    cudaError_t e = launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld,
-                                        bytes(ws) + lay.idx_plan, err, st);
-    if (e != cudaSuccess) return cuda_status(e, "decode_step/index_scores");
-    e = launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
-    if (e != cudaSuccess) return cuda_status(e, "decode_step/topk_select");
+    cudaError_t e;
+    if (index_select_fused_eligible(sh, b)) {
+        e = launch_index_select_fused(sh, b, q_idx, w, k_idx, scores, ld, idx, n_sel,
+                                      bytes(ws) + lay.sel,
+                                      reinterpret_cast<uint32_t*>(bytes(ws) + kWsGridBarOffset),
+                                      err, st);
+        if (e != cudaSuccess) return cuda_status(e, "decode_step/index_select_fused");
+    } else {
+        e = launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld,
+                                bytes(ws) + lay.idx_plan, err, st);
+        if (e != cudaSuccess) return cuda_status(e, "decode_step/index_scores");
+        e = launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
+        if (e != cudaSuccess) return cuda_status(e, "decode_step/topk_select");
+    }
     e = launch_sparse_mla(sh, b, q_abs, cache, idx, n_sel, out, lse, bytes(ws) + lay.attn,
                           lay.total - lay.attn, err, st);
     return cuda_status(e, "decode_step/sparse_mla_attn");
@@ -303,7 +322,9 @@ dsa_status dsa_check_device_error(void* ws, size_t ws_bytes, void* stream, int32
     if (trace_on())
         fprintf(stderr, "[dsa] device error %d (detail %d, kernel %d)\n", words[0], words[1],
                 words[2]);
-    e = cudaMemset(ws, 0, sizeof(words));
+    // an interrupted launch may leave the selection state and the grid
+    // barrier dirty: start them from zero again
+    e = cudaMemset(ws, 0, ws_bytes < ws_zero_bytes() ? ws_bytes : ws_zero_bytes());
     if (e != cudaSuccess) return cuda_status(e, "check_device_error/clear");
     return words[0] == kDevTimeout ? DSA_ERR_TIMEOUT : DSA_ERR_DEVICE;
 }
@@ -312,7 +333,8 @@ dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (ws == nullptr || ws_bytes < kWsHeaderBytes ||
         (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
         return DSA_ERR_WORKSPACE;
-    return cuda_status(cudaMemsetAsync(ws, 0, kWsHeaderBytes, static_cast<cudaStream_t>(stream)),
+    const size_t n = ws_bytes < ws_zero_bytes() ? ws_bytes : ws_zero_bytes();
+    return cuda_status(cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)),
                        "workspace_init");
 }
 

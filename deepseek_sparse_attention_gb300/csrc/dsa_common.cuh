@@ -16,6 +16,8 @@ namespace dsa {
 // Every workspace starts with this many bytes of header; word 0 is the device
 // error code, word 1 the first error's detail, word 2 the kernel that set it.
 constexpr size_t kWsHeaderBytes = 256;
+// Byte offset in the header of the fused kernel's grid barrier (two words).
+constexpr size_t kWsGridBarOffset = 64;
 
 enum DeviceError : int32_t {
     kDevOk = 0,

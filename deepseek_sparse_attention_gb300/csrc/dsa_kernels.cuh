@@ -29,6 +29,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Bytes at the start of a workspace that must be zero before a decode step:
+// the header and the fused selection state (dsa_api.cu).
+size_t ws_zero_bytes();
+
 // Validated layer geometry (see dsa_shape in dsa.h).
 struct Shape {
     int32_t idx_heads, idx_dim, heads, kv_lora, rope, top_k, kpool;
@@ -63,6 +67,21 @@ cudaError_t launch_topk_select_cluster(const Shape& sh, const BatchDev& b, const
 cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* scores,
                                int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
                                cudaStream_t st);
+
+// Steps 1 and 2 fused for decode batches (index_select_fused.cu): one
+// cooperative launch of the tensor-core indexer that also selects, for at most
+// kFusedMaxQ queries each scored as its own group.  `state` holds
+// index_select_fused_state_bytes() bytes that must be zero before the first
+// launch (each launch leaves them zero); `gbar` two zeroed words for the grid
+// barrier.  DSA_FUSED_SELECT=0 in the environment turns the path off.
+constexpr int kFusedMaxQ = 64;
+constexpr int kFusedMaxGrid = 256;
+bool index_select_fused_eligible(const Shape& sh, const BatchDev& b);
+size_t index_select_fused_state_bytes();
+cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const void* q_idx,
+                                      const float* w, const void* k_idx, float* scores,
+                                      int64_t ld, int32_t* idx, int32_t* n_sel, void* state,
+                                      uint32_t* gbar, int32_t* err, cudaStream_t st);
 
 // Step 3.  bf16 rows run on the tensor cores (sparse_mla_tc.cu), float32 rows
 // on CUDA cores (sparse_mla.cu).  Row splits per query and the scratch for the

@@ -17,12 +17,13 @@
 // device current) and caches it; that first call should therefore come before
 // any stream capture.  All calls share the array and it keeps the previous
 // call's contents: each call clears the part that must start at zero (the error
-// word) on its stream, and two calls whose work overlaps on the GPU -- on
-// different streams, or different host threads -- race on the array.
+// word, the grid barrier and the fused selection histograms) on its stream,
+// and two calls whose work overlaps on the GPU -- on different streams, or
+// different host threads -- race on the array.
 #include <mutex>
 
 #include "dsa.h"
-#include "dsa_common.cuh"
+#include "dsa_kernels.cuh"
 
 namespace {
 
@@ -68,7 +69,7 @@ extern "C" dsa_status dsa_decode_step_noalloc(const dsa_shape* shape, const dsa_
     void* scratch = nullptr;
     if ((s = scratch_for_current_device(&scratch)) != DSA_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(scratch, 0, dsa::kWsHeaderBytes, st) != cudaSuccess) return DSA_ERR_CUDA;
+    if (cudaMemsetAsync(scratch, 0, dsa::ws_zero_bytes(), st) != cudaSuccess) return DSA_ERR_CUDA;
     return dsa_decode_step(shape, batch, q_idx, w, k_idx, q_abs, cache, out, lse, idx_out,
                            n_sel_out, scratch, (size_t)DSA_NOALLOC_SCRATCH_BYTES, stream);
 }

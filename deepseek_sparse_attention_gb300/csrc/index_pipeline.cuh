@@ -29,6 +29,13 @@ constexpr uint32_t kABoxBytes = kTileKeys * kRowHalfBytes;    // 16 KB
 constexpr uint32_t kABytes = 2 * kABoxBytes;                  // 32 KB per key tile
 constexpr uint64_t kWaitNs = 2000000000ull;         // bounded waits: 2 s
 
+// Host side (index_scores_tc.cu): a tensor map over a row-major [rows, 128]
+// bf16 matrix read in boxes of box_rows x 64 columns with the 128-byte swizzle
+// (false when the driver entry point is missing or the encoder refuses), and
+// the device's SM count.
+bool make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);
+int sm_count();
+
 struct IdxGroup {          // consecutive queries of one sequence scored together
     int64_t key0;          // first indexer key of the sequence
     int32_t q0;            // first query of the group
@@ -80,6 +87,36 @@ struct Cursor {                       // walks (group, tile) units in order
     }
     __device__ bool last_of_group() const { return tile_off[g] + t + 1 >= tile_off[g + 1]; }
 };
+
+// One group per query (decode batches of at most Cfg::kLocalMaxQ queries):
+// every CTA derives the (group, tile) schedule itself into shared memory --
+// groups at kOffPlanG, the exclusive prefix of tiles per group at kOffPlanT --
+// and returns the group count.  A query whose offsets fail the batch checks
+// gets an empty group (nq = 0, no tiles).  Called by every thread.
+template <class C>
+__device__ int64_t local_decode_plan(uint8_t* smem, const BatchDev& bq, int32_t kpool,
+                                     int32_t* err, int32_t where) {
+    IdxGroup* gs = reinterpret_cast<IdxGroup*>(smem + C::kOffPlanG);
+    int64_t* ts = reinterpret_cast<int64_t*>(smem + C::kOffPlanT);
+    if (threadIdx.x < bq.n_q) {
+        QueryInfo qi;
+        IdxGroup G{0, (int32_t)threadIdx.x, 0, 0, 0};
+        if (query_info(bq, threadIdx.x, qi, err, where)) {
+            G.key0 = qi.key0;
+            G.nq = 1;
+            G.L_last = (int32_t)qi.L;
+        }
+        gs[threadIdx.x] = G;
+        ts[threadIdx.x + 1] = G.nq ? (G.L_last / kpool + kTileKeys - 1) / kTileKeys : 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ts[0] = 0;
+        for (int i = 1; i <= bq.n_q; ++i) ts[i] += ts[i - 1];
+    }
+    __syncthreads();
+    return bq.n_q;
+}
 
 // Barrier init, TMEM allocation, the three roles over [u_begin, u_end), and
 // TMEM release.  Called by every thread of the CTA (Cfg::kThreads).

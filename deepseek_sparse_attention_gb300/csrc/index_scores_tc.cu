@@ -23,6 +23,51 @@
 #include "index_pipeline.cuh"
 
 namespace dsa {
+namespace idxp {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiledFn) nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Row-major [rows, 128] bf16 matrix read in boxes of box_rows x 64 columns with
+// the 128-byte swizzle.
+bool make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr || rows == 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kIdxDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kIdxDim * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
+}  // namespace idxp
+
 namespace {
 
 using namespace sm100;
@@ -128,29 +173,9 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     int64_t n_groups;
     if (!local_plan) pdl_wait();                      // the plan kernel's arrays
     if (local_plan) {
-        // one group per query (decode); every CTA derives the schedule itself
-        IdxGroup* gs = reinterpret_cast<IdxGroup*>(smem + C::kOffPlanG);
-        int64_t* ts = reinterpret_cast<int64_t*>(smem + C::kOffPlanT);
-        if (threadIdx.x < bq.n_q) {
-            QueryInfo qi;
-            IdxGroup G{0, (int32_t)threadIdx.x, 0, 0, 0};
-            if (query_info(bq, threadIdx.x, qi, err, /*where=*/4)) {
-                G.key0 = qi.key0;
-                G.nq = 1;
-                G.L_last = (int32_t)qi.L;
-            }
-            gs[threadIdx.x] = G;
-            ts[threadIdx.x + 1] = G.nq ? (G.L_last / kpool + kTileKeys - 1) / kTileKeys : 0;
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            ts[0] = 0;
-            for (int i = 1; i <= bq.n_q; ++i) ts[i] += ts[i - 1];
-        }
-        __syncthreads();
-        groups = gs;
-        tile_off = ts;
-        n_groups = bq.n_q;
+        n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/4);
+        groups = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
+        tile_off = reinterpret_cast<const int64_t*>(smem + C::kOffPlanT);
     } else {
         n_groups = seq_goff[n_seq];
     }
@@ -165,47 +190,6 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 }
 
 // ---------------------------------------------------------------- host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return (EncodeTiledFn) nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-// Row-major [rows, 128] bf16 matrix read in boxes of box_rows x 64 columns with
-// the 128-byte swizzle.
-bool make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (enc == nullptr || rows == 0) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kIdxDim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kIdxDim * 2};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        return 148;
-    return n;
-}
 
 struct PlanArrays {
     int64_t* seq_goff;

@@ -140,10 +140,14 @@ typedef struct {
 dsa_status dsa_plan(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
                     dsa_plan_info *info);
 
-/* Zeroes the workspace header (its device error word) on `stream`.  Call once
- * on a freshly allocated workspace that was not allocated zero-filled; after
- * that dsa_check_device_error() keeps the word clear.  `ws` must be 256-byte
- * aligned and at least 256 bytes. */
+/* Zeroes the start of the workspace on `stream`: the 256-byte header (device
+ * error word, grid barrier) and the decode step's selection state that
+ * follows it (DSA_WS_ZERO_BYTES in all, or the whole of a smaller workspace).
+ * Call once on a freshly allocated workspace that was not allocated
+ * zero-filled; after that every completed call leaves this region as it must
+ * be, and dsa_check_device_error() re-zeroes it when a kernel reported an
+ * error.  `ws` must be 256-byte aligned and at least 256 bytes. */
+#define DSA_WS_ZERO_BYTES (256u + 64u * 5120u * 4u + 64u * 256u * 8u)
 dsa_status dsa_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Step 1: lightning-indexer scores ("GLM 5.2 in one C file", "The Lightning
@@ -195,7 +199,16 @@ dsa_status dsa_sparse_mla_attn(const dsa_shape *shape, const dsa_batch *batch, c
 /* The whole hot path for every query of the batch: steps 1-3 in one call.
  * Scores and selections live in the workspace unless idx_out / n_sel_out are
  * given (then the selection is also written there, laid out as for
- * dsa_topk_select).  Works for decode and for chunks of prefill alike. */
+ * dsa_topk_select).  Works for decode and for chunks of prefill alike.
+ * Decode batches of at most 64 queries with bf16 inputs and 32 indexer heads
+ * run steps 1 and 2 as one cooperative launch whose CTAs wait on one another
+ * through the workspace (a grid barrier and per-query histograms that each
+ * launch leaves zero): the workspace must have been zeroed once
+ * (dsa_workspace_init, or allocated zero-filled), and two calls sharing one
+ * workspace must not run concurrently.  The launch needs every CTA resident at
+ * once; DSA_ERR_CUDA is returned if the device cannot give it that.
+ * DSA_FUSED_SELECT=0 in the environment selects the two-launch path instead
+ * (the results are the same). */
 dsa_status dsa_decode_step(const dsa_shape *shape, const dsa_batch *batch, const void *q_idx,
                            const float *w, const void *k_idx, const void *q_abs,
                            const void *cache, float *out, float *lse, int32_t *idx_out,
@@ -213,11 +226,11 @@ dsa_status dsa_decode_step(const dsa_shape *shape, const dsa_batch *batch, const
  *   Arguments and results are those of dsa_decode_step without ws/ws_bytes.
  *   Returns DSA_ERR_UNSUPPORTED when the step needs more scratch than the
  *   array holds (dsa_workspace_size(DSA_OP_DECODE_STEP) > the limit; a batch-1
- *   decode at 131072 tokens needs under 5 MiB).
+ *   decode at 131072 tokens needs under 6 MiB).
  *   The first call on a device looks up the array's device address (with that
  *   device current) and caches it; make that first call before any stream
  *   capture.  All calls share the array and it keeps the previous call's
- *   contents; each call zeroes its error word on `stream` first.  Calls whose
+ *   contents; each call zeroes its first DSA_WS_ZERO_BYTES on `stream` first.  Calls whose
  *   work overlaps on the GPU (other streams, other threads) race on the array:
  *   serialise them.  Device-side checks record into the array's error word,
  *   which is not reported back; use dsa_decode_step to read it. */
