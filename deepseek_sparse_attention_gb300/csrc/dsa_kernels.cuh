@@ -74,7 +74,7 @@ cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* 
 // index_select_fused_state_bytes() bytes that must be zero before the first
 // launch (each launch leaves them zero); `gbar` two zeroed words for the grid
 // barrier.  DSA_FUSED_SELECT=0 in the environment turns the path off.
-constexpr int kFusedMaxQ = 64;
+constexpr int kFusedMaxQ = 16;
 constexpr int kFusedMaxGrid = 256;
 bool index_select_fused_eligible(const Shape& sh, const BatchDev& b);
 size_t index_select_fused_state_bytes();

@@ -13,23 +13,30 @@
 // would leave all but one SM idle in a per-query selection kernel, and a
 // separate launch costs its own ramp-up.  Here the persistent indexer grid (one
 // CTA per SM, a contiguous range of (query, key tile) units each) keeps its
-// scores and selects in place, all CTAs of a query cooperating through global
-// histograms and grid barriers:
-//   score   the tensor-core indexer pipeline (index_pipeline.cuh) writes the
-//           CTA's scores; they come back (from L2) as order-preserving keys
-//           into the shared memory the pipeline's ring used;
-//   level 1 histogram of key bits 31..21 per query (shared, then added into
-//           the query's global histogram); barrier; every CTA of the query
-//           finds the bin b1 that holds the k-th largest key;
-//   level 2 the same over bits 20..10 of the keys in b1; barrier;
-//   level 3 bits 9..0 of the keys in (b1, b2); barrier: the k-th largest key T
-//           is known exactly, and how many keys above it the query has;
-//   counts  each CTA publishes how many of its keys are > T and == T; barrier;
-//   emit    a CTA's output offset is the count of selected keys of the CTAs
-//           before it (keys equal to T go to the lowest indices first); a block
-//           scan over its keys writes its selections in ascending order.
-// The global histograms are cleared by the launch that used them, as soon as
-// every CTA has read them, so they are zero again for the next launch.
+// scores and selects in place.  Scores map to order-preserving uint32 keys; the
+// selection is every key above the query's k-th largest key T plus the
+// lowest-index keys equal to T.  All CTAs holding keys of a query cooperate
+// through global memory and grid barriers:
+//   score     the tensor-core indexer pipeline (index_pipeline.cuh) writes the
+//             CTA's scores; they come back (from L2) as keys into the shared
+//             memory the pipeline's ring used;
+//   level 1   histogram of key bits 31..19 (8192 bins) per query, added into
+//             the query's global histogram;                         barrier 1
+//   bin       every CTA finds the bin b1 that holds the k-th largest key; it
+//             publishes how many of its keys lie above b1 and appends its keys
+//             in b1 -- the candidates, a few hundred per query -- to the
+//             query's global candidate list;                        barrier 2
+//   resolve   every CTA reads the whole candidate list and resolves T and the
+//             last index taken at T exactly, by a radix select in shared memory;
+//   emit      a CTA's output offset is the count of selected keys of the CTAs
+//             before it (keys above b1 from the published counts, candidates
+//             from the list); a block scan writes its selections in order.
+// When a query's candidates overflow the list (heavy ties), the grid instead
+// resolves that query by two more histogram levels (bits 18..9 and 8..0) and a
+// round of per-CTA counts above and at T, three more barriers.  Global
+// histograms are cleared by the launch that used them once every CTA has read
+// them; candidate counters are cleared before the barrier that precedes their
+// first use.  So the state is zero again for the next launch.
 #include "index_pipeline.cuh"
 
 namespace dsa {
@@ -42,19 +49,27 @@ using namespace idxp;
 using C = Cfg<1>;
 constexpr int kThreads = C::kThreads;                 // 256
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins1 = 2048;                          // key bits 31..21
-constexpr int kBins2 = 2048;                          // key bits 20..10
-constexpr int kBins3 = 1024;                          // key bits 9..0
-constexpr int kHistWords = kBins1 + kBins2 + kBins3;  // per query
+constexpr int kBits1 = 11, kBits2 = 11, kBits3 = 10;  // 11 + 11 + 10 = 32 key bits
+constexpr int kBins1 = 1 << kBits1;
+constexpr int kBins2 = 1 << kBits2;
+constexpr int kBins3 = 1 << kBits3;
+constexpr int kShift1 = 32 - kBits1;                  // 21
+constexpr int kShift2 = kBits3;                       // 10
+constexpr int kCandCap = 8192;                        // candidates per query
+constexpr int kCandSpec = 3072;                       // read before the count is known
 constexpr int kItems = 8;                             // keys per thread per emission round
 
-// Shared memory after the indexer pipeline: the ring (C::kOffA .. C::kOffB)
-// holds the CTA's keys, a histogram, per-query state and scan scratch.
-constexpr uint32_t kOffHist = C::kOffB - 16384;
-constexpr uint32_t kMaxCtaKeys = kOffHist / 4;
-constexpr uint32_t kMaxCtaTiles = kMaxCtaKeys / kTileKeys;
-constexpr uint32_t kOffSeg = kOffHist + kBins1 * 4;
-struct SegState {          // one query's part of this CTA's unit range
+// Global state per query (32-bit words; the stride keeps every part 16-byte aligned).
+constexpr int kOffH1 = 0;
+constexpr int kOffH2 = kOffH1 + kBins1;
+constexpr int kOffH3 = kOffH2 + kBins2;
+constexpr int kOffCandN = kOffH3 + kBins3;           // candidate count (+3 words pad)
+constexpr int kOffCand = kOffCandN + 4;              // kCandCap x {key, index}
+constexpr int kQueryWords = kOffCand + 2 * kCandCap;
+static_assert(kQueryWords % 4 == 0 && kOffCand % 2 == 0, "alignment of the state");
+static_assert(kCandSpec % 256 == 0 && kCandSpec <= kCandCap, "speculative candidate reads");
+
+struct SegState {          // one query's part of this CTA's unit range (48 bytes)
     int32_t q;
     int32_t n;             // keys (tokens or pools) in the part
     int32_t koff;          // first key's slot in shared memory
@@ -63,56 +78,70 @@ struct SegState {          // one query's part of this CTA's unit range
     int32_t above;         // keys of the query above the resolved prefix
     int32_t need_eq;       // keys equal to T the query keeps
     int32_t eq;            // keys of this part equal to T
+    int32_t c_first;       // first CTA holding keys of the query
+    int32_t pad[3];
 };
+static_assert(sizeof(SegState) == 48, "state layout");
+
+// Shared memory.  Beside the indexer pipeline's layout: a histogram (the
+// epilogue's level-1 counts, later every shared-memory level), per-query state
+// and scan scratch.  After the pipeline its ring (C::kOffA .. C::kOffB) holds
+// the CTA's keys and the staged candidate list.
+constexpr uint32_t kOffHist = (C::kOffPlanT + (C::kLocalMaxQ + 1) * 8 + 15) / 16 * 16;
+constexpr uint32_t kOffSeg = kOffHist + kBins1 * 4;
 constexpr uint32_t kOffRed = kOffSeg + kFusedMaxQ * sizeof(SegState);
-static_assert(kOffRed + 256 <= C::kOffB, "selection state must fit in the ring");
+constexpr uint32_t kSmemBytes = kOffRed + 256 + 1024;           // + alignment slack
+constexpr uint32_t kOffCandS = C::kOffB - (uint32_t)kCandCap * 8;
+constexpr uint32_t kMaxCtaKeys = kOffCandS / 4;
+constexpr uint32_t kMaxCtaTiles = kMaxCtaKeys / kTileKeys;
 static_assert(C::kOffA == 0, "keys start at the ring");
-static_assert(kWsHeaderBytes + (size_t)kFusedMaxQ * kHistWords * 4 +
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kBins2 <= kBins1 && kBins3 <= kBins1, "one shared histogram serves every level");
+static_assert(kWsHeaderBytes + (size_t)kFusedMaxQ * kQueryWords * 4 +
                       (size_t)kFusedMaxQ * kFusedMaxGrid * 8 == DSA_WS_ZERO_BYTES,
               "the zeroed workspace prefix is documented in dsa.h");
+static_assert(kWsGridBarOffset % 8 == 0, "64-bit barrier counter");
+static_assert(kMaxCtaTiles >= 128, "room for the keys of a CTA");
+
+
+// Scratch words in `red`: [0, kWarps) scans, then named results.
+// [32, 32 + kFusedMaxQ) each query's candidate count.
+enum : int { kR0 = 16, kR1 = 17, kR2 = 18, kR3 = 19, kRFlag = 20, kRNseg = 21, kROver = 22,
+             kRHistQ = 23 };
+static_assert(32 + kFusedMaxQ <= 64, "scratch words");
 
 // ------------------------------------------------------------ grid barrier
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Every CTA of the grid arrives; the last one resets the count and advances
-// the generation word that the others wait on (a bounded wait: on timeout the
-// error word is set and false returned).  bar[0] = arrivals, bar[1] = generation.
-__device__ bool grid_barrier(uint32_t* bar, volatile int* flag, int32_t* err, int32_t where) {
+// Every CTA arrives once on a 64-bit counter that only grows; the barrier is
+// complete when the counter reaches the next multiple of the grid size.  One
+// atomic per CTA and acquire loads while waiting (bounded: on timeout the error
+// word is set and false returned).  The counter starts at zero and each launch
+// adds a whole number of grid sizes.
+__device__ bool grid_barrier(unsigned long long* bar, int* red, int32_t* err, int32_t where) {
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        const uint32_t gen = ld_acquire_gpu(bar + 1);
         __threadfence();
-        const uint32_t arrived = atomicAdd(bar, 1u);
-        if (arrived == gridDim.x - 1) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            st_release_gpu(bar + 1, gen + 1);
-        } else {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire_gpu(bar + 1) == gen) {
-                if (globaltimer_ns() - t0 > kWaitNs) {
-                    record_error(err, kDevTimeout, where, 6);
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(32);
+        const unsigned long long arrived = atomicAdd(bar, 1ull);
+        const unsigned long long target = (arrived / gridDim.x + 1) * gridDim.x;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_u64(bar) < target) {
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                record_error(err, kDevTimeout, where, 6);
+                ok = 0;
+                break;
             }
         }
-        __threadfence();
-        *flag = ok;
+        *reinterpret_cast<volatile int*>(red + kRFlag) = ok;
     }
     __syncthreads();
-    return *flag != 0;
+    return *reinterpret_cast<volatile int*>(red + kRFlag) != 0;
 }
 
 // ------------------------------------------------------------ block helpers
@@ -144,24 +173,37 @@ __device__ int block_excl_scan(int v, int* total, int* red) {
     return excl;
 }
 
-// In a global histogram of nb bins (nb / kThreads consecutive bins per thread),
-// the bin b holding the need-th largest key counted from the top, and the
-// count of keys in bins above b.  Result in red[16], red[17].
-template <int NB>
-__device__ void find_bin(const uint32_t* __restrict__ gh, int need, int* red) {
+__device__ __forceinline__ int block_sum(int v, int* red) {
+    int tot;
+    block_excl_scan(v, &tot, red);
+    return tot;
+}
+
+// In a histogram of NB bins (NB / kThreads consecutive bins per thread; global
+// memory read through L2, or shared memory), the bin b holding the need-th
+// largest key counted from the top, and the count of keys in bins above b:
+// red[kR0] = b, red[kR1] = count.  (0, 0) if the histogram holds fewer keys.
+template <int NB, bool kGlobal>
+__device__ void find_bin(const uint32_t* hist, int need, int* red) {
     constexpr int kPer = NB / kThreads;
-    static_assert(kPer == 4 || kPer == 8, "4 or 8 bins per thread");
+    static_assert(kPer % 2 == 0 && kPer >= 2, "bins per thread");
     uint32_t c[kPer];
-    const uint4* src = reinterpret_cast<const uint4*>(gh + threadIdx.x * kPer);
+    if (kGlobal && kPer % 4 == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(hist + threadIdx.x * kPer);
 #pragma unroll
-    for (int i = 0; i < kPer / 4; ++i) {
-        const uint4 v = __ldcg(src + i);
-        c[4 * i + 0] = v.x; c[4 * i + 1] = v.y; c[4 * i + 2] = v.z; c[4 * i + 3] = v.w;
+        for (int i = 0; i < kPer / 4; ++i) {
+            const uint4 v = __ldcg(src + i);
+            c[4 * i + 0] = v.x; c[4 * i + 1] = v.y; c[4 * i + 2] = v.z; c[4 * i + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            c[i] = kGlobal ? __ldcg(hist + threadIdx.x * kPer + i) : hist[threadIdx.x * kPer + i];
     }
     int local = 0;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) local += (int)c[i];
-    if (threadIdx.x == 0) { red[16] = 0; red[17] = 0; }
+    if (threadIdx.x == 0) { red[kR0] = 0; red[kR1] = 0; }
     int total;
     const int excl = block_excl_scan(local, &total, red);
     int above = total - excl - local;                 // keys in the bins of later threads
@@ -169,8 +211,8 @@ __device__ void find_bin(const uint32_t* __restrict__ gh, int need, int* red) {
 #pragma unroll
         for (int i = kPer - 1; i >= 0; --i) {
             if (above + (int)c[i] >= need) {
-                red[16] = threadIdx.x * kPer + i;
-                red[17] = above;
+                red[kR0] = threadIdx.x * kPer + i;
+                red[kR1] = above;
                 break;
             }
             above += (int)c[i];
@@ -179,7 +221,8 @@ __device__ void find_bin(const uint32_t* __restrict__ gh, int need, int* red) {
     __syncthreads();
 }
 
-// Adds the shared histogram into the global one and clears it.
+// Adds the first NB bins of the shared histogram into the global one and
+// clears them.
 template <int NB>
 __device__ void flush_hist(uint32_t* hist, uint32_t* __restrict__ gh) {
     __syncthreads();
@@ -193,13 +236,11 @@ __device__ void flush_hist(uint32_t* hist, uint32_t* __restrict__ gh) {
     __syncthreads();
 }
 
-// Zeroes words [off, off + len) of every query's global histogram, spread
-// over the grid.
-__device__ void clear_level(uint32_t* __restrict__ gh, int n_q, int off, int len) {
-    const int64_t n = (int64_t)n_q * len;
-    for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < n;
-         e += (int64_t)gridDim.x * kThreads)
-        gh[(e / len) * kHistWords + off + (e % len)] = 0;
+// Zeroes words [off, off + len) of every query's global state, spread over the grid.
+__device__ void clear_level(uint32_t* __restrict__ gs, int n_q, int off, int len) {
+    const int n = n_q * len;                            // at most 16 x 2048
+    for (int e = blockIdx.x * kThreads + threadIdx.x; e < n; e += gridDim.x * kThreads)
+        gs[(size_t)(e / len) * kQueryWords + off + (e % len)] = 0;
 }
 
 __device__ __forceinline__ void put(int32_t* out, int64_t pos, int64_t t, int kpool) {
@@ -210,26 +251,194 @@ __device__ __forceinline__ void put(int32_t* out, int64_t pos, int64_t t, int kp
     }
 }
 
-// The epilogue policy: scores to the workspace row of the query.
-struct ScoreStore {
-    float* scores;
+// Loads, by warp 0, the published counts of the CTAs c_first .. this one - 1
+// (every CTA holding keys of the query before this one; a CTA without units
+// publishes zeros): up to 8 per lane, all issued at once.  sum_counts()
+// reduces them later.
+constexpr int kCntPerLane = kFusedMaxGrid / 32;
+struct CountLoads {
+    int2 v[kCntPerLane];
+};
+__device__ __forceinline__ void load_counts(const int2* __restrict__ gcnt_q, int c_first,
+                                            CountLoads& cl) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 0; k < kCntPerLane; ++k) {
+        const int c = c_first + lane + 32 * k;
+        cl.v[k] = c < (int)blockIdx.x ? __ldcg(gcnt_q + c) : make_int2(0, 0);
+    }
+}
+// Warp 0: sums of .x and .y into red[kR2], red[kR3].
+__device__ __forceinline__ void sum_counts(const CountLoads& cl, int* red) {
+    int a = 0, b = 0;
+#pragma unroll
+    for (int k = 0; k < kCntPerLane; ++k) { a += cl.v[k].x; b += cl.v[k].y; }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, off);
+        b += __shfl_xor_sync(0xffffffffu, b, off);
+    }
+    if ((threadIdx.x & 31) == 0) { red[kR2] = a; red[kR3] = b; }
+}
+
+// Writes this CTA's selections of one query in ascending order from position
+// `base`: keys above T, and keys equal to T that are taken -- by index (at most
+// t_last) or, when `ranked`, the first `take` of them in this part.
+__device__ void emit_part(const SegState& S, const uint32_t* keys, uint32_t T, int base,
+                          int32_t t_last, bool ranked, int take, int keep, int kpool,
+                          int32_t* out, int* red) {
+    const int tid = threadIdx.x;
+    int sel_carry = 0, eq_carry = 0;
+    for (int c0 = 0; c0 < S.n; c0 += kThreads * kItems) {
+        const int j0 = c0 + tid * kItems;
+        uint32_t k[kItems];
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) k[r] = j0 + r < S.n ? keys[S.koff + j0 + r] : 0u;
+        int eq_rank = 0;
+        if (ranked) {
+            int ne = 0;
+#pragma unroll
+            for (int r = 0; r < kItems; ++r) ne += (j0 + r < S.n) && k[r] == T;
+            int tot;
+            eq_rank = eq_carry + block_excl_scan(ne, &tot, red);
+            eq_carry += tot;
+        }
+        uint32_t selmask = 0;
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) {
+            if (j0 + r >= S.n) continue;
+            bool sel = k[r] > T;
+            if (k[r] == T) {
+                sel = ranked ? eq_rank < take : S.t_lo + j0 + r <= t_last;
+                ++eq_rank;
+            }
+            selmask |= (uint32_t)sel << r;
+        }
+        int tot;
+        int pos = base + sel_carry + block_excl_scan(__popc(selmask), &tot, red);
+        sel_carry += tot;
+#pragma unroll
+        for (int r = 0; r < kItems; ++r) {
+            // positions stay below keep when the counts are consistent; the
+            // check keeps a corrupted state from writing past the row
+            if ((selmask & (1u << r)) && (unsigned)pos < (unsigned)keep)
+                put(out, pos, (int64_t)S.t_lo + j0 + r, kpool);
+            pos += (selmask >> r) & 1u;
+        }
+    }
+}
+
+// Resolves one query from its candidate list (all keys in bin b1, staged in
+// shared memory as {key, index}): T, the last index taken at T, and this CTA's
+// output offset; then emits.  `need` = keep - (keys above b1); n_cand <= kCandCap.
+// The first `staged` entries of the list and (warp 0) the counts `cl` of the
+// earlier CTAs may already be loaded.
+__device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
+                                        const int2* __restrict__ gcnt_q, int n_cand, int staged,
+                                        CountLoads& cl, bool counts_loaded, int need,
+                                        uint32_t b1, const uint32_t* keys, uint32_t* hist, int2* cand,
+                                        int keep, int kpool, int32_t* out, int* red) {
+    const int tid = threadIdx.x;
+    if (tid < 32 && !counts_loaded) load_counts(gcnt_q, S.c_first, cl);
+    const int2* src = reinterpret_cast<const int2*>(gsq + kOffCand);
+    for (int i0 = staged; i0 < n_cand; i0 += 4 * kThreads) {   // four loads in flight
+        int2 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int i = i0 + tid + k * kThreads;
+            v[k] = i < n_cand ? __ldcg(src + i) : make_int2(0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (i0 + tid + k * kThreads < n_cand) cand[i0 + tid + k * kThreads] = v[k];
+    }
+    __syncthreads();
+    // bits 20..10
+    for (int i = tid; i < n_cand; i += kThreads)
+        atomicAdd(&hist[((uint32_t)cand[i].x >> kShift2) & (kBins2 - 1)], 1u);
+    __syncthreads();
+    find_bin<kBins2, false>(hist, need, red);
+    const uint32_t b2 = (uint32_t)red[kR0];
+    const int above2 = red[kR1];
+    for (int i = tid; i < kBins2; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    // bits 9..0 of the candidates in (b1, b2)
+    const uint32_t pre = (b1 << kBits2) | b2;
+    for (int i = tid; i < n_cand; i += kThreads) {
+        const uint32_t k = (uint32_t)cand[i].x;
+        if ((k >> kShift2) == pre) atomicAdd(&hist[k & (kBins3 - 1)], 1u);
+    }
+    __syncthreads();
+    find_bin<kBins3, false>(hist, need - above2, red);
+    const uint32_t T = (pre << kBits3) | (uint32_t)red[kR0];
+    const int need_eq = need - above2 - red[kR1];      // candidates equal to T that are kept
+    for (int i = tid; i < kBins3; i += kThreads) hist[i] = 0;
+    // the last index taken at T: all of them when need_eq covers them, else
+    // the need_eq-th smallest index among them (indices are distinct)
+    int n_eq = 0;
+    for (int i = tid; i < n_cand; i += kThreads) n_eq += (uint32_t)cand[i].x == T;
+    n_eq = block_sum(n_eq, red);
+    int32_t t_last = 0x7fffffff;
+    if (need_eq < n_eq) {
+        if (tid == 0) red[kR0] = -1;
+        __syncthreads();
+        for (int i = tid; i < n_cand; i += kThreads) {
+            if ((uint32_t)cand[i].x != T) continue;
+            const int32_t ti = cand[i].y;
+            int rank = 0;
+            for (int j = 0; j < n_cand; ++j) rank += (uint32_t)cand[j].x == T && cand[j].y < ti;
+            if (rank == need_eq - 1) red[kR0] = ti;
+        }
+        __syncthreads();
+        t_last = red[kR0];
+    }
+    // offset: kept keys above b1 in earlier CTAs, plus kept candidates below
+    // this part's first index
+    int before = 0;
+    for (int i = tid; i < n_cand; i += kThreads) {
+        const uint32_t k = (uint32_t)cand[i].x;
+        const int32_t ti = cand[i].y;
+        before += ti < S.t_lo && (k > T || (k == T && ti <= t_last));
+    }
+    before = block_sum(before, red);
+    if (tid < 32) sum_counts(cl, red);
+    __syncthreads();
+    const int base = red[kR2] + before;
+    emit_part(S, keys, T, base, t_last, false, 0, keep, kpool, out, red);
+}
+
+// The epilogue policy: each score as its order-preserving key into the
+// workspace row of its query, and into the shared level-1 histogram when the
+// key belongs to `hist_q` (the first query this CTA selects for).
+struct KeyStore {
+    uint32_t* keys;
     int64_t ld;
+    uint32_t* hist;
+    int32_t hist_q;
     __device__ void begin() {}
     __device__ void emit(const IdxGroup& G, int j, int64_t t_row, bool valid, int64_t, int, float s) {
-        if (valid) scores[(int64_t)(G.q0 + j) * ld + t_row] = s;
+        if (!valid) return;
+        const uint32_t k = order_key(s);
+        keys[(int64_t)(G.q0 + j) * ld + t_row] = k;
+        if (G.q0 + j == hist_q) atomicAdd(&hist[k >> kShift1], 1u);
     }
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
 index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    const float* __restrict__ w, BatchDev bq, int32_t top_k, int32_t kpool,
-                   float* __restrict__ scores, int64_t ld, int32_t* __restrict__ idx,
-                   int32_t* __restrict__ n_sel, int64_t width, uint32_t* __restrict__ ghist,
-                   int2* __restrict__ gcnt, uint32_t* gbar, int32_t* err) {
+                   uint32_t* __restrict__ gkeys, int64_t ld, int32_t* __restrict__ idx,
+                   int32_t* __restrict__ n_sel, int64_t width, uint32_t* __restrict__ gstate,
+                   int2* __restrict__ gcnt, unsigned long long* gbar, int32_t* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int cta = blockIdx.x, grid = gridDim.x;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
+    int2* cand = reinterpret_cast<int2*>(smem + kOffCandS);
+    SegState* seg = reinterpret_cast<SegState*>(smem + kOffSeg);
+    int* red = reinterpret_cast<int*>(smem + kOffRed);
 
     const int64_t n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/6);
     const IdxGroup* gs = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
@@ -238,26 +447,12 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int64_t u_begin = (int64_t)cta * U / grid, u_end = (int64_t)(cta + 1) * U / grid;
     const int keep = top_k / kpool;
     const bool fits = u_end - u_begin <= (int64_t)kMaxCtaTiles;
-    if (!fits && tid == 0) record_error(err, kDevBadBatch, cta, 6);
 
-    // ---- scores of this CTA's units
-    if (u_begin < u_end && fits) {
-        ScoreStore epi{scores, ld};
-        run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_end, w, kpool, epi, err);
-    }
-    fence_proxy_async_smem();                 // the ring is reused by generic accesses
-
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
-    SegState* seg = reinterpret_cast<SegState*>(smem + kOffSeg);
-    int* red = reinterpret_cast<int*>(smem + kOffRed);
-    volatile int* flag = red + 20;
-    volatile int* s_nseg = red + 21;
-
-    // ---- this CTA's part of each query (sparse queries only) and whole rows
+    // ---- this CTA's part of each sparse query, whole rows, candidate counters
     for (int i = tid; i < kBins1; i += kThreads) hist[i] = 0;
     if (tid == 0) {
         int ns = 0;
+        if (!fits) record_error(err, kDevBadBatch, cta, 6);
         if (u_begin < u_end && fits) {
             int64_t g = 0;
             while (ts[g + 1] <= u_begin) ++g;
@@ -275,13 +470,19 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 S.n = (int32_t)(t_hi - t_lo);
                 S.koff = (int32_t)((ul - u_begin) * kTileKeys);
                 S.t_lo = (int32_t)t_lo;
+                // the CTA whose units contain the query's first unit ts[g]:
+                // the smallest c with floor((c + 1) U / grid) > ts[g]
+                S.c_first = (int32_t)(((ts[g] + 1) * grid + U - 1) / U - 1);
                 seg[ns++] = S;
             }
         }
-        *s_nseg = ns;
+        red[kRNseg] = ns;
+        red[kRHistQ] = ns > 0 ? seg[0].q : -1;
     }
     // rows one CTA writes whole: failed and dense queries; the tail and the
-    // padding of sparse rows (the selected body is written by the emission)
+    // padding of sparse rows (the selected body is written by the emission).
+    // The same CTA zeroes the query's candidate counter, first used after
+    // barrier 1.
     for (int q = cta; q < bq.n_q; q += grid) {
         const IdxGroup G = gs[q];
         int32_t* out = idx + (int64_t)q * width;
@@ -301,156 +502,201 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         for (int64_t i = from + tid; i < width; i += kThreads)
             out[i] = i < to_sel ? (int32_t)(i + L_sel) : -1;
-        if (tid == 0) n_sel[q] = (int32_t)n_tot;
+        if (tid == 0) {
+            n_sel[q] = (int32_t)n_tot;
+            gstate[(int64_t)q * kQueryWords + kOffCandN] = 0;
+        }
     }
     __syncthreads();
-    const int nseg = *s_nseg;
+    const int nseg = red[kRNseg];
 
-    // ---- level 1: keys into shared memory, histogram of bits 31..21
+    // ---- scores of this CTA's units (keys to global, level-1 counts of hist_q)
+    if (u_begin < u_end && fits) {
+        KeyStore epi{gkeys, ld, hist, red[kRHistQ]};
+        run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_end, w, kpool, epi, err);
+    }
+    fence_proxy_async_smem();                 // the ring is reused by generic accesses
+
+    // ---- keys back into shared memory (asynchronous copies, 16 bytes each:
+    // part starts are tile-aligned and rows padded to 4 keys), level-1 counts
     for (int s = 0; s < nseg; ++s) {
         const SegState S = seg[s];
-        const float* src = scores + (int64_t)S.q * ld + S.t_lo;
-        for (int i = tid; i < S.n; i += kThreads) {
-            const uint32_t k = order_key(__ldcg(src + i));
-            keys[S.koff + i] = k;
-            atomicAdd(&hist[k >> 21], 1u);
-        }
-        flush_hist<kBins1>(hist, ghist + (int64_t)S.q * kHistWords);
+        const uint32_t* src = gkeys + (int64_t)S.q * ld + S.t_lo;
+        const uint32_t dst = smem_u32(keys + S.koff);
+        for (int c = tid; c < (S.n + 3) / 4; c += kThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16 * c),
+                         "l"(src + 4 * c)
+                         : "memory");
     }
-    if (!grid_barrier(gbar, flag, err, 61)) return;
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (nseg > 0) flush_hist<kBins1>(hist, gstate + (int64_t)seg[0].q * kQueryWords + kOffH1);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    for (int s = 1; s < nseg; ++s) {
+        const SegState S = seg[s];
+        for (int i = tid; i < S.n; i += kThreads) atomicAdd(&hist[keys[S.koff + i] >> kShift1], 1u);
+        flush_hist<kBins1>(hist, gstate + (int64_t)S.q * kQueryWords + kOffH1);
+    }
+    if (!grid_barrier(gbar, red, err, 61)) return;
 
-    // ---- level 2: bits 20..10 of the keys in b1
+    // ---- b1; counts above it; candidates in it
     for (int s = 0; s < nseg; ++s) {
         const SegState S = seg[s];          // read before the helpers' barriers
-        uint32_t* gh = ghist + (int64_t)S.q * kHistWords;
-        find_bin<kBins1>(gh, keep, red);
-        const uint32_t b1 = (uint32_t)red[16];
-        if (tid == 0) { seg[s].prefix = b1; seg[s].above = red[17]; }
+        uint32_t* gsq = gstate + (int64_t)S.q * kQueryWords;
+        find_bin<kBins1, true>(gsq + kOffH1, keep, red);
+        const uint32_t b1 = (uint32_t)red[kR0];
+        if (tid == 0) { seg[s].prefix = b1; seg[s].above = red[kR1]; }
+        // above b1 in the high half, in b1 in the low half (each < 2^16 per CTA)
+        int packed = 0;
         for (int i = tid; i < S.n; i += kThreads) {
-            const uint32_t k = keys[S.koff + i];
-            if ((k >> 21) == b1) atomicAdd(&hist[(k >> 10) & (kBins2 - 1)], 1u);
+            const uint32_t bin = keys[S.koff + i] >> kShift1;
+            packed += bin > b1 ? 0x10000 : (bin == b1 ? 1 : 0);
         }
-        flush_hist<kBins2>(hist, gh + kBins1);
+        int tot;
+        int pos = block_excl_scan(packed, &tot, red) & 0xffff;
+        int nc = packed & 0xffff;
+        if (tid == 0) {
+            const int n_in = tot & 0xffff;
+            red[kR2] = n_in ? (int)atomicAdd(gsq + kOffCandN, (uint32_t)n_in) : 0;
+            gcnt[(int64_t)S.q * kFusedMaxGrid + cta] = make_int2(tot >> 16, 0);
+        }
+        __syncthreads();
+        pos += red[kR2];
+        int2* dst = reinterpret_cast<int2*>(gsq + kOffCand);
+        for (int i = tid; i < S.n && nc > 0; i += kThreads) {
+            const uint32_t k = keys[S.koff + i];
+            if ((k >> kShift1) == b1) {
+                if (pos < kCandCap) dst[pos] = make_int2((int)k, S.t_lo + i);
+                ++pos;
+                --nc;
+            }
+        }
     }
-    if (!grid_barrier(gbar, flag, err, 62)) return;
-    clear_level(ghist, bq.n_q, 0, kBins1);
+    if (u_begin >= u_end)                   // no units: zero counts for every query
+        for (int q = tid; q < bq.n_q; q += kThreads)
+            gcnt[(int64_t)q * kFusedMaxGrid + cta] = make_int2(0, 0);
+    if (!grid_barrier(gbar, red, err, 62)) return;
+    clear_level(gstate, bq.n_q, kOffH1, kBins1);
 
-    // ---- level 3: bits 9..0 of the keys in (b1, b2)
+    // ---- one round of loads: every query's candidate count (does any need
+    // the histogram levels? grid-uniform), and for the first part the counts of
+    // the earlier CTAs and the head of the candidate list
+    int* n_cand_q = red + 32;                         // [kFusedMaxQ]
+    CountLoads cl;
+    if (nseg > 0) {
+        const int q0 = seg[0].q;
+        if (tid < 32) load_counts(gcnt + (int64_t)q0 * kFusedMaxGrid, seg[0].c_first, cl);
+        const int2* src = reinterpret_cast<const int2*>(gstate + (int64_t)q0 * kQueryWords + kOffCand);
+        int2 v[kCandSpec / kThreads];                 // all in flight at once
+#pragma unroll
+        for (int k = 0; k < kCandSpec / kThreads; ++k) v[k] = __ldcg(src + tid + k * kThreads);
+#pragma unroll
+        for (int k = 0; k < kCandSpec / kThreads; ++k) cand[tid + k * kThreads] = v[k];
+    }
+    if (tid < 32) {
+        int over = 0;
+        if (tid < bq.n_q) {
+            const uint32_t n = __ldcg(gstate + (int64_t)tid * kQueryWords + kOffCandN);
+            n_cand_q[tid] = (int)n;
+            over = n > (uint32_t)kCandCap;
+        }
+        over = __any_sync(0xffffffffu, over);
+        if (tid == 0) red[kROver] = over;
+    }
+    __syncthreads();
+    const bool any_over = red[kROver] != 0;
+
+    // ---- resolve from the candidate lists
     for (int s = 0; s < nseg; ++s) {
         const SegState S = seg[s];
-        uint32_t* gh = ghist + (int64_t)S.q * kHistWords;
-        find_bin<kBins2>(gh + kBins1, keep - S.above, red);
-        const uint32_t prefix = (S.prefix << 11) | (uint32_t)red[16];
-        if (tid == 0) { seg[s].prefix = prefix; seg[s].above = S.above + red[17]; }
+        const uint32_t* gsq = gstate + (int64_t)S.q * kQueryWords;
+        const int n_cand = n_cand_q[S.q];
+        if (n_cand > kCandCap) continue;
+        const int staged = s == 0 ? (n_cand < kCandSpec ? n_cand : kCandSpec) : 0;
+        resolve_from_candidates(S, gsq, gcnt + (int64_t)S.q * kFusedMaxGrid, n_cand, staged, cl,
+                                s == 0, keep - S.above, S.prefix, keys, hist, cand, keep, kpool,
+                                idx + (int64_t)S.q * width, red);
+    }
+    if (!any_over) {
+        pdl_trigger();
+        return;
+    }
+
+    // ---- overflow: bits 20..10 of the keys in b1
+    for (int s = 0; s < nseg; ++s) {
+        const SegState S = seg[s];
+        uint32_t* gsq = gstate + (int64_t)S.q * kQueryWords;
+        if (n_cand_q[S.q] <= kCandCap) continue;
         for (int i = tid; i < S.n; i += kThreads) {
             const uint32_t k = keys[S.koff + i];
-            if ((k >> 10) == prefix) atomicAdd(&hist[k & (kBins3 - 1)], 1u);
+            if ((k >> kShift1) == S.prefix) atomicAdd(&hist[(k >> kShift2) & (kBins2 - 1)], 1u);
         }
-        flush_hist<kBins3>(hist, gh + kBins1 + kBins2);
+        flush_hist<kBins2>(hist, gsq + kOffH2);
     }
-    if (!grid_barrier(gbar, flag, err, 63)) return;
-    clear_level(ghist, bq.n_q, kBins1, kBins2);
+    if (!grid_barrier(gbar, red, err, 63)) return;
+
+    // ---- bits 9..0 of the keys in (b1, b2)
+    for (int s = 0; s < nseg; ++s) {
+        const SegState S = seg[s];
+        uint32_t* gsq = gstate + (int64_t)S.q * kQueryWords;
+        if (n_cand_q[S.q] <= kCandCap) continue;
+        find_bin<kBins2, true>(gsq + kOffH2, keep - S.above, red);
+        const uint32_t pre = (S.prefix << kBits2) | (uint32_t)red[kR0];
+        if (tid == 0) { seg[s].prefix = pre; seg[s].above = S.above + red[kR1]; }
+        for (int i = tid; i < S.n; i += kThreads) {
+            const uint32_t k = keys[S.koff + i];
+            if ((k >> kShift2) == pre) atomicAdd(&hist[k & (kBins3 - 1)], 1u);
+        }
+        flush_hist<kBins3>(hist, gsq + kOffH3);
+    }
+    if (!grid_barrier(gbar, red, err, 64)) return;
 
     // ---- T exact; this CTA's counts above and at T
     for (int s = 0; s < nseg; ++s) {
         const SegState S = seg[s];
-        const uint32_t* gh = ghist + (int64_t)S.q * kHistWords;
-        find_bin<kBins3>(gh + kBins1 + kBins2, keep - S.above, red);
-        const uint32_t T = (S.prefix << 10) | (uint32_t)red[16];
-        const int above = S.above + red[17];
+        const uint32_t* gsq = gstate + (int64_t)S.q * kQueryWords;
+        if (n_cand_q[S.q] <= kCandCap) continue;
+        find_bin<kBins3, true>(gsq + kOffH3, keep - S.above, red);
+        const uint32_t T = (S.prefix << kBits3) | (uint32_t)red[kR0];
+        const int above = S.above + red[kR1];
         int gt = 0, eq = 0;
         for (int i = tid; i < S.n; i += kThreads) {
             const uint32_t k = keys[S.koff + i];
             gt += k > T;
             eq += k == T;
         }
-        int tot_gt, tot_eq;
-        block_excl_scan(gt, &tot_gt, red);
-        block_excl_scan(eq, &tot_eq, red);
+        gt = block_sum(gt, red);
+        eq = block_sum(eq, red);
         if (tid == 0) {
             seg[s].prefix = T;
             seg[s].need_eq = keep - above;
-            seg[s].eq = tot_eq;
-            gcnt[(int64_t)S.q * kFusedMaxGrid + cta] = make_int2(tot_gt, tot_eq);
+            seg[s].eq = eq;
+            gcnt[(int64_t)S.q * kFusedMaxGrid + cta] = make_int2(gt, eq);
         }
         __syncthreads();
     }
-    if (!grid_barrier(gbar, flag, err, 64)) return;
-    clear_level(ghist, bq.n_q, kBins1 + kBins2, kBins3);
+    if (!grid_barrier(gbar, red, err, 65)) return;
+    clear_level(gstate, bq.n_q, kOffH2, kBins2 + kBins3);
     pdl_trigger();
 
-    // ---- emission
+    // ---- emission of the overflowed queries
     for (int s = 0; s < nseg; ++s) {
         const SegState S = seg[s];
-        const int64_t q_first_unit = ts[S.q];
-        if (warp == 0) {
-            // CTAs before this one that hold keys of the query
-            int g_before = 0, e_before = 0;
-            for (int c = lane; c < cta; c += 32) {
-                const int64_t ub = (int64_t)c * U / grid, ue = (int64_t)(c + 1) * U / grid;
-                if (ub < ue && ue > q_first_unit) {
-                    const int2 v = __ldcg(gcnt + (int64_t)S.q * kFusedMaxGrid + c);
-                    g_before += v.x;
-                    e_before += v.y;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                g_before += __shfl_xor_sync(0xffffffffu, g_before, off);
-                e_before += __shfl_xor_sync(0xffffffffu, e_before, off);
-            }
-            if (lane == 0) {
-                const int taken_before = e_before < S.need_eq ? e_before : S.need_eq;
-                int take = S.need_eq - e_before;
-                take = take < 0 ? 0 : (take > S.eq ? S.eq : take);
-                red[18] = g_before + taken_before;
-                red[19] = take;
-            }
+        if (n_cand_q[S.q] <= kCandCap) continue;
+        if (tid < 32) {
+            CountLoads cl2;
+            load_counts(gcnt + (int64_t)S.q * kFusedMaxGrid, S.c_first, cl2);
+            sum_counts(cl2, red);
         }
         __syncthreads();
-        const int base = red[18], take = red[19];
-        const bool partial = take > 0 && take < S.eq;     // uniform in the CTA
-        const uint32_t T = S.prefix;
-        int32_t* out = idx + (int64_t)S.q * width;
-        int sel_carry = 0, eq_carry = 0;
-        for (int c0 = 0; c0 < S.n; c0 += kThreads * kItems) {
-            const int j0 = c0 + tid * kItems;
-            uint32_t k[kItems];
-#pragma unroll
-            for (int r = 0; r < kItems; ++r)
-                k[r] = j0 + r < S.n ? keys[S.koff + j0 + r] : 0u;
-            int eq_rank = 0;
-            if (partial) {
-                int ne = 0;
-#pragma unroll
-                for (int r = 0; r < kItems; ++r) ne += (j0 + r < S.n) && k[r] == T;
-                int tot;
-                eq_rank = eq_carry + block_excl_scan(ne, &tot, red);
-                eq_carry += tot;
-            }
-            uint32_t selmask = 0;
-#pragma unroll
-            for (int r = 0; r < kItems; ++r) {
-                if (j0 + r >= S.n) continue;
-                bool sel = k[r] > T;
-                if (k[r] == T) {
-                    sel = partial ? eq_rank < take : take > 0;
-                    ++eq_rank;
-                }
-                selmask |= (uint32_t)sel << r;
-            }
-            int tot;
-            int pos = base + sel_carry + block_excl_scan(__popc(selmask), &tot, red);
-            sel_carry += tot;
-#pragma unroll
-            for (int r = 0; r < kItems; ++r) {
-                // positions stay below keep when the counts are consistent; the
-                // check keeps a corrupted state from writing past the row
-                if ((selmask & (1u << r)) && (unsigned)pos < (unsigned)keep)
-                    put(out, pos, (int64_t)S.t_lo + j0 + r, kpool);
-                pos += (selmask >> r) & 1u;
-            }
-        }
+        const int g_before = red[kR2], e_before = red[kR3];
+        const int taken_before = e_before < S.need_eq ? e_before : S.need_eq;
+        int take = S.need_eq - e_before;
+        take = take < 0 ? 0 : (take > S.eq ? S.eq : take);
+        __syncthreads();
+        // keys equal to T: the first `take` of this part (ranked), or none
+        emit_part(S, keys, S.prefix, g_before + taken_before, -1, take > 0, take, keep, kpool,
+                  idx + (int64_t)S.q * width, red);
     }
 }
 
@@ -479,7 +725,7 @@ bool index_select_fused_eligible(const Shape& sh, const BatchDev& b) {
 }
 
 size_t index_select_fused_state_bytes() {
-    return (size_t)kFusedMaxQ * kHistWords * 4 +
+    return (size_t)kFusedMaxQ * kQueryWords * 4 +
            (size_t)kFusedMaxQ * kFusedMaxGrid * sizeof(int2);
 }
 
@@ -493,19 +739,19 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(index_select_fused,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmemBytes);
+                                         (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_select_fused, kThreads,
-                                                      C::kSmemBytes);
+                                                      kSmemBytes);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-    uint32_t* ghist = static_cast<uint32_t*>(state);
-    int2* gcnt = reinterpret_cast<int2*>(ghist + (size_t)kFusedMaxQ * kHistWords);
+    uint32_t* gstate = static_cast<uint32_t*>(state);
+    int2* gcnt = reinterpret_cast<int2*>(gstate + (size_t)kFusedMaxQ * kQueryWords);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)sm_count());
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -513,8 +759,8 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, index_select_fused, tm_k, tm_q, w, b, sh.top_k, sh.kpool,
-                              scores, ld, idx, n_sel, sh.index_row_width(), ghist, gcnt, gbar,
-                              err);
+                              reinterpret_cast<uint32_t*>(scores), ld, idx, n_sel, sh.index_row_width(), gstate, gcnt,
+                              reinterpret_cast<unsigned long long*>(gbar), err);
 }
 
 }  // namespace dsa

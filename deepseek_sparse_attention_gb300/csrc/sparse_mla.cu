@@ -226,31 +226,61 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
     }
 }
 
-// Log-sum-exp merge of the splits of one query: one CTA per (head, 128 latent
-// columns), one column per thread, so the partials are read by many SMs at once.
+// Log-sum-exp merge of the splits of one query: one CTA per (query, head), four
+// latent columns per thread.  Loads are issued eight splits at a time with no
+// data-dependent branch between them, so a thread waits for two rounds of
+// memory latency per eight splits rather than one per split.  An empty split
+// has m = -inf (weight 0; its zero partial is never used).
 __global__ void __launch_bounds__(128)
 merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __restrict__ part_ml,
              float* __restrict__ out, float* __restrict__ lse) {
     asm volatile("griddepcontrol.wait;" ::: "memory");      // the partials must be complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int h = blockIdx.x >> 2;
-    const int c = ((blockIdx.x & 3) << 7) + threadIdx.x;
+    constexpr int kB = 8;
+    const int h = blockIdx.x, c4 = threadIdx.x;             // columns 4 c4 .. 4 c4 + 3
     const int64_t q = blockIdx.y;
-    const float* ml = part_ml + (q * n_split * kHeads + h) * 2;     // split s at + s*kHeads*2
+    const float2* ml = reinterpret_cast<const float2*>(part_ml) + q * n_split * kHeads + h;
+    const float4* po = reinterpret_cast<const float4*>(part_o) +
+                       (q * n_split * kHeads + h) * (int64_t)(kLatent / 4) + c4;
+    const int64_t o_stride = (int64_t)kHeads * (kLatent / 4);   // float4s between splits
     float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) M = fmaxf(M, __ldg(ml + (int64_t)s * kHeads * 2));
-    float Lsum = 0.f, acc = 0.f;
+    for (int s0 = 0; s0 < n_split; s0 += kB) {
+        float2 v[kB];
+#pragma unroll
+        for (int k = 0; k < kB; ++k)
+            v[k] = s0 + k < n_split ? __ldg(ml + (int64_t)(s0 + k) * kHeads)
+                                    : make_float2(-INFINITY, 0.f);
+#pragma unroll
+        for (int k = 0; k < kB; ++k) M = fmaxf(M, v[k].x);
+    }
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-        for (int s = 0; s < n_split; ++s) {
-            const float ms = __ldg(ml + (int64_t)s * kHeads * 2);
-            if (ms == -INFINITY) continue;
-            const float f = expf(ms - M);
-            Lsum = fmaf(__ldg(ml + (int64_t)s * kHeads * 2 + 1), f, Lsum);
-            acc = fmaf(__ldg(part_o + ((q * n_split + s) * kHeads + h) * (int64_t)kLatent + c), f, acc);
+        for (int s0 = 0; s0 < n_split; s0 += kB) {
+            float2 v[kB];
+            float4 o[kB];
+#pragma unroll
+            for (int k = 0; k < kB; ++k) {
+                const bool in = s0 + k < n_split;
+                v[k] = in ? __ldg(ml + (int64_t)(s0 + k) * kHeads) : make_float2(-INFINITY, 0.f);
+                o[k] = in ? __ldg(po + (int64_t)(s0 + k) * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < kB; ++k) {
+                if (v[k].x == -INFINITY) continue;
+                const float f = expf(v[k].x - M);
+                L = fmaf(v[k].y, f, L);
+                acc.x = fmaf(o[k].x, f, acc.x);
+                acc.y = fmaf(o[k].y, f, acc.y);
+                acc.z = fmaf(o[k].z, f, acc.z);
+                acc.w = fmaf(o[k].w, f, acc.w);
+            }
         }
     }
-    out[(q * kHeads + h) * (int64_t)kLatent + c] = Lsum > 0.f ? acc / Lsum : 0.f;
-    if (lse != nullptr && c == 0) lse[q * kHeads + h] = Lsum > 0.f ? M + logf(Lsum) : -INFINITY;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    reinterpret_cast<float4*>(out)[(q * kHeads + h) * (int64_t)(kLatent / 4) + c4] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (lse != nullptr && c4 == 0) lse[q * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
 // Rows per split: enough CTAs to fill the GPU about twice, at least 64 rows each.
@@ -295,7 +325,7 @@ cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, 
 
 cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
                                 const float* part_ml, float* out, float* lse, cudaStream_t st) {
-    return launch_pdl(merge_splits, dim3(kHeads * (kLatent / 128), (unsigned)n_q), dim3(128), 0, st,
+    return launch_pdl(merge_splits, dim3(kHeads, (unsigned)n_q), dim3(kLatent / 4), 0, st,
                       n_split, part_o, part_ml, out, lse);
 }
 

@@ -147,7 +147,7 @@ dsa_status dsa_plan(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
  * zero-filled; after that every completed call leaves this region as it must
  * be, and dsa_check_device_error() re-zeroes it when a kernel reported an
  * error.  `ws` must be 256-byte aligned and at least 256 bytes. */
-#define DSA_WS_ZERO_BYTES (256u + 64u * 5120u * 4u + 64u * 256u * 8u)
+#define DSA_WS_ZERO_BYTES (256u + 16u * 21508u * 4u + 16u * 256u * 8u)
 dsa_status dsa_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Step 1: lightning-indexer scores ("GLM 5.2 in one C file", "The Lightning
@@ -200,10 +200,10 @@ dsa_status dsa_sparse_mla_attn(const dsa_shape *shape, const dsa_batch *batch, c
  * Scores and selections live in the workspace unless idx_out / n_sel_out are
  * given (then the selection is also written there, laid out as for
  * dsa_topk_select).  Works for decode and for chunks of prefill alike.
- * Decode batches of at most 64 queries with bf16 inputs and 32 indexer heads
+ * Decode batches of at most 16 queries with bf16 inputs and 32 indexer heads
  * run steps 1 and 2 as one cooperative launch whose CTAs wait on one another
- * through the workspace (a grid barrier and per-query histograms that each
- * launch leaves zero): the workspace must have been zeroed once
+ * through the workspace (a grid barrier and per-query histograms and
+ * candidate counters that each launch leaves as it found them): the workspace must have been zeroed once
  * (dsa_workspace_init, or allocated zero-filled), and two calls sharing one
  * workspace must not run concurrently.  The launch needs every CTA resident at
  * once; DSA_ERR_CUDA is returned if the device cannot give it that.
