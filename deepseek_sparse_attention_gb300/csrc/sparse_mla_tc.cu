@@ -8,22 +8,31 @@
 // scale 1/16; "Add GLM-5.3-Flash support": a NoPE row is the 512-wide latent,
 // key and value alike).
 //
-// One CTA handles a range of one query's selected rows in tiles of 128 rows:
+// One CTA handles a range of one query's selected rows in tiles of 64 rows,
+// two row buffers deep, so that one tile's gather overlaps the previous
+// tile's softmax and value product:
 //   warps 0,2,3 load the query once (TMA tiles) and gather each tile's rows
 //              with 16-byte cp.async copies straight into the 128-byte swizzle
-//              layout -- thousands of copies in flight per SM, where a TMA
-//              gather4 (four 128-byte row pieces per request) kept too few;
-//   warp 1     issues S^T = R . Q^T (M = 128 rows, N = 64 heads, K = the row
-//              width) into TMEM, then O^T += R^T . P^T (M = 128 latent columns
-//              x 4, N = 64 heads, K = 128 rows) with both operands MN-major --
-//              the same gathered tile serves as K-major A for the scores and as
-//              MN-major A for the values;
-//   warps 4-11 softmax across the tile's rows: one TMEM lane (row) and half the
-//              heads per thread, per-head tile maxima by warp reductions, a running maximum that
-//              is raised (and O^T rescaled in TMEM) only when a tile exceeds it
-//              by more than 2^8, exp2, P^T written to shared memory (into the
-//              rope block, which the scores no longer need), per-thread partial
-//              row sums reduced once at the end.
+//              layout of buffer t % 2 -- thousands of copies in flight per SM,
+//              where a TMA gather4 (four 128-byte row pieces per request) kept
+//              too few;
+//   warp 1     issues S^T = R . Q^T (M = 64 rows, N = 64 heads, K = the row
+//              width) into one of two TMEM score buffers -- the next tile's
+//              scores before this tile's values -- then O^T += R^T . P^T
+//              (M = 128 latent columns x 4, N = 64 heads, K = 64 rows) with both
+//              operands MN-major: the same gathered tile serves as K-major A for
+//              the scores and as MN-major A for the values;
+// P is split into bf16 hi + lo parts and the value product runs once on each
+// (through the same shared-memory buffer), carrying P to ~2^-16 relative where
+// bf16 alone (2^-9) would not meet the output tolerance.
+//   warps 4-11 softmax across the tile's rows: an M = 64 accumulator puts row
+//              16 q + i in lane i of TMEM quadrant q, so lanes 0..15 of each warp
+//              own one row and half the heads; per-head tile maxima by warp
+//              reductions, a running maximum that is raised (and O^T rescaled in
+//              TMEM, after the previous tile's values are in) only when a tile
+//              exceeds it by more than 2^8, exp2, P^T written to shared memory
+//              (into the buffer's rope block, which the scores no longer need),
+//              per-thread partial row sums reduced once at the end.
 // Splits of one query are combined by the log-sum-exp merge.
 #include <math.h>
 
@@ -36,13 +45,15 @@ namespace {
 using namespace sm100;
 
 constexpr int kHeads = 64;
-constexpr int kTileRows = 128;
+constexpr int kTileRows = 64;                       // rows per tile (MMA M of the scores)
+constexpr int kOBlock = 128;                        // latent columns per O^T block (MMA M)
 constexpr int kLatent = 512;
 constexpr uint32_t kQBlock = kHeads * 128;          // one 64-column block of Q: 8 KB
-constexpr uint32_t kRBlock = kTileRows * 128;       // one 64-column block of a row tile: 16 KB
-constexpr uint32_t kTmemCols = 512;                 // S^T 0..63, O^T 64..319, P lo 320..351
-constexpr uint32_t kOCol = 64;
-constexpr uint32_t kLoCol = 320;
+constexpr uint32_t kRBlock = kTileRows * 128;       // one 64-column block of a row tile: 8 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 0;                       // S^T of buffer b: columns 64 b .. 64 b + 63
+constexpr uint32_t kOCol = 128;                     // O^T: 128 .. 383
+constexpr uint32_t kLoCol = 384;                    // P lo of buffer b, warpgroup g: 384 + 32 b + 16 g
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -55,19 +66,22 @@ template <int W>
 struct Cfg {
     static constexpr int kCB = W / 64;               // 64-column blocks of a row
     static constexpr uint32_t kOffQ = 0;
-    static constexpr uint32_t kOffR = kCB * kQBlock;
-    // P^T [128 rows x 64 heads] bf16: the rope block of the tile when there is
-    // one (no longer needed once the scores are formed), else its own block.
-    static constexpr uint32_t kOffP = W == 576 ? kOffR + 8 * kRBlock : kOffR + kCB * kRBlock;
-    static constexpr uint32_t kOffBar = (W == 576 ? kOffR + kCB * kRBlock : kOffP + kRBlock);
-    // q_full, r_full, s_full, p_full, pv_done, drain, pv_hi
-    static constexpr uint32_t kOffRed = kOffBar + 64;          // [2][4][64] int
+    static constexpr uint32_t kOffR = kCB * kQBlock;                 // two row buffers
+    static constexpr uint32_t kBufBytes = kCB * kRBlock;
+    // P^T [64 rows x 64 heads] bf16 of buffer b: the buffer's rope block when
+    // there is one (no longer needed once the scores are formed), else its own.
+    static constexpr uint32_t kOffPx = kOffR + 2 * kBufBytes;         // NoPE: two P blocks
+    static constexpr uint32_t kOffBar = W == 576 ? kOffPx : kOffPx + 2 * kRBlock;
+    // q_full, drain, r_full[2], s_full[2], p_full[2], pv_hi[2], pv_done[2]
+    static constexpr uint32_t kOffRed = kOffBar + 128;          // [2][4][64] int
     static constexpr uint32_t kOffL = kOffRed + 2 * 4 * 64 * 4; // [64] float
     static constexpr uint32_t kOffM = kOffL + 64 * 4;           // [64] float
-    static constexpr uint32_t kOffRows = kOffM + 64 * 4;       // [128] int64 row addresses
-    static constexpr uint32_t kOffMisc = kOffRows + 128 * 8;
+    static constexpr uint32_t kOffMisc = kOffM + 64 * 4;
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    __device__ static uint32_t off_p(int b) {
+        return W == 576 ? kOffR + b * kBufBytes + 8 * kRBlock : kOffPx + b * kRBlock;
+    }
 };
 
 __device__ __forceinline__ int fkey(float f) {           // order-preserving float -> int
@@ -87,12 +101,11 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-    uint64_t *q_full = bars, *r_full = bars + 1, *s_full = bars + 2, *p_full = bars + 3,
-             *pv_done = bars + 4, *drain = bars + 5, *pv_hi = bars + 6;
+    uint64_t *q_full = bars, *drain = bars + 1, *r_full = bars + 2, *s_full = bars + 4,
+             *p_full = bars + 6, *pv_hi = bars + 8, *pv_done = bars + 10;
     int* red = reinterpret_cast<int*>(smem + C::kOffRed);
     float* l_fin = reinterpret_cast<float*>(smem + C::kOffL);
     float* m_fin = reinterpret_cast<float*>(smem + C::kOffM);
-    int64_t* row_s = reinterpret_cast<int64_t*>(smem + C::kOffRows);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -125,8 +138,15 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     const int n_tiles = (int)((j1 - j0 + kTileRows - 1) / kTileRows);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 7; ++i)
-            mbar_init(&bars[i], i == 3 ? kSoftmaxThreads : (i == 1 ? kLoaders : 1));
+        mbar_init(q_full, 1);
+        mbar_init(drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&r_full[i], kLoaders);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], kSoftmaxThreads);
+            mbar_init(&pv_hi[i], 1);
+            mbar_init(&pv_done[i], 1);
+        }
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -141,9 +161,15 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
 
     if (warp != 1 && warp < 4) {                                      // ---- loads
         // warps 0, 2, 3: 96 threads copy each tile's rows with 16-byte cp.async
-        // into the 128-byte swizzle layout (many copies in flight per SM), then
-        // make them visible to the tensor core's async proxy and arrive.
+        // into the 128-byte swizzle layout of buffer t % 2, eight threads per
+        // row (one 128-byte line of a 64-column block each), twelve rows at a
+        // time; then make them visible to the tensor core's async proxy and
+        // arrive.  A thread's row indices for tile t + 1 are read while tile t
+        // is copied, and tile t + 1 loads while tile t is in the softmax and PV.
         const int p = warp == 0 ? lane : 32 * (warp - 1) + lane;
+        const int rsub = p >> 3, k8 = p & 7;
+        constexpr int kRowsPerPass = kLoaders / 8;
+        constexpr int kPasses = (kTileRows + kRowsPerPass - 1) / kRowsPerPass;
         bool ok = true;
         if (p == 0) {
             mbar_arrive_expect_tx(q_full, C::kCB * kQBlock);
@@ -153,20 +179,65 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         }
         const int32_t* irow = idx + q * idx_width;
         const unsigned char* cbase = static_cast<const unsigned char*>(cache);
-        for (int t = 0; t < n_tiles && ok; ++t) {
-            if (t > 0) ok = mbar_wait(pv_done, (uint32_t)((t - 1) & 1), kWaitNs);
-            // this tile's row addresses, staged in shared memory
-            for (int r = p; r < kTileRows; r += kLoaders) {
+        // cache rows of this thread's rows of tile t (row 0 of the sequence
+        // past the selection or for an index out of range, which the softmax
+        // gives no weight)
+        auto rows_of = [&](int t, int64_t (&rows)[kPasses]) {
+#pragma unroll
+            for (int ps = 0; ps < kPasses; ++ps) {
+                const int r = kRowsPerPass * ps + rsub;
                 const int64_t j = j0 + (int64_t)t * kTileRows + r;
                 int32_t rr = 0;
-                if (j < j1) {
+                if (r < kTileRows && j < j1) {
                     rr = irow[j];
                     if (rr < 0 || rr >= qi.L) {
                         record_error(err, kDevBadIndex, (int32_t)q, /*where=*/8);
                         rr = 0;
                     }
                 }
-                row_s[r] = qi.row0 + rr;
+                rows[ps] = qi.row0 + rr;
+            }
+        };
+        // copies of tile t into buffer t % 2 (one cp.async group per tile)
+        auto issue = [&](int t, const int64_t (&rows)[kPasses]) {
+            const uint32_t rbase = smem_u32(smem + C::kOffR + (t & 1) * C::kBufBytes);
+#pragma unroll
+            for (int ps = 0; ps < kPasses; ++ps) {
+                const int r = kRowsPerPass * ps + rsub;
+                if (r >= kTileRows) continue;
+                const unsigned char* src = cbase + (rows[ps] * W + k8 * 8) * 2;
+                const uint32_t dst = rbase + r * 128 + ((k8 ^ (r & 7)) << 4);
+#pragma unroll
+                for (int cb = 0; cb < C::kCB; ++cb)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                                 ::"r"(dst + cb * kRBlock), "l"(src + cb * 128)
+                                 : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+        // The next tile's copies go out before this tile's are awaited when
+        // its buffer is already free (always for the second tile), so that two
+        // tiles' rows are in flight; otherwise after this tile's arrival.
+        int64_t rows_t[kPasses];
+        rows_of(0, rows_t);
+        issue(0, rows_t);
+        int issued = 1;
+        for (int t = 0; t < n_tiles && ok; ++t) {
+            if (issued == t + 1 && t + 1 < n_tiles &&
+                (t + 1 < 2 ||
+                 mbar_test_wait(&pv_done[(t + 1) & 1], (uint32_t)(((t - 1) >> 1) & 1)))) {
+                rows_of(t + 1, rows_t);
+                issue(t + 1, rows_t);
+                ++issued;
+            }
+            if (issued == t + 2) asm volatile("cp.async.wait_group 1;" ::: "memory");
+            else asm volatile("cp.async.wait_group 0;" ::: "memory");
+            fence_proxy_async_smem();
+            mbar_arrive(&r_full[t & 1]);
+            if (issued == t + 1 && t + 1 < n_tiles) {
+                rows_of(t + 1, rows_t);
+                // the buffer's previous tile (t - 1) must be through its PV
+                if (t >= 1) ok = mbar_wait(&pv_done[(t + 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), kWaitNs);
             }
             {   // all loaders agree on whether to proceed
                 uint32_t all_ok;
@@ -178,53 +249,54 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                     : "memory");
                 ok = all_ok != 0;
             }
-            if (ok) {
-                constexpr int kChunks = W / 8;                 // 16-byte chunks per row
-                for (int c = p; c < kTileRows * kChunks; c += kLoaders) {
-                    const int r = c / kChunks, c16 = c - r * kChunks;
-                    const int cb = c16 >> 3, k = c16 & 7;
-                    const uint32_t dst = smem_u32(smem + C::kOffR + cb * kRBlock + r * 128 +
-                                                  ((k ^ (r & 7)) << 4));
-                    const unsigned char* src = cbase + (row_s[r] * W + c16 * 8) * 2;
-                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src)
-                                 : "memory");
-                }
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                fence_proxy_async_smem();
+            if (ok && issued == t + 1 && t + 1 < n_tiles) {
+                issue(t + 1, rows_t);
+                ++issued;
             }
-            mbar_arrive(r_full);
-            asm volatile("bar.sync 2, %0;" ::"n"(kLoaders) : "memory");   // row_s reusable
         }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
         if (!ok && p == 0) record_error(err, kDevTimeout, (int32_t)q, /*where=*/9);
     } else if (warp == 1) {                                           // ---- MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kTileRows, kHeads);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32_major(kTileRows, kHeads, 1, 1);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32_major(kOBlock, kHeads, 1, 1);
             const uint32_t q0 = smem_u32(smem + C::kOffQ);
-            const uint32_t r0 = smem_u32(smem + C::kOffR);
-            const uint32_t p0 = smem_u32(smem + C::kOffP);
             bool ok = mbar_wait(q_full, 0, kWaitNs);
-            for (int t = 0; t < n_tiles && ok; ++t) {
-                ok = mbar_wait(r_full, (uint32_t)(t & 1), kWaitNs);
-                if (!ok) break;
-                tc_fence_after();
-                for (int cb = 0; cb < C::kCB; ++cb) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        mma_bf16_ss(tmem_base, sdesc_kmajor_sw128(r0 + cb * kRBlock + kk * 32),
-                                    sdesc_kmajor_sw128(q0 + cb * kQBlock + kk * 32), idesc_s,
-                                    (cb | kk) != 0 ? 1u : 0u);
-                    }
-                }
-                mma_commit(s_full);
-                // P = P_hi + P_lo, both bf16, through the same buffer: the value
-                // product carries P to ~2^-16 relative, not bf16's 2^-9.
-                for (int part = 0; part < 2 && ok; ++part) {
-                    ok = mbar_wait(p_full, (uint32_t)part, kWaitNs);
-                    if (!ok) break;
+            // Issue whatever is ready, in dependency order: the scores S(s) of
+            // tile s once its rows are in (and at most one tile ahead of the
+            // values, whose softmax frees the other score buffer), and the
+            // value products of tile v -- the P_hi pass, then the P_lo pass --
+            // as soon as the softmax hands each over.
+            int next_s = 0, next_v = 0, part = 0;
+            uint64_t t_prog = globaltimer_ns();
+            while (ok && next_v < n_tiles) {
+                bool progressed = false;
+                if (next_s < n_tiles && next_s <= next_v + 1 &&
+                    mbar_test_wait(&r_full[next_s & 1], (uint32_t)((next_s >> 1) & 1))) {
+                    // S^T(s) = R(s) Q^T: M = 64 rows, N = 64 heads, K = the row width
                     tc_fence_after();
-                    // A = R^T: MN-major, 64-column blocks 16 KB apart, 8-row groups
-                    // 1 KB apart.  B = P^T: MN-major, the 64 heads are one block.
+                    const int bs = next_s & 1;
+                    const uint32_t r0 = smem_u32(smem + C::kOffR + bs * C::kBufBytes);
+                    for (int cb = 0; cb < C::kCB; ++cb) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            mma_bf16_ss(tmem_base + kSCol + 64 * bs,
+                                        sdesc_kmajor_sw128(r0 + cb * kRBlock + kk * 32),
+                                        sdesc_kmajor_sw128(q0 + cb * kQBlock + kk * 32), idesc_s,
+                                        (cb | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&s_full[bs]);
+                    ++next_s;
+                    progressed = true;
+                }
+                if (next_v < next_s && mbar_test_wait(&p_full[next_v & 1], (uint32_t)part)) {
+                    // A = R^T: MN-major, 64-column blocks 8 KB apart, 8-row
+                    // groups 1 KB apart.  B = P^T: MN-major, the 64 heads are one block.
+                    tc_fence_after();
+                    const int bv = next_v & 1;
+                    const uint32_t r0 = smem_u32(smem + C::kOffR + bv * C::kBufBytes);
+                    const uint32_t p0 = smem_u32(smem + C::off_p(bv));
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -232,23 +304,35 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                             mma_bf16_ss(tmem_base + kOCol + 64 * i,
                                         sdesc_sw128(r0 + 2 * i * kRBlock + kk * 2048, kRBlock, 1024),
                                         sdesc_sw128(p0 + kk * 2048, 1024, 1024), idesc_pv,
-                                        (t > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                                        (next_v > 0 || part > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
-                    mma_commit(part == 0 ? pv_hi : pv_done);
+                    mma_commit(part == 0 ? &pv_hi[bv] : &pv_done[bv]);
+                    if (part == 0) {
+                        part = 1;
+                    } else {
+                        part = 0;
+                        ++next_v;
+                    }
+                    progressed = true;
                 }
-                if (!ok) break;
+                if (progressed) t_prog = globaltimer_ns();
+                else if (globaltimer_ns() - t_prog > kWaitNs) ok = false;
             }
             if (!ok) record_error(err, kDevTimeout, (int32_t)q, /*where=*/10);
             mma_commit(drain);
             mbar_wait(drain, 0, 50000000ull);
         }
     } else if (warp >= 4) {                                           // ---- softmax
-        // two warpgroups over the same 128 rows: warpgroup sg owns heads
-        // [32 sg, 32 sg + 32) of every row (warps w and w + 4 share a TMEM quadrant)
+        // two warpgroups over the same 64 rows: warpgroup sg owns heads
+        // [32 sg, 32 sg + 32).  The scores of an M = 64 tile sit in lanes 0..15
+        // of each 32-lane TMEM quadrant: warps w and w + 4 (quadrant wq) hold
+        // rows 16 wq .. 16 wq + 15, one per lane 0..15; lanes 16..31 carry none.
         const int wq = warp & 3, sg = (warp - 4) >> 2;
-        const int row = 32 * wq + lane;
+        const bool has_row = lane < 16;
+        const int row = 16 * wq + (lane & 15);
         const int hb = 32 * sg;                      // first head of this thread
+        const bool head_owner = wq == 0;             // warps 4, 8: head hb + lane
         const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * wq) << 16);
         const float c2 = scale * kLog2e;
         float l_part[32];
@@ -257,16 +341,16 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         // running maxima (one writer per head) and rescale factors live in shared memory
         float* m_sh = m_fin;
         float* alpha_s = l_fin;
-        if (row < 32) m_sh[hb + row] = -INFINITY;
-        uint8_t* prow = smem + C::kOffP + row * 128;
+        if (head_owner) m_sh[hb + lane] = -INFINITY;
         bool ok = true;
         for (int t = 0; t < n_tiles; ++t) {
-            if (ok) ok = mbar_wait(s_full, (uint32_t)(t & 1), kWaitNs);
+            const int bf = t & 1;
+            if (ok) ok = mbar_wait(&s_full[bf], (uint32_t)((t >> 1) & 1), kWaitNs);
             tc_fence_after();
             // rows past the split, and rows whose index is out of range (reported
             // by the loader), take no weight
             const int64_t jrow = j0 + (int64_t)t * kTileRows + row;
-            bool valid = jrow < j1;
+            bool valid = has_row && jrow < j1;
             if (valid) {
                 const int32_t r = idx[q * idx_width + jrow];
                 valid = r >= 0 && r < qi.L;
@@ -274,44 +358,63 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             float x[32];
             {
                 float v[32];
-                tmem_ld_32cols(lane_addr + hb, v);
+                tmem_ld_32cols(lane_addr + kSCol + 64 * bf + hb, v);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[e] = valid ? v[e] * c2 : -INFINITY;
             }
-            // per-head maximum over the tile's 128 rows
-            int* rb = red + (t & 1) * 4 * kHeads + wq * kHeads + hb;
+            // Does any score of the tile exceed its head's running maximum by
+            // more than the slack?  If none does (the usual case after the
+            // first tiles) the maxima stay and no reduction is needed.
+            uint32_t exceed = 0;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int mk = __reduce_max_sync(0xffffffffu, fkey(x[e]));
-                if (lane == e) rb[e] = mk;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-            uint32_t raised = 0;
-            if (row < 32) {                            // head hb + row: raise its running maximum?
-                const int h = hb + row;
-                const int* rt = red + (t & 1) * 4 * kHeads;
-                const int mk = max(max(rt[h], rt[kHeads + h]), max(rt[2 * kHeads + h], rt[3 * kHeads + h]));
-                const float tmax = fval(mk), m_old = m_sh[h];
-                float a = 1.f;
-                if (tmax > m_old + kSlack) {
-                    a = m_old == -INFINITY ? 0.f : exp2f(m_old - tmax);
-                    m_sh[h] = tmax;
-                    raised = 1;
-                }
-                alpha_s[h] = a;
-            }
-            uint32_t any_raised;
+            for (int e = 0; e < 32; ++e) exceed |= (uint32_t)(x[e] > m_sh[hb + e] + kSlack);
+            uint32_t any_exceed;
             asm volatile(
                 "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
                 "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-                : "=r"(any_raised)
-                : "r"(raised), "n"(kSoftmaxThreads)
+                : "=r"(any_exceed)
+                : "r"(exceed), "n"(kSoftmaxThreads)
                 : "memory");
+            uint32_t any_raised = 0;
+            if (any_exceed) {
+                // per-head maximum over the tile's 64 rows
+                int* rb = red + (t & 1) * 4 * kHeads + wq * kHeads + hb;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int mk = __reduce_max_sync(0xffffffffu, fkey(x[e]));
+                    if (lane == e) rb[e] = mk;
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+                uint32_t raised = 0;
+                if (head_owner) {                      // head hb + lane: raise its running maximum?
+                    const int h = hb + lane;
+                    const int* rt = red + (t & 1) * 4 * kHeads;
+                    const int mk = max(max(rt[h], rt[kHeads + h]), max(rt[2 * kHeads + h], rt[3 * kHeads + h]));
+                    const float tmax = fval(mk), m_old = m_sh[h];
+                    float a = 1.f;
+                    if (tmax > m_old + kSlack) {
+                        a = m_old == -INFINITY ? 0.f : exp2f(m_old - tmax);
+                        m_sh[h] = tmax;
+                        raised = 1;
+                    }
+                    alpha_s[h] = a;
+                }
+                asm volatile(
+                    "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                    "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                    : "=r"(any_raised)
+                    : "r"(raised), "n"(kSoftmaxThreads)
+                    : "memory");
+            }
             if (any_raised) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) l_part[e] *= alpha_s[hb + e];
             }
             if (any_raised && t > 0) {                 // O^T follows the new maxima
+                // the previous tile's PV may still be accumulating into O^T
+                const int pb = (t - 1) & 1;
+                if (ok) ok = mbar_wait(&pv_done[pb], (uint32_t)(((t - 1) >> 1) & 1), kWaitNs);
+                tc_fence_after();
 #pragma unroll 1
                 for (int i = 0; i < 4; ++i) {
                     float v[32];
@@ -321,11 +424,14 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                     for (int c = 0; c < 32; ++c) v[c] *= alpha_s[hb + c];
                     tmem_st_32cols(a, v);
                 }
+                tc_fence_before();
                 asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
             }
             // this thread's half of its P^T row: 32 bf16 in the 128-byte swizzle
             // layout.  p = hi + lo with hi = bf16(p), lo = bf16(p - hi); hi goes to
             // shared memory now, lo waits in spare TMEM columns for the second pass.
+            uint8_t* prow = smem + C::off_p(bf) + row * 128;
+            const uint32_t lo_addr = lane_addr + kLoCol + 32 * bf + 16 * sg;
             float lo_bits[16];
 #pragma unroll
             for (int c16 = 0; c16 < 4; ++c16) {
@@ -345,50 +451,59 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                     lo_bits[4 * c16 + e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&lo));
                 }
                 const int chunk = 4 * sg + c16;
-                *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                if (has_row)
+                    *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            tmem_st_16cols(lane_addr + kLoCol + 16 * sg, lo_bits);
+            tmem_st_16cols(lo_addr, lo_bits);
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[bf]);
             // second pass: the lo parts, once the hi product has read the buffer
-            if (ok) ok = mbar_wait(pv_hi, (uint32_t)(t & 1), kWaitNs);
+            if (ok) ok = mbar_wait(&pv_hi[bf], (uint32_t)((t >> 1) & 1), kWaitNs);
             tc_fence_after();
-            tmem_ld_16cols(lane_addr + kLoCol + 16 * sg, lo_bits);
+            tmem_ld_16cols(lo_addr, lo_bits);
 #pragma unroll
             for (int c16 = 0; c16 < 4; ++c16) {
                 const int chunk = 4 * sg + c16;
-                *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-                    make_uint4(__float_as_uint(lo_bits[4 * c16]), __float_as_uint(lo_bits[4 * c16 + 1]),
-                               __float_as_uint(lo_bits[4 * c16 + 2]), __float_as_uint(lo_bits[4 * c16 + 3]));
+                if (has_row)
+                    *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(__float_as_uint(lo_bits[4 * c16]), __float_as_uint(lo_bits[4 * c16 + 1]),
+                                   __float_as_uint(lo_bits[4 * c16 + 2]), __float_as_uint(lo_bits[4 * c16 + 3]));
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(p_full);
+            mbar_arrive(&p_full[bf]);
         }
-        if (ok) ok = mbar_wait(pv_done, (uint32_t)((n_tiles - 1) & 1), kWaitNs);
+        {
+            const int tl = n_tiles - 1;
+            if (ok) ok = mbar_wait(&pv_done[tl & 1], (uint32_t)((tl >> 1) & 1), kWaitNs);
+        }
         if (!ok) record_error(err, kDevTimeout, (int32_t)q, /*where=*/11);
         tc_fence_after();
         // row sums: per-thread partials -> per-head totals (through shared memory;
-        // the row tile is free once the last PV has completed)
+        // the row buffers are free once the last PV has completed)
         float* lsc = reinterpret_cast<float*>(smem + C::kOffR);
+        if (has_row) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) lsc[row * (kHeads + 1) + hb + e] = l_part[e];
-        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-        if (sg == 0 && row < kHeads) {
-            float sum = 0.f;
-            for (int r = 0; r < kTileRows; ++r) sum += lsc[r * (kHeads + 1) + row];
-            l_fin[row] = sum;
+            for (int e = 0; e < 32; ++e) lsc[row * (kHeads + 1) + hb + e] = l_part[e];
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-        // O^T lane `row` holds latent columns row + 128 i; this thread writes heads hb..
+        if (head_owner) {
+            const int h = hb + lane;
+            float sum = 0.f;
+            for (int r = 0; r < kTileRows; ++r) sum += lsc[r * (kHeads + 1) + h];
+            l_fin[h] = sum;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        // O^T lane 32 wq + lane holds latent columns 32 wq + lane + 128 i (an
+        // M = 128 accumulator); this thread writes heads hb ..
         const bool final_out = n_split == 1;
         const int64_t part = q * n_split + split;
         float* dst = final_out ? out + q * kHeads * kLatent : part_o + part * kHeads * kLatent;
 #pragma unroll 1
         for (int i = 0; i < 4; ++i) {
-            const int c = row + kTileRows * i;
+            const int c = 32 * wq + lane + kOBlock * i;
             float v[32];
             tmem_ld_32cols(lane_addr + kOCol + 64 * i + hb, v);
 #pragma unroll
@@ -397,15 +512,16 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 dst[(hb + e) * kLatent + c] = final_out ? (l > 0.f ? v[e] / l : 0.f) : v[e];
             }
         }
-        if (sg == 0 && row < kHeads) {
-            const float l = l_fin[row];
-            const float m = m_fin[row];
+        if (head_owner) {
+            const int h = hb + lane;
+            const float l = l_fin[h];
+            const float m = m_fin[h];
             if (final_out) {
                 if (lse != nullptr)
-                    lse[q * kHeads + row] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                    lse[q * kHeads + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
             } else {
-                part_ml[(part * kHeads + row) * 2] = l > 0.f ? m * kLn2 : -INFINITY;
-                part_ml[(part * kHeads + row) * 2 + 1] = l;
+                part_ml[(part * kHeads + h) * 2] = l > 0.f ? m * kLn2 : -INFINITY;
+                part_ml[(part * kHeads + h) * 2 + 1] = l;
             }
         }
     }
@@ -478,7 +594,7 @@ bool sparse_mla_tc_eligible(const Shape& sh, const BatchDev& b) {
            b.total_rows < ((int64_t)1 << 31) && (int64_t)b.n_q * kHeads < ((int64_t)1 << 31);
 }
 
-// Tiles of 128 rows; enough CTAs (one per SM) to fill the GPU about twice.
+// Tiles of 64 rows; enough CTAs (one per SM) to fill the GPU about twice.
 void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
                               int32_t* rows_per_split, int32_t* n_split) {
     int64_t max_rows = sh.index_row_width();
@@ -487,7 +603,10 @@ void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
     const int64_t tiles = (max_rows + kTileRows - 1) / kTileRows;
     const int64_t target_ctas = 2 * 152;
     int64_t splits = (target_ctas + n_q - 1) / n_q;
-    if (splits > tiles) splits = tiles;
+    // at least two tiles per split where there are enough, so that each split
+    // overlaps one tile's gather with the previous tile's softmax and PV
+    const int64_t max_splits = tiles >= 2 ? tiles / 2 : 1;
+    if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
     const int64_t tiles_per = (tiles + splits - 1) / splits;
     splits = (tiles + tiles_per - 1) / tiles_per;
