@@ -29,15 +29,16 @@ import torch
 __all__ = [
     "DsaError", "Shape", "Batch", "load", "make_shape", "make_batch", "workspace_size",
     "alloc_workspace", "dsa_version", "dsa_index_row_width", "dsa_workspace_size",
-    "dsa_workspace_init", "dsa_plan", "dsa_index_scores", "dsa_topk_select", "dsa_sparse_mla_attn",
+    "dsa_workspace_init", "dsa_plan", "dsa_index_scores", "dsa_topk_select", "dsa_index_select",
+    "dsa_sparse_mla_attn",
     "dsa_decode_step", "dsa_decode_step_noalloc", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
-    "OP_INDEX_SCORES", "OP_TOPK_SELECT", "OP_SPARSE_MLA", "OP_DECODE_STEP",
+    "OP_INDEX_SCORES", "OP_TOPK_SELECT", "OP_SPARSE_MLA", "OP_DECODE_STEP", "OP_INDEX_SELECT",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
 
 DSA_F32, DSA_BF16 = 0, 1
-OP_INDEX_SCORES, OP_TOPK_SELECT, OP_SPARSE_MLA, OP_DECODE_STEP = 0, 1, 2, 3
+OP_INDEX_SCORES, OP_TOPK_SELECT, OP_SPARSE_MLA, OP_DECODE_STEP, OP_INDEX_SELECT = 0, 1, 2, 3, 4
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
           3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE", 6: "DSA_ERR_TIMEOUT"}
 
@@ -94,6 +95,7 @@ def load() -> ctypes.CDLL:
             "dsa_plan": ([S, B, i32, ctypes.POINTER(PlanInfo)], ctypes.c_int),
             "dsa_index_scores": ([S, B, P, P, P, P, i64, P, sz, P], ctypes.c_int),
             "dsa_topk_select": ([S, B, P, i64, P, P, P, sz, P], ctypes.c_int),
+            "dsa_index_select": ([S, B, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_sparse_mla_attn": ([S, B, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_decode_step": ([S, B, P, P, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_check_device_error": ([P, sz, P, ctypes.POINTER(i32)], ctypes.c_int),
@@ -201,6 +203,11 @@ def dsa_index_scores(shape, batch, q_idx, w, k_idx, scores, ld, ws, stream=None)
 def dsa_topk_select(shape, batch, scores, ld, idx, n_sel, ws, stream=None) -> None:
     _call("dsa_topk_select", ctypes.byref(shape), ctypes.byref(batch), _ptr(scores), int(ld),
           _ptr(idx), _ptr(n_sel), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def dsa_index_select(shape, batch, q_idx, w, k_idx, idx, n_sel, ws, stream=None) -> None:
+    _call("dsa_index_select", ctypes.byref(shape), ctypes.byref(batch), _ptr(q_idx), _ptr(w),
+          _ptr(k_idx), _ptr(idx), _ptr(n_sel), _ptr(ws), ws.numel(), _stream(stream))
 
 
 def dsa_sparse_mla_attn(shape, batch, q_abs, cache, idx, n_sel, out, lse, ws, stream=None) -> None:

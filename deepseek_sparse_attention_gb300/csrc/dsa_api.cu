@@ -107,6 +107,7 @@ size_t op_bytes(const Shape& sh, const BatchDev& b, int32_t op) {
         case DSA_OP_SPARSE_MLA:
             return align_up(kWsHeaderBytes + sparse_mla_scratch_bytes(sh, b));
         case DSA_OP_DECODE_STEP: return step_layout(sh, b).total;
+        case DSA_OP_INDEX_SELECT: return step_layout(sh, b).attn;
         default: return 0;
     }
 }
@@ -124,6 +125,30 @@ dsa_status cuda_status(cudaError_t e, const char* what) {
 }
 
 unsigned char* bytes(void* p) { return static_cast<unsigned char*>(p); }
+
+// Steps 1 and 2 into idx / n_sel: the fused launch where it applies, else the
+// indexer and the selection.
+cudaError_t enqueue_index_select(const Shape& sh, const BatchDev& b, const StepLayout& lay,
+                                 void* ws, const void* q_idx, const float* w, const void* k_idx,
+                                 int32_t* idx, int32_t* n_sel, cudaStream_t st,
+                                 const char** what) {
+    int32_t* err = static_cast<int32_t*>(ws);
+    float* scores = reinterpret_cast<float*>(bytes(ws) + lay.scores);
+    const int64_t ld = default_ld(sh, b);
+    if (index_select_fused_eligible(sh, b)) {
+        *what = "index_select_fused";
+        return launch_index_select_fused(sh, b, q_idx, w, k_idx, scores, ld, idx, n_sel,
+                                         bytes(ws) + lay.sel,
+                                         reinterpret_cast<uint32_t*>(bytes(ws) + kWsGridBarOffset),
+                                         err, st);
+    }
+    *what = "index_scores";
+    cudaError_t e = launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld,
+                                        bytes(ws) + lay.idx_plan, err, st);
+    if (e != cudaSuccess) return e;
+    *what = "topk_select";
+    return launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
+}
 
 }  // namespace
 }  // namespace dsa
@@ -166,7 +191,7 @@ dsa_status dsa_workspace_size(const dsa_shape* shape, const dsa_batch* batch, in
     b = BatchDev{nullptr,           nullptr,           nullptr,           batch->n_seq,
                  batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
                  batch->total_keys, sh.kpool};
-    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_DECODE_STEP) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_INDEX_SELECT) return DSA_ERR_INVALID_ARG;
     *out_bytes = op_bytes(sh, b, op);
     return DSA_OK;
 }
@@ -178,7 +203,7 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
     dsa_status s = check_shape(shape, &sh);
     if (s != DSA_OK) return s;
     if (batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
-    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_DECODE_STEP) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_INDEX_SELECT) return DSA_ERR_INVALID_ARG;
     const BatchDev bh{nullptr,           nullptr,           nullptr,           batch->n_seq,
                       batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
                       batch->total_keys, sh.kpool};
@@ -194,6 +219,7 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
             case DSA_OP_INDEX_SCORES: n = idx; break;
             case DSA_OP_TOPK_SELECT: n = 1; break;
             case DSA_OP_SPARSE_MLA: n = attn; break;
+            case DSA_OP_INDEX_SELECT: n = index_select_fused_eligible(sh, bh) ? 1 : idx + 1; break;
             default: n = (index_select_fused_eligible(sh, bh) ? 1 : idx + 1) + attn; break;
         }
     }
@@ -283,30 +309,40 @@ dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const
     if (b.n_q == 0) return DSA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int32_t* err = static_cast<int32_t*>(ws);
-    float* scores = reinterpret_cast<float*>(bytes(ws) + lay.scores);
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(bytes(ws) + lay.idx);
     int32_t* n_sel = n_sel_out ? n_sel_out : reinterpret_cast<int32_t*>(bytes(ws) + lay.n_sel);
-    const int64_t ld = default_ld(sh, b);
     if (trace_on())
-        fprintf(stderr, "[dsa] decode_step n_q=%d max_kv=%lld ld=%lld ws=%zu\n", b.n_q,
-                (long long)b.max_kv_len, (long long)ld, lay.total);
-    cudaError_t e;
-    if (index_select_fused_eligible(sh, b)) {
-        e = launch_index_select_fused(sh, b, q_idx, w, k_idx, scores, ld, idx, n_sel,
-                                      bytes(ws) + lay.sel,
-                                      reinterpret_cast<uint32_t*>(bytes(ws) + kWsGridBarOffset),
-                                      err, st);
-        if (e != cudaSuccess) return cuda_status(e, "decode_step/index_select_fused");
-    } else {
-        e = launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld,
-                                bytes(ws) + lay.idx_plan, err, st);
-        if (e != cudaSuccess) return cuda_status(e, "decode_step/index_scores");
-        e = launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
-        if (e != cudaSuccess) return cuda_status(e, "decode_step/topk_select");
-    }
+        fprintf(stderr, "[dsa] decode_step n_q=%d max_kv=%lld ws=%zu\n", b.n_q,
+                (long long)b.max_kv_len, lay.total);
+    const char* what = "";
+    cudaError_t e = enqueue_index_select(sh, b, lay, ws, q_idx, w, k_idx, idx, n_sel, st, &what);
+    if (e != cudaSuccess) return cuda_status(e, what);
     e = launch_sparse_mla(sh, b, q_abs, cache, idx, n_sel, out, lse, bytes(ws) + lay.attn,
                           lay.total - lay.attn, err, st);
     return cuda_status(e, "decode_step/sparse_mla_attn");
+}
+
+dsa_status dsa_index_select(const dsa_shape* shape, const dsa_batch* batch, const void* q_idx,
+                            const float* w, const void* k_idx, int32_t* idx, int32_t* n_sel,
+                            void* ws, size_t ws_bytes, void* stream) {
+    Shape sh;
+    BatchDev b;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    if (b.n_q > 0 && (q_idx == nullptr || w == nullptr || k_idx == nullptr || idx == nullptr ||
+                      n_sel == nullptr))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(idx) ||
+        !aligned16(n_sel))
+        return DSA_ERR_INVALID_ARG;
+    const StepLayout lay = step_layout(sh, b);
+    if ((s = check_ws(ws, ws_bytes, lay.attn)) != DSA_OK) return s;
+    if (b.n_q == 0) return DSA_OK;
+    const char* what = "";
+    const cudaError_t e = enqueue_index_select(sh, b, lay, ws, q_idx, w, k_idx, idx, n_sel,
+                                               static_cast<cudaStream_t>(stream), &what);
+    return cuda_status(e, what);
 }
 
 dsa_status dsa_check_device_error(void* ws, size_t ws_bytes, void* stream, int32_t* code) {

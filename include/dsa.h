@@ -125,6 +125,7 @@ int64_t dsa_index_row_width(const dsa_shape *shape);
 #define DSA_OP_TOPK_SELECT 1
 #define DSA_OP_SPARSE_MLA 2
 #define DSA_OP_DECODE_STEP 3
+#define DSA_OP_INDEX_SELECT 4
 dsa_status dsa_workspace_size(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
                               size_t *bytes);
 
@@ -180,6 +181,17 @@ dsa_status dsa_index_scores(const dsa_shape *shape, const dsa_batch *batch, cons
 dsa_status dsa_topk_select(const dsa_shape *shape, const dsa_batch *batch, const float *scores,
                            int64_t ld, int32_t *idx, int32_t *n_sel, void *ws, size_t ws_bytes,
                            void *stream);
+
+/* Steps 1 and 2 together: the selection dsa_topk_select makes from the scores
+ * dsa_index_scores computes, without returning the scores (they stay in the
+ * workspace, or never leave the chip).  Arguments as for those two calls;
+ * idx / n_sel as for dsa_topk_select; the workspace is sized with
+ * DSA_OP_INDEX_SELECT.  Decode batches of at most 16 queries with bf16 inputs
+ * and 32 indexer heads run as one cooperative launch, under the conditions
+ * stated at dsa_decode_step; other batches as the two launches. */
+dsa_status dsa_index_select(const dsa_shape *shape, const dsa_batch *batch, const void *q_idx,
+                            const float *w, const void *k_idx, int32_t *idx, int32_t *n_sel,
+                            void *ws, size_t ws_bytes, void *stream);
 
 /* Step 3: absorbed-MLA attention over the selected rows ("GLM 5.2 in one C
  * file", MLA decode path; "GLM-5.x", "The block").

@@ -72,6 +72,15 @@ def test_workspace_sizes(lib):
     assert rc == 0 and n >= 256 and n % 256 == 0
     rc, n = _size(sh, _batch(), dsa.OP_TOPK_SELECT)
     assert rc == 0 and n == 256
+    rc, n_sel = _size(sh, _batch(max_kv=131072), dsa.OP_INDEX_SELECT)
+    rc2, n_step = _size(sh, _batch(max_kv=131072), dsa.OP_DECODE_STEP)
+    # everything the decode step needs but the attention scratch; the fixed
+    # selection state of the fused launch comes first
+    assert rc == 0 and rc2 == 0 and n_sel % 256 == 0
+    assert 256 + 131072 * 4 <= n_sel <= n_step
+    assert n_sel >= 256 + 16 * 21508 * 4 + 16 * 256 * 8          # DSA_WS_ZERO_BYTES of dsa.h
+    rc, _ = _size(sh, _batch(), 5)
+    assert rc == 1
     rc, _ = _size(sh, _batch(), 7)
     assert rc == 1
 

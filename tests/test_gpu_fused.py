@@ -190,3 +190,24 @@ def test_fused_workspace_reuse_across_batches():
                 got = _step(wl, d, ws)
                 for x, y in zip(got, fresh):
                     assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("wl", [FUSED[0], FUSED[2],
+                                workloads.small("twenty_queries", [9000] * 20, top_k=2048, seed=5)],
+                         ids=lambda w: w.name)
+def test_index_select_entry_matches_decode_step(wl):
+    """dsa_index_select (steps 1 and 2 alone) writes the selection the whole
+    step uses, on the fused path and (20 queries) on the two-launch path."""
+    host = workloads.make(wl, "cpu")
+    d = to_device(host)
+    sh, b = gpu_shape(wl), gpu_batch(wl, d)
+    _, _, idx_ref, n_ref = _step(wl, d)
+    ws = dsa.alloc_workspace(sh, b, dsa.OP_INDEX_SELECT)
+    width = dsa.dsa_index_row_width(sh)
+    idx = torch.full((wl.n_q, width), -7, dtype=torch.int32, device="cuda")
+    n_sel = torch.full((wl.n_q,), -7, dtype=torch.int32, device="cuda")
+    for _ in range(2):                       # the second call reuses the workspace state
+        dsa.dsa_index_select(sh, b, d["q_idx"], d["w"], d["k_idx"], idx, n_sel, ws)
+        assert dsa.dsa_check_device_error(ws) == 0
+        assert np.array_equal(idx.cpu().numpy(), idx_ref)
+        assert np.array_equal(n_sel.cpu().numpy(), n_ref)
