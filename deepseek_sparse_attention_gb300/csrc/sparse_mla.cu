@@ -230,7 +230,7 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
 // latent columns per thread.  Loads are issued eight splits at a time with no
 // data-dependent branch between them, so a thread waits for two rounds of
 // memory latency per eight splits rather than one per split.  An empty split
-// has m = -inf (weight 0; its zero partial is never used).
+// has m = -inf: weight 0, and its output (never written) is not used.
 __global__ void __launch_bounds__(128)
 merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __restrict__ part_ml,
              float* __restrict__ out, float* __restrict__ lse) {

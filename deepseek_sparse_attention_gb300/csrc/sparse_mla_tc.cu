@@ -119,19 +119,15 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
     const int64_t j0 = (int64_t)split * rows_per_split;
     const int64_t j1 = j0 + rows_per_split < ns ? j0 + rows_per_split : ns;
-    if (j0 >= j1) {                                   // empty split: neutral partial
-        if (n_split == 1) {
+    if (j0 >= j1) {
+        if (n_split == 1) {                           // no rows: out = 0, lse = -inf
             for (int i = threadIdx.x; i < kHeads * kLatent; i += blockDim.x)
                 out[q * kHeads * kLatent + i] = 0.f;
             if (lse != nullptr && threadIdx.x < kHeads) lse[q * kHeads + threadIdx.x] = -INFINITY;
-        } else {
-            const int64_t part = q * n_split + split;
-            for (int i = threadIdx.x; i < kHeads * kLatent; i += blockDim.x)
-                part_o[part * kHeads * kLatent + i] = 0.f;
-            if (threadIdx.x < kHeads) {
-                part_ml[(part * kHeads + threadIdx.x) * 2] = -INFINITY;
-                part_ml[(part * kHeads + threadIdx.x) * 2 + 1] = 0.f;
-            }
+        } else if (threadIdx.x < kHeads) {            // empty split: weight 0 in the merge,
+            const int64_t part = q * n_split + split;  // which then never reads its output
+            part_ml[(part * kHeads + threadIdx.x) * 2] = -INFINITY;
+            part_ml[(part * kHeads + threadIdx.x) * 2 + 1] = 0.f;
         }
         return;
     }
@@ -489,11 +485,12 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             for (int e = 0; e < 32; ++e) lsc[row * (kHeads + 1) + hb + e] = l_part[e];
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-        if (head_owner) {
+        if (head_owner) {                          // four independent sums, loads in flight together
             const int h = hb + lane;
-            float sum = 0.f;
-            for (int r = 0; r < kTileRows; ++r) sum += lsc[r * (kHeads + 1) + h];
-            l_fin[h] = sum;
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < kTileRows; ++r) s4[r & 3] += lsc[r * (kHeads + 1) + h];
+            l_fin[h] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
         // O^T lane 32 wq + lane holds latent columns 32 wq + lane + 128 i (an
@@ -603,9 +600,10 @@ void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
     const int64_t tiles = (max_rows + kTileRows - 1) / kTileRows;
     const int64_t target_ctas = 2 * 152;
     int64_t splits = (target_ctas + n_q - 1) / n_q;
-    // at least two tiles per split where there are enough, so that each split
-    // overlaps one tile's gather with the previous tile's softmax and PV
-    const int64_t max_splits = tiles >= 2 ? tiles / 2 : 1;
+    // A split's partial output (64 x 512 floats, written and merged) costs as
+    // much as gathering about a hundred rows, so splits keep two tiles each,
+    // except for a lone query, whose latency wants every split it can get.
+    const int64_t max_splits = (n_q == 1 || tiles < 2) ? tiles : tiles / 2;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
     const int64_t tiles_per = (tiles + splits - 1) / splits;
