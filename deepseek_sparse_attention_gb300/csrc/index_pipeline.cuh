@@ -51,7 +51,7 @@ struct Cfg {
     static constexpr uint32_t kBBoxBytes = N * kRowHalfBytes;
     static constexpr uint32_t kBBytes = 2 * kBBoxBytes;
     static constexpr uint32_t kTmemCols = 2 * N;                  // two accumulators
-    static constexpr int kEpiWarps = GQ == 1 ? 4 : 8;
+    static constexpr int kEpiWarps = GQ == 1 ? 4 : 16;          // 16: two queries per warpgroup
     static constexpr int kEpiGroups = kEpiWarps / 4;              // warpgroups in the epilogue
     static constexpr int kThreads = (4 + kEpiWarps) * 32;
     static constexpr uint32_t kOffA = 0;
@@ -274,15 +274,16 @@ __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap*
                 tmem_ld_32cols(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(ab * C::N + 32 * j), v);
                 // the query's head weights: warp-uniform addresses, one broadcast each
                 const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)(G.q0 + j) * kIdxHeads);
-                float s = 0.f;
+                // four partial sums (heads 4i, 4i+1, 4i+2, 4i+3 of each group of
+                // four), two packed FMAs per group: short dependency chains
+                float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
                 for (int h4 = 0; h4 < kIdxHeads / 4; ++h4) {
                     const float4 wv = __ldg(w4 + h4);
-                    s = fmaf(wv.x, fmaxf(v[4 * h4 + 0], 0.f), s);
-                    s = fmaf(wv.y, fmaxf(v[4 * h4 + 1], 0.f), s);
-                    s = fmaf(wv.z, fmaxf(v[4 * h4 + 2], 0.f), s);
-                    s = fmaf(wv.w, fmaxf(v[4 * h4 + 3], 0.f), s);
+                    fma2(a0, a1, wv.x, wv.y, fmaxf(v[4 * h4 + 0], 0.f), fmaxf(v[4 * h4 + 1], 0.f));
+                    fma2(b0, b1, wv.z, wv.w, fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f));
                 }
+                const float s = (a0 + a1) + (b0 + b1);
                 const int64_t nk = (int64_t)(G.L_last - (G.nq - 1 - j)) / kpool;
                 epi.emit(G, j, t_row, t_row < nk, u, row, s);
             }

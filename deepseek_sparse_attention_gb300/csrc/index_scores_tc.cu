@@ -15,8 +15,10 @@
 //   warp 1     MMA issuer: 8 x tcgen05.mma (K = 16 each) per tile into one of
 //              two TMEM accumulators, commits that free the stage and hand the
 //              accumulator to the epilogue;
-//   warps 4..  epilogue: tcgen05.ld of each key's 32 head dots (one TMEM lane
-//              per key), relu, weighted head sum, coalesced score stores.
+//   warps 4..  epilogue (4 warps for decode, 16 for a group of 8 queries:
+//              each warpgroup takes two of them): tcgen05.ld of each key's 32
+//              head dots (one TMEM lane per key), relu, weighted head sum with
+//              packed FMAs into four partial sums, coalesced score stores.
 // Decode streams every key once from HBM and is bound by HBM bandwidth; a
 // prefill chunk re-reads each key tile for every query group (from L2) and is
 // bound by the tensor pipe.

@@ -127,6 +127,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// (a0, a1) += (x0 * y0, x1 * y1): two independent fp32 FMAs in one packed
+// instruction, each rounded as fmaf would round it.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float y0, float y1) {
+    asm("{\n\t.reg .b64 x, y, a;\n\t"
+        "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 a, {%0, %1};\n\t"
+        "fma.rn.f32x2 a, x, y, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Allocate `ncols` TMEM columns (a power of two >= 32); the base address is
