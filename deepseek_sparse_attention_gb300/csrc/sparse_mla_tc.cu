@@ -339,18 +339,22 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         float* alpha_s = l_fin;
         if (head_owner) m_sh[hb + lane] = -INFINITY;
         bool ok = true;
+        // this thread's row index, read a tile ahead so that the load overlaps
+        // the previous tile's work (-1: no row)
+        auto row_index = [&](int t) -> int32_t {
+            const int64_t jrow = j0 + (int64_t)t * kTileRows + row;
+            return (has_row && t < n_tiles && jrow < j1) ? idx[q * idx_width + jrow] : -1;
+        };
+        int32_t r_cur = row_index(0);
         for (int t = 0; t < n_tiles; ++t) {
             const int bf = t & 1;
+            const int32_t r_next = row_index(t + 1);
             if (ok) ok = mbar_wait(&s_full[bf], (uint32_t)((t >> 1) & 1), kWaitNs);
             tc_fence_after();
             // rows past the split, and rows whose index is out of range (reported
             // by the loader), take no weight
-            const int64_t jrow = j0 + (int64_t)t * kTileRows + row;
-            bool valid = has_row && jrow < j1;
-            if (valid) {
-                const int32_t r = idx[q * idx_width + jrow];
-                valid = r >= 0 && r < qi.L;
-            }
+            const bool valid = r_cur >= 0 && r_cur < qi.L;
+            r_cur = r_next;
             float x[32];
             {
                 float v[32];
