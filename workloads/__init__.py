@@ -105,6 +105,11 @@ def named(name: str, seed: int = 0) -> Workload:
         return Workload(name, "bf16", [65536], [4096], top_k=2048, seed=seed,
                         description="4096 new queries after 61440 cached tokens (65536 rows), "
                                     "causal, top-k 2048, bf16, N(0,1)")
+    if name == "chunked_prefill_1024":
+        return Workload(name, "bf16", [65536], [1024], top_k=2048, seed=seed,
+                        description="1024 new queries after 64512 cached tokens (65536 rows), "
+                                    "causal, top-k 2048, bf16, N(0,1); the prefill chunk reduced "
+                                    "for profiling captures")
     if name == "kpool_nope_1m":
         return Workload(name, "bf16", [1048576] * 4, [1] * 4, top_k=2048, kpool=4, rope=0,
                         seed=seed,
