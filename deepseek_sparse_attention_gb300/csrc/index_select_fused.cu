@@ -68,6 +68,7 @@ constexpr int kOffCand = kOffCandN + 4;              // kCandCap x {key, index}
 constexpr int kQueryWords = kOffCand + 2 * kCandCap;
 static_assert(kQueryWords % 4 == 0 && kOffCand % 2 == 0, "alignment of the state");
 static_assert(kCandSpec % 256 == 0 && kCandSpec <= kCandCap, "speculative candidate reads");
+static_assert(kCandCap < (1 << 15), "two candidate counts share one 32-bit sum");
 
 struct SegState {          // one query's part of this CTA's unit range (48 bytes)
     int32_t q;
@@ -373,11 +374,22 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
     const uint32_t T = (pre << kBits3) | (uint32_t)red[kR0];
     const int need_eq = need - above2 - red[kR1];      // candidates equal to T that are kept
     for (int i = tid; i < kBins3; i += kThreads) hist[i] = 0;
-    // the last index taken at T: all of them when need_eq covers them, else
-    // the need_eq-th smallest index among them (indices are distinct)
-    int n_eq = 0;
-    for (int i = tid; i < n_cand; i += kThreads) n_eq += (uint32_t)cand[i].x == T;
-    n_eq = block_sum(n_eq, red);
+    // Candidates equal to T, and the kept candidates below this part's first
+    // index, assuming every candidate equal to T is kept (packed in one sum:
+    // both are below 2^15); when fewer are kept, the last index taken at T is
+    // the need_eq-th smallest among them (indices are distinct) and the
+    // second count is taken again.
+    int n_eq = 0, before = 0;
+    for (int i = tid; i < n_cand; i += kThreads) {
+        const uint32_t k = (uint32_t)cand[i].x;
+        n_eq += k == T;
+        before += cand[i].y < S.t_lo && k >= T;
+    }
+    {
+        const int packed = block_sum((before << 16) | n_eq, red);
+        n_eq = packed & 0xffff;
+        before = packed >> 16;
+    }
     int32_t t_last = 0x7fffffff;
     if (need_eq < n_eq) {
         if (tid == 0) red[kR0] = -1;
@@ -391,16 +403,14 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
         }
         __syncthreads();
         t_last = red[kR0];
+        before = 0;
+        for (int i = tid; i < n_cand; i += kThreads) {
+            const uint32_t k = (uint32_t)cand[i].x;
+            const int32_t ti = cand[i].y;
+            before += ti < S.t_lo && (k > T || (k == T && ti <= t_last));
+        }
+        before = block_sum(before, red);
     }
-    // offset: kept keys above b1 in earlier CTAs, plus kept candidates below
-    // this part's first index
-    int before = 0;
-    for (int i = tid; i < n_cand; i += kThreads) {
-        const uint32_t k = (uint32_t)cand[i].x;
-        const int32_t ti = cand[i].y;
-        before += ti < S.t_lo && (k > T || (k == T && ti <= t_last));
-    }
-    before = block_sum(before, red);
     if (tid < 32) sum_counts(cl, red);
     __syncthreads();
     const int base = red[kR2] + before;
@@ -448,8 +458,30 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int keep = top_k / kpool;
     const bool fits = u_end - u_begin <= (int64_t)kMaxCtaTiles;
 
-    // ---- this CTA's part of each sparse query, whole rows, candidate counters
+    // ---- before scoring: only what the epilogue needs, the first query this
+    // CTA selects for (its level-1 counts are taken while scoring)
     for (int i = tid; i < kBins1; i += kThreads) hist[i] = 0;
+    if (tid == 0) {
+        int hq = -1;
+        if (u_begin < u_end && fits) {
+            int64_t g = 0;
+            while (ts[g + 1] <= u_begin) ++g;
+            for (; g < n_groups && ts[g] < u_end && hq < 0; ++g)
+                if (ts[g + 1] > ts[g] && gs[g].L_last / kpool > keep) hq = gs[g].q0;
+        }
+        red[kRHistQ] = hq;
+    }
+    __syncthreads();
+
+    // ---- scores of this CTA's units (keys to global, level-1 counts of hist_q)
+    if (u_begin < u_end && fits) {
+        KeyStore epi{gkeys, ld, hist, red[kRHistQ]};
+        run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_end, w, kpool, epi, err);
+    }
+    fence_proxy_async_smem();                 // the ring is reused by generic accesses
+
+    // ---- this CTA's part of each sparse query (the first is hist_q's), whole
+    // rows, candidate counters
     if (tid == 0) {
         int ns = 0;
         if (!fits) record_error(err, kDevBadBatch, cta, 6);
@@ -477,7 +509,6 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             }
         }
         red[kRNseg] = ns;
-        red[kRHistQ] = ns > 0 ? seg[0].q : -1;
     }
     // rows one CTA writes whole: failed and dense queries; the tail and the
     // padding of sparse rows (the selected body is written by the emission).
@@ -509,13 +540,6 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
     __syncthreads();
     const int nseg = red[kRNseg];
-
-    // ---- scores of this CTA's units (keys to global, level-1 counts of hist_q)
-    if (u_begin < u_end && fits) {
-        KeyStore epi{gkeys, ld, hist, red[kRHistQ]};
-        run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_end, w, kpool, epi, err);
-    }
-    fence_proxy_async_smem();                 // the ring is reused by generic accesses
 
     // ---- keys back into shared memory (asynchronous copies, 16 bytes each:
     // part starts are tile-aligned and rows padded to 4 keys), level-1 counts
