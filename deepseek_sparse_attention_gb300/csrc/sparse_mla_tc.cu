@@ -53,7 +53,6 @@ constexpr uint32_t kRBlock = kTileRows * 128;       // one 64-column block of a 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;                       // S^T of buffer b: columns 64 b .. 64 b + 63
 constexpr uint32_t kOCol = 128;                     // O^T: 128 .. 383
-constexpr uint32_t kLoCol = 384;                    // P lo of buffer b, warpgroup g: 384 + 32 b + 16 g
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -68,13 +67,16 @@ struct Cfg {
     static constexpr uint32_t kOffQ = 0;
     static constexpr uint32_t kOffR = kCB * kQBlock;                 // two row buffers
     static constexpr uint32_t kBufBytes = kCB * kRBlock;
-    // P^T [64 rows x 64 heads] bf16 of buffer b: the buffer's rope block when
+    // P_hi^T [64 rows x 64 heads] bf16 of buffer b: the buffer's rope block when
     // there is one (no longer needed once the scores are formed), else its own.
-    static constexpr uint32_t kOffPx = kOffR + 2 * kBufBytes;         // NoPE: two P blocks
-    static constexpr uint32_t kOffBar = W == 576 ? kOffPx : kOffPx + 2 * kRBlock;
-    // q_full, drain, r_full[2], s_full[2], p_full[2], pv_hi[2], pv_done[2]
-    static constexpr uint32_t kOffRed = kOffBar + 128;          // [2][4][64] int
-    static constexpr uint32_t kOffL = kOffRed + 2 * 4 * 64 * 4; // [64] float
+    static constexpr uint32_t kOffPx = kOffR + 2 * kBufBytes;         // NoPE: two P_hi blocks
+    // P_lo^T: one block shared by the two buffers (a tile writes it once the
+    // previous tile's value products are done)
+    static constexpr uint32_t kOffPlo = W == 576 ? kOffPx : kOffPx + 2 * kRBlock;
+    static constexpr uint32_t kOffBar = kOffPlo + kRBlock;
+    // q_full, drain, r_full[2], s_full[2], p_full[2], pv_done[2]
+    static constexpr uint32_t kOffRed = kOffBar + 128;          // [4][64] int
+    static constexpr uint32_t kOffL = kOffRed + 4 * 64 * 4;     // [64] float
     static constexpr uint32_t kOffM = kOffL + 64 * 4;           // [64] float
     static constexpr uint32_t kOffMisc = kOffM + 64 * 4;
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
@@ -102,7 +104,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t *q_full = bars, *drain = bars + 1, *r_full = bars + 2, *s_full = bars + 4,
-             *p_full = bars + 6, *pv_hi = bars + 8, *pv_done = bars + 10;
+             *p_full = bars + 6, *pv_done = bars + 8;
     int* red = reinterpret_cast<int*>(smem + C::kOffRed);
     float* l_fin = reinterpret_cast<float*>(smem + C::kOffL);
     float* m_fin = reinterpret_cast<float*>(smem + C::kOffM);
@@ -140,7 +142,6 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             mbar_init(&r_full[i], kLoaders);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], kSoftmaxThreads);
-            mbar_init(&pv_hi[i], 1);
             mbar_init(&pv_done[i], 1);
         }
         fence_mbarrier_init();
@@ -261,9 +262,9 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             // Issue whatever is ready, in dependency order: the scores S(s) of
             // tile s once its rows are in (and at most one tile ahead of the
             // values, whose softmax frees the other score buffer), and the
-            // value products of tile v -- the P_hi pass, then the P_lo pass --
-            // as soon as the softmax hands each over.
-            int next_s = 0, next_v = 0, part = 0;
+            // value products of tile v -- on P_hi, then on P_lo -- as soon as
+            // the softmax hands both over.
+            int next_s = 0, next_v = 0;
             uint64_t t_prog = globaltimer_ns();
             while (ok && next_v < n_tiles) {
                 bool progressed = false;
@@ -286,30 +287,28 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                     ++next_s;
                     progressed = true;
                 }
-                if (next_v < next_s && mbar_test_wait(&p_full[next_v & 1], (uint32_t)part)) {
+                if (next_v < next_s &&
+                    mbar_test_wait(&p_full[next_v & 1], (uint32_t)((next_v >> 1) & 1))) {
                     // A = R^T: MN-major, 64-column blocks 8 KB apart, 8-row
                     // groups 1 KB apart.  B = P^T: MN-major, the 64 heads are one block.
                     tc_fence_after();
                     const int bv = next_v & 1;
                     const uint32_t r0 = smem_u32(smem + C::kOffR + bv * C::kBufBytes);
-                    const uint32_t p0 = smem_u32(smem + C::off_p(bv));
+                    for (int part = 0; part < 2; ++part) {
+                        const uint32_t p0 = smem_u32(smem + (part == 0 ? C::off_p(bv) : C::kOffPlo));
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                        for (int i = 0; i < 4; ++i) {
 #pragma unroll
-                        for (int kk = 0; kk < kTileRows / 16; ++kk) {
-                            mma_bf16_ss(tmem_base + kOCol + 64 * i,
-                                        sdesc_sw128(r0 + 2 * i * kRBlock + kk * 2048, kRBlock, 1024),
-                                        sdesc_sw128(p0 + kk * 2048, 1024, 1024), idesc_pv,
-                                        (next_v > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < kTileRows / 16; ++kk) {
+                                mma_bf16_ss(tmem_base + kOCol + 64 * i,
+                                            sdesc_sw128(r0 + 2 * i * kRBlock + kk * 2048, kRBlock, 1024),
+                                            sdesc_sw128(p0 + kk * 2048, 1024, 1024), idesc_pv,
+                                            (next_v > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                            }
                         }
                     }
-                    mma_commit(part == 0 ? &pv_hi[bv] : &pv_done[bv]);
-                    if (part == 0) {
-                        part = 1;
-                    } else {
-                        part = 0;
-                        ++next_v;
-                    }
+                    mma_commit(&pv_done[bv]);
+                    ++next_v;
                     progressed = true;
                 }
                 if (progressed) t_prog = globaltimer_ns();
@@ -378,7 +377,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             uint32_t any_raised = 0;
             if (any_exceed) {
                 // per-head maximum over the tile's 64 rows
-                int* rb = red + (t & 1) * 4 * kHeads + wq * kHeads + hb;
+                int* rb = red + wq * kHeads + hb;
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
                     const int mk = __reduce_max_sync(0xffffffffu, fkey(x[e]));
@@ -388,7 +387,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 uint32_t raised = 0;
                 if (head_owner) {                      // head hb + lane: raise its running maximum?
                     const int h = hb + lane;
-                    const int* rt = red + (t & 1) * 4 * kHeads;
+                    const int* rt = red;
                     const int mk = max(max(rt[h], rt[kHeads + h]), max(rt[2 * kHeads + h], rt[3 * kHeads + h]));
                     const float tmax = fval(mk), m_old = m_sh[h];
                     float a = 1.f;
@@ -428,11 +427,13 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
             }
             // this thread's half of its P^T row: 32 bf16 in the 128-byte swizzle
-            // layout.  p = hi + lo with hi = bf16(p), lo = bf16(p - hi); hi goes to
-            // shared memory now, lo waits in spare TMEM columns for the second pass.
+            // layout, twice: p = hi + lo with hi = bf16(p), lo = bf16(p - hi), so
+            // that the two value products carry P to ~2^-16 relative.  hi goes
+            // to the buffer's P block, lo to the shared P_lo block once the
+            // previous tile's value products (which read it) are done.
             uint8_t* prow = smem + C::off_p(bf) + row * 128;
-            const uint32_t lo_addr = lane_addr + kLoCol + 32 * bf + 16 * sg;
-            float lo_bits[16];
+            uint8_t* plow = smem + C::kOffPlo + row * 128;
+            uint32_t lo4[4][4];
 #pragma unroll
             for (int c16 = 0; c16 < 4; ++c16) {
                 uint32_t w4[4];
@@ -448,28 +449,21 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                     l_part[hl] += hf.x + lf.x;
                     l_part[hl + 1] += hf.y + lf.y;
                     w4[e] = *reinterpret_cast<const uint32_t*>(&hi);
-                    lo_bits[4 * c16 + e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&lo));
+                    lo4[c16][e] = *reinterpret_cast<const uint32_t*>(&lo);
                 }
                 const int chunk = 4 * sg + c16;
                 if (has_row)
                     *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
                         make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            tmem_st_16cols(lo_addr, lo_bits);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&p_full[bf]);
-            // second pass: the lo parts, once the hi product has read the buffer
-            if (ok) ok = mbar_wait(&pv_hi[bf], (uint32_t)((t >> 1) & 1), kWaitNs);
-            tc_fence_after();
-            tmem_ld_16cols(lo_addr, lo_bits);
+            if (t > 0 && ok)
+                ok = mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), kWaitNs);
 #pragma unroll
             for (int c16 = 0; c16 < 4; ++c16) {
                 const int chunk = 4 * sg + c16;
                 if (has_row)
-                    *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(__float_as_uint(lo_bits[4 * c16]), __float_as_uint(lo_bits[4 * c16 + 1]),
-                                   __float_as_uint(lo_bits[4 * c16 + 2]), __float_as_uint(lo_bits[4 * c16 + 3]));
+                    *reinterpret_cast<uint4*>(plow + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(lo4[c16][0], lo4[c16][1], lo4[c16][2], lo4[c16][3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
