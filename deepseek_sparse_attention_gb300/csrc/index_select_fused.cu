@@ -450,6 +450,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     SegState* seg = reinterpret_cast<SegState*>(smem + kOffSeg);
     int* red = reinterpret_cast<int*>(smem + kOffRed);
 
+    pdl_wait();                               // the inputs of the previous kernels
     const int64_t n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/6);
     const IdxGroup* gs = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
     const int64_t* ts = reinterpret_cast<const int64_t*>(smem + C::kOffPlanT);
@@ -777,14 +778,31 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    // Cooperative (every CTA resident: the grid barriers), and with programmatic
+    // stream serialization, so that the launch overlaps the previous kernel's
+    // tail; the kernel waits for it (griddepcontrol.wait) before reading
+    // anything.  Should a driver refuse the pair, the launch is cooperative only.
+    static bool pdl_ok = true;
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, index_select_fused, tm_k, tm_q, w, b, sh.top_k, sh.kpool,
-                              reinterpret_cast<uint32_t*>(scores), ld, idx, n_sel, sh.index_row_width(), gstate, gcnt,
-                              reinterpret_cast<unsigned long long*>(gbar), err);
+    auto go = [&](unsigned n_attr) {
+        cfg.numAttrs = n_attr;
+        return cudaLaunchKernelEx(&cfg, index_select_fused, tm_k, tm_q, w, b, sh.top_k, sh.kpool,
+                                  reinterpret_cast<uint32_t*>(scores), ld, idx, n_sel,
+                                  sh.index_row_width(), gstate, gcnt,
+                                  reinterpret_cast<unsigned long long*>(gbar), err);
+    };
+    if (pdl_ok) {
+        e = go(2);
+        if (e != cudaErrorNotSupported && e != cudaErrorInvalidValue) return e;
+        (void)cudaGetLastError();
+        pdl_ok = false;
+    }
+    return go(1);
 }
 
 }  // namespace dsa

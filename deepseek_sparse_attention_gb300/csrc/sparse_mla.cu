@@ -227,55 +227,52 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
 }
 
 // Log-sum-exp merge of the splits of one query: one CTA per (query, head), four
-// latent columns per thread.  Loads are issued eight splits at a time with no
-// data-dependent branch between them, so a thread waits for two rounds of
-// memory latency per eight splits rather than one per split.  An empty split
-// has m = -inf: weight 0, and its output (never written) is not used.
+// latent columns per thread.  Loads are issued sixteen splits at a time with no
+// data-dependent branch between them, so a thread waits for one round of
+// memory latency per sixteen splits; a running maximum rescales what is summed
+// so far.  An empty split has m = -inf: weight 0, and its output (never
+// written) is not used.
 __global__ void __launch_bounds__(128)
 merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __restrict__ part_ml,
              float* __restrict__ out, float* __restrict__ lse) {
     asm volatile("griddepcontrol.wait;" ::: "memory");      // the partials must be complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    constexpr int kB = 8;
+    constexpr int kB = 16;
     const int h = blockIdx.x, c4 = threadIdx.x;             // columns 4 c4 .. 4 c4 + 3
     const int64_t q = blockIdx.y;
     const float2* ml = reinterpret_cast<const float2*>(part_ml) + q * n_split * kHeads + h;
     const float4* po = reinterpret_cast<const float4*>(part_o) +
                        (q * n_split * kHeads + h) * (int64_t)(kLatent / 4) + c4;
     const int64_t o_stride = (int64_t)kHeads * (kLatent / 4);   // float4s between splits
-    float M = -INFINITY;
+    float M = -INFINITY, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < n_split; s0 += kB) {
         float2 v[kB];
+        float4 o[kB];
 #pragma unroll
-        for (int k = 0; k < kB; ++k)
-            v[k] = s0 + k < n_split ? __ldg(ml + (int64_t)(s0 + k) * kHeads)
-                                    : make_float2(-INFINITY, 0.f);
-#pragma unroll
-        for (int k = 0; k < kB; ++k) M = fmaxf(M, v[k].x);
-    }
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-        for (int s0 = 0; s0 < n_split; s0 += kB) {
-            float2 v[kB];
-            float4 o[kB];
-#pragma unroll
-            for (int k = 0; k < kB; ++k) {
-                const bool in = s0 + k < n_split;
-                v[k] = in ? __ldg(ml + (int64_t)(s0 + k) * kHeads) : make_float2(-INFINITY, 0.f);
-                o[k] = in ? __ldg(po + (int64_t)(s0 + k) * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int k = 0; k < kB; ++k) {
-                if (v[k].x == -INFINITY) continue;
-                const float f = expf(v[k].x - M);
-                L = fmaf(v[k].y, f, L);
-                acc.x = fmaf(o[k].x, f, acc.x);
-                acc.y = fmaf(o[k].y, f, acc.y);
-                acc.z = fmaf(o[k].z, f, acc.z);
-                acc.w = fmaf(o[k].w, f, acc.w);
-            }
+        for (int k = 0; k < kB; ++k) {
+            const bool in = s0 + k < n_split;
+            v[k] = in ? __ldg(ml + (int64_t)(s0 + k) * kHeads) : make_float2(-INFINITY, 0.f);
+            o[k] = in ? __ldg(po + (int64_t)(s0 + k) * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        float Mb = M;
+#pragma unroll
+        for (int k = 0; k < kB; ++k) Mb = fmaxf(Mb, v[k].x);
+        if (Mb == -INFINITY) continue;                      // no weight yet
+        const float r = expf(M - Mb);                       // 0 while M is -inf
+        L *= r;
+        acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+            if (v[k].x == -INFINITY) continue;              // empty split: its output is never read
+            const float f = expf(v[k].x - Mb);
+            L = fmaf(v[k].y, f, L);
+            acc.x = fmaf(o[k].x, f, acc.x);
+            acc.y = fmaf(o[k].y, f, acc.y);
+            acc.z = fmaf(o[k].z, f, acc.z);
+            acc.w = fmaf(o[k].w, f, acc.w);
+        }
+        M = Mb;
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     reinterpret_cast<float4*>(out)[(q * kHeads + h) * (int64_t)(kLatent / 4) + c4] =

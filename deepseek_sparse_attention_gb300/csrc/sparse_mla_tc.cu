@@ -115,11 +115,25 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     const int split = blockIdx.x;
     pdl_wait();                                       // the selection must be complete
     pdl_trigger();
+    // Three independent reads go out together: the selection count, a loader's
+    // indices of the first tile (whatever the count; unused past it) and the
+    // batch arrays.
+    const int64_t j0 = (int64_t)split * rows_per_split;
+    constexpr int kRowsPerPass = kLoaders / 8;
+    constexpr int kPasses = (kTileRows + kRowsPerPass - 1) / kRowsPerPass;
+    const int p_ld = warp == 0 ? lane : 32 * (warp - 1) + lane;    // loader slot (warps 0, 2, 3)
+    const int rsub = p_ld >> 3;
+    int64_t ns = n_sel[q];
+    int32_t idx_t0[kPasses];
+#pragma unroll
+    for (int ps = 0; ps < kPasses; ++ps) {
+        const int r = kRowsPerPass * ps + rsub;
+        idx_t0[ps] = (warp != 1 && warp < 4 && r < kTileRows && j0 + r < idx_width)
+                         ? idx[q * idx_width + j0 + r] : 0;
+    }
     QueryInfo qi;
     if (!query_info(b, q, qi, err, /*where=*/8)) return;
-    int64_t ns = n_sel[q];
     ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
-    const int64_t j0 = (int64_t)split * rows_per_split;
     const int64_t j1 = j0 + rows_per_split < ns ? j0 + rows_per_split : ns;
     if (j0 >= j1) {
         if (n_split == 1) {                           // no rows: out = 0, lse = -inf
@@ -163,10 +177,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         // time; then make them visible to the tensor core's async proxy and
         // arrive.  A thread's row indices for tile t + 1 are read while tile t
         // is copied, and tile t + 1 loads while tile t is in the softmax and PV.
-        const int p = warp == 0 ? lane : 32 * (warp - 1) + lane;
-        const int rsub = p >> 3, k8 = p & 7;
-        constexpr int kRowsPerPass = kLoaders / 8;
-        constexpr int kPasses = (kTileRows + kRowsPerPass - 1) / kRowsPerPass;
+        const int p = p_ld, k8 = p & 7;
         bool ok = true;
         if (p == 0) {
             mbar_arrive_expect_tx(q_full, C::kCB * kQBlock);
@@ -186,7 +197,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 const int64_t j = j0 + (int64_t)t * kTileRows + r;
                 int32_t rr = 0;
                 if (r < kTileRows && j < j1) {
-                    rr = irow[j];
+                    rr = t == 0 ? idx_t0[ps] : irow[j];
                     if (rr < 0 || rr >= qi.L) {
                         record_error(err, kDevBadIndex, (int32_t)q, /*where=*/8);
                         rr = 0;
