@@ -51,6 +51,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true",
+                   help="launch each step on the stream instead of replaying CUDA graphs")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU work of the oracle baseline sample")
     return p.parse_args(argv)
@@ -390,10 +392,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     keys, caches = d["k_idx_copies"], d["cache_copies"]
 
-    def step(i):
+    def launch(i, st):
         c = i % copies
         dsa.dsa_decode_step(sh, b, d["q_idx"], d["w"], keys[c], d["q_abs"], caches[c], out, lse,
-                            idx, n_sel, ws, stream)
+                            idx, n_sel, ws, st)
+
+    def step(i):
+        launch(i, stream)
 
     # default step count: about two seconds of timed work
     warm = args.warmup if args.warmup is not None else 20
@@ -402,12 +407,47 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     if dsa.dsa_check_device_error(ws, stream) != 0:
         raise RuntimeError("device error during warm-up")
+    # A decode loop replays its step from CUDA graphs (the launches of a step
+    # and of consecutive steps then overlap through programmatic dependent
+    # launch without host round trips): one graph of G steps over the input
+    # copies in turn, and one single-step graph per copy for the remainder, so
+    # that exactly K steps run.
+    run_steps = None
+    launch_mode = "stream launches"
+    if not args.no_graph:
+        G = copies * max(1, 12 // copies)
+        g_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_all):
+            for i in range(G):
+                launch(i, torch.cuda.current_stream(dev))
+        g_one = []
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                launch(c, torch.cuda.current_stream(dev))
+            g_one.append(g)
+
+        def run_steps(n):
+            for _ in range(n // G):
+                g_all.replay()
+            for i in range(n % G):
+                g_one[i % copies].replay()
+
+        run_steps(G)                                 # untimed: the graphs' first replays
+        torch.cuda.synchronize(dev)
+        if dsa.dsa_check_device_error(ws, stream) != 0:
+            raise RuntimeError("device error in the graph warm-up")
+        launch_mode = f"CUDA graphs of {G} steps (+ single-step graphs for the remainder)"
+    else:
+        def run_steps(n):
+            for i in range(n):
+                step(i)
+
     if args.steps is None:
         t0 = time.perf_counter()
-        for i in range(20):
-            step(i)
+        run_steps(60)
         torch.cuda.synchronize(dev)
-        per = (time.perf_counter() - t0) / 20
+        per = (time.perf_counter() - t0) / 60
         steps = int(min(200000, max(20, 2.0 / max(per, 1e-7))))
     else:
         steps = args.steps
@@ -420,8 +460,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(steps):
-        step(i)
+    run_steps(steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     if pg:
@@ -535,7 +574,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": max(warm, 3), "ms_per_step": per_step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": workload_config(wl, world),
+        "config": dict(workload_config(wl, world), launch=launch_mode),
         "tokens_per_s": work["scored_keys"] / (per_step_ms / 1e3) * world,
         "step_hbm_gbs": work["compulsory_bytes"] / (per_step_ms / 1e3) / 1e9,
         "step_hbm_frac": work["compulsory_bytes"] / (per_step_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
