@@ -600,18 +600,20 @@ bool sparse_mla_tc_eligible(const Shape& sh, const BatchDev& b) {
            b.total_rows < ((int64_t)1 << 31) && (int64_t)b.n_q * kHeads < ((int64_t)1 << 31);
 }
 
-// Tiles of 64 rows; enough CTAs (one per SM) to fill the GPU about twice.
+// Tiles of 64 rows; at most one CTA per SM in a single wave.  A split's
+// partial output (64 x 512 floats, written and merged) costs about as much as
+// gathering a hundred rows, and a second wave of CTAs costs a wave's tiles, so
+// a batch takes the most splits per query that still fit one wave (64 ragged
+// decode queries: 2 splits, 128 CTAs, measured faster than 4 or 5 over two or
+// three waves).  Splits keep two tiles each, except for a lone query, whose
+// latency wants every split it can get.
 void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
                               int32_t* rows_per_split, int32_t* n_split) {
     int64_t max_rows = sh.index_row_width();
     if (max_kv_len < max_rows) max_rows = max_kv_len;
     if (max_rows < 1) max_rows = 1;
     const int64_t tiles = (max_rows + kTileRows - 1) / kTileRows;
-    const int64_t target_ctas = 2 * 152;
-    int64_t splits = (target_ctas + n_q - 1) / n_q;
-    // A split's partial output (64 x 512 floats, written and merged) costs as
-    // much as gathering about a hundred rows, so splits keep two tiles each,
-    // except for a lone query, whose latency wants every split it can get.
+    int64_t splits = n_q <= 152 ? 152 / n_q : 1;
     const int64_t max_splits = (n_q == 1 || tiles < 2) ? tiles : tiles / 2;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
