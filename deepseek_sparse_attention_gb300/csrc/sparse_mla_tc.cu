@@ -60,6 +60,9 @@ constexpr float kSlack = 8.f;                       // lazy rescale threshold (l
 constexpr int kLoaders = 96;                        // threads that gather rows
 constexpr int kSoftmaxThreads = 256;                // two warpgroups
 constexpr int kThreads = 128 + kSoftmaxThreads;     // loaders + MMA warp, then softmax
+constexpr int kIssuers = kLoaders + kSoftmaxThreads; // threads that copy rows: 352
+constexpr int kRowSlots = kIssuers / 8;             // rows a tile's copy round covers: 44
+static_assert(kIssuers % 8 == 0 && 2 * kRowSlots >= 64, "two rows per slot cover a tile");
 
 template <int W>
 struct Cfg {
@@ -115,22 +118,22 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     const int split = blockIdx.x;
     pdl_wait();                                       // the selection must be complete
     pdl_trigger();
-    // Three independent reads go out together: the selection count, a loader's
-    // indices of the first tile (whatever the count; unused past it) and the
-    // batch arrays.
+    // Row gather slots: every thread but the MMA warp's copies rows -- eight
+    // threads per row (one 16-byte piece of each 64-column block's 128-byte
+    // line), kIssuers / 8 rows at a time: slot s takes rows s / 8 and, where
+    // it exists, s / 8 + kRowSlots of each tile.
+    const int slot = warp == 0 ? lane : (warp < 4 ? 32 * (warp - 1) + lane : threadIdx.x - 32);
+    const int rs = slot >> 3, k8 = slot & 7;
+    const bool issuer = warp != 1;
+    const bool two_rows = rs + kRowSlots < kTileRows;
+    // Three independent reads go out together: the selection count, this
+    // thread's indices of the first tile (whatever the count; unused past it)
+    // and the batch arrays.
     const int64_t j0 = (int64_t)split * rows_per_split;
-    constexpr int kRowsPerPass = kLoaders / 8;
-    constexpr int kPasses = (kTileRows + kRowsPerPass - 1) / kRowsPerPass;
-    const int p_ld = warp == 0 ? lane : 32 * (warp - 1) + lane;    // loader slot (warps 0, 2, 3)
-    const int rsub = p_ld >> 3;
     int64_t ns = n_sel[q];
-    int32_t idx_t0[kPasses];
-#pragma unroll
-    for (int ps = 0; ps < kPasses; ++ps) {
-        const int r = kRowsPerPass * ps + rsub;
-        idx_t0[ps] = (warp != 1 && warp < 4 && r < kTileRows && j0 + r < idx_width)
-                         ? idx[q * idx_width + j0 + r] : 0;
-    }
+    int32_t ia = issuer && j0 + rs < idx_width ? idx[q * idx_width + j0 + rs] : 0;
+    int32_t ib = issuer && two_rows && j0 + rs + kRowSlots < idx_width
+                     ? idx[q * idx_width + j0 + rs + kRowSlots] : 0;
     QueryInfo qi;
     if (!query_info(b, q, qi, err, /*where=*/8)) return;
     ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
@@ -153,7 +156,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         mbar_init(q_full, 1);
         mbar_init(drain, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&r_full[i], kLoaders);
+            mbar_init(&r_full[i], kIssuers);
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], kSoftmaxThreads);
             mbar_init(&pv_done[i], 1);
@@ -170,50 +173,93 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // Copies of this thread's rows of tile t (indices ra, rb read from the
+    // selection) into buffer t % 2 in the 128-byte swizzle layout; the
+    // buffer's r_full barrier counts this thread's arrival once they have all
+    // landed (cp.async.mbarrier.arrive), so no thread waits for its copies.
+    // Rows past the split, and indices out of range (reported), copy row 0 of
+    // the sequence, which the softmax gives no weight.
+    const unsigned char* cbase = static_cast<const unsigned char*>(cache);
+    auto issue_rows = [&](int t, int32_t ra, int32_t rb) {
+        const uint32_t rbase = smem_u32(smem + C::kOffR + (t & 1) * C::kBufBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = rs + h * kRowSlots;
+            if (r >= kTileRows) continue;
+            const int64_t j = j0 + (int64_t)t * kTileRows + r;
+            int32_t rr = h == 0 ? ra : rb;
+            if (j >= j1) {
+                rr = 0;
+            } else if (rr < 0 || rr >= qi.L) {
+                record_error(err, kDevBadIndex, (int32_t)q, /*where=*/8);
+                rr = 0;
+            }
+            const unsigned char* src = cbase + ((qi.row0 + rr) * W + k8 * 8) * 2;
+            const uint32_t dst = rbase + r * 128 + ((k8 ^ (r & 7)) << 4);
+#pragma unroll
+            for (int cb = 0; cb < C::kCB; ++cb)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             ::"r"(dst + cb * kRBlock), "l"(src + cb * 128)
+                             : "memory");
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
+                     ::"r"(smem_u32(&r_full[t & 1]))
+                     : "memory");
+    };
+    // this thread's indices of tile t (read a tile ahead of their copies)
+    auto fetch_rows = [&](int t, int32_t& ra, int32_t& rb) {
+        const int64_t j = j0 + (int64_t)t * kTileRows + rs;
+        ra = j < j1 ? idx[q * idx_width + j] : 0;
+        rb = two_rows && j + kRowSlots < j1 ? idx[q * idx_width + j + kRowSlots] : 0;
+    };
+    if (issuer) issue_rows(0, ia, ib);
+
     if (warp != 1 && warp < 4) {                                      // ---- loads
-        // warps 0, 2, 3: 96 threads copy each tile's rows with 16-byte cp.async
-        // into the 128-byte swizzle layout of buffer t % 2, eight threads per
-        // row (one 128-byte line of a 64-column block each), twelve rows at a
-        // time; then make them visible to the tensor core's async proxy and
-        // arrive.  A thread's row indices for tile t + 1 are read while tile t
-        // is copied, and tile t + 1 loads while tile t is in the softmax and PV.
-        const int p = p_ld, k8 = p & 7;
+        // warps 0, 2, 3: the query once (TMA tiles), their share of the
+        // second tile at once, then tile t + 1 as soon as its buffer is free
+        // (the PV of tile t - 1 has completed).
         bool ok = true;
-        if (p == 0) {
+        if (slot == 0) {
             mbar_arrive_expect_tx(q_full, C::kCB * kQBlock);
             for (int cb = 0; cb < C::kCB; ++cb)
                 tma_load_2d(smem + C::kOffQ + cb * kQBlock, &tm_q, q_full, 64 * cb,
                             (int32_t)(q * kHeads));
         }
-        const int32_t* irow = idx + q * idx_width;
-        const unsigned char* cbase = static_cast<const unsigned char*>(cache);
-        // cache rows of this thread's rows of tile t (row 0 of the sequence
-        // past the selection or for an index out of range, which the softmax
-        // gives no weight)
-        auto rows_of = [&](int t, int64_t (&rows)[kPasses]) {
+        // From the third tile on the loaders copy whole tiles alone (eight
+        // threads per row, twelve rows a pass), keeping the softmax warps' time
+        // for the softmax; those arrive on the barrier without copies.
+        constexpr int kRowsPerPass = kLoaders / 8;
+        constexpr int kPasses = (kTileRows + kRowsPerPass - 1) / kRowsPerPass;
+        const int rsub = slot >> 3;
+        for (int t = 0; t + 1 < n_tiles && ok; ++t) {
+            if (t == 0) {
+                fetch_rows(1, ia, ib);
+                issue_rows(1, ia, ib);
+                continue;
+            }
+            int32_t rr[kPasses];
 #pragma unroll
             for (int ps = 0; ps < kPasses; ++ps) {
                 const int r = kRowsPerPass * ps + rsub;
-                const int64_t j = j0 + (int64_t)t * kTileRows + r;
-                int32_t rr = 0;
-                if (r < kTileRows && j < j1) {
-                    rr = t == 0 ? idx_t0[ps] : irow[j];
-                    if (rr < 0 || rr >= qi.L) {
-                        record_error(err, kDevBadIndex, (int32_t)q, /*where=*/8);
-                        rr = 0;
-                    }
-                }
-                rows[ps] = qi.row0 + rr;
+                const int64_t j = j0 + (int64_t)(t + 1) * kTileRows + r;
+                rr[ps] = r < kTileRows && j < j1 ? idx[q * idx_width + j] : 0;
             }
-        };
-        // copies of tile t into buffer t % 2 (one cp.async group per tile)
-        auto issue = [&](int t, const int64_t (&rows)[kPasses]) {
-            const uint32_t rbase = smem_u32(smem + C::kOffR + (t & 1) * C::kBufBytes);
+            ok = mbar_wait(&pv_done[(t + 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), kWaitNs);
+            if (!ok) break;
+            const uint32_t rbase = smem_u32(smem + C::kOffR + ((t + 1) & 1) * C::kBufBytes);
 #pragma unroll
             for (int ps = 0; ps < kPasses; ++ps) {
                 const int r = kRowsPerPass * ps + rsub;
                 if (r >= kTileRows) continue;
-                const unsigned char* src = cbase + (rows[ps] * W + k8 * 8) * 2;
+                const int64_t j = j0 + (int64_t)(t + 1) * kTileRows + r;
+                int32_t row = rr[ps];
+                if (j >= j1) {
+                    row = 0;
+                } else if (row < 0 || row >= qi.L) {
+                    record_error(err, kDevBadIndex, (int32_t)q, /*where=*/8);
+                    row = 0;
+                }
+                const unsigned char* src = cbase + ((qi.row0 + row) * W + k8 * 8) * 2;
                 const uint32_t dst = rbase + r * 128 + ((k8 ^ (r & 7)) << 4);
 #pragma unroll
                 for (int cb = 0; cb < C::kCB; ++cb)
@@ -221,49 +267,12 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                                  ::"r"(dst + cb * kRBlock), "l"(src + cb * 128)
                                  : "memory");
             }
-            asm volatile("cp.async.commit_group;" ::: "memory");
-        };
-        // The next tile's copies go out before this tile's are awaited when
-        // its buffer is already free (always for the second tile), so that two
-        // tiles' rows are in flight; otherwise after this tile's arrival.
-        int64_t rows_t[kPasses];
-        rows_of(0, rows_t);
-        issue(0, rows_t);
-        int issued = 1;
-        for (int t = 0; t < n_tiles && ok; ++t) {
-            if (issued == t + 1 && t + 1 < n_tiles &&
-                (t + 1 < 2 ||
-                 mbar_test_wait(&pv_done[(t + 1) & 1], (uint32_t)(((t - 1) >> 1) & 1)))) {
-                rows_of(t + 1, rows_t);
-                issue(t + 1, rows_t);
-                ++issued;
-            }
-            if (issued == t + 2) asm volatile("cp.async.wait_group 1;" ::: "memory");
-            else asm volatile("cp.async.wait_group 0;" ::: "memory");
-            fence_proxy_async_smem();
-            mbar_arrive(&r_full[t & 1]);
-            if (issued == t + 1 && t + 1 < n_tiles) {
-                rows_of(t + 1, rows_t);
-                // the buffer's previous tile (t - 1) must be through its PV
-                if (t >= 1) ok = mbar_wait(&pv_done[(t + 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), kWaitNs);
-            }
-            {   // all loaders agree on whether to proceed
-                uint32_t all_ok;
-                asm volatile(
-                    "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-                    "bar.red.and.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-                    : "=r"(all_ok)
-                    : "r"((uint32_t)ok), "n"(kLoaders)
-                    : "memory");
-                ok = all_ok != 0;
-            }
-            if (ok && issued == t + 1 && t + 1 < n_tiles) {
-                issue(t + 1, rows_t);
-                ++issued;
-            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
+                         ::"r"(smem_u32(&r_full[(t + 1) & 1]))
+                         : "memory");
         }
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        if (!ok && p == 0) record_error(err, kDevTimeout, (int32_t)q, /*where=*/9);
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (!ok && slot == 0) record_error(err, kDevTimeout, (int32_t)q, /*where=*/9);
     } else if (warp == 1) {                                           // ---- MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kTileRows, kHeads);
@@ -281,7 +290,10 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 bool progressed = false;
                 if (next_s < n_tiles && next_s <= next_v + 1 &&
                     mbar_test_wait(&r_full[next_s & 1], (uint32_t)((next_s >> 1) & 1))) {
-                    // S^T(s) = R(s) Q^T: M = 64 rows, N = 64 heads, K = the row width
+                    // S^T(s) = R(s) Q^T: M = 64 rows, N = 64 heads, K = the row width.
+                    // The rows were written by cp.async (generic proxy): fence
+                    // before the tensor core (async proxy) reads them.
+                    fence_proxy_async_smem();
                     tc_fence_after();
                     const int bs = next_s & 1;
                     const uint32_t r0 = smem_u32(smem + C::kOffR + bs * C::kBufBytes);
@@ -355,10 +367,19 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             const int64_t jrow = j0 + (int64_t)t * kTileRows + row;
             return (has_row && t < n_tiles && jrow < j1) ? idx[q * idx_width + jrow] : -1;
         };
+        // this thread's copies of tile 1 (its buffer is free from the start)
+        if (n_tiles > 1) {
+            fetch_rows(1, ia, ib);
+            issue_rows(1, ia, ib);
+        }
         int32_t r_cur = row_index(0);
         for (int t = 0; t < n_tiles; ++t) {
             const int bf = t & 1;
             const int32_t r_next = row_index(t + 1);
+            // tiles from the third on are copied by the loaders alone: this
+            // thread's arrival for tile t + 1 (its buffer's previous phase,
+            // tile t - 1, completed before this tile's scores)
+            if (t >= 1 && t + 1 < n_tiles) mbar_arrive(&r_full[(t + 1) & 1]);
             if (ok) ok = mbar_wait(&s_full[bf], (uint32_t)((t >> 1) & 1), kWaitNs);
             tc_fence_after();
             // rows past the split, and rows whose index is out of range (reported
@@ -480,6 +501,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             tc_fence_before();
             mbar_arrive(&p_full[bf]);
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
         {
             const int tl = n_tiles - 1;
             if (ok) ok = mbar_wait(&pv_done[tl & 1], (uint32_t)((tl >> 1) & 1), kWaitNs);

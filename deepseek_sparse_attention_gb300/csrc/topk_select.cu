@@ -279,20 +279,27 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
                 const int64_t t = base + lane + 32 * r;
                 v[r] = t < n ? __ldg(sc + t) : -INFINITY;
             }
+            // the round's hits counted, one slot allocation per warp for all of
+            // them, then (ballots again) each hit's slot
+            int n_hit = 0;
 #pragma unroll
-            for (int r = 0; r < kBatch; ++r) {
-                const uint32_t hit = __ballot_sync(0xffffffffu, v[r] >= t_lo);
-                if (hit) {
-                    int slot0 = 0;
-                    if (lane == 0) slot0 = atomicAdd(s_count, __popc(hit));
-                    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+            for (int r = 0; r < kBatch; ++r) n_hit += __popc(__ballot_sync(0xffffffffu, v[r] >= t_lo));
+            if (n_hit) {
+                int slot = 0;
+                if (lane == 0) slot = atomicAdd(s_count, n_hit);
+                slot = __shfl_sync(0xffffffffu, slot, 0);
+                const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+                for (int r = 0; r < kBatch; ++r) {
+                    const uint32_t hit = __ballot_sync(0xffffffffu, v[r] >= t_lo);
                     if ((hit >> lane) & 1u) {
-                        const int slot = slot0 + __popc(hit & ((1u << lane) - 1u));
-                        if (slot < kCandCap) {
-                            cand_key[slot] = order_key(v[r]);
-                            cand_idx[slot] = (int32_t)(base + lane + 32 * r);
+                        const int sl = slot + __popc(hit & below);
+                        if (sl < kCandCap) {
+                            cand_key[sl] = order_key(v[r]);
+                            cand_idx[sl] = (int32_t)(base + lane + 32 * r);
                         }
                     }
+                    slot += __popc(hit);
                 }
             }
         }
