@@ -25,7 +25,11 @@
 // holds (many equal or adversarially ordered scores), the CTA falls back to
 // three radix levels over the scores in global memory and an emission pass that
 // re-reads them; queries too long for the shared bitmaps use that path.
+#include <cooperative_groups.h>
+
 #include "dsa_kernels.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 namespace {
@@ -203,7 +207,12 @@ __device__ void select_multilevel(const float* __restrict__ sc, int64_t n, int64
     *n_out = out_base;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// CL CTAs per query (1, or a cluster of 2): CTA rank r streams, marks and
+// emits the r-th half of the row; the two exchange their candidates through
+// distributed shared memory, so each finds the same threshold, and the second
+// starts its output after the first half's selections.
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
 topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __restrict__ scores,
                    int64_t ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
                    int64_t width, int32_t bitmap_words, int32_t* err) {
@@ -219,14 +228,18 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
     uint32_t* eq_bits = sel_bits + bitmap_words;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t q = blockIdx.x;
+    const int64_t q = CL == 1 ? blockIdx.x : blockIdx.y;
+    const int rank = CL == 1 ? 0 : (int)cg::this_cluster().block_rank();
     int32_t* out = idx + q * width;
     asm volatile("griddepcontrol.wait;" ::: "memory");      // the scores must be complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     QueryInfo qi;
+    // (every CTA of a cluster takes the same branches up to the exchange)
     if (!query_info(b, q, qi, err, /*where=*/2)) {
-        for (int64_t i = tid; i < width; i += kThreads) out[i] = -1;
-        if (tid == 0) n_sel[q] = 0;
+        if (rank == 0) {
+            for (int64_t i = tid; i < width; i += kThreads) out[i] = -1;
+            if (tid == 0) n_sel[q] = 0;
+        }
         return;
     }
     const int64_t L = qi.L;
@@ -234,16 +247,23 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
     const int64_t keep = top_k / kpool;     // how many of them it keeps
 
     if (n <= keep) {                        // dense: every visible row
-        for (int64_t i = tid; i < width; i += kThreads) out[i] = i < L ? (int32_t)i : -1;
-        if (tid == 0) n_sel[q] = (int32_t)L;
+        if (rank == 0) {
+            for (int64_t i = tid; i < width; i += kThreads) out[i] = i < L ? (int32_t)i : -1;
+            if (tid == 0) n_sel[q] = (int32_t)L;
+        }
         return;
     }
     const float* sc = scores + q * ld;
     int64_t n_out = 0;
-    const int64_t words = (n + 31) / 32;
-
+    // this CTA's part of the row: [lo, hi), a whole number of bitmap words
+    const int64_t half = CL == 1 ? n : ((n + 1) / 2 + 31) / 32 * 32;
+    const int64_t lo = rank * half;
+    const int64_t hi = lo + half < n ? lo + half : n;
+    const int64_t words = (hi - lo + 31) / 32;
+    const int64_t words_first = ((half < n ? half : n) + 31) / 32;   // the larger part, for
+                                                                      // a decision both CTAs share
     bool done = false;
-    if (words <= bitmap_words) {
+    if (words_first <= bitmap_words) {
         // ---- a lower bound t_lo on the k-th largest score from a strided sample:
         // the key (to 22 bits) of the sample element ranked at 1.5x the kept
         // fraction plus a margin, found by two radix levels over the sample.
@@ -270,14 +290,14 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
         const float t_lo = key_to_float((sb1 << 21) | (*s_digit << 10));
         __syncthreads();
 
-        // ---- one streaming pass: every score >= t_lo becomes a candidate
-        for (int64_t base = (int64_t)warp * 32 * kBatch; base < n;
+        // ---- one streaming pass over [lo, hi): every score >= t_lo becomes a candidate
+        for (int64_t base = lo + (int64_t)warp * 32 * kBatch; base < hi;
              base += (int64_t)kWarps * 32 * kBatch) {
             float v[kBatch];
 #pragma unroll
             for (int r = 0; r < kBatch; ++r) {
                 const int64_t t = base + lane + 32 * r;
-                v[r] = t < n ? __ldg(sc + t) : -INFINITY;
+                v[r] = t < hi ? __ldg(sc + t) : -INFINITY;
             }
             // the round's hits counted, one slot allocation per warp for all of
             // them, then (ballots again) each hit's slot
@@ -305,7 +325,25 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
         }
         for (int64_t w = tid; w < words; w += kThreads) { sel_bits[w] = 0; eq_bits[w] = 0; }
         __syncthreads();
-        const int n_cand = *s_count;
+        int n_cand = *s_count;
+        if (CL == 2) {
+            // the peer's candidates after this CTA's own: both hold the whole list
+            cg::cluster_group cluster = cg::this_cluster();
+            cluster.sync();                              // both passes are complete
+            const int* peer_count = cluster.map_shared_rank(s_count, rank ^ 1);
+            const int n_peer = *peer_count;
+            const int n_all = n_cand + n_peer;
+            if (n_cand <= kCandCap && n_all <= kCandCap) {
+                const uint32_t* pk = cluster.map_shared_rank(cand_key, rank ^ 1);
+                const int32_t* pi = cluster.map_shared_rank(cand_idx, rank ^ 1);
+                for (int i = tid; i < n_peer; i += kThreads) {
+                    cand_key[n_cand + i] = pk[i];
+                    cand_idx[n_cand + i] = pi[i];
+                }
+            }
+            cluster.sync();                              // no DSMEM reads after this
+            n_cand = n_all;
+        }
         __syncthreads();
         if (n_cand >= keep && n_cand <= kCandCap) {
             // ---- exact k-th key T among the candidates (three radix levels)
@@ -332,15 +370,33 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
                 __syncthreads();
             }
             const uint32_t T = prefix;
+            // this part's candidates into the bitmaps; the earlier part's
+            // selections (keys above T, and how many equal to T) for the offsets
+            int gt_before = 0, eq_before = 0;
             for (int i = tid; i < n_cand; i += kThreads) {
                 const uint32_t key = cand_key[i];
                 const int32_t t = cand_idx[i];
-                if (key > T) atomicOr(&sel_bits[t >> 5], 1u << (t & 31));
-                else if (key == T) atomicOr(&eq_bits[t >> 5], 1u << (t & 31));
+                if (t < lo) {
+                    gt_before += key > T;
+                    eq_before += key == T;
+                } else if (t < hi) {
+                    const int32_t u = (int32_t)(t - lo);
+                    if (key > T) atomicOr(&sel_bits[u >> 5], 1u << (u & 31));
+                    else if (key == T) atomicOr(&eq_bits[u >> 5], 1u << (u & 31));
+                }
+            }
+            int64_t eq_base = 0, out_base = 0;
+            if (CL == 2 && rank > 0) {
+                int tot;
+                block_exclusive_scan(gt_before, &tot, warp_sums);
+                gt_before = tot;
+                block_exclusive_scan(eq_before, &tot, warp_sums);
+                eq_before = tot;
+                eq_base = eq_before;
+                out_base = gt_before + (eq_before < k_rem ? eq_before : k_rem);
             }
             __syncthreads();
             // ---- emission in ascending order: keys > T, then the first k_rem keys == T
-            int64_t eq_base = 0, out_base = 0;
             for (int64_t w0 = 0; w0 < words; w0 += kThreads) {
                 const int64_t w = w0 + tid;
                 const uint32_t sw = w < words ? sel_bits[w] : 0u;
@@ -358,7 +414,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
                 while (comb != 0u && pos < keep) {
                     const int bit = __ffs(comb) - 1;
                     comb &= comb - 1u;
-                    put(out, pos++, w * 32 + bit, kpool);
+                    put(out, pos++, lo + w * 32 + bit, kpool);
                 }
                 eq_base += eq_total;
                 out_base += sel_total;
@@ -367,9 +423,13 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
             done = true;
         }
     }
-    if (!done)
+    if (!done) {                            // the whole row, by the first CTA alone
+        if (rank > 0) return;
         select_multilevel(sc, n, keep, kpool, out, hist, warp_sums, s_digit, s_above, &n_out);
-    if (tid == 0 && n_out != keep) record_error(err, kDevBadIndex, (int32_t)q, /*where=*/2);
+    }
+    if (tid == 0 && rank == (done ? CL - 1 : 0) && n_out != keep)
+        record_error(err, kDevBadIndex, (int32_t)q, /*where=*/2);
+    if (rank > 0) return;
 
     // ---- unfilled tail (k-pool), then padding
     const int64_t body = keep * kpool;
@@ -382,23 +442,32 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
 
 }  // namespace
 
+// Two CTAs per query when that still fits one wave and the rows are long
+// enough for the halves to pay for the exchange.
+bool topk_pair_eligible(const Shape& sh, const BatchDev& b) {
+    return b.n_q >= 1 && 2 * (int64_t)b.n_q <= 152 && b.max_kv_len / sh.kpool >= 16384;
+}
+
 cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* scores,
                                int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
                                cudaStream_t st) {
     if (b.n_q == 0) return cudaSuccess;
     if (topk_cluster_eligible(sh, b))
         return launch_topk_select_cluster(sh, b, scores, ld, idx, n_sel, err, st);
-    // Bitmaps for the longest query if they fit; otherwise every query that
-    // needs more takes the multi-level path.
-    int64_t words = (b.max_kv_len / sh.kpool + 31) / 32;
+    const bool pair = topk_pair_eligible(sh, b);
+    // Bitmaps for the longest query's (first) part if they fit; otherwise
+    // every query that needs more takes the multi-level path.
+    const int64_t n_max = b.max_kv_len / sh.kpool;
+    const int64_t part = pair ? ((n_max + 1) / 2 + 31) / 32 * 32 : n_max;
+    int64_t words = (part + 31) / 32;
     if (kFixedSmem + (size_t)words * 8 > kMaxSmem) words = 0;
     const size_t smem = kFixedSmem + (size_t)words * 8;
-    cudaError_t e = cudaFuncSetAttribute(topk_select_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = pair ? topk_select_kernel<2> : topk_select_kernel<1>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(topk_select_kernel, dim3((unsigned)b.n_q), dim3(kThreads), smem, st, b,
-                      sh.top_k, sh.kpool, scores, ld, idx, n_sel, sh.index_row_width(),
-                      (int32_t)words, err);
+    const dim3 grid = pair ? dim3(2, (unsigned)b.n_q) : dim3((unsigned)b.n_q);
+    return launch_pdl(kern, grid, dim3(kThreads), smem, st, b, sh.top_k, sh.kpool, scores, ld, idx,
+                      n_sel, sh.index_row_width(), (int32_t)words, err);
 }
 
 }  // namespace dsa

@@ -33,6 +33,9 @@ SMALL = [
     workloads.small("fp32_kpool", [777, 130], top_k=64, kpool=4, rope=0, dtype="f32"),
     workloads.small("mixed_chunks", [3000, 2100, 900, 5000], q_lens=[1, 37, 1, 8], top_k=256),
     workloads.small("small_chunk", [600], q_lens=[5], top_k=128),
+    # 24 decode queries with long rows: selection by a pair of CTAs per query
+    workloads.small("pair_select_batch", [16384 + 997 * i for i in range(22)] + [1500, 40001],
+                    top_k=2048, seed=9),
 ]
 
 
@@ -137,6 +140,31 @@ def test_topk_select_bit_exact(kind):
     for i, L in enumerate(L_list):
         ref = oracle.topk(s[i, :L].astype(np.float64), top_k)
         assert np.array_equal(idx[i, : n_sel[i]], ref)
+
+
+@pytest.mark.parametrize("kind", ["normal", "int_ties", "all_zero", "signed_zeros"])
+def test_topk_select_pair_bit_exact(kind):
+    """24 queries with long rows take two CTAs per query (each half of the row,
+    candidates exchanged): the same bit-exact selection, ties included, with
+    odd lengths, a dense row and a row at the split boundary."""
+    rng = np.random.default_rng({"normal": 11, "int_ties": 12, "all_zero": 13,
+                                 "signed_zeros": 14}[kind])
+    L_list = [16384, 16385, 16447, 20001, 2047, 65536, 99999] + [17000 + 3001 * i for i in range(17)]
+    top_k = 2048
+    ld = max(L_list)
+    s = np.zeros((len(L_list), ld), np.float32)
+    for i, L in enumerate(L_list):
+        if kind == "normal":
+            s[i, :L] = rng.standard_normal(L)
+        elif kind == "int_ties":
+            s[i, :L] = rng.integers(-5, 6, L)
+        elif kind == "signed_zeros":
+            s[i, :L] = np.where(rng.random(L) < 0.5, -0.0, 0.0)
+            s[i, :L:97] = 1.0
+    idx, n_sel = _select(s, L_list, top_k, 1)
+    for i, L in enumerate(L_list):
+        ref = oracle.topk(s[i, :L].astype(np.float64), top_k)
+        assert np.array_equal(idx[i, : n_sel[i]], ref), f"L={L}"
 
 
 @pytest.mark.parametrize("ties", [False, True])
