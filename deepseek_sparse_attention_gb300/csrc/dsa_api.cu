@@ -209,7 +209,9 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
                       batch->total_keys, sh.kpool};
     int32_t rps = 0, splits = 0;
     plan_attention_splits(sh, bh, &rps, &splits);
-    const int32_t attn = splits > 1 ? 2 : 1;
+    // attention, then the split merge -- except for two tensor-core splits,
+    // which merge inside the attention launch (a CTA pair)
+    const int32_t attn = splits > 2 || (splits == 2 && !sparse_mla_tc_eligible(sh, bh)) ? 2 : 1;
     const int32_t idx = batch->max_kv_len / sh.kpool > 0
                             ? (index_scores_tc_eligible(sh, bh) ? index_scores_tc_launches(sh, bh) : 1)
                             : 0;

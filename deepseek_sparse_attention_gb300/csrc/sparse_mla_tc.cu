@@ -33,11 +33,17 @@
 //              exceeds it by more than 2^8, exp2, P^T written to shared memory
 //              (into the buffer's rope block, which the scores no longer need),
 //              per-thread partial row sums reduced once at the end.
-// Splits of one query are combined by the log-sum-exp merge.
+// Splits of one query are combined by the log-sum-exp merge: a separate
+// launch over the partials in global memory, or, for two splits, inside this
+// launch by the two CTAs of a cluster through distributed shared memory.
 #include <math.h>
+
+#include <cooperative_groups.h>
 
 #include "dsa_kernels.cuh"
 #include "sm100.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 namespace {
@@ -100,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__ cache,
               BatchDev b, float scale, const int32_t* __restrict__ idx,
               const int32_t* __restrict__ n_sel, int64_t idx_width, int32_t rows_per_split,
-              int32_t n_split, float* __restrict__ out, float* __restrict__ lse,
+              int32_t n_split, int32_t pair, float* __restrict__ out, float* __restrict__ lse,
               float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* err) {
     using C = Cfg<W>;
     extern __shared__ uint8_t smem_raw[];
@@ -116,6 +122,44 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t q = blockIdx.y;
     const int split = blockIdx.x;
+    // Two splits of a query launched as a cluster (pair != 0): each stages its
+    // unnormalised O as [head][latent] in its own shared memory and its row
+    // maxima and sums stay in m_fin / l_fin; then each combines half of the
+    // heads from both through distributed shared memory and writes the final
+    // output -- no partials in global memory and no merge launch.  Every
+    // thread of both CTAs calls this once (an empty split too, with l = 0).
+    float* stage = reinterpret_cast<float*>(smem);    // the query and row buffers, once free
+    auto pair_merge = [&]() {
+        cg::cluster_group cl = cg::this_cluster();
+        cl.sync();                                    // both stages are written
+        const int rank = (int)cl.block_rank();
+        const float4* st0 = reinterpret_cast<const float4*>(stage);
+        const float4* st1 = reinterpret_cast<const float4*>(cl.map_shared_rank(stage, rank ^ 1));
+        const float* m1p = cl.map_shared_rank(m_fin, rank ^ 1);
+        const float* l1p = cl.map_shared_rank(l_fin, rank ^ 1);
+        float4* o4 = reinterpret_cast<float4*>(out);
+        constexpr int kC4 = kLatent / 4;
+        for (int i = threadIdx.x; i < (kHeads / 2) * kC4; i += blockDim.x) {
+            const int h = (kHeads / 2) * rank + i / kC4, c4 = i % kC4;
+            const float l0 = l_fin[h], l1 = l1p[h];
+            const float m0 = l0 > 0.f ? m_fin[h] : -INFINITY, m1 = l1 > 0.f ? m1p[h] : -INFINITY;
+            const float M = fmaxf(m0, m1);
+            const float f0 = l0 > 0.f ? exp2f(m0 - M) : 0.f, f1 = l1 > 0.f ? exp2f(m1 - M) : 0.f;
+            const float L = l0 * f0 + l1 * f1;
+            float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (L > 0.f) {
+                const float inv = 1.f / L;
+                const float4 a = l0 > 0.f ? st0[h * kC4 + c4] : r;
+                const float4 c = l1 > 0.f ? st1[h * kC4 + c4] : r;
+                r = make_float4((a.x * f0 + c.x * f1) * inv, (a.y * f0 + c.y * f1) * inv,
+                                (a.z * f0 + c.z * f1) * inv, (a.w * f0 + c.w * f1) * inv);
+            }
+            o4[(q * kHeads + h) * kC4 + c4] = r;
+            if (c4 == 0 && lse != nullptr)
+                lse[q * kHeads + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        }
+        cl.sync();                                    // the peer's reads of this stage are done
+    };
     pdl_wait();                                       // the selection must be complete
     pdl_trigger();
     // Row gather slots: every thread but the MMA warp's copies rows -- eight
@@ -139,7 +183,11 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
     const int64_t j1 = j0 + rows_per_split < ns ? j0 + rows_per_split : ns;
     if (j0 >= j1) {
-        if (n_split == 1) {                           // no rows: out = 0, lse = -inf
+        if (pair) {                                   // no weight from this half
+            if (threadIdx.x < kHeads) { m_fin[threadIdx.x] = -INFINITY; l_fin[threadIdx.x] = 0.f; }
+            __syncthreads();
+            pair_merge();
+        } else if (n_split == 1) {                    // no rows: out = 0, lse = -inf
             for (int i = threadIdx.x; i < kHeads * kLatent; i += blockDim.x)
                 out[q * kHeads * kLatent + i] = 0.f;
             if (lse != nullptr && threadIdx.x < kHeads) lse[q * kHeads + threadIdx.x] = -INFINITY;
@@ -526,11 +574,21 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
         // O^T lane 32 wq + lane holds latent columns 32 wq + lane + 128 i (an
         // M = 128 accumulator); this thread writes heads hb ..
+        if (pair) {                                   // staged for the pair merge
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const int c = 32 * wq + lane + kOBlock * i;
+                float v[32];
+                tmem_ld_32cols(lane_addr + kOCol + 64 * i + hb, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) stage[(hb + e) * kLatent + c] = v[e];
+            }
+        }
         const bool final_out = n_split == 1;
         const int64_t part = q * n_split + split;
         float* dst = final_out ? out + q * kHeads * kLatent : part_o + part * kHeads * kLatent;
 #pragma unroll 1
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 4 && !pair; ++i) {
             const int c = 32 * wq + lane + kOBlock * i;
             float v[32];
             tmem_ld_32cols(lane_addr + kOCol + 64 * i + hb, v);
@@ -540,7 +598,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 dst[(hb + e) * kLatent + c] = final_out ? (l > 0.f ? v[e] / l : 0.f) : v[e];
             }
         }
-        if (head_owner) {
+        if (head_owner && !pair) {
             const int h = hb + lane;
             const float l = l_fin[h];
             const float m = m_fin[h];
@@ -556,6 +614,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
 
     tc_fence_before();
     __syncthreads();
+    if (pair) pair_merge();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
@@ -607,11 +666,32 @@ cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, cons
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3((unsigned)n_split, (unsigned)b.n_q), dim3(kThreads), C::kSmemBytes, st,
-                   tm_q, cache, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split, out,
-                   lse, part_o, part_ml, err);
-    if (e != cudaSuccess || n_split == 1) return e;
-    return launch_merge_splits(b.n_q, n_split, part_o, part_ml, out, lse, st);
+    const int32_t pair = n_split == 2 ? 1 : 0;
+    if (!pair) {
+        e = launch_pdl(kern, dim3((unsigned)n_split, (unsigned)b.n_q), dim3(kThreads), C::kSmemBytes,
+                       st, tm_q, cache, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split,
+                       pair, out, lse, part_o, part_ml, err);
+        if (e != cudaSuccess || n_split == 1) return e;
+        return launch_merge_splits(b.n_q, n_split, part_o, part_ml, out, lse, st);
+    }
+    // two splits per query: a cluster of two CTAs merges in distributed shared memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, (unsigned)b.n_q);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, tm_q, cache, b, sh.scale, idx, n_sel,
+                              sh.index_row_width(), rps, n_split, pair, out, lse, part_o, part_ml,
+                              err);
 }
 
 }  // namespace

@@ -36,6 +36,10 @@ SMALL = [
     # 24 decode queries with long rows: selection by a pair of CTAs per query
     workloads.small("pair_select_batch", [16384 + 997 * i for i in range(22)] + [1500, 40001],
                     top_k=2048, seed=9),
+    # 60 decode queries: two attention splits per query, merged by a CTA pair
+    # (an empty second split for L <= 1024, a one-row one for L = 1025)
+    workloads.small("pair_merge_batch", [700, 1024, 1025, 30] + [3000 + 97 * i for i in range(56)],
+                    top_k=2048, seed=10),
 ]
 
 
