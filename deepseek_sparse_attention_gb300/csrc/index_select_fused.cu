@@ -20,7 +20,7 @@
 //   score     the tensor-core indexer pipeline (index_pipeline.cuh) writes the
 //             CTA's scores; they come back (from L2) as keys into the shared
 //             memory the pipeline's ring used;
-//   level 1   histogram of key bits 31..19 (8192 bins) per query, added into
+//   level 1   histogram of key bits 31..21 (2048 bins) per query, added into
 //             the query's global histogram;                         barrier 1
 //   bin       every CTA finds the bin b1 that holds the k-th largest key; it
 //             publishes how many of its keys lie above b1 and appends its keys
@@ -32,7 +32,7 @@
 //             before it (keys above b1 from the published counts, candidates
 //             from the list); a block scan writes its selections in order.
 // When a query's candidates overflow the list (heavy ties), the grid instead
-// resolves that query by two more histogram levels (bits 18..9 and 8..0) and a
+// resolves that query by two more histogram levels (bits 20..10 and 9..0) and a
 // round of per-CTA counts above and at T, three more barriers.  Global
 // histograms are cleared by the launch that used them once every CTA has read
 // them; candidate counters are cleared before the barrier that precedes their
@@ -57,7 +57,6 @@ constexpr int kShift1 = 32 - kBits1;                  // 21
 constexpr int kShift2 = kBits3;                       // 10
 constexpr int kCandCap = 8192;                        // candidates per query
 constexpr int kCandSpec = 3072;                       // read before the count is known
-constexpr int kItems = 8;                             // keys per thread per emission round
 
 // Global state per query (32-bit words; the stride keeps every part 16-byte aligned).
 constexpr int kOffH1 = 0;
@@ -284,47 +283,43 @@ __device__ __forceinline__ void sum_counts(const CountLoads& cl, int* red) {
 
 // Writes this CTA's selections of one query in ascending order from position
 // `base`: keys above T, and keys equal to T that are taken -- by index (at most
-// t_last) or, when `ranked`, the first `take` of them in this part.
+// t_last) or, when `ranked`, the first `take` of them in this part.  Each
+// thread owns a contiguous run of the part's keys (thread order = index
+// order): a count, one block scan for the offsets (two when ranked), a write.
 __device__ void emit_part(const SegState& S, const uint32_t* keys, uint32_t T, int base,
                           int32_t t_last, bool ranked, int take, int keep, int kpool,
                           int32_t* out, int* red) {
     const int tid = threadIdx.x;
-    int sel_carry = 0, eq_carry = 0;
-    for (int c0 = 0; c0 < S.n; c0 += kThreads * kItems) {
-        const int j0 = c0 + tid * kItems;
-        uint32_t k[kItems];
-#pragma unroll
-        for (int r = 0; r < kItems; ++r) k[r] = j0 + r < S.n ? keys[S.koff + j0 + r] : 0u;
-        int eq_rank = 0;
-        if (ranked) {
-            int ne = 0;
-#pragma unroll
-            for (int r = 0; r < kItems; ++r) ne += (j0 + r < S.n) && k[r] == T;
-            int tot;
-            eq_rank = eq_carry + block_excl_scan(ne, &tot, red);
-            eq_carry += tot;
+    const int per = (S.n + kThreads - 1) / kThreads;
+    const int j_a = tid * per < S.n ? tid * per : S.n;
+    const int j_b = j_a + per < S.n ? j_a + per : S.n;
+    const uint32_t* k = keys + S.koff;
+    int n_gt = 0, n_eq = 0, n_eq_ok = 0;
+    for (int j = j_a; j < j_b; ++j) {
+        const uint32_t x = k[j];
+        n_gt += x > T;
+        n_eq += x == T;
+        n_eq_ok += x == T && S.t_lo + j <= t_last;
+    }
+    int eq_rank = 0, tot;
+    if (ranked) {
+        eq_rank = block_excl_scan(n_eq, &tot, red);
+        int t = take - eq_rank;
+        n_eq_ok = t < 0 ? 0 : (t > n_eq ? n_eq : t);
+    }
+    int pos = base + block_excl_scan(n_gt + n_eq_ok, &tot, red);
+    for (int j = j_a; j < j_b; ++j) {
+        const uint32_t x = k[j];
+        bool sel = x > T;
+        if (x == T) {
+            sel = ranked ? eq_rank < take : S.t_lo + j <= t_last;
+            ++eq_rank;
         }
-        uint32_t selmask = 0;
-#pragma unroll
-        for (int r = 0; r < kItems; ++r) {
-            if (j0 + r >= S.n) continue;
-            bool sel = k[r] > T;
-            if (k[r] == T) {
-                sel = ranked ? eq_rank < take : S.t_lo + j0 + r <= t_last;
-                ++eq_rank;
-            }
-            selmask |= (uint32_t)sel << r;
-        }
-        int tot;
-        int pos = base + sel_carry + block_excl_scan(__popc(selmask), &tot, red);
-        sel_carry += tot;
-#pragma unroll
-        for (int r = 0; r < kItems; ++r) {
-            // positions stay below keep when the counts are consistent; the
-            // check keeps a corrupted state from writing past the row
-            if ((selmask & (1u << r)) && (unsigned)pos < (unsigned)keep)
-                put(out, pos, (int64_t)S.t_lo + j0 + r, kpool);
-            pos += (selmask >> r) & 1u;
+        // positions stay below keep when the counts are consistent; the check
+        // keeps a corrupted state from writing past the row
+        if (sel) {
+            if ((unsigned)pos < (unsigned)keep) put(out, pos, (int64_t)S.t_lo + j, kpool);
+            ++pos;
         }
     }
 }
