@@ -17,9 +17,10 @@
 // selection is every key above the query's k-th largest key T plus the
 // lowest-index keys equal to T.  All CTAs holding keys of a query cooperate
 // through global memory and grid barriers:
-//   score     the tensor-core indexer pipeline (index_pipeline.cuh) writes the
-//             CTA's scores; they come back (from L2) as keys into the shared
-//             memory the pipeline's ring used;
+//   score     the tensor-core indexer pipeline (index_pipeline.cuh) turns the
+//             CTA's scores into keys in shared memory (a CTA with more units
+//             than that region holds writes them to global memory and reads
+//             them back, from L2, into the shared memory the ring used);
 //   level 1   histogram of key bits 31..21 (2048 bins) per query, added into
 //             the query's global histogram;                         barrier 1
 //   bin       every CTA finds the bin b1 that holds the k-th largest key; it
@@ -46,7 +47,7 @@ namespace {
 using namespace sm100;
 using namespace idxp;
 
-using C = Cfg<1>;
+using C = Cfg<1, 5>;                                  // five stages: room for the keys below
 constexpr int kThreads = C::kThreads;                 // 256
 constexpr int kWarps = kThreads / 32;
 constexpr int kBits1 = 11, kBits2 = 11, kBits3 = 10;  // 11 + 11 + 10 = 32 key bits
@@ -90,7 +91,12 @@ static_assert(sizeof(SegState) == 48, "state layout");
 constexpr uint32_t kOffHist = (C::kOffPlanT + (C::kLocalMaxQ + 1) * 8 + 15) / 16 * 16;
 constexpr uint32_t kOffSeg = kOffHist + kBins1 * 4;
 constexpr uint32_t kOffRed = kOffSeg + kFusedMaxQ * sizeof(SegState);
-constexpr uint32_t kSmemBytes = kOffRed + 256 + 1024;           // + alignment slack
+// The CTA's keys, written there by the epilogue when its units fit (a
+// CTA with more units writes them to global memory and reads them back into
+// the ring once scoring is done).
+constexpr uint32_t kOffSKeys = kOffRed + 256;
+constexpr uint32_t kSKeyTiles = 80;
+constexpr uint32_t kSmemBytes = kOffSKeys + kSKeyTiles * kTileKeys * 4 + 1024;  // + alignment slack
 constexpr uint32_t kOffCandS = C::kOffB - (uint32_t)kCandCap * 8;
 constexpr uint32_t kMaxCtaKeys = kOffCandS / 4;
 constexpr uint32_t kMaxCtaTiles = kMaxCtaKeys / kTileKeys;
@@ -416,15 +422,19 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
 // workspace row of its query, and into the shared level-1 histogram when the
 // key belongs to `hist_q` (the first query this CTA selects for).
 struct KeyStore {
-    uint32_t* keys;
+    uint32_t* keys;        // global [query][ld], or (skeys) shared [unit - u_begin][128]
     int64_t ld;
+    uint32_t* skeys;
+    int64_t u_begin;
     uint32_t* hist;
     int32_t hist_q;
     __device__ void begin() {}
-    __device__ void emit(const IdxGroup& G, int j, int64_t t_row, bool valid, int64_t, int, float s) {
+    __device__ void emit(const IdxGroup& G, int j, int64_t t_row, bool valid, int64_t u, int row,
+                         float s) {
         if (!valid) return;
         const uint32_t k = order_key(s);
-        keys[(int64_t)(G.q0 + j) * ld + t_row] = k;
+        if (skeys != nullptr) skeys[(u - u_begin) * kTileKeys + row] = k;
+        else keys[(int64_t)(G.q0 + j) * ld + t_row] = k;
         if (G.q0 + j == hist_q) atomicAdd(&hist[k >> kShift1], 1u);
     }
 };
@@ -439,7 +449,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const int tid = threadIdx.x;
     const int cta = blockIdx.x, grid = gridDim.x;
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);     // re-pointed below when direct
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kOffHist);
     int2* cand = reinterpret_cast<int2*>(smem + kOffCandS);
     SegState* seg = reinterpret_cast<SegState*>(smem + kOffSeg);
@@ -453,6 +463,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int64_t u_begin = (int64_t)cta * U / grid, u_end = (int64_t)(cta + 1) * U / grid;
     const int keep = top_k / kpool;
     const bool fits = u_end - u_begin <= (int64_t)kMaxCtaTiles;
+    const bool direct = u_end - u_begin <= (int64_t)kSKeyTiles;   // keys straight to shared memory
+    if (direct) keys = reinterpret_cast<uint32_t*>(smem + kOffSKeys);
 
     // ---- before scoring: only what the epilogue needs, the first query this
     // CTA selects for (its level-1 counts are taken while scoring)
@@ -471,7 +483,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
     // ---- scores of this CTA's units (keys to global, level-1 counts of hist_q)
     if (u_begin < u_end && fits) {
-        KeyStore epi{gkeys, ld, hist, red[kRHistQ]};
+        KeyStore epi{gkeys, ld, direct ? keys : nullptr, u_begin, hist, red[kRHistQ]};
         run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_end, w, kpool, epi, err);
     }
     fence_proxy_async_smem();                 // the ring is reused by generic accesses
@@ -539,7 +551,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
     // ---- keys back into shared memory (asynchronous copies, 16 bytes each:
     // part starts are tile-aligned and rows padded to 4 keys), level-1 counts
-    for (int s = 0; s < nseg; ++s) {
+    for (int s = 0; s < nseg && !direct; ++s) {
         const SegState S = seg[s];
         const uint32_t* src = gkeys + (int64_t)S.q * ld + S.t_lo;
         const uint32_t dst = smem_u32(keys + S.koff);
