@@ -56,19 +56,39 @@ struct QueryInfo {
     int64_t n_keys;    // keys it scores: floor(L / kpool)
 };
 
-// Sequence of query q by binary search over q_off, then its visible length.
+// Sequence of query q, then its visible length.  In a decode batch (one
+// query per sequence: n_q == n_seq) query q is sequence q: the offsets of that
+// guess are all read at once (one round trip) and checked; otherwise, or when
+// the check fails, a binary search over q_off finds the sequence.
 // Returns false (and records kDevBadBatch) when the offsets contradict the
 // host bounds; the caller then skips the query.
 __device__ __forceinline__ bool query_info(const BatchDev& b, int64_t q, QueryInfo& qi,
                                            int32_t* err, int32_t where) {
-    int32_t lo = 0, hi = b.n_seq - 1;
-    while (lo < hi) {                       // last s with q_off[s] <= q
-        int32_t mid = (lo + hi + 1) >> 1;
-        if (b.q_off[mid] <= q) lo = mid; else hi = mid - 1;
+    int32_t s = -1;
+    int64_t q0 = 0, q1 = 0, r0 = 0, r1 = 0, k0 = 0, k1 = 0;
+    if (b.n_q == b.n_seq && q >= 0 && q < b.n_seq) {
+        q0 = b.q_off[q];
+        q1 = b.q_off[q + 1];
+        r0 = b.row_off[q];
+        r1 = b.row_off[q + 1];
+        k0 = b.key_off[q];
+        k1 = b.key_off[q + 1];
+        if (q0 <= q && q < q1) s = (int32_t)q;
     }
-    const int32_t s = lo;
-    const int64_t q0 = b.q_off[s], q1 = b.q_off[s + 1];
-    const int64_t r0 = b.row_off[s], r1 = b.row_off[s + 1];
+    if (s < 0) {
+        int32_t lo = 0, hi = b.n_seq - 1;
+        while (lo < hi) {                   // last s with q_off[s] <= q
+            int32_t mid = (lo + hi + 1) >> 1;
+            if (b.q_off[mid] <= q) lo = mid; else hi = mid - 1;
+        }
+        s = lo;
+        q0 = b.q_off[s];
+        q1 = b.q_off[s + 1];
+        r0 = b.row_off[s];
+        r1 = b.row_off[s + 1];
+        k0 = b.key_off[s];
+        k1 = b.key_off[s + 1];
+    }
     const int64_t kv_len = r1 - r0, q_len = q1 - q0;
     const int64_t L = kv_len - q_len + 1 + (q - q0);
     if (q < q0 || q >= q1 || q_len > kv_len || kv_len > b.max_kv_len || L < 1 || r0 < 0 ||
@@ -78,11 +98,10 @@ __device__ __forceinline__ bool query_info(const BatchDev& b, int64_t q, QueryIn
     }
     qi.seq = s;
     qi.row0 = r0;
-    qi.key0 = b.key_off[s];
+    qi.key0 = k0;
     qi.L = L;
     qi.n_keys = L / b.kpool;
-    if (b.key_off[s + 1] - qi.key0 < kv_len / b.kpool || qi.key0 < 0 ||
-        b.key_off[s + 1] > b.total_keys) {
+    if (k1 - k0 < kv_len / b.kpool || k0 < 0 || k1 > b.total_keys) {
         record_error(err, kDevBadBatch, (int32_t)q, where);
         return false;
     }
