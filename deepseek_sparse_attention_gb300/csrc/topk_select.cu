@@ -34,11 +34,9 @@ namespace cg = cooperative_groups;
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
 constexpr int kL1Bits = 11;                   // first radix level: top 11 key bits
 constexpr int kL1Bins = 1 << kL1Bits;
-constexpr int kHistCopies = 4;
+constexpr int kHistCopies = 2;             // 4096 bins: the first multi-level radix level
 constexpr int kCandCap = 8192;
 constexpr int kSample = 2048;                 // scores sampled to bound the threshold
 constexpr int kItems = 8;                     // scores per thread per emission round (fallback)
@@ -91,9 +89,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* warp
 
 // The digit d of a histogram of nb bins at which the count of keys in bins
 // above d is < k_rem <= that count plus hist[d]; *above gets the former.
+template <int NT>
 __device__ void find_digit(const uint32_t* hist, int nb, int64_t k_rem, int* warp_sums,
                            uint32_t* s_digit, int64_t* s_above) {
-    const int per = nb >= kThreads ? nb / kThreads : 1;
+    const int per = nb >= NT ? nb / NT : 1;
     const int first = threadIdx.x * per;
     int local = 0;
     for (int r = 0; r < per; ++r)
@@ -131,6 +130,7 @@ __device__ __forceinline__ void put(int32_t* out, int64_t pos, int64_t t, int kp
 
 // Selection by three radix levels over the scores in global memory, then an
 // emission pass over them in ascending order.  `hist` has 4096 entries.
+template <int NT>
 __device__ void select_multilevel(const float* __restrict__ sc, int64_t n, int64_t keep, int kpool,
                                   int32_t* out, uint32_t* hist, int* warp_sums, uint32_t* s_digit,
                                   int64_t* s_above, int64_t* n_out) {
@@ -142,12 +142,12 @@ __device__ void select_multilevel(const float* __restrict__ sc, int64_t n, int64
     for (int lvl = 0; lvl < 3; ++lvl) {
         const int bits = lvl == 0 ? 12 : 10;
         const int nb = 1 << bits;
-        for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
+        for (int i = tid; i < nb; i += NT) hist[i] = 0;
         __syncthreads();
         const int shift = 32 - pbits - bits;
         const int lane = tid & 31, warp = tid >> 5;
         for (int64_t base = (int64_t)warp * 32 * kBatch; base < n;
-             base += (int64_t)kWarps * 32 * kBatch) {
+             base += (int64_t)(NT / 32) * 32 * kBatch) {
             uint32_t key[kBatch];
             load_keys(sc, base, n, lane, key);
 #pragma unroll
@@ -158,7 +158,7 @@ __device__ void select_multilevel(const float* __restrict__ sc, int64_t n, int64
             }
         }
         __syncthreads();
-        find_digit(hist, nb, k_rem, warp_sums, s_digit, s_above);
+        find_digit<NT>(hist, nb, k_rem, warp_sums, s_digit, s_above);
         k_rem -= *s_above;
         prefix = (prefix << bits) | *s_digit;
         pbits += bits;
@@ -166,7 +166,7 @@ __device__ void select_multilevel(const float* __restrict__ sc, int64_t n, int64
     }
     const uint32_t T = prefix;
     int64_t eq_base = 0, out_base = 0;
-    for (int64_t c0 = 0; c0 < n; c0 += (int64_t)kThreads * kItems) {
+    for (int64_t c0 = 0; c0 < n; c0 += (int64_t)NT * kItems) {
         const int64_t t_begin = c0 + (int64_t)tid * kItems;
         uint32_t keys[kItems];
         int n_eq = 0, valid = 0;
@@ -211,8 +211,8 @@ __device__ void select_multilevel(const float* __restrict__ sc, int64_t n, int64
 // emits the r-th half of the row; the two exchange their candidates through
 // distributed shared memory, so each finds the same threshold, and the second
 // starts its output after the first half's selections.
-template <int CL>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kThreads, 1)
+template <int CL, int NT>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NT, 1024 / NT)
 topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __restrict__ scores,
                    int64_t ld, int32_t* __restrict__ idx, int32_t* __restrict__ n_sel,
                    int64_t width, int32_t bitmap_words, int32_t* err) {
@@ -237,7 +237,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
     // (every CTA of a cluster takes the same branches up to the exchange)
     if (!query_info(b, q, qi, err, /*where=*/2)) {
         if (rank == 0) {
-            for (int64_t i = tid; i < width; i += kThreads) out[i] = -1;
+            for (int64_t i = tid; i < width; i += NT) out[i] = -1;
             if (tid == 0) n_sel[q] = 0;
         }
         return;
@@ -248,7 +248,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
 
     if (n <= keep) {                        // dense: every visible row
         if (rank == 0) {
-            for (int64_t i = tid; i < width; i += kThreads) out[i] = i < L ? (int32_t)i : -1;
+            for (int64_t i = tid; i < width; i += NT) out[i] = i < L ? (int32_t)i : -1;
             if (tid == 0) n_sel[q] = (int32_t)L;
         }
         return;
@@ -268,31 +268,31 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
         // the key (to 22 bits) of the sample element ranked at 1.5x the kept
         // fraction plus a margin, found by two radix levels over the sample.
         uint32_t* samp = cand_key;                       // the sample lives where candidates will
-        for (int i = tid; i < kL1Bins; i += kThreads) hist[i] = 0;
+        for (int i = tid; i < kL1Bins; i += NT) hist[i] = 0;
         if (tid == 0) *s_count = 0;
         const int64_t n_samp = n < kSample ? n : kSample;
-        for (int64_t i = tid; i < n_samp; i += kThreads) samp[i] = order_key(__ldg(sc + i * n / n_samp));
+        for (int64_t i = tid; i < n_samp; i += NT) samp[i] = order_key(__ldg(sc + i * n / n_samp));
         __syncthreads();
-        for (int64_t i = tid; i < n_samp; i += kThreads) atomicAdd(&hist[samp[i] >> 21], 1u);
+        for (int64_t i = tid; i < n_samp; i += NT) atomicAdd(&hist[samp[i] >> 21], 1u);
         __syncthreads();
         int64_t target = (keep * n_samp * 3 + 2 * n - 1) / (2 * n) + 8;
         target = target < n_samp ? target : n_samp;
-        find_digit(hist, kL1Bins, target, warp_sums, s_digit, s_above);
+        find_digit<NT>(hist, kL1Bins, target, warp_sums, s_digit, s_above);
         const uint32_t sb1 = *s_digit;
         target -= *s_above;
         __syncthreads();
-        for (int i = tid; i < kL1Bins; i += kThreads) hist[i] = 0;
+        for (int i = tid; i < kL1Bins; i += NT) hist[i] = 0;
         __syncthreads();
-        for (int64_t i = tid; i < n_samp; i += kThreads)
+        for (int64_t i = tid; i < n_samp; i += NT)
             if ((samp[i] >> 21) == sb1) atomicAdd(&hist[(samp[i] >> 10) & (kL1Bins - 1)], 1u);
         __syncthreads();
-        find_digit(hist, kL1Bins, target, warp_sums, s_digit, s_above);
+        find_digit<NT>(hist, kL1Bins, target, warp_sums, s_digit, s_above);
         const float t_lo = key_to_float((sb1 << 21) | (*s_digit << 10));
         __syncthreads();
 
         // ---- one streaming pass over [lo, hi): every score >= t_lo becomes a candidate
         for (int64_t base = lo + (int64_t)warp * 32 * kBatch; base < hi;
-             base += (int64_t)kWarps * 32 * kBatch) {
+             base += (int64_t)(NT / 32) * 32 * kBatch) {
             float v[kBatch];
 #pragma unroll
             for (int r = 0; r < kBatch; ++r) {
@@ -323,7 +323,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
                 }
             }
         }
-        for (int64_t w = tid; w < words; w += kThreads) { sel_bits[w] = 0; eq_bits[w] = 0; }
+        for (int64_t w = tid; w < words; w += NT) { sel_bits[w] = 0; eq_bits[w] = 0; }
         __syncthreads();
         int n_cand = *s_count;
         if (CL == 2) {
@@ -336,7 +336,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
             if (n_cand <= kCandCap && n_all <= kCandCap) {
                 const uint32_t* pk = cluster.map_shared_rank(cand_key, rank ^ 1);
                 const int32_t* pi = cluster.map_shared_rank(cand_idx, rank ^ 1);
-                for (int i = tid; i < n_peer; i += kThreads) {
+                for (int i = tid; i < n_peer; i += NT) {
                     cand_key[n_cand + i] = pk[i];
                     cand_idx[n_cand + i] = pi[i];
                 }
@@ -355,15 +355,15 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
                 const int bits = lvl == 2 ? 10 : 11;
                 const int nb = 1 << bits;
                 const int shift = 32 - pbits - bits;
-                for (int i = tid; i < nb; i += kThreads) hist[i] = 0;
+                for (int i = tid; i < nb; i += NT) hist[i] = 0;
                 __syncthreads();
-                for (int i = tid; i < n_cand; i += kThreads) {
+                for (int i = tid; i < n_cand; i += NT) {
                     const uint32_t key = cand_key[i];
                     if (pbits == 0 || (key >> (32 - pbits)) == prefix)
                         atomicAdd(&hist[(key >> shift) & (uint32_t)(nb - 1)], 1u);
                 }
                 __syncthreads();
-                find_digit(hist, nb, k_rem, warp_sums, s_digit, s_above);
+                find_digit<NT>(hist, nb, k_rem, warp_sums, s_digit, s_above);
                 k_rem -= *s_above;
                 prefix = (prefix << bits) | *s_digit;
                 pbits += bits;
@@ -373,7 +373,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
             // this part's candidates into the bitmaps; the earlier part's
             // selections (keys above T, and how many equal to T) for the offsets
             int gt_before = 0, eq_before = 0;
-            for (int i = tid; i < n_cand; i += kThreads) {
+            for (int i = tid; i < n_cand; i += NT) {
                 const uint32_t key = cand_key[i];
                 const int32_t t = cand_idx[i];
                 if (t < lo) {
@@ -397,7 +397,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
             }
             __syncthreads();
             // ---- emission in ascending order: keys > T, then the first k_rem keys == T
-            for (int64_t w0 = 0; w0 < words; w0 += kThreads) {
+            for (int64_t w0 = 0; w0 < words; w0 += NT) {
                 const int64_t w = w0 + tid;
                 const uint32_t sw = w < words ? sel_bits[w] : 0u;
                 const uint32_t ew = w < words ? eq_bits[w] : 0u;
@@ -425,7 +425,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
     }
     if (!done) {                            // the whole row, by the first CTA alone
         if (rank > 0) return;
-        select_multilevel(sc, n, keep, kpool, out, hist, warp_sums, s_digit, s_above, &n_out);
+        select_multilevel<NT>(sc, n, keep, kpool, out, hist, warp_sums, s_digit, s_above, &n_out);
     }
     if (tid == 0 && rank == (done ? CL - 1 : 0) && n_out != keep)
         record_error(err, kDevBadIndex, (int32_t)q, /*where=*/2);
@@ -434,9 +434,9 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
     // ---- unfilled tail (k-pool), then padding
     const int64_t body = keep * kpool;
     const int64_t tail = L - n * kpool;
-    for (int64_t i = tid; i < tail; i += kThreads) out[body + i] = (int32_t)(n * kpool + i);
+    for (int64_t i = tid; i < tail; i += NT) out[body + i] = (int32_t)(n * kpool + i);
     const int64_t total_sel = body + tail;
-    for (int64_t i = total_sel + tid; i < width; i += kThreads) out[i] = -1;
+    for (int64_t i = total_sel + tid; i < width; i += NT) out[i] = -1;
     if (tid == 0) n_sel[q] = (int32_t)total_sel;
 }
 
@@ -462,11 +462,15 @@ cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* 
     int64_t words = (part + 31) / 32;
     if (kFixedSmem + (size_t)words * 8 > kMaxSmem) words = 0;
     const size_t smem = kFixedSmem + (size_t)words * 8;
-    auto kern = pair ? topk_select_kernel<2> : topk_select_kernel<1>;
+    // A pair has 1024 threads per CTA (one wave: latency wants threads); one
+    // CTA per query has 512, two CTAs per SM overlapping their latency chains
+    // across the many waves of a prefill chunk.
+    auto kern = pair ? topk_select_kernel<2, 1024> : topk_select_kernel<1, 512>;
+    const int nt = pair ? 1024 : 512;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid = pair ? dim3(2, (unsigned)b.n_q) : dim3((unsigned)b.n_q);
-    return launch_pdl(kern, grid, dim3(kThreads), smem, st, b, sh.top_k, sh.kpool, scores, ld, idx,
+    return launch_pdl(kern, grid, dim3(nt), smem, st, b, sh.top_k, sh.kpool, scores, ld, idx,
                       n_sel, sh.index_row_width(), (int32_t)words, err);
 }
 
