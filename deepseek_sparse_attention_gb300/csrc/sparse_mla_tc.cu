@@ -160,6 +160,44 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         }
         cl.sync();                                    // the peer's reads of this stage are done
     };
+    // Before the selection is waited for: barriers, TMEM and the query tile
+    // (the query is an input; the kernels before this one do not write it).
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&r_full[i], kIssuers);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], kSoftmaxThreads);
+            mbar_init(&pv_done[i], 1);
+        }
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_q);
+        mbar_arrive_expect_tx(q_full, C::kCB * kQBlock);
+        for (int cb = 0; cb < C::kCB; ++cb)
+            tma_load_2d(smem + C::kOffQ + cb * kQBlock, &tm_q, q_full, 64 * cb, (int32_t)(q * kHeads));
+    }
+    // A CTA leaving before its pipeline runs: the query tile must have landed
+    // and TMEM goes back.
+    auto leave_early = [&]() {
+        if (threadIdx.x == 0) mbar_wait(q_full, 0, kWaitNs);
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem_base, kTmemCols);
+        }
+    };
     pdl_wait();                                       // the selection must be complete
     pdl_trigger();
     // Row gather slots: every thread but the MMA warp's copies rows -- eight
@@ -179,7 +217,10 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     int32_t ib = issuer && two_rows && j0 + rs + kRowSlots < idx_width
                      ? idx[q * idx_width + j0 + rs + kRowSlots] : 0;
     QueryInfo qi;
-    if (!query_info(b, q, qi, err, /*where=*/8)) return;
+    if (!query_info(b, q, qi, err, /*where=*/8)) {
+        leave_early();
+        return;
+    }
     ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
     const int64_t j1 = j0 + rows_per_split < ns ? j0 + rows_per_split : ns;
     if (j0 >= j1) {
@@ -196,30 +237,11 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             part_ml[(part * kHeads + threadIdx.x) * 2] = -INFINITY;
             part_ml[(part * kHeads + threadIdx.x) * 2 + 1] = 0.f;
         }
+        leave_early();
         return;
     }
     const int n_tiles = (int)((j1 - j0 + kTileRows - 1) / kTileRows);
 
-    if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(drain, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&r_full[i], kIssuers);
-            mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], kSoftmaxThreads);
-            mbar_init(&pv_done[i], 1);
-        }
-        fence_mbarrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-    if (warp == 0 && lane == 0) prefetch_tensormap(&tm_q);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
 
     // Copies of this thread's rows of tile t (indices ra, rb read from the
     // selection) into buffer t % 2 in the 128-byte swizzle layout; the
@@ -263,16 +285,10 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     if (issuer) issue_rows(0, ia, ib);
 
     if (warp != 1 && warp < 4) {                                      // ---- loads
-        // warps 0, 2, 3: the query once (TMA tiles), their share of the
-        // second tile at once, then tile t + 1 as soon as its buffer is free
-        // (the PV of tile t - 1 has completed).
+        // warps 0, 2, 3: their share of the second tile at once, then tile
+        // t + 1 as soon as its buffer is free (the PV of tile t - 1 has
+        // completed).
         bool ok = true;
-        if (slot == 0) {
-            mbar_arrive_expect_tx(q_full, C::kCB * kQBlock);
-            for (int cb = 0; cb < C::kCB; ++cb)
-                tma_load_2d(smem + C::kOffQ + cb * kQBlock, &tm_q, q_full, 64 * cb,
-                            (int32_t)(q * kHeads));
-        }
         // From the third tile on the loaders copy whole tiles alone (eight
         // threads per row, twelve rows a pass), keeping the softmax warps' time
         // for the softmax; those arrive on the barrier without copies.
