@@ -274,6 +274,29 @@ __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const float (&v)[
 }
 
 // 16-column variants of the TMEM load and store above.
+// 16 lanes x 64 columns from the warp's TMEM quadrant (lanes 0..15 of it,
+// where an M = 64 accumulator keeps its rows), all 32 threads busy: thread t
+// gets lane (t >> 2) + 8 (t & 1) and the columns of parity (t >> 1) & 1,
+// v[k] = column 2 k + ((t >> 1) & 1) (the 16x64b shape, 32 repetitions).
+__device__ __forceinline__ void tmem_ld_16x64b_32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x64b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile(

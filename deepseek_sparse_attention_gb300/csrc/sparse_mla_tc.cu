@@ -63,9 +63,11 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kSlack = 8.f;                       // lazy rescale threshold (log2 units)
-constexpr int kLoaders = 96;                        // threads that gather rows
-constexpr int kSoftmaxThreads = 256;                // two warpgroups
-constexpr int kThreads = 128 + kSoftmaxThreads;     // loaders + MMA warp, then softmax
+// Warps 0, 2, 3 and 8-11 gather rows (224 threads), warp 1 issues the MMAs,
+// warps 4-7 run the softmax; all but warp 1 copy the first two tiles.
+constexpr int kLoaders = 224;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 384;
 constexpr int kIssuers = kLoaders + kSoftmaxThreads; // threads that copy rows: 352
 constexpr int kRowSlots = kIssuers / 8;             // rows a tile's copy round covers: 44
 static_assert(kIssuers % 8 == 0 && 2 * kRowSlots >= 64, "two rows per slot cover a tile");
@@ -162,6 +164,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     };
     // Before the selection is waited for: barriers, TMEM and the query tile
     // (the query is an input; the kernels before this one do not write it).
+    if (threadIdx.x < kHeads) m_fin[threadIdx.x] = -INFINITY;   // the running maxima
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(drain, 1);
@@ -284,17 +287,18 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     };
     if (issuer) issue_rows(0, ia, ib);
 
-    if (warp != 1 && warp < 4) {                                      // ---- loads
-        // warps 0, 2, 3: their share of the second tile at once, then tile
-        // t + 1 as soon as its buffer is free (the PV of tile t - 1 has
+    if ((warp != 1 && warp < 4) || warp >= 8) {                      // ---- loads
+        // warps 0, 2, 3, 8-11: their share of the second tile at once, then
+        // tile t + 1 as soon as its buffer is free (the PV of tile t - 1 has
         // completed).
         bool ok = true;
         // From the third tile on the loaders copy whole tiles alone (eight
-        // threads per row, twelve rows a pass), keeping the softmax warps' time
+        // threads per row, 28 rows a pass), keeping the softmax warps' time
         // for the softmax; those arrive on the barrier without copies.
         constexpr int kRowsPerPass = kLoaders / 8;
         constexpr int kPasses = (kTileRows + kRowsPerPass - 1) / kRowsPerPass;
-        const int rsub = slot >> 3;
+        const int ls = warp == 0 ? lane : (warp < 4 ? 32 * (warp - 1) + lane : 96 + 32 * (warp - 8) + lane);
+        const int rsub = ls >> 3, k8l = ls & 7;
         for (int t = 0; t + 1 < n_tiles && ok; ++t) {
             if (t == 0) {
                 fetch_rows(1, ia, ib);
@@ -323,8 +327,8 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                     record_error(err, kDevBadIndex, (int32_t)q, /*where=*/8);
                     row = 0;
                 }
-                const unsigned char* src = cbase + ((qi.row0 + row) * W + k8 * 8) * 2;
-                const uint32_t dst = rbase + r * 128 + ((k8 ^ (r & 7)) << 4);
+                const unsigned char* src = cbase + ((qi.row0 + row) * W + k8l * 8) * 2;
+                const uint32_t dst = rbase + r * 128 + ((k8l ^ (r & 7)) << 4);
 #pragma unroll
                 for (int cb = 0; cb < C::kCB; ++cb)
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
@@ -336,7 +340,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                          : "memory");
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
-        if (!ok && slot == 0) record_error(err, kDevTimeout, (int32_t)q, /*where=*/9);
+        if (!ok && ls == 0) record_error(err, kDevTimeout, (int32_t)q, /*where=*/9);
     } else if (warp == 1) {                                           // ---- MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(kTileRows, kHeads);
@@ -405,31 +409,31 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             mma_commit(drain);
             mbar_wait(drain, 0, 50000000ull);
         }
-    } else if (warp >= 4) {                                           // ---- softmax
-        // two warpgroups over the same 64 rows: warpgroup sg owns heads
-        // [32 sg, 32 sg + 32).  The scores of an M = 64 tile sit in lanes 0..15
-        // of each 32-lane TMEM quadrant: warps w and w + 4 (quadrant wq) hold
-        // rows 16 wq .. 16 wq + 15, one per lane 0..15; lanes 16..31 carry none.
-        const int wq = warp & 3, sg = (warp - 4) >> 2;
-        const bool has_row = lane < 16;
-        const int row = 16 * wq + (lane & 15);
-        const int hb = 32 * sg;                      // first head of this thread
-        const bool head_owner = wq == 0;             // warps 4, 8: head hb + lane
+    } else {                                                          // ---- softmax
+        // warps 4-7, one warpgroup.  The scores of an M = 64 tile sit in lanes
+        // 0..15 of TMEM quadrant wq; a 16x64b load gives lane l of warp 4 + wq
+        // the row 16 wq + (l >> 2) + 8 (l & 1) and the 32 heads of parity
+        // p = (l >> 1) & 1 (p, p + 2, ..., p + 62): every lane a row.
+        const int wq = warp & 3;
+        const int p = (lane >> 1) & 1;
+        const int row = 16 * wq + (lane >> 2) + 8 * (lane & 1);
+        const int ts = threadIdx.x - 128;            // 0..127; 0..63 own a head each
         const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * wq) << 16);
         const float c2 = scale * kLog2e;
+        // partial row sums of heads 32 p .. 32 p + 31 of this row (the heads a
+        // lane holds after the exchange with lane ^ 2, below)
         float l_part[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) l_part[e] = 0.f;
         // running maxima (one writer per head) and rescale factors live in shared memory
         float* m_sh = m_fin;
         float* alpha_s = l_fin;
-        if (head_owner) m_sh[hb + lane] = -INFINITY;
         bool ok = true;
         // this thread's row index, read a tile ahead so that the load overlaps
         // the previous tile's work (-1: no row)
         auto row_index = [&](int t) -> int32_t {
             const int64_t jrow = j0 + (int64_t)t * kTileRows + row;
-            return (has_row && t < n_tiles && jrow < j1) ? idx[q * idx_width + jrow] : -1;
+            return (t < n_tiles && jrow < j1) ? idx[q * idx_width + jrow] : -1;
         };
         // this thread's copies of tile 1 (its buffer is free from the start)
         if (n_tiles > 1) {
@@ -450,10 +454,10 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             // by the loader), take no weight
             const bool valid = r_cur >= 0 && r_cur < qi.L;
             r_cur = r_next;
-            float x[32];
+            float x[32];                             // x[k]: head p + 2 k
             {
                 float v[32];
-                tmem_ld_32cols(lane_addr + kSCol + 64 * bf + hb, v);
+                tmem_ld_16x64b_32(lane_addr + kSCol + 64 * bf, v);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[e] = valid ? v[e] * c2 : -INFINITY;
             }
@@ -462,7 +466,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             // first tiles) the maxima stay and no reduction is needed.
             uint32_t exceed = 0;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) exceed |= (uint32_t)(x[e] > m_sh[hb + e] + kSlack);
+            for (int e = 0; e < 32; ++e) exceed |= (uint32_t)(x[e] > m_sh[p + 2 * e] + kSlack);
             uint32_t any_exceed;
             asm volatile(
                 "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
@@ -472,19 +476,55 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 : "memory");
             uint32_t any_raised = 0;
             if (any_exceed) {
-                // per-head maximum over the tile's 64 rows
-                int* rb = red + wq * kHeads + hb;
+                // per-head maximum over the warp's 16 rows (the 16 lanes of a
+                // parity: lane bits 0, 2, 3, 4), then over the four warps.  A
+                // halving exchange: at each step a lane keeps half of its
+                // values, swaps the other half with the partner across one lane
+                // bit and takes the maximum, so that after four steps each lane
+                // holds two heads' maxima (30 shuffles for 32 heads).
+                int* rb = red + wq * kHeads;
+                float m16[16], m8[8], m4[4], m2[2];
+                {
+                    const bool b = (lane >> 4) & 1;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int mk = __reduce_max_sync(0xffffffffu, fkey(x[e]));
-                    if (lane == e) rb[e] = mk;
+                    for (int i = 0; i < 16; ++i) {
+                        const float r = __shfl_xor_sync(0xffffffffu, b ? x[i] : x[i + 16], 16);
+                        m16[i] = fmaxf(b ? x[i + 16] : x[i], r);
+                    }
                 }
+                {
+                    const bool b = (lane >> 3) & 1;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float r = __shfl_xor_sync(0xffffffffu, b ? m16[i] : m16[i + 8], 8);
+                        m8[i] = fmaxf(b ? m16[i + 8] : m16[i], r);
+                    }
+                }
+                {
+                    const bool b = (lane >> 2) & 1;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float r = __shfl_xor_sync(0xffffffffu, b ? m8[i] : m8[i + 4], 4);
+                        m4[i] = fmaxf(b ? m8[i + 4] : m8[i], r);
+                    }
+                }
+                {
+                    const bool b = lane & 1;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float r = __shfl_xor_sync(0xffffffffu, b ? m4[i] : m4[i + 2], 1);
+                        m2[i] = fmaxf(b ? m4[i + 2] : m4[i], r);
+                    }
+                }
+                // m2[i]: the maximum of x[e], e = i + 2 (lane & 1) + 4 ((lane >> 2) & 7)
+                const int e0 = 2 * (lane & 1) + 4 * ((lane >> 2) & 7);
+                rb[p + 2 * e0] = fkey(m2[0]);
+                rb[p + 2 * e0 + 2] = fkey(m2[1]);
                 asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
                 uint32_t raised = 0;
-                if (head_owner) {                      // head hb + lane: raise its running maximum?
-                    const int h = hb + lane;
-                    const int* rt = red;
-                    const int mk = max(max(rt[h], rt[kHeads + h]), max(rt[2 * kHeads + h], rt[3 * kHeads + h]));
+                if (ts < kHeads) {                     // head ts: raise its running maximum?
+                    const int h = ts;
+                    const int mk = max(max(red[h], red[kHeads + h]), max(red[2 * kHeads + h], red[3 * kHeads + h]));
                     const float tmax = fval(mk), m_old = m_sh[h];
                     float a = 1.f;
                     if (tmax > m_old + kSlack) {
@@ -503,7 +543,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             }
             if (any_raised) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) l_part[e] *= alpha_s[hb + e];
+                for (int e = 0; e < 32; ++e) l_part[e] *= alpha_s[32 * p + e];
             }
             if (any_raised && t > 0) {                 // O^T follows the new maxima
                 // the previous tile's PV may still be accumulating into O^T
@@ -511,22 +551,27 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 if (ok) ok = mbar_wait(&pv_done[pb], (uint32_t)(((t - 1) >> 1) & 1), kWaitNs);
                 tc_fence_after();
 #pragma unroll 1
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 8; ++i) {          // 4 blocks x two halves of the heads
                     float v[32];
-                    const uint32_t a = lane_addr + kOCol + 64 * i + hb;
+                    const int hh = 32 * (i & 1);
+                    const uint32_t a = lane_addr + kOCol + 64 * (i >> 1) + hh;
                     tmem_ld_32cols(a, v);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) v[c] *= alpha_s[hb + c];
+                    for (int c = 0; c < 32; ++c) v[c] *= alpha_s[hh + c];
                     tmem_st_32cols(a, v);
                 }
                 tc_fence_before();
                 asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
             }
-            // this thread's half of its P^T row: 32 bf16 in the 128-byte swizzle
-            // layout, twice: p = hi + lo with hi = bf16(p), lo = bf16(p - hi), so
-            // that the two value products carry P to ~2^-16 relative.  hi goes
-            // to the buffer's P block, lo to the shared P_lo block once the
-            // previous tile's value products (which read it) are done.
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = exp2f(x[e] - m_sh[p + 2 * e]);
+            // P^T row: this lane and lane ^ 2 (same row, other parity) swap
+            // halves so that this lane holds heads 32 p .. 32 p + 31 as pairs
+            // (32 p + 2 k, 32 p + 2 k + 1); 32 bf16 in the 128-byte swizzle layout,
+            // twice: p = hi + lo with hi = bf16(p), lo = bf16(p - hi), so that
+            // the two value products carry P to ~2^-16 relative.  hi goes to the
+            // buffer's P block, lo to the shared P_lo block once the previous
+            // tile's value products (which read it) are done.
             uint8_t* prow = smem + C::off_p(bf) + row * 128;
             uint8_t* plow = smem + C::kOffPlo + row * 128;
             uint32_t lo4[4][4];
@@ -535,31 +580,31 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 uint32_t w4[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int hl = 8 * c16 + 2 * e;
-                    const float p0 = exp2f(x[hl] - m_sh[hb + hl]);
-                    const float p1 = exp2f(x[hl + 1] - m_sh[hb + hl + 1]);
+                    const int k = 4 * c16 + e;
+                    const float send = p ? x[k] : x[k + 16];
+                    const float r = __shfl_xor_sync(0xffffffffu, send, 2);
+                    const float p0 = p ? r : x[k];
+                    const float p1 = p ? x[k + 16] : r;
                     const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
                     const float2 hf = __bfloat1622float2(hi);
                     const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
                     const float2 lf = __bfloat1622float2(lo);
-                    l_part[hl] += hf.x + lf.x;
-                    l_part[hl + 1] += hf.y + lf.y;
+                    l_part[2 * k] += hf.x + lf.x;
+                    l_part[2 * k + 1] += hf.y + lf.y;
                     w4[e] = *reinterpret_cast<const uint32_t*>(&hi);
                     lo4[c16][e] = *reinterpret_cast<const uint32_t*>(&lo);
                 }
-                const int chunk = 4 * sg + c16;
-                if (has_row)
-                    *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                const int chunk = 4 * p + c16;
+                *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
             if (t > 0 && ok)
                 ok = mbar_wait(&pv_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), kWaitNs);
 #pragma unroll
             for (int c16 = 0; c16 < 4; ++c16) {
-                const int chunk = 4 * sg + c16;
-                if (has_row)
-                    *reinterpret_cast<uint4*>(plow + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(lo4[c16][0], lo4[c16][1], lo4[c16][2], lo4[c16][3]);
+                const int chunk = 4 * p + c16;
+                *reinterpret_cast<uint4*>(plow + ((chunk ^ (row & 7)) << 4)) =
+                    make_uint4(lo4[c16][0], lo4[c16][1], lo4[c16][2], lo4[c16][3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -571,23 +616,30 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             if (ok) ok = mbar_wait(&pv_done[tl & 1], (uint32_t)((tl >> 1) & 1), kWaitNs);
         }
         if (!ok) record_error(err, kDevTimeout, (int32_t)q, /*where=*/11);
-        tc_fence_after();
-        // row sums: per-thread partials -> per-head totals (through shared memory;
-        // the row buffers are free once the last PV has completed)
+        // row sums: per-thread partials -> shared memory (the row buffers are
+        // free once the last PV has completed), summed per head below
         float* lsc = reinterpret_cast<float*>(smem + C::kOffR);
-        if (has_row) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) lsc[row * (kHeads + 1) + hb + e] = l_part[e];
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        for (int e = 0; e < 32; ++e) lsc[row * (kHeads + 1) + 32 * p + e] = l_part[e];
+    }
+
+    // ---- epilogue, warps 4-11: per-head sums, then O^T read out of TMEM
+    if (warp >= 4) {
+        asm volatile("bar.sync 3, %0;" ::"n"(2 * kSoftmaxThreads) : "memory");
+        tc_fence_after();
+        const int wq = warp & 3, sg = (warp - 4) >> 2;
+        const int hb = 32 * sg;                      // this warp's heads: hb .. hb + 31
+        const bool head_owner = warp == 4 || warp == 5;    // head (warp - 4) * 32 + lane
+        const int ho = (warp - 4) * 32 + lane;
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * wq) << 16);
+        const float* lsc = reinterpret_cast<const float*>(smem + C::kOffR);
         if (head_owner) {                          // four independent sums, loads in flight together
-            const int h = hb + lane;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int r = 0; r < kTileRows; ++r) s4[r & 3] += lsc[r * (kHeads + 1) + h];
-            l_fin[h] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            for (int r = 0; r < kTileRows; ++r) s4[r & 3] += lsc[r * (kHeads + 1) + ho];
+            l_fin[ho] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        asm volatile("bar.sync 3, %0;" ::"n"(2 * kSoftmaxThreads) : "memory");
         // O^T lane 32 wq + lane holds latent columns 32 wq + lane + 128 i (an
         // M = 128 accumulator); this thread writes heads hb ..
         if (pair) {                                   // staged for the pair merge
@@ -615,7 +667,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             }
         }
         if (head_owner && !pair) {
-            const int h = hb + lane;
+            const int h = ho;
             const float l = l_fin[h];
             const float m = m_fin[h];
             if (final_out) {
