@@ -284,8 +284,10 @@ __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap*
                     fma2(b0, b1, wv.z, wv.w, fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f));
                 }
                 const float s = (a0 + a1) + (b0 + b1);
-                const int64_t nk = (int64_t)(G.L_last - (G.nq - 1 - j)) / kpool;
-                epi.emit(G, j, t_row, t_row < nk, u, row, s);
+                // visible: t_row < floor(rows seen by the query / kpool), without
+                // the (emulated) 64-bit division
+                const int64_t seen = (int64_t)(G.L_last - (G.nq - 1 - j));
+                epi.emit(G, j, t_row, (t_row + 1) * kpool <= seen, u, row, s);
             }
             tc_fence_before();
             __syncwarp();

@@ -89,6 +89,63 @@ def test_decode_step_matches_oracle(wl):
             check_attention(out[q], lse[q], r["out"], r["lse"], wl.dtype)
 
 
+# Structured indexer keys for the fused decode selection: the selected keys
+# concentrated in a few CTAs' ranges, and blocks of equal top scores, resolved
+# from the level-1 candidates or -- tie blocks larger than the candidate list --
+# by the two further histogram levels and the ranked emission at T.
+#   hot:        keys of a 1000-token window scaled by 3 (ReLU is positively
+#               homogeneous: those scores triple and fill the top)
+#   ties:       the query's best-scoring key vector, scaled by 3, repeated
+#               over 3000 tokens: equal top scores, the lowest indices win
+#   ties_over:  the same over 12000 tokens (k-pool: 12000 pools), more
+#               candidates than the list holds
+STRUCTURED = [
+    ("hot", [40000, 61000], 1, 2048),
+    ("hot", [5000], 1, 2048),                    # fewer key tiles than CTAs
+    ("ties", [40000], 1, 2048),
+    ("ties_over", [40000, 30000], 1, 2048),
+    ("hot", [64000, 9000], 4, 2048),             # k-pool: pool keys
+    ("ties_over", [200000], 4, 2048),
+]
+
+
+@pytest.mark.parametrize("kind,kv_lens,kpool,top_k", STRUCTURED,
+                         ids=[f"{k}-{'-'.join(map(str, L))}-p{p}" for k, L, p, _ in STRUCTURED])
+def test_decode_step_structured_scores(kind, kv_lens, kpool, top_k):
+    wl = workloads.small(f"struct_{kind}", kv_lens, top_k=top_k, kpool=kpool,
+                         rope=0 if kpool > 1 else 64, seed=21)
+    host = workloads.make(wl, "cpu")
+    k = host["k_idx"].clone()
+    key_off = np.concatenate([[0], np.cumsum([L // kpool for L in kv_lens])])
+    for i, L in enumerate(kv_lens):
+        n = L // kpool
+        k0 = int(key_off[i])
+        a = k0 + n // 3
+        if kind == "hot":
+            m = 1000 // kpool
+            k[a:a + m] = (k[a:a + m].float() * 3).to(k.dtype)
+        else:
+            m = 3000 if kind == "ties" else 12000
+            # the best key of the sequence for its query, by its score on the host
+            kk = host_f32(k[k0:k0 + n]).astype(np.float64)
+            qi = host_f32(host["q_idx"][i]).astype(np.float64)
+            wi = host_f32(host["w"][i]).astype(np.float64)
+            best = int(np.argmax(np.maximum(kk @ qi.T, 0) @ wi))
+            k[a:a + m] = (k[k0 + best].float() * 3).to(k.dtype).unsqueeze(0).expand(m, -1)
+    host["k_idx"] = k
+    out, lse, idx, n_sel = run_step(wl, to_device(host))
+    for q in range(wl.n_q):
+        r = oracle_query(wl, host, q)
+        sel = idx[q, : n_sel[q]]
+        check_selection(sel, r, wl.top_k, wl.kpool)
+        if kind != "hot":
+            # equal keys are bit-identical on both sides: the tie-break by
+            # index is exact
+            assert np.array_equal(sel, r["idx"])
+        o_ref, l_ref = oracle.sparse_mla(r["q_abs"], r["rows"], sel, wl.scale, wl.kv_lora)
+        check_attention(out[q], lse[q], o_ref, l_ref, wl.dtype)
+
+
 def test_dense_below_k_equals_dense_attention():
     """Below top-k the path is exactly dense attention over every visible row."""
     wl = workloads.small("dense", [700], top_k=2048)
