@@ -62,16 +62,25 @@ struct Cfg {
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     // decode batches plan their (query, key tile) units in shared memory
     static constexpr int kLocalMaxQ = 256;
-    static constexpr uint32_t kOffPlanG = (kOffMisc + 16 + 15) / 16 * 16;           // IdxGroup[256]
+    // grouped queries: each epilogue warp's copy of its two queries' head weights
+    static constexpr uint32_t kOffW = (kOffMisc + 16 + 15) / 16 * 16;
+    static constexpr uint32_t kOffPlanG = kOffW + (GQ > 1 ? kEpiWarps * 2 * kIdxHeads * 4 : 0);  // IdxGroup[256]
     static constexpr uint32_t kOffPlanT = kOffPlanG + kLocalMaxQ * 24;             // int64[257]
     static constexpr uint32_t kSmemBytes = kOffPlanT + (kLocalMaxQ + 1) * 8 + 1024;
     static_assert(kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
                   "TMEM allocation must be a power of two");
 };
 
-struct Cursor {                       // walks (group, tile) units in order
+// Walks (group, tile) units in order.  kCache keeps tile_off[g] and
+// tile_off[g + 1] in registers (read once per group: the grouped plan lives in
+// global memory); the decode plan is in shared memory and is read directly.
+template <bool kCache>
+struct Cursor {
     const int64_t* tile_off;
     int64_t g, t;
+    int64_t beg, end;                 // kCache: tile_off[g], tile_off[g + 1]
+    __device__ int64_t b0() const { return kCache ? beg : tile_off[g]; }
+    __device__ int64_t b1() const { return kCache ? end : tile_off[g + 1]; }
     __device__ void seek(int64_t u, int64_t n_groups) {
         int64_t lo = 0, hi = n_groups - 1;           // last g with tile_off[g] <= u
         while (lo < hi) {
@@ -79,13 +88,18 @@ struct Cursor {                       // walks (group, tile) units in order
             if (tile_off[mid] <= u) lo = mid; else hi = mid - 1;
         }
         g = lo;
+        if (kCache) { beg = tile_off[g]; end = tile_off[g + 1]; }
         t = u - tile_off[g];
     }
     __device__ void next() {
         ++t;
-        while (tile_off[g] + t >= tile_off[g + 1]) { ++g; t = 0; }
+        while (b0() + t >= b1()) {
+            ++g;
+            t = 0;
+            if (kCache) { beg = end; end = tile_off[g + 1]; }
+        }
     }
-    __device__ bool last_of_group() const { return tile_off[g] + t + 1 >= tile_off[g + 1]; }
+    __device__ bool last_of_group() const { return b0() + t + 1 >= b1(); }
 };
 
 // One group per query (decode batches of at most Cfg::kLocalMaxQ queries):
@@ -164,7 +178,7 @@ __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap*
 
     if (warp == 0) {
         if (lane == 0) {                                           // ---- TMA producer
-            Cursor c{tile_off, 0, 0};
+            Cursor<(GQ > 1)> c{tile_off, 0, 0, 0, 0};
             c.seek(u_begin, n_groups);
             int stage = 0;
             uint32_t phase = 0, b_empty_par = 0;
@@ -208,7 +222,7 @@ __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap*
     } else if (warp == 1) {
         if (lane == 0) {                                           // ---- MMA issuer
             constexpr uint32_t idesc = idesc_bf16_f32(kTileKeys, C::N);
-            Cursor c{tile_off, 0, 0};
+            Cursor<(GQ > 1)> c{tile_off, 0, 0, 0, 0};
             c.seek(u_begin, n_groups);
             int stage = 0, ab = 0;
             uint32_t phase = 0, acc_par = 0, b_full_par = 0;
@@ -255,13 +269,32 @@ __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap*
         const int wg = ew >> 2;                                    // epilogue warpgroup
         const int lane_base = 32 * (warp & 3);                     // this warp's TMEM lanes
         const int row = lane_base + lane;
-        Cursor c{tile_off, 0, 0};
+        // grouped queries: this warp's queries' head weights in its own slice of
+        // shared memory, refreshed when the group changes (warp-private: no
+        // synchronisation beyond the warp)
+        float* w_s = reinterpret_cast<float*>(smem + C::kOffW) + ew * 2 * kIdxHeads;
+        Cursor<(GQ > 1)> c{tile_off, 0, 0, 0, 0};
         c.seek(u_begin, n_groups);
         int ab = 0;
         uint32_t acc_par = 0;
         epi.begin();
+        int64_t g_loaded = -1;
+        IdxGroup G{};
         for (int64_t u = u_begin; u < u_end; ++u) {
-            const IdxGroup G = groups[c.g];
+            if (GQ == 1 || c.g != g_loaded) {                      // grouped: once per group
+                G = groups[c.g];
+                g_loaded = c.g;
+                if (GQ > 1) {
+                    __syncwarp();
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int j = wg + r * C::kEpiGroups;
+                        w_s[r * kIdxHeads + lane] =
+                            j < G.nq ? w[(int64_t)(G.q0 + j) * kIdxHeads + lane] : 0.f;
+                    }
+                    __syncwarp();
+                }
+            }
             if (*abort_flag || !mbar_wait(&acc_full[ab], acc_par, kWaitNs)) {
                 record_error(err, kDevTimeout, blockIdx.x, /*where=*/7);
                 *abort_flag = 1;
@@ -273,13 +306,15 @@ __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap*
                 float v[32];
                 tmem_ld_32cols(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(ab * C::N + 32 * j), v);
                 // the query's head weights: warp-uniform addresses, one broadcast each
-                const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)(G.q0 + j) * kIdxHeads);
+                const float4* w4 =
+                    GQ > 1 ? reinterpret_cast<const float4*>(w_s + ((j - wg) / C::kEpiGroups) * kIdxHeads)
+                           : reinterpret_cast<const float4*>(w + (int64_t)(G.q0 + j) * kIdxHeads);
                 // four partial sums (heads 4i, 4i+1, 4i+2, 4i+3 of each group of
                 // four), two packed FMAs per group: short dependency chains
                 float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
                 for (int h4 = 0; h4 < kIdxHeads / 4; ++h4) {
-                    const float4 wv = __ldg(w4 + h4);
+                    const float4 wv = GQ > 1 ? w4[h4] : __ldg(w4 + h4);
                     fma2(a0, a1, wv.x, wv.y, fmaxf(v[4 * h4 + 0], 0.f), fmaxf(v[4 * h4 + 1], 0.f));
                     fma2(b0, b1, wv.z, wv.w, fmaxf(v[4 * h4 + 2], 0.f), fmaxf(v[4 * h4 + 3], 0.f));
                 }
