@@ -58,9 +58,11 @@ def _load():
             lib.oracle_dense_masked_mla.argtypes = [P, P, i64, i32, i32, i32, f64, P, P, P]
             lib.oracle_decode_step.argtypes = [P, P, P, i32, i32, P, P, i64, i32, i32, i32,
                                                f64, i64, i32, P, P, P, P, P]
+            lib.oracle_pool_compress.argtypes = [P, i64, P, i32, i32, P]
+            lib.oracle_new_pools.argtypes = [i64, i64, i32, P, P]
             for fn in (lib.oracle_index_scores, lib.oracle_topk, lib.oracle_kpool_select,
                        lib.oracle_sparse_mla, lib.oracle_dense_masked_mla,
-                       lib.oracle_decode_step):
+                       lib.oracle_decode_step, lib.oracle_pool_compress, lib.oracle_new_pools):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -174,3 +176,26 @@ def decode_step(q_idx, w, keys, q_abs, rows, L: int, k: int, kpool: int, scale: 
 
 if __name__ == "__main__":  # pragma: no cover - manual build helper
     print(build(force="--force" in sys.argv))
+
+
+def pool_compress(cells, pos) -> np.ndarray:
+    """Compressed keys of complete pools: cells [n_pools, kpool, 2*dim] ([key | gate]
+    per cell), pos [kpool, dim] -> [n_pools, dim] float64 (softmax over the slots of
+    gate + pos, per channel, weighting the keys)."""
+    cells, pos = _f32(cells), _f32(pos)
+    n_pools, kpool, w2 = cells.shape
+    dim = w2 // 2
+    assert w2 == 2 * dim and pos.shape == (kpool, dim)
+    out = np.empty((n_pools, dim), dtype=np.float64)
+    _check(_load().oracle_pool_compress(_ptr(cells) if n_pools else None, n_pools, _ptr(pos),
+                                        kpool, dim, _ptr(out) if n_pools else None),
+           "oracle_pool_compress")
+    return out
+
+
+def new_pools(L: int, q_len: int, kpool: int):
+    """(j0, j1): the complete pools whose last token is among the last q_len of L."""
+    j0, j1 = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(_load().oracle_new_pools(L, q_len, kpool, ctypes.byref(j0), ctypes.byref(j1)),
+           "oracle_new_pools")
+    return j0.value, j1.value

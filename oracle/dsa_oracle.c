@@ -203,3 +203,41 @@ int oracle_decode_step(const float *q_idx, const float *w, const float *keys,
     if (sc != scores_out) free(sc);
     return rc;
 }
+
+int oracle_pool_compress(const float *cells, int64_t n_pools, const float *pos, int32_t kpool,
+                         int32_t dim, double *out)
+{
+    if (n_pools < 0 || kpool <= 0 || dim <= 0) return -1;
+    if (n_pools > 0 && (!cells || !pos || !out)) return -1;
+    const int64_t cell_w = 2 * (int64_t)dim;               /* key then gate */
+#pragma omp parallel for schedule(static)
+    for (int64_t p = 0; p < n_pools; p++) {
+        const float *pool = cells + p * kpool * cell_w;
+        for (int32_t c = 0; c < dim; c++) {
+            /* logits of the slots: the cell's gate plus its slot's embedding */
+            double zmax = -INFINITY;
+            for (int32_t i = 0; i < kpool; i++) {
+                const double z = (double)pool[i * cell_w + dim + c] + (double)pos[(int64_t)i * dim + c];
+                if (z > zmax) zmax = z;
+            }
+            /* softmax over the slots (max-subtracted), weighted sum of the keys */
+            double den = 0.0, num = 0.0;
+            for (int32_t i = 0; i < kpool; i++) {
+                const double z = (double)pool[i * cell_w + dim + c] + (double)pos[(int64_t)i * dim + c];
+                const double e = exp(z - zmax);
+                den += e;
+                num += e * (double)pool[i * cell_w + c];
+            }
+            out[p * dim + c] = num / den;
+        }
+    }
+    return 0;
+}
+
+int oracle_new_pools(int64_t L, int64_t q_len, int32_t kpool, int64_t *j0, int64_t *j1)
+{
+    if (L < 0 || q_len < 0 || q_len > L || kpool <= 0 || !j0 || !j1) return -1;
+    *j0 = (L - q_len) / kpool;
+    *j1 = L / kpool;
+    return 0;
+}

@@ -102,6 +102,31 @@ int oracle_decode_step(const float *q_idx, const float *w, const float *keys,
                        double *scores_out, int32_t *idx, int64_t *n_sel,
                        double *out, double *lse);
 
+/* Pool-key compression ([GLM-DOC] "GLM-5.3-Flash (glm5next)" table, row
+ * "Pooled indexer": each cell caches [key|gate], a softmax over the gates plus
+ * a per-slot position embedding compresses each pool; [WASTE] "DeepSeek Sparse
+ * Attention, k-pool flavour": one 128-wide key per pool of kpool tokens, made
+ * once, when the pool's last token arrives).
+ *   cells [n_pools * kpool * 2 * dim]  the pools' cells in token order, each
+ *                                      cell = key[dim] then gate[dim]
+ *   pos   [kpool * dim]                position embedding of slot i (the
+ *                                      cell's place in its pool)
+ *   out   [n_pools * dim]              out: for pool p and channel c,
+ *     z_i = gate_i[c] + pos[i][c]  (i < kpool: the pool's cells in order)
+ *     a_i = exp(z_i) / sum_j exp(z_j)          softmax over the slots
+ *     out[p][c] = sum_i a_i * key_i[c]
+ * Readings (the pages name the parts, not the formula): the gate has the key's
+ * width (one softmax per channel), and the position embedding is added to the
+ * gate logits inside the softmax. */
+int oracle_pool_compress(const float *cells, int64_t n_pools, const float *pos, int32_t kpool,
+                         int32_t dim, double *out);
+
+/* The pools a call writes for a sequence of L tokens whose last q_len tokens
+ * are new ([WASTE]: a pool's key is computed once, when its last token
+ * arrives): pools j0 <= j < j1 with j0 = floor((L - q_len) / kpool) and
+ * j1 = floor(L / kpool) -- the complete pools whose last token is new. */
+int oracle_new_pools(int64_t L, int64_t q_len, int32_t kpool, int64_t *j0, int64_t *j1);
+
 #ifdef __cplusplus
 }
 #endif

@@ -342,6 +342,116 @@ def test_decode_step_kpool_nope_composition():
     np.testing.assert_array_equal(r["out"], o)
 
 
+# ---------------------------------------------------------------- pool-key compression
+# "GLM-5.x (glm-dsa, glm5next)", table "GLM-5.3-Flash", row "Pooled indexer":
+# [key|gate] per cell, a softmax over the gates plus a per-slot position
+# embedding compresses each pool.  "GLM-5.3-Flash on WASTE", "DeepSeek Sparse
+# Attention, k-pool flavour": one 128-wide key per pool of 4 tokens.
+
+def _cells(keys, gates):
+    """[n_pools, kpool, dim] keys and gates -> [n_pools, kpool, 2*dim] cells."""
+    return np.concatenate([keys, gates], axis=2).astype(np.float32)
+
+
+def test_pool_compress_equal_logits_give_the_mean_key():
+    """Equal gates and a zero embedding: every slot weighs 1/kpool."""
+    rng = np.random.default_rng(40)
+    keys = rng.integers(-8, 9, size=(5, 4, 128)).astype(np.float32)
+    gates = np.tile(rng.standard_normal((5, 1, 128)).astype(np.float32), (1, 4, 1))
+    out = oracle.pool_compress(_cells(keys, gates), np.zeros((4, 128), np.float32))
+    np.testing.assert_allclose(out, keys.astype(np.float64).mean(axis=1), rtol=0, atol=1e-12)
+
+
+def test_pool_compress_position_embedding_weights_the_slots():
+    """Zero gates and pos_i = ln(i + 1): the weights are 1/10, 2/10, 3/10, 4/10
+    in slot order -- the embedding sits inside the softmax, per slot."""
+    keys = np.zeros((1, 4, 128), np.float32)
+    keys[0, :, 0] = [10, 20, 30, 40]                    # channel 0: 1 + 4 + 9 + 16 = 30
+    keys[0, :, 1] = [1, 0, 0, 0]                        # channel 1: the first weight, 0.1
+    keys[0, :, 2] = [0, 0, 0, 1]                        # channel 2: the last weight, 0.4
+    pos = np.tile(np.log(np.arange(1, 5, dtype=np.float64)).astype(np.float32)[:, None], (1, 128))
+    out = oracle.pool_compress(_cells(keys, np.zeros_like(keys)), pos)
+    np.testing.assert_allclose(out[0, :3], [30.0, 0.1, 0.4], rtol=1e-6)
+    assert np.all(out[0, 3:] == 0.0)
+
+
+def test_pool_compress_dominant_gate_selects_its_key():
+    rng = np.random.default_rng(41)
+    keys = rng.standard_normal((3, 4, 128)).astype(np.float32)
+    gates = rng.standard_normal((3, 4, 128)).astype(np.float32)
+    gates[:, 2, :] += 60.0                              # slot 2 outweighs the others by e^55
+    out = oracle.pool_compress(_cells(keys, gates), np.zeros((4, 128), np.float32))
+    np.testing.assert_allclose(out, keys[:, 2, :].astype(np.float64), rtol=0, atol=1e-20)
+
+
+def test_pool_compress_softmax_runs_over_the_slots_per_channel():
+    """Keys all one: the output is one in every channel (the slot weights of a
+    channel sum to one -- a softmax over channels would not give this); a shift
+    of one channel's four gates leaves that channel unchanged."""
+    rng = np.random.default_rng(42)
+    gates = (3 * rng.standard_normal((4, 4, 128))).astype(np.float32)
+    pos = rng.standard_normal((4, 128)).astype(np.float32)
+    ones = oracle.pool_compress(_cells(np.ones((4, 4, 128), np.float32), gates), pos)
+    np.testing.assert_allclose(ones, 1.0, rtol=0, atol=1e-14)
+    keys = rng.standard_normal((4, 4, 128)).astype(np.float32)
+    shift = np.zeros((4, 1, 128), np.float32)
+    shift[:, :, 5] = 7.0                                # exact in float: small-integer shift
+    a = oracle.pool_compress(_cells(keys, gates), pos)
+    b = oracle.pool_compress(_cells(keys, np.round(gates) + shift), pos)
+    c = oracle.pool_compress(_cells(keys, np.round(gates)), pos)
+    np.testing.assert_allclose(b, c, rtol=1e-12, atol=1e-12)
+    assert np.all(a.min() >= keys.min()) and np.all(a.max() <= keys.max())
+    # each output lies between the smallest and largest key of its channel
+    assert np.all(a >= keys.min(axis=1) - 1e-12) and np.all(a <= keys.max(axis=1) + 1e-12)
+
+
+def test_pool_compress_slot_order_and_pool_independence():
+    """Permuting the cells of a pool together with the embedding rows leaves the
+    key unchanged; permuting the cells alone changes it (the embedding belongs to
+    the slot); each pool depends only on its own cells."""
+    rng = np.random.default_rng(43)
+    keys = rng.standard_normal((6, 4, 128)).astype(np.float32)
+    gates = rng.standard_normal((6, 4, 128)).astype(np.float32)
+    pos = (2 * rng.standard_normal((4, 128))).astype(np.float32)
+    base = oracle.pool_compress(_cells(keys, gates), pos)
+    perm = np.array([2, 0, 3, 1])
+    both = oracle.pool_compress(_cells(keys[:, perm], gates[:, perm]), pos[perm])
+    np.testing.assert_allclose(both, base, rtol=1e-12, atol=1e-12)
+    cells_only = oracle.pool_compress(_cells(keys[:, perm], gates[:, perm]), pos)
+    assert np.abs(cells_only - base).max() > 1e-3
+    alone = np.stack([oracle.pool_compress(_cells(keys[p:p + 1], gates[p:p + 1]), pos)[0]
+                      for p in range(6)])
+    assert np.array_equal(alone, base)
+
+
+def test_pool_compress_rival_reading_fails():
+    """The embedding added to the keys (after a softmax of the gates alone) is a
+    plausible misreading: with zero gates it would give mean(key) + mean(pos)."""
+    keys = np.zeros((1, 4, 128), np.float32)
+    keys[0, :, 0] = [10, 20, 30, 40]
+    pos = np.tile(np.log(np.arange(1, 5, dtype=np.float64)).astype(np.float32)[:, None], (1, 128))
+    out = oracle.pool_compress(_cells(keys, np.zeros_like(keys)), pos)
+    rival = keys[0, :, 0].astype(np.float64).mean() + pos[:, 0].astype(np.float64).mean()
+    assert abs(out[0, 0] - rival) > 1.0
+
+
+def test_new_pools_golden_table():
+    for r in _table("new_pools.txt"):
+        L, q_len, kpool, j0, j1 = (int(x) for x in r[:5])
+        assert oracle.new_pools(L, q_len, kpool) == (j0, j1), r
+
+
+def test_new_pools_brute_force():
+    """A pool is made by the call iff its last token is one of the new tokens."""
+    for kpool in (1, 2, 4, 5):
+        for L in range(0, 23):
+            for q_len in range(0, L + 1):
+                made = [j for j in range(L // kpool)
+                        if L - q_len <= kpool * j + kpool - 1 < L]
+                j0, j1 = oracle.new_pools(L, q_len, kpool)
+                assert list(range(j0, j1)) == made, (L, q_len, kpool)
+
+
 def test_oracle_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.sparse_mla(np.zeros((2, 8), np.float32), np.zeros((4, 8), np.float32),
