@@ -505,6 +505,38 @@ def run_ours(args):
         if dsa.dsa_check_device_error(ws_s, stream) != 0:
             raise RuntimeError("device error in the fused selection loop")
 
+    # k-pool workloads: the pool-key compression of every pool of the
+    # workload's sequences (q_len = kv_len: a prefill's worth of cells, seeded
+    # synthetic [key | gate] cells and slot embedding), timed alone
+    pool = None
+    if wl.kpool > 1:
+        gen = torch.Generator(device=dev).manual_seed(wl.seed + 4242)
+        n_rows = sum(wl.kv_lens)
+        cells = torch.randn((n_rows, 2 * wl.idx_dim), generator=gen, device=dev).to(keys[0].dtype)
+        pos = 0.5 * torch.randn((wl.kpool, wl.idx_dim), generator=gen, device=dev)
+        pkeys = torch.empty_like(keys[0])
+        bp = dsa.make_batch(d["row_off"], d["key_off"], d["row_off"], n_rows, max(wl.kv_lens),
+                            max(wl.kv_lens), n_rows, sum(wl.key_counts()))
+        ws_p = dsa.alloc_workspace(sh, bp, dsa.OP_POOL_COMPRESS, dev)
+        for i in range(3):
+            dsa.dsa_pool_compress(sh, bp, cells, pos, pkeys, ws_p, stream)
+        n_pc = 10
+        k0.record(stream)
+        for i in range(n_pc):
+            dsa.dsa_pool_compress(sh, bp, cells, pos, pkeys, ws_p, stream)
+        k1.record(stream)
+        torch.cuda.synchronize(dev)
+        if dsa.dsa_check_device_error(ws_p, stream) != 0:
+            raise RuntimeError("device error in the pool compression loop")
+        pc_ms = k0.elapsed_time(k1) / n_pc
+        n_pools = sum(L // wl.kpool for L in wl.kv_lens)
+        esz = cells.element_size()
+        pc_bytes = n_pools * (wl.kpool * 2 * wl.idx_dim + wl.idx_dim) * esz + pos.numel() * 4
+        pool = {"kernel": "pool_compress", "launch_us": pc_ms * 1e3, "pools": n_pools,
+                "work": "every pool of the workload's sequences: cells [key | gate] -> pool keys",
+                "bytes_per_launch": pc_bytes, "achieved_gbs": pc_bytes / (pc_ms / 1e3) / 1e9}
+        del cells, pkeys
+
     # end to end through the public call: pinned host inputs in, result out
     e2e = None
     if not args.no_e2e:
@@ -590,6 +622,10 @@ def run_ours(args):
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if pool is not None:
+        pool["frac"] = pool["achieved_gbs"] / peaks["hbm_gbs"]
+        pool["peak_source"] = f"{peak_src} hbm_gbs"
+        line["pool_compress"] = pool
     if not args.no_cpu_baseline:
         n, el, threads = oracle_sample(wl, host_query_args(wl, d), args.cpu_seconds)
         line["cpu_baseline"] = {

@@ -33,12 +33,14 @@ __all__ = [
     "dsa_sparse_mla_attn",
     "dsa_decode_step", "dsa_decode_step_noalloc", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
     "OP_INDEX_SCORES", "OP_TOPK_SELECT", "OP_SPARSE_MLA", "OP_DECODE_STEP", "OP_INDEX_SELECT",
+    "OP_POOL_COMPRESS", "dsa_pool_compress",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
 
 DSA_F32, DSA_BF16 = 0, 1
 OP_INDEX_SCORES, OP_TOPK_SELECT, OP_SPARSE_MLA, OP_DECODE_STEP, OP_INDEX_SELECT = 0, 1, 2, 3, 4
+OP_POOL_COMPRESS = 5
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
           3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE", 6: "DSA_ERR_TIMEOUT"}
 
@@ -100,6 +102,7 @@ def load() -> ctypes.CDLL:
             "dsa_decode_step": ([S, B, P, P, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_check_device_error": ([P, sz, P, ctypes.POINTER(i32)], ctypes.c_int),
             "dsa_decode_step_noalloc": ([S, B, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "dsa_pool_compress": ([S, B, P, P, P, P, sz, P], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -230,6 +233,12 @@ def dsa_decode_step_noalloc(shape, batch, q_idx, w, k_idx, q_abs, cache, out, ls
     _call("dsa_decode_step_noalloc", ctypes.byref(shape), ctypes.byref(batch), _ptr(q_idx),
           _ptr(w), _ptr(k_idx), _ptr(q_abs), _ptr(cache), _ptr(out), _ptr(lse), _ptr(idx_out),
           _ptr(n_sel_out), _stream(stream))
+
+
+def dsa_pool_compress(shape, batch, cells, pos, pool_keys, ws, stream=None) -> None:
+    """Compressed keys of the pools completed by each sequence's new tokens (see dsa.h)."""
+    _call("dsa_pool_compress", ctypes.byref(shape), ctypes.byref(batch), _ptr(cells), _ptr(pos),
+          _ptr(pool_keys), _ptr(ws), ws.numel(), _stream(stream))
 
 
 def dsa_check_device_error(ws: torch.Tensor, stream=None) -> int:

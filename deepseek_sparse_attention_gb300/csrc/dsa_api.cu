@@ -48,7 +48,10 @@ dsa_status check_shape(const dsa_shape* s, Shape* out) {
     return DSA_OK;
 }
 
-dsa_status check_batch(const dsa_batch* b, const Shape& sh, BatchDev* out) {
+// max_n_q: the query count this entry point's grids take (the queries of the
+// pool compression are the new tokens, which a prompt may have millions of).
+dsa_status check_batch(const dsa_batch* b, const Shape& sh, BatchDev* out,
+                       int64_t max_n_q = 65535) {
     if (b == nullptr) return DSA_ERR_INVALID_ARG;
     if (b->n_seq < 0 || b->n_q < 0 || b->max_q_len < 0 || b->max_kv_len < 0 || b->reserved != 0 ||
         b->total_rows < 0 || b->total_keys < 0)
@@ -61,7 +64,7 @@ dsa_status check_batch(const dsa_batch* b, const Shape& sh, BatchDev* out) {
         if (b->total_rows < 1) return DSA_ERR_INVALID_ARG;
     }
     if (b->max_kv_len >= ((int64_t)1 << 31)) return DSA_ERR_UNSUPPORTED;
-    if (b->n_q > 65535) return DSA_ERR_UNSUPPORTED;
+    if (b->n_q > max_n_q) return DSA_ERR_UNSUPPORTED;
     *out = BatchDev{b->row_off,    b->key_off,    b->q_off,      b->n_seq, b->n_q,
                     b->max_q_len,  b->max_kv_len, b->total_rows, b->total_keys, sh.kpool};
     return DSA_OK;
@@ -108,6 +111,7 @@ size_t op_bytes(const Shape& sh, const BatchDev& b, int32_t op) {
             return align_up(kWsHeaderBytes + sparse_mla_scratch_bytes(sh, b));
         case DSA_OP_DECODE_STEP: return step_layout(sh, b).total;
         case DSA_OP_INDEX_SELECT: return step_layout(sh, b).attn;
+        case DSA_OP_POOL_COMPRESS: return kWsHeaderBytes;
         default: return 0;
     }
 }
@@ -187,11 +191,13 @@ dsa_status dsa_workspace_size(const dsa_shape* shape, const dsa_batch* batch, in
     if (s != DSA_OK) return s;
     // Sizing needs only the host scalars of the batch.
     if (batch == nullptr || batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
-    if (batch->max_kv_len >= ((int64_t)1 << 31) || batch->n_q > 65535) return DSA_ERR_UNSUPPORTED;
+    if (batch->max_kv_len >= ((int64_t)1 << 31) ||
+        (batch->n_q > 65535 && op != DSA_OP_POOL_COMPRESS))
+        return DSA_ERR_UNSUPPORTED;
     b = BatchDev{nullptr,           nullptr,           nullptr,           batch->n_seq,
                  batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
                  batch->total_keys, sh.kpool};
-    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_INDEX_SELECT) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_POOL_COMPRESS) return DSA_ERR_INVALID_ARG;
     *out_bytes = op_bytes(sh, b, op);
     return DSA_OK;
 }
@@ -203,7 +209,7 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
     dsa_status s = check_shape(shape, &sh);
     if (s != DSA_OK) return s;
     if (batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
-    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_INDEX_SELECT) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_POOL_COMPRESS) return DSA_ERR_INVALID_ARG;
     const BatchDev bh{nullptr,           nullptr,           nullptr,           batch->n_seq,
                       batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
                       batch->total_keys, sh.kpool};
@@ -222,6 +228,7 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
             case DSA_OP_TOPK_SELECT: n = 1; break;
             case DSA_OP_SPARSE_MLA: n = attn; break;
             case DSA_OP_INDEX_SELECT: n = index_select_fused_eligible(sh, bh) ? 1 : idx + 1; break;
+            case DSA_OP_POOL_COMPRESS: n = sh.kpool > 1 ? 1 : 0; break;
             default: n = (index_select_fused_eligible(sh, bh) ? 1 : idx + 1) + attn; break;
         }
     }
@@ -289,6 +296,27 @@ dsa_status dsa_sparse_mla_attn(const dsa_shape* shape, const dsa_batch* batch, c
                                          bytes(ws) + kWsHeaderBytes, need - kWsHeaderBytes, err,
                                          static_cast<cudaStream_t>(stream)),
                        "sparse_mla_attn");
+}
+
+dsa_status dsa_pool_compress(const dsa_shape* shape, const dsa_batch* batch, const void* cells,
+                             const float* pos, void* pool_keys, void* ws, size_t ws_bytes,
+                             void* stream) {
+    Shape sh;
+    BatchDev b;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if (sh.kpool < 2) return DSA_ERR_INVALID_ARG;          // token mode has no pools
+    if ((s = check_batch(batch, sh, &b, 0x7fffffff)) != DSA_OK) return s;
+    if (b.n_seq > 65535) return DSA_ERR_UNSUPPORTED;
+    if (b.n_q > 0 && (cells == nullptr || pos == nullptr || pool_keys == nullptr))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(cells) || !aligned16(pos) || !aligned16(pool_keys)) return DSA_ERR_INVALID_ARG;
+    if ((s = check_ws(ws, ws_bytes, op_bytes(sh, b, DSA_OP_POOL_COMPRESS))) != DSA_OK) return s;
+    if (b.n_q == 0) return DSA_OK;
+    int32_t* err = static_cast<int32_t*>(ws);
+    return cuda_status(launch_pool_compress(sh, b, cells, pos, pool_keys, err,
+                                            static_cast<cudaStream_t>(stream)),
+                       "pool_compress");
 }
 
 dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const void* q_idx,

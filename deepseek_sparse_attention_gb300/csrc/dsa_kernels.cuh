@@ -83,6 +83,14 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
                                       int64_t ld, int32_t* idx, int32_t* n_sel, void* state,
                                       uint32_t* gbar, int32_t* err, cudaStream_t st);
 
+// Pool-key compression (pool_compress.cu): the complete pools of each sequence
+// whose last token is one of its new tokens (q_off), from the per-row cells
+// [key | gate] (2 x 128 values, dtype) and the per-slot embedding pos
+// [kpool, 128] float32, into pool_keys at key_off (dtype).
+cudaError_t launch_pool_compress(const Shape& sh, const BatchDev& b, const void* cells,
+                                 const float* pos, void* pool_keys, int32_t* err,
+                                 cudaStream_t st);
+
 // Step 3.  bf16 rows run on the tensor cores (sparse_mla_tc.cu), float32 rows
 // on CUDA cores (sparse_mla.cu).  Row splits per query and the scratch for the
 // split-row partials (bytes; 0 if none is needed).

@@ -126,6 +126,7 @@ int64_t dsa_index_row_width(const dsa_shape *shape);
 #define DSA_OP_SPARSE_MLA 2
 #define DSA_OP_DECODE_STEP 3
 #define DSA_OP_INDEX_SELECT 4
+#define DSA_OP_POOL_COMPRESS 5
 dsa_status dsa_workspace_size(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
                               size_t *bytes);
 
@@ -192,6 +193,38 @@ dsa_status dsa_topk_select(const dsa_shape *shape, const dsa_batch *batch, const
 dsa_status dsa_index_select(const dsa_shape *shape, const dsa_batch *batch, const void *q_idx,
                             const float *w, const void *k_idx, int32_t *idx, int32_t *n_sel,
                             void *ws, size_t ws_bytes, void *stream);
+
+/* Pool-key compression for the k-pool indexer ("GLM-5.x (glm-dsa, glm5next)",
+ * table "GLM-5.3-Flash", row "Pooled indexer": each cell caches [key|gate], and
+ * a softmax over the gates plus a per-slot position embedding compresses each
+ * pool; "GLM-5.3-Flash on WASTE", "DeepSeek Sparse Attention, k-pool flavour":
+ * one 128-wide key per pool of kpool tokens, computed once, when the pool's last
+ * token arrives).  Requires kpool >= 2.
+ *   cells     [total_rows, 2 * idx_dim] dtype: one cell per cache row (token),
+ *             its key then its gate; the cells of sequence s start at
+ *             row_off[s], like its cache rows
+ *   pos       [kpool, idx_dim] float32: position embedding of slot i, the
+ *             place of a token in its pool
+ *   pool_keys [total_keys, idx_dim] dtype, in/out: the k_idx array of the
+ *             k-pool entry points (pool j of sequence s at key_off[s] + j)
+ * For every sequence s (kv_len_s rows, the last q_len_s of them new) and every
+ * pool j with floor((kv_len_s - q_len_s) / kpool) <= j < floor(kv_len_s / kpool)
+ * -- the complete pools whose last token is new --
+ *     z_i[c] = gate(kpool*j + i)[c] + pos[i][c]            (i < kpool)
+ *     pool_keys[key_off[s] + j][c] = sum_i softmax_i(z[c]) * key(kpool*j + i)[c]
+ * computed in float32 and rounded to dtype; no other pool key is written and no
+ * other cell is read.  A decode step (q_len 1) writes a key exactly when its
+ * token completes a pool; a chunk writes the pools it completes; q_len_s =
+ * kv_len_s writes them all.  The batch's queries are only the new tokens here:
+ * n_q = q_off[n_seq] (not limited to 65535 for this entry point), max_q_len
+ * bounds each q_len_s.  A sequence whose offsets
+ * break the host bounds is skipped and sets the error word.  The gate has the
+ * key's width and the embedding is added to the gate logits: the pages name the
+ * parts of the compressor, not its formula.  Workspace: dsa_workspace_size
+ * (DSA_OP_POOL_COMPRESS), the 256-byte header (the error word). */
+dsa_status dsa_pool_compress(const dsa_shape *shape, const dsa_batch *batch, const void *cells,
+                             const float *pos, void *pool_keys, void *ws, size_t ws_bytes,
+                             void *stream);
 
 /* Step 3: absorbed-MLA attention over the selected rows ("GLM 5.2 in one C
  * file", MLA decode path; "GLM-5.x", "The block").

@@ -79,7 +79,9 @@ def test_workspace_sizes(lib):
     assert rc == 0 and rc2 == 0 and n_sel % 256 == 0
     assert 256 + 131072 * 4 <= n_sel <= n_step
     assert n_sel >= 256 + 16 * 21508 * 4 + 16 * 256 * 8          # DSA_WS_ZERO_BYTES of dsa.h
-    rc, _ = _size(sh, _batch(), 5)
+    rc, n = _size(sh, _batch(), dsa.OP_POOL_COMPRESS)     # the header: the error word
+    assert rc == 0 and n == 256
+    rc, _ = _size(sh, _batch(), 6)
     assert rc == 1
     rc, _ = _size(sh, _batch(), 7)
     assert rc == 1
@@ -130,6 +132,25 @@ def test_entry_points_reject_before_enqueue(lib):
     assert lib.dsa_decode_step(ctypes.byref(sh), ctypes.byref(b), good, good, good, good, good,
                                good, None, None, None, good, 16, None) == 3   # ws too small
     assert lib.dsa_check_device_error(None, 0, None, None) == 3
+
+
+def test_pool_compress_rejects_before_enqueue(lib):
+    """dsa_pool_compress: token mode has no pools, and the usual argument,
+    alignment and workspace checks run before anything is enqueued."""
+    P = ctypes.c_void_p
+    good = P(256)
+    b = _batch()
+    sh1, sh4 = dsa.make_shape(kpool=1), dsa.make_shape(kpool=4, rope_dim=0)
+    f = lib.dsa_pool_compress
+    assert f(ctypes.byref(sh1), ctypes.byref(b), good, good, good, good, 256, None) == 1
+    assert f(ctypes.byref(sh4), ctypes.byref(b), None, good, good, good, 256, None) == 1
+    assert f(ctypes.byref(sh4), ctypes.byref(b), good, P(260), good, good, 256, None) == 1
+    assert f(ctypes.byref(sh4), ctypes.byref(b), good, good, good, good, 16, None) == 3
+    assert f(ctypes.byref(sh4), ctypes.byref(b), good, good, good, P(264), 256, None) == 3
+    assert f(ctypes.byref(sh4), ctypes.byref(_batch(max_q=2, max_kv=1)), good, good, good, good,
+             256, None) == 1
+    plan = dsa.dsa_plan(sh4, b, dsa.OP_POOL_COMPRESS)
+    assert plan["kernel_launches"] == 1
 
 
 def test_python_binding_rejects_host_tensors(lib):
