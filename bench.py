@@ -625,6 +625,7 @@ def run_ours(args):
     if pool is not None:
         pool["frac"] = pool["achieved_gbs"] / peaks["hbm_gbs"]
         pool["peak_source"] = f"{peak_src} hbm_gbs"
+        pool["traffic"] = kernel_traffic("pool_compress", wl.name)
         line["pool_compress"] = pool
     if not args.no_cpu_baseline:
         n, el, threads = oracle_sample(wl, host_query_args(wl, d), args.cpu_seconds)
