@@ -60,9 +60,13 @@ def _load():
                                                f64, i64, i32, P, P, P, P, P]
             lib.oracle_pool_compress.argtypes = [P, i64, P, i32, i32, P]
             lib.oracle_new_pools.argtypes = [i64, i64, i32, P, P]
+            lib.oracle_hadamard.argtypes = [P, i32, P]
+            lib.oracle_rope.argtypes = [P, i32, i32, f64, i64, P]
+            lib.oracle_index_prepare.argtypes = [P, P, i64, i32, i32, f64, P]
             for fn in (lib.oracle_index_scores, lib.oracle_topk, lib.oracle_kpool_select,
                        lib.oracle_sparse_mla, lib.oracle_dense_masked_mla,
-                       lib.oracle_decode_step, lib.oracle_pool_compress, lib.oracle_new_pools):
+                       lib.oracle_decode_step, lib.oracle_pool_compress, lib.oracle_new_pools,
+                       lib.oracle_hadamard, lib.oracle_rope, lib.oracle_index_prepare):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -199,3 +203,32 @@ def new_pools(L: int, q_len: int, kpool: int):
     _check(_load().oracle_new_pools(L, q_len, kpool, ctypes.byref(j0), ctypes.byref(j1)),
            "oracle_new_pools")
     return j0.value, j1.value
+
+
+def hadamard(x) -> np.ndarray:
+    """H x with H the orthonormal Sylvester-Hadamard matrix (len(x) a power of two)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    _check(_load().oracle_hadamard(_ptr(x), x.shape[0], _ptr(out)), "oracle_hadamard")
+    return out
+
+
+def rope(x, rope_dims: int, base: float, pos: int) -> np.ndarray:
+    """Rotary embedding of adjacent pairs of the first rope_dims dims at position pos."""
+    x = _f32(x)
+    out = np.empty(x.shape[0], dtype=np.float64)
+    _check(_load().oracle_rope(_ptr(x), x.shape[0], rope_dims, float(base), int(pos), _ptr(out)),
+           "oracle_rope")
+    return out
+
+
+def index_prepare(x, pos, rope_dims: int, base: float) -> np.ndarray:
+    """H rope(x[v], pos[v]) for each row v of x [n, dim] (float64 out)."""
+    x = _f32(x)
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    n, dim = x.shape
+    out = np.empty((n, dim), dtype=np.float64)
+    _check(_load().oracle_index_prepare(_ptr(x) if n else None, _ptr(p) if n else None, n, dim,
+                                        rope_dims, float(base), _ptr(out) if n else None),
+           "oracle_index_prepare")
+    return out

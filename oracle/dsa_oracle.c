@@ -241,3 +241,51 @@ int oracle_new_pools(int64_t L, int64_t q_len, int32_t kpool, int64_t *j0, int64
     *j1 = L / kpool;
     return 0;
 }
+
+int oracle_hadamard(const double *x, int32_t n, double *out)
+{
+    if (n <= 0 || (n & (n - 1)) != 0 || !x || !out || x == out) return -1;
+    const double norm = 1.0 / sqrt((double)n);
+    for (int32_t i = 0; i < n; i++) {
+        double s = 0.0;
+        for (int32_t j = 0; j < n; j++) {
+            const int odd = __builtin_popcount((unsigned)(i & j)) & 1;   /* sign (-1)^popcount */
+            s += odd ? -x[j] : x[j];
+        }
+        out[i] = s * norm;
+    }
+    return 0;
+}
+
+int oracle_rope(const float *x, int32_t dim, int32_t rope_dims, double base, int64_t pos,
+                double *out)
+{
+    if (dim <= 0 || rope_dims < 0 || rope_dims > dim || (rope_dims & 1) || !(base > 0.0) ||
+        !x || !out)
+        return -1;
+    for (int32_t i = 0; i < rope_dims / 2; i++) {
+        const double theta = pow(base, -2.0 * i / (double)rope_dims);
+        const double a = (double)pos * theta;
+        const double c = cos(a), s = sin(a);
+        const double x0 = x[2 * i], x1 = x[2 * i + 1];
+        out[2 * i] = x0 * c - x1 * s;
+        out[2 * i + 1] = x0 * s + x1 * c;
+    }
+    for (int32_t d = rope_dims; d < dim; d++) out[d] = x[d];
+    return 0;
+}
+
+int oracle_index_prepare(const float *x, const int64_t *pos, int64_t n, int32_t dim,
+                         int32_t rope_dims, double base, double *out)
+{
+    if (n < 0 || dim <= 0 || dim > 4096) return -1;
+    if (n > 0 && (!x || !pos || !out)) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(|:bad)
+    for (int64_t v = 0; v < n; v++) {
+        double r[4096];
+        bad |= oracle_rope(x + v * dim, dim, rope_dims, base, pos[v], r) != 0;   /* rope first */
+        bad |= oracle_hadamard(r, dim, out + v * dim) != 0;                      /* then rotate */
+    }
+    return bad ? -1 : 0;
+}

@@ -127,6 +127,30 @@ int oracle_pool_compress(const float *cells, int64_t n_pools, const float *pos, 
  * j1 = floor(L / kpool) -- the complete pools whose last token is new. */
 int oracle_new_pools(int64_t L, int64_t q_len, int32_t kpool, int64_t *j0, int64_t *j1);
 
+/* Walsh-Hadamard rotation of one n-vector (n a power of two): out = H x with
+ * H[i][j] = (-1)^popcount(i & j) / sqrt(n), the orthonormal Sylvester-Hadamard
+ * matrix -- symmetric and its own inverse ([GLM-DOC] "The sparse-attention
+ * path": the indexer applies a Walsh-Hadamard rotation, an orthonormal
+ * involution, to both sides of its dot product before the keys are rounded to
+ * the cache's 16-bit format).  The plain matrix-vector product. */
+int oracle_hadamard(const double *x, int32_t n, double *out);
+
+/* Rotary position embedding of one dim-vector at position pos ([GLM-DOC] "The
+ * block", row "RoPE": NORM mode, base 8e6): for each pair i < rope_dims / 2 of
+ * adjacent dimensions (2i, 2i+1), theta_i = base^(-2i / rope_dims) and
+ * a = pos * theta_i,
+ *     out[2i]   = x[2i] cos a - x[2i+1] sin a
+ *     out[2i+1] = x[2i] sin a + x[2i+1] cos a;
+ * dimensions rope_dims .. dim-1 are copied. */
+int oracle_rope(const float *x, int32_t dim, int32_t rope_dims, double base, int64_t pos,
+                double *out);
+
+/* Indexer query / key preparation ([GLM-DOC] "The sparse-attention path": past
+ * top-k the indexer applies rope, then the Walsh-Hadamard rotation, then
+ * scores): out[v] = H (rope(x[v], pos[v])) for each of n vectors of dim. */
+int oracle_index_prepare(const float *x, const int64_t *pos, int64_t n, int32_t dim,
+                         int32_t rope_dims, double base, double *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -452,6 +452,99 @@ def test_new_pools_brute_force():
                 assert list(range(j0, j1)) == made, (L, q_len, kpool)
 
 
+# ---------------------------------------------------------------- indexer rope + Hadamard
+# "GLM-5.x (glm-dsa, glm5next)", "The sparse-attention path": past top-k the
+# indexer applies rope, then a Walsh-Hadamard rotation -- an orthonormal
+# involution on both sides of the dot product -- before the keys are rounded;
+# "The block", row "RoPE": NORM mode, base 8e6.
+
+def test_hadamard_equals_the_library_matrix():
+    """The special case a library computes: scipy's Sylvester Hadamard matrix,
+    scaled by 1/sqrt(n), times the vector."""
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(50)
+    for n in (1, 2, 4, 128):
+        x = rng.standard_normal(n)
+        ref = scipy_linalg.hadamard(n).astype(np.float64) @ x / math.sqrt(n)
+        np.testing.assert_allclose(oracle.hadamard(x), ref, rtol=0, atol=1e-13)
+
+
+def test_hadamard_closed_forms_and_involution():
+    n = 128
+    e0 = np.zeros(n); e0[0] = 1.0
+    np.testing.assert_allclose(oracle.hadamard(e0), np.full(n, 1 / math.sqrt(n)), atol=1e-15)
+    e1 = np.zeros(n); e1[1] = 1.0                       # column 1: +, -, +, -, ...
+    np.testing.assert_allclose(oracle.hadamard(e1), np.tile([1, -1], n // 2) / math.sqrt(n),
+                               atol=1e-15)
+    np.testing.assert_allclose(oracle.hadamard(np.array([3.0, 1.0])),
+                               [4 / math.sqrt(2), 2 / math.sqrt(2)], atol=1e-15)
+    rng = np.random.default_rng(51)
+    q, k = rng.standard_normal(n), rng.standard_normal(n)
+    hq, hk = oracle.hadamard(q), oracle.hadamard(k)
+    np.testing.assert_allclose(oracle.hadamard(hq), q, atol=1e-13)      # its own inverse
+    assert abs(np.dot(hq, hk) - np.dot(q, k)) < 1e-12                  # dot products kept
+    assert abs(np.linalg.norm(hq) - np.linalg.norm(q)) < 1e-12
+
+
+def test_rope_closed_forms():
+    d, base = 64, 8e6
+    x = np.zeros(128, np.float32); x[0] = 1.0
+    for pos in (0, 1, 5, 70000):
+        out = oracle.rope(x, d, base, pos)                 # pair 0: theta = 1 rad per position
+        np.testing.assert_allclose(out[:2], [math.cos(pos), math.sin(pos)], atol=1e-12)
+        assert np.all(out[2:] == 0)
+    i = d // 2 - 1                                         # the last pair: theta = base^(-(d-2)/d)
+    x = np.zeros(128, np.float32); x[2 * i + 1] = 2.0
+    a = 1000 * base ** (-(d - 2) / d)
+    np.testing.assert_allclose(oracle.rope(x, d, base, 1000)[2 * i: 2 * i + 2],
+                               [-2 * math.sin(a), 2 * math.cos(a)], atol=1e-12)
+    rng = np.random.default_rng(52)
+    y = rng.standard_normal(128).astype(np.float32)
+    assert np.array_equal(oracle.rope(y, d, base, 0), y.astype(np.float64))      # position 0
+    assert np.array_equal(oracle.rope(y, d, base, 12345)[d:], y[d:].astype(np.float64))
+
+
+def test_rope_pairs_adjacent_dims_and_keeps_relative_position():
+    """NORM mode rotates adjacent pairs (2i, 2i+1): e_1 moves into dim 0, not
+    into dim 1 + d/2 (the rival NEOX pairing); the rotated dot product depends
+    only on the position difference."""
+    d, base = 64, 8e6
+    e1 = np.zeros(128, np.float32); e1[1] = 1.0
+    out = oracle.rope(e1, d, base, 3)
+    np.testing.assert_allclose(out[:2], [-math.sin(3), math.cos(3)], atol=1e-12)
+    assert np.all(out[2:] == 0)
+    rng = np.random.default_rng(53)
+    q, k = rng.standard_normal(128).astype(np.float32), rng.standard_normal(128).astype(np.float32)
+    a = np.dot(oracle.rope(q, d, base, 900), oracle.rope(k, d, base, 850))
+    b = np.dot(oracle.rope(q, d, base, 150), oracle.rope(k, d, base, 100))
+    assert abs(a - b) < 1e-9
+
+
+def test_index_prepare_is_rope_then_hadamard():
+    """rope first, then the rotation: the order matters (the two do not commute)
+    and the indexer score of prepared vectors equals that of roped ones -- the
+    rotation cancels in exact arithmetic."""
+    rng = np.random.default_rng(54)
+    x = rng.standard_normal((6, 128)).astype(np.float32)
+    pos = np.array([0, 1, 7, 4096, 65535, 1048575], np.int64)
+    got = oracle.index_prepare(x, pos, 64, 8e6)
+    for v in range(6):
+        r = oracle.rope(x[v], 64, 8e6, int(pos[v]))
+        np.testing.assert_allclose(got[v], oracle.hadamard(r), atol=1e-12)
+        rival = oracle.rope(oracle.hadamard(x[v].astype(np.float64)).astype(np.float32), 64, 8e6,
+                            int(pos[v]))
+        if pos[v] != 0:
+            assert np.abs(rival - got[v]).max() > 1e-3
+    q = rng.standard_normal((32, 128)).astype(np.float32)
+    w = rng.standard_normal(32).astype(np.float32)
+    qp = oracle.index_prepare(q, np.full(32, 70000, np.int64), 64, 8e6)
+    qr = np.stack([oracle.rope(q[h], 64, 8e6, 70000) for h in range(32)])
+    kr = np.stack([oracle.rope(x[v], 64, 8e6, int(pos[v])) for v in range(6)])
+    s_prep = np.maximum(got @ qp.T, 0) @ w.astype(np.float64)
+    s_rope = np.maximum(kr @ qr.T, 0) @ w.astype(np.float64)
+    np.testing.assert_allclose(s_prep, s_rope, rtol=1e-12, atol=1e-10)
+
+
 def test_oracle_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.sparse_mla(np.zeros((2, 8), np.float32), np.zeros((4, 8), np.float32),
