@@ -33,7 +33,7 @@ __all__ = [
     "dsa_sparse_mla_attn",
     "dsa_decode_step", "dsa_decode_step_noalloc", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
     "OP_INDEX_SCORES", "OP_TOPK_SELECT", "OP_SPARSE_MLA", "OP_DECODE_STEP", "OP_INDEX_SELECT",
-    "OP_POOL_COMPRESS", "dsa_pool_compress",
+    "OP_POOL_COMPRESS", "dsa_pool_compress", "dsa_index_prepare",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
@@ -103,6 +103,7 @@ def load() -> ctypes.CDLL:
             "dsa_check_device_error": ([P, sz, P, ctypes.POINTER(i32)], ctypes.c_int),
             "dsa_decode_step_noalloc": ([S, B, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "dsa_pool_compress": ([S, B, P, P, P, P, sz, P], ctypes.c_int),
+            "dsa_index_prepare": ([S, i64, P, P, i32, ctypes.c_double, P, P], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -239,6 +240,12 @@ def dsa_pool_compress(shape, batch, cells, pos, pool_keys, ws, stream=None) -> N
     """Compressed keys of the pools completed by each sequence's new tokens (see dsa.h)."""
     _call("dsa_pool_compress", ctypes.byref(shape), ctypes.byref(batch), _ptr(cells), _ptr(pos),
           _ptr(pool_keys), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def dsa_index_prepare(shape, x, pos, rope_dims, rope_base, out, stream=None) -> None:
+    """out = H . rope(x, pos), rounded to the shape's dtype (see dsa.h)."""
+    _call("dsa_index_prepare", ctypes.byref(shape), int(x.shape[0]), _ptr(x), _ptr(pos),
+          int(rope_dims), float(rope_base), _ptr(out), _stream(stream))
 
 
 def dsa_check_device_error(ws: torch.Tensor, stream=None) -> int:

@@ -298,6 +298,24 @@ dsa_status dsa_sparse_mla_attn(const dsa_shape* shape, const dsa_batch* batch, c
                        "sparse_mla_attn");
 }
 
+dsa_status dsa_index_prepare(const dsa_shape* shape, int64_t n_vec, const float* x,
+                             const int64_t* pos, int32_t rope_dims, double rope_base, void* out,
+                             void* stream) {
+    Shape sh;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if (n_vec < 0 || rope_dims < 0 || rope_dims > sh.idx_dim || (rope_dims & 1) ||
+        !isfinite(rope_base) || !(rope_base > 0.0))
+        return DSA_ERR_INVALID_ARG;
+    if (n_vec > 0 && (x == nullptr || out == nullptr || (rope_dims > 0 && pos == nullptr)))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || (reinterpret_cast<uintptr_t>(pos) & 7) != 0)
+        return DSA_ERR_INVALID_ARG;
+    return cuda_status(launch_index_prepare(sh, n_vec, x, pos, rope_dims, rope_base, out,
+                                            static_cast<cudaStream_t>(stream)),
+                       "index_prepare");
+}
+
 dsa_status dsa_pool_compress(const dsa_shape* shape, const dsa_batch* batch, const void* cells,
                              const float* pos, void* pool_keys, void* ws, size_t ws_bytes,
                              void* stream) {

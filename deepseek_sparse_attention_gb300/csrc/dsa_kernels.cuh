@@ -83,6 +83,12 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
                                       int64_t ld, int32_t* idx, int32_t* n_sel, void* state,
                                       uint32_t* gbar, int32_t* err, cudaStream_t st);
 
+// Indexer query / key preparation (index_prepare.cu): out[v] = H rope(x[v],
+// pos[v]) for n_vec float32 vectors of 128, rounded to the shape's dtype.
+cudaError_t launch_index_prepare(const Shape& sh, int64_t n_vec, const float* x,
+                                 const int64_t* pos, int32_t rope_dims, double base, void* out,
+                                 cudaStream_t st);
+
 // Pool-key compression (pool_compress.cu): the complete pools of each sequence
 // whose last token is one of its new tokens (q_off), from the per-row cells
 // [key | gate] (2 x 128 values, dtype) and the per-slot embedding pos

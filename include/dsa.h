@@ -194,6 +194,29 @@ dsa_status dsa_index_select(const dsa_shape *shape, const dsa_batch *batch, cons
                             const float *w, const void *k_idx, int32_t *idx, int32_t *n_sel,
                             void *ws, size_t ws_bytes, void *stream);
 
+/* Indexer query / key preparation ("GLM-5.x (glm-dsa, glm5next)", "The
+ * sparse-attention path": past top-k the indexer applies rope, then a
+ * Walsh-Hadamard rotation -- an orthonormal involution on both sides of the dot
+ * product, so the scores are unchanged in exact arithmetic while the rounding of
+ * the 16-bit key cache is spread evenly over the 128 dimensions; "The block",
+ * row "RoPE": NORM mode, base 8e6).
+ *   x   [n_vec, idx_dim] float32: projected indexer vectors -- keys (one per
+ *       token) or queries (one row per head, idx_heads rows per query)
+ *   pos [n_vec] int64: each row's token position (a query's heads share one);
+ *       may be NULL when rope_dims == 0
+ *   out [n_vec, idx_dim] dtype: H . rope(x[v], pos[v]), rounded -- the q_idx or
+ *       k_idx layout of the other entry points
+ * rope rotates the adjacent pairs (2i, 2i+1) of the first rope_dims dimensions
+ * (even, 0..idx_dim) by pos * rope_base^(-2i / rope_dims); H is the orthonormal
+ * Sylvester-Hadamard matrix of order idx_dim, H[i][j] = (-1)^popcount(i & j) /
+ * sqrt(idx_dim).  Which of the indexer's 128 dimensions carry rope is not stated
+ * on the pages: it is the caller's rope_dims (64 = the first half, the MLA rope
+ * width, is the reading this library's tests use).  float32 arithmetic (the
+ * rope angle in double).  No workspace; nothing the device can find wrong. */
+dsa_status dsa_index_prepare(const dsa_shape *shape, int64_t n_vec, const float *x,
+                             const int64_t *pos, int32_t rope_dims, double rope_base, void *out,
+                             void *stream);
+
 /* Pool-key compression for the k-pool indexer ("GLM-5.x (glm-dsa, glm5next)",
  * table "GLM-5.3-Flash", row "Pooled indexer": each cell caches [key|gate], and
  * a softmax over the gates plus a per-slot position embedding compresses each

@@ -153,6 +153,20 @@ def test_pool_compress_rejects_before_enqueue(lib):
     assert plan["kernel_launches"] == 1
 
 
+def test_index_prepare_rejects_before_enqueue(lib):
+    P = ctypes.c_void_p
+    good = P(256)
+    sh = dsa.make_shape()
+    f = lib.dsa_index_prepare
+    assert f(ctypes.byref(sh), 4, good, good, 63, 8e6, good, None) == 1      # odd rope width
+    assert f(ctypes.byref(sh), 4, good, good, 130, 8e6, good, None) == 1     # wider than a head
+    assert f(ctypes.byref(sh), 4, good, good, 64, 0.0, good, None) == 1      # base must be > 0
+    assert f(ctypes.byref(sh), 4, good, None, 64, 8e6, good, None) == 1      # rope needs positions
+    assert f(ctypes.byref(sh), 4, P(260), good, 64, 8e6, good, None) == 1    # misaligned x
+    assert f(ctypes.byref(sh), -1, good, good, 64, 8e6, good, None) == 1
+    assert f(ctypes.byref(sh), 0, None, None, 0, 8e6, None, None) == 0       # nothing to do
+
+
 def test_python_binding_rejects_host_tensors(lib):
     sh = dsa.make_shape()
     with pytest.raises(ValueError):
