@@ -11,11 +11,12 @@
 // One CTA handles a range of one query's selected rows in tiles of 64 rows,
 // two row buffers deep, so that one tile's gather overlaps the previous
 // tile's softmax and value product:
-//   warps 0,2,3 load the query once (TMA tiles) and gather each tile's rows
-//              with 16-byte cp.async copies straight into the 128-byte swizzle
-//              layout of buffer t % 2 -- thousands of copies in flight per SM,
-//              where a TMA gather4 (four 128-byte row pieces per request) kept
-//              too few;
+//   warps 0,2,3 and 8-11 gather each tile's rows with 16-byte cp.async copies
+//              straight into the 128-byte swizzle layout of buffer t % 2 --
+//              thousands of copies in flight per SM, where a TMA gather4 (four
+//              128-byte row pieces per request) kept too few (the first two
+//              tiles are copied by every thread but warp 1's; thread 0 loads
+//              the query once by TMA);
 //   warp 1     issues S^T = R . Q^T (M = 64 rows, N = 64 heads, K = the row
 //              width) into one of two TMEM score buffers -- the next tile's
 //              scores before this tile's values -- then O^T += R^T . P^T
@@ -24,15 +25,16 @@
 //              the scores and as MN-major A for the values;
 // P is split into bf16 hi + lo parts and the value product runs once on each
 // (through the same shared-memory buffer), carrying P to ~2^-16 relative where
-// bf16 alone (2^-9) would not meet the output tolerance.
-//   warps 4-11 softmax across the tile's rows: an M = 64 accumulator puts row
-//              16 q + i in lane i of TMEM quadrant q, so lanes 0..15 of each warp
-//              own one row and half the heads; per-head tile maxima by warp
-//              reductions, a running maximum that is raised (and O^T rescaled in
-//              TMEM, after the previous tile's values are in) only when a tile
-//              exceeds it by more than 2^8, exp2, P^T written to shared memory
-//              (into the buffer's rope block, which the scores no longer need),
-//              per-thread partial row sums reduced once at the end.
+// bf16 alone (up to 2^-8) would not meet the output tolerance in every case.
+//   warps 4-7  softmax across the tile's rows: an M = 64 accumulator puts row
+//              16 q + i in lane i of TMEM quadrant q; a 16x64b load gives every
+//              lane a row and the 32 heads of one parity; per-head tile maxima
+//              by a halving shuffle exchange, a running maximum that is raised
+//              (and O^T rescaled in TMEM, after the previous tile's values are
+//              in) only when a tile exceeds it by more than 2^8, exp2, P^T
+//              written to shared memory (into the buffer's rope block, which
+//              the scores no longer need), per-thread partial row sums reduced
+//              once at the end; warps 4-11 then read O^T out of TMEM.
 // Splits of one query are combined by the log-sum-exp merge: a separate
 // launch over the partials in global memory, or, for two splits, inside this
 // launch by the two CTAs of a cluster through distributed shared memory.
