@@ -63,10 +63,13 @@ def _load():
             lib.oracle_hadamard.argtypes = [P, i32, P]
             lib.oracle_rope.argtypes = [P, i32, i32, f64, i64, P]
             lib.oracle_index_prepare.argtypes = [P, P, i64, i32, i32, f64, P]
+            lib.oracle_absorb_q.argtypes = [P, P, i32, i32, i32, i32, P]
+            lib.oracle_up_project.argtypes = [P, P, i32, i32, i32, P]
             for fn in (lib.oracle_index_scores, lib.oracle_topk, lib.oracle_kpool_select,
                        lib.oracle_sparse_mla, lib.oracle_dense_masked_mla,
                        lib.oracle_decode_step, lib.oracle_pool_compress, lib.oracle_new_pools,
-                       lib.oracle_hadamard, lib.oracle_rope, lib.oracle_index_prepare):
+                       lib.oracle_hadamard, lib.oracle_rope, lib.oracle_index_prepare,
+                       lib.oracle_absorb_q, lib.oracle_up_project):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -231,4 +234,27 @@ def index_prepare(x, pos, rope_dims: int, base: float) -> np.ndarray:
     _check(_load().oracle_index_prepare(_ptr(x) if n else None, _ptr(p) if n else None, n, dim,
                                         rope_dims, float(base), _ptr(out) if n else None),
            "oracle_index_prepare")
+    return out
+
+
+def absorb_q(q, w_uk, rope: int) -> np.ndarray:
+    """q [heads, nope + rope], w_uk [heads, nope, kv_lora] -> q_abs [heads, kv_lora + rope]."""
+    q, w_uk = _f32(q), _f32(w_uk)
+    heads, nope, kv_lora = w_uk.shape
+    assert q.shape == (heads, nope + rope)
+    out = np.empty((heads, kv_lora + rope), dtype=np.float64)
+    _check(_load().oracle_absorb_q(_ptr(q), _ptr(w_uk), heads, nope, rope, kv_lora, _ptr(out)),
+           "oracle_absorb_q")
+    return out
+
+
+def up_project(o, w_uv) -> np.ndarray:
+    """o [heads, kv_lora] (latent), w_uv [heads, v_dim, kv_lora] -> [heads, v_dim]."""
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    w_uv = _f32(w_uv)
+    heads, v_dim, kv_lora = w_uv.shape
+    assert o.shape == (heads, kv_lora)
+    out = np.empty((heads, v_dim), dtype=np.float64)
+    _check(_load().oracle_up_project(_ptr(o), _ptr(w_uv), heads, kv_lora, v_dim, _ptr(out)),
+           "oracle_up_project")
     return out

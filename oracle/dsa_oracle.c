@@ -289,3 +289,40 @@ int oracle_index_prepare(const float *x, const int64_t *pos, int64_t n, int32_t 
     }
     return bad ? -1 : 0;
 }
+
+int oracle_absorb_q(const float *q, const float *w_uk, int32_t heads, int32_t nope, int32_t rope,
+                    int32_t kv_lora, double *q_abs)
+{
+    if (heads <= 0 || nope < 0 || rope < 0 || kv_lora <= 0 || !q || !q_abs) return -1;
+    if (nope > 0 && !w_uk) return -1;
+    const int64_t qw = (int64_t)nope + rope, aw = (int64_t)kv_lora + rope;
+#pragma omp parallel for schedule(static)
+    for (int32_t h = 0; h < heads; h++) {
+        const float *qh = q + h * qw;
+        const float *wh = w_uk + (int64_t)h * nope * kv_lora;
+        for (int32_t i = 0; i < kv_lora; i++) {
+            double s = 0.0;
+            for (int32_t d = 0; d < nope; d++) s += (double)qh[d] * (double)wh[(int64_t)d * kv_lora + i];
+            q_abs[h * aw + i] = s;                       /* the query in the latent */
+        }
+        for (int32_t r = 0; r < rope; r++) q_abs[h * aw + kv_lora + r] = qh[nope + r];
+    }
+    return 0;
+}
+
+int oracle_up_project(const double *o, const float *w_uv, int32_t heads, int32_t kv_lora,
+                      int32_t v_dim, double *out)
+{
+    if (heads <= 0 || kv_lora <= 0 || v_dim <= 0 || !o || !w_uv || !out) return -1;
+#pragma omp parallel for schedule(static)
+    for (int32_t h = 0; h < heads; h++) {
+        const double *oh = o + (int64_t)h * kv_lora;
+        const float *wh = w_uv + (int64_t)h * v_dim * kv_lora;
+        for (int32_t v = 0; v < v_dim; v++) {
+            double s = 0.0;
+            for (int32_t i = 0; i < kv_lora; i++) s += (double)wh[(int64_t)v * kv_lora + i] * oh[i];
+            out[(int64_t)h * v_dim + v] = s;
+        }
+    }
+    return 0;
+}

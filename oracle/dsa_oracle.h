@@ -151,6 +151,29 @@ int oracle_rope(const float *x, int32_t dim, int32_t rope_dims, double base, int
 int oracle_index_prepare(const float *x, const int64_t *pos, int64_t n, int32_t dim,
                          int32_t rope_dims, double base, double *out);
 
+/* Query absorption ([ONE-C] "Attention: Multi head Latent Attention With a
+ * Tiny KV Cache": the key up-projection is absorbed into the query, which then
+ * scores the latents directly; [GLM-DOC] "The block": the per-head K
+ * decompression is folded into the query, attn_k_b).
+ *   q     [heads * (nope + rope)]         per head: the nope part, then the
+ *                                         (already rotated) rope part
+ *   w_uk  [heads * nope * kv_lora]        per head: row d is the latent-space
+ *                                         image of nope dimension d
+ *   q_abs [heads * (kv_lora + rope)]      out: q_abs[h][i] = sum_d q[h][d] *
+ *                                         w_uk[h][d][i] for i < kv_lora, then the
+ *                                         rope part copied */
+int oracle_absorb_q(const float *q, const float *w_uk, int32_t heads, int32_t nope, int32_t rope,
+                    int32_t kv_lora, double *q_abs);
+
+/* Output up-projection ([ONE-C]: the pooled latent is mapped to the head's value
+ * space; [GLM-DOC] "The block": the V decompression folded into the output,
+ * attn_v_b).
+ *   o     [heads * kv_lora]     attention output in the latent
+ *   w_uv  [heads * v_dim * kv_lora]  per head: row v maps the latent to value dim v
+ *   out   [heads * v_dim]       out: out[h][v] = sum_i w_uv[h][v][i] * o[h][i] */
+int oracle_up_project(const double *o, const float *w_uv, int32_t heads, int32_t kv_lora,
+                      int32_t v_dim, double *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -545,6 +545,67 @@ def test_index_prepare_is_rope_then_hadamard():
     np.testing.assert_allclose(s_prep, s_rope, rtol=1e-12, atol=1e-10)
 
 
+# ---------------------------------------------------------------- absorption
+# "GLM 5.2 in one C file", "Attention: Multi head Latent Attention With a Tiny
+# KV Cache": the key up-projection is absorbed into the query and the value
+# up-projection applied to the pooled latent -- "a reformulation, not an
+# approximation".  "GLM-5.x (glm-dsa, glm5next)", "The block": 64 heads, head
+# size 256 with n_rot 64 (so a 192-wide nope part), kv_lora 512.
+
+H, NOPE, ROPE, KVL, VD = 64, 192, 64, 512, 256
+
+
+def test_absorbed_scores_equal_explicit_decompression():
+    """q_abs . [latent, rope key] equals q_nope . (W_UK latent) + q_rope . rope key
+    for every head and row: the order of the two products is all that changes."""
+    rng = np.random.default_rng(80)
+    q = rng.standard_normal((H, NOPE + ROPE)).astype(np.float32)
+    w_uk = (rng.standard_normal((H, NOPE, KVL)) / 16).astype(np.float32)
+    rows = rng.standard_normal((7, KVL + ROPE)).astype(np.float32)
+    q_abs = oracle.absorb_q(q, w_uk, ROPE)
+    absorbed = q_abs @ rows.astype(np.float64).T                       # [H, 7]
+    k_nope = np.einsum("hdi,ji->hjd", w_uk.astype(np.float64), rows[:, :KVL].astype(np.float64))
+    explicit = (np.einsum("hd,hjd->hj", q[:, :NOPE].astype(np.float64), k_nope) +
+                q[:, NOPE:].astype(np.float64) @ rows[:, KVL:].astype(np.float64).T)
+    np.testing.assert_allclose(absorbed, explicit, rtol=1e-12, atol=1e-10)
+
+
+def test_absorption_closed_forms():
+    """W_UK = [I | 0] per head: the query's nope part lands in the first 192
+    latent dims, the rest zero, the rope part copied behind the latent."""
+    rng = np.random.default_rng(81)
+    q = rng.standard_normal((H, NOPE + ROPE)).astype(np.float32)
+    w = np.zeros((H, NOPE, KVL), np.float32)
+    w[:, np.arange(NOPE), np.arange(NOPE)] = 1.0
+    out = oracle.absorb_q(q, w, ROPE)
+    assert np.array_equal(out[:, :NOPE], q[:, :NOPE].astype(np.float64))
+    assert np.all(out[:, NOPE:KVL] == 0)
+    assert np.array_equal(out[:, KVL:], q[:, NOPE:].astype(np.float64))
+
+
+def test_up_projection_equals_explicit_values():
+    """Attention over explicitly decompressed values (v_j = W_UV latent_j) equals
+    the up-projection of the attention over the latents (linearity), with the
+    attention itself from the oracle."""
+    rng = np.random.default_rng(82)
+    q_abs = (rng.standard_normal((H, KVL + ROPE)) * 0.2).astype(np.float32)
+    rows = rng.standard_normal((9, KVL + ROPE)).astype(np.float32)
+    w_uv = (rng.standard_normal((H, VD, KVL)) / 16).astype(np.float32)
+    idx = np.arange(9, dtype=np.int32)
+    o_lat, lse = oracle.sparse_mla(q_abs, rows, idx, 1 / 16, KVL)
+    got = oracle.up_project(o_lat, w_uv)
+    # the softmax weights from the oracle's lse: p_j = exp(z_j - lse)
+    z = (q_abs.astype(np.float64) @ rows.astype(np.float64).T) / 16
+    p = np.exp(z - lse[:, None])
+    v = np.einsum("hvi,ji->hjv", w_uv.astype(np.float64), rows[:, :KVL].astype(np.float64))
+    explicit = np.einsum("hj,hjv->hv", p, v)
+    np.testing.assert_allclose(got, explicit, rtol=1e-10, atol=1e-10)
+    sel = np.zeros((H, VD, KVL), np.float32)              # a selection matrix: out = o[perm]
+    perm = rng.permutation(KVL)[:VD]
+    sel[:, np.arange(VD), perm] = 1.0
+    np.testing.assert_array_equal(oracle.up_project(o_lat, sel), o_lat[:, perm])
+
+
 def test_oracle_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.sparse_mla(np.zeros((2, 8), np.float32), np.zeros((4, 8), np.float32),
