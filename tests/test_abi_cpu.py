@@ -167,6 +167,35 @@ def test_index_prepare_rejects_before_enqueue(lib):
     assert f(ctypes.byref(sh), 0, None, None, 0, 8e6, None, None) == 0       # nothing to do
 
 
+@pytest.mark.parametrize("name,launches,splits,rows_per_split", [
+    # decode of one query: the fused indexer + selection, 32 one-tile attention
+    # splits (one wave of CTAs), the split merge
+    ("glm52_decode_128k", 3, 32, 64),
+    # 64 decode queries: the indexer, the selection, the attention with two
+    # splits per query merged inside its launch by a CTA pair
+    ("ragged_decode_64", 3, 2, 1024),
+    # a prefill chunk: the indexer's group plan and the indexer, the selection,
+    # one attention split per query (no merge)
+    ("chunked_prefill_4096", 4, 1, 2048),
+    # four 1M-token k-pool decode queries: fused, 11 splits of three tiles, merge
+    ("kpool_nope_1m", 3, 11, 192),
+])
+def test_plan_of_the_benchmark_workloads(lib, name, launches, splits, rows_per_split):
+    """The host-side plan (launch count, attention splits) of each benchmark
+    workload, from the batch's host scalars alone."""
+    import workloads
+    wl = workloads.named(name)
+    sh = dsa.make_shape(wl.idx_heads, wl.idx_dim, wl.heads, wl.kv_lora, wl.rope, wl.top_k,
+                        wl.kpool, wl.scale, wl.dtype)
+    P = ctypes.c_void_p(16)
+    b = dsa.Batch(len(wl.kv_lens), wl.n_q, max(wl.q_lens), 0, max(wl.kv_lens), sum(wl.kv_lens),
+                  sum(wl.key_counts()), P, P, P)
+    plan = dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP)
+    assert plan == {"kernel_launches": launches, "attn_splits": splits,
+                    "attn_rows_per_split": rows_per_split}
+    assert splits * rows_per_split >= min(max(wl.kv_lens), dsa.dsa_index_row_width(sh))
+
+
 def test_python_binding_rejects_host_tensors(lib):
     sh = dsa.make_shape()
     with pytest.raises(ValueError):
