@@ -9,6 +9,11 @@
  *   3. absorbed-MLA attention     over only the selected 576-wide (512 latent +
  *      64 rope) or 512-wide (NoPE) cache rows, output in the 512-wide latent
  *
+ * and two producers of the indexer's inputs: dsa_index_prepare (rope, then the
+ * Walsh-Hadamard rotation of projected indexer queries and keys, rounded to the
+ * cache's dtype) and dsa_pool_compress (the k-pool keys, one per 4 tokens, from
+ * the tokens' [key | gate] cells).
+ *
  * Sources (page title -- section):
  *   "GLM-5.x (glm-dsa, glm5next)" (TensorSharp model notes) -- "The block"
  *     (64 query heads, one 576-wide cache row per token, indexer 32 x 128,
