@@ -216,8 +216,11 @@ dsa_status dsa_index_select(const dsa_shape *shape, const dsa_batch *batch, cons
  * Sylvester-Hadamard matrix of order idx_dim, H[i][j] = (-1)^popcount(i & j) /
  * sqrt(idx_dim).  Which of the indexer's 128 dimensions carry rope is not stated
  * on the pages: it is the caller's rope_dims (64 = the first half, the MLA rope
- * width, is the reading this library's tests use).  float32 arithmetic (the
- * rope angle in double).  No workspace; nothing the device can find wrong. */
+ * width, is the reading this library's tests use).  float32 arithmetic; the
+ * rope angle is exact modulo one turn (each pair's rate theta_i / 2 pi as a
+ * 64-bit binary fraction, times the position), so large positions lose nothing.
+ * x and out 16-byte aligned, pos 8-byte aligned (else DSA_ERR_INVALID_ARG).  No
+ * workspace; nothing the device can find wrong. */
 dsa_status dsa_index_prepare(const dsa_shape *shape, int64_t n_vec, const float *x,
                              const int64_t *pos, int32_t rope_dims, double rope_base, void *out,
                              void *stream);
