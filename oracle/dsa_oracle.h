@@ -116,8 +116,10 @@ int oracle_decode_step(const float *q_idx, const float *w, const float *keys,
  *     a_i = exp(z_i) / sum_j exp(z_j)          softmax over the slots
  *     out[p][c] = sum_i a_i * key_i[c]
  * Readings (the pages name the parts, not the formula): the gate has the key's
- * width (one softmax per channel), and the position embedding is added to the
- * gate logits inside the softmax. */
+ * width and there is one softmax per key dimension -- [STRATA] "Tests" lists
+ * one softmax over the whole pool block instead of per key-dim as a rival
+ * reading -- and the position embedding is added to the gate logits inside the
+ * softmax. */
 int oracle_pool_compress(const float *cells, int64_t n_pools, const float *pos, int32_t kpool,
                          int32_t dim, double *out);
 

@@ -435,6 +435,22 @@ def test_pool_compress_rival_reading_fails():
     assert abs(out[0, 0] - rival) > 1.0
 
 
+def test_pool_compress_rival_whole_block_softmax_fails():
+    """"Add GLM-5.3-Flash support", "Tests": one softmax over the whole pool block
+    instead of per key-dim is a rival reading that must disagree.  With all keys
+    one, the per-dimension softmax returns one in every dimension; a softmax over
+    the block's 4 x 128 logits would return each dimension's share of the block."""
+    rng = np.random.default_rng(44)
+    gates = rng.standard_normal((1, 4, 128)).astype(np.float32)
+    pos = rng.standard_normal((4, 128)).astype(np.float32)
+    ours = oracle.pool_compress(_cells(np.ones((1, 4, 128), np.float32), gates), pos)
+    z = gates[0].astype(np.float64) + pos.astype(np.float64)
+    block = np.exp(z - z.max()) / np.exp(z - z.max()).sum()        # the rival's weights
+    rival = block.sum(axis=0)                                      # keys all one
+    np.testing.assert_allclose(ours[0], 1.0, atol=1e-14)
+    assert np.abs(rival - ours[0]).max() > 0.5
+
+
 def test_new_pools_golden_table():
     for r in _table("new_pools.txt"):
         L, q_len, kpool, j0, j1 = (int(x) for x in r[:5])
