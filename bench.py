@@ -54,7 +54,10 @@ def parse_args(argv=None):
     p.add_argument("--no-graph", action="store_true",
                    help="launch each step on the stream instead of replaying CUDA graphs")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
-                   help="target CPU work of the oracle baseline sample")
+                   help="target CPU work of the oracle baseline sample (all threads; a third "
+                        "of it on one thread)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="time only --workload, not the other workloads of the suite")
     return p.parse_args(argv)
 
 
@@ -222,22 +225,42 @@ def algorithmic(wl):
 
 # ------------------------------------------------------------------ CPU arm
 
-def oracle_sample(wl, d_host_fn, seconds: float, max_queries: int = 1 << 30):
-    """Run the oracle over queries of the workload until `seconds` of wall time
-    have passed (at least one query); returns (queries, elapsed, threads)."""
+def oracle_baseline(wl, d, seconds: float, single_seconds: float):
+    """The oracle on this machine's cores, as the CPU baseline.
+
+    Host float copies of (at most two of) the workload's queries are made
+    before any clock starts; the timed loops run only the oracle over them:
+    every thread for about `seconds`, then one thread for about
+    `single_seconds` (at least one query each)."""
     import oracle
 
     oracle.build()
-    done, t0 = 0, time.perf_counter()
-    nq = wl.n_q
-    while True:
-        q = (done * 7919) % nq          # spread the sample over the batch
-        args = d_host_fn(q)
-        oracle.decode_step(*args)
-        done += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or done >= max_queries:
-            return done, el, oracle.threads()
+    fn = host_query_args(wl, d)
+    qs = list(dict.fromkeys((i * 7919) % wl.n_q for i in range(min(wl.n_q, 2))))
+    args = [fn(q) for q in qs]
+
+    def run(sec):
+        done, t0 = 0, time.perf_counter()
+        while True:
+            oracle.decode_step(*args[done % len(args)])
+            done += 1
+            el = time.perf_counter() - t0
+            if el >= sec:
+                return done, el
+
+    full = oracle.threads()
+    n, el = run(seconds)
+    oracle.set_threads(1)
+    try:
+        n1, el1 = run(single_seconds)
+    finally:
+        oracle.set_threads(full)
+    what = f"the {wl.name} workload (quer{'y' if len(qs) == 1 else 'ies'} {qs}) through the oracle"
+    return {"value": n / el, "unit": UNIT, "cores": full, "kind": "oracle",
+            "sample": f"{n} queries of {what}, double precision, {full} OpenMP threads, "
+                      f"{el:.1f} s; inputs copied to host memory before timing",
+            "single_thread": {"value": n1 / el1, "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} queries of {what} on one thread, {el1:.1f} s"}}
 
 
 def host_query_args(wl, d):
@@ -351,6 +374,223 @@ def workload_config(wl, world):
 
 # ------------------------------------------------------------------ GPU arm
 
+def dominant_launch(dsa, wl, sh, b, d, keys, copies, stream, n_rep):
+    """The launch that carries the step's dominant work, timed alone with CUDA
+    events on the stream it runs on, over the same input rotation: the fused
+    indexer + selection for small decode batches, else the indexer.  Also the
+    indexer alone.  Returns (fused?, fused ms, indexer ms)."""
+    import torch
+
+    sb = torch.empty((wl.n_q, max(max(wl.kv_lens) // wl.kpool, 4)), device=keys[0].device)
+    ld = sb.shape[1]
+    ws_i = dsa.alloc_workspace(sh, b, dsa.OP_INDEX_SCORES, keys[0].device)
+    for i in range(3):
+        dsa.dsa_index_scores(sh, b, d["q_idx"], d["w"], keys[i % copies], sb, ld, ws_i, stream)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for i in range(n_rep):
+        dsa.dsa_index_scores(sh, b, d["q_idx"], d["w"], keys[i % copies], sb, ld, ws_i, stream)
+    k1.record(stream)
+    torch.cuda.synchronize()
+    idx_ms = k0.elapsed_time(k1) / n_rep
+    if dsa.dsa_check_device_error(ws_i, stream) != 0:
+        raise RuntimeError("device error in the indexer loop")
+    del sb
+    fused = dsa.dsa_plan(sh, b, dsa.OP_INDEX_SELECT)["kernel_launches"] == 1
+    sel_ms = 0.0
+    if fused:
+        ws_s = dsa.alloc_workspace(sh, b, dsa.OP_INDEX_SELECT, keys[0].device)
+        width = dsa.dsa_index_row_width(sh)
+        idx_s = torch.empty((wl.n_q, width), dtype=torch.int32, device=keys[0].device)
+        nsel_s = torch.empty(wl.n_q, dtype=torch.int32, device=keys[0].device)
+        for i in range(3):
+            dsa.dsa_index_select(sh, b, d["q_idx"], d["w"], keys[i % copies], idx_s, nsel_s, ws_s,
+                                 stream)
+        k0.record(stream)
+        for i in range(n_rep):
+            dsa.dsa_index_select(sh, b, d["q_idx"], d["w"], keys[i % copies], idx_s, nsel_s, ws_s,
+                                 stream)
+        k1.record(stream)
+        torch.cuda.synchronize()
+        sel_ms = k0.elapsed_time(k1) / n_rep
+        if dsa.dsa_check_device_error(ws_s, stream) != 0:
+            raise RuntimeError("device error in the fused selection loop")
+    return fused, sel_ms, idx_ms
+
+
+def roofline_of(wl, fused, sel_ms, idx_ms, peaks, peak_src):
+    """The roofline object of the dominant launch (see dominant_launch)."""
+    work = algorithmic(wl)
+    if fused:
+        dom = {"kernel": "index_select_fused", "ms": sel_ms,
+               "bytes": work["index_launch_bytes"] + work["select_bytes"]}
+    else:
+        dom = {"kernel": "index_scores_tc", "ms": idx_ms, "bytes": work["index_launch_bytes"]}
+    # A prefill chunk re-reads each key tile for many queries: its indexer does
+    # far more flops per byte than the GPU's flop/byte balance and is bound by
+    # the tensor pipe, so its roofline is in TFLOP/s against the bf16 peak.
+    tensor_bound = (work["flops_index"] / max(work["index_launch_bytes"], 1) >
+                    peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9))
+    if tensor_bound and not fused:
+        roof = {"bound": "tensor", "kernel": dom["kernel"],
+                "achieved": work["flops_index"] / (dom["ms"] / 1e3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "flops_per_launch": work["flops_index"], "peak_source": f"{peak_src} bf16_tflops"}
+    else:
+        roof = {"bound": "hbm", "kernel": dom["kernel"],
+                "achieved": dom["bytes"] / (dom["ms"] / 1e3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "bytes_per_launch": dom["bytes"],
+                "peak_source": f"{peak_src} hbm_gbs"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = kernel_traffic(dom["kernel"], wl.name)
+    roof["launch_us"] = dom["ms"] * 1e3
+    return roof
+
+
+class StepBench:
+    """One workload's inputs on the device and its timed step loop."""
+
+    def __init__(self, dsa, wl, dev, stream, no_graph: bool):
+        import torch
+        import workloads
+
+        self.dsa, self.wl, self.dev, self.stream = dsa, wl, dev, stream
+        per_copy = algorithmic(wl)["step_bytes"]
+        self.copies = min(8, max(2, math.ceil(2 * L2_BYTES / max(per_copy, 1))))
+        d = self.d = workloads.make(wl, dev, copies=self.copies)
+        self.sh = dsa.make_shape(wl.idx_heads, wl.idx_dim, wl.heads, wl.kv_lora, wl.rope,
+                                 wl.top_k, wl.kpool, wl.scale, wl.dtype)
+        self.b = dsa.make_batch(d["row_off"], d["key_off"], d["q_off"], wl.n_q, max(wl.q_lens),
+                                max(wl.kv_lens), sum(wl.kv_lens), sum(wl.key_counts()))
+        self.ws = dsa.alloc_workspace(self.sh, self.b, dsa.OP_DECODE_STEP, dev)
+        width = dsa.dsa_index_row_width(self.sh)
+        self.plan = dsa.dsa_plan(self.sh, self.b, dsa.OP_DECODE_STEP)
+        self.out = torch.empty((wl.n_q, wl.heads, wl.kv_lora), device=dev)
+        self.lse = torch.empty((wl.n_q, wl.heads), device=dev)
+        self.idx = torch.empty((wl.n_q, width), dtype=torch.int32, device=dev)
+        self.n_sel = torch.empty(wl.n_q, dtype=torch.int32, device=dev)
+        self.keys, self.caches = d["k_idx_copies"], d["cache_copies"]
+        self.no_graph = no_graph
+        self.launch_mode = "stream launches"
+
+    def launch(self, i, st):
+        c = i % self.copies
+        self.dsa.dsa_decode_step(self.sh, self.b, self.d["q_idx"], self.d["w"], self.keys[c],
+                                 self.d["q_abs"], self.caches[c], self.out, self.lse, self.idx,
+                                 self.n_sel, self.ws, st)
+
+    def prepare(self, warm: int):
+        """Warm-up steps, then the CUDA graphs the timed steps replay: a decode
+        loop replays its step from graphs (the launches of a step and of
+        consecutive steps then overlap through programmatic dependent launch
+        without host round trips): one graph of G steps over the input copies
+        in turn, and one single-step graph per copy for the remainder, so that
+        exactly K steps run."""
+        import torch
+
+        dsa, dev = self.dsa, self.dev
+        for i in range(max(warm, 3)):
+            self.launch(i, self.stream)
+        torch.cuda.synchronize(dev)
+        if dsa.dsa_check_device_error(self.ws, self.stream) != 0:
+            raise RuntimeError(f"device error during warm-up ({self.wl.name})")
+        if self.no_graph:
+            self.run_steps = lambda n: [self.launch(i, self.stream) for i in range(n)]
+            return
+        G = self.copies * max(1, 12 // self.copies)
+        g_all = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_all):
+            for i in range(G):
+                self.launch(i, torch.cuda.current_stream(dev))
+        g_one = []
+        for c in range(self.copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.launch(c, torch.cuda.current_stream(dev))
+            g_one.append(g)
+
+        def run_steps(n):
+            for _ in range(n // G):
+                g_all.replay()
+            for i in range(n % G):
+                g_one[i % self.copies].replay()
+
+        self.run_steps = run_steps
+        self._graphs = (g_all, g_one)
+        run_steps(G)                                 # untimed: the graphs' first replays
+        torch.cuda.synchronize(dev)
+        if dsa.dsa_check_device_error(self.ws, self.stream) != 0:
+            raise RuntimeError(f"device error in the graph warm-up ({self.wl.name})")
+        self.launch_mode = f"CUDA graphs of {G} steps (+ single-step graphs for the remainder)"
+
+    def calibrate(self, seconds: float, lo: int = 20, hi: int = 200000) -> int:
+        import torch
+
+        t0 = time.perf_counter()
+        self.run_steps(10)
+        torch.cuda.synchronize(self.dev)
+        per = (time.perf_counter() - t0) / 10
+        return int(min(hi, max(lo, seconds / max(per, 1e-7))))
+
+    def timed(self, steps: int, pg, local: int):
+        """(ms for `steps` steps, clock record) between barriers and syncs."""
+        import torch
+
+        clocks = ClockSampler(local)
+        clocks.start()
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize(self.dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        self.run_steps(steps)
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        if pg:
+            pg.barrier()
+        clk = clocks.stop()
+        if self.dsa.dsa_check_device_error(self.ws, self.stream) != 0:
+            raise RuntimeError(f"device error during the timed region ({self.wl.name})")
+        return e0.elapsed_time(e1), clk
+
+
+def step_metrics(wl, per_step_ms, world, peaks):
+    """Throughput and whole-step roofline figures of one step time."""
+    work = algorithmic(wl)
+    gbs = work["compulsory_bytes"] / (per_step_ms / 1e3) / 1e9
+    tfs = work["flops"] / (per_step_ms / 1e3) / 1e12
+    return {"value": job_throughput(world, wl.n_q, per_step_ms),
+            "tokens_per_s": work["scored_keys"] / (per_step_ms / 1e3) * world,
+            "step_hbm_gbs": gbs, "step_hbm_frac": gbs / peaks["hbm_gbs"],
+            "step_tflops": tfs, "step_tensor_frac": tfs / peaks["bf16_tflops"]}
+
+
+def other_config(dsa, name, dev, stream, no_graph, pg, local, world, peaks, peak_src):
+    """One more workload of the suite, timed like the headline (graph replay,
+    rotated copies, clocks sampled): step time, throughput, the dominant
+    launch's roofline."""
+    import torch
+    import workloads
+
+    wl = workloads.named(name)
+    sb = StepBench(dsa, wl, dev, stream, no_graph)
+    sb.prepare(5)
+    steps = agree_steps(pg, sb.calibrate(1.0), dev)
+    ms, clk = sb.timed(steps, pg, local)
+    fused, sel_ms, idx_ms = dominant_launch(dsa, wl, sb.sh, sb.b, sb.d, sb.keys, sb.copies, stream,
+                                            max(10, min(steps, 200)))
+    ms, sel_ms, idx_ms = max_over_ranks(pg, [ms, sel_ms, idx_ms], dev)
+    per = ms / steps
+    ent = {"unit": UNIT, "steps": steps, "ms_per_step": per, "dtype": wl.dtype,
+           "config": workload_config(wl, world), "launch": sb.launch_mode,
+           "gpu_launches": sb.plan["kernel_launches"] * steps, "plan": sb.plan, "clocks": clk}
+    ent.update(step_metrics(wl, per, world, peaks))
+    ent["roofline"] = roofline_of(wl, fused, sel_ms, idx_ms, peaks, peak_src)
+    del sb
+    torch.cuda.empty_cache()
+    return ent
+
+
 def run_ours(args):
     import torch
 
@@ -374,136 +614,21 @@ def run_ours(args):
     dsa.load()
 
     wl = workloads.named(args.workload)
-    per_copy = algorithmic(wl)["step_bytes"]
-    copies = max(2, math.ceil(2 * L2_BYTES / max(per_copy, 1)))
-    copies = min(copies, 8)
-    d = workloads.make(wl, dev, copies=copies)
-    sh = dsa.make_shape(wl.idx_heads, wl.idx_dim, wl.heads, wl.kv_lora, wl.rope, wl.top_k,
-                        wl.kpool, wl.scale, wl.dtype)
-    b = dsa.make_batch(d["row_off"], d["key_off"], d["q_off"], wl.n_q, max(wl.q_lens),
-                       max(wl.kv_lens), sum(wl.kv_lens), sum(wl.key_counts()))
-    ws = dsa.alloc_workspace(sh, b, dsa.OP_DECODE_STEP, dev)
-    width = dsa.dsa_index_row_width(sh)
-    plan = dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP)
-    out = torch.empty((wl.n_q, wl.heads, wl.kv_lora), device=dev)
-    lse = torch.empty((wl.n_q, wl.heads), device=dev)
-    idx = torch.empty((wl.n_q, width), dtype=torch.int32, device=dev)
-    n_sel = torch.empty(wl.n_q, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    keys, caches = d["k_idx_copies"], d["cache_copies"]
-
-    def launch(i, st):
-        c = i % copies
-        dsa.dsa_decode_step(sh, b, d["q_idx"], d["w"], keys[c], d["q_abs"], caches[c], out, lse,
-                            idx, n_sel, ws, st)
-
-    def step(i):
-        launch(i, stream)
-
-    # default step count: about two seconds of timed work
+    sb = StepBench(dsa, wl, dev, stream, args.no_graph)
+    sh, b, d, keys, caches, copies = sb.sh, sb.b, sb.d, sb.keys, sb.caches, sb.copies
+    out, lse, idx, n_sel, ws = sb.out, sb.lse, sb.idx, sb.n_sel, sb.ws
     warm = args.warmup if args.warmup is not None else 20
-    for i in range(max(warm, 3)):
-        step(i)
-    torch.cuda.synchronize(dev)
-    if dsa.dsa_check_device_error(ws, stream) != 0:
-        raise RuntimeError("device error during warm-up")
-    # A decode loop replays its step from CUDA graphs (the launches of a step
-    # and of consecutive steps then overlap through programmatic dependent
-    # launch without host round trips): one graph of G steps over the input
-    # copies in turn, and one single-step graph per copy for the remainder, so
-    # that exactly K steps run.
-    run_steps = None
-    launch_mode = "stream launches"
-    if not args.no_graph:
-        G = copies * max(1, 12 // copies)
-        g_all = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_all):
-            for i in range(G):
-                launch(i, torch.cuda.current_stream(dev))
-        g_one = []
-        for c in range(copies):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                launch(c, torch.cuda.current_stream(dev))
-            g_one.append(g)
-
-        def run_steps(n):
-            for _ in range(n // G):
-                g_all.replay()
-            for i in range(n % G):
-                g_one[i % copies].replay()
-
-        run_steps(G)                                 # untimed: the graphs' first replays
-        torch.cuda.synchronize(dev)
-        if dsa.dsa_check_device_error(ws, stream) != 0:
-            raise RuntimeError("device error in the graph warm-up")
-        launch_mode = f"CUDA graphs of {G} steps (+ single-step graphs for the remainder)"
-    else:
-        def run_steps(n):
-            for i in range(n):
-                step(i)
-
-    if args.steps is None:
-        t0 = time.perf_counter()
-        run_steps(60)
-        torch.cuda.synchronize(dev)
-        per = (time.perf_counter() - t0) / 60
-        steps = int(min(200000, max(20, 2.0 / max(per, 1e-7))))
-    else:
-        steps = args.steps
+    sb.prepare(warm)
+    launch_mode, plan = sb.launch_mode, sb.plan
+    # default step count: about two seconds of timed work
+    steps = args.steps if args.steps is not None else sb.calibrate(2.0)
     steps = agree_steps(pg, steps, dev)
+    ms, clk = sb.timed(steps, pg, local)
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    run_steps(steps)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    if pg:
-        pg.barrier()
-    clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if dsa.dsa_check_device_error(ws, stream) != 0:
-        raise RuntimeError("device error during the timed region")
-
-    # dominant kernel, timed alone on the same stream with the same rotation
-    sb = torch.empty((wl.n_q, max(max(wl.kv_lens) // wl.kpool, 4)), device=dev)
-    ld = sb.shape[1]
-    ws_i = dsa.alloc_workspace(sh, b, dsa.OP_INDEX_SCORES, dev)
-    n_idx = max(10, min(steps, 2000))
-    for i in range(3):
-        dsa.dsa_index_scores(sh, b, d["q_idx"], d["w"], keys[i % copies], sb, ld, ws_i, stream)
+    fused, sel_ms, idx_ms = dominant_launch(dsa, wl, sh, b, d, keys, copies, stream,
+                                            max(10, min(steps, 2000)))
     k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for i in range(n_idx):
-        dsa.dsa_index_scores(sh, b, d["q_idx"], d["w"], keys[i % copies], sb, ld, ws_i, stream)
-    k1.record(stream)
-    torch.cuda.synchronize(dev)
-    idx_ms = k0.elapsed_time(k1) / n_idx
-
-    # steps 1 and 2 as the step runs them: one fused launch for small decode
-    # batches, which is then the step's dominant kernel
-    fused = dsa.dsa_plan(sh, b, dsa.OP_INDEX_SELECT)["kernel_launches"] == 1
-    sel_ms = 0.0
-    if fused:
-        ws_s = dsa.alloc_workspace(sh, b, dsa.OP_INDEX_SELECT, dev)
-        idx_s, nsel_s = torch.empty_like(idx), torch.empty_like(n_sel)
-        for i in range(3):
-            dsa.dsa_index_select(sh, b, d["q_idx"], d["w"], keys[i % copies], idx_s, nsel_s, ws_s,
-                                 stream)
-        k0.record(stream)
-        for i in range(n_idx):
-            dsa.dsa_index_select(sh, b, d["q_idx"], d["w"], keys[i % copies], idx_s, nsel_s, ws_s,
-                                 stream)
-        k1.record(stream)
-        torch.cuda.synchronize(dev)
-        sel_ms = k0.elapsed_time(k1) / n_idx
-        if dsa.dsa_check_device_error(ws_s, stream) != 0:
-            raise RuntimeError("device error in the fused selection loop")
 
     # k-pool workloads: the pool-key compression of every pool of the
     # workload's sequences (q_len = kv_len: a prefill's worth of cells, seeded
@@ -594,6 +719,21 @@ def run_ours(args):
         e2e["ms_per_step"] = max_over_ranks(pg, [e2e["ms_per_step"]], dev)[0]
         e2e["value"] = job_throughput(world, wl.n_q, e2e["ms_per_step"])
 
+    peaks, peak_src = measured_peaks()
+    # the other workloads of the suite, each timed the same way
+    configs = {}
+    if not args.no_configs:
+        names = [n for n in workloads.NAMES if n != wl.name]
+        # the headline's inputs the CPU baseline reads stay; the rotated copies go
+        host_d = {k: d[k] for k in ("q_idx", "w", "q_abs", "k_idx", "cache", "row_off",
+                                    "key_off", "q_off")} if not args.no_cpu_baseline else None
+        del sb, keys, caches, d, out, lse, idx, n_sel, ws
+        torch.cuda.empty_cache()
+        for name in names:
+            configs[name] = other_config(dsa, name, dev, stream, args.no_graph, pg, local, world,
+                                         peaks, peak_src)
+        d = host_d
+
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -601,42 +741,17 @@ def run_ours(args):
 
     per_step_ms = ms / steps
     work = algorithmic(wl)
-    value = job_throughput(world, wl.n_q, per_step_ms)
-    peaks, peak_src = measured_peaks()
     achieved_idx = work["index_launch_bytes"] / (idx_ms / 1e3) / 1e9
-    if fused:
-        dom = {"kernel": "index_select_fused", "ms": sel_ms,
-               "bytes": work["index_launch_bytes"] + work["select_bytes"]}
-    else:
-        dom = {"kernel": "index_scores_tc", "ms": idx_ms, "bytes": work["index_launch_bytes"]}
-    achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
-    # A prefill chunk re-reads each key tile for many queries: its indexer does
-    # far more flops per byte than the GPU's flop/byte balance and is bound by
-    # the tensor pipe, so its roofline is in TFLOP/s against the bf16 peak.
-    tensor_bound = (work["flops_index"] / max(work["index_launch_bytes"], 1) >
-                    peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9))
-    if tensor_bound and not fused:
-        roof = {"bound": "tensor", "kernel": dom["kernel"],
-                "achieved": work["flops_index"] / (dom["ms"] / 1e3) / 1e12,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "flops_per_launch": work["flops_index"], "peak_source": f"{peak_src} bf16_tflops"}
-    else:
-        roof = {"bound": "hbm", "kernel": dom["kernel"], "achieved": achieved,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "bytes_per_launch": dom["bytes"],
-                "peak_source": f"{peak_src} hbm_gbs"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = kernel_traffic(dom["kernel"], wl.name)
-    roof["launch_us"] = dom["ms"] * 1e3
+    sm = step_metrics(wl, per_step_ms, world, peaks)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "metric": METRIC, "value": sm["value"], "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": max(warm, 3), "ms_per_step": per_step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": dict(workload_config(wl, world), launch=launch_mode),
-        "tokens_per_s": work["scored_keys"] / (per_step_ms / 1e3) * world,
-        "step_hbm_gbs": work["compulsory_bytes"] / (per_step_ms / 1e3) / 1e9,
-        "step_hbm_frac": work["compulsory_bytes"] / (per_step_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-        "step_tflops": work["flops"] / (per_step_ms / 1e3) / 1e12,
-        "roofline": roof,
+        "config": workload_config(wl, world), "launch": launch_mode,
+        "tokens_per_s": sm["tokens_per_s"],
+        "step_hbm_gbs": sm["step_hbm_gbs"], "step_hbm_frac": sm["step_hbm_frac"],
+        "step_tflops": sm["step_tflops"],
+        "roofline": roofline_of(wl, fused, sel_ms, idx_ms, peaks, peak_src),
         "indexer_alone": {"kernel": "index_scores_tc", "launch_us": idx_ms * 1e3,
                           "bytes_per_launch": work["index_launch_bytes"],
                           "achieved_gbs": achieved_idx, "frac": achieved_idx / peaks["hbm_gbs"],
@@ -656,12 +771,10 @@ def run_ours(args):
         pool["peak_source"] = f"{peak_src} hbm_gbs"
         pool["traffic"] = kernel_traffic("pool_compress", wl.name)
         line["pool_compress"] = pool
+    if configs:
+        line["configs"] = configs
     if not args.no_cpu_baseline:
-        n, el, threads = oracle_sample(wl, host_query_args(wl, d), args.cpu_seconds)
-        line["cpu_baseline"] = {
-            "value": n / el, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} quer{'y' if n == 1 else 'ies'} of the {wl.name} workload through the "
-                      f"oracle (double precision, {threads} OpenMP threads), {el:.1f} s"}
+        line["cpu_baseline"] = oracle_baseline(wl, d, args.cpu_seconds, args.cpu_seconds / 3)
     if pg:
         pg.destroy_process_group()
     return line

@@ -33,7 +33,8 @@ __all__ = [
     "dsa_sparse_mla_attn",
     "dsa_decode_step", "dsa_decode_step_noalloc", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
     "OP_INDEX_SCORES", "OP_TOPK_SELECT", "OP_SPARSE_MLA", "OP_DECODE_STEP", "OP_INDEX_SELECT",
-    "OP_POOL_COMPRESS", "dsa_pool_compress", "dsa_index_prepare",
+    "OP_POOL_COMPRESS", "dsa_pool_compress", "dsa_index_prepare", "dsa_workspace_set_wait_budget",
+    "FLAG_TWO_LAUNCH", "FLAG_DESC_ORDER", "FLAG_DENSE",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
@@ -41,6 +42,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
 DSA_F32, DSA_BF16 = 0, 1
 OP_INDEX_SCORES, OP_TOPK_SELECT, OP_SPARSE_MLA, OP_DECODE_STEP, OP_INDEX_SELECT = 0, 1, 2, 3, 4
 OP_POOL_COMPRESS = 5
+FLAG_TWO_LAUNCH, FLAG_DESC_ORDER, FLAG_DENSE = 0x1, 0x2, 0x4
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
           3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE", 6: "DSA_ERR_TIMEOUT"}
 
@@ -60,7 +62,7 @@ class Shape(ctypes.Structure):
 
 class Batch(ctypes.Structure):
     _fields_ = [("n_seq", ctypes.c_int32), ("n_q", ctypes.c_int32),
-                ("max_q_len", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("max_q_len", ctypes.c_int32), ("flags", ctypes.c_uint32),
                 ("max_kv_len", ctypes.c_int64), ("total_rows", ctypes.c_int64),
                 ("total_keys", ctypes.c_int64), ("row_off", ctypes.c_void_p),
                 ("key_off", ctypes.c_void_p), ("q_off", ctypes.c_void_p)]
@@ -104,6 +106,7 @@ def load() -> ctypes.CDLL:
             "dsa_decode_step_noalloc": ([S, B, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "dsa_pool_compress": ([S, B, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_index_prepare": ([S, i64, P, P, i32, ctypes.c_double, P, P], ctypes.c_int),
+            "dsa_workspace_set_wait_budget": ([P, sz, ctypes.c_uint64, P], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -145,18 +148,19 @@ def make_shape(idx_heads=32, idx_dim=128, heads=64, kv_lora=512, rope_dim=64, to
 
 
 def make_batch(row_off: torch.Tensor, key_off: torch.Tensor, q_off: torch.Tensor, n_q: int,
-               max_q_len: int, max_kv_len: int, total_rows: int, total_keys: int) -> Batch:
+               max_q_len: int, max_kv_len: int, total_rows: int, total_keys: int,
+               flags: int = 0) -> Batch:
     """Batch descriptor over int64 device offset arrays of n_seq+1 entries.
 
     ``total_rows`` / ``total_keys`` are the row counts of the cache and key
-    tensors.  The returned structure holds raw pointers: keep the three
-    tensors alive while it is in use.
+    tensors; ``flags`` the call's ``FLAG_*`` options.  The returned structure
+    holds raw pointers: keep the three tensors alive while it is in use.
     """
     for t in (row_off, key_off, q_off):
         if t.dtype != torch.int64:
             raise ValueError("offset arrays are int64")
     n_seq = row_off.numel() - 1
-    b = Batch(n_seq, int(n_q), int(max_q_len), 0, int(max_kv_len), int(total_rows),
+    b = Batch(n_seq, int(n_q), int(max_q_len), int(flags), int(max_kv_len), int(total_rows),
               int(total_keys), _ptr(row_off), _ptr(key_off), _ptr(q_off))
     b._keep = (row_off, key_off, q_off)
     return b
@@ -248,13 +252,20 @@ def dsa_index_prepare(shape, x, pos, rope_dims, rope_base, out, stream=None) -> 
           int(rope_dims), float(rope_base), _ptr(out), _stream(stream))
 
 
-def dsa_check_device_error(ws: torch.Tensor, stream=None) -> int:
-    """Synchronise the stream and return (and clear) the device error code."""
+def dsa_check_device_error(ws: Optional[torch.Tensor], stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error code;
+    ``ws=None`` reads the no-allocation entry point's scratch array."""
     code = ctypes.c_int32(0)
-    rc = load().dsa_check_device_error(_ptr(ws), ws.numel(), _stream(stream), ctypes.byref(code))
+    rc = load().dsa_check_device_error(_ptr(ws), ws.numel() if ws is not None else 0,
+                                       _stream(stream), ctypes.byref(code))
     if rc not in (0, 5, 6):
         raise DsaError("dsa_check_device_error", rc)
     return int(code.value)
+
+
+def dsa_workspace_set_wait_budget(ws: torch.Tensor, ns: int, stream=None) -> None:
+    """Budget of the waits between CTAs of kernels using ``ws`` (0 = default)."""
+    _call("dsa_workspace_set_wait_budget", _ptr(ws), ws.numel(), int(ns), _stream(stream))
 
 
 class DecodeStep:

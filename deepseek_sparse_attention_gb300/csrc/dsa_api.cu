@@ -12,6 +12,7 @@ namespace dsa {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr uint32_t kKnownFlags = DSA_FLAG_TWO_LAUNCH | DSA_FLAG_DESC_ORDER | DSA_FLAG_DENSE;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -53,8 +54,8 @@ dsa_status check_shape(const dsa_shape* s, Shape* out) {
 dsa_status check_batch(const dsa_batch* b, const Shape& sh, BatchDev* out,
                        int64_t max_n_q = 65535) {
     if (b == nullptr) return DSA_ERR_INVALID_ARG;
-    if (b->n_seq < 0 || b->n_q < 0 || b->max_q_len < 0 || b->max_kv_len < 0 || b->reserved != 0 ||
-        b->total_rows < 0 || b->total_keys < 0)
+    if (b->n_seq < 0 || b->n_q < 0 || b->max_q_len < 0 || b->max_kv_len < 0 ||
+        (b->flags & ~kKnownFlags) != 0 || b->total_rows < 0 || b->total_keys < 0)
         return DSA_ERR_INVALID_ARG;
     if (b->n_q > 0) {
         if (b->n_seq < 1 || b->row_off == nullptr || b->key_off == nullptr || b->q_off == nullptr)
@@ -65,9 +66,19 @@ dsa_status check_batch(const dsa_batch* b, const Shape& sh, BatchDev* out,
     }
     if (b->max_kv_len >= ((int64_t)1 << 31)) return DSA_ERR_UNSUPPORTED;
     if (b->n_q > max_n_q) return DSA_ERR_UNSUPPORTED;
-    *out = BatchDev{b->row_off,    b->key_off,    b->q_off,      b->n_seq, b->n_q,
-                    b->max_q_len,  b->max_kv_len, b->total_rows, b->total_keys, sh.kpool};
+    // descending order sorts a query's selected units in shared memory
+    if ((b->flags & DSA_FLAG_DESC_ORDER) && sh.top_k / sh.kpool > 16384) return DSA_ERR_UNSUPPORTED;
+    *out = BatchDev{b->row_off,    b->key_off,    b->q_off,      b->n_seq,      b->n_q,
+                    b->max_q_len,  b->max_kv_len, b->total_rows, b->total_keys, sh.kpool,
+                    b->flags};
     return DSA_OK;
+}
+
+// The host scalars of a batch, for sizing and planning (no device pointers).
+BatchDev host_batch(const dsa_batch* batch, const Shape& sh) {
+    return BatchDev{nullptr,           nullptr,           nullptr,           batch->n_seq,
+                    batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
+                    batch->total_keys, sh.kpool,          batch->flags};
 }
 
 // Keys a query may score at most, and the default score row stride.
@@ -131,7 +142,8 @@ dsa_status cuda_status(cudaError_t e, const char* what) {
 unsigned char* bytes(void* p) { return static_cast<unsigned char*>(p); }
 
 // Steps 1 and 2 into idx / n_sel: the fused launch where it applies, else the
-// indexer and the selection.
+// indexer and the selection; with DSA_FLAG_DESC_ORDER each row is then put in
+// descending score order.
 cudaError_t enqueue_index_select(const Shape& sh, const BatchDev& b, const StepLayout& lay,
                                  void* ws, const void* q_idx, const float* w, const void* k_idx,
                                  int32_t* idx, int32_t* n_sel, cudaStream_t st,
@@ -151,10 +163,62 @@ cudaError_t enqueue_index_select(const Shape& sh, const BatchDev& b, const StepL
                                         bytes(ws) + lay.idx_plan, err, st);
     if (e != cudaSuccess) return e;
     *what = "topk_select";
-    return launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
+    e = launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
+    if (e != cudaSuccess || !(b.flags & DSA_FLAG_DESC_ORDER)) return e;
+    *what = "select_order";
+    return launch_select_order_desc(sh, b, scores, ld, idx, n_sel, err, st);
+}
+
+// Kernels one call of `op` enqueues for this shape and batch bound.
+int32_t plan_launches(const Shape& sh, const BatchDev& bh, int32_t op, int32_t splits) {
+    if (bh.n_q <= 0) return 0;
+    // attention, then the split merge -- except for two tensor-core splits,
+    // which merge inside the attention launch (a CTA pair)
+    const int32_t attn = splits > 2 || (splits == 2 && !sparse_mla_tc_eligible(sh, bh)) ? 2 : 1;
+    const int32_t idx = bh.max_kv_len / sh.kpool > 0
+                            ? (index_scores_tc_eligible(sh, bh) ? index_scores_tc_launches(sh, bh) : 1)
+                            : 0;
+    const int32_t order = (bh.flags & DSA_FLAG_DESC_ORDER) ? 1 : 0;
+    const int32_t sel = index_select_fused_eligible(sh, bh) ? 1 : idx + 1 + order;
+    switch (op) {
+        case DSA_OP_INDEX_SCORES: return idx;
+        case DSA_OP_TOPK_SELECT: return 1 + order;
+        case DSA_OP_SPARSE_MLA: return attn;
+        case DSA_OP_INDEX_SELECT: return sel;
+        case DSA_OP_POOL_COMPRESS: return sh.kpool > 1 ? 1 : 0;
+        default: return (bh.flags & DSA_FLAG_DENSE) ? attn : sel + attn;
+    }
 }
 
 }  // namespace
+
+// Host validation of dsa_decode_step's arguments, everything but the
+// workspace: shapes, pointers, alignment, flags.  *ws_need receives the bytes
+// of workspace the step needs and *n_q its query count.
+dsa_status decode_step_check(const dsa_shape* shape, const dsa_batch* batch, const void* q_idx,
+                             const float* w, const void* k_idx, const void* q_abs,
+                             const void* cache, const float* out, const float* lse,
+                             const int32_t* idx_out, const int32_t* n_sel_out, size_t* ws_need,
+                             int32_t* n_q) {
+    Shape sh;
+    BatchDev b;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    const bool dense = (b.flags & DSA_FLAG_DENSE) != 0;
+    if (dense && (idx_out != nullptr || n_sel_out != nullptr)) return DSA_ERR_INVALID_ARG;
+    if (b.n_q > 0 && (q_abs == nullptr || cache == nullptr || out == nullptr ||
+                      (!dense && (q_idx == nullptr || w == nullptr || k_idx == nullptr))))
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q_abs) ||
+        !aligned16(cache) || !aligned16(out) || !aligned16(idx_out) || !aligned16(n_sel_out) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        return DSA_ERR_INVALID_ARG;
+    if (ws_need != nullptr) *ws_need = step_layout(sh, b).total;
+    if (n_q != nullptr) *n_q = b.n_q;
+    return DSA_OK;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -185,20 +249,18 @@ int64_t dsa_index_row_width(const dsa_shape* shape) {
 dsa_status dsa_workspace_size(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
                               size_t* out_bytes) {
     Shape sh;
-    BatchDev b;
     if (out_bytes == nullptr) return DSA_ERR_INVALID_ARG;
     dsa_status s = check_shape(shape, &sh);
     if (s != DSA_OK) return s;
     // Sizing needs only the host scalars of the batch.
-    if (batch == nullptr || batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
+    if (batch == nullptr || batch->n_q < 0 || batch->max_kv_len < 0 ||
+        (batch->flags & ~kKnownFlags) != 0)
+        return DSA_ERR_INVALID_ARG;
     if (batch->max_kv_len >= ((int64_t)1 << 31) ||
         (batch->n_q > 65535 && op != DSA_OP_POOL_COMPRESS))
         return DSA_ERR_UNSUPPORTED;
-    b = BatchDev{nullptr,           nullptr,           nullptr,           batch->n_seq,
-                 batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
-                 batch->total_keys, sh.kpool};
     if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_POOL_COMPRESS) return DSA_ERR_INVALID_ARG;
-    *out_bytes = op_bytes(sh, b, op);
+    *out_bytes = op_bytes(sh, host_batch(batch, sh), op);
     return DSA_OK;
 }
 
@@ -208,31 +270,13 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
     if (info == nullptr || batch == nullptr) return DSA_ERR_INVALID_ARG;
     dsa_status s = check_shape(shape, &sh);
     if (s != DSA_OK) return s;
-    if (batch->n_q < 0 || batch->max_kv_len < 0) return DSA_ERR_INVALID_ARG;
+    if (batch->n_q < 0 || batch->max_kv_len < 0 || (batch->flags & ~kKnownFlags) != 0)
+        return DSA_ERR_INVALID_ARG;
     if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_POOL_COMPRESS) return DSA_ERR_INVALID_ARG;
-    const BatchDev bh{nullptr,           nullptr,           nullptr,           batch->n_seq,
-                      batch->n_q,        batch->max_q_len,  batch->max_kv_len, batch->total_rows,
-                      batch->total_keys, sh.kpool};
+    const BatchDev bh = host_batch(batch, sh);
     int32_t rps = 0, splits = 0;
     plan_attention_splits(sh, bh, &rps, &splits);
-    // attention, then the split merge -- except for two tensor-core splits,
-    // which merge inside the attention launch (a CTA pair)
-    const int32_t attn = splits > 2 || (splits == 2 && !sparse_mla_tc_eligible(sh, bh)) ? 2 : 1;
-    const int32_t idx = batch->max_kv_len / sh.kpool > 0
-                            ? (index_scores_tc_eligible(sh, bh) ? index_scores_tc_launches(sh, bh) : 1)
-                            : 0;
-    int32_t n = 0;
-    if (batch->n_q > 0) {
-        switch (op) {
-            case DSA_OP_INDEX_SCORES: n = idx; break;
-            case DSA_OP_TOPK_SELECT: n = 1; break;
-            case DSA_OP_SPARSE_MLA: n = attn; break;
-            case DSA_OP_INDEX_SELECT: n = index_select_fused_eligible(sh, bh) ? 1 : idx + 1; break;
-            case DSA_OP_POOL_COMPRESS: n = sh.kpool > 1 ? 1 : 0; break;
-            default: n = (index_select_fused_eligible(sh, bh) ? 1 : idx + 1) + attn; break;
-        }
-    }
-    *info = dsa_plan_info{n, splits, rps, 0};
+    *info = dsa_plan_info{plan_launches(sh, bh, op, splits), splits, rps, 0};
     return DSA_OK;
 }
 
@@ -265,15 +309,18 @@ dsa_status dsa_topk_select(const dsa_shape* shape, const dsa_batch* batch, const
     dsa_status s = check_shape(shape, &sh);
     if (s != DSA_OK) return s;
     if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    if (b.flags & DSA_FLAG_DENSE) return DSA_ERR_INVALID_ARG;   // no selection to make
     if (b.n_q > 0 && (scores == nullptr || idx == nullptr || n_sel == nullptr))
         return DSA_ERR_INVALID_ARG;
     if (!aligned16(scores) || !aligned16(idx) || !aligned16(n_sel)) return DSA_ERR_INVALID_ARG;
     if (ld < max_keys(sh, b) || ld < 1) return DSA_ERR_INVALID_ARG;
     if ((s = check_ws(ws, ws_bytes, op_bytes(sh, b, DSA_OP_TOPK_SELECT))) != DSA_OK) return s;
     int32_t* err = static_cast<int32_t*>(ws);
-    return cuda_status(launch_topk_select(sh, b, scores, ld, idx, n_sel, err,
-                                          static_cast<cudaStream_t>(stream)),
-                       "topk_select");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_topk_select(sh, b, scores, ld, idx, n_sel, err, st);
+    if (e == cudaSuccess && (b.flags & DSA_FLAG_DESC_ORDER))
+        e = launch_select_order_desc(sh, b, scores, ld, idx, n_sel, err, st);
+    return cuda_status(e, "topk_select");
 }
 
 dsa_status dsa_sparse_mla_attn(const dsa_shape* shape, const dsa_batch* batch, const void* q_abs,
@@ -284,17 +331,21 @@ dsa_status dsa_sparse_mla_attn(const dsa_shape* shape, const dsa_batch* batch, c
     dsa_status s = check_shape(shape, &sh);
     if (s != DSA_OK) return s;
     if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
-    if (b.n_q > 0 && (q_abs == nullptr || cache == nullptr || idx == nullptr || n_sel == nullptr ||
-                      out == nullptr))
+    const bool dense = (b.flags & DSA_FLAG_DENSE) != 0;
+    if (b.n_q > 0 && (q_abs == nullptr || cache == nullptr || out == nullptr ||
+                      (!dense && (idx == nullptr || n_sel == nullptr))))
         return DSA_ERR_INVALID_ARG;
     if (!aligned16(q_abs) || !aligned16(cache) || !aligned16(out) || !aligned16(idx))
         return DSA_ERR_INVALID_ARG;
     const size_t need = op_bytes(sh, b, DSA_OP_SPARSE_MLA);
     if ((s = check_ws(ws, ws_bytes, need)) != DSA_OK) return s;
     int32_t* err = static_cast<int32_t*>(ws);
-    return cuda_status(launch_sparse_mla(sh, b, q_abs, cache, idx, n_sel, out, lse,
+    // The previous kernel in the stream is the caller's: the query is read
+    // only after it has completed.
+    return cuda_status(launch_sparse_mla(sh, b, q_abs, cache, dense ? nullptr : idx,
+                                         dense ? nullptr : n_sel, out, lse,
                                          bytes(ws) + kWsHeaderBytes, need - kWsHeaderBytes, err,
-                                         static_cast<cudaStream_t>(stream)),
+                                         /*q_early=*/false, static_cast<cudaStream_t>(stream)),
                        "sparse_mla_attn");
 }
 
@@ -341,32 +392,40 @@ dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const
                            const float* w, const void* k_idx, const void* q_abs,
                            const void* cache, float* out, float* lse, int32_t* idx_out,
                            int32_t* n_sel_out, void* ws, size_t ws_bytes, void* stream) {
+    size_t need = 0;
+    int32_t n_q = 0;
+    dsa_status s = decode_step_check(shape, batch, q_idx, w, k_idx, q_abs, cache, out, lse,
+                                     idx_out, n_sel_out, &need, &n_q);
+    if (s != DSA_OK) return s;
+    if ((s = check_ws(ws, ws_bytes, need)) != DSA_OK) return s;
+    if (n_q == 0) return DSA_OK;
     Shape sh;
     BatchDev b;
-    dsa_status s = check_shape(shape, &sh);
-    if (s != DSA_OK) return s;
-    if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
-    if (b.n_q > 0 && (q_idx == nullptr || w == nullptr || k_idx == nullptr || q_abs == nullptr ||
-                      cache == nullptr || out == nullptr))
-        return DSA_ERR_INVALID_ARG;
-    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(k_idx) || !aligned16(q_abs) ||
-        !aligned16(cache) || !aligned16(out) || !aligned16(idx_out) || !aligned16(n_sel_out))
-        return DSA_ERR_INVALID_ARG;
+    check_shape(shape, &sh);
+    check_batch(batch, sh, &b);
     const StepLayout lay = step_layout(sh, b);
-    if ((s = check_ws(ws, ws_bytes, lay.total)) != DSA_OK) return s;
-    if (b.n_q == 0) return DSA_OK;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int32_t* err = static_cast<int32_t*>(ws);
+    if (trace_on())
+        fprintf(stderr, "[dsa] decode_step n_q=%d max_kv=%lld flags=%u ws=%zu\n", b.n_q,
+                (long long)b.max_kv_len, b.flags, lay.total);
+    if (b.flags & DSA_FLAG_DENSE) {
+        // the indexer's A/B switch: every visible row, no scoring or selection
+        return cuda_status(launch_sparse_mla(sh, b, q_abs, cache, nullptr, nullptr, out, lse,
+                                             bytes(ws) + lay.attn, lay.total - lay.attn, err,
+                                             /*q_early=*/false, st),
+                           "decode_step/dense attention");
+    }
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(bytes(ws) + lay.idx);
     int32_t* n_sel = n_sel_out ? n_sel_out : reinterpret_cast<int32_t*>(bytes(ws) + lay.n_sel);
-    if (trace_on())
-        fprintf(stderr, "[dsa] decode_step n_q=%d max_kv=%lld ws=%zu\n", b.n_q,
-                (long long)b.max_kv_len, lay.total);
     const char* what = "";
     cudaError_t e = enqueue_index_select(sh, b, lay, ws, q_idx, w, k_idx, idx, n_sel, st, &what);
     if (e != cudaSuccess) return cuda_status(e, what);
+    // The kernel before the attention is this step's selection, which released
+    // its dependents only after waiting for the caller's kernels: the query
+    // may be loaded before the attention waits for the selection.
     e = launch_sparse_mla(sh, b, q_abs, cache, idx, n_sel, out, lse, bytes(ws) + lay.attn,
-                          lay.total - lay.attn, err, st);
+                          lay.total - lay.attn, err, /*q_early=*/true, st);
     return cuda_status(e, "decode_step/sparse_mla_attn");
 }
 
@@ -378,6 +437,7 @@ dsa_status dsa_index_select(const dsa_shape* shape, const dsa_batch* batch, cons
     dsa_status s = check_shape(shape, &sh);
     if (s != DSA_OK) return s;
     if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    if (b.flags & DSA_FLAG_DENSE) return DSA_ERR_INVALID_ARG;   // no selection to make
     if (b.n_q > 0 && (q_idx == nullptr || w == nullptr || k_idx == nullptr || idx == nullptr ||
                       n_sel == nullptr))
         return DSA_ERR_INVALID_ARG;
@@ -394,7 +454,13 @@ dsa_status dsa_index_select(const dsa_shape* shape, const dsa_batch* batch, cons
 }
 
 dsa_status dsa_check_device_error(void* ws, size_t ws_bytes, void* stream, int32_t* code) {
-    if (ws == nullptr || ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
+    if (ws == nullptr) {
+        // the no-allocation entry point's scratch array on the current device
+        dsa_status s = noalloc_scratch(&ws);
+        if (s != DSA_OK) return s;
+        ws_bytes = DSA_NOALLOC_SCRATCH_BYTES;
+    }
+    if (ws_bytes < kWsHeaderBytes) return DSA_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_status(e, "check_device_error/sync");
@@ -420,6 +486,17 @@ dsa_status dsa_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     const size_t n = ws_bytes < ws_zero_bytes() ? ws_bytes : ws_zero_bytes();
     return cuda_status(cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)),
                        "workspace_init");
+}
+
+dsa_status dsa_workspace_set_wait_budget(void* ws, size_t ws_bytes, uint64_t ns, void* stream) {
+    if (ws == nullptr || ws_bytes < kWsHeaderBytes ||
+        (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0)
+        return DSA_ERR_WORKSPACE;
+    // from pageable host memory: staged before the call returns
+    const uint64_t v = ns;
+    return cuda_status(cudaMemcpyAsync(bytes(ws) + kWsWaitBudgetOffset, &v, sizeof(v),
+                                       cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)),
+                       "workspace_set_wait_budget");
 }
 
 }  // extern "C"

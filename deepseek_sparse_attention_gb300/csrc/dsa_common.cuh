@@ -18,6 +18,10 @@ namespace dsa {
 constexpr size_t kWsHeaderBytes = 256;
 // Byte offset in the header of the fused kernel's grid barrier (two words).
 constexpr size_t kWsGridBarOffset = 64;
+// Byte offset in the header of the budget, in nanoseconds, of every wait of a
+// CTA on other CTAs (64 bits; 0 = the default of 2 s).
+constexpr size_t kWsWaitBudgetOffset = 128;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 enum DeviceError : int32_t {
     kDevOk = 0,
@@ -46,6 +50,7 @@ struct BatchDev {
     int64_t total_rows;
     int64_t total_keys;
     int32_t kpool;
+    uint32_t flags;        // DSA_FLAG_* of the call
 };
 
 struct QueryInfo {

@@ -33,6 +33,23 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // the header and the fused selection state (dsa_api.cu).
 size_t ws_zero_bytes();
 
+// Host validation of dsa_decode_step's arguments other than the workspace
+// (dsa_api.cu); *ws_need gets the workspace bytes the step needs, *n_q its
+// query count.
+dsa_status decode_step_check(const dsa_shape* shape, const dsa_batch* batch, const void* q_idx,
+                             const float* w, const void* k_idx, const void* q_abs,
+                             const void* cache, const float* out, const float* lse,
+                             const int32_t* idx_out, const int32_t* n_sel_out, size_t* ws_need,
+                             int32_t* n_q);
+
+// Device address of the no-allocation entry point's scratch array on the
+// current device (dsa_noalloc.cu), looked up once per device.
+dsa_status noalloc_scratch(void** out);
+
+// Streaming multiprocessors of the current device (index_scores_tc.cu); grid
+// and wave sizes derive from it.
+int sm_count();
+
 // Validated layer geometry (see dsa_shape in dsa.h).
 struct Shape {
     int32_t idx_heads, idx_dim, heads, kv_lora, rope, top_k, kpool;
@@ -68,12 +85,20 @@ cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* 
                                int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
                                cudaStream_t st);
 
+// Selections in descending score order (select_order.cu): each query's row
+// of ascending selections, reordered by (score descending, index ascending);
+// in k-pool mode by pool, each pool's rows kept together, the tail last.
+cudaError_t launch_select_order_desc(const Shape& sh, const BatchDev& b, const float* scores,
+                                     int64_t ld, int32_t* idx, const int32_t* n_sel, int32_t* err,
+                                     cudaStream_t st);
+
 // Steps 1 and 2 fused for decode batches (index_select_fused.cu): one
 // cooperative launch of the tensor-core indexer that also selects, for at most
 // kFusedMaxQ queries each scored as its own group.  `state` holds
 // index_select_fused_state_bytes() bytes that must be zero before the first
 // launch (each launch leaves them zero); `gbar` two zeroed words for the grid
-// barrier.  DSA_FUSED_SELECT=0 in the environment turns the path off.
+// barrier, followed in the header by the wait budget.  DSA_FLAG_TWO_LAUNCH
+// and DSA_FLAG_DESC_ORDER turn the path off.
 constexpr int kFusedMaxQ = 16;
 constexpr int kFusedMaxGrid = 256;
 bool index_select_fused_eligible(const Shape& sh, const BatchDev& b);
@@ -99,22 +124,27 @@ cudaError_t launch_pool_compress(const Shape& sh, const BatchDev& b, const void*
 
 // Step 3.  bf16 rows run on the tensor cores (sparse_mla_tc.cu), float32 rows
 // on CUDA cores (sparse_mla.cu).  Row splits per query and the scratch for the
-// split-row partials (bytes; 0 if none is needed).
+// split-row partials (bytes; 0 if none is needed).  idx == nullptr (and
+// n_sel == nullptr) attends over every visible row (DSA_FLAG_DENSE).
+// q_early: the query may be loaded before the kernel waits for the previous
+// one (only when that kernel is this library's and released its dependents
+// after waiting for its own predecessors).
 void plan_attention_splits(const Shape& sh, const BatchDev& b, int32_t* rows_per_split,
                            int32_t* n_split);
 size_t sparse_mla_scratch_bytes(const Shape& sh, const BatchDev& b);
 cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
                                 const float* part_ml, float* out, float* lse, cudaStream_t st);
 bool sparse_mla_tc_eligible(const Shape& sh, const BatchDev& b);
-void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
-                              int32_t* rows_per_split, int32_t* n_split);
+void plan_attention_splits_tc(int32_t n_q, int64_t max_rows, int32_t* rows_per_split,
+                              int32_t* n_split);
 cudaError_t launch_sparse_mla_tc(const Shape& sh, const BatchDev& b, const void* q_abs,
                                  const void* cache, const int32_t* idx, const int32_t* n_sel,
                                  float* out, float* lse, float* part_o, float* part_ml,
-                                 int32_t rps, int32_t n_split, int32_t* err, cudaStream_t st);
+                                 int32_t rps, int32_t n_split, int32_t* err, bool q_early,
+                                 cudaStream_t st);
 cudaError_t launch_sparse_mla(const Shape& sh, const BatchDev& b, const void* q_abs,
                               const void* cache, const int32_t* idx, const int32_t* n_sel,
                               float* out, float* lse, void* scratch, size_t scratch_bytes,
-                              int32_t* err, cudaStream_t st);
+                              int32_t* err, bool q_early, cudaStream_t st);
 
 }  // namespace dsa

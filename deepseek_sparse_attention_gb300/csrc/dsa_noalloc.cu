@@ -19,7 +19,8 @@
 // call's contents: each call clears the part that must start at zero (the error
 // word, the grid barrier and the fused selection histograms) on its stream,
 // and two calls whose work overlaps on the GPU -- on different streams, or
-// different host threads -- race on the array.
+// different host threads -- race on the array.  The error word a call's kernels
+// record is read (and cleared) by dsa_check_device_error with a NULL workspace.
 #include <mutex>
 
 #include "dsa.h"
@@ -33,8 +34,12 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_ptr[kMaxDevices] = {};
 
+}  // namespace
+
+namespace dsa {
+
 // Device address of the scratch array on the current device (set up once).
-dsa_status scratch_for_current_device(void** out) {
+dsa_status noalloc_scratch(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
@@ -49,7 +54,7 @@ dsa_status scratch_for_current_device(void** out) {
     return DSA_OK;
 }
 
-}  // namespace
+}  // namespace dsa
 
 extern "C" dsa_status dsa_decode_step_noalloc(const dsa_shape* shape, const dsa_batch* batch,
                                               const void* q_idx, const float* w,
@@ -57,17 +62,16 @@ extern "C" dsa_status dsa_decode_step_noalloc(const dsa_shape* shape, const dsa_
                                               const void* cache, float* out, float* lse,
                                               int32_t* idx_out, int32_t* n_sel_out,
                                               void* stream) {
+    // every argument is checked before anything is enqueued
     size_t need = 0;
-    dsa_status s = dsa_workspace_size(shape, batch, DSA_OP_DECODE_STEP, &need);
+    int32_t n_q = 0;
+    dsa_status s = dsa::decode_step_check(shape, batch, q_idx, w, k_idx, q_abs, cache, out, lse,
+                                          idx_out, n_sel_out, &need, &n_q);
     if (s != DSA_OK) return s;
-    if (batch->n_q > 0 &&
-        (batch->row_off == nullptr || batch->key_off == nullptr || batch->q_off == nullptr ||
-         q_idx == nullptr || w == nullptr || k_idx == nullptr || q_abs == nullptr ||
-         cache == nullptr || out == nullptr))
-        return DSA_ERR_INVALID_ARG;
     if (need > (size_t)DSA_NOALLOC_SCRATCH_BYTES) return DSA_ERR_UNSUPPORTED;
+    if (n_q == 0) return DSA_OK;
     void* scratch = nullptr;
-    if ((s = scratch_for_current_device(&scratch)) != DSA_OK) return s;
+    if ((s = dsa::noalloc_scratch(&scratch)) != DSA_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(scratch, 0, dsa::ws_zero_bytes(), st) != cudaSuccess) return DSA_ERR_CUDA;
     return dsa_decode_step(shape, batch, q_idx, w, k_idx, q_abs, cache, out, lse, idx_out,

@@ -31,10 +31,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;         // bounded waits: 2 s
 
 // Host side (index_scores_tc.cu): a tensor map over a row-major [rows, 128]
 // bf16 matrix read in boxes of box_rows x 64 columns with the 128-byte swizzle
-// (false when the driver entry point is missing or the encoder refuses), and
-// the device's SM count.
+// (false when the driver entry point is missing or the encoder refuses).
 bool make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);
-int sm_count();
 
 struct IdxGroup {          // consecutive queries of one sequence scored together
     int64_t key0;          // first indexer key of the sequence

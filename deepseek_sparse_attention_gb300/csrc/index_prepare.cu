@@ -98,7 +98,7 @@ cudaError_t launch_index_prepare(const Shape& sh, int64_t n_vec, const float* x,
     // a persistent grid: enough CTAs to fill the GPU, each sets up its rope
     // rates once and walks vectors
     int64_t blocks = (n_vec + kWarpsPerCta - 1) / kWarpsPerCta;
-    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks > (int64_t)sm_count() * 8) blocks = (int64_t)sm_count() * 8;
     if (sh.dtype == DSA_BF16)
         index_prepare_kernel<__nv_bfloat16><<<(unsigned)blocks, 32 * kWarpsPerCta, 0, st>>>(
             n_vec, x, pos, rope_dims, base, static_cast<__nv_bfloat16*>(out));

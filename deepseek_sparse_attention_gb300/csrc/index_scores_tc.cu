@@ -60,6 +60,8 @@ bool make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t 
            CUDA_SUCCESS;
 }
 
+}  // namespace idxp
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -67,8 +69,6 @@ int sm_count() {
         return 148;
     return n;
 }
-
-}  // namespace idxp
 
 namespace {
 
@@ -150,12 +150,12 @@ idx_group_plan(BatchDev b, int32_t gq, int64_t* seq_goff, IdxGroup* groups, int6
 
 // ---------------------------------------------------------------- the kernel
 
-// The standalone indexer's epilogue policy: scores to global memory, once the
-// previous kernel in the stream (which may still read the score rows) is done.
+// The standalone indexer's epilogue policy: scores to global memory (the
+// kernel has waited for the previous kernel, which may read the score rows).
 struct ScoreStore {
     float* scores;
     int64_t ld;
-    __device__ void begin() { pdl_wait(); }
+    __device__ void begin() {}
     __device__ void emit(const IdxGroup& G, int j, int64_t t_row, bool valid, int64_t, int, float s) {
         if (valid) scores[(int64_t)(G.q0 + j) * ld + t_row] = s;
     }
@@ -172,8 +172,11 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     pdl_trigger();
+    // Everything below reads memory an earlier kernel may write -- the batch
+    // offsets, the plan kernel's arrays, the queries and keys the TMA loads --
+    // so nothing is read before the previous kernel is complete and visible.
+    pdl_wait();
     int64_t n_groups;
-    if (!local_plan) pdl_wait();                      // the plan kernel's arrays
     if (local_plan) {
         n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/4);
         groups = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);

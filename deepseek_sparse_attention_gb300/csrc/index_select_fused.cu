@@ -126,10 +126,12 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 
 // Every CTA arrives once on a 64-bit counter that only grows; the barrier is
 // complete when the counter reaches the next multiple of the grid size.  One
-// atomic per CTA and acquire loads while waiting (bounded: on timeout the error
-// word is set and false returned).  The counter starts at zero and each launch
-// adds a whole number of grid sizes.
-__device__ bool grid_barrier(unsigned long long* bar, int* red, int32_t* err, int32_t where) {
+// atomic per CTA and acquire loads while waiting, for at most `budget_ns` (the
+// workspace's wait budget): on timeout the error word is set and false
+// returned.  The counter starts at zero and each launch adds a whole number of
+// grid sizes.
+__device__ bool grid_barrier(unsigned long long* bar, int* red, int32_t* err, int32_t where,
+                             uint64_t budget_ns) {
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
@@ -138,7 +140,7 @@ __device__ bool grid_barrier(unsigned long long* bar, int* red, int32_t* err, in
         const unsigned long long target = (arrived / gridDim.x + 1) * gridDim.x;
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_u64(bar) < target) {
-            if (globaltimer_ns() - t0 > kWaitNs) {
+            if (globaltimer_ns() - t0 > budget_ns) {
                 record_error(err, kDevTimeout, where, 6);
                 ok = 0;
                 break;
@@ -456,6 +458,10 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     int* red = reinterpret_cast<int*>(smem + kOffRed);
 
     pdl_wait();                               // the inputs of the previous kernels
+    // the budget of the waits on other CTAs, from the workspace header (0: default)
+    uint64_t budget = *reinterpret_cast<const volatile uint64_t*>(
+        reinterpret_cast<const uint8_t*>(err) + kWsWaitBudgetOffset);
+    if (budget == 0) budget = kDefaultWaitNs;
     const int64_t n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/6);
     const IdxGroup* gs = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
     const int64_t* ts = reinterpret_cast<const int64_t*>(smem + C::kOffPlanT);
@@ -569,7 +575,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         for (int i = tid; i < S.n; i += kThreads) atomicAdd(&hist[keys[S.koff + i] >> kShift1], 1u);
         flush_hist<kBins1>(hist, gstate + (int64_t)S.q * kQueryWords + kOffH1);
     }
-    if (!grid_barrier(gbar, red, err, 61)) return;
+    if (!grid_barrier(gbar, red, err, 61, budget)) return;
 
     // ---- b1; counts above it; candidates in it
     for (int s = 0; s < nseg; ++s) {
@@ -607,7 +613,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     if (u_begin >= u_end)                   // no units: zero counts for every query
         for (int q = tid; q < bq.n_q; q += kThreads)
             gcnt[(int64_t)q * kFusedMaxGrid + cta] = make_int2(0, 0);
-    if (!grid_barrier(gbar, red, err, 62)) return;
+    if (!grid_barrier(gbar, red, err, 62, budget)) return;
     clear_level(gstate, bq.n_q, kOffH1, kBins1);
 
     // ---- one round of loads: every query's candidate count (does any need
@@ -665,7 +671,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         flush_hist<kBins2>(hist, gsq + kOffH2);
     }
-    if (!grid_barrier(gbar, red, err, 63)) return;
+    if (!grid_barrier(gbar, red, err, 63, budget)) return;
 
     // ---- bits 9..0 of the keys in (b1, b2)
     for (int s = 0; s < nseg; ++s) {
@@ -681,7 +687,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         flush_hist<kBins3>(hist, gsq + kOffH3);
     }
-    if (!grid_barrier(gbar, red, err, 64)) return;
+    if (!grid_barrier(gbar, red, err, 64, budget)) return;
 
     // ---- T exact; this CTA's counts above and at T
     for (int s = 0; s < nseg; ++s) {
@@ -707,7 +713,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         __syncthreads();
     }
-    if (!grid_barrier(gbar, red, err, 65)) return;
+    if (!grid_barrier(gbar, red, err, 65, budget)) return;
     clear_level(gstate, bq.n_q, kOffH2, kBins2 + kBins3);
     pdl_trigger();
 
@@ -734,13 +740,11 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
 }  // namespace
 
-bool index_select_fused_enabled() {
-    const char* v = getenv("DSA_FUSED_SELECT");
-    return !(v != nullptr && v[0] == '0');
-}
-
 bool index_select_fused_eligible(const Shape& sh, const BatchDev& b) {
-    if (!index_select_fused_enabled() || !index_scores_tc_eligible(sh, b)) return false;
+    // the two-launch plan on request; descending order needs the scores the
+    // two-launch indexer keeps
+    if (b.flags & (DSA_FLAG_TWO_LAUNCH | DSA_FLAG_DESC_ORDER | DSA_FLAG_DENSE)) return false;
+    if (!index_scores_tc_eligible(sh, b)) return false;
     if (!(b.max_q_len <= 1 || b.n_q < 8)) return false;           // one query per group
     if (b.n_q < 1 || b.n_q > kFusedMaxQ || b.max_kv_len >= ((int64_t)1 << 31)) return false;
     const int grid = sm_count();

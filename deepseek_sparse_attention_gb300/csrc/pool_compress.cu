@@ -93,11 +93,11 @@ pool_compress_kernel(BatchDev b, const T* __restrict__ cells, const float* __res
             float den = 0.f, num = 0.f;
 #pragma unroll
             for (int i = 0; i < KP; ++i) {
-                const float w = expf(z[i] - zmax);
+                const float w = z[i] == -INFINITY ? 0.f : expf(z[i] - zmax);   // masked slot
                 den += w;
                 num += w * key[i].v[e];
             }
-            out.v[e] = num / den;
+            out.v[e] = den > 0.f ? num / den : 0.f;          // every slot masked: 0
         }
     } else {
         float m[4], den[4], num[4];
@@ -117,7 +117,7 @@ pool_compress_kernel(BatchDev b, const T* __restrict__ cells, const float* __res
                     den[e] = den[e] * r + 1.f;
                     num[e] = num[e] * r + key.v[e];
                     m[e] = z;
-                } else {
+                } else if (z != -INFINITY) {                 // a masked slot weighs 0
                     const float w = expf(z - m[e]);
                     den[e] += w;
                     num[e] += w * key.v[e];
@@ -125,7 +125,7 @@ pool_compress_kernel(BatchDev b, const T* __restrict__ cells, const float* __res
             }
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) out.v[e] = num[e] / den[e];
+        for (int e = 0; e < 4; ++e) out.v[e] = den[e] > 0.f ? num[e] / den[e] : 0.f;
     }
     store4(pool_keys + (k0 + j) * kDim + c, out);
 }

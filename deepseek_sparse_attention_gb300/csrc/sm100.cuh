@@ -108,19 +108,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
-// Four arbitrary rows (r0..r3) of a 2-D tensor, columns [x, x + box width),
-// into shared memory as four consecutive rows (tensor map box one row high).
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t x, int32_t r0, int32_t r1, int32_t r2,
-                                            int32_t r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1),
-        "r"(r2), "r"(r3)
-        : "memory");
-}
-
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads of them (a tcgen05.mma operand written with st.shared).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -27,7 +27,6 @@ constexpr int kHeads = 64;
 constexpr int kTile = 16;        // rows per tile
 constexpr int kLatent = 512;     // value width
 constexpr int kSsStride = kTile + 1;
-constexpr int64_t kPlanSMs = 152;   // GB300 streaming multiprocessors
 
 // Shared-memory row stride in elements: the row width plus 16 bytes, so that
 // 16-byte reads of eight consecutive rows land in distinct banks.
@@ -97,8 +96,9 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
     const int split = blockIdx.x;
     QueryInfo qi;
     if (!query_info(b, q, qi, err, /*where=*/3)) return;
-    int64_t ns = n_sel[q];
-    ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
+    // no selection (idx == nullptr): every visible row, row j being row j
+    int64_t ns = idx == nullptr ? qi.L : n_sel[q];
+    if (idx != nullptr) ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
     const int64_t j_begin = (int64_t)split * rows_per_split;
     const int64_t j_end = j_begin + rows_per_split < ns ? j_begin + rows_per_split : ns;
 
@@ -121,7 +121,7 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
         if (tid < kTile) {
             int32_t r = -1;
             if (tid < nrows) {
-                r = idx[q * idx_width + j0 + tid];
+                r = idx == nullptr ? (int32_t)(j0 + tid) : idx[q * idx_width + j0 + tid];
                 if (r < 0 || r >= qi.L) {
                     record_error(err, kDevBadIndex, (int32_t)q, /*where=*/3);
                     r = -1;
@@ -281,12 +281,9 @@ merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __r
 }
 
 // Rows per split: enough CTAs to fill the GPU about twice, at least 64 rows each.
-void plan_splits_simt(const Shape& sh, int32_t n_q, int64_t max_kv_len, int32_t* rows_per_split,
-                      int32_t* n_split) {
-    int64_t max_rows = sh.index_row_width();
-    if (max_kv_len < max_rows) max_rows = max_kv_len;
+void plan_splits_simt(int32_t n_q, int64_t max_rows, int32_t* rows_per_split, int32_t* n_split) {
     if (max_rows < 1) max_rows = 1;
-    const int64_t target_ctas = 2 * kPlanSMs;
+    const int64_t target_ctas = 2 * (int64_t)sm_count();
     int64_t splits = (target_ctas + n_q - 1) / n_q;
     const int64_t max_splits = (max_rows + 63) / 64;
     if (splits > max_splits) splits = max_splits;
@@ -329,10 +326,14 @@ cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_
 void plan_attention_splits(const Shape& sh, const BatchDev& b, int32_t* rows_per_split,
                            int32_t* n_split) {
     const int32_t n_q = b.n_q > 0 ? b.n_q : 1;
+    // rows a query attends over at most: its selection, or every visible row
+    int64_t max_rows = b.max_kv_len;
+    if (!(b.flags & DSA_FLAG_DENSE) && sh.index_row_width() < max_rows)
+        max_rows = sh.index_row_width();
     if (sparse_mla_tc_eligible(sh, b))
-        plan_attention_splits_tc(sh, n_q, b.max_kv_len, rows_per_split, n_split);
+        plan_attention_splits_tc(n_q, max_rows, rows_per_split, n_split);
     else
-        plan_splits_simt(sh, n_q, b.max_kv_len, rows_per_split, n_split);
+        plan_splits_simt(n_q, max_rows, rows_per_split, n_split);
 }
 
 size_t sparse_mla_scratch_bytes(const Shape& sh, const BatchDev& b) {
@@ -346,7 +347,7 @@ size_t sparse_mla_scratch_bytes(const Shape& sh, const BatchDev& b) {
 cudaError_t launch_sparse_mla(const Shape& sh, const BatchDev& b, const void* q_abs,
                               const void* cache, const int32_t* idx, const int32_t* n_sel,
                               float* out, float* lse, void* scratch, size_t scratch_bytes,
-                              int32_t* err, cudaStream_t st) {
+                              int32_t* err, bool q_early, cudaStream_t st) {
     if (b.n_q == 0) return cudaSuccess;
     int32_t rps, n_split;
     plan_attention_splits(sh, b, &rps, &n_split);
@@ -361,7 +362,7 @@ cudaError_t launch_sparse_mla(const Shape& sh, const BatchDev& b, const void* q_
     }
     if (sparse_mla_tc_eligible(sh, b))
         return launch_sparse_mla_tc(sh, b, q_abs, cache, idx, n_sel, out, lse, part_o, part_ml,
-                                    rps, n_split, err, st);
+                                    rps, n_split, err, q_early, st);
     const bool f32 = sh.dtype == DSA_F32;
     if (sh.width() == 576) {
         return f32 ? launch_typed<float, 576>(sh, b, q_abs, cache, idx, n_sel, out, lse, part_o,

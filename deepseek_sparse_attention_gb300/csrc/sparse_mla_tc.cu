@@ -110,8 +110,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__ cache,
               BatchDev b, float scale, const int32_t* __restrict__ idx,
               const int32_t* __restrict__ n_sel, int64_t idx_width, int32_t rows_per_split,
-              int32_t n_split, int32_t pair, float* __restrict__ out, float* __restrict__ lse,
-              float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* err) {
+              int32_t n_split, int32_t pair, int32_t q_early, float* __restrict__ out,
+              float* __restrict__ lse, float* __restrict__ part_o, float* __restrict__ part_ml,
+              int32_t* err) {
     using C = Cfg<W>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -164,8 +165,9 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         }
         cl.sync();                                    // the peer's reads of this stage are done
     };
-    // Before the selection is waited for: barriers, TMEM and the query tile
-    // (the query is an input; the kernels before this one do not write it).
+    // Before the selection is waited for: barriers, TMEM, and -- when the
+    // previous kernel is this library's selection, launched after the caller's
+    // kernels completed -- the query tile.
     if (threadIdx.x < kHeads) m_fin[threadIdx.x] = -INFINITY;   // the running maxima
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -186,11 +188,14 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    if (threadIdx.x == 0) {
-        prefetch_tensormap(&tm_q);
+    auto load_query = [&]() {
         mbar_arrive_expect_tx(q_full, C::kCB * kQBlock);
         for (int cb = 0; cb < C::kCB; ++cb)
             tma_load_2d(smem + C::kOffQ + cb * kQBlock, &tm_q, q_full, 64 * cb, (int32_t)(q * kHeads));
+    };
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tm_q);
+        if (q_early) load_query();
     }
     // A CTA leaving before its pipeline runs: the query tile must have landed
     // and TMEM goes back.
@@ -205,6 +210,13 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     };
     pdl_wait();                                       // the selection must be complete
     pdl_trigger();
+    if (threadIdx.x == 0 && !q_early) load_query();
+    // Selected row j of the query: idx[q][j], or row j itself when there is
+    // no selection (dense: every visible row).
+    const bool dense = idx == nullptr;
+    auto sel_row = [&](int64_t j) -> int32_t {
+        return dense ? (int32_t)j : idx[q * idx_width + j];
+    };
     // Row gather slots: every thread but the MMA warp's copies rows -- eight
     // threads per row (one 16-byte piece of each 64-column block's 128-byte
     // line), kIssuers / 8 rows at a time: slot s takes rows s / 8 and, where
@@ -217,16 +229,17 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     // thread's indices of the first tile (whatever the count; unused past it)
     // and the batch arrays.
     const int64_t j0 = (int64_t)split * rows_per_split;
-    int64_t ns = n_sel[q];
-    int32_t ia = issuer && j0 + rs < idx_width ? idx[q * idx_width + j0 + rs] : 0;
-    int32_t ib = issuer && two_rows && j0 + rs + kRowSlots < idx_width
-                     ? idx[q * idx_width + j0 + rs + kRowSlots] : 0;
+    int64_t ns = dense ? 0 : n_sel[q];
+    int32_t ia = issuer && (dense || j0 + rs < idx_width) ? sel_row(j0 + rs) : 0;
+    int32_t ib = issuer && two_rows && (dense || j0 + rs + kRowSlots < idx_width)
+                     ? sel_row(j0 + rs + kRowSlots) : 0;
     QueryInfo qi;
     if (!query_info(b, q, qi, err, /*where=*/8)) {
         leave_early();
         return;
     }
-    ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
+    if (dense) ns = qi.L;
+    else ns = ns < 0 ? 0 : (ns > idx_width ? idx_width : ns);
     const int64_t j1 = j0 + rows_per_split < ns ? j0 + rows_per_split : ns;
     if (j0 >= j1) {
         if (pair) {                                   // no weight from this half
@@ -284,8 +297,8 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     // this thread's indices of tile t (read a tile ahead of their copies)
     auto fetch_rows = [&](int t, int32_t& ra, int32_t& rb) {
         const int64_t j = j0 + (int64_t)t * kTileRows + rs;
-        ra = j < j1 ? idx[q * idx_width + j] : 0;
-        rb = two_rows && j + kRowSlots < j1 ? idx[q * idx_width + j + kRowSlots] : 0;
+        ra = j < j1 ? sel_row(j) : 0;
+        rb = two_rows && j + kRowSlots < j1 ? sel_row(j + kRowSlots) : 0;
     };
     if (issuer) issue_rows(0, ia, ib);
 
@@ -312,7 +325,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             for (int ps = 0; ps < kPasses; ++ps) {
                 const int r = kRowsPerPass * ps + rsub;
                 const int64_t j = j0 + (int64_t)(t + 1) * kTileRows + r;
-                rr[ps] = r < kTileRows && j < j1 ? idx[q * idx_width + j] : 0;
+                rr[ps] = r < kTileRows && j < j1 ? sel_row(j) : 0;
             }
             ok = mbar_wait(&pv_done[(t + 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), kWaitNs);
             if (!ok) break;
@@ -435,7 +448,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         // the previous tile's work (-1: no row)
         auto row_index = [&](int t) -> int32_t {
             const int64_t jrow = j0 + (int64_t)t * kTileRows + row;
-            return (t < n_tiles && jrow < j1) ? idx[q * idx_width + jrow] : -1;
+            return (t < n_tiles && jrow < j1) ? sel_row(jrow) : -1;
         };
         // this thread's copies of tile 1 (its buffer is free from the start)
         if (n_tiles > 1) {
@@ -728,7 +741,7 @@ template <int W>
 cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, const void* cache,
                      const int32_t* idx, const int32_t* n_sel, float* out, float* lse,
                      float* part_o, float* part_ml, int32_t rps, int32_t n_split, int32_t* err,
-                     cudaStream_t st) {
+                     bool q_early, cudaStream_t st) {
     using C = Cfg<W>;
     CUtensorMap tm_q;
     if (!make_map(&tm_q, q_abs, (uint64_t)b.n_q * kHeads, W, kHeads)) return cudaErrorInvalidValue;
@@ -740,7 +753,7 @@ cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, cons
     if (!pair) {
         e = launch_pdl(kern, dim3((unsigned)n_split, (unsigned)b.n_q), dim3(kThreads), C::kSmemBytes,
                        st, tm_q, cache, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split,
-                       pair, out, lse, part_o, part_ml, err);
+                       pair, (int32_t)q_early, out, lse, part_o, part_ml, err);
         if (e != cudaSuccess || n_split == 1) return e;
         return launch_merge_splits(b.n_q, n_split, part_o, part_ml, out, lse, st);
     }
@@ -760,8 +773,8 @@ cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, cons
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tm_q, cache, b, sh.scale, idx, n_sel,
-                              sh.index_row_width(), rps, n_split, pair, out, lse, part_o, part_ml,
-                              err);
+                              sh.index_row_width(), rps, n_split, pair, (int32_t)q_early, out, lse,
+                              part_o, part_ml, err);
 }
 
 }  // namespace
@@ -779,13 +792,12 @@ bool sparse_mla_tc_eligible(const Shape& sh, const BatchDev& b) {
 // decode queries: 2 splits, 128 CTAs, measured faster than 4 or 5 over two or
 // three waves).  Splits keep two tiles each, except for a lone query, whose
 // latency wants every split it can get.
-void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
-                              int32_t* rows_per_split, int32_t* n_split) {
-    int64_t max_rows = sh.index_row_width();
-    if (max_kv_len < max_rows) max_rows = max_kv_len;
+void plan_attention_splits_tc(int32_t n_q, int64_t max_rows, int32_t* rows_per_split,
+                              int32_t* n_split) {
     if (max_rows < 1) max_rows = 1;
     const int64_t tiles = (max_rows + kTileRows - 1) / kTileRows;
-    int64_t splits = n_q <= 152 ? 152 / n_q : 1;
+    const int64_t sms = sm_count();
+    int64_t splits = n_q <= sms ? sms / n_q : 1;
     const int64_t max_splits = (n_q == 1 || tiles < 2) ? tiles : tiles / 2;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
@@ -798,12 +810,13 @@ void plan_attention_splits_tc(const Shape& sh, int32_t n_q, int64_t max_kv_len,
 cudaError_t launch_sparse_mla_tc(const Shape& sh, const BatchDev& b, const void* q_abs,
                                  const void* cache, const int32_t* idx, const int32_t* n_sel,
                                  float* out, float* lse, float* part_o, float* part_ml,
-                                 int32_t rps, int32_t n_split, int32_t* err, cudaStream_t st) {
+                                 int32_t rps, int32_t n_split, int32_t* err, bool q_early,
+                                 cudaStream_t st) {
     if (sh.width() == 576)
         return launch_w<576>(sh, b, q_abs, cache, idx, n_sel, out, lse, part_o, part_ml, rps,
-                             n_split, err, st);
+                             n_split, err, q_early, st);
     return launch_w<512>(sh, b, q_abs, cache, idx, n_sel, out, lse, part_o, part_ml, rps, n_split,
-                         err, st);
+                         err, q_early, st);
 }
 
 }  // namespace dsa

@@ -445,7 +445,7 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
 // Two CTAs per query when that still fits one wave and the rows are long
 // enough for the halves to pay for the exchange.
 bool topk_pair_eligible(const Shape& sh, const BatchDev& b) {
-    return b.n_q >= 1 && 2 * (int64_t)b.n_q <= 152 && b.max_kv_len / sh.kpool >= 16384;
+    return b.n_q >= 1 && 2 * (int64_t)b.n_q <= sm_count() && b.max_kv_len / sh.kpool >= 16384;
 }
 
 cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* scores,

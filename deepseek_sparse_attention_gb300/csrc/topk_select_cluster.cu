@@ -351,7 +351,7 @@ topk_select_cluster(BatchDev b, int32_t top_k, int32_t kpool, const float* __res
 
 bool topk_cluster_eligible(const Shape& sh, const BatchDev& b) {
     const int64_t n_max = b.max_kv_len / sh.kpool;
-    return b.n_q >= 1 && b.n_q * kCtas <= 2 * 152 && n_max >= 32768 &&
+    return b.n_q >= 1 && b.n_q * kCtas <= 2 * sm_count() && n_max >= 32768 &&
            n_max <= (int64_t)kCtas * kMaxSlice;
 }
 

@@ -68,7 +68,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 typedef enum {
     DSA_OK = 0,
@@ -98,6 +98,31 @@ typedef struct {
     int32_t dtype;             /* a dsa_dtype                                     */
 } dsa_shape;
 
+/* Options of a call, in dsa_batch.flags (0 = the defaults; an unknown bit is
+ * DSA_ERR_INVALID_ARG):
+ *   DSA_FLAG_TWO_LAUNCH  steps 1 and 2 as two launches (the indexer, then the
+ *                        selection) even where one cooperative launch would
+ *                        run them; the results are the same.
+ *   DSA_FLAG_DESC_ORDER  selections in descending score order instead of
+ *                        ascending row order ("Add GLM-5.3-Flash support", DSA
+ *                        verification: the descending-score order of a selection
+ *                        list is a promise of its own): by (score descending,
+ *                        index ascending); in k-pool mode by pool, each pool's
+ *                        rows together in ascending order, the unfilled tail
+ *                        last.  Same set, same count; dense selections too.
+ *                        Implies the two-launch plan.  top_k / kpool <= 16384.
+ *   DSA_FLAG_DENSE       the indexer's A/B switch ("GLM-5.x (glm-dsa,
+ *                        glm5next)", environment knobs: top-k 0 attends densely
+ *                        even past the indexer's top-k): attention over every
+ *                        visible row of each query, no scoring or selection.
+ *                        dsa_decode_step then ignores q_idx, w and k_idx (may be
+ *                        NULL) and takes idx_out = n_sel_out = NULL;
+ *                        dsa_sparse_mla_attn ignores idx and n_sel;
+ *                        dsa_topk_select and dsa_index_select refuse it. */
+#define DSA_FLAG_TWO_LAUNCH 0x1u
+#define DSA_FLAG_DESC_ORDER 0x2u
+#define DSA_FLAG_DENSE 0x4u
+
 /* Batch description.  The three offset arrays are DEVICE arrays of n_seq+1
  * non-decreasing int64 values starting at 0; the host scalars must bound them
  * (they size grids and tensor maps, and the kernels check the offsets against
@@ -106,7 +131,7 @@ typedef struct {
     int32_t n_seq;             /* sequences                                        */
     int32_t n_q;               /* queries in total, = q_off[n_seq]                 */
     int32_t max_q_len;         /* host bound: max_s q_len_s                        */
-    int32_t reserved;          /* must be 0                                        */
+    uint32_t flags;            /* DSA_FLAG_* options of the call (0: defaults)     */
     int64_t max_kv_len;        /* host bound: max_s kv_len_s (< 2^31)              */
     int64_t total_rows;        /* rows of `cache` (bounds row_off[n_seq])          */
     int64_t total_keys;        /* rows of `k_idx` (bounds key_off[n_seq])          */
@@ -148,8 +173,8 @@ dsa_status dsa_plan(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
                     dsa_plan_info *info);
 
 /* Zeroes the start of the workspace on `stream`: the 256-byte header (device
- * error word, grid barrier) and the decode step's selection state that
- * follows it (DSA_WS_ZERO_BYTES in all, or the whole of a smaller workspace).
+ * error word, grid barrier, wait budget) and the decode step's selection state
+ * that follows it (DSA_WS_ZERO_BYTES in all, or the whole of a smaller workspace).
  * Call once on a freshly allocated workspace that was not allocated
  * zero-filled; after that every completed call leaves this region as it must
  * be, and dsa_check_device_error() re-zeroes it when a kernel reported an
@@ -244,7 +269,9 @@ dsa_status dsa_index_prepare(const dsa_shape *shape, int64_t n_vec, const float 
  *     z_i[c] = gate(kpool*j + i)[c] + pos[i][c]            (i < kpool)
  *     pool_keys[key_off[s] + j][c] = sum_i softmax_i(z[c]) * key(kpool*j + i)[c]
  * computed in float32 and rounded to dtype; no other pool key is written and no
- * other cell is read.  A decode step (q_len 1) writes a key exactly when its
+ * other cell is read.  A gate of -inf masks its slot (weight 0), and a channel
+ * whose slots are all masked gets 0; gates are otherwise finite (+inf and NaN
+ * give NaN).  A decode step (q_len 1) writes a key exactly when its
  * token completes a pool; a chunk writes the pools it completes; q_len_s =
  * kv_len_s writes them all.  The batch's queries are only the new tokens here:
  * n_q = q_off[n_seq] (not limited to 65535 for this entry point), max_q_len
@@ -267,7 +294,9 @@ dsa_status dsa_pool_compress(const dsa_shape *shape, const dsa_batch *batch, con
  *   out [n_q, heads, kv_lora] float32: o = sum_j softmax_j(z)_j * latent_j with
  *       z_j = scale * (q_abs . row_j) over the full row width
  *   lse [n_q, heads] float32 or NULL: log sum_j exp(z_j).
- * A query with n_sel == 0 gets out = 0 and lse = -inf. */
+ * A query with n_sel == 0 gets out = 0 and lse = -inf.  With DSA_FLAG_DENSE
+ * every visible row 0..L-1 is attended over and idx / n_sel are not read.
+ * `lse` may be unaligned only to 4 bytes. */
 dsa_status dsa_sparse_mla_attn(const dsa_shape *shape, const dsa_batch *batch, const void *q_abs,
                                const void *cache, const int32_t *idx, const int32_t *n_sel,
                                float *out, float *lse, void *ws, size_t ws_bytes, void *stream);
@@ -282,9 +311,12 @@ dsa_status dsa_sparse_mla_attn(const dsa_shape *shape, const dsa_batch *batch, c
  * candidate counters that each launch leaves as it found them): the workspace must have been zeroed once
  * (dsa_workspace_init, or allocated zero-filled), and two calls sharing one
  * workspace must not run concurrently.  The launch needs every CTA resident at
- * once; DSA_ERR_CUDA is returned if the device cannot give it that.
- * DSA_FUSED_SELECT=0 in the environment selects the two-launch path instead
- * (the results are the same). */
+ * once; DSA_ERR_CUDA is returned if the device cannot give it that.  Its CTAs'
+ * waits on one another give up after the workspace's wait budget
+ * (dsa_workspace_set_wait_budget; 2 s by default), recording DSA_ERR_TIMEOUT.
+ * DSA_FLAG_TWO_LAUNCH selects the two-launch path (the results are the same);
+ * DSA_FLAG_DESC_ORDER orders idx_out by score; DSA_FLAG_DENSE attends over
+ * every visible row (see the flags above). */
 dsa_status dsa_decode_step(const dsa_shape *shape, const dsa_batch *batch, const void *q_idx,
                            const float *w, const void *k_idx, const void *q_abs,
                            const void *cache, float *out, float *lse, int32_t *idx_out,
@@ -303,13 +335,14 @@ dsa_status dsa_decode_step(const dsa_shape *shape, const dsa_batch *batch, const
  *   Returns DSA_ERR_UNSUPPORTED when the step needs more scratch than the
  *   array holds (dsa_workspace_size(DSA_OP_DECODE_STEP) > the limit; a batch-1
  *   decode at 131072 tokens needs under 6 MiB).
+ *   Every argument is checked before anything is enqueued.
  *   The first call on a device looks up the array's device address (with that
  *   device current) and caches it; make that first call before any stream
  *   capture.  All calls share the array and it keeps the previous call's
  *   contents; each call zeroes its first DSA_WS_ZERO_BYTES on `stream` first.  Calls whose
  *   work overlaps on the GPU (other streams, other threads) race on the array:
- *   serialise them.  Device-side checks record into the array's error word,
- *   which is not reported back; use dsa_decode_step to read it. */
+ *   serialise them.  Device-side checks record into the array's error word:
+ *   dsa_check_device_error(NULL, 0, stream, &code) reads and clears it. */
 #define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)
 dsa_status dsa_decode_step_noalloc(const dsa_shape *shape, const dsa_batch *batch,
                                    const void *q_idx, const float *w, const void *k_idx,
@@ -319,8 +352,20 @@ dsa_status dsa_decode_step_noalloc(const dsa_shape *shape, const dsa_batch *batc
 /* Synchronises `stream`, then reads and clears the workspace error word.
  * *code (may be NULL) receives the first device-side error recorded (0 if
  * none).  Returns DSA_OK, DSA_ERR_DEVICE / DSA_ERR_TIMEOUT when a kernel
- * reported one, or DSA_ERR_CUDA. */
+ * reported one, or DSA_ERR_CUDA.  After an error it re-zeroes the workspace's
+ * first DSA_WS_ZERO_BYTES (an interrupted launch may leave its selection state
+ * dirty).  ws == NULL reads the scratch array of dsa_decode_step_noalloc on the
+ * current device. */
 dsa_status dsa_check_device_error(void *ws, size_t ws_bytes, void *stream, int32_t *code);
+
+/* Sets the budget, in nanoseconds, of every wait of a CTA on other CTAs in the
+ * kernels that use this workspace (the fused decode launch's grid barriers);
+ * 0 restores the default of 2 s.  A wait that runs out records DSA_ERR_TIMEOUT
+ * in the error word and its kernel winds down: nothing waits forever.  The
+ * value lives in the workspace header, so dsa_workspace_init and the clearing
+ * after an error restore the default.  Enqueued on `stream` (a copy from host
+ * memory: not for use while the stream is being captured). */
+dsa_status dsa_workspace_set_wait_budget(void *ws, size_t ws_bytes, uint64_t ns, void *stream);
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,10 @@ def _load():
             lib.oracle_index_prepare.argtypes = [P, P, i64, i32, i32, f64, P]
             lib.oracle_absorb_q.argtypes = [P, P, i32, i32, i32, i32, P]
             lib.oracle_up_project.argtypes = [P, P, i32, i32, i32, P]
+            lib.oracle_order_desc.argtypes = [P, i64, P, i64, i64, i32, P]
+            lib.oracle_order_desc.restype = ctypes.c_int
+            lib.oracle_set_threads.argtypes = [i32]
+            lib.oracle_set_threads.restype = ctypes.c_int
             for fn in (lib.oracle_index_scores, lib.oracle_topk, lib.oracle_kpool_select,
                        lib.oracle_sparse_mla, lib.oracle_dense_masked_mla,
                        lib.oracle_decode_step, lib.oracle_pool_compress, lib.oracle_new_pools,
@@ -89,11 +93,13 @@ def _check(rc: int, name: str):
 
 
 def threads() -> int:
-    """Number of OpenMP threads the oracle will use (OMP_NUM_THREADS or all cores)."""
-    env = os.environ.get("OMP_NUM_THREADS")
-    if env:
-        return int(env)
-    return os.cpu_count() or 1
+    """Number of OpenMP threads the oracle's parallel loops use."""
+    return int(_load().oracle_set_threads(0))
+
+
+def set_threads(n: int) -> int:
+    """Use n threads from now on (n > 0); returns the number in effect."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 def index_scores(q, w, keys) -> np.ndarray:
@@ -126,6 +132,18 @@ def kpool_select(pool_scores, L: int, k: int, kpool: int) -> np.ndarray:
     _check(_load().oracle_kpool_select(_ptr(s) if s.size else None, L, k, kpool, _ptr(idx),
                                        ctypes.byref(n_sel)), "oracle_kpool_select")
     return idx[: n_sel.value].copy()
+
+
+def order_desc(unit_scores, sel, L: int, kpool: int) -> np.ndarray:
+    """The selection `sel` (ascending, as the select functions emit it) with its
+    units sorted by score descending, ties by ascending unit, the tail last."""
+    s = np.ascontiguousarray(unit_scores, dtype=np.float64)
+    sel = np.ascontiguousarray(sel, dtype=np.int32)
+    out = np.empty(max(sel.shape[0], 1), dtype=np.int32)
+    _check(_load().oracle_order_desc(_ptr(s) if s.size else None, s.shape[0],
+                                     _ptr(sel) if sel.size else None, sel.shape[0], L, kpool,
+                                     _ptr(out)), "oracle_order_desc")
+    return out[: sel.shape[0]].copy()
 
 
 def sparse_mla(q_abs, rows, idx, scale: float, dv: int):

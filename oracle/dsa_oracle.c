@@ -12,8 +12,14 @@
 #include "dsa_oracle.h"
 
 #include <math.h>
+#include <omp.h>
 #include <stdlib.h>
 #include <string.h>
+
+int oracle_set_threads(int32_t n) {
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+}
 
 int oracle_index_scores(const float *q, const float *w, const float *keys,
                         int64_t n_keys, int32_t heads, int32_t dim, double *scores)
@@ -131,6 +137,41 @@ static double dot_row(const float *q, const float *r, int32_t width)
     return a;
 }
 
+/* (score, unit) pairs for the descending sort: larger score first, then the
+ * smaller unit. */
+typedef struct { double s; int64_t u; } unit_key;
+
+static int cmp_desc(const void *pa, const void *pb)
+{
+    const unit_key *a = (const unit_key *)pa, *b = (const unit_key *)pb;
+    if (a->s != b->s) return a->s > b->s ? -1 : 1;
+    return (a->u > b->u) - (a->u < b->u);
+}
+
+int oracle_order_desc(const double *unit_scores, int64_t n_units, const int32_t *sel,
+                      int64_t n_sel, int64_t L, int32_t kpool, int32_t *out)
+{
+    if (n_sel < 0 || kpool <= 0 || L < 0 || n_units < 0) return -1;
+    if (n_sel > 0 && (!sel || !out || !unit_scores)) return -1;
+    const int64_t tail = kpool > 1 ? L % kpool : 0;       /* rows of the unfilled pool */
+    if (n_sel < tail || (n_sel - tail) % kpool != 0) return -1;
+    const int64_t n = (n_sel - tail) / kpool;               /* selected units */
+    unit_key *k = (unit_key *)malloc((size_t)(n > 0 ? n : 1) * sizeof(unit_key));
+    if (!k) return -1;
+    for (int64_t i = 0; i < n; i++) {
+        const int64_t u = sel[i * kpool] / kpool;           /* the unit's first row / kpool */
+        if (u < 0 || u >= n_units) { free(k); return -1; }
+        k[i].s = unit_scores[u];
+        k[i].u = u;
+    }
+    qsort(k, (size_t)n, sizeof(unit_key), cmp_desc);
+    for (int64_t i = 0; i < n; i++)
+        for (int32_t r = 0; r < kpool; r++) out[i * kpool + r] = (int32_t)(k[i].u * kpool + r);
+    for (int64_t i = n * kpool; i < n_sel; i++) out[i] = sel[i];   /* the tail, as it was */
+    free(k);
+    return 0;
+}
+
 int oracle_sparse_mla(const float *q_abs, const float *rows, int64_t n_rows, int32_t heads,
                       int32_t width, int32_t dv, double scale, const int32_t *idx,
                       int64_t n_sel, double *out, double *lse)
@@ -220,7 +261,13 @@ int oracle_pool_compress(const float *cells, int64_t n_pools, const float *pos, 
                 const double z = (double)pool[i * cell_w + dim + c] + (double)pos[(int64_t)i * dim + c];
                 if (z > zmax) zmax = z;
             }
-            /* softmax over the slots (max-subtracted), weighted sum of the keys */
+            /* every slot masked (logit -inf): no weight anywhere, the key is 0 */
+            if (zmax == -INFINITY) {
+                out[p * dim + c] = 0.0;
+                continue;
+            }
+            /* softmax over the slots (max-subtracted), weighted sum of the keys;
+             * a masked slot has weight exp(-inf) = 0 */
             double den = 0.0, num = 0.0;
             for (int32_t i = 0; i < kpool; i++) {
                 const double z = (double)pool[i * cell_w + dim + c] + (double)pos[(int64_t)i * dim + c];

@@ -35,6 +35,10 @@
 extern "C" {
 #endif
 
+/* Threads the parallel loops below use: sets them to n when n > 0, and
+ * returns the number in effect (timing support; no arithmetic). */
+int oracle_set_threads(int32_t n);
+
 /* Lightning-indexer score of n_keys keys against one query.
  *   q      [heads * dim]   indexer query, head-major
  *   w      [heads]         per-head weights
@@ -67,6 +71,21 @@ int oracle_topk(const double *scores, int64_t n, int64_t k, int32_t *idx, int64_
  * kpool == 1 is token mode and equals oracle_topk. */
 int oracle_kpool_select(const double *pool_scores, int64_t L, int64_t k, int32_t kpool,
                         int32_t *idx, int64_t *n_sel);
+
+/* A selection put in descending score order ([STRATA] "DSA verification":
+ * the descending-score order of a selection list is a promise of its own).
+ *   unit_scores [n_units]  the query's scores: one per token (kpool == 1) or
+ *                          per pool
+ *   sel [n_sel]            a selection as oracle_kpool_select emits it
+ *                          (ascending; in k-pool mode whole pools, then the
+ *                          L mod kpool tail rows)
+ *   out [n_sel]            out: the same rows with the units (tokens, or
+ *                          pools with their kpool rows in ascending order)
+ *                          sorted by score descending, ties by ascending unit
+ *                          (the selection's own tie rule), the tail last in
+ *                          ascending order. */
+int oracle_order_desc(const double *unit_scores, int64_t n_units, const int32_t *sel,
+                      int64_t n_sel, int64_t L, int32_t kpool, int32_t *out);
 
 /* Absorbed-MLA attention of one query over the selected cache rows.
  *   q_abs [heads * width]     absorbed query (latent part then rope part)
@@ -115,6 +134,8 @@ int oracle_decode_step(const float *q_idx, const float *w, const float *keys,
  *     z_i = gate_i[c] + pos[i][c]  (i < kpool: the pool's cells in order)
  *     a_i = exp(z_i) / sum_j exp(z_j)          softmax over the slots
  *     out[p][c] = sum_i a_i * key_i[c]
+ * A logit of -inf masks its slot (weight 0); a channel whose slots are all
+ * masked gets 0 (an empty weighted sum).  Gates are otherwise finite.
  * Readings (the pages name the parts, not the formula): the gate has the key's
  * width and there is one softmax per key dimension -- [STRATA] "Tests" lists
  * one softmax over the whole pool block instead of per key-dim as a rival

@@ -7,13 +7,20 @@ Acceptance bars:
 * selections: bit-exact against the oracle's, except candidates whose oracle
   score lies within 1e-5 relative of the oracle's k-th score (near-ties the
   GPU's float32 accumulation order may legitimately swap);
-* attention outputs: |gpu - oracle| <= 2e-3 + 1e-2 |oracle| element-wise for
-  bf16 inputs with float32 accumulation; float32 inputs use 1e-4 + 1e-3 |oracle|;
+* attention outputs, for bf16 inputs with float32 accumulation: both the
+  maximum absolute error max|gpu - oracle| <= 2e-3 over every element, and the
+  relative error max|gpu - oracle| / max|oracle| <= 1e-2 (the maximum error
+  relative to the output's scale: an element-wise ratio is undefined where the
+  output crosses zero); float32 inputs 1e-4 and 1e-3.  The log-sum-exp takes
+  the same two bounds.  Every check records its achieved errors (printed at the
+  end of the run by conftest.py);
 * indexer scores: |gpu - oracle| <= 1e-5 * M_t + 1e-6, with M_t = sum_h |w_h|
   sum_i |q_hi k_ti| the magnitude bound of the sum (float32 accumulation of
   128-term dots, then 32 weighted terms, rounds to well under 1e-5 of M_t).
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import torch
@@ -23,6 +30,9 @@ import oracle
 
 ATT_TOL = {"bf16": (2e-3, 1e-2), "f32": (1e-4, 1e-3)}
 NEAR_TIE_REL = 1e-5
+
+# (test id, dtype, max-abs error, relative error) of every attention check
+ACHIEVED = []
 
 
 def host_f32(t: torch.Tensor) -> np.ndarray:
@@ -46,9 +56,9 @@ def gpu_shape(wl):
                           wl.kpool, wl.scale, wl.dtype)
 
 
-def gpu_batch(wl, d):
+def gpu_batch(wl, d, flags: int = 0):
     return dsa.make_batch(d["row_off"], d["key_off"], d["q_off"], wl.n_q, max(wl.q_lens),
-                          max(wl.kv_lens), sum(wl.kv_lens), sum(wl.key_counts()))
+                          max(wl.kv_lens), sum(wl.kv_lens), sum(wl.key_counts()), flags)
 
 
 def query_slices(wl, d, q):
@@ -109,14 +119,28 @@ def check_selection(gpu_idx: np.ndarray, r: dict, top_k: int, kpool: int):
     return len(units)
 
 
+def _errors(got: np.ndarray, ref: np.ndarray):
+    """(max |got - ref|, that over max |ref|) in float64; -inf == -inf counts as 0."""
+    g, r = got.astype(np.float64), np.asarray(ref, dtype=np.float64)
+    same = (g == r)                                   # equal infinities included
+    err = np.where(same, 0.0, np.abs(g - r))
+    scale = np.abs(r[np.isfinite(r)]).max() if np.isfinite(r).any() else 0.0
+    mx = float(err.max()) if err.size else 0.0
+    return mx, (mx / scale if scale > 0 else (0.0 if mx == 0 else float("inf")))
+
+
 def check_attention(out: np.ndarray, lse: np.ndarray, ref_out: np.ndarray, ref_lse: np.ndarray,
-                    dtype: str):
+                    dtype: str, label: str = None):
+    """Max-abs and relative error of the output (and lse) within the bars."""
     atol, rtol = ATT_TOL[dtype]
-    err = np.abs(out.astype(np.float64) - ref_out)
-    lim = atol + rtol * np.abs(ref_out)
     assert np.all(np.isfinite(out)), "non-finite output"
-    assert np.all(err <= lim), f"max abs err {err.max():.3e} (limit {atol}+{rtol}|ref|)"
+    abs_e, rel_e = _errors(out, ref_out)
+    if label is None:
+        label = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    ACHIEVED.append((label, dtype, abs_e, rel_e))
+    assert abs_e <= atol, f"max abs err {abs_e:.3e} > {atol}"
+    assert rel_e <= rtol, f"relative err {rel_e:.3e} > {rtol} (max abs {abs_e:.3e})"
     if lse is not None:
-        e2 = np.abs(lse.astype(np.float64) - ref_lse)
-        assert np.all(e2 <= atol + rtol * np.abs(ref_lse)), f"lse err {e2.max():.3e}"
-    return float(err.max())
+        l_abs, l_rel = _errors(lse, ref_lse)
+        assert l_abs <= atol and l_rel <= rtol, f"lse err {l_abs:.3e} (rel {l_rel:.3e})"
+    return abs_e

@@ -43,14 +43,14 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_row_width(lib):
-    assert dsa.dsa_version() == 1
+    assert dsa.dsa_version() == 2
     assert dsa.dsa_index_row_width(dsa.make_shape(kpool=1)) == 2048
     assert dsa.dsa_index_row_width(dsa.make_shape(kpool=4)) == 2051
     assert dsa.dsa_index_row_width(dsa.make_shape(heads=32)) == -1   # unsupported geometry
 
 
-def _batch(n_seq=1, n_q=1, max_q=1, max_kv=4096):
-    b = dsa.Batch(n_seq, n_q, max_q, 0, max_kv, max_kv, max_kv, ctypes.c_void_p(16),
+def _batch(n_seq=1, n_q=1, max_q=1, max_kv=4096, flags=0):
+    b = dsa.Batch(n_seq, n_q, max_q, flags, max_kv, max_kv, max_kv, ctypes.c_void_p(16),
                   ctypes.c_void_p(16), ctypes.c_void_p(16))
     return b
 
@@ -131,7 +131,57 @@ def test_entry_points_reject_before_enqueue(lib):
                                    good, None, good, 1 << 20, None) == 2
     assert lib.dsa_decode_step(ctypes.byref(sh), ctypes.byref(b), good, good, good, good, good,
                                good, None, None, None, good, 16, None) == 3   # ws too small
-    assert lib.dsa_check_device_error(None, 0, None, None) == 3
+    # a NULL workspace reads the no-allocation scratch array: a CUDA call,
+    # which fails on a machine without a device
+    if not torch.cuda.is_available():
+        assert lib.dsa_check_device_error(None, 0, None, None) == 4
+    assert lib.dsa_check_device_error(P(256), 16, None, None) == 3   # smaller than the header
+
+
+def test_flags_validation(lib):
+    """Unknown flag bits are malformed; the dense switch leaves the selection
+    entry points nothing to do and takes no selection outputs in the step."""
+    P = ctypes.c_void_p
+    good = P(256)
+    sh = dsa.make_shape()
+    assert _size(sh, _batch(flags=0x8), dsa.OP_DECODE_STEP)[0] == 1
+    assert _size(sh, _batch(flags=0x7), dsa.OP_DECODE_STEP)[0] == 0
+    dense = _batch(flags=dsa.FLAG_DENSE)
+    assert lib.dsa_topk_select(ctypes.byref(sh), ctypes.byref(dense), good, 4096, good, good,
+                               good, 256, None) == 1
+    assert lib.dsa_index_select(ctypes.byref(sh), ctypes.byref(dense), good, good, good, good,
+                                good, good, 1 << 30, None) == 1
+    # the step with the dense switch: selection outputs must be NULL ...
+    assert lib.dsa_decode_step(ctypes.byref(sh), ctypes.byref(dense), None, None, None, good,
+                               good, good, None, good, None, good, 1 << 30, None) == 1
+    # ... and the indexer inputs may be (the workspace check comes next)
+    assert lib.dsa_decode_step(ctypes.byref(sh), ctypes.byref(dense), None, None, None, good,
+                               good, good, None, None, None, good, 16, None) == 3
+    # descending order sorts at most 16384 units per query
+    big_k = dsa.make_shape(top_k=32768)
+    assert _size(big_k, _batch(flags=dsa.FLAG_DESC_ORDER), dsa.OP_DECODE_STEP)[0] == 0
+    assert lib.dsa_topk_select(ctypes.byref(big_k), ctypes.byref(_batch(flags=dsa.FLAG_DESC_ORDER)),
+                               good, 4096, good, good, good, 256, None) == 2
+
+
+def test_noalloc_checks_everything_before_enqueue(lib):
+    """dsa_decode_step_noalloc validates its arguments before it clears its
+    scratch, and a batch without queries enqueues nothing (no device here: any
+    CUDA call would surface as DSA_ERR_CUDA)."""
+    P = ctypes.c_void_p
+    good = P(256)
+    sh = dsa.make_shape()
+    f = lib.dsa_decode_step_noalloc
+    b = _batch()
+    assert f(ctypes.byref(sh), ctypes.byref(b), good, good, good, good, good, P(260), None, None,
+             None, None) == 1                                    # misaligned output
+    assert f(ctypes.byref(sh), ctypes.byref(b), good, good, good, good, good, good, None, P(258),
+             None, None) == 1                                    # misaligned selection
+    assert f(ctypes.byref(sh), ctypes.byref(_batch(flags=0x10)), good, good, good, good, good,
+             good, None, None, None, None) == 1                  # unknown flag
+    empty = _batch(n_q=0, max_q=0)
+    assert f(ctypes.byref(sh), ctypes.byref(empty), None, None, None, None, None, None, None,
+             None, None, None) == 0
 
 
 def test_pool_compress_rejects_before_enqueue(lib):
@@ -194,6 +244,17 @@ def test_plan_of_the_benchmark_workloads(lib, name, launches, splits, rows_per_s
     assert plan == {"kernel_launches": launches, "attn_splits": splits,
                     "attn_rows_per_split": rows_per_split}
     assert splits * rows_per_split >= min(max(wl.kv_lens), dsa.dsa_index_row_width(sh))
+    # the two-launch plan adds the indexer's own launch where the fused one
+    # applied; descending order one more; the dense switch only attends
+    b.flags = dsa.FLAG_TWO_LAUNCH
+    two = dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP)["kernel_launches"]
+    b.flags = dsa.FLAG_DESC_ORDER
+    desc = dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP)["kernel_launches"]
+    assert desc == two + 1 and two >= launches
+    b.flags = dsa.FLAG_DENSE
+    dense = dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP)
+    assert dense["attn_splits"] * dense["attn_rows_per_split"] >= max(wl.kv_lens)
+    assert dense["kernel_launches"] == (2 if dense["attn_splits"] > 2 else 1)
 
 
 def test_python_binding_rejects_host_tensors(lib):

@@ -10,8 +10,6 @@ CTAs (duplicated keys; all-zero keys, whose candidates overflow the list
 and take the histogram levels; signed zeros), and reuse of one workspace
 across launches of different batches.
 """
-import os
-
 import numpy as np
 import pytest
 import torch
@@ -47,25 +45,9 @@ FUSED = [
 ]
 
 
-class fused_mode:
-    """DSA_FUSED_SELECT for the duration of a block (the library reads it per call)."""
-
-    def __init__(self, on: bool):
-        self.on = on
-
-    def __enter__(self):
-        self.old = os.environ.get("DSA_FUSED_SELECT")
-        os.environ["DSA_FUSED_SELECT"] = "1" if self.on else "0"
-
-    def __exit__(self, *exc):
-        if self.old is None:
-            os.environ.pop("DSA_FUSED_SELECT", None)
-        else:
-            os.environ["DSA_FUSED_SELECT"] = self.old
-
-
-def _step(wl, d, ws=None):
-    sh, b = gpu_shape(wl), gpu_batch(wl, d)
+def _step(wl, d, ws=None, flags=0):
+    """The whole step; flags=dsa.FLAG_TWO_LAUNCH takes the two-launch path."""
+    sh, b = gpu_shape(wl), gpu_batch(wl, d, flags)
     if ws is None:
         ws = dsa.alloc_workspace(sh, b, dsa.OP_DECODE_STEP)
     width = dsa.dsa_index_row_width(sh)
@@ -77,6 +59,9 @@ def _step(wl, d, ws=None):
                         idx, n_sel, ws)
     assert dsa.dsa_check_device_error(ws) == 0
     return out.cpu().numpy(), lse.cpu().numpy(), idx.cpu().numpy(), n_sel.cpu().numpy()
+
+
+TWO = dsa.FLAG_TWO_LAUNCH
 
 
 def _gpu_scores(wl, d):
@@ -109,10 +94,8 @@ def _check_exact(wl, host, d, idx, n_sel):
 
 
 def _assert_eligible(wl, d):
-    with fused_mode(True):
-        plan = dsa.dsa_plan(gpu_shape(wl), gpu_batch(wl, d), dsa.OP_DECODE_STEP)
-    with fused_mode(False):
-        plan2 = dsa.dsa_plan(gpu_shape(wl), gpu_batch(wl, d), dsa.OP_DECODE_STEP)
+    plan = dsa.dsa_plan(gpu_shape(wl), gpu_batch(wl, d), dsa.OP_DECODE_STEP)
+    plan2 = dsa.dsa_plan(gpu_shape(wl), gpu_batch(wl, d, TWO), dsa.OP_DECODE_STEP)
     assert plan["kernel_launches"] < plan2["kernel_launches"], "fused path not taken"
 
 
@@ -121,11 +104,9 @@ def test_fused_selection_is_exact_and_matches_two_launch_path(wl):
     host = workloads.make(wl, "cpu")
     d = to_device(host)
     _assert_eligible(wl, d)
-    with fused_mode(True):
-        out, lse, idx, n_sel = _step(wl, d)
+    out, lse, idx, n_sel = _step(wl, d)
     _check_exact(wl, host, d, idx, n_sel)
-    with fused_mode(False):
-        out2, lse2, idx2, n_sel2 = _step(wl, d)
+    out2, lse2, idx2, n_sel2 = _step(wl, d, flags=TWO)
     assert np.array_equal(idx, idx2) and np.array_equal(n_sel, n_sel2)
     # same selection, same attention kernels: identical outputs
     assert np.array_equal(out, out2, equal_nan=False)
@@ -159,11 +140,9 @@ def test_fused_ties_across_ctas(kind):
     wl, host = _tie_inputs(kind)
     d = to_device(host)
     _assert_eligible(wl, d)
-    with fused_mode(True):
-        _, _, idx, n_sel = _step(wl, d)
+    _, _, idx, n_sel = _step(wl, d)
     _check_exact(wl, host, d, idx, n_sel)
-    with fused_mode(False):
-        _, _, idx2, n_sel2 = _step(wl, d)
+    _, _, idx2, n_sel2 = _step(wl, d, flags=TWO)
     assert np.array_equal(idx, idx2) and np.array_equal(n_sel, n_sel2)
     if kind == "zero_keys":
         # every score ties: the lowest indices win
@@ -179,17 +158,16 @@ def test_fused_workspace_reuse_across_batches():
     wb = workloads.small("reuse_b", [9000, 70000, 3000], top_k=512, seed=22)
     ha, hb = workloads.make(wa, "cpu"), workloads.make(wb, "cpu")
     da, db = to_device(ha), to_device(hb)
-    with fused_mode(True):
-        wsa = dsa.alloc_workspace(gpu_shape(wa), gpu_batch(wa, da), dsa.OP_DECODE_STEP)
-        wsb = dsa.alloc_workspace(gpu_shape(wb), gpu_batch(wb, db), dsa.OP_DECODE_STEP)
-        ws = wsa if wsa.numel() >= wsb.numel() else wsb
-        fresh_a = _step(wa, da)
-        fresh_b = _step(wb, db)
-        for _ in range(3):
-            for wl, d, fresh in ((wa, da, fresh_a), (wb, db, fresh_b)):
-                got = _step(wl, d, ws)
-                for x, y in zip(got, fresh):
-                    assert np.array_equal(x, y)
+    wsa = dsa.alloc_workspace(gpu_shape(wa), gpu_batch(wa, da), dsa.OP_DECODE_STEP)
+    wsb = dsa.alloc_workspace(gpu_shape(wb), gpu_batch(wb, db), dsa.OP_DECODE_STEP)
+    ws = wsa if wsa.numel() >= wsb.numel() else wsb
+    fresh_a = _step(wa, da)
+    fresh_b = _step(wb, db)
+    for _ in range(3):
+        for wl, d, fresh in ((wa, da, fresh_a), (wb, db, fresh_b)):
+            got = _step(wl, d, ws)
+            for x, y in zip(got, fresh):
+                assert np.array_equal(x, y)
 
 
 @pytest.mark.parametrize("wl", [FUSED[0], FUSED[2],
@@ -211,3 +189,35 @@ def test_index_select_entry_matches_decode_step(wl):
         assert dsa.dsa_check_device_error(ws) == 0
         assert np.array_equal(idx.cpu().numpy(), idx_ref)
         assert np.array_equal(n_sel.cpu().numpy(), n_ref)
+
+
+def test_wait_budget_runs_out_and_the_workspace_recovers():
+    """The fused launch's CTAs wait on one another at grid barriers, each wait
+    bounded by the workspace's budget.  With a budget of 1 ns the waits give up
+    (a CTA reaching a barrier before the last one arrives records a timeout and
+    returns): the call still completes, dsa_check_device_error reports
+    DSA_ERR_TIMEOUT and re-zeroes the selection state, and the next call on the
+    same workspace, at the default budget, is exact.  No wait is unbounded, so
+    nothing hangs."""
+    wl = FUSED[0]
+    host = workloads.make(wl, "cpu")
+    d = to_device(host)
+    _assert_eligible(wl, d)
+    sh, b = gpu_shape(wl), gpu_batch(wl, d)
+    ref = _step(wl, d)
+    ws = dsa.alloc_workspace(sh, b, dsa.OP_DECODE_STEP)
+    width = dsa.dsa_index_row_width(sh)
+    idx = torch.empty((wl.n_q, width), dtype=torch.int32, device="cuda")
+    n_sel = torch.empty((wl.n_q,), dtype=torch.int32, device="cuda")
+    codes = []
+    for _ in range(5):              # the CTAs' arrivals spread over microseconds
+        dsa.dsa_workspace_set_wait_budget(ws, 1)
+        dsa.dsa_index_select(sh, b, d["q_idx"], d["w"], d["k_idx"], idx, n_sel, ws)
+        codes.append(dsa.dsa_check_device_error(ws))
+        if codes[-1] != 0:
+            break
+    assert codes[-1] == 3, f"no wait ran out: {codes}"          # a bounded wait gave up
+    for _ in range(2):
+        got = _step(wl, d, ws)
+        for x, y in zip(got, ref):
+            assert np.array_equal(x, y)

@@ -105,6 +105,28 @@ def test_pool_compress_matches_oracle(dtype, case, kpool):
         k0 += n_keys
 
 
+@pytest.mark.parametrize("kpool", [4, 2])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_masked_gates_match_oracle(dtype, kpool):
+    """Gates of -inf (masked slots), in some channels every slot of a pool:
+    the masked slots weigh 0 and an all-masked channel gives 0, as the oracle."""
+    L = 64 * kpool
+    cells, pos = _inputs(L, dtype, seed=9, kpool=kpool)
+    c = cells.float()
+    g = torch.Generator().manual_seed(10)
+    mask = torch.rand(L, DIM, generator=g) < 0.4
+    c[:, DIM:][mask] = float("-inf")
+    c[: kpool * 8, DIM + 3] = float("-inf")              # channel 3 of the first 8 pools
+    cells = c.to(cells.dtype)
+    pool_keys = torch.full((L // kpool, DIM), SENTINEL, dtype=cells.dtype, device="cuda")
+    assert _compress([L], [L], cells.cuda(), pos.cuda(), pool_keys, dtype, kpool) == 0
+    got = host_f32(pool_keys)
+    pools = host_f32(cells).reshape(L // kpool, kpool, 2 * DIM)
+    ref = oracle.pool_compress(pools, host_f32(pos))
+    assert np.all(np.isfinite(got)) and np.all(got[:8, 3] == 0.0)
+    _check_pools(got, ref, np.abs(pools[:, :, :DIM]).max(axis=1), dtype)
+
+
 def test_incremental_decode_equals_one_bulk_call():
     """A prompt of 4093 tokens, then seven decode steps (4094 .. 4100 tokens):
     the pool keys made one step at a time equal, bit for bit, those of one call

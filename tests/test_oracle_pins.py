@@ -375,6 +375,21 @@ def test_pool_compress_position_embedding_weights_the_slots():
     assert np.all(out[0, 3:] == 0.0)
 
 
+def test_pool_compress_masked_slots_weigh_nothing():
+    """A gate of -inf masks its slot: the key is the softmax over the other
+    slots alone (equal gates: their mean), and a channel with every slot masked
+    is 0 -- never NaN, which would sort above every score in the selection."""
+    keys = np.zeros((1, 4, 128), np.float32)
+    keys[0, :, :] = np.array([1.0, 2.0, 4.0, 8.0], np.float32)[:, None]
+    gates = np.zeros((1, 4, 128), np.float32)
+    gates[0, 0, :] = -np.inf                            # slot 0 masked everywhere
+    gates[0, :, 7] = -np.inf                            # channel 7: every slot masked
+    out = oracle.pool_compress(_cells(keys, gates), np.zeros((4, 128), np.float32))
+    assert np.all(np.isfinite(out))
+    np.testing.assert_allclose(np.delete(out[0], 7), (2 + 4 + 8) / 3.0, rtol=1e-15)
+    assert out[0, 7] == 0.0
+
+
 def test_pool_compress_dominant_gate_selects_its_key():
     rng = np.random.default_rng(41)
     keys = rng.standard_normal((3, 4, 128)).astype(np.float32)
@@ -628,3 +643,61 @@ def test_oracle_rejects_bad_arguments():
                           np.array([0, 4]), 1.0, 8)        # index out of range
     with pytest.raises(ValueError):
         oracle.kpool_select(np.zeros(2), 8, 6, 4)          # top_k not a multiple of kpool
+
+
+# ------------------------------------------------------------ descending order
+
+def _order_by_repeated_max(scores, units):
+    """Brute force: repeatedly take the unit of largest score, the lowest unit
+    among equals (an O(n^2) scan, independent of any sort routine)."""
+    left = list(units)
+    out = []
+    while left:
+        best = left[0]
+        for u in left[1:]:
+            if scores[u] > scores[best] or (scores[u] == scores[best] and u < best):
+                best = u
+        out.append(best)
+        left.remove(best)
+    return out
+
+
+@pytest.mark.parametrize("kpool,L,k", [(1, 300, 64), (1, 50, 64), (4, 403, 64), (4, 130, 64),
+                                       (4, 2059, 2048), (1, 40, 8)])
+def test_order_desc_matches_brute_force(kpool, L, k):
+    rng = np.random.default_rng(L + kpool)
+    n_units = L // kpool
+    s = rng.integers(-3, 4, n_units).astype(np.float64)      # many ties
+    sel = oracle.kpool_select(s, L, k, kpool) if kpool > 1 else oracle.topk(s, k)
+    got = oracle.order_desc(s, sel, L, kpool)
+    tail = L % kpool if kpool > 1 else 0
+    units = [int(sel[i]) // kpool for i in range(0, len(sel) - tail, kpool)]
+    want = []
+    for u in _order_by_repeated_max(s, units):
+        want += [u * kpool + r for r in range(kpool)]
+    want += list(sel[len(sel) - tail:]) if tail else []
+    assert got.tolist() == want
+    assert sorted(got.tolist()) == sorted(sel.tolist())       # same set
+
+
+def test_order_desc_invariants_and_rivals():
+    """Scores never increase along the list; equal scores keep ascending units;
+    the tail comes last.  Rival readings (ties to the higher unit; the tail
+    first) give other lists."""
+    rng = np.random.default_rng(77)
+    L, kp = 4000 * 4 + 3, 4
+    s = rng.integers(0, 6, L // kp).astype(np.float64)
+    sel = oracle.kpool_select(s, L, 2048, kp)
+    got = oracle.order_desc(s, sel, L, kp)
+    body = got[:-3]
+    units = body[::kp] // kp
+    assert np.all(np.diff(s[units]) <= 0)
+    for a, b in zip(units[:-1], units[1:]):
+        if s[a] == s[b]:
+            assert a < b
+    for i in range(0, len(body), kp):                          # pools stay whole, ascending
+        assert np.array_equal(body[i:i + kp], body[i] + np.arange(kp))
+    assert np.array_equal(got[-3:], [L - 3, L - 2, L - 1])
+    higher_first = sorted(units.tolist(), key=lambda u: (-s[u], -u))
+    assert higher_first != units.tolist()
+    assert not np.array_equal(np.concatenate([got[-3:], got[:-3]]), got)
