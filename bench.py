@@ -425,7 +425,8 @@ def roofline_of(wl, fused, sel_ms, idx_ms, peaks, peak_src):
         dom = {"kernel": "index_select_fused", "ms": sel_ms,
                "bytes": work["index_launch_bytes"] + work["select_bytes"]}
     else:
-        dom = {"kernel": "index_scores_tc", "ms": idx_ms, "bytes": work["index_launch_bytes"]}
+        dom = {"kernel": "index_scores_tc" if wl.dtype == "bf16" else "index_scores (CUDA cores)",
+               "ms": idx_ms, "bytes": work["index_launch_bytes"]}
     # A prefill chunk re-reads each key tile for many queries: its indexer does
     # far more flops per byte than the GPU's flop/byte balance and is bound by
     # the tensor pipe, so its roofline is in TFLOP/s against the bf16 peak.
@@ -445,6 +446,71 @@ def roofline_of(wl, fused, sel_ms, idx_ms, peaks, peak_src):
     roof["traffic"] = kernel_traffic(dom["kernel"], wl.name)
     roof["launch_us"] = dom["ms"] * 1e3
     return roof
+
+
+def time_projections(dsa, wl, dev, stream, peaks, peak_src, n_rep=50):
+    """The query absorption and the output up-projection of the workload's
+    queries, each timed alone with CUDA events, the weights rotating over
+    copies larger than L2 (each layer of a model has its own).  Algorithmic
+    bytes: the weights, the inputs and the outputs once; flops 2 per
+    multiply-add."""
+    import torch
+    import workloads
+
+    nope, v_dim = 192, 256
+    esz = 2 if wl.dtype == "bf16" else 4
+    w_bytes = wl.heads * (nope + v_dim) * wl.kv_lora * esz
+    copies = min(16, max(2, math.ceil(2 * L2_BYTES / w_bytes)))
+    p = workloads.projections(wl, dev, nope=nope, v_dim=v_dim, copies=copies)
+    sh = dsa.make_shape(wl.idx_heads, wl.idx_dim, wl.heads, wl.kv_lora, wl.rope, wl.top_k,
+                        wl.kpool, wl.scale, wl.dtype)
+    zero = torch.zeros(2, dtype=torch.int64, device=dev)
+    ws = dsa.alloc_workspace(sh, dsa.make_batch(zero, zero, zero, 0, 0, 0, 1, 1),
+                             dsa.OP_PROJECT, dev)
+    q_abs = torch.empty((wl.n_q, wl.heads, wl.kv_lora + wl.rope), dtype=p["q_full"].dtype,
+                        device=dev)
+    out = torch.empty((wl.n_q, wl.heads, v_dim), device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    res = {}
+    for name in ("absorb_q", "up_project"):
+        def call(i):
+            if name == "absorb_q":
+                dsa.dsa_absorb_q(sh, p["q_full"], p["w_uk_copies"][i % copies], q_abs, ws, stream)
+            else:
+                dsa.dsa_up_project(sh, p["o"], p["w_uv_copies"][i % copies], out, ws, stream)
+        for i in range(3):
+            call(i)
+        e0.record(stream)
+        for i in range(n_rep):
+            call(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if dsa.dsa_check_device_error(ws, stream) != 0:
+            raise RuntimeError(f"device error in the {name} loop")
+        ms = e0.elapsed_time(e1) / n_rep
+        if name == "absorb_q":
+            byts = (wl.heads * nope * wl.kv_lora * esz + p["q_full"].numel() * esz
+                    + q_abs.numel() * esz)
+            flops = 2 * wl.n_q * wl.heads * nope * wl.kv_lora
+        else:
+            byts = wl.heads * v_dim * wl.kv_lora * esz + p["o"].numel() * 4 + out.numel() * 4
+            flops = 2 * wl.n_q * wl.heads * v_dim * wl.kv_lora
+        t_mem = byts / (peaks["hbm_gbs"] * 1e9)
+        t_flop = flops / (peaks["bf16_tflops"] * 1e12)
+        ent = {"launch_us": ms * 1e3, "bytes_per_launch": byts, "flops_per_launch": flops,
+               "weight_copies": copies}
+        if t_mem >= t_flop:
+            ach = byts / (ms / 1e3) / 1e9
+            ent.update(bound="hbm", achieved=ach, unit="GB/s", peak=peaks["hbm_gbs"],
+                       frac=ach / peaks["hbm_gbs"], peak_source=f"{peak_src} hbm_gbs")
+        else:
+            ach = flops / (ms / 1e3) / 1e12
+            ent.update(bound="tensor", achieved=ach, unit="TFLOP/s", peak=peaks["bf16_tflops"],
+                       frac=ach / peaks["bf16_tflops"], peak_source=f"{peak_src} bf16_tflops")
+        res[name] = ent
+    del p
+    torch.cuda.empty_cache()
+    return res
 
 
 class StepBench:
@@ -588,6 +654,7 @@ def other_config(dsa, name, dev, stream, no_graph, pg, local, world, peaks, peak
     ent["roofline"] = roofline_of(wl, fused, sel_ms, idx_ms, peaks, peak_src)
     del sb
     torch.cuda.empty_cache()
+    ent["projections"] = time_projections(dsa, wl, dev, stream, peaks, peak_src)
     return ent
 
 
@@ -720,6 +787,7 @@ def run_ours(args):
         e2e["value"] = job_throughput(world, wl.n_q, e2e["ms_per_step"])
 
     peaks, peak_src = measured_peaks()
+    projections = time_projections(dsa, wl, dev, stream, peaks, peak_src)
     # the other workloads of the suite, each timed the same way
     configs = {}
     if not args.no_configs:
@@ -771,6 +839,7 @@ def run_ours(args):
         pool["peak_source"] = f"{peak_src} hbm_gbs"
         pool["traffic"] = kernel_traffic("pool_compress", wl.name)
         line["pool_compress"] = pool
+    line["projections"] = projections
     if configs:
         line["configs"] = configs
     if not args.no_cpu_baseline:

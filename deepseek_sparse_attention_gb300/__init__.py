@@ -34,7 +34,8 @@ __all__ = [
     "dsa_decode_step", "dsa_decode_step_noalloc", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
     "OP_INDEX_SCORES", "OP_TOPK_SELECT", "OP_SPARSE_MLA", "OP_DECODE_STEP", "OP_INDEX_SELECT",
     "OP_POOL_COMPRESS", "dsa_pool_compress", "dsa_index_prepare", "dsa_workspace_set_wait_budget",
-    "FLAG_TWO_LAUNCH", "FLAG_DESC_ORDER", "FLAG_DENSE",
+    "FLAG_TWO_LAUNCH", "FLAG_DESC_ORDER", "FLAG_DENSE", "OP_PROJECT", "dsa_absorb_q",
+    "dsa_up_project",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
@@ -42,6 +43,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
 DSA_F32, DSA_BF16 = 0, 1
 OP_INDEX_SCORES, OP_TOPK_SELECT, OP_SPARSE_MLA, OP_DECODE_STEP, OP_INDEX_SELECT = 0, 1, 2, 3, 4
 OP_POOL_COMPRESS = 5
+OP_PROJECT = 6
 FLAG_TWO_LAUNCH, FLAG_DESC_ORDER, FLAG_DENSE = 0x1, 0x2, 0x4
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
           3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE", 6: "DSA_ERR_TIMEOUT"}
@@ -107,6 +109,8 @@ def load() -> ctypes.CDLL:
             "dsa_pool_compress": ([S, B, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_index_prepare": ([S, i64, P, P, i32, ctypes.c_double, P, P], ctypes.c_int),
             "dsa_workspace_set_wait_budget": ([P, sz, ctypes.c_uint64, P], ctypes.c_int),
+            "dsa_absorb_q": ([S, i32, i32, P, P, P, P, sz, P], ctypes.c_int),
+            "dsa_up_project": ([S, i32, i32, P, P, P, P, sz, P], ctypes.c_int),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -261,6 +265,18 @@ def dsa_check_device_error(ws: Optional[torch.Tensor], stream=None) -> int:
     if rc not in (0, 5, 6):
         raise DsaError("dsa_check_device_error", rc)
     return int(code.value)
+
+
+def dsa_absorb_q(shape, q, w_uk, q_abs, ws, stream=None) -> None:
+    """q [n_q, heads, nope + rope], w_uk [heads, nope, kv_lora] -> q_abs (see dsa.h)."""
+    _call("dsa_absorb_q", ctypes.byref(shape), int(q.shape[0]), int(w_uk.shape[1]), _ptr(q),
+          _ptr(w_uk), _ptr(q_abs), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def dsa_up_project(shape, o, w_uv, out, ws, stream=None) -> None:
+    """o [n_q, heads, kv_lora] float32, w_uv [heads, v_dim, kv_lora] -> out (see dsa.h)."""
+    _call("dsa_up_project", ctypes.byref(shape), int(o.shape[0]), int(w_uv.shape[1]), _ptr(o),
+          _ptr(w_uv), _ptr(out), _ptr(ws), ws.numel(), _stream(stream))
 
 
 def dsa_workspace_set_wait_budget(ws: torch.Tensor, ns: int, stream=None) -> None:

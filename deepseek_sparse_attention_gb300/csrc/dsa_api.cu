@@ -113,16 +113,22 @@ StepLayout step_layout(const Shape& sh, const BatchDev& b) {
     return L;
 }
 
+// Where the scratch of the single-step entry points begins: after the prefix
+// the fused decode launch keeps zero, so that one workspace can serve every
+// entry point in turn.
+size_t scratch_off() { return align_up(ws_zero_bytes()); }
+
 size_t op_bytes(const Shape& sh, const BatchDev& b, int32_t op) {
     switch (op) {
         case DSA_OP_INDEX_SCORES:
-            return align_up(kWsHeaderBytes + index_scores_scratch_bytes(sh, b));
+            return align_up(scratch_off() + index_scores_scratch_bytes(sh, b));
         case DSA_OP_TOPK_SELECT: return kWsHeaderBytes;
         case DSA_OP_SPARSE_MLA:
-            return align_up(kWsHeaderBytes + sparse_mla_scratch_bytes(sh, b));
+            return align_up(scratch_off() + sparse_mla_scratch_bytes(sh, b));
         case DSA_OP_DECODE_STEP: return step_layout(sh, b).total;
         case DSA_OP_INDEX_SELECT: return step_layout(sh, b).attn;
         case DSA_OP_POOL_COMPRESS: return kWsHeaderBytes;
+        case DSA_OP_PROJECT: return kWsHeaderBytes;
         default: return 0;
     }
 }
@@ -186,6 +192,7 @@ int32_t plan_launches(const Shape& sh, const BatchDev& bh, int32_t op, int32_t s
         case DSA_OP_SPARSE_MLA: return attn;
         case DSA_OP_INDEX_SELECT: return sel;
         case DSA_OP_POOL_COMPRESS: return sh.kpool > 1 ? 1 : 0;
+        case DSA_OP_PROJECT: return 1;
         default: return (bh.flags & DSA_FLAG_DENSE) ? attn : sel + attn;
     }
 }
@@ -259,7 +266,7 @@ dsa_status dsa_workspace_size(const dsa_shape* shape, const dsa_batch* batch, in
     if (batch->max_kv_len >= ((int64_t)1 << 31) ||
         (batch->n_q > 65535 && op != DSA_OP_POOL_COMPRESS))
         return DSA_ERR_UNSUPPORTED;
-    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_POOL_COMPRESS) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_PROJECT) return DSA_ERR_INVALID_ARG;
     *out_bytes = op_bytes(sh, host_batch(batch, sh), op);
     return DSA_OK;
 }
@@ -272,7 +279,7 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
     if (s != DSA_OK) return s;
     if (batch->n_q < 0 || batch->max_kv_len < 0 || (batch->flags & ~kKnownFlags) != 0)
         return DSA_ERR_INVALID_ARG;
-    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_POOL_COMPRESS) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_PROJECT) return DSA_ERR_INVALID_ARG;
     const BatchDev bh = host_batch(batch, sh);
     int32_t rps = 0, splits = 0;
     plan_attention_splits(sh, bh, &rps, &splits);
@@ -296,7 +303,7 @@ dsa_status dsa_index_scores(const dsa_shape* shape, const dsa_batch* batch, cons
     if ((s = check_ws(ws, ws_bytes, op_bytes(sh, b, DSA_OP_INDEX_SCORES))) != DSA_OK) return s;
     int32_t* err = static_cast<int32_t*>(ws);
     return cuda_status(launch_index_scores(sh, b, max_keys(sh, b), q_idx, w, k_idx, scores, ld,
-                                           bytes(ws) + kWsHeaderBytes, err,
+                                           bytes(ws) + scratch_off(), err,
                                            static_cast<cudaStream_t>(stream)),
                        "index_scores");
 }
@@ -344,7 +351,7 @@ dsa_status dsa_sparse_mla_attn(const dsa_shape* shape, const dsa_batch* batch, c
     // only after it has completed.
     return cuda_status(launch_sparse_mla(sh, b, q_abs, cache, dense ? nullptr : idx,
                                          dense ? nullptr : n_sel, out, lse,
-                                         bytes(ws) + kWsHeaderBytes, need - kWsHeaderBytes, err,
+                                         bytes(ws) + scratch_off(), need - scratch_off(), err,
                                          /*q_early=*/false, static_cast<cudaStream_t>(stream)),
                        "sparse_mla_attn");
 }
@@ -386,6 +393,40 @@ dsa_status dsa_pool_compress(const dsa_shape* shape, const dsa_batch* batch, con
     return cuda_status(launch_pool_compress(sh, b, cells, pos, pool_keys, err,
                                             static_cast<cudaStream_t>(stream)),
                        "pool_compress");
+}
+
+// The projections' common checks: sizes, pointers (16-byte aligned), workspace.
+static dsa_status check_projection(const dsa_shape* shape, int32_t n_q, int32_t k_dim, int32_t k_unit,
+                            const void* in, const void* w, const void* out, void* ws,
+                            size_t ws_bytes, Shape* sh) {
+    dsa_status s = check_shape(shape, sh);
+    if (s != DSA_OK) return s;
+    if (n_q < 0 || k_dim < k_unit || k_dim % k_unit != 0) return DSA_ERR_INVALID_ARG;
+    if (k_dim > 512 || n_q > (1 << 24)) return DSA_ERR_UNSUPPORTED;
+    if (n_q > 0 && (in == nullptr || w == nullptr || out == nullptr)) return DSA_ERR_INVALID_ARG;
+    if (!aligned16(in) || !aligned16(w) || !aligned16(out)) return DSA_ERR_INVALID_ARG;
+    return check_ws(ws, ws_bytes, kWsHeaderBytes);
+}
+
+dsa_status dsa_absorb_q(const dsa_shape* shape, int32_t n_q, int32_t nope_dim, const void* q,
+                        const void* w_uk, void* q_abs, void* ws, size_t ws_bytes, void* stream) {
+    Shape sh;
+    dsa_status s = check_projection(shape, n_q, nope_dim, 64, q, w_uk, q_abs, ws, ws_bytes, &sh);
+    if (s != DSA_OK) return s;
+    return cuda_status(launch_absorb_q(sh, n_q, nope_dim, q, w_uk, q_abs,
+                                       static_cast<int32_t*>(ws),
+                                       static_cast<cudaStream_t>(stream)),
+                       "absorb_q");
+}
+
+dsa_status dsa_up_project(const dsa_shape* shape, int32_t n_q, int32_t v_dim, const float* o,
+                          const void* w_uv, float* out, void* ws, size_t ws_bytes, void* stream) {
+    Shape sh;
+    dsa_status s = check_projection(shape, n_q, v_dim, 128, o, w_uv, out, ws, ws_bytes, &sh);
+    if (s != DSA_OK) return s;
+    return cuda_status(launch_up_project(sh, n_q, v_dim, o, w_uv, out, static_cast<int32_t*>(ws),
+                                         static_cast<cudaStream_t>(stream)),
+                       "up_project");
 }
 
 dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const void* q_idx,

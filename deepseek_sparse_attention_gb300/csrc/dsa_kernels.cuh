@@ -1,6 +1,7 @@
 // dsa_kernels.cuh -- host-side launchers of the DSA kernels (internal to libdsa).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -49,6 +50,14 @@ dsa_status noalloc_scratch(void** out);
 // Streaming multiprocessors of the current device (index_scores_tc.cu); grid
 // and wave sizes derive from it.
 int sm_count();
+
+// A tiled TMA descriptor over a bfloat16 tensor of `rank` dimensions, the
+// innermost first: dims[rank] in elements, strides[rank - 1] the byte strides
+// of dimensions 1.., box[rank] in elements, the 128-byte swizzle, out-of-range
+// elements read as zero (index_scores_tc.cu).  False when the driver's encoder
+// is missing or refuses the arguments.
+bool encode_bf16_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box);
 
 // Validated layer geometry (see dsa_shape in dsa.h).
 struct Shape {
@@ -121,6 +130,15 @@ cudaError_t launch_index_prepare(const Shape& sh, int64_t n_vec, const float* x,
 cudaError_t launch_pool_compress(const Shape& sh, const BatchDev& b, const void* cells,
                                  const float* pos, void* pool_keys, int32_t* err,
                                  cudaStream_t st);
+
+// The projections around the attention (proj.cu): query absorption
+// q_abs[q,h] = (q[q,h,:nope] . w_uk[h], q[q,h,nope:]) and the output
+// up-projection out[q,h] = w_uv[h] . o[q,h]; bf16 on the tensor cores, float32
+// on CUDA cores.
+cudaError_t launch_absorb_q(const Shape& sh, int32_t n_q, int32_t nope, const void* q,
+                            const void* w_uk, void* q_abs, int32_t* err, cudaStream_t st);
+cudaError_t launch_up_project(const Shape& sh, int32_t n_q, int32_t v_dim, const float* o,
+                              const void* w_uv, float* out, int32_t* err, cudaStream_t st);
 
 // Step 3.  bf16 rows run on the tensor cores (sparse_mla_tc.cu), float32 rows
 // on CUDA cores (sparse_mla.cu).  Row splits per query and the scratch for the

@@ -27,12 +27,26 @@
 namespace dsa {
 namespace idxp {
 
+// Row-major [rows, 128] bf16 matrix read in boxes of box_rows x 64 columns with
+// the 128-byte swizzle.
+bool make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+    if (rows == 0) return false;
+    const uint64_t dims[2] = {(uint64_t)kIdxDim, rows};
+    const uint64_t strides[1] = {(uint64_t)kIdxDim * 2};
+    const uint32_t box[2] = {64, box_rows};
+    return encode_bf16_map(m, base, 2, dims, strides, box);
+}
+
+}  // namespace idxp
+
+namespace {
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-static EncodeTiledFn encode_fn() {
+EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -45,22 +59,26 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Row-major [rows, 128] bf16 matrix read in boxes of box_rows x 64 columns with
-// the 128-byte swizzle.
-bool make_rows128_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+}  // namespace
+
+bool encode_bf16_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box) {
     EncodeTiledFn enc = encode_fn();
-    if (enc == nullptr || rows == 0) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kIdxDim, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kIdxDim * 2};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (enc == nullptr || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        if (dims[i] == 0) return false;
+        d[i] = dims[i];
+        bx[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), d,
+               st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
-
-}  // namespace idxp
 
 int sm_count() {
     int dev = 0, n = 0;

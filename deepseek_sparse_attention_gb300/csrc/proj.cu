@@ -1,0 +1,371 @@
+// proj.cu -- the two projections around the absorbed attention: query
+// absorption and the output up-projection.
+//
+// "GLM-5.x (glm-dsa, glm5next)", "The block": the per-head key and value
+// decompressions of MLA are folded into the query (attn_k_b) and into the
+// output (attn_v_b); "GLM 5.2 in one C file", "Attention: Multi head Latent
+// Attention With a Tiny KV Cache": the key up-projection is absorbed into the
+// query, which then scores the cached latents directly, and the pooled latent
+// is projected to the head's value space once, at the end.
+//
+//   absorb  q_abs[q,h,i] = sum_{d < nope} q[q,h,d] * w_uk[h,d,i]   (i < kv_lora)
+//           q_abs[q,h,kv_lora + r] = q[q,h,nope + r]               (the rope part)
+//   up      out[q,h,v]   = sum_{i < kv_lora} w_uv[h,v,i] * o[q,h,i]
+//
+// Per head both are a weight matrix times the queries' vectors.  On the
+// tensor cores the weights are M (128 output features per tile) and the
+// queries N (up to 256 per tile, a decode batch padded to 16): the weights --
+// 12.6 MB for absorb, 16.8 MB for up at 64 heads -- stream once per query
+// tile, which for decode is once.  One CTA per (head, 128-feature block, query
+// tile); K in blocks of 64 (one 128-byte swizzle row) through a ring of
+// shared-memory stages:
+//   warp 0     TMA: the weight block -- absorb: w_uk rows d (K) of 64 features
+//              each (MN-major A, two boxes for 128 features); up: w_uv rows v
+//              (K-major A) -- and, for absorb, the queries' k-block (a 3-D box
+//              of 64 dims x 1 head x N queries, K-major B);
+//   warps 2-7  (up) the attention output o is float32: each k-block is split
+//              into bf16 hi and lo = o - hi, written in the 128-byte swizzle
+//              layout; both are multiplied into the one accumulator, carrying
+//              o to about 2^-16 relative (bf16 alone: 2^-9);
+//   warp 1     one thread issues the MMAs into a TMEM accumulator [128 x N];
+//   warps 4-7  epilogue, one TMEM lane (output feature) per thread: the N query
+//              columns read back and stored (absorb: rounded to bf16); warps
+//              2-3 of absorb copy the rope part.
+// Float32 inputs take a CUDA-core kernel.  All waits are bounded: a timeout
+// records the error word and the CTA winds down.
+#include "dsa_kernels.cuh"
+#include "sm100.cuh"
+
+namespace dsa {
+namespace {
+
+using namespace sm100;
+
+constexpr int kThreads = 256;
+constexpr int kM = 128;                      // output features per tile (MMA M)
+constexpr uint32_t kABytes = kM * 128;       // one k-block of weights: 16 KB
+constexpr int kConv = 192;                   // up: threads splitting o (warps 2-7)
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+template <int MODE>                          // 0: absorb, 1: up
+struct PCfg {
+    static constexpr int kStages = MODE == 0 ? 3 : 2;
+    // per stage: the weight k-block, then the queries' k-block (up: hi and lo)
+    static uint32_t b_bytes(int n) { return (uint32_t)n * 128u * (MODE == 0 ? 1u : 2u); }
+    static uint32_t stage_bytes(int n) { return kABytes + b_bytes(n); }
+    static uint32_t off_bar(int n) { return kStages * stage_bytes(n); }
+    static uint32_t smem_bytes(int n) { return off_bar(n) + 128 + 1024; }
+};
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 2)
+proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
+        const __nv_bfloat16* __restrict__ q_src, const float* __restrict__ o, void* __restrict__ out,
+        int32_t n_q, int32_t heads, int32_t N, int32_t n_mblk, int32_t nope, int32_t rope,
+        int32_t kv_lora, int32_t v_dim, int32_t* err) {
+    using C = PCfg<MODE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t stage_bytes = kABytes + (uint32_t)N * 128u * (MODE == 0 ? 1u : 2u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * stage_bytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::kStages;
+    uint64_t* acc_full = bars + 2 * C::kStages;
+    uint64_t* drain = acc_full + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 2);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.x / n_mblk, mb = blockIdx.x % n_mblk;
+    const int64_t q0 = (int64_t)blockIdx.y * N;
+    const int n_kb = (MODE == 0 ? nope : kv_lora) / 64;
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < (uint32_t)N) tmem_cols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], MODE == 0 ? 1 : 1 + kConv);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        prefetch_tensormap(&tm_w);
+        if (MODE == 0) prefetch_tensormap(&tm_q);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    // the inputs may come from the previous kernel in the stream
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {                                           // ---- TMA producer
+            int8_t issued_par[C::kStages];
+            for (int s = 0; s < C::kStages; ++s) issued_par[s] = -1;
+            bool ok = true;
+            for (int kb = 0; kb < n_kb && ok; ++kb) {
+                const int s = kb % C::kStages;
+                const uint32_t ph = (uint32_t)(kb / C::kStages) & 1u;
+                if (*abort_flag) { ok = false; break; }
+                ok = mbar_wait(&empty[s], ph ^ 1u, kWaitNs);
+                if (!ok) break;
+                uint8_t* st = smem + s * stage_bytes;
+                mbar_arrive_expect_tx(&full[s], kABytes + (MODE == 0 ? (uint32_t)N * 128u : 0u));
+                if (MODE == 0) {
+                    const int32_t y = h * nope + kb * 64;
+                    tma_load_2d(st, &tm_w, &full[s], mb * kM, y);
+                    tma_load_2d(st + kABytes / 2, &tm_w, &full[s], mb * kM + 64, y);
+                    tma_load_3d(st + kABytes, &tm_q, &full[s], kb * 64, h, (int32_t)q0);
+                } else {
+                    tma_load_2d(st, &tm_w, &full[s], kb * 64, h * v_dim + mb * kM);
+                }
+                issued_par[s] = (int8_t)ph;
+            }
+            if (!ok) {
+                record_error(err, kDevTimeout, blockIdx.x, /*where=*/30);
+                *abort_flag = 1;
+                for (int s = 0; s < C::kStages; ++s)       // copies in flight land first
+                    if (issued_par[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_par[s], 50000000ull);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {                                           // ---- MMA issuer
+            const uint32_t idesc = MODE == 0 ? idesc_bf16_f32_major(kM, N, 1, 0)
+                                             : idesc_bf16_f32(kM, N);
+            bool ok = true;
+            for (int kb = 0; kb < n_kb; ++kb) {
+                const int s = kb % C::kStages;
+                const uint32_t ph = (uint32_t)(kb / C::kStages) & 1u;
+                if (*abort_flag || !mbar_wait(&full[s], ph, kWaitNs)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a = smem_u32(smem + s * stage_bytes);
+                const uint32_t b = a + kABytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    if (MODE == 0) {
+                        // A: [64 rows d][64 features] blocks, the two feature
+                        // halves 8 KB apart (LBO), 8-row groups 1 KB apart (SBO)
+                        mma_bf16_ss(tmem_base, sdesc_sw128(a + kk * 2048, kABytes / 2, 1024),
+                                    sdesc_kmajor_sw128(b + kk * 32), idesc, (kb | kk) != 0);
+                    } else {
+                        const uint64_t ad = sdesc_kmajor_sw128(a + kk * 32);
+                        mma_bf16_ss(tmem_base, ad, sdesc_kmajor_sw128(b + kk * 32), idesc,
+                                    (kb | kk) != 0);
+                        mma_bf16_ss(tmem_base, ad, sdesc_kmajor_sw128(b + N * 128 + kk * 32),
+                                    idesc, 1u);
+                    }
+                }
+                mma_commit(&empty[s]);
+            }
+            if (!ok) {
+                record_error(err, kDevTimeout, blockIdx.x, /*where=*/31);
+                *abort_flag = 1;
+            } else {
+                mma_commit(acc_full);
+            }
+            mma_commit(drain);                                     // every issued MMA retired
+            mbar_wait(drain, 0, 50000000ull);
+        }
+    } else if (MODE == 1) {                                        // ---- o -> bf16 hi, lo
+        const int tc = threadIdx.x - 64;                           // 0 .. kConv-1
+        for (int kb = 0; kb < n_kb; ++kb) {
+            const int s = kb % C::kStages;
+            const uint32_t ph = (uint32_t)(kb / C::kStages) & 1u;
+            if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, kWaitNs)) {
+                record_error(err, kDevTimeout, blockIdx.x, /*where=*/32);
+                *abort_flag = 1;
+                break;
+            }
+            uint8_t* hi = smem + s * stage_bytes + kABytes;
+            uint8_t* lo = hi + N * 128;
+            for (int c = tc; c < N * 8; c += kConv) {
+                const int n = c >> 3, k8 = c & 7;
+                const int64_t q = q0 + n;
+                float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+                if (q < n_q) {
+                    const float4* src = reinterpret_cast<const float4*>(
+                        o + (q * heads + h) * (int64_t)kv_lora + kb * 64 + k8 * 8);
+                    x0 = __ldg(src);
+                    x1 = __ldg(src + 1);
+                }
+                const float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                uint32_t vh[4], vl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __nv_bfloat162 hv = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+                    const float2 hf = __bfloat1622float2(hv);
+                    vh[e] = *reinterpret_cast<const uint32_t*>(&hv);
+                    vl[e] = bf16x2_bits(f[2 * e] - hf.x, f[2 * e + 1] - hf.y);
+                }
+                const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(k8 ^ (n & 7)) << 4);
+                *reinterpret_cast<uint4*>(hi + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+                *reinterpret_cast<uint4*>(lo + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+            }
+            fence_proxy_async_smem();                              // generic writes -> MMA reads
+            mbar_arrive(&full[s]);
+        }
+    } else if (warp < 4 && mb == 0 && rope > 0) {                  // ---- absorb: the rope part
+        const int t = threadIdx.x - 64;                            // 0..63
+        __nv_bfloat16* qa = static_cast<__nv_bfloat16*>(out);
+        const int W = kv_lora + rope, Q = nope + rope;
+        for (int n = 0; n < N && t < rope; ++n) {
+            const int64_t q = q0 + n;
+            if (q >= n_q) break;
+            qa[(q * heads + h) * W + kv_lora + t] = q_src[(q * heads + h) * Q + nope + t];
+        }
+    }
+
+    if (warp >= 4) {                                               // ---- epilogue
+        const bool ok = !*abort_flag && mbar_wait(acc_full, 0, kWaitNs);
+        if (!ok) {
+            if (lane == 0) record_error(err, kDevTimeout, blockIdx.x, /*where=*/33);
+        } else {
+            tc_fence_after();
+            const int m = (warp - 4) * 32 + lane;                  // TMEM lane = output feature
+            const uint32_t lane_addr = tmem_base + ((uint32_t)((warp - 4) * 32) << 16);
+            for (int c0 = 0; c0 < N; c0 += 32) {
+                float v[32];
+                if (N - c0 >= 32) {
+                    tmem_ld_32cols(lane_addr + c0, v);
+                } else {
+                    float v16[16];
+                    tmem_ld_16cols(lane_addr + c0, v16);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) { v[e] = v16[e]; v[e + 16] = 0.f; }
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int64_t q = q0 + c0 + e;
+                    if (c0 + e >= N || q >= n_q) continue;
+                    if (MODE == 0) {
+                        static_cast<__nv_bfloat16*>(out)[(q * heads + h) * (kv_lora + rope) +
+                                                         mb * kM + m] = __float2bfloat16_rn(v[e]);
+                    } else {
+                        static_cast<float*>(out)[(q * heads + h) * v_dim + mb * kM + m] = v[e];
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tmem_cols);
+    }
+}
+
+// Float32 inputs: one output element per thread (absorb) or per warp (up),
+// float32 accumulation in the order of the sum.
+__global__ void __launch_bounds__(256)
+absorb_simt(const float* __restrict__ q, const float* __restrict__ w_uk, float* __restrict__ q_abs,
+            int32_t heads, int32_t nope, int32_t rope, int32_t kv_lora) {
+    const int64_t qh = blockIdx.x;                     // (query, head)
+    const int h = (int)(qh % heads);
+    const float* qv = q + qh * (nope + rope);
+    float* dst = q_abs + qh * (kv_lora + rope);
+    for (int i = threadIdx.x; i < kv_lora; i += blockDim.x) {
+        float acc = 0.f;
+        for (int d = 0; d < nope; ++d) acc = fmaf(qv[d], w_uk[((int64_t)h * nope + d) * kv_lora + i], acc);
+        dst[i] = acc;
+    }
+    for (int r = threadIdx.x; r < rope; r += blockDim.x) dst[kv_lora + r] = qv[nope + r];
+}
+
+__global__ void __launch_bounds__(256)
+up_simt(const float* __restrict__ o, const float* __restrict__ w_uv, float* __restrict__ out,
+        int32_t heads, int32_t kv_lora, int32_t v_dim) {
+    const int64_t qh = blockIdx.x;
+    const int h = (int)(qh % heads);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float* ov = o + qh * kv_lora;
+    for (int v = warp; v < v_dim; v += blockDim.x >> 5) {
+        const float* wr = w_uv + ((int64_t)h * v_dim + v) * kv_lora;
+        float acc = 0.f;
+        for (int i = lane; i < kv_lora; i += 32) acc = fmaf(wr[i], ov[i], acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) out[qh * v_dim + v] = acc;
+    }
+}
+
+int query_tile(int32_t n_q) {
+    int n = (n_q + 15) / 16 * 16;
+    return n > 256 ? 256 : (n < 16 ? 16 : n);
+}
+
+template <int MODE>
+cudaError_t launch_tc(const Shape& sh, int32_t n_q, int32_t nope, int32_t v_dim, const void* q,
+                      const void* w, const float* o, void* out, int32_t* err, cudaStream_t st) {
+    using C = PCfg<MODE>;
+    const int N = query_tile(n_q);
+    CUtensorMap tm_w, tm_q;
+    if (MODE == 0) {
+        const uint64_t wd[2] = {(uint64_t)sh.kv_lora, (uint64_t)sh.heads * nope};
+        const uint64_t ws[1] = {(uint64_t)sh.kv_lora * 2};
+        const uint32_t wb[2] = {64, 64};
+        const int Q = nope + sh.rope;
+        const uint64_t qd[3] = {(uint64_t)Q, (uint64_t)sh.heads, (uint64_t)n_q};
+        const uint64_t qs[2] = {(uint64_t)Q * 2, (uint64_t)sh.heads * Q * 2};
+        const uint32_t qb[3] = {64, 1, (uint32_t)N};
+        if (!encode_bf16_map(&tm_w, w, 2, wd, ws, wb) || !encode_bf16_map(&tm_q, q, 3, qd, qs, qb))
+            return cudaErrorInvalidValue;
+    } else {
+        const uint64_t wd[2] = {(uint64_t)sh.kv_lora, (uint64_t)sh.heads * v_dim};
+        const uint64_t ws[1] = {(uint64_t)sh.kv_lora * 2};
+        const uint32_t wb[2] = {64, (uint32_t)kM};
+        if (!encode_bf16_map(&tm_w, w, 2, wd, ws, wb)) return cudaErrorInvalidValue;
+        tm_q = tm_w;                                   // unused
+    }
+    const int n_mblk = (MODE == 0 ? sh.kv_lora : v_dim) / kM;
+    const size_t smem = C::smem_bytes(N);
+    auto kern = proj_tc<MODE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)(n_mblk * sh.heads), (unsigned)((n_q + N - 1) / N));
+    return launch_pdl(kern, grid, dim3(kThreads), smem, st, tm_w, tm_q,
+                      static_cast<const __nv_bfloat16*>(q), o, out, n_q, (int32_t)sh.heads,
+                      (int32_t)N, (int32_t)n_mblk, nope, (int32_t)sh.rope, (int32_t)sh.kv_lora,
+                      v_dim, err);
+}
+
+}  // namespace
+
+cudaError_t launch_absorb_q(const Shape& sh, int32_t n_q, int32_t nope, const void* q,
+                            const void* w_uk, void* q_abs, int32_t* err, cudaStream_t st) {
+    if (n_q == 0) return cudaSuccess;
+    if (sh.dtype == DSA_BF16)
+        return launch_tc<0>(sh, n_q, nope, 0, q, w_uk, nullptr, q_abs, err, st);
+    absorb_simt<<<(unsigned)((int64_t)n_q * sh.heads), 256, 0, st>>>(
+        static_cast<const float*>(q), static_cast<const float*>(w_uk), static_cast<float*>(q_abs),
+        sh.heads, nope, sh.rope, sh.kv_lora);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_up_project(const Shape& sh, int32_t n_q, int32_t v_dim, const float* o,
+                              const void* w_uv, float* out, int32_t* err, cudaStream_t st) {
+    if (n_q == 0) return cudaSuccess;
+    if (sh.dtype == DSA_BF16)
+        return launch_tc<1>(sh, n_q, 0, v_dim, nullptr, w_uv, o, out, err, st);
+    up_simt<<<(unsigned)((int64_t)n_q * sh.heads), 256, 0, st>>>(
+        o, static_cast<const float*>(w_uv), out, sh.heads, sh.kv_lora, v_dim);
+    return cudaGetLastError();
+}
+
+}  // namespace dsa

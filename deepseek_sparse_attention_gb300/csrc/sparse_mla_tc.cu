@@ -704,37 +704,14 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &qr) != cudaSuccess ||
-            qr != cudaDriverEntryPointSuccess)
-            return (EncodeTiledFn) nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
 // Row-major [rows, width] bf16 matrix read in boxes of box_rows x 64 columns
 // with the 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t width, uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (enc == nullptr || rows == 0) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)width * 2};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+    if (rows == 0) return false;
+    const uint64_t dims[2] = {(uint64_t)width, rows};
+    const uint64_t strides[1] = {(uint64_t)width * 2};
+    const uint32_t box[2] = {64, box_rows};
+    return encode_bf16_map(m, base, 2, dims, strides, box);
 }
 
 template <int W>

@@ -157,6 +157,7 @@ int64_t dsa_index_row_width(const dsa_shape *shape);
 #define DSA_OP_DECODE_STEP 3
 #define DSA_OP_INDEX_SELECT 4
 #define DSA_OP_POOL_COMPRESS 5
+#define DSA_OP_PROJECT 6
 dsa_status dsa_workspace_size(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
                               size_t *bytes);
 
@@ -177,8 +178,9 @@ dsa_status dsa_plan(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
  * that follows it (DSA_WS_ZERO_BYTES in all, or the whole of a smaller workspace).
  * Call once on a freshly allocated workspace that was not allocated
  * zero-filled; after that every completed call leaves this region as it must
- * be, and dsa_check_device_error() re-zeroes it when a kernel reported an
- * error.  `ws` must be 256-byte aligned and at least 256 bytes. */
+ * be (no entry point uses it as scratch, so one workspace may serve all of
+ * them in turn), and dsa_check_device_error() re-zeroes it when a kernel
+ * reported an error.  `ws` must be 256-byte aligned and at least 256 bytes. */
 #define DSA_WS_ZERO_BYTES (256u + 16u * 21508u * 4u + 16u * 256u * 8u)
 dsa_status dsa_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
@@ -283,6 +285,37 @@ dsa_status dsa_index_prepare(const dsa_shape *shape, int64_t n_vec, const float 
 dsa_status dsa_pool_compress(const dsa_shape *shape, const dsa_batch *batch, const void *cells,
                              const float *pos, void *pool_keys, void *ws, size_t ws_bytes,
                              void *stream);
+
+/* Query absorption, the producer of step 3's query ("GLM-5.x (glm-dsa,
+ * glm5next)", "The block": the per-head key decompression of MLA is folded into
+ * the query, attn_k_b; "GLM 5.2 in one C file", "Attention: Multi head Latent
+ * Attention With a Tiny KV Cache": the key up-projection is absorbed into the
+ * query, which then scores the cached latents directly).
+ *   q     [n_q, heads, nope_dim + rope_dim] dtype: per head the no-rope part
+ *         of the query, then its (already rotated) rope part
+ *   w_uk  [heads, nope_dim, kv_lora] dtype: row d of head h is the latent-space
+ *         image of no-rope dimension d
+ *   q_abs [n_q, heads, kv_lora + rope_dim] dtype out: the q_abs of step 3,
+ *         q_abs[q,h,i] = sum_d q[q,h,d] * w_uk[h,d,i] for i < kv_lora, rounded
+ *         to dtype; then the rope part copied
+ * nope_dim a multiple of 64 up to 512 (192 for GLM-5.x: a 256-wide key head is
+ * 192 no-rope + 64 rope dimensions).  float32 accumulation.  Pointers 16-byte
+ * aligned.  Workspace: DSA_OP_PROJECT (the error word). */
+dsa_status dsa_absorb_q(const dsa_shape *shape, int32_t n_q, int32_t nope_dim, const void *q,
+                        const void *w_uk, void *q_abs, void *ws, size_t ws_bytes, void *stream);
+
+/* Output up-projection, the consumer of step 3's output ("GLM-5.x", "The
+ * block": the value decompression folded into the output, attn_v_b; "GLM 5.2
+ * in one C file": the pooled latent is projected to the head's value space).
+ *   o     [n_q, heads, kv_lora] float32: step 3's out
+ *   w_uv  [heads, v_dim, kv_lora] dtype: row v of head h maps the latent to
+ *         value dimension v
+ *   out   [n_q, heads, v_dim] float32 out: out[q,h,v] = sum_i w_uv[h,v,i] * o[q,h,i]
+ * v_dim a multiple of 128 up to 512 (256 for GLM-5.x).  bf16 weights multiply
+ * o split into two bf16 parts (o to about 2^-16 relative), float32
+ * accumulation.  Pointers 16-byte aligned.  Workspace: DSA_OP_PROJECT. */
+dsa_status dsa_up_project(const dsa_shape *shape, int32_t n_q, int32_t v_dim, const float *o,
+                          const void *w_uv, float *out, void *ws, size_t ws_bytes, void *stream);
 
 /* Step 3: absorbed-MLA attention over the selected rows ("GLM 5.2 in one C
  * file", MLA decode path; "GLM-5.x", "The block").

@@ -81,10 +81,13 @@ def test_workspace_sizes(lib):
     assert n_sel >= 256 + 16 * 21508 * 4 + 16 * 256 * 8          # DSA_WS_ZERO_BYTES of dsa.h
     rc, n = _size(sh, _batch(), dsa.OP_POOL_COMPRESS)     # the header: the error word
     assert rc == 0 and n == 256
-    rc, _ = _size(sh, _batch(), 6)
-    assert rc == 1
+    rc, n = _size(sh, _batch(), dsa.OP_PROJECT)            # the header: the error word
+    assert rc == 0 and n == 256
     rc, _ = _size(sh, _batch(), 7)
     assert rc == 1
+    # the single-step entry points keep their scratch clear of the zeroed prefix
+    rc, n_idx = _size(sh, _batch(), dsa.OP_INDEX_SCORES)
+    assert n_idx >= 256 + 16 * 21508 * 4 + 16 * 256 * 8
 
 
 @pytest.mark.parametrize("field,value,code", [
@@ -255,6 +258,28 @@ def test_plan_of_the_benchmark_workloads(lib, name, launches, splits, rows_per_s
     dense = dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP)
     assert dense["attn_splits"] * dense["attn_rows_per_split"] >= max(wl.kv_lens)
     assert dense["kernel_launches"] == (2 if dense["attn_splits"] > 2 else 1)
+
+
+def test_projections_reject_before_enqueue(lib):
+    """dsa_absorb_q / dsa_up_project: widths (no-rope part a multiple of 64,
+    value width of 128, at most 512), pointers, alignment and the workspace are
+    checked before anything is enqueued."""
+    P = ctypes.c_void_p
+    good = P(256)
+    sh = dsa.make_shape()
+    fa, fu = lib.dsa_absorb_q, lib.dsa_up_project
+    assert fa(ctypes.byref(sh), 4, 100, good, good, good, good, 256, None) == 1     # nope % 64
+    assert fa(ctypes.byref(sh), 4, 576, good, good, good, good, 256, None) == 2     # > 512
+    assert fa(ctypes.byref(sh), 4, 192, None, good, good, good, 256, None) == 1
+    assert fa(ctypes.byref(sh), 4, 192, good, P(264), good, good, 256, None) == 1   # misaligned
+    assert fa(ctypes.byref(sh), 4, 192, good, good, good, good, 16, None) == 3      # workspace
+    assert fa(ctypes.byref(sh), -1, 192, good, good, good, good, 256, None) == 1
+    assert fu(ctypes.byref(sh), 4, 200, good, good, good, good, 256, None) == 1     # v % 128
+    assert fu(ctypes.byref(sh), 4, 256, good, good, None, good, 256, None) == 1
+    assert fu(ctypes.byref(sh), 4, 256, good, good, good, None, 256, None) == 3
+    # nothing to do: no query
+    assert fa(ctypes.byref(sh), 0, 192, None, None, None, good, 256, None) == 0
+    assert fu(ctypes.byref(sh), 0, 256, None, None, None, good, 256, None) == 0
 
 
 def test_python_binding_rejects_host_tensors(lib):

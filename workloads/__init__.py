@@ -33,7 +33,8 @@ from typing import Dict, List, Optional
 
 import torch
 
-_TAGS = {"q_idx": 1, "w": 2, "k_idx": 3, "q_abs": 4, "cache": 5, "lengths": 6}
+_TAGS = {"q_idx": 1, "w": 2, "k_idx": 3, "q_abs": 4, "cache": 5, "lengths": 6, "q_full": 7,
+         "w_uk": 8, "w_uv": 9, "o": 10}
 
 
 @dataclasses.dataclass
@@ -185,3 +186,31 @@ def small(name: str, kv_lens: List[int], q_lens: Optional[List[int]] = None, top
     return Workload(name, dtype, list(kv_lens), list(q_lens or [1] * len(kv_lens)), top_k=top_k,
                     kpool=kpool, rope=rope, seed=seed, w_std=w_std, cache_scale=cache_scale,
                     description=f"reduced {name}")
+
+
+def projections(wl: Workload, device="cpu", nope: int = 192, v_dim: int = 256, copies: int = 1,
+                seed_offset: int = 0) -> Dict[str, object]:
+    """Seeded inputs of the two projections around the attention, for the
+    workload's queries and heads:
+
+    * ``q_full`` [n_q, heads, nope + rope]  per head the no-rope query, then the
+      rope part (N(0,1), dtype)
+    * ``w_uk``   [heads, nope, kv_lora]     key up-projection, N(0, 1/nope) (dtype)
+    * ``w_uv``   [heads, v_dim, kv_lora]    value up-projection, N(0, 1/kv_lora)
+      (dtype)
+    * ``o``      [n_q, heads, kv_lora]      an attention output, N(0, 1/16) float32
+
+    ``copies > 1`` draws further independent weight sets (``w_uk_copies``,
+    ``w_uv_copies``) for timing loops that must not find the weights in L2.
+    """
+    dt = wl.torch_dtype()
+    seed = wl.seed + seed_offset
+    d: Dict[str, object] = {}
+    d["q_full"] = _randn((wl.n_q, wl.heads, nope + wl.rope), _TAGS["q_full"], seed, 1.0, dt, device)
+    d["o"] = _randn((wl.n_q, wl.heads, wl.kv_lora), _TAGS["o"], seed, 0.25, torch.float32, device)
+    d["w_uk_copies"] = [_randn((wl.heads, nope, wl.kv_lora), _TAGS["w_uk"], seed + 7919 * c,
+                               1.0 / math.sqrt(nope), dt, device) for c in range(copies)]
+    d["w_uv_copies"] = [_randn((wl.heads, v_dim, wl.kv_lora), _TAGS["w_uv"], seed + 7919 * c,
+                               1.0 / math.sqrt(wl.kv_lora), dt, device) for c in range(copies)]
+    d["w_uk"], d["w_uv"] = d["w_uk_copies"][0], d["w_uv_copies"][0]
+    return d
