@@ -798,8 +798,12 @@ def run_ours(args):
         del sb, keys, caches, d, out, lse, idx, n_sel, ws
         torch.cuda.empty_cache()
         for name in names:
-            configs[name] = other_config(dsa, name, dev, stream, args.no_graph, pg, local, world,
-                                         peaks, peak_src)
+            try:
+                configs[name] = other_config(dsa, name, dev, stream, args.no_graph, pg, local,
+                                             world, peaks, peak_src)
+            except (RuntimeError, dsa.DsaError) as exc:     # recorded, not hidden
+                configs[name] = {"error": f"{type(exc).__name__}: {exc}"}
+                torch.cuda.synchronize(dev)
         d = host_d
 
     if rank != 0:

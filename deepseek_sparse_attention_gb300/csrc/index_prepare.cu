@@ -100,12 +100,13 @@ cudaError_t launch_index_prepare(const Shape& sh, int64_t n_vec, const float* x,
     int64_t blocks = (n_vec + kWarpsPerCta - 1) / kWarpsPerCta;
     if (blocks > (int64_t)sm_count() * 8) blocks = (int64_t)sm_count() * 8;
     if (sh.dtype == DSA_BF16)
-        index_prepare_kernel<__nv_bfloat16><<<(unsigned)blocks, 32 * kWarpsPerCta, 0, st>>>(
-            n_vec, x, pos, rope_dims, base, static_cast<__nv_bfloat16*>(out));
+        return launch_plain(index_prepare_kernel<__nv_bfloat16>, dim3((unsigned)blocks),
+                            dim3(32 * kWarpsPerCta), 0, st, n_vec, x, pos, rope_dims, base,
+                            static_cast<__nv_bfloat16*>(out));
     else
-        index_prepare_kernel<float><<<(unsigned)blocks, 32 * kWarpsPerCta, 0, st>>>(
-            n_vec, x, pos, rope_dims, base, static_cast<float*>(out));
-    return cudaGetLastError();
+        return launch_plain(index_prepare_kernel<float>, dim3((unsigned)blocks),
+                            dim3(32 * kWarpsPerCta), 0, st, n_vec, x, pos, rope_dims, base,
+                            static_cast<float*>(out));
 }
 
 }  // namespace dsa

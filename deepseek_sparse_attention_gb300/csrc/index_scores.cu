@@ -98,16 +98,13 @@ cudaError_t launch_index_scores(const Shape& sh, const BatchDev& b, int64_t max_
     if (index_scores_tc_eligible(sh, b))
         return launch_index_scores_tc(sh, b, q_idx, w, k_idx, scores, ld, scratch, err, st);
     const dim3 grid((unsigned)((max_keys + kKeysPerCta - 1) / kKeysPerCta), (unsigned)b.n_q);
-    if (sh.dtype == DSA_F32) {
-        index_scores_simt<float><<<grid, kKeysPerCta, 0, st>>>(
-            b, sh.idx_heads, static_cast<const float*>(q_idx), w,
-            static_cast<const float*>(k_idx), scores, ld, err);
-    } else {
-        index_scores_simt<__nv_bfloat16><<<grid, kKeysPerCta, 0, st>>>(
-            b, sh.idx_heads, static_cast<const __nv_bfloat16*>(q_idx), w,
-            static_cast<const __nv_bfloat16*>(k_idx), scores, ld, err);
-    }
-    return cudaGetLastError();
+    if (sh.dtype == DSA_F32)
+        return launch_plain(index_scores_simt<float>, grid, dim3(kKeysPerCta), 0, st, b,
+                            sh.idx_heads, static_cast<const float*>(q_idx), w,
+                            static_cast<const float*>(k_idx), scores, ld, err);
+    return launch_plain(index_scores_simt<__nv_bfloat16>, grid, dim3(kKeysPerCta), 0, st, b,
+                        sh.idx_heads, static_cast<const __nv_bfloat16*>(q_idx), w,
+                        static_cast<const __nv_bfloat16*>(k_idx), scores, ld, err);
 }
 
 }  // namespace dsa

@@ -243,8 +243,8 @@ cudaError_t launch_tc(const Shape& sh, const BatchDev& b, const void* q_idx, con
     const bool local = GQ == 1 && b.n_q <= C::kLocalMaxQ;
     cudaError_t e;
     if (!local) {
-        idx_group_plan<<<1, 1024, 0, st>>>(b, GQ, pa.seq_goff, pa.groups, pa.tile_off, err);
-        e = cudaGetLastError();
+        e = launch_plain(idx_group_plan, dim3(1), dim3(1024), 0, st, b, (int32_t)GQ, pa.seq_goff,
+                         pa.groups, pa.tile_off, err);
         if (e != cudaSuccess) return e;
     }
     auto kern = index_scores_tc<GQ>;

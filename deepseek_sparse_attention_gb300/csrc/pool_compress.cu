@@ -144,14 +144,15 @@ cudaError_t launch_pool_compress(const Shape& sh, const BatchDev& b, const void*
     const bool four = sh.kpool == 4;
     if (sh.dtype == DSA_BF16) {
         auto k = four ? pool_compress_kernel<__nv_bfloat16, 4> : pool_compress_kernel<__nv_bfloat16, 0>;
-        k<<<grid, 32 * kWarpsPerCta, 0, st>>>(b, static_cast<const __nv_bfloat16*>(cells), pos,
-                                              static_cast<__nv_bfloat16*>(pool_keys), err);
+        return launch_plain(k, grid, dim3(32 * kWarpsPerCta), 0, st, b,
+                            static_cast<const __nv_bfloat16*>(cells), pos,
+                            static_cast<__nv_bfloat16*>(pool_keys), err);
     } else {
         auto k = four ? pool_compress_kernel<float, 4> : pool_compress_kernel<float, 0>;
-        k<<<grid, 32 * kWarpsPerCta, 0, st>>>(b, static_cast<const float*>(cells), pos,
-                                              static_cast<float*>(pool_keys), err);
+        return launch_plain(k, grid, dim3(32 * kWarpsPerCta), 0, st, b,
+                            static_cast<const float*>(cells), pos, static_cast<float*>(pool_keys),
+                            err);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace dsa

@@ -352,10 +352,10 @@ cudaError_t launch_absorb_q(const Shape& sh, int32_t n_q, int32_t nope, const vo
     if (n_q == 0) return cudaSuccess;
     if (sh.dtype == DSA_BF16)
         return launch_tc<0>(sh, n_q, nope, 0, q, w_uk, nullptr, q_abs, err, st);
-    absorb_simt<<<(unsigned)((int64_t)n_q * sh.heads), 256, 0, st>>>(
-        static_cast<const float*>(q), static_cast<const float*>(w_uk), static_cast<float*>(q_abs),
-        sh.heads, nope, sh.rope, sh.kv_lora);
-    return cudaGetLastError();
+    return launch_plain(absorb_simt, dim3((unsigned)((int64_t)n_q * sh.heads)), dim3(256), 0, st,
+                        static_cast<const float*>(q), static_cast<const float*>(w_uk),
+                        static_cast<float*>(q_abs), (int32_t)sh.heads, nope, (int32_t)sh.rope,
+                        (int32_t)sh.kv_lora);
 }
 
 cudaError_t launch_up_project(const Shape& sh, int32_t n_q, int32_t v_dim, const float* o,
@@ -363,9 +363,9 @@ cudaError_t launch_up_project(const Shape& sh, int32_t n_q, int32_t v_dim, const
     if (n_q == 0) return cudaSuccess;
     if (sh.dtype == DSA_BF16)
         return launch_tc<1>(sh, n_q, 0, v_dim, nullptr, w_uv, o, out, err, st);
-    up_simt<<<(unsigned)((int64_t)n_q * sh.heads), 256, 0, st>>>(
-        o, static_cast<const float*>(w_uv), out, sh.heads, sh.kv_lora, v_dim);
-    return cudaGetLastError();
+    return launch_plain(up_simt, dim3((unsigned)((int64_t)n_q * sh.heads)), dim3(256), 0, st, o,
+                        static_cast<const float*>(w_uv), out, (int32_t)sh.heads,
+                        (int32_t)sh.kv_lora, v_dim);
 }
 
 }  // namespace dsa

@@ -306,11 +306,9 @@ cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, 
                                          (int)S::kTotal);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)n_split, (unsigned)b.n_q);
-    kern<<<grid, kThreads, S::kTotal, st>>>(b, sh.scale, static_cast<const T*>(q_abs),
-                                            static_cast<const T*>(cache), idx, n_sel,
-                                            sh.index_row_width(), rps, n_split, out, lse, part_o,
-                                            part_ml, err);
-    e = cudaGetLastError();
+    e = launch_plain(kern, grid, dim3(kThreads), S::kTotal, st, b, sh.scale,
+                     static_cast<const T*>(q_abs), static_cast<const T*>(cache), idx, n_sel,
+                     sh.index_row_width(), rps, n_split, out, lse, part_o, part_ml, err);
     if (e != cudaSuccess || n_split == 1) return e;
     return launch_merge_splits(b.n_q, n_split, part_o, part_ml, out, lse, st);
 }
