@@ -152,8 +152,8 @@ unsigned char* bytes(void* p) { return static_cast<unsigned char*>(p); }
 // descending score order.
 cudaError_t enqueue_index_select(const Shape& sh, const BatchDev& b, const StepLayout& lay,
                                  void* ws, const void* q_idx, const float* w, const void* k_idx,
-                                 int32_t* idx, int32_t* n_sel, cudaStream_t st,
-                                 const char** what) {
+                                 int32_t* idx, int32_t* n_sel, const void* cache,
+                                 cudaStream_t st, const char** what) {
     int32_t* err = static_cast<int32_t*>(ws);
     float* scores = reinterpret_cast<float*>(bytes(ws) + lay.scores);
     const int64_t ld = default_ld(sh, b);
@@ -162,6 +162,7 @@ cudaError_t enqueue_index_select(const Shape& sh, const BatchDev& b, const StepL
         return launch_index_select_fused(sh, b, q_idx, w, k_idx, scores, ld, idx, n_sel,
                                          bytes(ws) + lay.sel,
                                          reinterpret_cast<uint32_t*>(bytes(ws) + kWsGridBarOffset),
+                                         cache, (int64_t)sh.width() * (int64_t)sh.elem_bytes(),
                                          err, st);
     }
     *what = "index_scores";
@@ -460,7 +461,8 @@ dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(bytes(ws) + lay.idx);
     int32_t* n_sel = n_sel_out ? n_sel_out : reinterpret_cast<int32_t*>(bytes(ws) + lay.n_sel);
     const char* what = "";
-    cudaError_t e = enqueue_index_select(sh, b, lay, ws, q_idx, w, k_idx, idx, n_sel, st, &what);
+    cudaError_t e = enqueue_index_select(sh, b, lay, ws, q_idx, w, k_idx, idx, n_sel, cache, st,
+                                         &what);
     if (e != cudaSuccess) return cuda_status(e, what);
     // The kernel before the attention is this step's selection, which released
     // its dependents only after waiting for the caller's kernels: the query
@@ -490,7 +492,7 @@ dsa_status dsa_index_select(const dsa_shape* shape, const dsa_batch* batch, cons
     if (b.n_q == 0) return DSA_OK;
     const char* what = "";
     const cudaError_t e = enqueue_index_select(sh, b, lay, ws, q_idx, w, k_idx, idx, n_sel,
-                                               static_cast<cudaStream_t>(stream), &what);
+                                               nullptr, static_cast<cudaStream_t>(stream), &what);
     return cuda_status(e, what);
 }
 

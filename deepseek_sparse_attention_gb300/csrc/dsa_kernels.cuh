@@ -123,7 +123,9 @@ cudaError_t launch_select_order_desc(const Shape& sh, const BatchDev& b, const f
 // index_select_fused_state_bytes() bytes that must be zero before the first
 // launch (each launch leaves them zero); `gbar` two zeroed words for the grid
 // barrier, followed in the header by the wait budget.  DSA_FLAG_TWO_LAUNCH
-// and DSA_FLAG_DESC_ORDER turn the path off.
+// and DSA_FLAG_DESC_ORDER turn the path off.  `cache` (may be null) is the
+// latent cache the step attends over next, rows of `row_bytes`: the rows
+// surely selected are prefetched into L2.
 constexpr int kFusedMaxQ = 16;
 constexpr int kFusedMaxGrid = 256;
 bool index_select_fused_eligible(const Shape& sh, const BatchDev& b);
@@ -131,7 +133,8 @@ size_t index_select_fused_state_bytes();
 cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const void* q_idx,
                                       const float* w, const void* k_idx, float* scores,
                                       int64_t ld, int32_t* idx, int32_t* n_sel, void* state,
-                                      uint32_t* gbar, int32_t* err, cudaStream_t st);
+                                      uint32_t* gbar, const void* cache, int64_t row_bytes,
+                                      int32_t* err, cudaStream_t st);
 
 // Indexer query / key preparation (index_prepare.cu): out[v] = H rope(x[v],
 // pos[v]) for n_vec float32 vectors of 128, rounded to the shape's dtype.

@@ -80,7 +80,8 @@ struct SegState {          // one query's part of this CTA's unit range (48 byte
     int32_t need_eq;       // keys equal to T the query keeps
     int32_t eq;            // keys of this part equal to T
     int32_t c_first;       // first CTA holding keys of the query
-    int32_t pad[3];
+    int32_t pad;
+    int64_t row0;          // the query's first cache row (for prefetches)
 };
 static_assert(sizeof(SegState) == 48, "state layout");
 
@@ -446,7 +447,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                    const float* __restrict__ w, BatchDev bq, int32_t top_k, int32_t kpool,
                    uint32_t* __restrict__ gkeys, int64_t ld, int32_t* __restrict__ idx,
                    int32_t* __restrict__ n_sel, int64_t width, uint32_t* __restrict__ gstate,
-                   int2* __restrict__ gcnt, unsigned long long* gbar, int32_t* err) {
+                   int2* __restrict__ gcnt, unsigned long long* gbar,
+                   const uint8_t* __restrict__ pf_cache, int64_t pf_row_bytes, int32_t* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const int tid = threadIdx.x;
@@ -457,6 +459,41 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     SegState* seg = reinterpret_cast<SegState*>(smem + kOffSeg);
     int* red = reinterpret_cast<int*>(smem + kOffRed);
 
+    // Before the wait for the previous kernel: this CTA's key tiles into L2,
+    // from a plan of the offsets as they read now.  A kernel still running may
+    // be writing them; they only choose what is prefetched, and a prefetch
+    // changes no value any later load returns.  Decode batches (one query per
+    // sequence) only.
+    if (tid < 32 && bq.n_q == bq.n_seq) {
+        int64_t nt = 0, key0 = 0;
+        if (tid < bq.n_q) {
+            const int64_t L = bq.row_off[tid + 1] - bq.row_off[tid];
+            key0 = bq.key_off[tid];
+            const int64_t nk = L > 0 ? L / kpool : 0;
+            nt = nk > 0 && nk <= bq.max_kv_len ? (nk + kTileKeys - 1) / kTileKeys : 0;
+        }
+        int64_t incl = nt;                               // tiles of queries 0..tid
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (tid >= off) incl += y;
+        }
+        const int64_t Us = __shfl_sync(0xffffffffu, incl, 31);
+        const int64_t ub = (int64_t)cta * Us / grid, ue = (int64_t)(cta + 1) * Us / grid;
+        for (int64_t u = ub; u < ue && u < ub + (int64_t)kMaxCtaTiles; ++u) {
+            // the query holding unit u: the lane whose range [incl - nt, incl) has u
+            const unsigned m = __ballot_sync(0xffffffffu, tid < bq.n_q && incl - nt <= u && u < incl);
+            if (m == 0) break;
+            const int src = __ffs(m) - 1;
+            const int64_t k0 = __shfl_sync(0xffffffffu, key0, src);
+            const int64_t first = __shfl_sync(0xffffffffu, incl - nt, src);
+            if (tid == 0) {
+                const int32_t y = (int32_t)(k0 + (u - first) * kTileKeys);
+                tma_prefetch_2d(&tm_k, 0, y);
+                tma_prefetch_2d(&tm_k, 64, y);
+            }
+        }
+    }
     pdl_wait();                               // the inputs of the previous kernels
     // the budget of the waits on other CTAs, from the workspace header (0: default)
     uint64_t budget = *reinterpret_cast<const volatile uint64_t*>(
@@ -519,6 +556,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 // the CTA whose units contain the query's first unit ts[g]:
                 // the smallest c with floor((c + 1) U / grid) > ts[g]
                 S.c_first = (int32_t)(((ts[g] + 1) * grid + U - 1) / U - 1);
+                QueryInfo qi;
+                S.row0 = pf_cache != nullptr && query_info(bq, S.q, qi, err, 6) ? qi.row0 : -1;
                 seg[ns++] = S;
             }
         }
@@ -585,10 +624,16 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const uint32_t b1 = (uint32_t)red[kR0];
         if (tid == 0) { seg[s].prefix = b1; seg[s].above = red[kR1]; }
         // above b1 in the high half, in b1 in the low half (each < 2^16 per CTA)
+        // Keys above b1 are selected whatever the rest of the resolve finds:
+        // their cache rows (a pool's kpool rows) go to L2 now, for the
+        // attention's gather after this launch.
         int packed = 0;
         for (int i = tid; i < S.n; i += kThreads) {
             const uint32_t bin = keys[S.koff + i] >> kShift1;
             packed += bin > b1 ? 0x10000 : (bin == b1 ? 1 : 0);
+            if (bin > b1 && S.row0 >= 0)
+                prefetch_l2_bytes(pf_cache + (S.row0 + (int64_t)(S.t_lo + i) * kpool) * pf_row_bytes,
+                                  (uint32_t)(kpool * pf_row_bytes));
         }
         int tot;
         int pos = block_excl_scan(packed, &tot, red) & 0xffff;
@@ -768,7 +813,8 @@ size_t index_select_fused_state_bytes() {
 cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const void* q_idx,
                                       const float* w, const void* k_idx, float* scores,
                                       int64_t ld, int32_t* idx, int32_t* n_sel, void* state,
-                                      uint32_t* gbar, int32_t* err, cudaStream_t st) {
+                                      uint32_t* gbar, const void* cache, int64_t row_bytes,
+                                      int32_t* err, cudaStream_t st) {
     CUtensorMap tm_k, tm_q;
     if (!make_rows128_map(&tm_k, k_idx, (uint64_t)b.total_keys, kTileKeys) ||
         !make_rows128_map(&tm_q, q_idx, (uint64_t)b.n_q * kIdxHeads, C::N))
@@ -805,7 +851,8 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
         return cudaLaunchKernelEx(&cfg, index_select_fused, tm_k, tm_q, w, b, sh.top_k, sh.kpool,
                                   reinterpret_cast<uint32_t*>(scores), ld, idx, n_sel,
                                   sh.index_row_width(), gstate, gcnt,
-                                  reinterpret_cast<unsigned long long*>(gbar), err);
+                                  reinterpret_cast<unsigned long long*>(gbar),
+                                  static_cast<const uint8_t*>(cache), row_bytes, err);
     };
     if (pdl_ok) {
         e = go(2);

@@ -41,21 +41,21 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kM = 128;                      // output features per tile (MMA M)
 constexpr uint32_t kABytes = kM * 128;       // one k-block of weights: 16 KB
-constexpr int kConv = 192;                   // up: threads splitting o (warps 2-7)
+constexpr int kConv = 320;                   // up: threads splitting o (warps 2-11)
+constexpr int kMaxStages = 8;
+constexpr int kMaxN = 256;
+constexpr int kConvIters = (kMaxN * 8 + kConv - 1) / kConv;   // 16-byte chunks per thread
+constexpr uint32_t kSmemBudget = 200u * 1024u;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-template <int MODE>                          // 0: absorb, 1: up
-struct PCfg {
-    static constexpr int kStages = MODE == 0 ? 3 : 2;
-    // per stage: the weight k-block, then the queries' k-block (up: hi and lo)
-    static uint32_t b_bytes(int n) { return (uint32_t)n * 128u * (MODE == 0 ? 1u : 2u); }
-    static uint32_t stage_bytes(int n) { return kABytes + b_bytes(n); }
-    static uint32_t off_bar(int n) { return kStages * stage_bytes(n); }
-    static uint32_t smem_bytes(int n) { return off_bar(n) + 128 + 1024; }
-};
+// Shared memory per stage: the weight k-block, then the queries' k-block
+// (up: its hi and lo parts).
+__host__ __device__ constexpr uint32_t stage_bytes(int mode, int n) {
+    return kABytes + (uint32_t)n * 128u * (mode == 0 ? 1u : 2u);
+}
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
@@ -63,21 +63,20 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
         const __nv_bfloat16* __restrict__ q_src, const float* __restrict__ o, void* __restrict__ out,
         int32_t n_q, int32_t heads, int32_t N, int32_t n_mblk, int32_t nope, int32_t rope,
-        int32_t kv_lora, int32_t v_dim, int32_t* err) {
-    using C = PCfg<MODE>;
+        int32_t kv_lora, int32_t v_dim, int32_t stages, int32_t* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    const uint32_t stage_bytes = kABytes + (uint32_t)N * 128u * (MODE == 0 ? 1u : 2u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * stage_bytes);
+    const uint32_t sbytes = stage_bytes(MODE, N);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * sbytes);
     uint64_t* full = bars;
-    uint64_t* empty = bars + C::kStages;
-    uint64_t* acc_full = bars + 2 * C::kStages;
+    uint64_t* empty = bars + kMaxStages;
+    uint64_t* acc_full = bars + 2 * kMaxStages;
     uint64_t* drain = acc_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 2);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -88,7 +87,7 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
     while (tmem_cols < (uint32_t)N) tmem_cols <<= 1;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], MODE == 0 ? 1 : 1 + kConv);
             mbar_init(&empty[s], 1);
         }
@@ -115,16 +114,16 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
 
     if (warp == 0) {
         if (lane == 0) {                                           // ---- TMA producer
-            int8_t issued_par[C::kStages];
-            for (int s = 0; s < C::kStages; ++s) issued_par[s] = -1;
+            int8_t issued_par[kMaxStages];
+            for (int s = 0; s < kMaxStages; ++s) issued_par[s] = -1;
             bool ok = true;
             for (int kb = 0; kb < n_kb && ok; ++kb) {
-                const int s = kb % C::kStages;
-                const uint32_t ph = (uint32_t)(kb / C::kStages) & 1u;
+                const int s = kb % stages;
+                const uint32_t ph = (uint32_t)(kb / stages) & 1u;
                 if (*abort_flag) { ok = false; break; }
                 ok = mbar_wait(&empty[s], ph ^ 1u, kWaitNs);
                 if (!ok) break;
-                uint8_t* st = smem + s * stage_bytes;
+                uint8_t* st = smem + s * sbytes;
                 mbar_arrive_expect_tx(&full[s], kABytes + (MODE == 0 ? (uint32_t)N * 128u : 0u));
                 if (MODE == 0) {
                     const int32_t y = h * nope + kb * 64;
@@ -139,7 +138,7 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
             if (!ok) {
                 record_error(err, kDevTimeout, blockIdx.x, /*where=*/30);
                 *abort_flag = 1;
-                for (int s = 0; s < C::kStages; ++s)       // copies in flight land first
+                for (int s = 0; s < kMaxStages; ++s)       // copies in flight land first
                     if (issued_par[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_par[s], 50000000ull);
             }
         }
@@ -149,11 +148,11 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
                                              : idesc_bf16_f32(kM, N);
             bool ok = true;
             for (int kb = 0; kb < n_kb; ++kb) {
-                const int s = kb % C::kStages;
-                const uint32_t ph = (uint32_t)(kb / C::kStages) & 1u;
+                const int s = kb % stages;
+                const uint32_t ph = (uint32_t)(kb / stages) & 1u;
                 if (*abort_flag || !mbar_wait(&full[s], ph, kWaitNs)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t a = smem_u32(smem + s * stage_bytes);
+                const uint32_t a = smem_u32(smem + s * sbytes);
                 const uint32_t b = a + kABytes;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -182,28 +181,40 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
             mbar_wait(drain, 0, 50000000ull);
         }
     } else if (MODE == 1) {                                        // ---- o -> bf16 hi, lo
+        // This thread's 16-byte chunks of a k-block: chunk c = tc + j kConv is
+        // query row c / 8, dims 8 (c % 8) .. + 7; every load of the k-block is
+        // issued before the first conversion.
         const int tc = threadIdx.x - 64;                           // 0 .. kConv-1
         for (int kb = 0; kb < n_kb; ++kb) {
-            const int s = kb % C::kStages;
-            const uint32_t ph = (uint32_t)(kb / C::kStages) & 1u;
+            const int s = kb % stages;
+            const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+            float4 xa[kConvIters], xb[kConvIters];
+#pragma unroll
+            for (int j = 0; j < kConvIters; ++j) {
+                const int c = tc + j * kConv;
+                const int64_t q = q0 + (c >> 3);
+                xa[j] = xb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c < N * 8 && q < n_q) {
+                    const float4* src = reinterpret_cast<const float4*>(
+                        o + (q * heads + h) * (int64_t)kv_lora + kb * 64 + (c & 7) * 8);
+                    xa[j] = __ldg(src);
+                    xb[j] = __ldg(src + 1);
+                }
+            }
             if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, kWaitNs)) {
                 record_error(err, kDevTimeout, blockIdx.x, /*where=*/32);
                 *abort_flag = 1;
                 break;
             }
-            uint8_t* hi = smem + s * stage_bytes + kABytes;
+            uint8_t* hi = smem + s * sbytes + kABytes;
             uint8_t* lo = hi + N * 128;
-            for (int c = tc; c < N * 8; c += kConv) {
+#pragma unroll
+            for (int j = 0; j < kConvIters; ++j) {
+                const int c = tc + j * kConv;
+                if (c >= N * 8) continue;
                 const int n = c >> 3, k8 = c & 7;
-                const int64_t q = q0 + n;
-                float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-                if (q < n_q) {
-                    const float4* src = reinterpret_cast<const float4*>(
-                        o + (q * heads + h) * (int64_t)kv_lora + kb * 64 + k8 * 8);
-                    x0 = __ldg(src);
-                    x1 = __ldg(src + 1);
-                }
-                const float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                const float f[8] = {xa[j].x, xa[j].y, xa[j].z, xa[j].w,
+                                    xb[j].x, xb[j].y, xb[j].z, xb[j].w};
                 uint32_t vh[4], vl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -220,17 +231,32 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
             mbar_arrive(&full[s]);
         }
     } else if (warp < 4 && mb == 0 && rope > 0) {                  // ---- absorb: the rope part
+        // 16-byte chunks: thread t copies chunk t % 8 of queries t / 8 + 8 i,
+        // eight loads in flight before their stores
         const int t = threadIdx.x - 64;                            // 0..63
-        __nv_bfloat16* qa = static_cast<__nv_bfloat16*>(out);
         const int W = kv_lora + rope, Q = nope + rope;
-        for (int n = 0; n < N && t < rope; ++n) {
-            const int64_t q = q0 + n;
-            if (q >= n_q) break;
-            qa[(q * heads + h) * W + kv_lora + t] = q_src[(q * heads + h) * Q + nope + t];
+        const int per_row = rope / 8, rows_per_pass = 64 / per_row;
+        const int k8 = t % per_row;
+        __nv_bfloat16* qa = static_cast<__nv_bfloat16*>(out);
+        for (int n0 = t / per_row; n0 < N; n0 += 8 * rows_per_pass) {
+            uint4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t q = q0 + n0 + i * rows_per_pass;
+                v[i] = make_uint4(0, 0, 0, 0);
+                if (n0 + i * rows_per_pass < N && q < n_q)
+                    v[i] = __ldg(reinterpret_cast<const uint4*>(q_src + (q * heads + h) * Q + nope) + k8);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t q = q0 + n0 + i * rows_per_pass;
+                if (n0 + i * rows_per_pass < N && q < n_q)
+                    reinterpret_cast<uint4*>(qa + (q * heads + h) * W + kv_lora)[k8] = v[i];
+            }
         }
     }
 
-    if (warp >= 4) {                                               // ---- epilogue
+    if (warp >= 4 && warp < 8) {                                   // ---- epilogue
         const bool ok = !*abort_flag && mbar_wait(acc_full, 0, kWaitNs);
         if (!ok) {
             if (lane == 0) record_error(err, kDevTimeout, blockIdx.x, /*where=*/33);
@@ -313,8 +339,14 @@ int query_tile(int32_t n_q) {
 template <int MODE>
 cudaError_t launch_tc(const Shape& sh, int32_t n_q, int32_t nope, int32_t v_dim, const void* q,
                       const void* w, const float* o, void* out, int32_t* err, cudaStream_t st) {
-    using C = PCfg<MODE>;
     const int N = query_tile(n_q);
+    // as many stages as k-blocks when they fit (a decode batch has every
+    // k-block in flight at once), else as many as fit
+    const int n_kb = (MODE == 0 ? nope : sh.kv_lora) / 64;
+    int stages = (int)(kSmemBudget / stage_bytes(MODE, N));
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages > n_kb) stages = n_kb;
+    if (stages < 1) return cudaErrorInvalidConfiguration;
     CUtensorMap tm_w, tm_q;
     if (MODE == 0) {
         const uint64_t wd[2] = {(uint64_t)sh.kv_lora, (uint64_t)sh.heads * nope};
@@ -334,7 +366,7 @@ cudaError_t launch_tc(const Shape& sh, int32_t n_q, int32_t nope, int32_t v_dim,
         tm_q = tm_w;                                   // unused
     }
     const int n_mblk = (MODE == 0 ? sh.kv_lora : v_dim) / kM;
-    const size_t smem = C::smem_bytes(N);
+    const size_t smem = (size_t)stages * stage_bytes(MODE, N) + (2 * kMaxStages + 4) * 8 + 1024;
     auto kern = proj_tc<MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -342,7 +374,7 @@ cudaError_t launch_tc(const Shape& sh, int32_t n_q, int32_t nope, int32_t v_dim,
     return launch_pdl(kern, grid, dim3(kThreads), smem, st, tm_w, tm_q,
                       static_cast<const __nv_bfloat16*>(q), o, out, n_q, (int32_t)sh.heads,
                       (int32_t)N, (int32_t)n_mblk, nope, (int32_t)sh.rope, (int32_t)sh.kv_lora,
-                      v_dim, err);
+                      v_dim, (int32_t)stages, err);
 }
 
 }  // namespace

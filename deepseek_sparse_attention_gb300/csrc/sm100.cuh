@@ -119,6 +119,20 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// L2 prefetches: hints that load nothing into the CTA and change no later
+// load's value (L2 is where the GPU's memory is coherent).  A tile of a
+// tensor map (coordinates outside the tensor are ignored), or `bytes` (a
+// multiple of 16) from a 16-byte-aligned global address.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_bytes(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads of them (a tcgen05.mma operand written with st.shared).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -227,7 +227,7 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
 }
 
 // Log-sum-exp merge of the splits of one query: one CTA per (query, head), four
-// latent columns per thread.  Loads are issued sixteen splits at a time with no
+// latent columns per thread.  Loads are issued 32 splits at a time with no
 // data-dependent branch between them, so a thread waits for one round of
 // memory latency per sixteen splits; a running maximum rescales what is summed
 // so far.  An empty split has m = -inf: weight 0, and its output (never
@@ -237,7 +237,7 @@ merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __r
              float* __restrict__ out, float* __restrict__ lse) {
     asm volatile("griddepcontrol.wait;" ::: "memory");      // the partials must be complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    constexpr int kB = 16;
+    constexpr int kB = 32;
     const int h = blockIdx.x, c4 = threadIdx.x;             // columns 4 c4 .. 4 c4 + 3
     const int64_t q = blockIdx.y;
     const float2* ml = reinterpret_cast<const float2*>(part_ml) + q * n_split * kHeads + h;
