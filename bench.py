@@ -23,6 +23,7 @@ comparison arm.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -555,6 +556,10 @@ class StepBench:
         import torch
 
         dsa, dev = self.dsa, self.dev
+        # Graphs of an earlier workload must not be destroyed while this one is
+        # being captured (destroying a graph is not allowed during a capture):
+        # collect any that are unreachable now.
+        gc.collect()
         for i in range(max(warm, 3)):
             self.launch(i, self.stream)
         torch.cuda.synchronize(dev)
@@ -574,20 +579,30 @@ class StepBench:
             with torch.cuda.graph(g):
                 self.launch(c, torch.cuda.current_stream(dev))
             g_one.append(g)
+        copies = self.copies
 
-        def run_steps(n):
+        def run_steps(n):                            # holds the graphs, not self
             for _ in range(n // G):
                 g_all.replay()
             for i in range(n % G):
-                g_one[i % self.copies].replay()
+                g_one[i % copies].replay()
 
         self.run_steps = run_steps
-        self._graphs = (g_all, g_one)
         run_steps(G)                                 # untimed: the graphs' first replays
         torch.cuda.synchronize(dev)
         if dsa.dsa_check_device_error(self.ws, self.stream) != 0:
             raise RuntimeError(f"device error in the graph warm-up ({self.wl.name})")
         self.launch_mode = f"CUDA graphs of {G} steps (+ single-step graphs for the remainder)"
+
+    def release(self):
+        """Destroys the graphs now (outside any capture) and frees the inputs."""
+        import torch
+
+        torch.cuda.synchronize(self.dev)
+        self.run_steps = None
+        self.d = self.keys = self.caches = None
+        gc.collect()
+        torch.cuda.empty_cache()
 
     def calibrate(self, seconds: float, lo: int = 20, hi: int = 200000) -> int:
         import torch
@@ -652,8 +667,8 @@ def other_config(dsa, name, dev, stream, no_graph, pg, local, world, peaks, peak
            "gpu_launches": sb.plan["kernel_launches"] * steps, "plan": sb.plan, "clocks": clk}
     ent.update(step_metrics(wl, per, world, peaks))
     ent["roofline"] = roofline_of(wl, fused, sel_ms, idx_ms, peaks, peak_src)
+    sb.release()
     del sb
-    torch.cuda.empty_cache()
     ent["projections"] = time_projections(dsa, wl, dev, stream, peaks, peak_src)
     return ent
 
@@ -795,8 +810,9 @@ def run_ours(args):
         # the headline's inputs the CPU baseline reads stay; the rotated copies go
         host_d = {k: d[k] for k in ("q_idx", "w", "q_abs", "k_idx", "cache", "row_off",
                                     "key_off", "q_off")} if not args.no_cpu_baseline else None
-        del sb, keys, caches, d, out, lse, idx, n_sel, ws
-        torch.cuda.empty_cache()
+        del keys, caches, d, out, lse, idx, n_sel, ws
+        sb.release()
+        del sb
         for name in names:
             try:
                 configs[name] = other_config(dsa, name, dev, stream, args.no_graph, pg, local,

@@ -10,7 +10,9 @@
 // One warp per 128-vector, four dimensions per lane, a persistent grid: rope on
 // the lane's two adjacent pairs, then the fast Walsh-Hadamard transform -- two
 // butterfly stages inside the lane, five across lanes by shuffles -- and the
-// 1/sqrt(128) scale.  HBM-bound streaming.  Positions reach 10^6 radians, so
+// 1/sqrt(128) scale.  HBM-bound streaming: a warp loads kUnroll vectors (and
+// their positions) before it transforms the first, to keep enough bytes in
+// flight.  Positions reach 10^6 radians, so
 // the angle is formed in turns with integers: each pair's rate theta_i / 2 pi
 // as a 64-bit binary fraction (once per CTA), times the position, wrapping --
 // the fractional turns exactly, with no double-precision work per element.
@@ -21,6 +23,7 @@ namespace {
 
 constexpr int kDim = 128;
 constexpr int kWarpsPerCta = 8;
+constexpr int kUnroll = 4;
 
 __device__ __forceinline__ void store4(float* p, const float (&e)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(e[0], e[1], e[2], e[3]);
@@ -46,46 +49,63 @@ index_prepare_kernel(int64_t n, const float* __restrict__ x, const int64_t* __re
                                         6.283185307179586, 64));
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int64_t v = (int64_t)blockIdx.x * kWarpsPerCta + warp; v < n;
-         v += (int64_t)gridDim.x * kWarpsPerCta) {
-        const float4 xv = __ldcs(reinterpret_cast<const float4*>(x + v * kDim) + lane);
-        float e[4] = {xv.x, xv.y, xv.z, xv.w};
-        // rope: pairs (4 lane, 4 lane + 1) and (4 lane + 2, 4 lane + 3)
-        if (4 * lane < rope_dims) {
-            const unsigned long long p = (unsigned long long)pos[v];
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
+    for (int64_t vb = (int64_t)blockIdx.x * kWarpsPerCta + warp; vb < n; vb += kUnroll * stride) {
+        float4 xs[kUnroll];
+        unsigned long long ps[kUnroll];
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int i = 2 * lane + k;
-                if (2 * i >= rope_dims) break;
-                // fractional turns of pos * theta_i / 2 pi (the product wraps
-                // modulo 2^64 = whole turns), as a signed fraction in [-1/2, 1/2)
-                const int t32 = (int)(unsigned int)((p * rate[i]) >> 32);
-                float s, c;
-                sincospif(2.0f * ((float)t32 * 2.3283064365386963e-10f), &s, &c);
-                const float x0 = e[2 * k], x1 = e[2 * k + 1];
-                e[2 * k] = x0 * c - x1 * s;
-                e[2 * k + 1] = x0 * s + x1 * c;
+        for (int r = 0; r < kUnroll; ++r) {
+            const int64_t v = vb + r * stride;
+            xs[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            ps[r] = 0;
+            if (v < n) {
+                xs[r] = __ldcs(reinterpret_cast<const float4*>(x + v * kDim) + lane);
+                if (rope_dims > 0) ps[r] = (unsigned long long)pos[v];
             }
         }
-        // Walsh-Hadamard: dimension d = 4 lane + j; the butterfly of bit b maps
-        // the pair (d, d | 2^b) with d's bit clear to (sum, difference)
-        {
-            const float a0 = e[0] + e[1], a1 = e[0] - e[1], a2 = e[2] + e[3], a3 = e[2] - e[3];
-            e[0] = a0 + a2; e[2] = a0 - a2; e[1] = a1 + a3; e[3] = a1 - a3;
-        }
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const bool upper = (lane & m) != 0;
+        for (int r = 0; r < kUnroll; ++r) {
+            const int64_t v = vb + r * stride;
+            if (v >= n) break;
+            const float4 xv = xs[r];
+            float e[4] = {xv.x, xv.y, xv.z, xv.w};
+            // rope: pairs (4 lane, 4 lane + 1) and (4 lane + 2, 4 lane + 3)
+            if (4 * lane < rope_dims) {
+                const unsigned long long p = ps[r];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float o = __shfl_xor_sync(0xffffffffu, e[j], m);
-                e[j] = upper ? o - e[j] : e[j] + o;
+                for (int k = 0; k < 2; ++k) {
+                    const int i = 2 * lane + k;
+                    if (2 * i >= rope_dims) break;
+                    // fractional turns of pos * theta_i / 2 pi (the product wraps
+                    // modulo 2^64 = whole turns), as a signed fraction in [-1/2, 1/2)
+                    const int t32 = (int)(unsigned int)((p * rate[i]) >> 32);
+                    float s, c;
+                    sincospif(2.0f * ((float)t32 * 2.3283064365386963e-10f), &s, &c);
+                    const float x0 = e[2 * k], x1 = e[2 * k + 1];
+                    e[2 * k] = x0 * c - x1 * s;
+                    e[2 * k + 1] = x0 * s + x1 * c;
+                }
             }
-        }
-        const float norm = 0.08838834764831845f;         // 1 / sqrt(128)
+            // Walsh-Hadamard: dimension d = 4 lane + j; the butterfly of bit b maps
+            // the pair (d, d | 2^b) with d's bit clear to (sum, difference)
+            {
+                const float a0 = e[0] + e[1], a1 = e[0] - e[1], a2 = e[2] + e[3], a3 = e[2] - e[3];
+                e[0] = a0 + a2; e[2] = a0 - a2; e[1] = a1 + a3; e[3] = a1 - a3;
+            }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) e[j] *= norm;
-        store4(out + v * kDim + 4 * lane, e);
+            for (int m = 1; m < 32; m <<= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float o = __shfl_xor_sync(0xffffffffu, e[j], m);
+                    e[j] = upper ? o - e[j] : e[j] + o;
+                }
+            }
+            const float norm = 0.08838834764831845f;         // 1 / sqrt(128)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) e[j] *= norm;
+            store4(out + v * kDim + 4 * lane, e);
+        }
     }
 }
 
