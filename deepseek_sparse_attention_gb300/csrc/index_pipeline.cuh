@@ -104,20 +104,23 @@ struct Cursor {
 // every CTA derives the (group, tile) schedule itself into shared memory --
 // groups at kOffPlanG, the exclusive prefix of tiles per group at kOffPlanT --
 // and returns the group count.  A query whose offsets fail the batch checks
-// gets an empty group (nq = 0, no tiles).  Called by every thread.
+// gets an empty group (nq = 0, no tiles).  Called by every thread.  `row0`,
+// when given, receives each query's first cache row (-1 for a failed query).
 template <class C>
 __device__ int64_t local_decode_plan(uint8_t* smem, const BatchDev& bq, int32_t kpool,
-                                     int32_t* err, int32_t where) {
+                                     int32_t* err, int32_t where, int64_t* row0 = nullptr) {
     IdxGroup* gs = reinterpret_cast<IdxGroup*>(smem + C::kOffPlanG);
     int64_t* ts = reinterpret_cast<int64_t*>(smem + C::kOffPlanT);
     if (threadIdx.x < bq.n_q) {
         QueryInfo qi;
         IdxGroup G{0, (int32_t)threadIdx.x, 0, 0, 0};
-        if (query_info(bq, threadIdx.x, qi, err, where)) {
+        const bool ok = query_info(bq, threadIdx.x, qi, err, where);
+        if (ok) {
             G.key0 = qi.key0;
             G.nq = 1;
             G.L_last = (int32_t)qi.L;
         }
+        if (row0 != nullptr) row0[threadIdx.x] = ok ? qi.row0 : -1;
         gs[threadIdx.x] = G;
         ts[threadIdx.x + 1] = G.nq ? (G.L_last / kpool + kTileKeys - 1) / kTileKeys : 0;
     }

@@ -92,10 +92,11 @@ static_assert(sizeof(SegState) == 48, "state layout");
 constexpr uint32_t kOffHist = (C::kOffPlanT + (C::kLocalMaxQ + 1) * 8 + 15) / 16 * 16;
 constexpr uint32_t kOffSeg = kOffHist + kBins1 * 4;
 constexpr uint32_t kOffRed = kOffSeg + kFusedMaxQ * sizeof(SegState);
+constexpr uint32_t kOffRow0 = kOffRed + 256;             // [kFusedMaxQ] int64: first cache rows
 // The CTA's keys, written there by the epilogue when its units fit (a
 // CTA with more units writes them to global memory and reads them back into
 // the ring once scoring is done).
-constexpr uint32_t kOffSKeys = kOffRed + 256;
+constexpr uint32_t kOffSKeys = kOffRow0 + kFusedMaxQ * 8;
 constexpr uint32_t kSKeyTiles = 80;
 constexpr uint32_t kSmemBytes = kOffSKeys + kSKeyTiles * kTileKeys * 4 + 1024;  // + alignment slack
 constexpr uint32_t kOffCandS = C::kOffB - (uint32_t)kCandCap * 8;
@@ -469,6 +470,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         if (tid < bq.n_q) {
             const int64_t L = bq.row_off[tid + 1] - bq.row_off[tid];
             key0 = bq.key_off[tid];
+            // the plan after the wait reads these and the query offsets: into L2
+            prefetch_l2_line(bq.q_off + tid);
             const int64_t nk = L > 0 ? L / kpool : 0;
             nt = nk > 0 && nk <= bq.max_kv_len ? (nk + kTileKeys - 1) / kTileKeys : 0;
         }
@@ -499,7 +502,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     uint64_t budget = *reinterpret_cast<const volatile uint64_t*>(
         reinterpret_cast<const uint8_t*>(err) + kWsWaitBudgetOffset);
     if (budget == 0) budget = kDefaultWaitNs;
-    const int64_t n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/6);
+    int64_t* row0s = reinterpret_cast<int64_t*>(smem + kOffRow0);
+    const int64_t n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/6, row0s);
     const IdxGroup* gs = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
     const int64_t* ts = reinterpret_cast<const int64_t*>(smem + C::kOffPlanT);
     const int64_t U = ts[n_groups];
@@ -556,8 +560,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 // the CTA whose units contain the query's first unit ts[g]:
                 // the smallest c with floor((c + 1) U / grid) > ts[g]
                 S.c_first = (int32_t)(((ts[g] + 1) * grid + U - 1) / U - 1);
-                QueryInfo qi;
-                S.row0 = pf_cache != nullptr && query_info(bq, S.q, qi, err, 6) ? qi.row0 : -1;
+                S.row0 = pf_cache != nullptr ? row0s[S.q] : -1;
                 seg[ns++] = S;
             }
         }

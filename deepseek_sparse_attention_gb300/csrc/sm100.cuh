@@ -132,6 +132,10 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t 
 __device__ __forceinline__ void prefetch_l2_bytes(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
+// The cache line holding `p` (any alignment) into L2.
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
 
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads of them (a tcgen05.mma operand written with st.shared).
