@@ -460,43 +460,6 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     SegState* seg = reinterpret_cast<SegState*>(smem + kOffSeg);
     int* red = reinterpret_cast<int*>(smem + kOffRed);
 
-    // Before the wait for the previous kernel: this CTA's key tiles into L2,
-    // from a plan of the offsets as they read now.  A kernel still running may
-    // be writing them; they only choose what is prefetched, and a prefetch
-    // changes no value any later load returns.  Decode batches (one query per
-    // sequence) only.
-    if (tid < 32 && bq.n_q == bq.n_seq) {
-        int64_t nt = 0, key0 = 0;
-        if (tid < bq.n_q) {
-            const int64_t L = bq.row_off[tid + 1] - bq.row_off[tid];
-            key0 = bq.key_off[tid];
-            // the plan after the wait reads these and the query offsets: into L2
-            prefetch_l2_line(bq.q_off + tid);
-            const int64_t nk = L > 0 ? L / kpool : 0;
-            nt = nk > 0 && nk <= bq.max_kv_len ? (nk + kTileKeys - 1) / kTileKeys : 0;
-        }
-        int64_t incl = nt;                               // tiles of queries 0..tid
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (tid >= off) incl += y;
-        }
-        const int64_t Us = __shfl_sync(0xffffffffu, incl, 31);
-        const int64_t ub = (int64_t)cta * Us / grid, ue = (int64_t)(cta + 1) * Us / grid;
-        for (int64_t u = ub; u < ue && u < ub + (int64_t)kMaxCtaTiles; ++u) {
-            // the query holding unit u: the lane whose range [incl - nt, incl) has u
-            const unsigned m = __ballot_sync(0xffffffffu, tid < bq.n_q && incl - nt <= u && u < incl);
-            if (m == 0) break;
-            const int src = __ffs(m) - 1;
-            const int64_t k0 = __shfl_sync(0xffffffffu, key0, src);
-            const int64_t first = __shfl_sync(0xffffffffu, incl - nt, src);
-            if (tid == 0) {
-                const int32_t y = (int32_t)(k0 + (u - first) * kTileKeys);
-                tma_prefetch_2d(&tm_k, 0, y);
-                tma_prefetch_2d(&tm_k, 64, y);
-            }
-        }
-    }
     pdl_wait();                               // the inputs of the previous kernels
     // the budget of the waits on other CTAs, from the workspace header (0: default)
     uint64_t budget = *reinterpret_cast<const volatile uint64_t*>(

@@ -71,7 +71,10 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t sbytes = stage_bytes(MODE, N);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + stages * sbytes);
+    // barriers after the stages, or after the output staging if that is larger
+    uint32_t pipe = (uint32_t)stages * sbytes;
+    if (pipe < (uint32_t)N * kM * (MODE == 0 ? 2u : 4u)) pipe = (uint32_t)N * kM * (MODE == 0 ? 2u : 4u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pipe);
     uint64_t* full = bars;
     uint64_t* empty = bars + kMaxStages;
     uint64_t* acc_full = bars + 2 * kMaxStages;
@@ -257,13 +260,29 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
     }
 
     if (warp >= 4 && warp < 8) {                                   // ---- epilogue
-        const bool ok = !*abort_flag && mbar_wait(acc_full, 0, kWaitNs);
+        // the four warps agree on whether the accumulator is ready (every one
+        // reaches this reduction), so all or none of them take the barrier below
+        const uint32_t mine = (!*abort_flag && mbar_wait(acc_full, 0, kWaitNs)) ? 1u : 0u;
+        uint32_t all;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, 2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(all)
+            : "r"(mine)
+            : "memory");
+        const bool ok = all != 0;
         if (!ok) {
             if (lane == 0) record_error(err, kDevTimeout, blockIdx.x, /*where=*/33);
         } else {
             tc_fence_after();
+            // The tile [N queries][128 features] (bf16 for absorb, float32 for
+            // up) is staged in the stage memory, free once every MMA is done,
+            // then written in 16-byte pieces: each (query, head) owns 128
+            // consecutive features of the output row.
             const int m = (warp - 4) * 32 + lane;                  // TMEM lane = output feature
             const uint32_t lane_addr = tmem_base + ((uint32_t)((warp - 4) * 32) << 16);
+            constexpr int kEsz = MODE == 0 ? 2 : 4;
+            uint8_t* stg = smem;
             for (int c0 = 0; c0 < N; c0 += 32) {
                 float v[32];
                 if (N - c0 >= 32) {
@@ -276,15 +295,25 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
                 }
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const int64_t q = q0 + c0 + e;
-                    if (c0 + e >= N || q >= n_q) continue;
-                    if (MODE == 0) {
-                        static_cast<__nv_bfloat16*>(out)[(q * heads + h) * (kv_lora + rope) +
-                                                         mb * kM + m] = __float2bfloat16_rn(v[e]);
-                    } else {
-                        static_cast<float*>(out)[(q * heads + h) * v_dim + mb * kM + m] = v[e];
-                    }
+                    const int n = c0 + e;
+                    if (n >= N) continue;
+                    if (MODE == 0)
+                        reinterpret_cast<__nv_bfloat16*>(stg)[n * kM + m] = __float2bfloat16_rn(v[e]);
+                    else
+                        reinterpret_cast<float*>(stg)[n * kM + m] = v[e];
                 }
+            }
+            asm volatile("bar.sync 1, 128;" ::: "memory");         // the four epilogue warps
+            constexpr int kChunks = kM * kEsz / 16;                 // 16-byte pieces per row
+            const int t = threadIdx.x - 128;
+            const int64_t w_out = MODE == 0 ? (int64_t)(kv_lora + rope) : (int64_t)v_dim;
+            uint8_t* dst0 = static_cast<uint8_t*>(out) + (int64_t)mb * kM * kEsz;
+            for (int ch = t; ch < N * kChunks; ch += 128) {
+                const int n = ch / kChunks, c = ch % kChunks;
+                const int64_t q = q0 + n;
+                if (q >= n_q) continue;
+                *reinterpret_cast<uint4*>(dst0 + ((q * heads + h) * w_out) * kEsz + c * 16) =
+                    *reinterpret_cast<const uint4*>(stg + (n * kM) * kEsz + c * 16);
             }
         }
     }
@@ -366,7 +395,11 @@ cudaError_t launch_tc(const Shape& sh, int32_t n_q, int32_t nope, int32_t v_dim,
         tm_q = tm_w;                                   // unused
     }
     const int n_mblk = (MODE == 0 ? sh.kv_lora : v_dim) / kM;
-    const size_t smem = (size_t)stages * stage_bytes(MODE, N) + (2 * kMaxStages + 4) * 8 + 1024;
+    // the pipeline's stages, which the epilogue then reuses to stage the output
+    size_t pipe = (size_t)stages * stage_bytes(MODE, N);
+    const size_t staged = (size_t)N * kM * (MODE == 0 ? 2 : 4);
+    if (pipe < staged) pipe = staged;
+    const size_t smem = pipe + (2 * kMaxStages + 4) * 8 + 1024;
     auto kern = proj_tc<MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

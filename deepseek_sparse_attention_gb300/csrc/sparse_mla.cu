@@ -226,19 +226,22 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
     }
 }
 
-// Log-sum-exp merge of the splits of one query: one CTA per (query, head), four
-// latent columns per thread.  Loads are issued 32 splits at a time with no
+// Log-sum-exp merge of the splits of one query: one CTA per (query, head, a
+// quarter of the latent columns), four columns per thread -- 256 CTAs of a
+// warp each for one query, so that the loads spread over the SMs.  Loads are
+// issued 32 splits at a time with no
 // data-dependent branch between them, so a thread waits for one round of
 // memory latency per sixteen splits; a running maximum rescales what is summed
 // so far.  An empty split has m = -inf: weight 0, and its output (never
 // written) is not used.
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(32)
 merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __restrict__ part_ml,
              float* __restrict__ out, float* __restrict__ lse) {
     asm volatile("griddepcontrol.wait;" ::: "memory");      // the partials must be complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int kB = 32;
-    const int h = blockIdx.x, c4 = threadIdx.x;             // columns 4 c4 .. 4 c4 + 3
+    const int h = blockIdx.x >> 2;
+    const int c4 = (blockIdx.x & 3) * 32 + threadIdx.x;     // columns 4 c4 .. 4 c4 + 3
     const int64_t q = blockIdx.y;
     const float2* ml = reinterpret_cast<const float2*>(part_ml) + q * n_split * kHeads + h;
     const float4* po = reinterpret_cast<const float4*>(part_o) +
@@ -317,7 +320,7 @@ cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, 
 
 cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
                                 const float* part_ml, float* out, float* lse, cudaStream_t st) {
-    return launch_pdl(merge_splits, dim3(kHeads, (unsigned)n_q), dim3(kLatent / 4), 0, st,
+    return launch_pdl(merge_splits, dim3(kHeads * 4, (unsigned)n_q), dim3(kLatent / 16), 0, st,
                       n_split, part_o, part_ml, out, lse);
 }
 
