@@ -546,13 +546,14 @@ class StepBench:
                                  self.d["q_abs"], self.caches[c], self.out, self.lse, self.idx,
                                  self.n_sel, self.ws, st)
 
-    def prepare(self, warm: int):
+    def prepare(self, warm: int, steps: int = None):
         """Warm-up steps, then the CUDA graphs the timed steps replay: a decode
         loop replays its step from graphs (the launches of a step and of
         consecutive steps then overlap through programmatic dependent launch
         without host round trips): one graph of G steps over the input copies
-        in turn, and one single-step graph per copy for the remainder, so that
-        exactly K steps run."""
+        in turn -- all K timed steps when K is known and at most 256 -- and one
+        single-step graph per copy for the remainder, so that exactly K steps
+        run."""
         import torch
 
         dsa, dev = self.dsa, self.dev
@@ -568,7 +569,7 @@ class StepBench:
         if self.no_graph:
             self.run_steps = lambda n: [self.launch(i, self.stream) for i in range(n)]
             return
-        G = self.copies * max(1, 12 // self.copies)
+        G = steps if steps is not None and 0 < steps <= 256 else self.copies * max(1, 48 // self.copies)
         g_all = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g_all):
             for i in range(G):
@@ -701,7 +702,7 @@ def run_ours(args):
     sh, b, d, keys, caches, copies = sb.sh, sb.b, sb.d, sb.keys, sb.caches, sb.copies
     out, lse, idx, n_sel, ws = sb.out, sb.lse, sb.idx, sb.n_sel, sb.ws
     warm = args.warmup if args.warmup is not None else 20
-    sb.prepare(warm)
+    sb.prepare(warm, args.steps)
     launch_mode, plan = sb.launch_mode, sb.plan
     # default step count: about two seconds of timed work
     steps = args.steps if args.steps is not None else sb.calibrate(2.0)

@@ -12,10 +12,13 @@
 // butterfly stages inside the lane, five across lanes by shuffles -- and the
 // 1/sqrt(128) scale.  HBM-bound streaming: a warp loads kUnroll vectors (and
 // their positions) before it transforms the first, to keep enough bytes in
-// flight.  Positions reach 10^6 radians, so
-// the angle is formed in turns with integers: each pair's rate theta_i / 2 pi
-// as a 64-bit binary fraction (once per CTA), times the position, wrapping --
-// the fractional turns exactly, with no double-precision work per element.
+// flight.  Positions reach 10^6 radians, so the angle is formed in turns with
+// integers: each pair's rate theta_i / 2 pi as a 64-bit binary fraction
+// (computed once, on the host, in double precision -- this GPU's double rate
+// is too low to spend on it per CTA), times the position, wrapping -- the
+// fractional turns exactly, with no double-precision work on the device.
+#include <math.h>
+
 #include "dsa_kernels.cuh"
 
 namespace dsa {
@@ -24,6 +27,12 @@ namespace {
 constexpr int kDim = 128;
 constexpr int kWarpsPerCta = 8;
 constexpr int kUnroll = 4;
+
+// Turns per position of pair i: base^(-2i / rope_dims) / (2 pi) < 1, as a
+// 64-bit binary fraction.
+struct RopeRates {
+    unsigned long long r[kDim / 2];
+};
 
 __device__ __forceinline__ void store4(float* p, const float (&e)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(e[0], e[1], e[2], e[3]);
@@ -40,14 +49,9 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&e)[4]) {
 template <typename T>
 __global__ void __launch_bounds__(32 * kWarpsPerCta)
 index_prepare_kernel(int64_t n, const float* __restrict__ x, const int64_t* __restrict__ pos,
-                     int32_t rope_dims, double base, T* __restrict__ out) {
-    // turns per position of pair i: base^(-2i / rope_dims) / (2 pi) < 1, as a
-    // 64-bit fraction (the double's 53 bits, then exact integer products)
-    __shared__ unsigned long long rate[kDim / 2];
-    for (int i = threadIdx.x; i < rope_dims / 2; i += blockDim.x)
-        rate[i] = __double2ull_rn(ldexp(pow(base, -2.0 * i / (double)rope_dims) /
-                                        6.283185307179586, 64));
-    __syncthreads();
+                     int32_t rope_dims, const __grid_constant__ RopeRates rates,
+                     T* __restrict__ out) {
+    const unsigned long long* rate = rates.r;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
     for (int64_t vb = (int64_t)blockIdx.x * kWarpsPerCta + warp; vb < n; vb += kUnroll * stride) {
@@ -119,13 +123,19 @@ cudaError_t launch_index_prepare(const Shape& sh, int64_t n_vec, const float* x,
     // rates once and walks vectors
     int64_t blocks = (n_vec + kWarpsPerCta - 1) / kWarpsPerCta;
     if (blocks > (int64_t)sm_count() * 8) blocks = (int64_t)sm_count() * 8;
+    // the 64-bit fraction of pos * theta_i / 2 pi per unit position: the
+    // double rounded to the nearest integer multiple of 2^-64
+    RopeRates rates{};
+    for (int i = 0; i < rope_dims / 2; ++i)
+        rates.r[i] = (unsigned long long)nearbyint(
+            ldexp(pow(base, -2.0 * i / (double)rope_dims) / 6.283185307179586, 64));
     if (sh.dtype == DSA_BF16)
         return launch_plain(index_prepare_kernel<__nv_bfloat16>, dim3((unsigned)blocks),
-                            dim3(32 * kWarpsPerCta), 0, st, n_vec, x, pos, rope_dims, base,
+                            dim3(32 * kWarpsPerCta), 0, st, n_vec, x, pos, rope_dims, rates,
                             static_cast<__nv_bfloat16*>(out));
     else
         return launch_plain(index_prepare_kernel<float>, dim3((unsigned)blocks),
-                            dim3(32 * kWarpsPerCta), 0, st, n_vec, x, pos, rope_dims, base,
+                            dim3(32 * kWarpsPerCta), 0, st, n_vec, x, pos, rope_dims, rates,
                             static_cast<float*>(out));
 }
 

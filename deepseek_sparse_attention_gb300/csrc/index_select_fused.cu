@@ -93,10 +93,12 @@ constexpr uint32_t kOffHist = (C::kOffPlanT + (C::kLocalMaxQ + 1) * 8 + 15) / 16
 constexpr uint32_t kOffSeg = kOffHist + kBins1 * 4;
 constexpr uint32_t kOffRed = kOffSeg + kFusedMaxQ * sizeof(SegState);
 constexpr uint32_t kOffRow0 = kOffRed + 256;             // [kFusedMaxQ] int64: first cache rows
+constexpr uint32_t kOffSmall = kOffRow0 + kFusedMaxQ * 8;  // [kSmallMax] {key, index}
+constexpr int kSmallMax = 32;
 // The CTA's keys, written there by the epilogue when its units fit (a
 // CTA with more units writes them to global memory and reads them back into
 // the ring once scoring is done).
-constexpr uint32_t kOffSKeys = kOffRow0 + kFusedMaxQ * 8;
+constexpr uint32_t kOffSKeys = kOffSmall + kSmallMax * 8;
 constexpr uint32_t kSKeyTiles = 80;
 constexpr uint32_t kSmemBytes = kOffSKeys + kSKeyTiles * kTileKeys * 4 + 1024;  // + alignment slack
 constexpr uint32_t kOffCandS = C::kOffB - (uint32_t)kCandCap * 8;
@@ -115,7 +117,7 @@ static_assert(kMaxCtaTiles >= 128, "room for the keys of a CTA");
 // Scratch words in `red`: [0, kWarps) scans, then named results.
 // [32, 32 + kFusedMaxQ) each query's candidate count.
 enum : int { kR0 = 16, kR1 = 17, kR2 = 18, kR3 = 19, kRFlag = 20, kRNseg = 21, kROver = 22,
-             kRHistQ = 23 };
+             kRHistQ = 23, kRSmallN = 24, kRT = 25, kRTLast = 26 };
 static_assert(32 + kFusedMaxQ <= 64, "scratch words");
 
 // ------------------------------------------------------------ grid barrier
@@ -367,55 +369,79 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
     const uint32_t b2 = (uint32_t)red[kR0];
     const int above2 = red[kR1];
     for (int i = tid; i < kBins2; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    // bits 9..0 of the candidates in (b1, b2)
     const uint32_t pre = (b1 << kBits2) | b2;
+    // The candidates in (b1, b2) -- the keys that agree with T on 22 bits,
+    // usually a handful -- into a small list.  The kept keys are the first
+    // `need` of the query's keys in the order (key descending, index
+    // ascending): above2 of them lie above (b1, b2), so the last kept key is
+    // the (need - above2)-th of the list in that order.  Its key is T and its
+    // index the last one taken at T (every key equal to T is in the list).
+    int2* small = reinterpret_cast<int2*>(reinterpret_cast<uint8_t*>(red) - kOffRed + kOffSmall);
+    if (tid == 0) { red[kRSmallN] = 0; red[kRT] = -1; red[kRTLast] = -1; }
+    __syncthreads();
     for (int i = tid; i < n_cand; i += kThreads) {
-        const uint32_t k = (uint32_t)cand[i].x;
-        if ((k >> kShift2) == pre) atomicAdd(&hist[k & (kBins3 - 1)], 1u);
+        if (((uint32_t)cand[i].x >> kShift2) == pre) {
+            const int slot = atomicAdd(&red[kRSmallN], 1);
+            if (slot < kSmallMax) small[slot] = cand[i];
+        }
     }
     __syncthreads();
-    find_bin<kBins3, false>(hist, need - above2, red);
-    const uint32_t T = (pre << kBits3) | (uint32_t)red[kR0];
-    const int need_eq = need - above2 - red[kR1];      // candidates equal to T that are kept
-    for (int i = tid; i < kBins3; i += kThreads) hist[i] = 0;
-    // Candidates equal to T, and the kept candidates below this part's first
-    // index, assuming every candidate equal to T is kept (packed in one sum:
-    // both are below 2^15); when fewer are kept, the last index taken at T is
-    // the need_eq-th smallest among them (indices are distinct) and the
-    // second count is taken again.
-    int n_eq = 0, before = 0;
-    for (int i = tid; i < n_cand; i += kThreads) {
-        const uint32_t k = (uint32_t)cand[i].x;
-        n_eq += k == T;
-        before += cand[i].y < S.t_lo && k >= T;
-    }
-    {
-        const int packed = block_sum((before << 16) | n_eq, red);
-        n_eq = packed & 0xffff;
-        before = packed >> 16;
-    }
-    int32_t t_last = 0x7fffffff;
-    if (need_eq < n_eq) {
-        if (tid == 0) red[kR0] = -1;
-        __syncthreads();
-        for (int i = tid; i < n_cand; i += kThreads) {
-            if ((uint32_t)cand[i].x != T) continue;
-            const int32_t ti = cand[i].y;
+    const int m = red[kRSmallN];
+    uint32_t T;
+    int32_t t_last;
+    if (m <= kSmallMax) {
+        if (tid < 32) {                               // one warp ranks the list
+            const int2 e = tid < m ? small[tid] : make_int2(0, 0);
+            const uint32_t ek = (uint32_t)e.x;
             int rank = 0;
-            for (int j = 0; j < n_cand; ++j) rank += (uint32_t)cand[j].x == T && cand[j].y < ti;
-            if (rank == need_eq - 1) red[kR0] = ti;
+            for (int j = 0; j < m; ++j) {
+                const uint32_t kj = __shfl_sync(0xffffffffu, ek, j);
+                const int32_t ij = __shfl_sync(0xffffffffu, e.y, j);
+                rank += kj > ek || (kj == ek && ij < e.y);
+            }
+            if (tid < m && rank == need - above2 - 1) { red[kRT] = (int)ek; red[kRTLast] = e.y; }
         }
         __syncthreads();
-        t_last = red[kR0];
-        before = 0;
+        T = (uint32_t)red[kRT];
+        t_last = red[kRTLast];
+    } else {
+        // more than kSmallMax keys share 22 bits (exact ties): bits 9..0 by a
+        // histogram, then the need_eq-th smallest index among the keys at T
         for (int i = tid; i < n_cand; i += kThreads) {
             const uint32_t k = (uint32_t)cand[i].x;
-            const int32_t ti = cand[i].y;
-            before += ti < S.t_lo && (k > T || (k == T && ti <= t_last));
+            if ((k >> kShift2) == pre) atomicAdd(&hist[k & (kBins3 - 1)], 1u);
         }
-        before = block_sum(before, red);
+        __syncthreads();
+        find_bin<kBins3, false>(hist, need - above2, red);
+        T = (pre << kBits3) | (uint32_t)red[kR0];
+        const int need_eq = need - above2 - red[kR1];  // keys equal to T that are kept
+        for (int i = tid; i < kBins3; i += kThreads) hist[i] = 0;
+        int n_eq = 0;
+        for (int i = tid; i < n_cand; i += kThreads) n_eq += (uint32_t)cand[i].x == T;
+        n_eq = block_sum(n_eq, red);
+        t_last = 0x7fffffff;
+        if (need_eq < n_eq) {
+            if (tid == 0) red[kR0] = -1;
+            __syncthreads();
+            for (int i = tid; i < n_cand; i += kThreads) {
+                if ((uint32_t)cand[i].x != T) continue;
+                const int32_t ti = cand[i].y;
+                int rank = 0;
+                for (int j = 0; j < n_cand; ++j) rank += (uint32_t)cand[j].x == T && cand[j].y < ti;
+                if (rank == need_eq - 1) red[kR0] = ti;
+            }
+            __syncthreads();
+            t_last = red[kR0];
+        }
     }
+    // kept candidates before this part's first index: this CTA's offset among them
+    int before = 0;
+    for (int i = tid; i < n_cand; i += kThreads) {
+        const uint32_t k = (uint32_t)cand[i].x;
+        const int32_t ti = cand[i].y;
+        before += ti < S.t_lo && (k > T || (k == T && ti <= t_last));
+    }
+    before = block_sum(before, red);
     if (tid < 32) sum_counts(cl, red);
     __syncthreads();
     const int base = red[kR2] + before;

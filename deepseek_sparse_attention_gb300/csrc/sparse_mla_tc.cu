@@ -657,28 +657,36 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         asm volatile("bar.sync 3, %0;" ::"n"(2 * kSoftmaxThreads) : "memory");
         // O^T lane 32 wq + lane holds latent columns 32 wq + lane + 128 i (an
         // M = 128 accumulator); this thread writes heads hb ..
+        // two latent blocks' TMEM loads in flight per wait
         if (pair) {                                   // staged for the pair merge
 #pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 4; i += 2) {
                 const int c = 32 * wq + lane + kOBlock * i;
-                float v[32];
-                tmem_ld_32cols(lane_addr + kOCol + 64 * i + hb, v);
+                float v[32], u[32];
+                tmem_ld_32cols_x2(lane_addr + kOCol + 64 * i + hb, lane_addr + kOCol + 64 * (i + 1) + hb,
+                                  v, u);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) stage[(hb + e) * kLatent + c] = v[e];
+                for (int e = 0; e < 32; ++e) {
+                    stage[(hb + e) * kLatent + c] = v[e];
+                    stage[(hb + e) * kLatent + c + kOBlock] = u[e];
+                }
             }
         }
         const bool final_out = n_split == 1;
         const int64_t part = q * n_split + split;
         float* dst = final_out ? out + q * kHeads * kLatent : part_o + part * kHeads * kLatent;
 #pragma unroll 1
-        for (int i = 0; i < 4 && !pair; ++i) {
+        for (int i = 0; i < 4 && !pair; i += 2) {
             const int c = 32 * wq + lane + kOBlock * i;
-            float v[32];
-            tmem_ld_32cols(lane_addr + kOCol + 64 * i + hb, v);
+            float v[32], u[32];
+            tmem_ld_32cols_x2(lane_addr + kOCol + 64 * i + hb, lane_addr + kOCol + 64 * (i + 1) + hb,
+                              v, u);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const float l = l_fin[hb + e];
-                dst[(hb + e) * kLatent + c] = final_out ? (l > 0.f ? v[e] / l : 0.f) : v[e];
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                dst[(hb + e) * kLatent + c] = final_out ? v[e] * inv : v[e];
+                dst[(hb + e) * kLatent + c + kOBlock] = final_out ? u[e] * inv : u[e];
             }
         }
         if (head_owner && !pair) {
