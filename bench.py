@@ -375,6 +375,35 @@ def workload_config(wl, world):
 
 # ------------------------------------------------------------------ GPU arm
 
+def graph_time_ms(call, n: int, stream) -> float:
+    """Mean device time of call(i) over n launches: three untimed calls, then
+    the n launches captured in one CUDA graph and replayed (once untimed), so
+    that the per-call host cost of the Python binding -- tens of
+    microseconds, longer than some of these kernels -- does not set the pace."""
+    import torch
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    gc.collect()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    del g
+    gc.collect()
+    return ms
+
+
 def dominant_launch(dsa, wl, sh, b, d, keys, copies, stream, n_rep):
     """The launch that carries the step's dominant work, timed alone with CUDA
     events on the stream it runs on, over the same input rotation: the fused
@@ -385,15 +414,9 @@ def dominant_launch(dsa, wl, sh, b, d, keys, copies, stream, n_rep):
     sb = torch.empty((wl.n_q, max(max(wl.kv_lens) // wl.kpool, 4)), device=keys[0].device)
     ld = sb.shape[1]
     ws_i = dsa.alloc_workspace(sh, b, dsa.OP_INDEX_SCORES, keys[0].device)
-    for i in range(3):
-        dsa.dsa_index_scores(sh, b, d["q_idx"], d["w"], keys[i % copies], sb, ld, ws_i, stream)
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for i in range(n_rep):
-        dsa.dsa_index_scores(sh, b, d["q_idx"], d["w"], keys[i % copies], sb, ld, ws_i, stream)
-    k1.record(stream)
-    torch.cuda.synchronize()
-    idx_ms = k0.elapsed_time(k1) / n_rep
+    idx_ms = graph_time_ms(lambda i: dsa.dsa_index_scores(sh, b, d["q_idx"], d["w"],
+                                                          keys[i % copies], sb, ld, ws_i),
+                           n_rep, stream)
     if dsa.dsa_check_device_error(ws_i, stream) != 0:
         raise RuntimeError("device error in the indexer loop")
     del sb
@@ -404,16 +427,10 @@ def dominant_launch(dsa, wl, sh, b, d, keys, copies, stream, n_rep):
         width = dsa.dsa_index_row_width(sh)
         idx_s = torch.empty((wl.n_q, width), dtype=torch.int32, device=keys[0].device)
         nsel_s = torch.empty(wl.n_q, dtype=torch.int32, device=keys[0].device)
-        for i in range(3):
-            dsa.dsa_index_select(sh, b, d["q_idx"], d["w"], keys[i % copies], idx_s, nsel_s, ws_s,
-                                 stream)
-        k0.record(stream)
-        for i in range(n_rep):
-            dsa.dsa_index_select(sh, b, d["q_idx"], d["w"], keys[i % copies], idx_s, nsel_s, ws_s,
-                                 stream)
-        k1.record(stream)
-        torch.cuda.synchronize()
-        sel_ms = k0.elapsed_time(k1) / n_rep
+        sel_ms = graph_time_ms(lambda i: dsa.dsa_index_select(sh, b, d["q_idx"], d["w"],
+                                                              keys[i % copies], idx_s, nsel_s,
+                                                              ws_s),
+                               n_rep, stream)
         if dsa.dsa_check_device_error(ws_s, stream) != 0:
             raise RuntimeError("device error in the fused selection loop")
     return fused, sel_ms, idx_ms
@@ -471,24 +488,16 @@ def time_projections(dsa, wl, dev, stream, peaks, peak_src, n_rep=50):
     q_abs = torch.empty((wl.n_q, wl.heads, wl.kv_lora + wl.rope), dtype=p["q_full"].dtype,
                         device=dev)
     out = torch.empty((wl.n_q, wl.heads, v_dim), device=dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     res = {}
     for name in ("absorb_q", "up_project"):
         def call(i):
             if name == "absorb_q":
-                dsa.dsa_absorb_q(sh, p["q_full"], p["w_uk_copies"][i % copies], q_abs, ws, stream)
+                dsa.dsa_absorb_q(sh, p["q_full"], p["w_uk_copies"][i % copies], q_abs, ws)
             else:
-                dsa.dsa_up_project(sh, p["o"], p["w_uv_copies"][i % copies], out, ws, stream)
-        for i in range(3):
-            call(i)
-        e0.record(stream)
-        for i in range(n_rep):
-            call(i)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+                dsa.dsa_up_project(sh, p["o"], p["w_uv_copies"][i % copies], out, ws)
+        ms = graph_time_ms(call, n_rep, stream)
         if dsa.dsa_check_device_error(ws, stream) != 0:
             raise RuntimeError(f"device error in the {name} loop")
-        ms = e0.elapsed_time(e1) / n_rep
         if name == "absorb_q":
             byts = (wl.heads * nope * wl.kv_lora * esz + p["q_full"].numel() * esz
                     + q_abs.numel() * esz)
@@ -711,8 +720,6 @@ def run_ours(args):
 
     fused, sel_ms, idx_ms = dominant_launch(dsa, wl, sh, b, d, keys, copies, stream,
                                             max(10, min(steps, 2000)))
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
     # k-pool workloads: the pool-key compression of every pool of the
     # workload's sequences (q_len = kv_len: a prefill's worth of cells, seeded
     # synthetic [key | gate] cells and slot embedding), timed alone
@@ -726,17 +733,10 @@ def run_ours(args):
         bp = dsa.make_batch(d["row_off"], d["key_off"], d["row_off"], n_rows, max(wl.kv_lens),
                             max(wl.kv_lens), n_rows, sum(wl.key_counts()))
         ws_p = dsa.alloc_workspace(sh, bp, dsa.OP_POOL_COMPRESS, dev)
-        for i in range(3):
-            dsa.dsa_pool_compress(sh, bp, cells, pos, pkeys, ws_p, stream)
-        n_pc = 10
-        k0.record(stream)
-        for i in range(n_pc):
-            dsa.dsa_pool_compress(sh, bp, cells, pos, pkeys, ws_p, stream)
-        k1.record(stream)
-        torch.cuda.synchronize(dev)
+        pc_ms = graph_time_ms(lambda i: dsa.dsa_pool_compress(sh, bp, cells, pos, pkeys, ws_p),
+                              10, stream)
         if dsa.dsa_check_device_error(ws_p, stream) != 0:
             raise RuntimeError("device error in the pool compression loop")
-        pc_ms = k0.elapsed_time(k1) / n_pc
         n_pools = sum(L // wl.kpool for L in wl.kv_lens)
         esz = cells.element_size()
         pc_bytes = n_pools * (wl.kpool * 2 * wl.idx_dim + wl.idx_dim) * esz + pos.numel() * 4
@@ -752,23 +752,17 @@ def run_ours(args):
     if wl.kpool == 1:
         gen = torch.Generator(device=dev).manual_seed(wl.seed + 4343)
         n_keys = sum(wl.key_counts())
-        xk = torch.randn((n_keys, wl.idx_dim), generator=gen, device=dev)
+        # three copies of the projections (more than the L2 holds) in turn
+        xks = [torch.randn((n_keys, wl.idx_dim), generator=gen, device=dev) for _ in range(3)]
         pk = torch.cat([torch.arange(L, device=dev, dtype=torch.int64) for L in wl.kv_lens])
         kout = torch.empty_like(keys[0])
-        for i in range(3):
-            dsa.dsa_index_prepare(sh, xk, pk, 64, 8e6, kout, stream)
-        n_pr = 20
-        k0.record(stream)
-        for i in range(n_pr):
-            dsa.dsa_index_prepare(sh, xk, pk, 64, 8e6, kout, stream)
-        k1.record(stream)
-        torch.cuda.synchronize(dev)
-        pr_ms = k0.elapsed_time(k1) / n_pr
+        pr_ms = graph_time_ms(lambda i: dsa.dsa_index_prepare(sh, xks[i % 3], pk, 64, 8e6, kout),
+                              21, stream)
         pr_bytes = n_keys * (wl.idx_dim * 4 + 8 + wl.idx_dim * kout.element_size())
         prep = {"kernel": "index_prepare", "launch_us": pr_ms * 1e3, "vectors": n_keys,
                 "work": "every key of the workload: float32 projection -> rope, Hadamard, dtype",
                 "bytes_per_launch": pr_bytes, "achieved_gbs": pr_bytes / (pr_ms / 1e3) / 1e9}
-        del xk, pk, kout
+        del xks, pk, kout
 
     # end to end through the public call: pinned host inputs in, result out
     e2e = None
