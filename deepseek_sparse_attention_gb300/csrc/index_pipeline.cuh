@@ -133,8 +133,47 @@ __device__ int64_t local_decode_plan(uint8_t* smem, const BatchDev& bq, int32_t 
     return bq.n_q;
 }
 
-// Barrier init, TMEM allocation, the three roles over [u_begin, u_end), and
-// TMEM release.  Called by every thread of the CTA (Cfg::kThreads).
+// Barrier init, TMEM allocation and the tensor maps' prefetch: work local to
+// the CTA that reads no global memory, so a kernel does it before it waits
+// for its predecessor.  Called by every thread; ends with a CTA barrier.
+template <int GQ, int STAGES>
+__device__ void setup(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p) {
+    using C = Cfg<GQ, STAGES>;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::kStages;
+    uint64_t* b_full = bars + 2 * C::kStages;
+    uint64_t* b_empty = b_full + 1;
+    uint64_t* acc_full = b_full + 2;
+    uint64_t* acc_empty = b_full + 4;
+    uint64_t* drain = b_full + 6;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(b_full, 1);
+        mbar_init(b_empty, 1);
+        for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], C::kEpiWarps); }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(tm_k_p);
+        prefetch_tensormap(tm_q_p);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// The three roles over [u_begin, u_end) (possibly empty), then TMEM release.
+// Called by every thread of the CTA (Cfg::kThreads) after setup().
 template <int GQ, int STAGES, class Epi>
 __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p,
                     const IdxGroup* __restrict__ groups, const int64_t* __restrict__ tile_off,
@@ -154,26 +193,6 @@ __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap*
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + C::kOffMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        mbar_init(b_full, 1);
-        mbar_init(b_empty, 1);
-        for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], C::kEpiWarps); }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_mbarrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, C::kTmemCols);
-        tmem_relinquish();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_q);
-    }
-    tc_fence_before();
-    __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 

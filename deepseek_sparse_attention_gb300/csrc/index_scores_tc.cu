@@ -190,6 +190,7 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     pdl_trigger();
+    setup<GQ, C::kStages>(smem, &tm_k, &tm_q);       // local to the CTA: before the wait
     // Everything below reads memory an earlier kernel may write -- the batch
     // offsets, the plan kernel's arrays, the queries and keys the TMA loads --
     // so nothing is read before the previous kernel is complete and visible.
@@ -205,9 +206,7 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int64_t U = tile_off[n_groups];
     const int64_t u_begin = (int64_t)blockIdx.x * U / gridDim.x;
     const int64_t u_end = (int64_t)(blockIdx.x + 1) * U / gridDim.x;
-    if (u_begin >= u_end) return;                    // uniform: no barrier or TMEM touched
-
-    ScoreStore epi{scores, ld};
+    ScoreStore epi{scores, ld};                      // an empty range only releases TMEM
     run<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off, n_groups, u_begin, u_end, w, kpool,
                         epi, err);
 }

@@ -70,7 +70,7 @@ static_assert(kQueryWords % 4 == 0 && kOffCand % 2 == 0, "alignment of the state
 static_assert(kCandSpec % 256 == 0 && kCandSpec <= kCandCap, "speculative candidate reads");
 static_assert(kCandCap < (1 << 15), "two candidate counts share one 32-bit sum");
 
-struct SegState {          // one query's part of this CTA's unit range (48 bytes)
+struct SegState {          // one query's part of this CTA's unit range (64 bytes)
     int32_t q;
     int32_t n;             // keys (tokens or pools) in the part
     int32_t koff;          // first key's slot in shared memory
@@ -80,10 +80,12 @@ struct SegState {          // one query's part of this CTA's unit range (48 byte
     int32_t need_eq;       // keys equal to T the query keeps
     int32_t eq;            // keys of this part equal to T
     int32_t c_first;       // first CTA holding keys of the query
-    int32_t pad;
+    int32_t hot_off;       // first slot of the part's hot list, -1 if it has none
     int64_t row0;          // the query's first cache row (for prefetches)
+    int32_t n_hot;         // entries of the hot list
+    int32_t pad[3];
 };
-static_assert(sizeof(SegState) == 48, "state layout");
+static_assert(sizeof(SegState) == 64, "state layout");
 
 // Shared memory.  Beside the indexer pipeline's layout: a histogram (the
 // epilogue's level-1 counts, later every shared-memory level), per-query state
@@ -117,7 +119,12 @@ static_assert(kMaxCtaTiles >= 128, "room for the keys of a CTA");
 // Scratch words in `red`: [0, kWarps) scans, then named results.
 // [32, 32 + kFusedMaxQ) each query's candidate count.
 enum : int { kR0 = 16, kR1 = 17, kR2 = 18, kR3 = 19, kRFlag = 20, kRNseg = 21, kROver = 22,
-             kRHistQ = 23, kRSmallN = 24, kRT = 25, kRTLast = 26 };
+             kRHistQ = 23, kRSmallN = 24, kRT = 25, kRTLast = 26, kRHotRun = 27 };
+// The hot lists: per part, in index order, the part's keys in or above the
+// threshold bin b1 as {key, index in the part} -- every key the selection can
+// take -- at the start of the ring, which holds no keys when they went straight
+// to shared memory (below the staged candidates).
+constexpr int kHotCap = (int)(kOffCandS / 8);
 static_assert(32 + kFusedMaxQ <= 64, "scratch words");
 
 // ------------------------------------------------------------ grid barrier
@@ -336,6 +343,31 @@ __device__ void emit_part(const SegState& S, const uint32_t* keys, uint32_t T, i
     }
 }
 
+// Writes this CTA's selections of one query from the part's hot list (every
+// key in or above the threshold bin, in index order): keys above T and keys
+// equal to T at index <= t_last, in ascending order from position `base`.
+// One block scan per kThreads entries (a few hundred keys out of thousands).
+__device__ void emit_hot(const SegState& S, const int2* hot, uint32_t T, int base, int32_t t_last,
+                         int keep, int kpool, int32_t* out, int* red) {
+    for (int c0 = 0; c0 < S.n_hot; c0 += kThreads) {
+        const int i = c0 + threadIdx.x;
+        int2 e = make_int2(0, 0);
+        bool sel = false;
+        if (i < S.n_hot) {
+            e = hot[S.hot_off + i];
+            const uint32_t x = (uint32_t)e.x;
+            sel = x > T || (x == T && S.t_lo + e.y <= t_last);
+        }
+        int tot;
+        const int off = block_excl_scan(sel ? 1 : 0, &tot, red);
+        // positions stay below keep when the counts are consistent; the check
+        // keeps a corrupted state from writing past the row
+        if (sel && (unsigned)(base + off) < (unsigned)keep)
+            put(out, base + off, (int64_t)S.t_lo + e.y, kpool);
+        base += tot;
+    }
+}
+
 // Resolves one query from its candidate list (all keys in bin b1, staged in
 // shared memory as {key, index}): T, the last index taken at T, and this CTA's
 // output offset; then emits.  `need` = keep - (keys above b1); n_cand <= kCandCap.
@@ -345,7 +377,8 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
                                         const int2* __restrict__ gcnt_q, int n_cand, int staged,
                                         CountLoads& cl, bool counts_loaded, int need,
                                         uint32_t b1, const uint32_t* keys, uint32_t* hist, int2* cand,
-                                        int keep, int kpool, int32_t* out, int* red) {
+                                        const int2* hot, int keep, int kpool, int32_t* out,
+                                        int* red) {
     const int tid = threadIdx.x;
     if (tid < 32 && !counts_loaded) load_counts(gcnt_q, S.c_first, cl);
     const int2* src = reinterpret_cast<const int2*>(gsq + kOffCand);
@@ -445,7 +478,8 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
     if (tid < 32) sum_counts(cl, red);
     __syncthreads();
     const int base = red[kR2] + before;
-    emit_part(S, keys, T, base, t_last, false, 0, keep, kpool, out, red);
+    if (S.hot_off >= 0) emit_hot(S, hot, T, base, t_last, keep, kpool, out, red);
+    else emit_part(S, keys, T, base, t_last, false, 0, keep, kpool, out, red);
 }
 
 // The epilogue policy: each score as its order-preserving key into the
@@ -486,6 +520,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     SegState* seg = reinterpret_cast<SegState*>(smem + kOffSeg);
     int* red = reinterpret_cast<int*>(smem + kOffRed);
 
+    setup<1, C::kStages>(smem, &tm_k, &tm_q);  // local to the CTA: before the wait
     pdl_wait();                               // the inputs of the previous kernels
     // the budget of the waits on other CTAs, from the workspace header (0: default)
     uint64_t budget = *reinterpret_cast<const volatile uint64_t*>(
@@ -518,9 +553,10 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     __syncthreads();
 
     // ---- scores of this CTA's units (keys to global, level-1 counts of hist_q)
-    if (u_begin < u_end && fits) {
+    {                                         // an empty range only releases TMEM
         KeyStore epi{gkeys, ld, direct ? keys : nullptr, u_begin, hist, red[kRHistQ]};
-        run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_end, w, kpool, epi, err);
+        run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin,
+                           u_begin < u_end && fits ? u_end : u_begin, w, kpool, epi, err);
     }
     fence_proxy_async_smem();                 // the ring is reused by generic accesses
 
@@ -608,42 +644,59 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
     if (!grid_barrier(gbar, red, err, 61, budget)) return;
 
-    // ---- b1; counts above it; candidates in it
+    // ---- b1; counts above it; candidates in it; the hot lists
+    if (tid == 0) red[kRHotRun] = 0;
+    int2* hot = reinterpret_cast<int2*>(smem);
     for (int s = 0; s < nseg; ++s) {
         const SegState S = seg[s];          // read before the helpers' barriers
         uint32_t* gsq = gstate + (int64_t)S.q * kQueryWords;
         find_bin<kBins1, true>(gsq + kOffH1, keep, red);
         const uint32_t b1 = (uint32_t)red[kR0];
         if (tid == 0) { seg[s].prefix = b1; seg[s].above = red[kR1]; }
-        // above b1 in the high half, in b1 in the low half (each < 2^16 per CTA)
-        // Keys above b1 are selected whatever the rest of the resolve finds:
-        // their cache rows (a pool's kpool rows) go to L2 now, for the
-        // attention's gather after this launch.
-        int packed = 0;
-        for (int i = tid; i < S.n; i += kThreads) {
-            const uint32_t bin = keys[S.koff + i] >> kShift1;
-            packed += bin > b1 ? 0x10000 : (bin == b1 ? 1 : 0);
+        // Pass 1 over this thread's contiguous run of the part (thread order is
+        // index order): keys above b1 and in b1.  Keys above b1 are selected
+        // whatever the rest of the resolve finds: their cache rows (a pool's
+        // kpool rows) go to L2 now, for the attention's gather after this launch.
+        const int per = (S.n + kThreads - 1) / kThreads;
+        const int j_a = tid * per < S.n ? tid * per : S.n;
+        const int j_b = j_a + per < S.n ? j_a + per : S.n;
+        int n_above = 0, n_in = 0;
+        for (int j = j_a; j < j_b; ++j) {
+            const uint32_t bin = keys[S.koff + j] >> kShift1;
+            n_above += bin > b1;
+            n_in += bin == b1;
             if (bin > b1 && S.row0 >= 0)
-                prefetch_l2_bytes(pf_cache + (S.row0 + (int64_t)(S.t_lo + i) * kpool) * pf_row_bytes,
+                prefetch_l2_bytes(pf_cache + (S.row0 + (int64_t)(S.t_lo + j) * kpool) * pf_row_bytes,
                                   (uint32_t)(kpool * pf_row_bytes));
         }
+        // above in the high half, in b1 in the low half (each < 2^16 per CTA)
         int tot;
-        int pos = block_excl_scan(packed, &tot, red) & 0xffff;
-        int nc = packed & 0xffff;
+        const int excl = block_excl_scan((n_above << 16) | n_in, &tot, red);
         if (tid == 0) {
-            const int n_in = tot & 0xffff;
-            red[kR2] = n_in ? (int)atomicAdd(gsq + kOffCandN, (uint32_t)n_in) : 0;
+            const int n_in_all = tot & 0xffff, n_hot = (tot >> 16) + n_in_all;
+            red[kR2] = n_in_all ? (int)atomicAdd(gsq + kOffCandN, (uint32_t)n_in_all) : 0;
             gcnt[(int64_t)S.q * kFusedMaxGrid + cta] = make_int2(tot >> 16, 0);
+            const int run = red[kRHotRun];
+            const bool room = direct && run + n_hot <= kHotCap;
+            seg[s].hot_off = room ? run : -1;
+            seg[s].n_hot = n_hot;
+            if (room) red[kRHotRun] = run + n_hot;
         }
         __syncthreads();
-        pos += red[kR2];
-        int2* dst = reinterpret_cast<int2*>(gsq + kOffCand);
-        for (int i = tid; i < S.n && nc > 0; i += kThreads) {
-            const uint32_t k = keys[S.koff + i];
-            if ((k >> kShift1) == b1) {
-                if (pos < kCandCap) dst[pos] = make_int2((int)k, S.t_lo + i);
-                ++pos;
-                --nc;
+        // Pass 2: the hot list and this CTA's candidates in the global list
+        if (n_above + n_in > 0) {
+            int cpos = red[kR2] + (excl & 0xffff);
+            int hpos = seg[s].hot_off >= 0 ? seg[s].hot_off + (excl >> 16) + (excl & 0xffff) : -1;
+            int2* dst = reinterpret_cast<int2*>(gsq + kOffCand);
+            for (int j = j_a; j < j_b; ++j) {
+                const uint32_t k = keys[S.koff + j];
+                const uint32_t bin = k >> kShift1;
+                if (bin < b1) continue;
+                if (hpos >= 0) hot[hpos++] = make_int2((int)k, j);
+                if (bin == b1) {
+                    if (cpos < kCandCap) dst[cpos] = make_int2((int)k, S.t_lo + j);
+                    ++cpos;
+                }
             }
         }
     }
@@ -689,7 +742,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         if (n_cand > kCandCap) continue;
         const int staged = s == 0 ? (n_cand < kCandSpec ? n_cand : kCandSpec) : 0;
         resolve_from_candidates(S, gsq, gcnt + (int64_t)S.q * kFusedMaxGrid, n_cand, staged, cl,
-                                s == 0, keep - S.above, S.prefix, keys, hist, cand, keep, kpool,
+                                s == 0, keep - S.above, S.prefix, keys, hist, cand,
+                                reinterpret_cast<const int2*>(smem), keep, kpool,
                                 idx + (int64_t)S.q * width, red);
     }
     if (!any_over) {

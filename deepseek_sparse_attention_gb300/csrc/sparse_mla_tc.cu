@@ -127,6 +127,12 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t q = blockIdx.y;
     const int split = blockIdx.x;
+    // Two CTAs per split (gridDim.z == 2) share a tile's gather, scores and
+    // softmax -- each computes them -- and divide the value product and the
+    // output by latent half: blocks 2 half and 2 half + 1 of the four.
+    const int half = blockIdx.z;
+    const bool halved = gridDim.z == 2;
+    auto owns = [&](int blk) { return !halved || (blk >> 1) == half; };
     // Two splits of a query launched as a cluster (pair != 0): each stages its
     // unnormalised O as [head][latent] in its own shared memory and its row
     // maxima and sums stay in m_fin / l_fin; then each combines half of the
@@ -250,7 +256,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
             for (int i = threadIdx.x; i < kHeads * kLatent; i += blockDim.x)
                 out[q * kHeads * kLatent + i] = 0.f;
             if (lse != nullptr && threadIdx.x < kHeads) lse[q * kHeads + threadIdx.x] = -INFINITY;
-        } else if (threadIdx.x < kHeads) {            // empty split: weight 0 in the merge,
+        } else if (threadIdx.x < kHeads && half == 0) {  // empty split: weight 0 in the merge,
             const int64_t part = q * n_split + split;  // which then never reads its output
             part_ml[(part * kHeads + threadIdx.x) * 2] = -INFINITY;
             part_ml[(part * kHeads + threadIdx.x) * 2 + 1] = 0.f;
@@ -404,6 +410,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                         const uint32_t p0 = smem_u32(smem + (part == 0 ? C::off_p(bv) : C::kOffPlo));
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
+                            if (!owns(i)) continue;
 #pragma unroll
                             for (int kk = 0; kk < kTileRows / 16; ++kk) {
                                 mma_bf16_ss(tmem_base + kOCol + 64 * i,
@@ -567,6 +574,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 tc_fence_after();
 #pragma unroll 1
                 for (int i = 0; i < 8; ++i) {          // 4 blocks x two halves of the heads
+                    if (!owns(i >> 1)) continue;
                     float v[32];
                     const int hh = 32 * (i & 1);
                     const uint32_t a = lane_addr + kOCol + 64 * (i >> 1) + hh;
@@ -677,6 +685,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
         float* dst = final_out ? out + q * kHeads * kLatent : part_o + part * kHeads * kLatent;
 #pragma unroll 1
         for (int i = 0; i < 4 && !pair; i += 2) {
+            if (!owns(i)) continue;
             const int c = 32 * wq + lane + kOBlock * i;
             float v[32], u[32];
             tmem_ld_32cols_x2(lane_addr + kOCol + 64 * i + hb, lane_addr + kOCol + 64 * (i + 1) + hb,
@@ -689,7 +698,7 @@ sparse_mla_tc(const __grid_constant__ CUtensorMap tm_q, const void* __restrict__
                 dst[(hb + e) * kLatent + c + kOBlock] = final_out ? u[e] * inv : u[e];
             }
         }
-        if (head_owner && !pair) {
+        if (head_owner && !pair && half == 0) {
             const int h = ho;
             const float l = l_fin[h];
             const float m = m_fin[h];
@@ -736,7 +745,11 @@ cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, cons
     if (e != cudaSuccess) return e;
     const int32_t pair = n_split == 2 ? 1 : 0;
     if (!pair) {
-        e = launch_pdl(kern, dim3((unsigned)n_split, (unsigned)b.n_q), dim3(kThreads), C::kSmemBytes,
+        // A launch of few CTAs (decode) doubles them to split the value product
+        // and the output store by latent half, while it still fits one wave.
+        const unsigned halves =
+            n_split > 2 && (int64_t)b.n_q * n_split * 2 <= (int64_t)sm_count() ? 2u : 1u;
+        e = launch_pdl(kern, dim3((unsigned)n_split, (unsigned)b.n_q, halves), dim3(kThreads), C::kSmemBytes,
                        st, tm_q, cache, b, sh.scale, idx, n_sel, sh.index_row_width(), rps, n_split,
                        pair, (int32_t)q_early, out, lse, part_o, part_ml, err);
         if (e != cudaSuccess || n_split == 1) return e;
