@@ -51,7 +51,11 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
 index_prepare_kernel(int64_t n, const float* __restrict__ x, const int64_t* __restrict__ pos,
                      int32_t rope_dims, const __grid_constant__ RopeRates rates,
                      T* __restrict__ out) {
-    const unsigned long long* rate = rates.r;
+    // into shared memory: lanes read different entries, which the parameter
+    // space would serve one address at a time
+    __shared__ unsigned long long rate[kDim / 2];
+    for (int i = threadIdx.x; i < kDim / 2; i += blockDim.x) rate[i] = rates.r[i];
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
     for (int64_t vb = (int64_t)blockIdx.x * kWarpsPerCta + warp; vb < n; vb += kUnroll * stride) {
