@@ -227,34 +227,40 @@ sparse_mla_simt(BatchDev b, float scale, const T* __restrict__ q_abs, const T* _
 }
 
 // Log-sum-exp merge of the splits of one query: one CTA per (query, head, a
-// quarter of the latent columns), four columns per thread -- 256 CTAs of a
-// warp each for one query, so that the loads spread over the SMs.  Loads are
-// issued 32 splits at a time with no
-// data-dependent branch between them, so a thread waits for one round of
-// memory latency per sixteen splits; a running maximum rescales what is summed
-// so far.  An empty split has m = -inf: weight 0, and its output (never
-// written) is not used.
-__global__ void __launch_bounds__(32)
+// quarter of the latent columns): 256 CTAs for one query, spread over the
+// SMs.  Its 128 threads are four groups of 32, each group a quarter of the
+// splits (every split's loads of a group issued at once, eight at a time),
+// four latent columns per thread; each group keeps a running maximum, and the
+// four groups' (maximum, sum, accumulator) are combined in shared memory.  An
+// empty split has m = -inf: weight 0, and its output (never written) is not
+// used.
+__global__ void __launch_bounds__(128)
 merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __restrict__ part_ml,
              float* __restrict__ out, float* __restrict__ lse) {
     asm volatile("griddepcontrol.wait;" ::: "memory");      // the partials must be complete
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    constexpr int kB = 32;
+    constexpr int kB = 8;
+    constexpr int kGroups = 4;
+    __shared__ float4 s_acc[kGroups][32];
+    __shared__ float s_m[kGroups][32], s_l[kGroups][32];
     const int h = blockIdx.x >> 2;
-    const int c4 = (blockIdx.x & 3) * 32 + threadIdx.x;     // columns 4 c4 .. 4 c4 + 3
+    const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+    const int c4 = (blockIdx.x & 3) * 32 + lane;            // columns 4 c4 .. 4 c4 + 3
     const int64_t q = blockIdx.y;
+    const int s_lo = (int)((int64_t)n_split * grp / kGroups);
+    const int s_hi = (int)((int64_t)n_split * (grp + 1) / kGroups);
     const float2* ml = reinterpret_cast<const float2*>(part_ml) + q * n_split * kHeads + h;
     const float4* po = reinterpret_cast<const float4*>(part_o) +
                        (q * n_split * kHeads + h) * (int64_t)(kLatent / 4) + c4;
     const int64_t o_stride = (int64_t)kHeads * (kLatent / 4);   // float4s between splits
     float M = -INFINITY, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < n_split; s0 += kB) {
+    for (int s0 = s_lo; s0 < s_hi; s0 += kB) {
         float2 v[kB];
         float4 o[kB];
 #pragma unroll
         for (int k = 0; k < kB; ++k) {
-            const bool in = s0 + k < n_split;
+            const bool in = s0 + k < s_hi;
             v[k] = in ? __ldg(ml + (int64_t)(s0 + k) * kHeads) : make_float2(-INFINITY, 0.f);
             o[k] = in ? __ldg(po + (int64_t)(s0 + k) * o_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -277,10 +283,33 @@ merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __r
         }
         M = Mb;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
+    s_acc[grp][lane] = acc;
+    s_m[grp][lane] = M;
+    s_l[grp][lane] = L;
+    __syncthreads();
+    if (grp != 0) return;
+    float Mt = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) Mt = fmaxf(Mt, s_m[g][lane]);
+    float Lt = 0.f;
+    float4 at = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (Mt != -INFINITY) {
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            if (s_m[g][lane] == -INFINITY) continue;        // a group without weight
+            const float f = expf(s_m[g][lane] - Mt);
+            const float4 a = s_acc[g][lane];
+            Lt = fmaf(s_l[g][lane], f, Lt);
+            at.x = fmaf(a.x, f, at.x);
+            at.y = fmaf(a.y, f, at.y);
+            at.z = fmaf(a.z, f, at.z);
+            at.w = fmaf(a.w, f, at.w);
+        }
+    }
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
     reinterpret_cast<float4*>(out)[(q * kHeads + h) * (int64_t)(kLatent / 4) + c4] =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (lse != nullptr && c4 == 0) lse[q * kHeads + h] = L > 0.f ? M + logf(L) : -INFINITY;
+        make_float4(at.x * inv, at.y * inv, at.z * inv, at.w * inv);
+    if (lse != nullptr && c4 == 0) lse[q * kHeads + h] = Lt > 0.f ? Mt + logf(Lt) : -INFINITY;
 }
 
 // Rows per split: enough CTAs to fill the GPU about twice, at least 64 rows each.
@@ -320,7 +349,7 @@ cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, 
 
 cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
                                 const float* part_ml, float* out, float* lse, cudaStream_t st) {
-    return launch_pdl(merge_splits, dim3(kHeads * 4, (unsigned)n_q), dim3(kLatent / 16), 0, st,
+    return launch_pdl(merge_splits, dim3(kHeads * 4, (unsigned)n_q), dim3(128), 0, st,
                       n_split, part_o, part_ml, out, lse);
 }
 
