@@ -66,6 +66,9 @@ dsa_status noalloc_scratch(void** out);
 // Streaming multiprocessors of the current device (index_scores_tc.cu); grid
 // and wave sizes derive from it.
 int sm_count();
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) of `func` on the current
+// device unless a limit at least as large was set there before.
+cudaError_t ensure_dyn_smem(const void* func, int bytes);
 
 // A tiled TMA descriptor over a bfloat16 tensor of `rank` dimensions, the
 // innermost first: dims[rank] in elements, strides[rank - 1] the byte strides
@@ -172,8 +175,10 @@ size_t sparse_mla_scratch_bytes(const Shape& sh, const BatchDev& b);
 cudaError_t launch_merge_splits(int32_t n_q, int32_t n_split, const float* part_o,
                                 const float* part_ml, float* out, float* lse, cudaStream_t st);
 bool sparse_mla_tc_eligible(const Shape& sh, const BatchDev& b);
-void plan_attention_splits_tc(int32_t n_q, int64_t max_rows, int32_t* rows_per_split,
-                              int32_t* n_split);
+// Splits of whole row tiles sized by main_rows; rows past them (up to
+// max_rows) go to further splits of the same size.
+void plan_attention_splits_tc(int32_t n_q, int64_t main_rows, int64_t max_rows,
+                              int32_t* rows_per_split, int32_t* n_split);
 cudaError_t launch_sparse_mla_tc(const Shape& sh, const BatchDev& b, const void* q_abs,
                                  const void* cache, const int32_t* idx, const int32_t* n_sel,
                                  float* out, float* lse, float* part_o, float* part_ml,

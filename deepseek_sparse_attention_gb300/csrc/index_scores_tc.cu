@@ -22,6 +22,9 @@
 // Decode streams every key once from HBM and is bound by HBM bandwidth; a
 // prefill chunk re-reads each key tile for every query group (from L2) and is
 // bound by the tensor pipe.
+#include <atomic>
+#include <mutex>
+
 #include "index_pipeline.cuh"
 
 namespace dsa {
@@ -80,12 +83,48 @@ bool encode_bf16_map(CUtensorMap* m, const void* base, int rank, const uint64_t*
            CUDA_SUCCESS;
 }
 
+// Host-side per-device facts, looked up once: a decode step is launched
+// thousands of times a second and each driver query costs host time.
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+struct SmemLimit {                       // the largest limit set so far, per (kernel, device)
+    const void* func;
+    int dev;
+    int bytes;
+};
+std::mutex g_smem_mu;
+SmemLimit g_smem[256];
+int g_smem_n = 0;
+}  // namespace
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < kMaxDevices) {
+        n = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (n > 0) return n;
+    }
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         return 148;
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
     return n;
+}
+
+cudaError_t ensure_dyn_smem(const void* func, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    int i = 0;
+    while (i < g_smem_n && !(g_smem[i].func == func && g_smem[i].dev == dev)) ++i;
+    if (i < g_smem_n && g_smem[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (i < g_smem_n) g_smem[i].bytes = bytes;
+    else if (g_smem_n < 256) g_smem[g_smem_n++] = SmemLimit{func, dev, bytes};
+    return cudaSuccess;
 }
 
 namespace {
@@ -139,7 +178,16 @@ idx_group_plan(BatchDev b, int32_t gq, int64_t* seq_goff, IdxGroup* groups, int6
     if (threadIdx.x == 0) seq_goff[0] = 0;
     __syncthreads();
     block_inclusive_scan(seq_goff + 1, b.n_seq, warp_tot);
-    for (int s = threadIdx.x; s < b.n_seq; s += blockDim.x) {
+    // one thread per group (a prefill chunk is one sequence of many groups):
+    // its sequence by binary search over the group offsets
+    const int64_t n_groups = seq_goff[b.n_seq];
+    for (int64_t g = threadIdx.x; g < n_groups; g += blockDim.x) {
+        int lo = 0, hi = b.n_seq - 1;                 // last s with seq_goff[s] <= g
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (seq_goff[mid] <= g) lo = mid; else hi = mid - 1;
+        }
+        const int s = lo;
         const int64_t q0 = b.q_off[s], q_len = b.q_off[s + 1] - q0;
         const int64_t r0 = b.row_off[s], kv_len = b.row_off[s + 1] - r0;
         const int64_t k0 = b.key_off[s], n_keys_seq = b.key_off[s + 1] - k0;
@@ -147,23 +195,22 @@ idx_group_plan(BatchDev b, int32_t gq, int64_t* seq_goff, IdxGroup* groups, int6
                         b.row_off[s + 1] <= b.total_rows && k0 >= 0 &&
                         n_keys_seq >= kv_len / b.kpool && b.key_off[s + 1] <= b.total_keys &&
                         q0 >= 0 && b.q_off[s + 1] <= b.n_q;
-        if (!ok && q_len > 0) record_error(err, kDevBadBatch, s, /*where=*/4);
-        int64_t g = seq_goff[s];
-        for (int64_t j = 0; j < q_len; j += gq, ++g) {
-            IdxGroup G;
-            G.key0 = k0;
-            G.q0 = (int32_t)(q0 + j);
-            G.nq = ok ? (int32_t)(q_len - j < gq ? q_len - j : gq) : 0;
-            G.L_last = ok ? (int32_t)(kv_len - q_len + j + G.nq) : 0;
-            G.pad = 0;
-            groups[g] = G;
-            const int64_t nk = G.nq > 0 ? G.L_last / b.kpool : 0;
-            tile_off[g + 1] = (nk + kTileKeys - 1) / kTileKeys;
-        }
+        const int64_t j = (g - seq_goff[s]) * gq;
+        if (!ok && j == 0) record_error(err, kDevBadBatch, s, /*where=*/4);
+        IdxGroup G;
+        G.key0 = k0;
+        G.q0 = (int32_t)(q0 + j);
+        G.nq = ok ? (int32_t)(q_len - j < gq ? q_len - j : gq) : 0;
+        // L_last < 2^31 (max_kv_len is), so 32-bit divisions
+        G.L_last = ok ? (int32_t)(kv_len - q_len + j + G.nq) : 0;
+        G.pad = 0;
+        groups[g] = G;
+        const int32_t nk = G.nq > 0 ? G.L_last / b.kpool : 0;
+        tile_off[g + 1] = (nk + kTileKeys - 1) / kTileKeys;
     }
     if (threadIdx.x == 0) tile_off[0] = 0;
     __syncthreads();
-    block_inclusive_scan(tile_off + 1, seq_goff[b.n_seq], warp_tot);
+    block_inclusive_scan(tile_off + 1, n_groups, warp_tot);
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -247,7 +294,7 @@ cudaError_t launch_tc(const Shape& sh, const BatchDev& b, const void* q_idx, con
         if (e != cudaSuccess) return e;
     }
     auto kern = index_scores_tc<GQ>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    e = ensure_dyn_smem((const void*)kern, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(sm_count()), dim3(C::kThreads), C::kSmemBytes, st, tm_k, tm_q, w,
                       (const IdxGroup*)pa.groups, (const int64_t*)pa.tile_off,

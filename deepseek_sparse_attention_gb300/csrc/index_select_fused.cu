@@ -38,6 +38,8 @@
 // histograms are cleared by the launch that used them once every CTA has read
 // them; candidate counters are cleared before the barrier that precedes their
 // first use.  So the state is zero again for the next launch.
+#include <atomic>
+
 #include "index_pipeline.cuh"
 
 namespace dsa {
@@ -136,21 +138,38 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 }
 
 // Every CTA arrives once on a 64-bit counter that only grows; the barrier is
-// complete when the counter reaches the next multiple of the grid size.  One
-// atomic per CTA and acquire loads while waiting, for at most `budget_ns` (the
-// workspace's wait budget): on timeout the error word is set and false
-// returned.  The counter starts at zero and each launch adds a whole number of
-// grid sizes.
-__device__ bool grid_barrier(unsigned long long* bar, int* red, int32_t* err, int32_t where,
-                             uint64_t budget_ns) {
+// complete when the counter reaches the next multiple of the grid size.  The
+// counter starts at zero and each launch adds a whole number of grid sizes, so
+// the value a CTA reads once its launch may start -- earlier launches done,
+// this one's first barrier not yet complete without this CTA -- rounds down to
+// the launch's base.  Thread 0 of each CTA keeps the count that completes its
+// next barrier.
+struct GridBar {
+    unsigned long long* ctr;
+    unsigned long long seen;     // the counter when the launch began (thread 0)
+    unsigned long long next;     // 0 until the first barrier derives it
+    uint64_t budget;             // the workspace's wait budget, 0 = default
+};
+
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Arrival by a releasing reduction (no return trip), then acquire loads while
+// waiting, for at most the wait budget: on timeout the error word is set and
+// false returned.
+__device__ bool grid_barrier(GridBar& gb, int* red, int32_t* err, int32_t where) {
     __syncthreads();
     if (threadIdx.x == 0) {
         int ok = 1;
-        __threadfence();
-        const unsigned long long arrived = atomicAdd(bar, 1ull);
-        const unsigned long long target = (arrived / gridDim.x + 1) * gridDim.x;
+        const unsigned long long g = gridDim.x;
+        if (gb.next == 0) gb.next = gb.seen - gb.seen % g + g;
+        const unsigned long long target = gb.next;
+        gb.next += g;
+        const uint64_t budget_ns = gb.budget != 0 ? gb.budget : kDefaultWaitNs;
+        red_release_add_u64(gb.ctr, 1ull);
         const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_u64(bar) < target) {
+        while (ld_acquire_u64(gb.ctr) < target) {
             if (globaltimer_ns() - t0 > budget_ns) {
                 record_error(err, kDevTimeout, where, 6);
                 ok = 0;
@@ -522,10 +541,14 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
 
     setup<1, C::kStages>(smem, &tm_k, &tm_q);  // local to the CTA: before the wait
     pdl_wait();                               // the inputs of the previous kernels
-    // the budget of the waits on other CTAs, from the workspace header (0: default)
-    uint64_t budget = *reinterpret_cast<const volatile uint64_t*>(
-        reinterpret_cast<const uint8_t*>(err) + kWsWaitBudgetOffset);
-    if (budget == 0) budget = kDefaultWaitNs;
+    // thread 0: the barrier counter's value at the start and the budget of the
+    // waits on other CTAs (workspace header); both first used at barrier 1
+    GridBar gb{gbar, 0, 0, 0};
+    if (tid == 0) {
+        gb.seen = ld_acquire_u64(gbar);
+        gb.budget = *reinterpret_cast<const volatile uint64_t*>(
+            reinterpret_cast<const uint8_t*>(err) + kWsWaitBudgetOffset);
+    }
     int64_t* row0s = reinterpret_cast<int64_t*>(smem + kOffRow0);
     const int64_t n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/6, row0s);
     const IdxGroup* gs = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
@@ -642,7 +665,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         for (int i = tid; i < S.n; i += kThreads) atomicAdd(&hist[keys[S.koff + i] >> kShift1], 1u);
         flush_hist<kBins1>(hist, gstate + (int64_t)S.q * kQueryWords + kOffH1);
     }
-    if (!grid_barrier(gbar, red, err, 61, budget)) return;
+    if (!grid_barrier(gb, red, err, 61)) return;
 
     // ---- b1; counts above it; candidates in it; the hot lists
     if (tid == 0) red[kRHotRun] = 0;
@@ -703,7 +726,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     if (u_begin >= u_end)                   // no units: zero counts for every query
         for (int q = tid; q < bq.n_q; q += kThreads)
             gcnt[(int64_t)q * kFusedMaxGrid + cta] = make_int2(0, 0);
-    if (!grid_barrier(gbar, red, err, 62, budget)) return;
+    if (!grid_barrier(gb, red, err, 62)) return;
     clear_level(gstate, bq.n_q, kOffH1, kBins1);
 
     // ---- one round of loads: every query's candidate count (does any need
@@ -762,7 +785,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         flush_hist<kBins2>(hist, gsq + kOffH2);
     }
-    if (!grid_barrier(gbar, red, err, 63, budget)) return;
+    if (!grid_barrier(gb, red, err, 63)) return;
 
     // ---- bits 9..0 of the keys in (b1, b2)
     for (int s = 0; s < nseg; ++s) {
@@ -778,7 +801,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         flush_hist<kBins3>(hist, gsq + kOffH3);
     }
-    if (!grid_barrier(gbar, red, err, 64, budget)) return;
+    if (!grid_barrier(gb, red, err, 64)) return;
 
     // ---- T exact; this CTA's counts above and at T
     for (int s = 0; s < nseg; ++s) {
@@ -804,7 +827,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         __syncthreads();
     }
-    if (!grid_barrier(gbar, red, err, 65, budget)) return;
+    if (!grid_barrier(gb, red, err, 65)) return;
     clear_level(gstate, bq.n_q, kOffH2, kBins2 + kBins3);
     pdl_trigger();
 
@@ -865,15 +888,22 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
     if (!make_rows128_map(&tm_k, k_idx, (uint64_t)b.total_keys, kTileKeys) ||
         !make_rows128_map(&tm_q, q_idx, (uint64_t)b.n_q * kIdxHeads, C::N))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(index_select_fused,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    cudaError_t e = ensure_dyn_smem((const void*)index_select_fused, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_select_fused, kThreads,
-                                                      kSmemBytes);
+    // one CTA must fit an SM (the cooperative grid is one per SM); checked
+    // once per device
+    static std::atomic<int> fits_sm[64];
+    int dev = 0;
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    if (dev < 0 || dev >= 64 || fits_sm[dev].load(std::memory_order_relaxed) == 0) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_select_fused, kThreads,
+                                                          kSmemBytes);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+        if (dev >= 0 && dev < 64) fits_sm[dev].store(1, std::memory_order_relaxed);
+    }
     uint32_t* gstate = static_cast<uint32_t*>(state);
     int2* gcnt = reinterpret_cast<int2*>(gstate + (size_t)kFusedMaxQ * kQueryWords);
     cudaLaunchConfig_t cfg = {};

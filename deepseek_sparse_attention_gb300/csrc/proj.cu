@@ -401,7 +401,7 @@ cudaError_t launch_tc(const Shape& sh, int32_t n_q, int32_t nope, int32_t v_dim,
     if (pipe < staged) pipe = staged;
     const size_t smem = pipe + (2 * kMaxStages + 4) * 8 + 1024;
     auto kern = proj_tc<MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_dyn_smem((const void*)kern, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(n_mblk * sh.heads), (unsigned)((n_q + N - 1) / N));
     return launch_pdl(kern, grid, dim3(kThreads), smem, st, tm_w, tm_q,

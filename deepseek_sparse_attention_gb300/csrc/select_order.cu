@@ -106,8 +106,7 @@ cudaError_t launch_select_order_desc(const Shape& sh, const BatchDev& b, const f
     int n_pow = 1;
     while (n_pow < units) n_pow <<= 1;
     const size_t smem = (size_t)n_pow * sizeof(unsigned long long);
-    cudaError_t e = cudaFuncSetAttribute(select_order_desc,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_dyn_smem((const void*)select_order_desc, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(select_order_desc, dim3((unsigned)b.n_q), dim3(kThreads), smem, st, b,
                       sh.kpool, scores, ld, idx, n_sel, sh.index_row_width(), n_pow, err);

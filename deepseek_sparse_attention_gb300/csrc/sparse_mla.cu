@@ -334,8 +334,7 @@ cudaError_t launch_typed(const Shape& sh, const BatchDev& b, const void* q_abs, 
                          cudaStream_t st) {
     using S = Smem<T, W>;
     auto kern = sparse_mla_simt<T, W>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)S::kTotal);
+    cudaError_t e = ensure_dyn_smem((const void*)kern, (int)S::kTotal);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)n_split, (unsigned)b.n_q);
     e = launch_plain(kern, grid, dim3(kThreads), S::kTotal, st, b, sh.scale,
@@ -357,11 +356,15 @@ void plan_attention_splits(const Shape& sh, const BatchDev& b, int32_t* rows_per
                            int32_t* n_split) {
     const int32_t n_q = b.n_q > 0 ? b.n_q : 1;
     // rows a query attends over at most: its selection, or every visible row
-    int64_t max_rows = b.max_kv_len;
-    if (!(b.flags & DSA_FLAG_DENSE) && sh.index_row_width() < max_rows)
+    int64_t max_rows = b.max_kv_len, main_rows = max_rows;
+    if (!(b.flags & DSA_FLAG_DENSE) && sh.index_row_width() < max_rows) {
         max_rows = sh.index_row_width();
+        // the k-pool tail (fewer than kpool rows past the selected pools'
+        // top_k rows) sizes no split: it spills into one more, short split
+        main_rows = sh.top_k;
+    }
     if (sparse_mla_tc_eligible(sh, b))
-        plan_attention_splits_tc(n_q, max_rows, rows_per_split, n_split);
+        plan_attention_splits_tc(n_q, main_rows, max_rows, rows_per_split, n_split);
     else
         plan_splits_simt(n_q, max_rows, rows_per_split, n_split);
 }

@@ -740,8 +740,7 @@ cudaError_t launch_w(const Shape& sh, const BatchDev& b, const void* q_abs, cons
     CUtensorMap tm_q;
     if (!make_map(&tm_q, q_abs, (uint64_t)b.n_q * kHeads, W, kHeads)) return cudaErrorInvalidValue;
     auto kern = sparse_mla_tc<W>;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    cudaError_t e = ensure_dyn_smem((const void*)kern, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int32_t pair = n_split == 2 ? 1 : 0;
     if (!pair) {
@@ -790,18 +789,20 @@ bool sparse_mla_tc_eligible(const Shape& sh, const BatchDev& b) {
 // decode queries: 2 splits, 128 CTAs, measured faster than 4 or 5 over two or
 // three waves).  Splits keep two tiles each, except for a lone query, whose
 // latency wants every split it can get.
-void plan_attention_splits_tc(int32_t n_q, int64_t max_rows, int32_t* rows_per_split,
-                              int32_t* n_split) {
+void plan_attention_splits_tc(int32_t n_q, int64_t main_rows, int64_t max_rows,
+                              int32_t* rows_per_split, int32_t* n_split) {
     if (max_rows < 1) max_rows = 1;
-    const int64_t tiles = (max_rows + kTileRows - 1) / kTileRows;
+    if (main_rows < 1 || main_rows > max_rows) main_rows = max_rows;
+    const int64_t tiles = (main_rows + kTileRows - 1) / kTileRows;
     const int64_t sms = sm_count();
     int64_t splits = n_q <= sms ? sms / n_q : 1;
     const int64_t max_splits = (n_q == 1 || tiles < 2) ? tiles : tiles / 2;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
     const int64_t tiles_per = (tiles + splits - 1) / splits;
-    splits = (tiles + tiles_per - 1) / tiles_per;
-    *rows_per_split = (int32_t)(tiles_per * kTileRows);
+    const int64_t rps = tiles_per * kTileRows;
+    splits = (max_rows + rps - 1) / rps;
+    *rows_per_split = (int32_t)rps;
     *n_split = (int32_t)splits;
 }
 

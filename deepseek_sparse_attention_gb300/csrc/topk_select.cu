@@ -467,7 +467,7 @@ cudaError_t launch_topk_select(const Shape& sh, const BatchDev& b, const float* 
     // across the many waves of a prefill chunk.
     auto kern = pair ? topk_select_kernel<2, 1024> : topk_select_kernel<1, 512>;
     const int nt = pair ? 1024 : 512;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_dyn_smem((const void*)kern, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid = pair ? dim3(2, (unsigned)b.n_q) : dim3((unsigned)b.n_q);
     return launch_pdl(kern, grid, dim3(nt), smem, st, b, sh.top_k, sh.kpool, scores, ld, idx,

@@ -359,8 +359,7 @@ cudaError_t launch_topk_select_cluster(const Shape& sh, const BatchDev& b, const
                                        int64_t ld, int32_t* idx, int32_t* n_sel, int32_t* err,
                                        cudaStream_t st) {
     const size_t smem = sizeof(Smem);
-    cudaError_t e = cudaFuncSetAttribute(topk_select_cluster,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_dyn_smem((const void*)topk_select_cluster, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk_select_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;

@@ -230,8 +230,10 @@ def test_index_prepare_rejects_before_enqueue(lib):
     # a prefill chunk: the indexer's group plan and the indexer, the selection,
     # one attention split per query (no merge)
     ("chunked_prefill_4096", 4, 1, 2048),
-    # four 1M-token k-pool decode queries: fused, 11 splits of three tiles, merge
-    ("kpool_nope_1m", 3, 11, 192),
+    # four 1M-token k-pool decode queries: fused, 16 splits of two tiles over
+    # the 2048 rows of the 512 selected pools and one more split for the tail
+    # of up to 3 rows, merge
+    ("kpool_nope_1m", 3, 17, 128),
 ])
 def test_plan_of_the_benchmark_workloads(lib, name, launches, splits, rows_per_split):
     """The host-side plan (launch count, attention splits) of each benchmark
