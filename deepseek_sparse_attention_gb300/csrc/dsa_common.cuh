@@ -22,6 +22,10 @@ constexpr size_t kWsGridBarOffset = 64;
 // CTA on other CTAs (64 bits; 0 = the default of 2 s).
 constexpr size_t kWsWaitBudgetOffset = 128;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+// Byte offset in the header of the count of completed fused selection
+// launches (32 bits): its parity picks the half of the double-buffered
+// per-query state a launch uses.
+constexpr size_t kWsLaunchCountOffset = 192;
 
 enum DeviceError : int32_t {
     kDevOk = 0,

@@ -25,10 +25,13 @@
 //             the query's global histogram;                         barrier 1
 //   bin       every CTA finds the bin b1 that holds the k-th largest key; it
 //             publishes how many of its keys lie above b1 and appends its keys
-//             in b1 -- the candidates, a few hundred per query -- to the
-//             query's global candidate list;                        barrier 2
-//   resolve   every CTA reads the whole candidate list and resolves T and the
-//             last index taken at T exactly, by a radix select in shared memory;
+//             in b1 -- the candidates, a few thousand per query -- to the
+//             query's global candidate list, counting their bits 20..10 in the
+//             query's level-2 histogram of candidates;             barrier 2
+//   resolve   every CTA finds the level-2 bin b2 in that histogram, reads the
+//             whole candidate list and, in one pass, collects the few keys in
+//             (b1, b2) -- ranked by one warp for T and the last index taken at
+//             T -- and counts the kept ones before its part;
 //   emit      a CTA's output offset is the count of selected keys of the CTAs
 //             before it (keys above b1 from the published counts, candidates
 //             from the list); a block scan writes its selections in order.
@@ -36,8 +39,10 @@
 // resolves that query by two more histogram levels (bits 20..10 and 9..0) and a
 // round of per-CTA counts above and at T, three more barriers.  Global
 // histograms are cleared by the launch that used them once every CTA has read
-// them; candidate counters are cleared before the barrier that precedes their
-// first use.  So the state is zero again for the next launch.
+// them, the level-2 histogram of candidates (read after the last barrier) by
+// the next launch, which uses the other of two copies; candidate counters are
+// cleared before the barrier that precedes their first use.  So the state is
+// as the next launch expects it.
 #include <atomic>
 
 #include "index_pipeline.cuh"
@@ -65,7 +70,11 @@ constexpr int kCandSpec = 3072;                       // read before the count i
 constexpr int kOffH1 = 0;
 constexpr int kOffH2 = kOffH1 + kBins1;
 constexpr int kOffH3 = kOffH2 + kBins2;
-constexpr int kOffCandN = kOffH3 + kBins3;           // candidate count (+3 words pad)
+// bits 20..10 of the candidates, counted as they are appended; two copies,
+// the launch count's parity picks one and the launch clears the other (the
+// previous launch's, complete before this one starts)
+constexpr int kOffH2c = kOffH3 + kBins3;
+constexpr int kOffCandN = kOffH2c + 2 * kBins2;     // candidate count (+3 words pad)
 constexpr int kOffCand = kOffCandN + 4;              // kCandCap x {key, index}
 constexpr int kQueryWords = kOffCand + 2 * kCandCap;
 static_assert(kQueryWords % 4 == 0 && kOffCand % 2 == 0, "alignment of the state");
@@ -121,7 +130,8 @@ static_assert(kMaxCtaTiles >= 128, "room for the keys of a CTA");
 // Scratch words in `red`: [0, kWarps) scans, then named results.
 // [32, 32 + kFusedMaxQ) each query's candidate count.
 enum : int { kR0 = 16, kR1 = 17, kR2 = 18, kR3 = 19, kRFlag = 20, kRNseg = 21, kROver = 22,
-             kRHistQ = 23, kRSmallN = 24, kRT = 25, kRTLast = 26, kRHotRun = 27 };
+             kRHistQ = 23, kRSmallN = 24, kRT = 25, kRTLast = 26, kRHotRun = 27,
+             kRSmallBefore = 28, kRPar = 29 };
 // The hot lists: per part, in index order, the part's keys in or above the
 // threshold bin b1 as {key, index in the part} -- every key the selection can
 // take -- at the start of the ring, which holds no keys when they went straight
@@ -391,15 +401,24 @@ __device__ void emit_hot(const SegState& S, const int2* hot, uint32_t T, int bas
 // shared memory as {key, index}): T, the last index taken at T, and this CTA's
 // output offset; then emits.  `need` = keep - (keys above b1); n_cand <= kCandCap.
 // The first `staged` entries of the list and (warp 0) the counts `cl` of the
-// earlier CTAs may already be loaded.
+// earlier CTAs may already be loaded, and the level-2 bin b2 with the count of
+// candidates above it (have_b2) taken from the query's global level-2
+// histogram of its candidates, `h2c`.
 __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
-                                        const int2* __restrict__ gcnt_q, int n_cand, int staged,
-                                        CountLoads& cl, bool counts_loaded, int need,
-                                        uint32_t b1, const uint32_t* keys, uint32_t* hist, int2* cand,
+                                        const uint32_t* h2c, const int2* __restrict__ gcnt_q,
+                                        int n_cand, int staged, CountLoads& cl,
+                                        bool counts_loaded, bool have_b2, uint32_t b2,
+                                        int above2, int need, uint32_t b1,
+                                        const uint32_t* keys, uint32_t* hist, int2* cand,
                                         const int2* hot, int keep, int kpool, int32_t* out,
                                         int* red) {
     const int tid = threadIdx.x;
     if (tid < 32 && !counts_loaded) load_counts(gcnt_q, S.c_first, cl);
+    if (!have_b2) {
+        find_bin<kBins2, true>(h2c, need, red);
+        b2 = (uint32_t)red[kR0];
+        above2 = red[kR1];
+    }
     const int2* src = reinterpret_cast<const int2*>(gsq + kOffCand);
     for (int i0 = staged; i0 < n_cand; i0 += 4 * kThreads) {   // four loads in flight
         int2 v[4];
@@ -412,32 +431,30 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
         for (int k = 0; k < 4; ++k)
             if (i0 + tid + k * kThreads < n_cand) cand[i0 + tid + k * kThreads] = v[k];
     }
+    if (tid == 0) { red[kRSmallN] = 0; red[kRT] = -1; red[kRTLast] = -1; red[kRSmallBefore] = 0; }
     __syncthreads();
-    // bits 20..10
-    for (int i = tid; i < n_cand; i += kThreads)
-        atomicAdd(&hist[((uint32_t)cand[i].x >> kShift2) & (kBins2 - 1)], 1u);
-    __syncthreads();
-    find_bin<kBins2, false>(hist, need, red);
-    const uint32_t b2 = (uint32_t)red[kR0];
-    const int above2 = red[kR1];
-    for (int i = tid; i < kBins2; i += kThreads) hist[i] = 0;
     const uint32_t pre = (b1 << kBits2) | b2;
-    // The candidates in (b1, b2) -- the keys that agree with T on 22 bits,
-    // usually a handful -- into a small list.  The kept keys are the first
-    // `need` of the query's keys in the order (key descending, index
-    // ascending): above2 of them lie above (b1, b2), so the last kept key is
-    // the (need - above2)-th of the list in that order.  Its key is T and its
-    // index the last one taken at T (every key equal to T is in the list).
+    // One pass over the list.  The kept keys are the first `need` of the
+    // query's candidates in the order (key descending, index ascending).  A
+    // candidate above (b1, b2) in its 22 high bits is kept, one below is not;
+    // those in (b1, b2) -- usually a handful -- go to a small list, where the
+    // last kept one is the (need - above2)-th in that order: its key is T and
+    // its index the last one taken at T (every key equal to T is in the list).
+    // The pass also counts the kept candidates above (b1, b2) that come
+    // before this part's first index.
     int2* small = reinterpret_cast<int2*>(reinterpret_cast<uint8_t*>(red) - kOffRed + kOffSmall);
-    if (tid == 0) { red[kRSmallN] = 0; red[kRT] = -1; red[kRTLast] = -1; }
-    __syncthreads();
+    int before = 0;
     for (int i = tid; i < n_cand; i += kThreads) {
-        if (((uint32_t)cand[i].x >> kShift2) == pre) {
+        const int2 e = cand[i];
+        const uint32_t hi = (uint32_t)e.x >> kShift2;
+        if (hi == pre) {
             const int slot = atomicAdd(&red[kRSmallN], 1);
-            if (slot < kSmallMax) small[slot] = cand[i];
+            if (slot < kSmallMax) small[slot] = e;
+        } else {
+            before += hi > pre && e.y < S.t_lo;
         }
     }
-    __syncthreads();
+    before = block_sum(before, red);
     const int m = red[kRSmallN];
     uint32_t T;
     int32_t t_last;
@@ -451,11 +468,24 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
                 const int32_t ij = __shfl_sync(0xffffffffu, e.y, j);
                 rank += kj > ek || (kj == ek && ij < e.y);
             }
-            if (tid < m && rank == need - above2 - 1) { red[kRT] = (int)ek; red[kRTLast] = e.y; }
+            const unsigned who = __ballot_sync(0xffffffffu, tid < m && rank == need - above2 - 1);
+            uint32_t t = 0xffffffffu;
+            int32_t tl = -1;
+            if (who != 0u) {
+                const int w = __ffs(who) - 1;
+                t = __shfl_sync(0xffffffffu, ek, w);
+                tl = __shfl_sync(0xffffffffu, e.y, w);
+            }
+            // kept entries of the small list before this part's first index
+            const bool kept = tid < m && (ek > t || (ek == t && e.y <= tl));
+            const int nb = __popc(__ballot_sync(0xffffffffu, kept && e.y < S.t_lo));
+            if (tid == 0) { red[kRT] = (int)t; red[kRTLast] = tl; red[kRSmallBefore] = nb; }
+            sum_counts(cl, red);
         }
         __syncthreads();
         T = (uint32_t)red[kRT];
         t_last = red[kRTLast];
+        before += red[kRSmallBefore];
     } else {
         // more than kSmallMax keys share 22 bits (exact ties): bits 9..0 by a
         // histogram, then the need_eq-th smallest index among the keys at T
@@ -485,17 +515,17 @@ __device__ void resolve_from_candidates(const SegState& S, const uint32_t* gsq,
             __syncthreads();
             t_last = red[kR0];
         }
+        // kept candidates of the small list's bits before this part's first index
+        int b_eq = 0;
+        for (int i = tid; i < n_cand; i += kThreads) {
+            const uint32_t k = (uint32_t)cand[i].x;
+            const int32_t ti = cand[i].y;
+            b_eq += (k >> kShift2) == pre && ti < S.t_lo && (k > T || (k == T && ti <= t_last));
+        }
+        before += block_sum(b_eq, red);
+        if (tid < 32) sum_counts(cl, red);
+        __syncthreads();
     }
-    // kept candidates before this part's first index: this CTA's offset among them
-    int before = 0;
-    for (int i = tid; i < n_cand; i += kThreads) {
-        const uint32_t k = (uint32_t)cand[i].x;
-        const int32_t ti = cand[i].y;
-        before += ti < S.t_lo && (k > T || (k == T && ti <= t_last));
-    }
-    before = block_sum(before, red);
-    if (tid < 32) sum_counts(cl, red);
-    __syncthreads();
     const int base = red[kR2] + before;
     if (S.hot_off >= 0) emit_hot(S, hot, T, base, t_last, keep, kpool, out, red);
     else emit_part(S, keys, T, base, t_last, false, 0, keep, kpool, out, red);
@@ -544,10 +574,14 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     // thread 0: the barrier counter's value at the start and the budget of the
     // waits on other CTAs (workspace header); both first used at barrier 1
     GridBar gb{gbar, 0, 0, 0};
+    uint32_t* launch_count = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(err) +
+                                                         kWsLaunchCountOffset);
+    uint32_t n_launch = 0;                    // thread 0: first used after scoring
     if (tid == 0) {
         gb.seen = ld_acquire_u64(gbar);
         gb.budget = *reinterpret_cast<const volatile uint64_t*>(
             reinterpret_cast<const uint8_t*>(err) + kWsWaitBudgetOffset);
+        n_launch = *reinterpret_cast<const volatile uint32_t*>(launch_count);
     }
     int64_t* row0s = reinterpret_cast<int64_t*>(smem + kOffRow0);
     const int64_t n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/6, row0s);
@@ -613,6 +647,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             }
         }
         red[kRNseg] = ns;
+        red[kRPar] = (int)(n_launch & 1u);
     }
     // rows one CTA writes whole: failed and dense queries; the tail and the
     // padding of sparse rows (the selected body is written by the emission).
@@ -644,6 +679,9 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
     __syncthreads();
     const int nseg = red[kRNseg];
+    const int par = red[kRPar];
+    // the previous launch's copy, for every query it may have had
+    clear_level(gstate, kFusedMaxQ, kOffH2c + (par ^ 1) * kBins2, kBins2);
 
     // ---- keys back into shared memory (asynchronous copies, 16 bytes each:
     // part starts are tile-aligned and rows padded to 4 keys), level-1 counts
@@ -711,6 +749,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             int cpos = red[kR2] + (excl & 0xffff);
             int hpos = seg[s].hot_off >= 0 ? seg[s].hot_off + (excl >> 16) + (excl & 0xffff) : -1;
             int2* dst = reinterpret_cast<int2*>(gsq + kOffCand);
+            uint32_t* h2c = gsq + kOffH2c + par * kBins2;
             for (int j = j_a; j < j_b; ++j) {
                 const uint32_t k = keys[S.koff + j];
                 const uint32_t bin = k >> kShift1;
@@ -719,6 +758,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 if (bin == b1) {
                     if (cpos < kCandCap) dst[cpos] = make_int2((int)k, S.t_lo + j);
                     ++cpos;
+                    atomicAdd(h2c + ((k >> kShift2) & (kBins2 - 1)), 1u);
                 }
             }
         }
@@ -729,18 +769,29 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     if (!grid_barrier(gb, red, err, 62)) return;
     clear_level(gstate, bq.n_q, kOffH1, kBins1);
 
+    // this launch's count, for the next one's parity (every CTA read it before barrier 1)
+    if (cta == 0 && tid == 0) atomicAdd(launch_count, 1u);
+
     // ---- one round of loads: every query's candidate count (does any need
     // the histogram levels? grid-uniform), and for the first part the counts of
-    // the earlier CTAs and the head of the candidate list
+    // the earlier CTAs, the head of the candidate list and the level-2
+    // histogram of the candidates
     int* n_cand_q = red + 32;                         // [kFusedMaxQ]
     CountLoads cl;
+    uint32_t b2_0 = 0;
+    int above2_0 = 0;
     if (nseg > 0) {
         const int q0 = seg[0].q;
+        const uint32_t* gsq0 = gstate + (int64_t)q0 * kQueryWords;
         if (tid < 32) load_counts(gcnt + (int64_t)q0 * kFusedMaxGrid, seg[0].c_first, cl);
-        const int2* src = reinterpret_cast<const int2*>(gstate + (int64_t)q0 * kQueryWords + kOffCand);
+        const int2* src = reinterpret_cast<const int2*>(gsq0 + kOffCand);
         int2 v[kCandSpec / kThreads];                 // all in flight at once
 #pragma unroll
         for (int k = 0; k < kCandSpec / kThreads; ++k) v[k] = __ldcg(src + tid + k * kThreads);
+        // with those loads in flight: the level-2 bin of the first part's query
+        find_bin<kBins2, true>(gsq0 + kOffH2c + par * kBins2, keep - seg[0].above, red);
+        b2_0 = (uint32_t)red[kR0];
+        above2_0 = red[kR1];
 #pragma unroll
         for (int k = 0; k < kCandSpec / kThreads; ++k) cand[tid + k * kThreads] = v[k];
     }
@@ -764,8 +815,9 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         const int n_cand = n_cand_q[S.q];
         if (n_cand > kCandCap) continue;
         const int staged = s == 0 ? (n_cand < kCandSpec ? n_cand : kCandSpec) : 0;
-        resolve_from_candidates(S, gsq, gcnt + (int64_t)S.q * kFusedMaxGrid, n_cand, staged, cl,
-                                s == 0, keep - S.above, S.prefix, keys, hist, cand,
+        resolve_from_candidates(S, gsq, gsq + kOffH2c + par * kBins2,
+                                gcnt + (int64_t)S.q * kFusedMaxGrid, n_cand, staged, cl, s == 0,
+                                s == 0, b2_0, above2_0, keep - S.above, S.prefix, keys, hist, cand,
                                 reinterpret_cast<const int2*>(smem), keep, kpool,
                                 idx + (int64_t)S.q * width, red);
     }

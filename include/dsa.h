@@ -174,14 +174,14 @@ dsa_status dsa_plan(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
                     dsa_plan_info *info);
 
 /* Zeroes the start of the workspace on `stream`: the 256-byte header (device
- * error word, grid barrier, wait budget) and the decode step's selection state
+ * error word, grid barrier, wait budget, launch count) and the decode step's selection state
  * that follows it (DSA_WS_ZERO_BYTES in all, or the whole of a smaller workspace).
  * Call once on a freshly allocated workspace that was not allocated
  * zero-filled; after that every completed call leaves this region as it must
  * be (no entry point uses it as scratch, so one workspace may serve all of
  * them in turn), and dsa_check_device_error() re-zeroes it when a kernel
  * reported an error.  `ws` must be 256-byte aligned and at least 256 bytes. */
-#define DSA_WS_ZERO_BYTES (256u + 16u * 21508u * 4u + 16u * 256u * 8u)
+#define DSA_WS_ZERO_BYTES (256u + 16u * 25604u * 4u + 16u * 256u * 8u)
 dsa_status dsa_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Step 1: lightning-indexer scores ("GLM 5.2 in one C file", "The Lightning

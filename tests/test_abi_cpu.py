@@ -78,7 +78,7 @@ def test_workspace_sizes(lib):
     # selection state of the fused launch comes first
     assert rc == 0 and rc2 == 0 and n_sel % 256 == 0
     assert 256 + 131072 * 4 <= n_sel <= n_step
-    assert n_sel >= 256 + 16 * 21508 * 4 + 16 * 256 * 8          # DSA_WS_ZERO_BYTES of dsa.h
+    assert n_sel >= 256 + 16 * 25604 * 4 + 16 * 256 * 8          # DSA_WS_ZERO_BYTES of dsa.h
     rc, n = _size(sh, _batch(), dsa.OP_POOL_COMPRESS)     # the header: the error word
     assert rc == 0 and n == 256
     rc, n = _size(sh, _batch(), dsa.OP_PROJECT)            # the header: the error word
@@ -87,7 +87,7 @@ def test_workspace_sizes(lib):
     assert rc == 1
     # the single-step entry points keep their scratch clear of the zeroed prefix
     rc, n_idx = _size(sh, _batch(), dsa.OP_INDEX_SCORES)
-    assert n_idx >= 256 + 16 * 21508 * 4 + 16 * 256 * 8
+    assert n_idx >= 256 + 16 * 25604 * 4 + 16 * 256 * 8
 
 
 @pytest.mark.parametrize("field,value,code", [

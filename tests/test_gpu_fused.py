@@ -152,8 +152,10 @@ def test_fused_ties_across_ctas(kind):
 
 
 def test_fused_workspace_reuse_across_batches():
-    """Each launch leaves the shared histograms and the grid barrier zero: one
-    workspace serves consecutive launches of different batches."""
+    """Each launch leaves the shared selection state as the next one expects it
+    (histograms cleared, the grid barrier at a whole number of rounds, the
+    candidates' level-2 copy of the other launch parity cleared): one workspace
+    serves consecutive launches of batches with different query counts."""
     wa = workloads.small("reuse_a", [40000, 5000], top_k=2048, seed=21)
     wb = workloads.small("reuse_b", [9000, 70000, 3000], top_k=512, seed=22)
     ha, hb = workloads.make(wa, "cpu"), workloads.make(wb, "cpu")
