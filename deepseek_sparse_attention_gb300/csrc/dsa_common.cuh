@@ -71,6 +71,17 @@ struct QueryInfo {
 // the check fails, a binary search over q_off finds the sequence.
 // Returns false (and records kDevBadBatch) when the offsets contradict the
 // host bounds; the caller then skips the query.
+// a * b / c for a, b, c >= 0, c > 0, in 32-bit arithmetic when the product
+// fits (the common case: tile ranges of one launch), else 64-bit.  A 64-bit
+// division is a long dependent instruction sequence on the GPU; on a kernel's
+// prologue it costs a visible fraction of a microsecond.
+__device__ __forceinline__ int64_t mul_div(int64_t a, int64_t b, int64_t c) {
+    const int64_t p = a * b;
+    if (p < ((int64_t)1 << 32) && c < ((int64_t)1 << 32))
+        return (int64_t)((uint32_t)p / (uint32_t)c);
+    return p / c;
+}
+
 __device__ __forceinline__ bool query_info(const BatchDev& b, int64_t q, QueryInfo& qi,
                                            int32_t* err, int32_t where) {
     int32_t s = -1;
@@ -109,8 +120,9 @@ __device__ __forceinline__ bool query_info(const BatchDev& b, int64_t q, QueryIn
     qi.row0 = r0;
     qi.key0 = k0;
     qi.L = L;
-    qi.n_keys = L / b.kpool;
-    if (k1 - k0 < kv_len / b.kpool || k0 < 0 || k1 > b.total_keys) {
+    // 0 < L <= kv_len <= max_kv_len < 2^31 here: 32-bit divisions
+    qi.n_keys = (int64_t)((uint32_t)L / (uint32_t)b.kpool);
+    if (k1 - k0 < (int64_t)((uint32_t)kv_len / (uint32_t)b.kpool) || k0 < 0 || k1 > b.total_keys) {
         record_error(err, kDevBadBatch, (int32_t)q, where);
         return false;
     }

@@ -7,12 +7,13 @@
 // arithmetic but spreads the rounding of the 16-bit key cache evenly over the
 // 128 dimensions; "The block", row "RoPE": NORM mode (adjacent pairs), base 8e6.
 //
-// One warp per 128-vector, four dimensions per lane, a persistent grid: rope on
-// the lane's two adjacent pairs, then the fast Walsh-Hadamard transform -- two
-// butterfly stages inside the lane, five across lanes by shuffles -- and the
-// 1/sqrt(128) scale.  HBM-bound streaming: a warp loads kUnroll vectors (and
-// their positions) before it transforms the first, to keep enough bytes in
-// flight.  Positions reach 10^6 radians, so the angle is formed in turns with
+// Half a warp per 128-vector, eight dimensions per lane, a persistent grid:
+// rope on the lane's four adjacent pairs, then the fast Walsh-Hadamard
+// transform -- three butterfly stages inside the lane, four across the 16
+// lanes by shuffles (eight independent ones per stage) -- and the 1/sqrt(128)
+// scale.  HBM-bound streaming: a warp loads kUnroll vector pairs (and their
+// positions) before it transforms the first, to keep enough bytes in flight.
+// Positions reach 10^6 radians, so the angle is formed in turns with
 // integers: each pair's rate theta_i / 2 pi as a 64-bit binary fraction
 // (computed once, on the host, in double precision -- this GPU's double rate
 // is too low to spend on it per CTA), times the position, wrapping -- the
@@ -26,7 +27,8 @@ namespace {
 
 constexpr int kDim = 128;
 constexpr int kWarpsPerCta = 8;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 4;                 // vector pairs in flight per warp
+constexpr int kCtasPerSm = 3;              // resident CTAs per SM (the register bound below)
 
 // Turns per position of pair i: base^(-2i / rope_dims) / (2 pi) < 1, as a
 // 64-bit binary fraction.
@@ -34,20 +36,23 @@ struct RopeRates {
     unsigned long long r[kDim / 2];
 };
 
-__device__ __forceinline__ void store4(float* p, const float (&e)[4]) {
-    *reinterpret_cast<float4*>(p) = make_float4(e[0], e[1], e[2], e[3]);
+__device__ __forceinline__ void store8(float* p, const float (&e)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(e[0], e[1], e[2], e[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(e[4], e[5], e[6], e[7]);
 }
-__device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&e)[4]) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(e[0], e[1]);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(e[2], e[3]);
-    uint2 x;
-    x.x = *reinterpret_cast<const uint32_t*>(&a);
-    x.y = *reinterpret_cast<const uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(p) = x;
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&e)[8]) {
+    uint4 x;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(e[2 * k], e[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(p) = x;
 }
 
 template <typename T>
-__global__ void __launch_bounds__(32 * kWarpsPerCta)
+__global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm)
 index_prepare_kernel(int64_t n, const float* __restrict__ x, const int64_t* __restrict__ pos,
                      int32_t rope_dims, const __grid_constant__ RopeRates rates,
                      T* __restrict__ out) {
@@ -57,62 +62,78 @@ index_prepare_kernel(int64_t n, const float* __restrict__ x, const int64_t* __re
     for (int i = threadIdx.x; i < kDim / 2; i += blockDim.x) rate[i] = rates.r[i];
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta;
-    for (int64_t vb = (int64_t)blockIdx.x * kWarpsPerCta + warp; vb < n; vb += kUnroll * stride) {
-        float4 xs[kUnroll];
+    const int half = lane >> 4, hl = lane & 15;      // the pair's vector, the lane in it
+    // a warp takes vectors vb + 2 r stride + {0, 1}
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerCta * 2;
+    for (int64_t vb = ((int64_t)blockIdx.x * kWarpsPerCta + warp) * 2; vb < n;
+         vb += kUnroll * stride) {
+        float4 xa[kUnroll], xb[kUnroll];
         unsigned long long ps[kUnroll];
 #pragma unroll
         for (int r = 0; r < kUnroll; ++r) {
-            const int64_t v = vb + r * stride;
-            xs[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int64_t v = vb + r * stride + half;
+            xa[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            xb[r] = xa[r];
             ps[r] = 0;
             if (v < n) {
-                xs[r] = __ldcs(reinterpret_cast<const float4*>(x + v * kDim) + lane);
+                const float4* src = reinterpret_cast<const float4*>(x + v * kDim) + 2 * hl;
+                xa[r] = __ldcs(src);
+                xb[r] = __ldcs(src + 1);
                 if (rope_dims > 0) ps[r] = (unsigned long long)pos[v];
             }
         }
 #pragma unroll
         for (int r = 0; r < kUnroll; ++r) {
-            const int64_t v = vb + r * stride;
-            if (v >= n) break;
-            const float4 xv = xs[r];
-            float e[4] = {xv.x, xv.y, xv.z, xv.w};
-            // rope: pairs (4 lane, 4 lane + 1) and (4 lane + 2, 4 lane + 3)
-            if (4 * lane < rope_dims) {
+            const int64_t v0 = vb + r * stride;
+            if (v0 >= n) break;                          // both halves out of range
+            const int64_t v = v0 + half;
+            float e[8] = {xa[r].x, xa[r].y, xa[r].z, xa[r].w, xb[r].x, xb[r].y, xb[r].z, xb[r].w};
+            // rope: pairs (8 hl + 2 k, 8 hl + 2 k + 1), k < 4
+            if (8 * hl < rope_dims) {
                 const unsigned long long p = ps[r];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int i = 2 * lane + k;
+                for (int k = 0; k < 4; ++k) {
+                    const int i = 4 * hl + k;
                     if (2 * i >= rope_dims) break;
                     // fractional turns of pos * theta_i / 2 pi (the product wraps
-                    // modulo 2^64 = whole turns), as a signed fraction in [-1/2, 1/2)
+                    // modulo 2^64 = whole turns), as a signed fraction in [-1/2, 1/2),
+                    // to radians in [-pi, pi): there the hardware sine and cosine
+                    // are within 2^-21.4 absolute, far below the output's rounding
                     const int t32 = (int)(unsigned int)((p * rate[i]) >> 32);
-                    float s, c;
-                    sincospif(2.0f * ((float)t32 * 2.3283064365386963e-10f), &s, &c);
+                    float sn, cs;
+                    __sincosf((float)t32 * 1.4629180792671596e-09f, &sn, &cs);   // 2 pi / 2^32
                     const float x0 = e[2 * k], x1 = e[2 * k + 1];
-                    e[2 * k] = x0 * c - x1 * s;
-                    e[2 * k + 1] = x0 * s + x1 * c;
+                    e[2 * k] = x0 * cs - x1 * sn;
+                    e[2 * k + 1] = x0 * sn + x1 * cs;
                 }
             }
-            // Walsh-Hadamard: dimension d = 4 lane + j; the butterfly of bit b maps
-            // the pair (d, d | 2^b) with d's bit clear to (sum, difference)
-            {
-                const float a0 = e[0] + e[1], a1 = e[0] - e[1], a2 = e[2] + e[3], a3 = e[2] - e[3];
-                e[0] = a0 + a2; e[2] = a0 - a2; e[1] = a1 + a3; e[3] = a1 - a3;
+            // Walsh-Hadamard: dimension d = 8 hl + j; the butterfly of bit b maps
+            // the pair (d, d | 2^b) with d's bit clear to (sum, difference).
+            // Bits 0..2 inside the lane:
+#pragma unroll
+            for (int m = 1; m < 8; m <<= 1) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j & m) continue;
+                    const float a = e[j], c = e[j | m];
+                    e[j] = a + c;
+                    e[j | m] = a - c;
+                }
             }
+            // bits 3..6 across the vector's 16 lanes (xor < 16 stays in the half)
 #pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-                const bool upper = (lane & m) != 0;
+            for (int m = 1; m < 16; m <<= 1) {
+                const bool upper = (hl & m) != 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 8; ++j) {
                     const float o = __shfl_xor_sync(0xffffffffu, e[j], m);
                     e[j] = upper ? o - e[j] : e[j] + o;
                 }
             }
             const float norm = 0.08838834764831845f;         // 1 / sqrt(128)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) e[j] *= norm;
-            store4(out + v * kDim + 4 * lane, e);
+            for (int j = 0; j < 8; ++j) e[j] *= norm;
+            if (v < n) store8(out + v * kDim + 8 * hl, e);
         }
     }
 }
@@ -123,10 +144,10 @@ cudaError_t launch_index_prepare(const Shape& sh, int64_t n_vec, const float* x,
                                  const int64_t* pos, int32_t rope_dims, double base, void* out,
                                  cudaStream_t st) {
     if (n_vec == 0) return cudaSuccess;
-    // a persistent grid: enough CTAs to fill the GPU, each sets up its rope
-    // rates once and walks vectors
-    int64_t blocks = (n_vec + kWarpsPerCta - 1) / kWarpsPerCta;
-    if (blocks > (int64_t)sm_count() * 8) blocks = (int64_t)sm_count() * 8;
+    // a persistent grid: one wave of CTAs (kCtasPerSm resident on each SM),
+    // each sets up its rope rates once and walks vectors, two per warp at a time
+    int64_t blocks = (n_vec + 2 * kWarpsPerCta - 1) / (2 * kWarpsPerCta);
+    if (blocks > (int64_t)sm_count() * kCtasPerSm) blocks = (int64_t)sm_count() * kCtasPerSm;
     // the 64-bit fraction of pos * theta_i / 2 pi per unit position: the
     // double rounded to the nearest integer multiple of 2^-64
     RopeRates rates{};

@@ -251,8 +251,8 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         n_groups = seq_goff[n_seq];
     }
     const int64_t U = tile_off[n_groups];
-    const int64_t u_begin = (int64_t)blockIdx.x * U / gridDim.x;
-    const int64_t u_end = (int64_t)(blockIdx.x + 1) * U / gridDim.x;
+    const int64_t u_begin = mul_div(blockIdx.x, U, gridDim.x);
+    const int64_t u_end = mul_div(blockIdx.x + 1, U, gridDim.x);
     ScoreStore epi{scores, ld};                      // an empty range only releases TMEM
     run<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off, n_groups, u_begin, u_end, w, kpool,
                         epi, err);

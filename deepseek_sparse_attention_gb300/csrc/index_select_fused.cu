@@ -141,6 +141,15 @@ static_assert(32 + kFusedMaxQ <= 64, "scratch words");
 
 // ------------------------------------------------------------ grid barrier
 
+// A plain (relaxed) load at GPU scope: the value only, no ordering -- an
+// acquire would hold back every later memory access of the thread until it
+// returns.
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
     unsigned long long v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -578,7 +587,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                                                          kWsLaunchCountOffset);
     uint32_t n_launch = 0;                    // thread 0: first used after scoring
     if (tid == 0) {
-        gb.seen = ld_acquire_u64(gbar);
+        gb.seen = ld_relaxed_u64(gbar);
         gb.budget = *reinterpret_cast<const volatile uint64_t*>(
             reinterpret_cast<const uint8_t*>(err) + kWsWaitBudgetOffset);
         n_launch = *reinterpret_cast<const volatile uint32_t*>(launch_count);
@@ -588,7 +597,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const IdxGroup* gs = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
     const int64_t* ts = reinterpret_cast<const int64_t*>(smem + C::kOffPlanT);
     const int64_t U = ts[n_groups];
-    const int64_t u_begin = (int64_t)cta * U / grid, u_end = (int64_t)(cta + 1) * U / grid;
+    const int64_t u_begin = mul_div(cta, U, grid), u_end = mul_div(cta + 1, U, grid);
     const int keep = top_k / kpool;
     const bool fits = u_end - u_begin <= (int64_t)kMaxCtaTiles;
     const bool direct = u_end - u_begin <= (int64_t)kSKeyTiles;   // keys straight to shared memory
@@ -603,7 +612,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             int64_t g = 0;
             while (ts[g + 1] <= u_begin) ++g;
             for (; g < n_groups && ts[g] < u_end && hq < 0; ++g)
-                if (ts[g + 1] > ts[g] && gs[g].L_last / kpool > keep) hq = gs[g].q0;
+                // floor(L / kpool) > keep, without the division
+                if (ts[g + 1] > ts[g] && gs[g].L_last >= (keep + 1) * kpool) hq = gs[g].q0;
         }
         red[kRHistQ] = hq;
     }
@@ -641,7 +651,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                 S.t_lo = (int32_t)t_lo;
                 // the CTA whose units contain the query's first unit ts[g]:
                 // the smallest c with floor((c + 1) U / grid) > ts[g]
-                S.c_first = (int32_t)(((ts[g] + 1) * grid + U - 1) / U - 1);
+                S.c_first = (int32_t)(mul_div(1, (ts[g] + 1) * grid + U - 1, U) - 1);
                 S.row0 = pf_cache != nullptr ? row0s[S.q] : -1;
                 seg[ns++] = S;
             }
@@ -660,7 +670,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         if (G.nq == 0) {
             from = 0; to_sel = 0; L_sel = 0; n_tot = 0;
         } else {
-            const int64_t L = G.L_last, nk = L / kpool;
+            const int64_t L = G.L_last, nk = G.L_last / kpool;   // 32-bit division
             if (nk <= keep) {
                 from = 0; to_sel = L; L_sel = 0; n_tot = L;
             } else {
