@@ -761,7 +761,8 @@ def run_ours(args):
         pr_bytes = n_keys * (wl.idx_dim * 4 + 8 + wl.idx_dim * kout.element_size())
         prep = {"kernel": "index_prepare", "launch_us": pr_ms * 1e3, "vectors": n_keys,
                 "work": "every key of the workload: float32 projection -> rope, Hadamard, dtype",
-                "bytes_per_launch": pr_bytes, "achieved_gbs": pr_bytes / (pr_ms / 1e3) / 1e9}
+                "bytes_per_launch": pr_bytes, "achieved_gbs": pr_bytes / (pr_ms / 1e3) / 1e9,
+                "traffic": kernel_traffic("index_prepare", wl.name)}
         del xks, pk, kout
 
     # end to end through the public call: every step copies its query inputs
