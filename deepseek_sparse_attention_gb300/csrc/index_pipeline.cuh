@@ -172,13 +172,49 @@ __device__ void setup(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMa
     tc_fence_after();
 }
 
+// The producer's first loads, by thread 0 alone, as soon as its range is
+// known -- before the rest of the CTA's set-up, so that the first bytes are
+// on their way while that runs: the query tile of the first unit's group and
+// up to STAGES key tiles of that group.  Returns how many key tiles it
+// issued (stages 0 .. n - 1, first phase); run() continues after them.
+template <int GQ, int STAGES>
+__device__ int issue_first(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p,
+                           const IdxGroup* __restrict__ groups, const int64_t* __restrict__ tile_off,
+                           int64_t n_groups, int64_t u_begin, int64_t u_end) {
+    using C = Cfg<GQ, STAGES>;
+    if (u_begin >= u_end) return 0;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* full = bars;
+    uint64_t* b_full = bars + 2 * C::kStages;
+    Cursor<(GQ > 1)> c{tile_off, 0, 0, 0, 0};
+    c.seek(u_begin, n_groups);
+    const IdxGroup G = groups[c.g];
+    uint8_t* bsm = smem + C::kOffB;
+    mbar_arrive_expect_tx(b_full, C::kBBytes);
+    tma_load_2d(bsm, tm_q_p, b_full, 0, G.q0 * kIdxHeads);
+    tma_load_2d(bsm + C::kBBoxBytes, tm_q_p, b_full, 64, G.q0 * kIdxHeads);
+    // the first group's tiles left from u_begin, the range's, the ring's
+    int64_t n = c.b1() - (c.b0() + c.t);
+    if (n > u_end - u_begin) n = u_end - u_begin;
+    if (n > C::kStages) n = C::kStages;
+    for (int s = 0; s < (int)n; ++s) {
+        uint8_t* asm_ = smem + C::kOffA + s * kABytes;
+        const int32_t y = (int32_t)(G.key0 + (c.t + s) * kTileKeys);
+        mbar_arrive_expect_tx(&full[s], kABytes);
+        tma_load_2d(asm_, tm_k_p, &full[s], 0, y);
+        tma_load_2d(asm_ + kABoxBytes, tm_k_p, &full[s], 64, y);
+    }
+    return (int)n;
+}
+
 // The three roles over [u_begin, u_end) (possibly empty), then TMEM release.
 // Called by every thread of the CTA (Cfg::kThreads) after setup().
 template <int GQ, int STAGES, class Epi>
 __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p,
                     const IdxGroup* __restrict__ groups, const int64_t* __restrict__ tile_off,
                     int64_t n_groups, int64_t u_begin, int64_t u_end,
-                    const float* __restrict__ w, int32_t kpool, Epi& epi, int32_t* err) {
+                    const float* __restrict__ w, int32_t kpool, Epi& epi, int32_t* err,
+                    int pre = 0) {
     using C = Cfg<GQ, STAGES>;
     const CUtensorMap& tm_k = *tm_k_p;
     const CUtensorMap& tm_q = *tm_q_p;
@@ -198,15 +234,23 @@ __device__ void run(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap*
 
     if (warp == 0) {
         if (lane == 0) {                                           // ---- TMA producer
+            // (thread 0: `pre` key tiles and their group's query tile may have
+            // been issued already by issue_first)
             Cursor<(GQ > 1)> c{tile_off, 0, 0, 0, 0};
             c.seek(u_begin, n_groups);
             int stage = 0;
             uint32_t phase = 0, b_empty_par = 0;
             int64_t b_group = -1;
             int8_t issued_par[C::kStages];
-            for (int s = 0; s < C::kStages; ++s) issued_par[s] = -1;
+            for (int s = 0; s < C::kStages; ++s) issued_par[s] = s < pre ? 0 : -1;
+            if (pre > 0) {
+                b_group = c.g;
+                stage = pre % C::kStages;
+                phase = pre == C::kStages ? 1u : 0u;
+                for (int s = 0; s < pre && u_begin + s + 1 < u_end; ++s) c.next();
+            }
             bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok; ++u) {
+            for (int64_t u = u_begin + pre; u < u_end && ok; ++u) {
                 const IdxGroup G = groups[c.g];
                 if (c.g != b_group) {
                     if (b_group >= 0) {

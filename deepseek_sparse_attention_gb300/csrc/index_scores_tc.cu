@@ -253,9 +253,13 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int64_t U = tile_off[n_groups];
     const int64_t u_begin = mul_div(blockIdx.x, U, gridDim.x);
     const int64_t u_end = mul_div(blockIdx.x + 1, U, gridDim.x);
+    int pre = 0;                                     // the first key tiles on their way now
+    if (threadIdx.x == 0)
+        pre = issue_first<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off, n_groups, u_begin,
+                                          u_end);
     ScoreStore epi{scores, ld};                      // an empty range only releases TMEM
     run<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off, n_groups, u_begin, u_end, w, kpool,
-                        epi, err);
+                        epi, err, pre);
 }
 
 // ---------------------------------------------------------------- host side

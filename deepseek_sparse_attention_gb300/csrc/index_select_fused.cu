@@ -602,6 +602,9 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const bool fits = u_end - u_begin <= (int64_t)kMaxCtaTiles;
     const bool direct = u_end - u_begin <= (int64_t)kSKeyTiles;   // keys straight to shared memory
     if (direct) keys = reinterpret_cast<uint32_t*>(smem + kOffSKeys);
+    const int64_t u_run = u_begin < u_end && fits ? u_end : u_begin;   // the range scored
+    int pre = 0;                              // thread 0: the first key tiles on their way now
+    if (tid == 0) pre = issue_first<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_run);
 
     // ---- before scoring: only what the epilogue needs, the first query this
     // CTA selects for (its level-1 counts are taken while scoring)
@@ -622,8 +625,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     // ---- scores of this CTA's units (keys to global, level-1 counts of hist_q)
     {                                         // an empty range only releases TMEM
         KeyStore epi{gkeys, ld, direct ? keys : nullptr, u_begin, hist, red[kRHistQ]};
-        run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin,
-                           u_begin < u_end && fits ? u_end : u_begin, w, kpool, epi, err);
+        run<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_run, w, kpool, epi,
+                           err, pre);
     }
     fence_proxy_async_smem();                 // the ring is reused by generic accesses
 
