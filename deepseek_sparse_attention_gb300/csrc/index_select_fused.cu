@@ -131,7 +131,7 @@ static_assert(kMaxCtaTiles >= 128, "room for the keys of a CTA");
 // [32, 32 + kFusedMaxQ) each query's candidate count.
 enum : int { kR0 = 16, kR1 = 17, kR2 = 18, kR3 = 19, kRFlag = 20, kRNseg = 21, kROver = 22,
              kRHistQ = 23, kRSmallN = 24, kRT = 25, kRTLast = 26, kRHotRun = 27,
-             kRSmallBefore = 28, kRPar = 29 };
+             kRSmallBefore = 28, kRPar = 29, kROnePart = 30 };
 // The hot lists: per part, in index order, the part's keys in or above the
 // threshold bin b1 as {key, index in the part} -- every key the selection can
 // take -- at the start of the ring, which holds no keys when they went straight
@@ -168,25 +168,34 @@ struct GridBar {
     unsigned long long seen;     // the counter when the launch began (thread 0)
     unsigned long long next;     // 0 until the first barrier derives it
     uint64_t budget;             // the workspace's wait budget, 0 = default
+    unsigned long long target;   // the count that completes the barrier arrived at
 };
 
 __device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Arrival by a releasing reduction (no return trip), then acquire loads while
-// waiting, for at most the wait budget: on timeout the error word is set and
-// false returned.
-__device__ bool grid_barrier(GridBar& gb, int* red, int32_t* err, int32_t where) {
+// Arrival by a releasing reduction (no return trip): every thread's writes
+// before it are visible to the CTAs that complete the barrier.  Work that no
+// other CTA needs before the barrier may run between the arrival and the wait.
+__device__ void grid_arrive(GridBar& gb) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        int ok = 1;
         const unsigned long long g = gridDim.x;
         if (gb.next == 0) gb.next = gb.seen - gb.seen % g + g;
-        const unsigned long long target = gb.next;
+        gb.target = gb.next;
         gb.next += g;
-        const uint64_t budget_ns = gb.budget != 0 ? gb.budget : kDefaultWaitNs;
         red_release_add_u64(gb.ctr, 1ull);
+    }
+}
+
+// Acquire loads until every CTA has arrived, for at most the wait budget: on
+// timeout the error word is set and false returned.
+__device__ bool grid_wait(GridBar& gb, int* red, int32_t* err, int32_t where) {
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const unsigned long long target = gb.target;
+        const uint64_t budget_ns = gb.budget != 0 ? gb.budget : kDefaultWaitNs;
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_u64(gb.ctr) < target) {
             if (globaltimer_ns() - t0 > budget_ns) {
@@ -199,6 +208,11 @@ __device__ bool grid_barrier(GridBar& gb, int* red, int32_t* err, int32_t where)
     }
     __syncthreads();
     return *reinterpret_cast<volatile int*>(red + kRFlag) != 0;
+}
+
+__device__ __forceinline__ bool grid_barrier(GridBar& gb, int* red, int32_t* err, int32_t where) {
+    grid_arrive(gb);
+    return grid_wait(gb, red, err, where);
 }
 
 // ------------------------------------------------------------ block helpers
@@ -582,7 +596,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     pdl_wait();                               // the inputs of the previous kernels
     // thread 0: the barrier counter's value at the start and the budget of the
     // waits on other CTAs (workspace header); both first used at barrier 1
-    GridBar gb{gbar, 0, 0, 0};
+    GridBar gb{gbar, 0, 0, 0, 0};
     uint32_t* launch_count = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(err) +
                                                          kWsLaunchCountOffset);
     uint32_t n_launch = 0;                    // thread 0: first used after scoring
@@ -630,8 +644,24 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
     fence_proxy_async_smem();                 // the ring is reused by generic accesses
 
-    // ---- this CTA's part of each sparse query (the first is hist_q's), whole
-    // rows, candidate counters
+    // ---- before barrier 1 only what the other CTAs read after it: the
+    // candidate counters zeroed and this CTA's level-1 counts -- its first
+    // query's, taken while scoring, flushed first.  A CTA whose scored range
+    // lies in one query's keys then arrives and does the rest while the others
+    // arrive; one straddling queries first counts and flushes its other parts.
+    const int hq = red[kRHistQ];
+    if (tid == 0) {
+        for (int q = cta; q < bq.n_q; q += grid) gstate[(int64_t)q * kQueryWords + kOffCandN] = 0;
+        int64_t g = 0;
+        while (g + 1 < n_groups && ts[g + 1] <= u_begin) ++g;
+        red[kROnePart] = u_run <= u_begin || ts[g + 1] >= u_run;
+    }
+    if (hq >= 0) flush_hist<kBins1>(hist, gstate + (int64_t)hq * kQueryWords + kOffH1);
+    else __syncthreads();
+    const bool one_part = red[kROnePart] != 0;
+    if (one_part) grid_arrive(gb);
+
+    // ---- this CTA's part of each sparse query (the first is hist_q's), whole rows
     if (tid == 0) {
         int ns = 0;
         if (!fits) record_error(err, kDevBadBatch, cta, 6);
@@ -663,9 +693,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         red[kRPar] = (int)(n_launch & 1u);
     }
     // rows one CTA writes whole: failed and dense queries; the tail and the
-    // padding of sparse rows (the selected body is written by the emission).
-    // The same CTA zeroes the query's candidate counter, first used after
-    // barrier 1.
+    // padding of sparse rows (the selected body is written by the emission)
     for (int q = cta; q < bq.n_q; q += grid) {
         const IdxGroup G = gs[q];
         int32_t* out = idx + (int64_t)q * width;
@@ -685,10 +713,7 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         }
         for (int64_t i = from + tid; i < width; i += kThreads)
             out[i] = i < to_sel ? (int32_t)(i + L_sel) : -1;
-        if (tid == 0) {
-            n_sel[q] = (int32_t)n_tot;
-            gstate[(int64_t)q * kQueryWords + kOffCandN] = 0;
-        }
+        if (tid == 0) n_sel[q] = (int32_t)n_tot;
     }
     __syncthreads();
     const int nseg = red[kRNseg];
@@ -697,7 +722,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     clear_level(gstate, kFusedMaxQ, kOffH2c + (par ^ 1) * kBins2, kBins2);
 
     // ---- keys back into shared memory (asynchronous copies, 16 bytes each:
-    // part starts are tile-aligned and rows padded to 4 keys), level-1 counts
+    // part starts are tile-aligned and rows padded to 4 keys), the other
+    // parts' level-1 counts
     for (int s = 0; s < nseg && !direct; ++s) {
         const SegState S = seg[s];
         const uint32_t* src = gkeys + (int64_t)S.q * ld + S.t_lo;
@@ -708,7 +734,6 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
                          : "memory");
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    if (nseg > 0) flush_hist<kBins1>(hist, gstate + (int64_t)seg[0].q * kQueryWords + kOffH1);
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     for (int s = 1; s < nseg; ++s) {
@@ -716,7 +741,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
         for (int i = tid; i < S.n; i += kThreads) atomicAdd(&hist[keys[S.koff + i] >> kShift1], 1u);
         flush_hist<kBins1>(hist, gstate + (int64_t)S.q * kQueryWords + kOffH1);
     }
-    if (!grid_barrier(gb, red, err, 61)) return;
+    if (!one_part) grid_arrive(gb);
+    if (!grid_wait(gb, red, err, 61)) return;
 
     // ---- b1; counts above it; candidates in it; the hot lists
     if (tid == 0) red[kRHotRun] = 0;
