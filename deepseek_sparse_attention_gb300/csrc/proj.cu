@@ -48,6 +48,7 @@ constexpr int kConv = 320;                   // up: threads splitting o (warps 2
 constexpr int kMaxStages = 8;
 constexpr int kMaxN = 256;
 constexpr int kConvIters = (kMaxN * 8 + kConv - 1) / kConv;   // 16-byte chunks per thread
+constexpr int kSmallKb = 8;                  // k-blocks held at once for a small query tile
 constexpr uint32_t kSmemBudget = 200u * 1024u;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
@@ -184,54 +185,90 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
             mbar_wait(drain, 0, 50000000ull);
         }
     } else if (MODE == 1) {                                        // ---- o -> bf16 hi, lo
-        // This thread's 16-byte chunks of a k-block: chunk c = tc + j kConv is
-        // query row c / 8, dims 8 (c % 8) .. + 7; every load of the k-block is
-        // issued before the first conversion.
         const int tc = threadIdx.x - 64;                           // 0 .. kConv-1
-        for (int kb = 0; kb < n_kb; ++kb) {
-            const int s = kb % stages;
-            const uint32_t ph = (uint32_t)(kb / stages) & 1u;
-            float4 xa[kConvIters], xb[kConvIters];
-#pragma unroll
-            for (int j = 0; j < kConvIters; ++j) {
-                const int c = tc + j * kConv;
-                const int64_t q = q0 + (c >> 3);
-                xa[j] = xb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (c < N * 8 && q < n_q) {
-                    const float4* src = reinterpret_cast<const float4*>(
-                        o + (q * heads + h) * (int64_t)kv_lora + kb * 64 + (c & 7) * 8);
-                    xa[j] = __ldg(src);
-                    xb[j] = __ldg(src + 1);
-                }
-            }
-            if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, kWaitNs)) {
-                record_error(err, kDevTimeout, blockIdx.x, /*where=*/32);
-                *abort_flag = 1;
-                break;
-            }
-            uint8_t* hi = smem + s * sbytes + kABytes;
+        // One 16-byte chunk c of a k-block: query row c / 8, dims 8 (c % 8) .. + 7,
+        // split into bf16 hi and lo in the k-block's stage.
+        auto convert = [&](int kb, int c, const float4& a, const float4& bq) {
+            uint8_t* hi = smem + (kb % stages) * sbytes + kABytes;
             uint8_t* lo = hi + N * 128;
+            const int n = c >> 3, k8 = c & 7;
+            const float f[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+            uint32_t vh[4], vl[4];
 #pragma unroll
-            for (int j = 0; j < kConvIters; ++j) {
-                const int c = tc + j * kConv;
-                if (c >= N * 8) continue;
-                const int n = c >> 3, k8 = c & 7;
-                const float f[8] = {xa[j].x, xa[j].y, xa[j].z, xa[j].w,
-                                    xb[j].x, xb[j].y, xb[j].z, xb[j].w};
-                uint32_t vh[4], vl[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const __nv_bfloat162 hv = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
-                    const float2 hf = __bfloat1622float2(hv);
-                    vh[e] = *reinterpret_cast<const uint32_t*>(&hv);
-                    vl[e] = bf16x2_bits(f[2 * e] - hf.x, f[2 * e + 1] - hf.y);
-                }
-                const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(k8 ^ (n & 7)) << 4);
-                *reinterpret_cast<uint4*>(hi + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
-                *reinterpret_cast<uint4*>(lo + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+                const float2 hf = __bfloat1622float2(hv);
+                vh[e] = *reinterpret_cast<const uint32_t*>(&hv);
+                vl[e] = bf16x2_bits(f[2 * e] - hf.x, f[2 * e + 1] - hf.y);
             }
-            fence_proxy_async_smem();                              // generic writes -> MMA reads
-            mbar_arrive(&full[s]);
+            const uint32_t off = (uint32_t)n * 128u + ((uint32_t)(k8 ^ (n & 7)) << 4);
+            *reinterpret_cast<uint4*>(hi + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+            *reinterpret_cast<uint4*>(lo + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+        };
+        auto chunk_src = [&](int kb, int c) {
+            const int64_t q = q0 + (c >> 3);
+            return reinterpret_cast<const float4*>(o + (q * heads + h) * (int64_t)kv_lora +
+                                                   kb * 64 + (c & 7) * 8);
+        };
+        if (N * 8 <= kConv && n_kb <= kSmallKb) {
+            // A small query tile (a decode batch): at most one chunk of each
+            // k-block per thread, and the loads of every k-block in flight at
+            // once -- not one k-block's round trip after another.
+            const bool has = tc < N * 8 && q0 + (tc >> 3) < n_q;
+            float4 xa[kSmallKb], xb[kSmallKb];
+#pragma unroll
+            for (int kb = 0; kb < kSmallKb; ++kb) {
+                xa[kb] = xb[kb] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (kb < n_kb && has) {
+                    const float4* src = chunk_src(kb, tc);
+                    xa[kb] = __ldg(src);
+                    xb[kb] = __ldg(src + 1);
+                }
+            }
+#pragma unroll
+            for (int kb = 0; kb < kSmallKb; ++kb) {
+                if (kb >= n_kb) break;
+                const int s = kb % stages;
+                const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+                if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, kWaitNs)) {
+                    record_error(err, kDevTimeout, blockIdx.x, /*where=*/32);
+                    *abort_flag = 1;
+                    break;
+                }
+                if (tc < N * 8) convert(kb, tc, xa[kb], xb[kb]);
+                fence_proxy_async_smem();                          // generic writes -> MMA reads
+                mbar_arrive(&full[s]);
+            }
+        } else {
+            // This thread's chunks of a k-block: c = tc + j kConv; every load of
+            // the k-block is issued before the first conversion.
+            for (int kb = 0; kb < n_kb; ++kb) {
+                const int s = kb % stages;
+                const uint32_t ph = (uint32_t)(kb / stages) & 1u;
+                float4 xa[kConvIters], xb[kConvIters];
+#pragma unroll
+                for (int j = 0; j < kConvIters; ++j) {
+                    const int c = tc + j * kConv;
+                    xa[j] = xb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (c < N * 8 && q0 + (c >> 3) < n_q) {
+                        const float4* src = chunk_src(kb, c);
+                        xa[j] = __ldg(src);
+                        xb[j] = __ldg(src + 1);
+                    }
+                }
+                if (*abort_flag || !mbar_wait(&empty[s], ph ^ 1u, kWaitNs)) {
+                    record_error(err, kDevTimeout, blockIdx.x, /*where=*/32);
+                    *abort_flag = 1;
+                    break;
+                }
+#pragma unroll
+                for (int j = 0; j < kConvIters; ++j) {
+                    const int c = tc + j * kConv;
+                    if (c < N * 8) convert(kb, c, xa[j], xb[j]);
+                }
+                fence_proxy_async_smem();                          // generic writes -> MMA reads
+                mbar_arrive(&full[s]);
+            }
         }
     } else if (warp < 4 && mb == 0 && rope > 0) {                  // ---- absorb: the rope part
         // 16-byte chunks: thread t copies chunk t % 8 of queries t / 8 + 8 i,
