@@ -39,6 +39,7 @@ constexpr int kL1Bins = 1 << kL1Bits;
 constexpr int kHistCopies = 2;             // 4096 bins: the first multi-level radix level
 constexpr int kCandCap = 8192;
 constexpr int kSample = 2048;                 // scores sampled to bound the threshold
+constexpr int kSampleLog2 = 11;
 constexpr int kItems = 8;                     // scores per thread per emission round (fallback)
 constexpr size_t kFixedSmem = (size_t)kHistCopies * kL1Bins * 4 + (size_t)kCandCap * 8 + 256;
 static_assert(kSample <= kCandCap, "the sample is staged in the candidate list");
@@ -271,7 +272,11 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
         for (int i = tid; i < kL1Bins; i += NT) hist[i] = 0;
         if (tid == 0) *s_count = 0;
         const int64_t n_samp = n < kSample ? n : kSample;
-        for (int64_t i = tid; i < n_samp; i += NT) samp[i] = order_key(__ldg(sc + i * n / n_samp));
+        // element i n / n_samp: a shift when the row is long (n_samp = kSample,
+        // a power of two), i itself otherwise -- no 64-bit division per element
+        static_assert((kSample & (kSample - 1)) == 0, "the sample size is a power of two");
+        for (int64_t i = tid; i < n_samp; i += NT)
+            samp[i] = order_key(__ldg(sc + (n_samp == kSample ? (i * n) >> kSampleLog2 : i)));
         __syncthreads();
         for (int64_t i = tid; i < n_samp; i += NT) atomicAdd(&hist[samp[i] >> 21], 1u);
         __syncthreads();
@@ -299,27 +304,31 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
                 const int64_t t = base + lane + 32 * r;
                 v[r] = t < hi ? __ldg(sc + t) : -INFINITY;
             }
-            // the round's hits counted, one slot allocation per warp for all of
-            // them, then (ballots again) each hit's slot
-            int n_hit = 0;
+            // the round's hits counted per lane, a warp prefix sum for each
+            // lane's first slot, one slot allocation per warp for all of them
+            int my = 0;
 #pragma unroll
-            for (int r = 0; r < kBatch; ++r) n_hit += __popc(__ballot_sync(0xffffffffu, v[r] >= t_lo));
+            for (int r = 0; r < kBatch; ++r) my += v[r] >= t_lo;
+            int incl = my;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const int n_hit = __shfl_sync(0xffffffffu, incl, 31);
             if (n_hit) {
                 int slot = 0;
                 if (lane == 0) slot = atomicAdd(s_count, n_hit);
-                slot = __shfl_sync(0xffffffffu, slot, 0);
-                const uint32_t below = (1u << lane) - 1u;
+                slot = __shfl_sync(0xffffffffu, slot, 0) + incl - my;
 #pragma unroll
                 for (int r = 0; r < kBatch; ++r) {
-                    const uint32_t hit = __ballot_sync(0xffffffffu, v[r] >= t_lo);
-                    if ((hit >> lane) & 1u) {
-                        const int sl = slot + __popc(hit & below);
-                        if (sl < kCandCap) {
-                            cand_key[sl] = order_key(v[r]);
-                            cand_idx[sl] = (int32_t)(base + lane + 32 * r);
+                    if (v[r] >= t_lo) {
+                        if (slot < kCandCap) {
+                            cand_key[slot] = order_key(v[r]);
+                            cand_idx[slot] = (int32_t)(base + lane + 32 * r);
                         }
+                        ++slot;
                     }
-                    slot += __popc(hit);
                 }
             }
         }
