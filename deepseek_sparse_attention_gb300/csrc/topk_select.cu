@@ -410,16 +410,24 @@ topk_select_kernel(BatchDev b, int32_t top_k, int32_t kpool, const float* __rest
                 const int64_t w = w0 + tid;
                 const uint32_t sw = w < words ? sel_bits[w] : 0u;
                 const uint32_t ew = w < words ? eq_bits[w] : 0u;
-                int eq_total;
-                const int eq_excl = block_exclusive_scan(__popc(ew), &eq_total, warp_sums);
-                int64_t take = k_rem - (eq_base + eq_excl);
+                // one scan of both counts (each below 2^16 per round): keys
+                // above T in the high half, keys equal to T in the low half
+                int tot;
+                const int excl = block_exclusive_scan((__popc(sw) << 16) | __popc(ew), &tot,
+                                                      warp_sums);
+                const int gt_excl = excl >> 16, eq_excl = excl & 0xffff;
+                const int gt_total = tot >> 16, eq_total = tot & 0xffff;
+                // keys equal to T are taken in word order while k_rem lasts
+                int64_t room = k_rem - eq_base;
+                room = room < 0 ? 0 : room;
+                int64_t take = room - eq_excl;
                 take = take < 0 ? 0 : (take > __popc(ew) ? __popc(ew) : take);
                 uint32_t m = ew, taken = 0;
                 for (int i = 0; i < take; ++i) { taken |= m & (~m + 1u); m &= m - 1u; }
                 uint32_t comb = sw | taken;
-                int sel_total;
-                const int sel_excl = block_exclusive_scan(__popc(comb), &sel_total, warp_sums);
-                int64_t pos = out_base + sel_excl;
+                const int64_t taken_before = room < eq_excl ? room : eq_excl;
+                const int sel_total = gt_total + (int)(room < eq_total ? room : eq_total);
+                int64_t pos = out_base + gt_excl + taken_before;
                 while (comb != 0u && pos < keep) {
                     const int bit = __ffs(comb) - 1;
                     comb &= comb - 1u;
