@@ -656,6 +656,72 @@ def step_metrics(wl, per_step_ms, world, peaks):
             "step_tflops": tfs, "step_tensor_frac": tfs / peaks["bf16_tflops"]}
 
 
+def time_e2e(dsa, sb, n_steps: int, no_graph: bool) -> dict:
+    """The step end to end through the public call a host-fed caller makes,
+    dsa_decode_step_host: every step's query inputs (q_idx, w, q_abs) are read
+    from one page-locked host buffer and its output is written to page-locked
+    host memory, inside the timed region.  Timed like the device-side value
+    (the calls captured in CUDA graphs of G steps over the input copies,
+    replayed), and also as plain stream calls, one per step."""
+    import torch
+
+    wl, d, dev, stream = sb.wl, sb.d, sb.dev, sb.stream
+    names = ("q_idx", "w", "q_abs")
+    offs, total = {}, 0
+    for k in names:
+        offs[k] = total
+        total += (d[k].numel() * d[k].element_size() + 255) // 256 * 256
+    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    hq = {}
+    for k in names:
+        n = d[k].numel() * d[k].element_size()
+        h_in[offs[k]:offs[k] + n].copy_(d[k].reshape(-1).view(torch.uint8).cpu())
+        hq[k] = h_in[offs[k]:offs[k] + n].view(d[k].dtype).view(d[k].shape)
+    h_out = torch.empty(sb.out.shape, dtype=sb.out.dtype).pin_memory()
+    ws = dsa.alloc_workspace(sb.sh, sb.b, dsa.OP_DECODE_STEP_HOST, dev)
+    h2d = sum(d[k].numel() * d[k].element_size() for k in names)
+    d2h = h_out.numel() * h_out.element_size()
+
+    def call(i, st):
+        c = i % sb.copies
+        dsa.dsa_decode_step_host(sb.sh, sb.b, hq["q_idx"], hq["w"], sb.keys[c], hq["q_abs"],
+                                 sb.caches[c], h_out, None, sb.idx, sb.n_sel, ws, st)
+
+    def timed(fn, n):
+        torch.cuda.synchronize(dev)
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        fn()
+        x1.record(stream)
+        torch.cuda.synchronize(dev)
+        return x0.elapsed_time(x1) / n
+
+    for i in range(3):
+        call(i, stream)
+    torch.cuda.synchronize(dev)
+    n_stream = min(n_steps, 2000)
+    stream_ms = timed(lambda: [call(i, stream) for i in range(n_stream)], n_stream)
+    if no_graph:
+        e2e_ms, launch = stream_ms, "stream launches"
+    else:
+        G = sb.copies * max(1, 48 // sb.copies)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(G):
+                call(i, torch.cuda.current_stream(dev))
+        g.replay()                                   # untimed: the graph's first replay
+        reps = max(1, n_steps // G)
+        e2e_ms = timed(lambda: [g.replay() for _ in range(reps)], reps * G)
+        launch = f"CUDA graphs of {G} calls"
+        torch.cuda.synchronize(dev)
+        del g
+    if dsa.dsa_check_device_error(ws, stream) != 0:
+        raise RuntimeError(f"device error in the end-to-end loop ({wl.name})")
+    return {"value": wl.n_q / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": "dsa_decode_step_host",
+            "launch": launch, "stream_calls_ms_per_step": stream_ms}
+
+
 def other_config(dsa, name, dev, stream, no_graph, pg, local, world, peaks, peak_src):
     """One more workload of the suite, timed like the headline (graph replay,
     rotated copies, clocks sampled): step time, throughput, the dominant
@@ -677,6 +743,10 @@ def other_config(dsa, name, dev, stream, no_graph, pg, local, world, peaks, peak
            "gpu_launches": sb.plan["kernel_launches"] * steps, "plan": sb.plan, "clocks": clk}
     ent.update(step_metrics(wl, per, world, peaks))
     ent["roofline"] = roofline_of(wl, fused, sel_ms, idx_ms, peaks, peak_src)
+    e2e = time_e2e(dsa, sb, max(20, steps // 2), no_graph)
+    e2e["ms_per_step"] = max_over_ranks(pg, [e2e["ms_per_step"]], dev)[0]
+    e2e["value"] = job_throughput(world, wl.n_q, e2e["ms_per_step"])
+    ent["e2e"] = e2e
     sb.release()
     del sb
     ent["projections"] = time_projections(dsa, wl, dev, stream, peaks, peak_src)
@@ -765,42 +835,10 @@ def run_ours(args):
                 "traffic": kernel_traffic("index_prepare", wl.name)}
         del xks, pk, kout
 
-    # end to end through the public call: every step copies its query inputs
-    # (q_idx, w, q_abs) from one pinned host buffer to the device, calls
-    # dsa_decode_step and reads its output back into pinned host memory, all in
-    # the step's stream order
+    # end to end through the public call fed from host memory
     e2e = None
     if not args.no_e2e:
-        names = ("q_idx", "w", "q_abs")
-        offs, total = {}, 0
-        for k in names:
-            offs[k] = total
-            total += (d[k].numel() * d[k].element_size() + 255) // 256 * 256
-        h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
-        d_in = torch.empty(total, dtype=torch.uint8, device=dev)
-        dq = {}
-        for k in names:
-            n = d[k].numel() * d[k].element_size()
-            h_in[offs[k]:offs[k] + n].copy_(d[k].reshape(-1).view(torch.uint8).cpu())
-            dq[k] = d_in[offs[k]:offs[k] + n].view(d[k].dtype).view(d[k].shape)
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h2d = total
-        d2h = h_out.numel() * h_out.element_size()
-        n_e2e = max(200, min(steps, 5000))
-        torch.cuda.synchronize(dev)
-        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        x0.record(stream)
-        for i in range(n_e2e):
-            d_in.copy_(h_in, non_blocking=True)
-            c = i % copies
-            dsa.dsa_decode_step(sh, b, dq["q_idx"], dq["w"], keys[c], dq["q_abs"], caches[c], out,
-                                lse, idx, n_sel, ws, stream)
-            h_out.copy_(out, non_blocking=True)
-        x1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = x0.elapsed_time(x1) / n_e2e
-        e2e = {"value": wl.n_q / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        e2e = time_e2e(dsa, sb, max(200, min(steps, 20000)), args.no_graph)
 
     ms, idx_ms, sel_ms = max_over_ranks(pg, [ms, idx_ms, sel_ms], dev)
     if e2e is not None:

@@ -31,11 +31,11 @@ __all__ = [
     "alloc_workspace", "dsa_version", "dsa_index_row_width", "dsa_workspace_size",
     "dsa_workspace_init", "dsa_plan", "dsa_index_scores", "dsa_topk_select", "dsa_index_select",
     "dsa_sparse_mla_attn",
-    "dsa_decode_step", "dsa_decode_step_noalloc", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
+    "dsa_decode_step", "dsa_decode_step_host", "dsa_decode_step_noalloc", "dsa_check_device_error", "DecodeStep", "LIB_PATH",
     "OP_INDEX_SCORES", "OP_TOPK_SELECT", "OP_SPARSE_MLA", "OP_DECODE_STEP", "OP_INDEX_SELECT",
     "OP_POOL_COMPRESS", "dsa_pool_compress", "dsa_index_prepare", "dsa_workspace_set_wait_budget",
     "FLAG_TWO_LAUNCH", "FLAG_DESC_ORDER", "FLAG_DENSE", "OP_PROJECT", "dsa_absorb_q",
-    "dsa_up_project",
+    "dsa_up_project", "OP_DECODE_STEP_HOST",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
@@ -44,6 +44,7 @@ DSA_F32, DSA_BF16 = 0, 1
 OP_INDEX_SCORES, OP_TOPK_SELECT, OP_SPARSE_MLA, OP_DECODE_STEP, OP_INDEX_SELECT = 0, 1, 2, 3, 4
 OP_POOL_COMPRESS = 5
 OP_PROJECT = 6
+OP_DECODE_STEP_HOST = 7
 FLAG_TWO_LAUNCH, FLAG_DESC_ORDER, FLAG_DENSE = 0x1, 0x2, 0x4
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED",
           3: "DSA_ERR_WORKSPACE", 4: "DSA_ERR_CUDA", 5: "DSA_ERR_DEVICE", 6: "DSA_ERR_TIMEOUT"}
@@ -104,6 +105,7 @@ def load() -> ctypes.CDLL:
             "dsa_index_select": ([S, B, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_sparse_mla_attn": ([S, B, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_decode_step": ([S, B, P, P, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
+            "dsa_decode_step_host": ([S, B, P, P, P, P, P, P, P, P, P, P, sz, P], ctypes.c_int),
             "dsa_check_device_error": ([P, sz, P, ctypes.POINTER(i32)], ctypes.c_int),
             "dsa_decode_step_noalloc": ([S, B, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "dsa_pool_compress": ([S, B, P, P, P, P, sz, P], ctypes.c_int),
@@ -232,6 +234,28 @@ def dsa_decode_step(shape, batch, q_idx, w, k_idx, q_abs, cache, out, lse=None, 
                     n_sel_out=None, ws=None, stream=None) -> None:
     _call("dsa_decode_step", ctypes.byref(shape), ctypes.byref(batch), _ptr(q_idx), _ptr(w),
           _ptr(k_idx), _ptr(q_abs), _ptr(cache), _ptr(out), _ptr(lse), _ptr(idx_out),
+          _ptr(n_sel_out), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream))
+
+
+def _host_ptr(t: Optional[torch.Tensor]):
+    """A pinned host tensor's address (or a CUDA tensor's): the per-step
+    buffers of dsa_decode_step_host."""
+    if t is None:
+        return None
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("dsa_decode_step_host takes pinned host (or CUDA) tensors")
+    if not t.is_contiguous():
+        raise ValueError("libdsa takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def dsa_decode_step_host(shape, batch, q_idx, w, k_idx, q_abs, cache, out, lse=None,
+                         idx_out=None, n_sel_out=None, ws=None, stream=None) -> None:
+    """dsa_decode_step with q_idx, w, q_abs, out and lse in page-locked host
+    memory (or device memory); the workspace is sized with OP_DECODE_STEP_HOST."""
+    _call("dsa_decode_step_host", ctypes.byref(shape), ctypes.byref(batch), _host_ptr(q_idx),
+          _host_ptr(w), _ptr(k_idx), _host_ptr(q_abs), _ptr(cache), _host_ptr(out),
+          _host_ptr(lse), _ptr(idx_out),
           _ptr(n_sel_out), _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream))
 
 

@@ -24,6 +24,25 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The address at which the current device reaches a caller's buffer: the
+// pointer itself for device or managed memory, the mapped address for
+// page-locked host memory; nullptr for memory the device cannot address
+// (pageable host memory) or a pointer the runtime cannot classify.
+const void* device_address(const void* p) {
+    if (p == nullptr) return nullptr;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();                       // leave no error behind for the caller
+        return nullptr;
+    }
+    switch (a.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged: return p;
+        case cudaMemoryTypeHost: return a.devicePointer;
+        default: return nullptr;
+    }
+}
+
 bool trace_on() {
     static const bool on = [] {
         const char* e = getenv("DSA_TRACE");
@@ -113,6 +132,24 @@ StepLayout step_layout(const Shape& sh, const BatchDev& b) {
     return L;
 }
 
+// Host-fed decode step: the step's workspace, then the staged query-side
+// inputs (indexer queries, head weights, absorbed queries).
+struct StageLayout {
+    size_t q_idx, w, q_abs, total;
+};
+StageLayout stage_layout(const Shape& sh, const BatchDev& b) {
+    StageLayout L{};
+    size_t off = step_layout(sh, b).total;
+    L.q_idx = off;
+    off = align_up(off + (size_t)b.n_q * sh.idx_heads * sh.idx_dim * sh.elem_bytes());
+    L.w = off;
+    off = align_up(off + (size_t)b.n_q * sh.idx_heads * sizeof(float));
+    L.q_abs = off;
+    off = align_up(off + (size_t)b.n_q * sh.heads * sh.width() * sh.elem_bytes());
+    L.total = off;
+    return L;
+}
+
 // Where the scratch of the single-step entry points begins: after the prefix
 // the fused decode launch keeps zero, so that one workspace can serve every
 // entry point in turn.
@@ -126,6 +163,7 @@ size_t op_bytes(const Shape& sh, const BatchDev& b, int32_t op) {
         case DSA_OP_SPARSE_MLA:
             return align_up(scratch_off() + sparse_mla_scratch_bytes(sh, b));
         case DSA_OP_DECODE_STEP: return step_layout(sh, b).total;
+        case DSA_OP_DECODE_STEP_HOST: return stage_layout(sh, b).total;
         case DSA_OP_INDEX_SELECT: return step_layout(sh, b).attn;
         case DSA_OP_POOL_COMPRESS: return kWsHeaderBytes;
         case DSA_OP_PROJECT: return kWsHeaderBytes;
@@ -194,6 +232,8 @@ int32_t plan_launches(const Shape& sh, const BatchDev& bh, int32_t op, int32_t s
         case DSA_OP_INDEX_SELECT: return sel;
         case DSA_OP_POOL_COMPRESS: return sh.kpool > 1 ? 1 : 0;
         case DSA_OP_PROJECT: return 1;
+        case DSA_OP_DECODE_STEP_HOST:                      // the input copy, then the step
+            return 1 + ((bh.flags & DSA_FLAG_DENSE) ? attn : sel + attn);
         default: return (bh.flags & DSA_FLAG_DENSE) ? attn : sel + attn;
     }
 }
@@ -267,7 +307,7 @@ dsa_status dsa_workspace_size(const dsa_shape* shape, const dsa_batch* batch, in
     if (batch->max_kv_len >= ((int64_t)1 << 31) ||
         (batch->n_q > 65535 && op != DSA_OP_POOL_COMPRESS))
         return DSA_ERR_UNSUPPORTED;
-    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_PROJECT) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_DECODE_STEP_HOST) return DSA_ERR_INVALID_ARG;
     *out_bytes = op_bytes(sh, host_batch(batch, sh), op);
     return DSA_OK;
 }
@@ -280,7 +320,7 @@ dsa_status dsa_plan(const dsa_shape* shape, const dsa_batch* batch, int32_t op,
     if (s != DSA_OK) return s;
     if (batch->n_q < 0 || batch->max_kv_len < 0 || (batch->flags & ~kKnownFlags) != 0)
         return DSA_ERR_INVALID_ARG;
-    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_PROJECT) return DSA_ERR_INVALID_ARG;
+    if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_DECODE_STEP_HOST) return DSA_ERR_INVALID_ARG;
     const BatchDev bh = host_batch(batch, sh);
     int32_t rps = 0, splits = 0;
     plan_attention_splits(sh, bh, &rps, &splits);
@@ -470,6 +510,61 @@ dsa_status dsa_decode_step(const dsa_shape* shape, const dsa_batch* batch, const
     e = launch_sparse_mla(sh, b, q_abs, cache, idx, n_sel, out, lse, bytes(ws) + lay.attn,
                           lay.total - lay.attn, err, /*q_early=*/true, st);
     return cuda_status(e, "decode_step/sparse_mla_attn");
+}
+
+dsa_status dsa_decode_step_host(const dsa_shape* shape, const dsa_batch* batch,
+                                const void* h_q_idx, const float* h_w, const void* k_idx,
+                                const void* h_q_abs, const void* cache, float* h_out,
+                                float* h_lse, int32_t* idx_out, int32_t* n_sel_out, void* ws,
+                                size_t ws_bytes, void* stream) {
+    Shape sh;
+    BatchDev b;
+    dsa_status s = check_shape(shape, &sh);
+    if (s != DSA_OK) return s;
+    if ((s = check_batch(batch, sh, &b)) != DSA_OK) return s;
+    const bool dense = (b.flags & DSA_FLAG_DENSE) != 0;
+    // the device's view of the caller's per-step buffers
+    const void *q_idx = nullptr, *w = nullptr, *q_abs = nullptr;
+    float *out = nullptr, *lse = nullptr;
+    if (b.n_q > 0) {
+        if (h_q_abs == nullptr || h_out == nullptr || (!dense && (h_q_idx == nullptr || h_w == nullptr)))
+            return DSA_ERR_INVALID_ARG;
+        q_abs = device_address(h_q_abs);
+        out = static_cast<float*>(const_cast<void*>(device_address(h_out)));
+        if (q_abs == nullptr || out == nullptr) return DSA_ERR_INVALID_ARG;
+        if (!dense) {
+            q_idx = device_address(h_q_idx);
+            w = device_address(h_w);
+            if (q_idx == nullptr || w == nullptr) return DSA_ERR_INVALID_ARG;
+        }
+        if (h_lse != nullptr) {
+            lse = static_cast<float*>(const_cast<void*>(device_address(h_lse)));
+            if (lse == nullptr) return DSA_ERR_INVALID_ARG;
+        }
+    }
+    if (!aligned16(q_idx) || !aligned16(w) || !aligned16(q_abs)) return DSA_ERR_INVALID_ARG;
+    const StageLayout sl = stage_layout(sh, b);
+    void* s_q_idx = dense ? nullptr : bytes(ws) + sl.q_idx;
+    float* s_w = dense ? nullptr : reinterpret_cast<float*>(bytes(ws) + sl.w);
+    void* s_q_abs = bytes(ws) + sl.q_abs;
+    int32_t n_q = 0;
+    s = decode_step_check(shape, batch, s_q_idx, s_w, k_idx, s_q_abs, cache, out, lse, idx_out,
+                          n_sel_out, nullptr, &n_q);
+    if (s != DSA_OK) return s;
+    if ((s = check_ws(ws, ws_bytes, sl.total)) != DSA_OK) return s;
+    if (n_q == 0) return DSA_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int64_t q_idx_vecs =
+        dense ? 0 : (int64_t)b.n_q * sh.idx_heads * sh.idx_dim * (int64_t)sh.elem_bytes() / 16;
+    const int64_t q_abs_vecs = (int64_t)b.n_q * sh.heads * sh.width() * (int64_t)sh.elem_bytes() / 16;
+    const StageSeg a{static_cast<const uint4*>(q_idx), static_cast<uint4*>(s_q_idx), q_idx_vecs};
+    const StageSeg c{static_cast<const uint4*>(q_abs), static_cast<uint4*>(s_q_abs), q_abs_vecs};
+    const int64_t w_words = dense ? 0 : (int64_t)b.n_q * sh.idx_heads;
+    cudaError_t e = launch_stage_inputs(a, c, static_cast<const uint32_t*>(w),
+                                        reinterpret_cast<uint32_t*>(s_w), w_words, st);
+    if (e != cudaSuccess) return cuda_status(e, "decode_step_host/stage_inputs");
+    return dsa_decode_step(shape, batch, s_q_idx, s_w, k_idx, s_q_abs, cache, out, lse, idx_out,
+                           n_sel_out, ws, ws_bytes, stream);
 }
 
 dsa_status dsa_index_select(const dsa_shape* shape, const dsa_batch* batch, const void* q_idx,

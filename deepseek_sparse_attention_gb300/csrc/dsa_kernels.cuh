@@ -162,6 +162,17 @@ cudaError_t launch_absorb_q(const Shape& sh, int32_t n_q, int32_t nope, const vo
 cudaError_t launch_up_project(const Shape& sh, int32_t n_q, int32_t v_dim, const float* o,
                               const void* w_uv, float* out, int32_t* err, cudaStream_t st);
 
+// The per-query inputs of a host-fed decode step copied into the workspace by
+// a kernel (stage_inputs.cu): the 16-byte vectors of two segments and the
+// 4-byte words of a third, after the wait for the previous kernel.
+struct StageSeg {
+    const uint4* src;
+    uint4* dst;
+    int64_t n;                                        // 16-byte vectors
+};
+cudaError_t launch_stage_inputs(StageSeg a, StageSeg b, const uint32_t* w_src, uint32_t* w_dst,
+                                int64_t w_n, cudaStream_t st);
+
 // Step 3.  bf16 rows run on the tensor cores (sparse_mla_tc.cu), float32 rows
 // on CUDA cores (sparse_mla.cu).  Row splits per query and the scratch for the
 // split-row partials (bytes; 0 if none is needed).  idx == nullptr (and

@@ -363,21 +363,36 @@ proj_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtens
     }
 }
 
-// Float32 inputs: one output element per thread (absorb) or per warp (up),
-// float32 accumulation in the order of the sum.
+// Float32 inputs.  Absorb: a CTA per (query, head, 64 output columns); its
+// 256 threads are the 64 columns times four interleaved quarters of the sum
+// over the nope dimensions, added in shared memory.  Up: a CTA per (query,
+// head, 32 outputs), a warp per output, the lanes' strided partial sums
+// added by shuffles.  Enough CTAs for one decode query to keep every SM's
+// loads in flight.  Float32 accumulation throughout.
+constexpr int kSimtAbsorbCols = 64;
+constexpr int kSimtUpRows = 32;
+
 __global__ void __launch_bounds__(256)
 absorb_simt(const float* __restrict__ q, const float* __restrict__ w_uk, float* __restrict__ q_abs,
             int32_t heads, int32_t nope, int32_t rope, int32_t kv_lora) {
+    __shared__ float part[4][kSimtAbsorbCols];
     const int64_t qh = blockIdx.x;                     // (query, head)
     const int h = (int)(qh % heads);
+    const int c = threadIdx.x % kSimtAbsorbCols, quarter = threadIdx.x / kSimtAbsorbCols;
+    const int i = (int)blockIdx.y * kSimtAbsorbCols + c;
     const float* qv = q + qh * (nope + rope);
     float* dst = q_abs + qh * (kv_lora + rope);
-    for (int i = threadIdx.x; i < kv_lora; i += blockDim.x) {
-        float acc = 0.f;
-        for (int d = 0; d < nope; ++d) acc = fmaf(qv[d], w_uk[((int64_t)h * nope + d) * kv_lora + i], acc);
-        dst[i] = acc;
+    float acc = 0.f;
+    if (i < kv_lora) {
+#pragma unroll 8
+        for (int d = quarter; d < nope; d += 4)
+            acc = fmaf(qv[d], w_uk[((int64_t)h * nope + d) * kv_lora + i], acc);
     }
-    for (int r = threadIdx.x; r < rope; r += blockDim.x) dst[kv_lora + r] = qv[nope + r];
+    part[quarter][c] = acc;
+    __syncthreads();
+    if (quarter == 0 && i < kv_lora) dst[i] = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+    if (blockIdx.y == 0)
+        for (int r = threadIdx.x; r < rope; r += blockDim.x) dst[kv_lora + r] = qv[nope + r];
 }
 
 __global__ void __launch_bounds__(256)
@@ -387,9 +402,12 @@ up_simt(const float* __restrict__ o, const float* __restrict__ w_uv, float* __re
     const int h = (int)(qh % heads);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float* ov = o + qh * kv_lora;
-    for (int v = warp; v < v_dim; v += blockDim.x >> 5) {
+    const int v0 = (int)blockIdx.y * kSimtUpRows;
+    const int v1 = v0 + kSimtUpRows < v_dim ? v0 + kSimtUpRows : v_dim;
+    for (int v = v0 + warp; v < v1; v += blockDim.x >> 5) {
         const float* wr = w_uv + ((int64_t)h * v_dim + v) * kv_lora;
         float acc = 0.f;
+#pragma unroll 8
         for (int i = lane; i < kv_lora; i += 32) acc = fmaf(wr[i], ov[i], acc);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -454,7 +472,9 @@ cudaError_t launch_absorb_q(const Shape& sh, int32_t n_q, int32_t nope, const vo
     if (n_q == 0) return cudaSuccess;
     if (sh.dtype == DSA_BF16)
         return launch_tc<0>(sh, n_q, nope, 0, q, w_uk, nullptr, q_abs, err, st);
-    return launch_plain(absorb_simt, dim3((unsigned)((int64_t)n_q * sh.heads)), dim3(256), 0, st,
+    const dim3 grid((unsigned)((int64_t)n_q * sh.heads),
+                    (unsigned)((sh.kv_lora + kSimtAbsorbCols - 1) / kSimtAbsorbCols));
+    return launch_plain(absorb_simt, grid, dim3(256), 0, st,
                         static_cast<const float*>(q), static_cast<const float*>(w_uk),
                         static_cast<float*>(q_abs), (int32_t)sh.heads, nope, (int32_t)sh.rope,
                         (int32_t)sh.kv_lora);
@@ -465,7 +485,8 @@ cudaError_t launch_up_project(const Shape& sh, int32_t n_q, int32_t v_dim, const
     if (n_q == 0) return cudaSuccess;
     if (sh.dtype == DSA_BF16)
         return launch_tc<1>(sh, n_q, 0, v_dim, nullptr, w_uv, o, out, err, st);
-    return launch_plain(up_simt, dim3((unsigned)((int64_t)n_q * sh.heads)), dim3(256), 0, st, o,
+    const dim3 grid((unsigned)((int64_t)n_q * sh.heads), (unsigned)((v_dim + kSimtUpRows - 1) / kSimtUpRows));
+    return launch_plain(up_simt, grid, dim3(256), 0, st, o,
                         static_cast<const float*>(w_uv), out, (int32_t)sh.heads,
                         (int32_t)sh.kv_lora, v_dim);
 }

@@ -312,12 +312,14 @@ merge_splits(int32_t n_split, const float* __restrict__ part_o, const float* __r
     if (lse != nullptr && c4 == 0) lse[q * kHeads + h] = Lt > 0.f ? Mt + logf(Lt) : -INFINITY;
 }
 
-// Rows per split: enough CTAs to fill the GPU about twice, at least 64 rows each.
+// Rows per split: enough CTAs to fill the GPU about twice, at least one
+// 16-row tile each (a CTA's time is its tile loop: a short query is spread
+// over as many CTAs as it has tiles).
 void plan_splits_simt(int32_t n_q, int64_t max_rows, int32_t* rows_per_split, int32_t* n_split) {
     if (max_rows < 1) max_rows = 1;
     const int64_t target_ctas = 2 * (int64_t)sm_count();
     int64_t splits = (target_ctas + n_q - 1) / n_q;
-    const int64_t max_splits = (max_rows + 63) / 64;
+    const int64_t max_splits = (max_rows + kTile - 1) / kTile;
     if (splits > max_splits) splits = max_splits;
     if (splits < 1) splits = 1;
     int64_t rps = (max_rows + splits - 1) / splits;

@@ -158,6 +158,7 @@ int64_t dsa_index_row_width(const dsa_shape *shape);
 #define DSA_OP_INDEX_SELECT 4
 #define DSA_OP_POOL_COMPRESS 5
 #define DSA_OP_PROJECT 6
+#define DSA_OP_DECODE_STEP_HOST 7
 dsa_status dsa_workspace_size(const dsa_shape *shape, const dsa_batch *batch, int32_t op,
                               size_t *bytes);
 
@@ -354,6 +355,35 @@ dsa_status dsa_decode_step(const dsa_shape *shape, const dsa_batch *batch, const
                            const float *w, const void *k_idx, const void *q_abs,
                            const void *cache, float *out, float *lse, int32_t *idx_out,
                            int32_t *n_sel_out, void *ws, size_t ws_bytes, void *stream);
+
+/* dsa_decode_step fed from host memory: the step's per-query inputs are read
+ * from, and its output written to, buffers the host fills and reads each step
+ * (the cache, the keys and the batch arrays stay on the device).  The pages
+ * have no counterpart: this is a convenience of this library, for a caller
+ * whose queries come from the host.
+ *   h_q_idx, h_w, h_q_abs  as q_idx, w, q_abs of dsa_decode_step, in
+ *       page-locked host memory that the device can address (cudaHostAlloc /
+ *       cudaMallocHost, or cudaHostRegister'ed and mapped), or device memory.
+ *       The call's first kernel copies them into the workspace -- a kernel,
+ *       not a copy-engine transfer, so that the copy is one more link of the
+ *       step's chain of programmatically dependent launches -- and the step
+ *       reads them there.  16-byte aligned.
+ *   h_out, h_lse (may be NULL)  as out, lse, likewise host (or device)
+ *       memory: the step's last kernel writes them there directly.
+ *   k_idx, cache, idx_out, n_sel_out, flags  as for dsa_decode_step (device
+ *       memory).
+ * Results are those of dsa_decode_step on the same inputs, bit for bit.  The
+ * workspace is sized with DSA_OP_DECODE_STEP_HOST: the step's, then room for
+ * the staged inputs; its zeroing and wait budget as for dsa_decode_step.  A
+ * buffer the device cannot address (pageable host memory, an unknown pointer)
+ * gives DSA_ERR_INVALID_ARG; every argument is checked before anything is
+ * enqueued.  The input buffers may be refilled, and the outputs read, once the
+ * stream has passed the call. */
+dsa_status dsa_decode_step_host(const dsa_shape *shape, const dsa_batch *batch,
+                                const void *h_q_idx, const float *h_w, const void *k_idx,
+                                const void *h_q_abs, const void *cache, float *h_out,
+                                float *h_lse, int32_t *idx_out, int32_t *n_sel_out, void *ws,
+                                size_t ws_bytes, void *stream);
 
 /* dsa_decode_step for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a convenience of this library.  Some callers may

@@ -83,7 +83,12 @@ def test_workspace_sizes(lib):
     assert rc == 0 and n == 256
     rc, n = _size(sh, _batch(), dsa.OP_PROJECT)            # the header: the error word
     assert rc == 0 and n == 256
-    rc, _ = _size(sh, _batch(), 7)
+    # the host-fed step: the step's workspace, then the staged query inputs
+    # (8 KB of indexer queries, 128 B of weights, 72 KB of absorbed queries)
+    rc, n_host = _size(sh, _batch(max_kv=131072), dsa.OP_DECODE_STEP_HOST)
+    assert rc == 0 and n_host % 256 == 0
+    assert n_host >= n_step + 32 * 128 * 2 + 32 * 4 + 64 * 576 * 2
+    rc, _ = _size(sh, _batch(), 8)
     assert rc == 1
     # the single-step entry points keep their scratch clear of the zeroed prefix
     rc, n_idx = _size(sh, _batch(), dsa.OP_INDEX_SCORES)
@@ -282,6 +287,34 @@ def test_projections_reject_before_enqueue(lib):
     # nothing to do: no query
     assert fa(ctypes.byref(sh), 0, 192, None, None, None, good, 256, None) == 0
     assert fu(ctypes.byref(sh), 0, 256, None, None, None, good, 256, None) == 0
+
+
+def test_decode_step_host_rejects_before_enqueue(lib):
+    """dsa_decode_step_host: a per-step buffer the device cannot address
+    (here: any pointer, the runtime having no device to classify it against;
+    on a GPU, pageable host memory) is refused before anything is enqueued,
+    as are missing buffers and a short workspace; no query, nothing to do."""
+    P = ctypes.c_void_p
+    good = P(256)
+    sh = dsa.make_shape()
+    f = lib.dsa_decode_step_host
+    b = _batch(max_kv=4096)
+    n = _size(sh, b, dsa.OP_DECODE_STEP_HOST)[1]
+    host = (ctypes.c_uint8 * 4096)()                     # pageable host memory
+    hp = P(ctypes.addressof(host) + (-ctypes.addressof(host)) % 16)
+    args = [hp, hp, good, hp, good, hp, None, None, None, good, n, None]
+    assert f(ctypes.byref(sh), ctypes.byref(b), *args) == 1
+    no_out = list(args)
+    no_out[5] = None
+    assert f(ctypes.byref(sh), ctypes.byref(b), *no_out) == 1
+    b0 = _batch(n_q=0)
+    assert f(ctypes.byref(sh), ctypes.byref(b0), None, None, None, None, None, None, None,
+             None, None, good, 256 + 16 * 25604 * 4 + 16 * 256 * 8 + 4096, None) == 0
+    # one more launch than the step: the input copy
+    step = dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP)["kernel_launches"]
+    assert dsa.dsa_plan(sh, b, dsa.OP_DECODE_STEP_HOST)["kernel_launches"] == step + 1
+    with pytest.raises(ValueError):
+        dsa.dsa_decode_step_host(sh, b, torch.zeros(4), None, None, None, None, None)
 
 
 def test_python_binding_rejects_host_tensors(lib):
