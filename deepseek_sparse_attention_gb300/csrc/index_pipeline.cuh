@@ -207,6 +207,79 @@ __device__ int issue_first(uint8_t* smem, const CUtensorMap* tm_k_p, const CUten
     return (int)n;
 }
 
+// A single decode query guesses its CTA's first key tiles before the batch
+// offsets are read: its keys start at row 0 of k_idx (the offsets start at 0)
+// and, when its sequence is as long as the batch's bound -- the usual case --
+// number floor(max_kv_len / kpool).  spec_issue (one thread other than
+// thread 0, right after the wait for the previous kernel, before the plan's
+// CTA barriers) issues the query tile and the first key tiles of the guessed
+// range of `max_tiles` at most and notes them in shared memory.  spec_settle
+// (thread 0, after the plan, and followed by a CTA barrier before any thread
+// enters run()) keeps them when the plan gives the same first tiles, else
+// lets them land, re-arms their barriers and issues the real ones.  It returns
+// the key tiles on their way: run()'s `pre`.
+template <int GQ, int STAGES>
+__device__ void spec_issue(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p,
+                           const BatchDev& bq, int32_t kpool, int64_t cta, int64_t grid,
+                           int64_t max_tiles) {
+    using C = Cfg<GQ, STAGES>;
+    int32_t* note = reinterpret_cast<int32_t*>(smem + C::kOffMisc + 8);
+    int spec = 0;
+    int64_t ub = 0;
+    if (GQ == 1 && bq.n_q == 1 && bq.n_seq == 1) {
+        int64_t nk = bq.max_kv_len / kpool;
+        if (nk > bq.total_keys) nk = bq.total_keys;
+        const int64_t u_all = (nk + kTileKeys - 1) / kTileKeys;
+        ub = mul_div(cta, u_all, grid);
+        const int64_t ue = mul_div(cta + 1, u_all, grid);
+        if (ub < ue && ue - ub <= max_tiles) {
+            const IdxGroup g0{0, 0, 1, (int32_t)(nk * kpool), 0};
+            const int64_t t0[2] = {0, u_all};
+            spec = issue_first<GQ, STAGES>(smem, tm_k_p, tm_q_p, &g0, t0, 1, ub, ue);
+        }
+    }
+    note[0] = spec;
+    note[1] = (int32_t)ub;
+}
+
+template <int GQ, int STAGES>
+__device__ int spec_settle(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p,
+                           const IdxGroup* __restrict__ groups,
+                           const int64_t* __restrict__ tile_off, int64_t n_groups,
+                           int64_t u_begin, int64_t u_end, int32_t* err, int32_t where) {
+    using C = Cfg<GQ, STAGES>;
+    const int32_t* note = reinterpret_cast<const int32_t*>(smem + C::kOffMisc + 8);
+    const int spec = note[0];
+    // the key tiles issue_first would issue now: the first group's from u_begin
+    int64_t n_now = 0;
+    if (u_begin < u_end && n_groups == 1) {
+        n_now = tile_off[1] - u_begin;
+        if (n_now > u_end - u_begin) n_now = u_end - u_begin;
+        if (n_now > C::kStages) n_now = C::kStages;
+    }
+    if (spec > 0 && n_groups == 1 && groups[0].q0 == 0 && groups[0].key0 == 0 &&
+        u_begin == (int64_t)note[1] && n_now == spec)
+        return spec;                                   // the guessed tiles are the first ones
+    if (spec > 0) {
+        // a wrong guess: its loads land, then their barriers start afresh
+        uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+        uint64_t* full = bars;
+        uint64_t* b_full = bars + 2 * C::kStages;
+        bool landed = mbar_wait(b_full, 0, kWaitNs);
+        for (int s = 0; s < spec; ++s) landed = mbar_wait(&full[s], 0, kWaitNs) && landed;
+        if (!landed) record_error(err, kDevTimeout, (int32_t)blockIdx.x, where);
+        mbar_inval(b_full);
+        mbar_init(b_full, 1);
+        for (int s = 0; s < spec; ++s) {
+            mbar_inval(&full[s]);
+            mbar_init(&full[s], 1);
+        }
+        fence_mbarrier_init();
+    }
+    return issue_first<GQ, STAGES>(smem, tm_k_p, tm_q_p, groups, tile_off, n_groups, u_begin,
+                                   u_end);
+}
+
 // The three roles over [u_begin, u_end) (possibly empty), then TMEM release.
 // Called by every thread of the CTA (Cfg::kThreads) after setup().
 template <int GQ, int STAGES, class Epi>

@@ -226,7 +226,9 @@ struct ScoreStore {
     }
 };
 
-template <int GQ>
+// kSpec: the single-query decode instantiation, which guesses its first key
+// tiles before the batch offsets are read (spec_issue / spec_settle).
+template <int GQ, bool kSpec>
 __global__ void __launch_bounds__(Cfg<GQ>::kThreads, 1)
 index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                 const float* __restrict__ w, const IdxGroup* __restrict__ groups,
@@ -244,6 +246,11 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     pdl_wait();
     int64_t n_groups;
     if (local_plan) {
+        // thread 32: a single query's first key tiles, guessed from the
+        // batch's bounds, while thread 0 reads the batch offsets
+        if (kSpec && threadIdx.x == 32)
+            spec_issue<GQ, C::kStages>(smem, &tm_k, &tm_q, bq, kpool, blockIdx.x, gridDim.x,
+                                       INT64_MAX);
         n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/4);
         groups = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
         tile_off = reinterpret_cast<const int64_t*>(smem + C::kOffPlanT);
@@ -255,8 +262,12 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int64_t u_end = mul_div(blockIdx.x + 1, U, gridDim.x);
     int pre = 0;                                     // the first key tiles on their way now
     if (threadIdx.x == 0)
-        pre = issue_first<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off, n_groups, u_begin,
-                                          u_end);
+        pre = kSpec && local_plan ? spec_settle<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off, n_groups,
+                                                       u_begin, u_end, err, /*where=*/65)
+                         : issue_first<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off,
+                                                       n_groups, u_begin, u_end);
+    // a wrong guess re-arms barriers that the other roles wait on in run()
+    if (kSpec) __syncthreads();
     ScoreStore epi{scores, ld};                      // an empty range only releases TMEM
     run<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off, n_groups, u_begin, u_end, w, kpool,
                         epi, err, pre);
@@ -297,7 +308,8 @@ cudaError_t launch_tc(const Shape& sh, const BatchDev& b, const void* q_idx, con
                          pa.groups, pa.tile_off, err);
         if (e != cudaSuccess) return e;
     }
-    auto kern = index_scores_tc<GQ>;
+    auto kern = local && b.n_q == 1 && b.n_seq == 1 ? index_scores_tc<GQ, true>
+                                                    : index_scores_tc<GQ, false>;
     e = ensure_dyn_smem((const void*)kern, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(sm_count()), dim3(C::kThreads), C::kSmemBytes, st, tm_k, tm_q, w,

@@ -575,6 +575,10 @@ struct KeyStore {
     }
 };
 
+// kSpec: the single-query instantiation, which guesses its first key tiles
+// before the batch offsets are read (spec_issue / spec_settle); batches of
+// several queries run the other, without that code.
+template <bool kSpec>
 __global__ void __launch_bounds__(kThreads, 1)
 index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    const float* __restrict__ w, BatchDev bq, int32_t top_k, int32_t kpool,
@@ -606,6 +610,10 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
             reinterpret_cast<const uint8_t*>(err) + kWsWaitBudgetOffset);
         n_launch = *reinterpret_cast<const volatile uint32_t*>(launch_count);
     }
+    // thread 32: a single query's first key tiles, guessed from the batch's
+    // bounds, while thread 0 reads the batch offsets (checked after the plan)
+    if (kSpec && tid == 32)
+        spec_issue<1, C::kStages>(smem, &tm_k, &tm_q, bq, kpool, cta, grid, (int64_t)kMaxCtaTiles);
     int64_t* row0s = reinterpret_cast<int64_t*>(smem + kOffRow0);
     const int64_t n_groups = local_decode_plan<C>(smem, bq, kpool, err, /*where=*/6, row0s);
     const IdxGroup* gs = reinterpret_cast<const IdxGroup*>(smem + C::kOffPlanG);
@@ -618,7 +626,11 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     if (direct) keys = reinterpret_cast<uint32_t*>(smem + kOffSKeys);
     const int64_t u_run = u_begin < u_end && fits ? u_end : u_begin;   // the range scored
     int pre = 0;                              // thread 0: the first key tiles on their way now
-    if (tid == 0) pre = issue_first<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin, u_run);
+    if (tid == 0)
+        pre = kSpec ? spec_settle<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin,
+                                                 u_run, err, /*where=*/64)
+                    : issue_first<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin,
+                                                 u_run);
 
     // ---- before scoring: only what the epilogue needs, the first query this
     // CTA selects for (its level-1 counts are taken while scoring)
@@ -979,21 +991,22 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
     if (!make_rows128_map(&tm_k, k_idx, (uint64_t)b.total_keys, kTileKeys) ||
         !make_rows128_map(&tm_q, q_idx, (uint64_t)b.n_q * kIdxHeads, C::N))
         return cudaErrorInvalidValue;
-    cudaError_t e = ensure_dyn_smem((const void*)index_select_fused, (int)kSmemBytes);
+    const int spec = b.n_q == 1 && b.n_seq == 1 ? 1 : 0;
+    auto kern = spec ? index_select_fused<true> : index_select_fused<false>;
+    cudaError_t e = ensure_dyn_smem((const void*)kern, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     // one CTA must fit an SM (the cooperative grid is one per SM); checked
-    // once per device
-    static std::atomic<int> fits_sm[64];
+    // once per device and instantiation
+    static std::atomic<int> fits_sm[2][64];
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || fits_sm[dev].load(std::memory_order_relaxed) == 0) {
+    if (dev < 0 || dev >= 64 || fits_sm[spec][dev].load(std::memory_order_relaxed) == 0) {
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, index_select_fused, kThreads,
-                                                          kSmemBytes);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-        if (dev >= 0 && dev < 64) fits_sm[dev].store(1, std::memory_order_relaxed);
+        if (dev >= 0 && dev < 64) fits_sm[spec][dev].store(1, std::memory_order_relaxed);
     }
     uint32_t* gstate = static_cast<uint32_t*>(state);
     int2* gcnt = reinterpret_cast<int2*>(gstate + (size_t)kFusedMaxQ * kQueryWords);
@@ -1015,7 +1028,7 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
     cfg.attrs = attr;
     auto go = [&](unsigned n_attr) {
         cfg.numAttrs = n_attr;
-        return cudaLaunchKernelEx(&cfg, index_select_fused, tm_k, tm_q, w, b, sh.top_k, sh.kpool,
+        return cudaLaunchKernelEx(&cfg, kern, tm_k, tm_q, w, b, sh.top_k, sh.kpool,
                                   reinterpret_cast<uint32_t*>(scores), ld, idx, n_sel,
                                   sh.index_row_width(), gstate, gcnt,
                                   reinterpret_cast<unsigned long long*>(gbar),

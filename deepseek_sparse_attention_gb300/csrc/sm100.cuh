@@ -39,6 +39,12 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                  : "memory");
 }
 
+// Retires a barrier none of whose arrivals or transactions is pending, so
+// that it may be initialised again.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbarrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

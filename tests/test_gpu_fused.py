@@ -119,6 +119,52 @@ def test_fused_selection_is_exact_and_matches_two_launch_path(wl):
         check_attention(out[q], lse[q], o_ref, l_ref, wl.dtype)
 
 
+def test_fused_single_query_shorter_than_its_bounds():
+    """One decode query whose sequence is shorter than the batch's bounds
+    (max_kv_len, total_keys and total_rows of a cache with spare rows after
+    it): the fused launch's CTAs guess their first key tiles from the bounds
+    before the offsets are read, and here the guess is wrong for most of them
+    -- those loads are drained and the real range issued.  The selection must
+    equal the two-launch path's and the oracle rule's on the GPU scores."""
+    wl = workloads.small("spare_rows", [5000], top_k=2048, w_std=1 / 32 ** 0.5, cache_scale=0.5)
+    big = workloads.small("spare_rows_big", [9000], top_k=2048, w_std=1 / 32 ** 0.5,
+                          cache_scale=0.5, seed=7)
+    host = workloads.make(wl, "cpu")
+    d = to_device(host)
+    db = to_device(workloads.make(big, "cpu"))
+    k_big = torch.cat([d["k_idx"], db["k_idx"][5000:]]).contiguous()
+    c_big = torch.cat([d["cache"], db["cache"][5000:]]).contiguous()
+    sh = gpu_shape(wl)
+    width = dsa.dsa_index_row_width(sh)
+    res = []
+    for flags in (0, TWO):
+        b = dsa.make_batch(d["row_off"], d["key_off"], d["q_off"], 1, 1, 9000, 9000, 9000, flags)
+        ws = dsa.alloc_workspace(sh, b, dsa.OP_DECODE_STEP)
+        out = torch.full((1, wl.heads, wl.kv_lora), float("nan"), device="cuda")
+        lse = torch.full((1, wl.heads), float("nan"), device="cuda")
+        idx = torch.full((1, width), -7, dtype=torch.int32, device="cuda")
+        n_sel = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+        for _ in range(2):                 # the workspace as the second launch finds it, too
+            dsa.dsa_decode_step(sh, b, d["q_idx"], d["w"], k_big, d["q_abs"], c_big, out, lse,
+                                idx, n_sel, ws)
+            assert dsa.dsa_check_device_error(ws) == 0
+        res.append((out.cpu().numpy(), idx.cpu().numpy(), n_sel.cpu().numpy()))
+    b0 = dsa.make_batch(d["row_off"], d["key_off"], d["q_off"], 1, 1, 9000, 9000, 9000)
+    assert dsa.dsa_plan(sh, b0, dsa.OP_DECODE_STEP)["kernel_launches"] == 3   # fused
+    (out, idx, n_sel), (out2, idx2, n_sel2) = res
+    assert np.array_equal(idx, idx2) and np.array_equal(n_sel, n_sel2)
+    assert np.array_equal(out, out2)
+    _check_exact(wl, host, d, idx, n_sel)
+    # the standalone indexer guesses the same way: its scores under the loose
+    # bounds equal those under the exact ones, bit for bit
+    ws = dsa.alloc_workspace(sh, b0, dsa.OP_INDEX_SCORES)
+    sc = torch.full((1, 9000), float("nan"), device="cuda")
+    dsa.dsa_index_scores(sh, b0, d["q_idx"], d["w"], k_big, sc, 9000, ws)
+    assert dsa.dsa_check_device_error(ws) == 0
+    assert np.array_equal(sc.cpu().numpy()[0, :5000], _gpu_scores(wl, d)[0, :5000])
+    assert bool(torch.all(torch.isnan(sc[0, 5000:])))          # nothing past the sequence
+
+
 def _tie_inputs(kind):
     wl = workloads.small(f"ties_{kind}", [30000, 2500, 9000], top_k=2048, seed=11)
     host = workloads.make(wl, "cpu")
