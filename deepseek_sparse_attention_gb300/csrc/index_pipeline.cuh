@@ -207,17 +207,50 @@ __device__ int issue_first(uint8_t* smem, const CUtensorMap* tm_k_p, const CUten
     return (int)n;
 }
 
-// A single decode query guesses its CTA's first key tiles before the batch
-// offsets are read: its keys start at row 0 of k_idx (the offsets start at 0)
-// and, when its sequence is as long as the batch's bound -- the usual case --
-// number floor(max_kv_len / kpool).  spec_issue (one thread other than
-// thread 0, right after the wait for the previous kernel, before the plan's
-// CTA barriers) issues the query tile and the first key tiles of the guessed
-// range of `max_tiles` at most and notes them in shared memory.  spec_settle
-// (thread 0, after the plan, and followed by a CTA barrier before any thread
-// enters run()) keeps them when the plan gives the same first tiles, else
-// lets them land, re-arms their barriers and issues the real ones.  It returns
-// the key tiles on their way: run()'s `pre`.
+// The decode plan a batch's host scalars imply when they leave it one
+// possibility worth guessing: *n_seqs sequences of *nk keys each, one query
+// each, the keys of sequence s from row s * nk of k_idx.  Only a single query
+// is guessed: its keys start at row 0 (the offsets start at 0) and, when its
+// sequence is as long as the batch's bound -- the usual case -- number
+// floor(max_kv_len / kpool) (or the keys there are, if fewer).  (For a batch
+// of equal sequences at the bound the scalars force every offset too, but
+// there the guess measured slower in the whole step: 74.2 -> 75.5 us on the
+// 1M-token k-pool decode, with the launch alone 1.4 us faster.)  False when
+// no guess is made.  A guess is only ever a guess: the kernels check it
+// against the plan they read.
+__host__ __device__ inline bool spec_plan_guess(const BatchDev& b, int32_t kpool, int64_t* nk,
+                                                int64_t* n_seqs) {
+    if (kpool < 1 || b.n_q != 1 || b.n_seq != 1) return false;
+    *nk = b.max_kv_len / kpool < b.total_keys ? b.max_kv_len / kpool : b.total_keys;
+    *n_seqs = 1;
+    return *nk > 0;
+}
+
+// A CTA's first key tiles under the guessed plan: spec_issue (one thread other
+// than thread 0, right after the wait for the previous kernel, before the
+// plan's CTA barriers) issues the query tile and the first key tiles of the
+// CTA's guessed range (of `max_tiles` at most) and notes how many in shared
+// memory; the batch offsets are read meanwhile.  spec_settle (thread 0, after
+// the plan, and followed by a CTA barrier before any thread enters run())
+// keeps them when the plan gives the same first tiles, else lets them land,
+// re-arms their barriers and issues the real ones.  It returns the key tiles
+// on their way: run()'s `pre`.
+struct SpecRange {
+    int64_t nk, per, ub, ue;          // keys and tiles per sequence, the CTA's guessed units
+};
+
+__device__ inline bool spec_range(const BatchDev& b, int32_t kpool, int64_t cta, int64_t grid,
+                                  SpecRange* r) {
+    int64_t nk = 0, n_seqs = 0;
+    if (!spec_plan_guess(b, kpool, &nk, &n_seqs)) return false;
+    r->nk = nk;
+    r->per = (nk + kTileKeys - 1) / kTileKeys;
+    const int64_t u_all = r->per * n_seqs;
+    r->ub = mul_div(cta, u_all, grid);
+    r->ue = mul_div(cta + 1, u_all, grid);
+    return r->ub < r->ue;
+}
+
 template <int GQ, int STAGES>
 __device__ void spec_issue(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p,
                            const BatchDev& bq, int32_t kpool, int64_t cta, int64_t grid,
@@ -225,56 +258,58 @@ __device__ void spec_issue(uint8_t* smem, const CUtensorMap* tm_k_p, const CUten
     using C = Cfg<GQ, STAGES>;
     int32_t* note = reinterpret_cast<int32_t*>(smem + C::kOffMisc + 8);
     int spec = 0;
-    int64_t ub = 0;
-    if (GQ == 1 && bq.n_q == 1 && bq.n_seq == 1) {
-        int64_t nk = bq.max_kv_len / kpool;
-        if (nk > bq.total_keys) nk = bq.total_keys;
-        const int64_t u_all = (nk + kTileKeys - 1) / kTileKeys;
-        ub = mul_div(cta, u_all, grid);
-        const int64_t ue = mul_div(cta + 1, u_all, grid);
-        if (ub < ue && ue - ub <= max_tiles) {
-            const IdxGroup g0{0, 0, 1, (int32_t)(nk * kpool), 0};
-            const int64_t t0[2] = {0, u_all};
-            spec = issue_first<GQ, STAGES>(smem, tm_k_p, tm_q_p, &g0, t0, 1, ub, ue);
-        }
+    SpecRange r;
+    if (GQ == 1 && spec_range(bq, kpool, cta, grid, &r) && r.ue - r.ub <= max_tiles) {
+        const int64_t g = r.ub / r.per;                // the guessed group of the first unit
+        const IdxGroup gg{g * r.nk, (int32_t)g, 1, (int32_t)(r.nk * kpool), 0};
+        const int64_t t0[2] = {g * r.per, (g + 1) * r.per};
+        spec = issue_first<GQ, STAGES>(smem, tm_k_p, tm_q_p, &gg, t0, 1, r.ub, r.ue);
     }
     note[0] = spec;
-    note[1] = (int32_t)ub;
+}
+
+// a wrong guess: its loads land, then their barriers start afresh
+static __device__ __noinline__ void spec_drain(uint64_t* bars, int stages, int spec, int32_t* err,
+                                        int32_t where) {
+    uint64_t* full = bars;
+    uint64_t* b_full = bars + 2 * stages;
+    bool landed = mbar_wait(b_full, 0, kWaitNs);
+#pragma unroll 1
+    for (int s = 0; s < spec; ++s) landed = mbar_wait(&full[s], 0, kWaitNs) && landed;
+    if (!landed) record_error(err, kDevTimeout, (int32_t)blockIdx.x, where);
+    mbar_inval(b_full);
+    mbar_init(b_full, 1);
+#pragma unroll 1
+    for (int s = 0; s < spec; ++s) {
+        mbar_inval(&full[s]);
+        mbar_init(&full[s], 1);
+    }
+    fence_mbarrier_init();
 }
 
 template <int GQ, int STAGES>
 __device__ int spec_settle(uint8_t* smem, const CUtensorMap* tm_k_p, const CUtensorMap* tm_q_p,
-                           const IdxGroup* __restrict__ groups,
+                           const BatchDev& bq, int32_t kpool, const IdxGroup* __restrict__ groups,
                            const int64_t* __restrict__ tile_off, int64_t n_groups,
                            int64_t u_begin, int64_t u_end, int32_t* err, int32_t where) {
     using C = Cfg<GQ, STAGES>;
-    const int32_t* note = reinterpret_cast<const int32_t*>(smem + C::kOffMisc + 8);
-    const int spec = note[0];
-    // the key tiles issue_first would issue now: the first group's from u_begin
-    int64_t n_now = 0;
-    if (u_begin < u_end && n_groups == 1) {
-        n_now = tile_off[1] - u_begin;
-        if (n_now > u_end - u_begin) n_now = u_end - u_begin;
-        if (n_now > C::kStages) n_now = C::kStages;
-    }
-    if (spec > 0 && n_groups == 1 && groups[0].q0 == 0 && groups[0].key0 == 0 &&
-        u_begin == (int64_t)note[1] && n_now == spec)
-        return spec;                                   // the guessed tiles are the first ones
+    const int spec = reinterpret_cast<const int32_t*>(smem + C::kOffMisc + 8)[0];
     if (spec > 0) {
-        // a wrong guess: its loads land, then their barriers start afresh
-        uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-        uint64_t* full = bars;
-        uint64_t* b_full = bars + 2 * C::kStages;
-        bool landed = mbar_wait(b_full, 0, kWaitNs);
-        for (int s = 0; s < spec; ++s) landed = mbar_wait(&full[s], 0, kWaitNs) && landed;
-        if (!landed) record_error(err, kDevTimeout, (int32_t)blockIdx.x, where);
-        mbar_inval(b_full);
-        mbar_init(b_full, 1);
-        for (int s = 0; s < spec; ++s) {
-            mbar_inval(&full[s]);
-            mbar_init(&full[s], 1);
+        SpecRange r;
+        spec_range(bq, kpool, blockIdx.x, gridDim.x, &r);
+        if (u_begin == r.ub && u_begin < u_end) {
+            // the plan's group of the first unit, and the key tiles
+            // issue_first would issue now: that group's from u_begin
+            Cursor<false> c{tile_off, 0, 0, 0, 0};
+            c.seek(u_begin, n_groups);
+            int64_t n_now = tile_off[c.g + 1] - u_begin;
+            if (n_now > u_end - u_begin) n_now = u_end - u_begin;
+            if (n_now > C::kStages) n_now = C::kStages;
+            const int64_t g = r.ub / r.per;
+            if (c.g == g && groups[c.g].q0 == g && groups[c.g].key0 == g * r.nk && n_now == spec)
+                return spec;                           // the guessed tiles are the first ones
         }
-        fence_mbarrier_init();
+        spec_drain(reinterpret_cast<uint64_t*>(smem + C::kOffBar), C::kStages, spec, err, where);
     }
     return issue_first<GQ, STAGES>(smem, tm_k_p, tm_q_p, groups, tile_off, n_groups, u_begin,
                                    u_end);

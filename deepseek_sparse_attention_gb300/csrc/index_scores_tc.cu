@@ -226,8 +226,9 @@ struct ScoreStore {
     }
 };
 
-// kSpec: the single-query decode instantiation, which guesses its first key
-// tiles before the batch offsets are read (spec_issue / spec_settle).
+// kSpec: the instantiation for decode batches whose host scalars imply their
+// plan (spec_plan_guess), which guesses its first key tiles before the batch
+// offsets are read (spec_issue / spec_settle).
 template <int GQ, bool kSpec>
 __global__ void __launch_bounds__(Cfg<GQ>::kThreads, 1)
 index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -262,8 +263,9 @@ index_scores_tc(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int64_t u_end = mul_div(blockIdx.x + 1, U, gridDim.x);
     int pre = 0;                                     // the first key tiles on their way now
     if (threadIdx.x == 0)
-        pre = kSpec && local_plan ? spec_settle<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off, n_groups,
-                                                       u_begin, u_end, err, /*where=*/65)
+        pre = kSpec && local_plan ? spec_settle<GQ, C::kStages>(smem, &tm_k, &tm_q, bq, kpool, groups,
+                                                                tile_off, n_groups, u_begin, u_end,
+                                                                err, /*where=*/65)
                          : issue_first<GQ, C::kStages>(smem, &tm_k, &tm_q, groups, tile_off,
                                                        n_groups, u_begin, u_end);
     // a wrong guess re-arms barriers that the other roles wait on in run()
@@ -308,8 +310,9 @@ cudaError_t launch_tc(const Shape& sh, const BatchDev& b, const void* q_idx, con
                          pa.groups, pa.tile_off, err);
         if (e != cudaSuccess) return e;
     }
-    auto kern = local && b.n_q == 1 && b.n_seq == 1 ? index_scores_tc<GQ, true>
-                                                    : index_scores_tc<GQ, false>;
+    int64_t g_nk = 0, g_ns = 0;
+    auto kern = local && spec_plan_guess(b, sh.kpool, &g_nk, &g_ns) ? index_scores_tc<GQ, true>
+                                                                    : index_scores_tc<GQ, false>;
     e = ensure_dyn_smem((const void*)kern, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(sm_count()), dim3(C::kThreads), C::kSmemBytes, st, tm_k, tm_q, w,

@@ -575,9 +575,10 @@ struct KeyStore {
     }
 };
 
-// kSpec: the single-query instantiation, which guesses its first key tiles
-// before the batch offsets are read (spec_issue / spec_settle); batches of
-// several queries run the other, without that code.
+// kSpec: the instantiation for batches whose host scalars imply their plan
+// (spec_plan_guess), which guesses its first key tiles before the batch
+// offsets are read (spec_issue / spec_settle); other batches run the one
+// without that code.
 template <bool kSpec>
 __global__ void __launch_bounds__(kThreads, 1)
 index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
@@ -627,8 +628,8 @@ index_select_fused(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     const int64_t u_run = u_begin < u_end && fits ? u_end : u_begin;   // the range scored
     int pre = 0;                              // thread 0: the first key tiles on their way now
     if (tid == 0)
-        pre = kSpec ? spec_settle<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin,
-                                                 u_run, err, /*where=*/64)
+        pre = kSpec ? spec_settle<1, C::kStages>(smem, &tm_k, &tm_q, bq, kpool, gs, ts, n_groups,
+                                                 u_begin, u_run, err, /*where=*/64)
                     : issue_first<1, C::kStages>(smem, &tm_k, &tm_q, gs, ts, n_groups, u_begin,
                                                  u_run);
 
@@ -991,7 +992,8 @@ cudaError_t launch_index_select_fused(const Shape& sh, const BatchDev& b, const 
     if (!make_rows128_map(&tm_k, k_idx, (uint64_t)b.total_keys, kTileKeys) ||
         !make_rows128_map(&tm_q, q_idx, (uint64_t)b.n_q * kIdxHeads, C::N))
         return cudaErrorInvalidValue;
-    const int spec = b.n_q == 1 && b.n_seq == 1 ? 1 : 0;
+    int64_t g_nk = 0, g_ns = 0;
+    const int spec = spec_plan_guess(b, sh.kpool, &g_nk, &g_ns) ? 1 : 0;
     auto kern = spec ? index_select_fused<true> : index_select_fused<false>;
     cudaError_t e = ensure_dyn_smem((const void*)kern, (int)kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -42,6 +42,9 @@ FUSED = [
                     rope=0),
     workloads.small("batch_16", _lens16(), top_k=2048, seed=3),
     workloads.small("small_k", [20000, 5000, 64], top_k=64),
+    # every sequence at the batch's bound
+    workloads.small("uniform_4", [20000] * 4, top_k=2048, seed=5),
+    workloads.small("uniform_kpool", [30000] * 3, top_k=2048, kpool=4, rope=0, seed=6),
 ]
 
 
