@@ -29,6 +29,10 @@ CASES = [
     (workloads.small("mixed_chunks", [3000, 2100, 900, 5000], q_lens=[1, 37, 1, 8], top_k=256), 0),
     (workloads.small("two_launch", [5000, 3000], top_k=2048), dsa.FLAG_TWO_LAUNCH),
     (workloads.small("dense", [700, 1500], top_k=256), dsa.FLAG_DENSE),
+    (workloads.small("desc_order", [5000, 2100], top_k=512), dsa.FLAG_DESC_ORDER),
+    # one query whose first key tiles the fused launch requests before the
+    # batch offsets are read
+    (workloads.small("one_query", [40000], top_k=2048, w_std=1 / 32 ** 0.5, cache_scale=0.5), 0),
 ]
 
 
